@@ -1,0 +1,36 @@
+"""GB300-native fused causal attention forwards.
+
+Two forwards that never materialise the T x T score matrix, each one CUDA
+kernel for sm_103a behind a C ABI (``include/bsa.h``, ``libbsa.so``):
+
+* ``tra_forward``        -- threshold rectified attention,
+  ``out = ReLU(Q K^T - tau(i))^p V`` with ``tau(i) = beta sqrt(2 ln(i+1)/D)``,
+  causal and unnormalised (page "triton_threshold_attention.py").
+* ``nsa_select_forward`` -- NSA selection-branch attention over gathered key
+  blocks, GQA, causal, scaled softmax (page "nsa_selection_kernel.py").
+
+The binding in ``bsa`` only marshals arguments; every step runs in the CUDA
+library, which is loaded on first use and must be built (``build.build()``).
+"""
+
+from .bsa import (  # noqa: F401
+    BsaError,
+    library_path,
+    load_library,
+    nsa_select_forward,
+    nsa_select_forward_raw,
+    status_string,
+    tra_forward,
+    tra_forward_raw,
+)
+
+__all__ = [
+    "BsaError",
+    "library_path",
+    "load_library",
+    "tra_forward",
+    "tra_forward_raw",
+    "nsa_select_forward",
+    "nsa_select_forward_raw",
+    "status_string",
+]

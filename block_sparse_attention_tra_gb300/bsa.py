@@ -1,0 +1,157 @@
+"""ctypes binding of ``libbsa.so`` (declared in ``include/bsa.h``).
+
+Argument marshalling only: every step of both forwards runs in the CUDA
+library.  PyTorch is used for device memory and streams.  There is no CPU
+fallback: if the library is missing or the device is not usable, the calls
+raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+BSA_F32 = 0
+BSA_BF16 = 1
+
+_STATUS = {
+    0: "BSA_OK",
+    1: "BSA_ERR_NULLPTR",
+    2: "BSA_ERR_SHAPE",
+    3: "BSA_ERR_DTYPE",
+    4: "BSA_ERR_UNSUPPORTED",
+    5: "BSA_ERR_LAUNCH",
+    6: "BSA_ERR_DEVICE",
+    7: "BSA_ERR_ALIGN",
+}
+
+
+class BsaError(RuntimeError):
+    """A libbsa call returned a non-zero bsa_status, or the library is absent."""
+
+    def __init__(self, msg, status=None):
+        super().__init__(msg)
+        self.status = status
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libbsa.so")
+
+
+def load_library():
+    """Load ``libbsa.so`` once and declare its C signatures."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise BsaError(f"{path} is not built; run block_sparse_attention_tra_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.tra_forward.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, vp]
+    lib.tra_forward.restype = i32
+    lib.nsa_select_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp]
+    lib.nsa_select_forward.restype = i32
+    lib.bsa_status_string.argtypes = [i32]
+    lib.bsa_status_string.restype = ctypes.c_char_p
+    lib.bsa_version.argtypes = []
+    lib.bsa_version.restype = i32
+    _LIB = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().bsa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise BsaError(f"{what} failed: {_STATUS.get(status, status)} ({status_string(status)})", status)
+
+
+def tra_forward_raw(q, k, v, out, B, H, T, D, beta, p, dtype, stream=0) -> int:
+    """Direct C call with integer device pointers; returns the bsa_status."""
+    return load_library().tra_forward(q, k, v, out, B, H, T, D, float(beta), float(p), int(dtype), stream)
+
+
+def nsa_select_forward_raw(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, block_size, S,
+                           stream=0) -> int:
+    """Direct C call with integer device pointers; returns the bsa_status."""
+    return load_library().nsa_select_forward(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D,
+                                             block_size, S, stream)
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t):
+    import torch
+
+    if t.dtype == torch.float32:
+        return BSA_F32
+    if t.dtype == torch.bfloat16:
+        return BSA_BF16
+    raise BsaError(f"unsupported dtype {t.dtype}", 3)
+
+
+def tra_forward(q, k, v, beta: float, p: float = 2.0, out=None, stream=None):
+    """Threshold rectified attention forward on CUDA tensors ``[B, H, T, D]``.
+
+    ``out = ReLU(q k^T - tau(i))^p v`` with ``tau(i) = beta sqrt(2 ln(i+1)/D)``,
+    causal, unnormalised; float32 or bfloat16 in, same dtype out.  Runs on
+    ``stream`` (default: torch's current stream) without synchronising.
+    """
+    if q.device.type != "cuda":
+        raise BsaError("tra_forward takes CUDA tensors (no CPU path)")
+    if not (q.shape == k.shape == v.shape) or q.dim() != 4:
+        raise BsaError("q, k, v must share one shape [B, H, T, D]", 2)
+    if not (q.dtype == k.dtype == v.dtype):
+        raise BsaError("q, k, v must share one dtype", 3)
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    if out is None:
+        import torch
+
+        out = torch.empty_like(q)
+    B, H, T, D = q.shape
+    st = tra_forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T, D,
+                         beta, p, _dtype_code(q), _stream_handle(stream))
+    _check(st, "tra_forward")
+    return out
+
+
+def nsa_select_forward(q, k, v, block_idx, block_size: int = 64, out=None, lse=None,
+                       return_lse: bool = False, stream=None):
+    """NSA selection-branch forward on CUDA tensors.
+
+    q ``[B, Hq, T, D]``, k/v ``[B, Hkv, T, D]`` bf16, ``block_idx [B, Hkv, T,
+    S]`` int32 (-1 = padding).  Returns ``out`` (and ``lse [B, Hq, T]`` fp32
+    when ``return_lse``).
+    """
+    import torch
+
+    if q.device.type != "cuda":
+        raise BsaError("nsa_select_forward takes CUDA tensors (no CPU path)")
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or block_idx.dim() != 4:
+        raise BsaError("q [B,Hq,T,D], k/v [B,Hkv,T,D], block_idx [B,Hkv,T,S] expected", 2)
+    B, Hq, T, D = q.shape
+    Hkv = k.shape[1]
+    S = block_idx.shape[-1]
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    idx = block_idx.to(torch.int32).contiguous()
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, T), device=q.device, dtype=torch.float32)
+    st = nsa_select_forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), idx.data_ptr(),
+                                out.data_ptr(), lse.data_ptr() if lse is not None else None,
+                                B, Hq, Hkv, T, D, block_size, S, _stream_handle(stream))
+    _check(st, "nsa_select_forward")
+    return (out, lse) if return_lse else out

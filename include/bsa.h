@@ -1,0 +1,133 @@
+/*
+ * bsa.h -- C ABI of libbsa.so: GB300 (sm_103a) fused causal attention forwards.
+ *
+ * Two forwards, each one CUDA kernel launch that never materialises the T x T
+ * score matrix:
+ *
+ *   tra_forward         threshold rectified attention (TRA)
+ *   nsa_select_forward  NSA selection-branch attention
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor pointer is caller-owned DEVICE memory (cudaMalloc or a
+ *   framework allocator) on the current device.  Tensors are dense, contiguous
+ *   and row-major in the shapes given below; there are no stride arguments.
+ *   q, k, v and out start on a 16-byte boundary.
+ * - The library allocates no device memory, keeps no state between calls and
+ *   never synchronises: work is enqueued on `stream` (0 = legacy default
+ *   stream) and the call returns after the launch.  Inputs must stay valid and
+ *   unmodified, and outputs untouched by others, until that work completes.
+ * - A call returns a bsa_status.  Argument errors are detected on the host
+ *   before anything is enqueued and leave every buffer untouched.  A launch
+ *   failure returns BSA_ERR_LAUNCH.  Nothing aborts or prints.
+ * - Out-of-range values inside the index tensor (see nsa_select_forward) are
+ *   a precondition violation: the kernel treats any negative index as padding
+ *   and never reads outside k/v for an index >= T / block_size (such a slot is
+ *   skipped), but results for such a row are unspecified.
+ */
+#ifndef BSA_H
+#define BSA_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of q, k, v and out. */
+typedef enum {
+  BSA_F32 = 0,  /* IEEE float32 */
+  BSA_BF16 = 1  /* bfloat16 (8-bit exponent, 7-bit mantissa) */
+} bsa_dtype;
+
+typedef enum {
+  BSA_OK = 0,
+  BSA_ERR_NULLPTR = 1,     /* a required pointer is NULL                     */
+  BSA_ERR_SHAPE = 2,       /* a size is out of range or inconsistent          */
+  BSA_ERR_DTYPE = 3,       /* dtype is not a bsa_dtype                        */
+  BSA_ERR_UNSUPPORTED = 4, /* a valid request this build does not implement,
+                              or a parameter outside the method (p <= 0,
+                              non-finite beta)                               */
+  BSA_ERR_LAUNCH = 5,      /* the CUDA launch failed (cudaGetLastError)       */
+  BSA_ERR_DEVICE = 6,      /* no usable sm_100-family device / driver entry   */
+  BSA_ERR_ALIGN = 7        /* a tensor pointer is not 16-byte aligned         */
+} bsa_status;
+
+/*
+ * tra_forward -- threshold rectified attention forward.
+ *
+ * Defined on the page "triton_threshold_attention.py" (snap-research/TDA):
+ * module docstring formula and the forward kernel _threshold_rela_fwd_kernel.
+ * For every (b, h) and query row i = 0..T-1:
+ *
+ *   tau(i)      = beta * sqrt(2 * ln(i + 1) / D)        (computed in fp32)
+ *   out[b,h,i,:] = sum_{j <= i} ReLU(q_i . k_j - tau(i))^p * v_j
+ *
+ * Causal, unnormalised, no 1/sqrt(D) factor on q.k.  p == 1 and p == 2 use
+ * the identity and a product; any other p > 0 uses x^p = exp2(p * log2 x).
+ * A masked (future) pair contributes nothing for every beta (the page's own
+ * code agrees for beta >= 0).
+ *
+ *   q, k, v, out : [B, H, T, D], element type `dtype`; out has the input type
+ *                  (the page casts its fp32 result back to the input dtype).
+ *   B, H, T      : >= 1; B * H <= 2^31 - 1 and B*H*T*D < 2^40.
+ *   D            : 64 or 128 (head dim).
+ *   beta         : finite.      p : finite and > 0.
+ *   dtype        : BSA_BF16 -- tensor-core (tcgen05) path, bf16 operands,
+ *                  fp32 accumulation, weights rounded to bf16 before W.V;
+ *                  BSA_F32  -- fp32 CUDA-core path (fp32 FMA throughout).
+ *   stream       : CUDA stream the kernel is enqueued on.
+ *
+ * Errors: BSA_ERR_NULLPTR, BSA_ERR_SHAPE (sizes), BSA_ERR_DTYPE,
+ * BSA_ERR_UNSUPPORTED (D not 64/128, p <= 0, non-finite beta/p),
+ * BSA_ERR_ALIGN, BSA_ERR_DEVICE, BSA_ERR_LAUNCH.
+ */
+int tra_forward(const void* q, const void* k, const void* v, void* out,
+                int B, int H, int T, int D, float beta, float p, int dtype,
+                cudaStream_t stream);
+
+/*
+ * nsa_select_forward -- NSA selection-branch attention forward (bf16).
+ *
+ * Defined on the page "nsa_selection_kernel.py" (openbox-llm): module
+ * docstring "The operation", the ground truth selection_forward_reference and
+ * the log-sum-exp of _selection_fwd_kernel.  With G = Hq / Hkv and query head
+ * h reading kv head h / G, for every (b, h, i):
+ *
+ *   J     = { j : j / block_size is a non-negative entry of
+ *                 block_idx[b, h/G, i, 0..S-1], and j <= i }
+ *   s_j   = (q[b,h,i] . k[b,h/G,j]) * D^-0.5
+ *   out[b,h,i] = sum_{j in J} softmax(s)_j * v[b,h/G,j]     (0 if J is empty)
+ *   lse[b,h,i] = ln sum_{j in J} exp(s_j)                   (-1e9 if J empty)
+ *
+ *   q, out     : [B, Hq, T, D] bf16.      k, v : [B, Hkv, T, D] bf16.
+ *   block_idx  : [B, Hkv, T, S] int32, shared by the G heads of a group;
+ *                -1 = padding.  The non-negative entries of one row must be
+ *                distinct (the page's reference treats a repeated block as
+ *                selected once; this kernel would count it twice).
+ *   lse        : [B, Hq, T] fp32, or NULL to skip it.
+ *   D          : 128 or 64.   block_size : 64.   1 <= S <= 32.
+ *   T          : multiple of block_size.   Hq % Hkv == 0, Hq / Hkv == 16.
+ *   stream     : CUDA stream the kernel is enqueued on.
+ *
+ * Errors: BSA_ERR_NULLPTR (q, k, v, block_idx or out NULL), BSA_ERR_SHAPE,
+ * BSA_ERR_UNSUPPORTED (other D, block_size or group size), BSA_ERR_ALIGN,
+ * BSA_ERR_DEVICE, BSA_ERR_LAUNCH.
+ */
+int nsa_select_forward(const void* q, const void* k, const void* v,
+                       const int32_t* block_idx, void* out, float* lse,
+                       int B, int Hq, int Hkv, int T, int D, int block_size,
+                       int S, cudaStream_t stream);
+
+/* Static, NUL-terminated description of a bsa_status value (never NULL). */
+const char* bsa_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int bsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSA_H */

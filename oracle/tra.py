@@ -1,0 +1,111 @@
+"""Threshold rectified attention (TRA) forward, float64 CPU oracle.
+
+Source page: "triton_threshold_attention.py" (snap-research/TDA).
+
+* Module docstring: ``out = (ReLU(Q@K^T - tau))^p @ V`` with the position
+  dependent threshold ``tau(i) = beta * sqrt(2 * log(i+1) / d)``.
+* ``_threshold_rela_fwd_kernel``: tau per query row from the 0-based row index
+  ``i`` as ``(i + 1)``, natural log, ``d`` = head dim; no ``1/sqrt(d)`` factor on
+  ``Q@K^T``; causal mask keeps keys ``j <= i``; power branches ``p == 2``,
+  ``p == 1`` and a general ``p`` through ``exp(p * log(x))``; the output is the
+  unnormalised sum ``sum_j w_ij v_j``.
+* ``ThresholdRelaFunction.forward``: q, k, v share the shape ``[B, H, T, D]``.
+
+Readings taken where the page is silent or ambiguous (each listed in the design
+notes of the repository):
+
+* Masked (future) pairs contribute nothing.  The page writes 0 into the score
+  of a masked pair *before* subtracting tau, which equals "nothing" whenever
+  ``beta >= 0`` (then ``ReLU(0 - tau) = 0``); for ``beta < 0`` the page would
+  leak ``|tau|^p`` from every future key, which contradicts its own comment
+  that a query attends only to positions ``<= i``.
+* The general power is the exact ``x**p`` for ``x > 0`` and 0 otherwise; the
+  page's ``+1e-10`` inside the log is a guard, not part of the method.
+* ``p > 0`` is required (``0**0`` and negative powers are undefined there).
+
+TEST INFRASTRUCTURE: see the package docstring for who may import this.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def tau(T: int, beta: float, D: int) -> np.ndarray:
+    """Per-row threshold ``tau(i) = beta * sqrt(2 ln(i+1) / D)`` for i = 0..T-1.
+
+    Forward kernel, "Compute tau for each query position": rows are 0-based and
+    shifted by one, ``log`` is the natural log, ``D`` is the head dimension.
+    """
+    i = np.arange(T, dtype=np.float64)
+    return float(beta) * np.sqrt(2.0 * np.log(i + 1.0) / float(D))
+
+
+def relu_power(x: np.ndarray, p: float) -> np.ndarray:
+    """``ReLU(x)**p``: ``x**p`` where ``x > 0``, else 0 (forward kernel,
+    "Apply threshold" and "Apply power")."""
+    if not p > 0:
+        raise ValueError("relu power p must be > 0")
+    out = np.zeros_like(x, dtype=np.float64)
+    pos = x > 0
+    out[pos] = np.power(x[pos], float(p))
+    return out
+
+
+def _check(q, k, v):
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    if q.ndim != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share one shape [B, H, T, D]")
+    return q, k, v
+
+
+def tra_forward(q, k, v, beta: float, p: float, block: int = 256) -> np.ndarray:
+    """Full TRA forward ``out[b,h,i] = sum_{j<=i} ReLU(q_i.k_j - tau(i))^p v_j``.
+
+    Computed row block by row block: for query rows ``i0..i1-1`` the scores
+    against keys ``0..i1-1`` come from one BLAS matmul, the causal mask and the
+    threshold/power are applied elementwise, and one more matmul multiplies by
+    V.  This is the definition written out; the blocking only bounds memory.
+    """
+    q, k, v = _check(q, k, v)
+    B, H, T, D = q.shape
+    t = tau(T, beta, D)
+    out = np.zeros((B, H, T, D), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            for i0 in range(0, T, block):
+                i1 = min(T, i0 + block)
+                s = q[b, h, i0:i1] @ k[b, h, :i1].T  # [i1-i0, i1]
+                x = s - t[i0:i1, None]
+                w = relu_power(x, p)
+                rows = np.arange(i0, i1)[:, None]
+                cols = np.arange(i1)[None, :]
+                w[cols > rows] = 0.0  # causal: keys j <= i only
+                out[b, h, i0:i1] = w @ v[b, h, :i1]
+    return out
+
+
+def tra_rows(q, k, v, beta: float, p: float, rows) -> np.ndarray:
+    """TRA forward for selected output rows only.
+
+    ``rows`` is a sequence of ``(b, h, i)``; returns an array ``[len(rows), D]``
+    holding ``out[b, h, i]``.  Used to check full-size launches on sampled rows
+    (each row costs O(i*D), independent of the others).
+    """
+    q, k, v = _check(q, k, v)
+    B, H, T, D = q.shape
+    t = tau(T, beta, D)
+    res = np.zeros((len(rows), D), dtype=np.float64)
+    for n, (b, h, i) in enumerate(rows):
+        s = k[b, h, : i + 1] @ q[b, h, i]  # [i+1]
+        w = relu_power(s - t[i], p)
+        res[n] = w @ v[b, h, : i + 1]
+    return res
+
+
+def tra_flops(B: int, H: int, T: int, D: int) -> int:
+    """Algorithmic FLOPs of one causal TRA forward: two multiply-adds of length
+    D (one for q_i.k_j, one for w_ij v_j) per causally valid pair (i, j<=i)."""
+    return 4 * D * B * H * (T * (T + 1) // 2)
