@@ -1,0 +1,449 @@
+"""Benchmark of the fused causal attention forwards on GB300.
+
+``python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+[--workload NAME] [--no-secondary]`` prints ONE JSON line.
+
+A step is one pass of the whole threshold-rectified-attention (TRA) path --
+tau table, Q K^T, causal mask, threshold and power, W V, store -- fused in one
+kernel launch, over one batch of synthetic input of the workload (default:
+bf16 B=4 H=16 T=4096 D=128, beta=1, p=2).  Inputs are resident in HBM when the
+timed region starts; the inputs plus output (268 MB) are larger than the
+129 MB L2, so no flush is done between steps of the headline workload.  The
+secondary workloads (the T=8192 general-power TRA and both NSA selection
+workloads) are measured in the same run with an L2 flush between iterations
+and reported under ``secondary``.
+
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU with no
+collective on the data path (the work is independent per (batch, head));
+``value`` is the total FLOPs of all ranks over the max elapsed time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal fwd TFLOP/s & % of dense BF16 tensor peak (threshold attn; NSA select)"
+DEFAULT_WORKLOAD = "tra_bf16_B4_H16_T4096_D128"
+SECONDARY = ["tra_bf16_B2_H32_T8192_D64", "nsa_bf16_B2_Hq32_Hkv2_T8192_D128", "nsa_bf16_B1_Hq64_Hkv4_T32768_D128"]
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = {
+    "tra": "block_sparse_attention_tra_gb300/csrc/tra_bf16.cu",
+    "tra_f32": "block_sparse_attention_tra_gb300/csrc/tra_f32.cu",
+    "nsa": "block_sparse_attention_tra_gb300/csrc/nsa_select.cu",
+}
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def source_hash(kind: str) -> str:
+    with open(os.path.join(ROOT, KERNEL_SOURCES[kind]), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        tab = json.load(f)
+    ent = tab.get(workload)
+    if not ent or ent.get("source_sha") != source_hash(kind):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity for a single process)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# --------------------------------------------------------------- our kernels
+
+def make_inputs(name, device):
+    from block_sparse_attention_tra_gb300 import workloads
+
+    w = workloads.TRA_WORKLOADS.get(name) or workloads.NSA_WORKLOADS[name]
+    tensors = workloads.workload_inputs(w)
+    return w, tensors, [t.to(device) for t in tensors]
+
+
+def launcher(w, dev_tensors, out, lse=None, stream=None):
+    from block_sparse_attention_tra_gb300 import bsa, workloads
+
+    if isinstance(w, workloads.TraWorkload):
+        q, k, v = dev_tensors
+        return lambda: bsa.tra_forward(q, k, v, w.beta, w.p, out=out, stream=stream)
+    q, k, v, idx = dev_tensors
+    return lambda: bsa.nsa_select_forward(q, k, v, idx, w.block_size, out=out, lse=lse, stream=stream)
+
+
+def roofline_for(w, ms_per_launch, pk, sustained: bool):
+    from block_sparse_attention_tra_gb300 import workloads
+
+    if isinstance(w, workloads.TraWorkload):
+        achieved = w.flops / (ms_per_launch * 1e-3) / 1e12
+        peak = pk["bf16_tflops_sustained"] if sustained and pk.get("bf16_tflops_sustained") else pk["bf16_tflops"]
+        if w.dtype == "f32":
+            peak = None  # fp32 CUDA-core path: no bf16 tensor roofline applies
+        return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4) if peak else None,
+                "peak_kind": ("sustained" if sustained else "burst") + " bf16 of " + pk["source"],
+                "traffic": ncu_traffic("tra", w.name), "kernel": "tra_bf16_tcgen05_kernel",
+                "algorithmic_flops_per_launch": w.flops}
+    achieved = w.algorithmic_bytes / (ms_per_launch * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4), "peak_kind": "copy bandwidth of " + pk["source"],
+            "traffic": ncu_traffic("nsa", w.name), "kernel": "nsa_select_kernel",
+            "algorithmic_bytes_per_launch": w.algorithmic_bytes,
+            "tflops": round(w.flops / (ms_per_launch * 1e-3) / 1e12, 2),
+            "unique_bytes_per_launch": w.unique_bytes}
+
+
+def time_resident(fn, steps, warmup, world, flush=None):
+    """Device time (ms) of `steps` launches with inputs resident.  Without a
+    flush the launches run back to back between two events; with a flush each
+    launch is bracketed by its own events and the flush runs outside them."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        total = e0.elapsed_time(e1)
+    else:
+        evs = []
+        for _ in range(steps):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        total = sum(a.elapsed_time(b) for a, b in evs)
+    barrier(world)
+    return total
+
+
+def run_ours(args):
+    import torch
+
+    from block_sparse_attention_tra_gb300 import bsa, build, workloads
+
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    build.build()
+    bsa.load_library()
+    pk = peaks()
+
+    w, host, dev = make_inputs(args.workload, device)
+    out = torch.empty_like(dev[0])
+    fn = launcher(w, dev, out)
+
+    # ---- device-resident timing of the headline workload
+    with ClockSampler(device.index) as cs:
+        total_ms = time_resident(fn, args.steps, args.warmup, world)
+    total_ms = reduce_max(total_ms, world, device)
+    ms = total_ms / args.steps
+    flops_all = w.flops * world
+    value = flops_all / (total_ms / args.steps * 1e-3) / 1e12
+
+    # ---- end to end through the public API: pinned host -> device, kernel, device -> host
+    pinned = [t.pin_memory() for t in host]
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dev2 = [torch.empty_like(t) for t in dev]
+    out2 = torch.empty_like(out)
+    fn2 = launcher(w, dev2, out2)
+
+    def e2e_step():
+        for d, h in zip(dev2, pinned):
+            d.copy_(h, non_blocking=True)
+        fn2()
+        out_host.copy_(out2, non_blocking=True)
+
+    e2e_ms = reduce_max(time_resident(e2e_step, max(3, args.steps // 2), 2, world), world, device)
+    e2e_ms /= max(3, args.steps // 2)
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = out.numel() * out.element_size()
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if getattr(w, "dtype", "bf16") == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) q,k,v; no dataset)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "D": w.D, "beta": w.beta, "p": w.p,
+                   "causal": True, "l2": "no flush: q,k,v,out = %d MB > 129 MB L2" % (w.io_bytes // 2**20),
+                   "parallelism": f"replica x{world} (independent (b,h) work per GPU)"},
+        "roofline": roofline_for(w, ms, pk, sustained=False),
+        "e2e": {"value": round(flops_all / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": cs.summary(),
+    }
+
+    # ---- secondary workloads (measured, reported beside the headline)
+    if not args.no_secondary:
+        flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+
+        def flush():
+            flush_buf.fill_(1.0)
+
+        sec = []
+        for name in SECONDARY:
+            del dev, out
+            torch.cuda.empty_cache()
+            w2, _, dev = make_inputs(name, device)
+            out = torch.empty_like(dev[0])
+            lse = None
+            if isinstance(w2, workloads.NsaWorkload):
+                lse = torch.empty((w2.B, w2.Hq, w2.T), dtype=torch.float32, device=device)
+            f = launcher(w2, dev, out, lse)
+            n = max(3, args.steps // 2)
+            t = reduce_max(time_resident(f, n, 2, world, flush=flush), world, device) / n
+            entry = {"workload": w2.name, "ms_per_launch": round(t, 4),
+                     "tflops": round(w2.flops * world / (t * 1e-3) / 1e12, 3),
+                     "roofline": roofline_for(w2, t, pk, sustained=False), "l2": "flushed between launches"}
+            sec.append(entry)
+        result["secondary"] = sec
+
+    if args.cpu_baseline and rank == 0 and world == 1:
+        result["cpu_baseline"] = cpu_baseline(w, host, budget_s=args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+# ------------------------------------------------------------ CPU oracle leg
+
+def cpu_baseline(w, host, budget_s=15.0):
+    """Time the float64 oracle on the host cores on a bounded sample of the
+    same workload: whole (b, h) heads (TRA) or query rows (NSA), until about
+    `budget_s` seconds have passed.  Returns the metric in the same unit."""
+    import numpy as np
+
+    from block_sparse_attention_tra_gb300 import workloads
+    from oracle import nsa as onsa
+    from oracle import tra as otra
+
+    cores = len(os.sched_getaffinity(0))
+    if isinstance(w, workloads.TraWorkload):
+        q, k, v = host
+        done, flops, heads = 0.0, 0, 0
+        t0 = time.perf_counter()
+        for b in range(w.B):
+            for h in range(w.H):
+                qq = q[b:b + 1, h:h + 1].double().numpy()
+                kk = k[b:b + 1, h:h + 1].double().numpy()
+                vv = v[b:b + 1, h:h + 1].double().numpy()
+                otra.tra_forward(qq, kk, vv, w.beta, w.p)
+                flops += otra.tra_flops(1, 1, w.T, w.D)
+                heads += 1
+                done = time.perf_counter() - t0
+                if done >= budget_s:
+                    break
+            if done >= budget_s:
+                break
+        return {"value": round(flops / done / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                "sample": f"{heads} of {w.B * w.H} (b,h) heads of {w.name}, float64 numpy/BLAS, {done:.1f} s"}
+    q, k, v, idx = host
+    G = w.G
+    rng = np.random.default_rng(0)
+    t0 = time.perf_counter()
+    n, pairs = 0, 0
+    while time.perf_counter() - t0 < budget_s:
+        b, g, i = int(rng.integers(w.B)), int(rng.integers(w.Hkv)), int(rng.integers(w.T))
+        toks = onsa.selected_tokens(idx[b, g, i].numpy(), i, w.block_size)
+        onsa.softmax_attend(q[b, g * G:(g + 1) * G, i].double().numpy(), k[b, g, toks].double().numpy(),
+                            v[b, g, toks].double().numpy(), w.D ** -0.5)
+        n += 1
+        pairs += toks.size
+    done = time.perf_counter() - t0
+    return {"value": round(4 * G * w.D * pairs / done / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "sample": f"{n} random query groups of {w.name}, float64 numpy, {done:.1f} s"}
+
+
+def run_reference(args):
+    """The reference arm: the float64 CPU oracle, timed on the host cores on a
+    bounded sample of the same workload (rank 0 only)."""
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return None
+    from block_sparse_attention_tra_gb300 import workloads
+
+    w = workloads.TRA_WORKLOADS.get(args.workload) or workloads.NSA_WORKLOADS[args.workload]
+    host = workloads.workload_inputs(w)
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_baseline(w, host, budget_s=min(2.0, per_step))
+    vals = [cpu_baseline(w, host, budget_s=per_step) for _ in range(args.steps)]
+    value = statistics.median(v["value"] for v in vals)
+    cb = dict(vals[0])
+    cb["value"] = value
+    flops_per_step = w.flops
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(flops_per_step / (value * 1e12) * 1e3, 3) if value else None,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) q,k,v; no dataset)",
+        "config": {"workload": w.name, "sample": "bounded per step; see cpu_baseline.sample"},
+        "cpu_baseline": cb,
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

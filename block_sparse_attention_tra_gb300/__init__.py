@@ -15,6 +15,7 @@ library, which is loaded on first use and must be built (``build.build()``).
 
 from .bsa import (  # noqa: F401
     BsaError,
+    device_error,
     library_path,
     load_library,
     nsa_select_forward,
@@ -26,6 +27,7 @@ from .bsa import (  # noqa: F401
 
 __all__ = [
     "BsaError",
+    "device_error",
     "library_path",
     "load_library",
     "tra_forward",

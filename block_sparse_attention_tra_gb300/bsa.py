@@ -59,12 +59,20 @@ def load_library():
     lib.bsa_status_string.restype = ctypes.c_char_p
     lib.bsa_version.argtypes = []
     lib.bsa_version.restype = i32
+    lib.bsa_device_error.argtypes = []
+    lib.bsa_device_error.restype = i32
     _LIB = lib
     return lib
 
 
 def status_string(status: int) -> str:
     return load_library().bsa_status_string(int(status)).decode()
+
+
+def device_error() -> int:
+    """Read and clear the library's device error words (0 = none, 1 = a
+    bounded wait inside a kernel timed out, -1 = could not be read)."""
+    return int(load_library().bsa_device_error())
 
 
 def _check(status: int, what: str):
@@ -141,6 +149,8 @@ def nsa_select_forward(q, k, v, block_idx, block_size: int = 64, out=None, lse=N
         raise BsaError("nsa_select_forward takes CUDA tensors (no CPU path)")
     if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or block_idx.dim() != 4:
         raise BsaError("q [B,Hq,T,D], k/v [B,Hkv,T,D], block_idx [B,Hkv,T,S] expected", 2)
+    if not (q.dtype == k.dtype == v.dtype == torch.bfloat16):
+        raise BsaError("nsa_select_forward takes bfloat16 q, k, v", 3)
     B, Hq, T, D = q.shape
     Hkv = k.shape[1]
     S = block_idx.shape[-1]

@@ -1,0 +1,132 @@
+// api.cu -- the C ABI of libbsa.so (declared in include/bsa.h): argument
+// validation, dtype / head-dim dispatch and launch on the caller's stream.
+// Validation happens on the host before any CUDA call, so a bad argument
+// returns an error without touching the device.
+#include <math.h>
+
+#include "../../include/bsa.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace bsa {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The kernels are built for sm_103a only; refuse other devices up front
+// instead of failing inside the launch.
+int check_device() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ERR_DEVICE;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return ERR_DEVICE;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return ERR_DEVICE;
+  if (major != 10 || minor != 3) return ERR_DEVICE;
+  return OK;
+}
+
+}  // namespace
+
+int encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1, uint32_t box2) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return ERR_DEVICE;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {box0, box1, box2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? OK : ERR_SHAPE;
+}
+
+}  // namespace bsa
+
+using namespace bsa;
+
+extern "C" {
+
+int tra_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int D, float beta,
+                float p, int dtype, cudaStream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return BSA_ERR_NULLPTR;
+  if (dtype != BSA_F32 && dtype != BSA_BF16) return BSA_ERR_DTYPE;
+  if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
+  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f)) return BSA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return BSA_ERR_ALIGN;
+  const int dv = check_device();
+  if (dv != OK) return dv;
+  if (dtype == BSA_F32)
+    return launch_tra_f32(static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+                          static_cast<float*>(out), B, H, T, D, beta, p, stream);
+  return launch_tra_bf16(q, k, v, out, B, H, T, D, beta, p, stream);
+}
+
+int nsa_select_forward(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out, float* lse,
+                       int B, int Hq, int Hkv, int T, int D, int block_size, int S, cudaStream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || block_idx == nullptr || out == nullptr)
+    return BSA_ERR_NULLPTR;
+  if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || D < 1 || block_size < 1 || S < 1) return BSA_ERR_SHAPE;
+  if (Hq % Hkv != 0) return BSA_ERR_SHAPE;
+  if (T % block_size != 0) return BSA_ERR_SHAPE;
+  if (S > 32) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * Hq * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * Hq > 0x7fffffffLL || static_cast<long long>(B) * Hkv * T * S >= (1LL << 40))
+    return BSA_ERR_SHAPE;
+  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (block_size != 64) return BSA_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16) return BSA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_idx) & 3u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return BSA_ERR_ALIGN;
+  const int dv = check_device();
+  if (dv != OK) return dv;
+  return launch_nsa_select(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, block_size, S, stream);
+}
+
+const char* bsa_status_string(int status) {
+  switch (status) {
+    case BSA_OK: return "success";
+    case BSA_ERR_NULLPTR: return "a required pointer is NULL";
+    case BSA_ERR_SHAPE: return "a size is out of range or inconsistent";
+    case BSA_ERR_DTYPE: return "dtype is not a bsa_dtype value";
+    case BSA_ERR_UNSUPPORTED: return "unsupported head dim, block size, group size or parameter value";
+    case BSA_ERR_LAUNCH: return "CUDA kernel launch failed";
+    case BSA_ERR_DEVICE: return "no usable sm_103 device or CUDA driver entry point";
+    case BSA_ERR_ALIGN: return "a tensor pointer is not suitably aligned";
+    default: return "unknown bsa_status";
+  }
+}
+
+int bsa_version(void) { return 100; }
+
+int bsa_device_error(void) {
+  const unsigned codes[3] = {tra_bf16_device_error(), tra_f32_device_error(), nsa_device_error()};
+  unsigned worst = 0;
+  for (unsigned c : codes) {
+    if (c == 0xffffffffu) return -1;
+    if (c > worst) worst = c;
+  }
+  return static_cast<int>(worst);
+}
+
+}  // extern "C"

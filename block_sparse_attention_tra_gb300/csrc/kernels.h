@@ -1,0 +1,53 @@
+// kernels.h -- host-side launchers shared between the C ABI (api.cu) and the
+// kernel translation units.  Internal to libbsa.so; not installed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bsa {
+
+// Status codes mirror bsa_status in include/bsa.h.
+enum Status : int {
+  OK = 0,
+  ERR_NULLPTR = 1,
+  ERR_SHAPE = 2,
+  ERR_DTYPE = 3,
+  ERR_UNSUPPORTED = 4,
+  ERR_LAUNCH = 5,
+  ERR_DEVICE = 6,
+  ERR_ALIGN = 7,
+};
+
+// Encode a rank-3 bf16 (or other 2-byte) tensor map with 128-byte swizzle.
+// dims / box are innermost first; strides are byte strides of dims 1 and 2.
+int encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
+                   uint32_t box2);
+
+// Threshold rectified attention, fp32 CUDA-core kernel.
+int launch_tra_f32(const float* q, const float* k, const float* v, float* out, int B, int H, int T, int D,
+                   float beta, float p, cudaStream_t stream);
+
+// Threshold rectified attention, bf16 tcgen05 kernel.
+int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int D,
+                    float beta, float p, cudaStream_t stream);
+
+// NSA selection attention, bf16 kernel.
+int launch_nsa_select(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out,
+                      float* lse, int B, int Hq, int Hkv, int T, int D, int block_size, int S,
+                      cudaStream_t stream);
+
+// Read-and-clear of each kernel file's device error word (0 = none,
+// 1 = a bounded wait timed out; 0xffffffff = the read itself failed).
+unsigned int tra_bf16_device_error();
+unsigned int tra_f32_device_error();
+unsigned int nsa_device_error();
+
+// Power class of the TRA epilogue: p == 1, p == 2, or the general exp2/log2 path.
+enum PowerClass : int { POW_GENERAL = 0, POW_ONE = 1, POW_TWO = 2 };
+
+inline int power_class(float p) { return p == 1.0f ? POW_ONE : (p == 2.0f ? POW_TWO : POW_GENERAL); }
+
+}  // namespace bsa

@@ -13,9 +13,10 @@
  *   framework allocator) on the current device.  Tensors are dense, contiguous
  *   and row-major in the shapes given below; there are no stride arguments.
  *   q, k, v and out start on a 16-byte boundary.
- * - The library allocates no device memory, keeps no state between calls and
- *   never synchronises: work is enqueued on `stream` (0 = legacy default
- *   stream) and the call returns after the launch.  Inputs must stay valid and
+ * - The library allocates no device memory and never synchronises: work is
+ *   enqueued on `stream` (0 = legacy default stream) and the call returns
+ *   after the launch.  Its only state is a device error word per kernel file,
+ *   written only when a bounded wait times out (see bsa_device_error).  Inputs must stay valid and
  *   unmodified, and outputs untouched by others, until that work completes.
  * - A call returns a bsa_status.  Argument errors are detected on the host
  *   before anything is enqueued and leave every buffer untouched.  A launch
@@ -30,6 +31,12 @@
 
 #include <stdint.h>
 #include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define BSA_API __attribute__((visibility("default")))
+#else
+#define BSA_API
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -83,9 +90,9 @@ typedef enum {
  * BSA_ERR_UNSUPPORTED (D not 64/128, p <= 0, non-finite beta/p),
  * BSA_ERR_ALIGN, BSA_ERR_DEVICE, BSA_ERR_LAUNCH.
  */
-int tra_forward(const void* q, const void* k, const void* v, void* out,
-                int B, int H, int T, int D, float beta, float p, int dtype,
-                cudaStream_t stream);
+BSA_API int tra_forward(const void* q, const void* k, const void* v, void* out,
+                        int B, int H, int T, int D, float beta, float p,
+                        int dtype, cudaStream_t stream);
 
 /*
  * nsa_select_forward -- NSA selection-branch attention forward (bf16).
@@ -108,23 +115,35 @@ int tra_forward(const void* q, const void* k, const void* v, void* out,
  *                selected once; this kernel would count it twice).
  *   lse        : [B, Hq, T] fp32, or NULL to skip it.
  *   D          : 128 or 64.   block_size : 64.   1 <= S <= 32.
- *   T          : multiple of block_size.   Hq % Hkv == 0, Hq / Hkv == 16.
+ *   T          : multiple of block_size.   Hq % Hkv == 0, 1 <= Hq / Hkv <= 16.
  *   stream     : CUDA stream the kernel is enqueued on.
  *
  * Errors: BSA_ERR_NULLPTR (q, k, v, block_idx or out NULL), BSA_ERR_SHAPE,
  * BSA_ERR_UNSUPPORTED (other D, block_size or group size), BSA_ERR_ALIGN,
  * BSA_ERR_DEVICE, BSA_ERR_LAUNCH.
  */
-int nsa_select_forward(const void* q, const void* k, const void* v,
-                       const int32_t* block_idx, void* out, float* lse,
-                       int B, int Hq, int Hkv, int T, int D, int block_size,
-                       int S, cudaStream_t stream);
+BSA_API int nsa_select_forward(const void* q, const void* k, const void* v,
+                               const int32_t* block_idx, void* out, float* lse,
+                               int B, int Hq, int Hkv, int T, int D,
+                               int block_size, int S, cudaStream_t stream);
 
 /* Static, NUL-terminated description of a bsa_status value (never NULL). */
-const char* bsa_status_string(int status);
+BSA_API const char* bsa_status_string(int status);
 
 /* Library version as 10000*major + 100*minor + patch. */
-int bsa_version(void);
+BSA_API int bsa_version(void);
+
+/*
+ * bsa_device_error -- read and clear the library's device-side error words.
+ *
+ * Every wait inside the kernels (on a TMA arrival, an MMA completion or a
+ * sibling warp) is bounded to about one second; a wait that runs out records
+ * code 1 here and the kernel winds down instead of hanging (its outputs are
+ * then unspecified).  Returns 0 when no kernel has timed out since the last
+ * call, 1 after a timeout, -1 if the words could not be read.  Synchronises
+ * with the current device (cudaMemcpyFromSymbol); not for the hot path.
+ */
+BSA_API int bsa_device_error(void);
 
 #ifdef __cplusplus
 }

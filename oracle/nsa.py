@@ -68,17 +68,19 @@ def selected_tokens(sel_row, i: int, block_size: int) -> np.ndarray:
     return toks[toks <= i]
 
 
-def _one_query(qg, kk, vv, toks, scale):
-    """Softmax attention of the G query rows ``qg [G, D]`` over the gathered
-    keys/values ``kk[toks], vv[toks]``; returns (out [G, D], lse [G])."""
+def softmax_attend(qg, ks, vs, scale):
+    """Softmax attention of the G query rows ``qg [G, D]`` over already
+    gathered keys/values ``ks, vs [n, D]``; returns (out [G, D], lse [G]).
+    With ``n == 0`` the row is empty: out 0, lse ``-1e9``."""
+    qg = np.asarray(qg, dtype=np.float64)
     G, D = qg.shape
-    if toks.size == 0:
+    if len(ks) == 0:
         return np.zeros((G, D)), np.full(G, LSE_EMPTY)
-    s = (qg @ kk[toks].T) * scale  # [G, |J|]
+    s = (qg @ np.asarray(ks, dtype=np.float64).T) * scale  # [G, n]
     m = s.max(axis=1, keepdims=True)
     e = np.exp(s - m)
     l = e.sum(axis=1, keepdims=True)
-    out = (e @ vv[toks]) / l
+    out = (e @ np.asarray(vs, dtype=np.float64)) / l
     lse = (m + np.log(l))[:, 0]
     return out, lse
 
@@ -97,7 +99,7 @@ def nsa_select_forward(q, k, v, block_idx, block_size: int):
             hs = slice(g * G, (g + 1) * G)
             for i in range(T):
                 toks = selected_tokens(idx[b, g, i], i, block_size)
-                o, l_ = _one_query(q[b, hs, i], k[b, g], v[b, g], toks, scale)
+                o, l_ = softmax_attend(q[b, hs, i], k[b, g, toks], v[b, g, toks], scale)
                 out[b, hs, i] = o
                 lse[b, hs, i] = l_
     return out, lse
@@ -118,7 +120,7 @@ def nsa_select_rows(q, k, v, block_idx, block_size: int, rows):
     lse = np.zeros((len(rows), G))
     for n, (b, g, i) in enumerate(rows):
         toks = selected_tokens(idx[b, g, i], i, block_size)
-        out[n], lse[n] = _one_query(q[b, g * G:(g + 1) * G, i], k[b, g], v[b, g], toks, scale)
+        out[n], lse[n] = softmax_attend(q[b, g * G:(g + 1) * G, i], k[b, g, toks], v[b, g, toks], scale)
     return out, lse
 
 

@@ -1,0 +1,112 @@
+"""CPU checks of the C ABI: the library loads, exports every entry point that
+``include/bsa.h`` declares, and rejects bad arguments on the host before any
+device work (no compute call is made here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_attention_tra_gb300 import build, bsa
+
+    build.build()
+    return bsa.load_library()
+
+
+def header_functions():
+    txt = open(os.path.join(ROOT, "include", "bsa.h")).read()
+    return re.findall(r"^BSA_API\s+[\w\s\*]+?\b(\w+)\(", txt, flags=re.M)
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    for n in ("tra_forward", "nsa_select_forward", "bsa_status_string", "bsa_version", "bsa_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    from block_sparse_attention_tra_gb300 import bsa
+
+    for code in range(8):
+        s = bsa.status_string(code)
+        assert s and s != "unknown bsa_status"
+    assert bsa.status_string(99) == "unknown bsa_status"
+    assert lib.bsa_version() >= 100
+
+
+P = 4096  # a fake, 16-byte aligned "device" address: validation must reject before using it
+
+
+def tra(lib, q=P, k=P, v=P, o=P, B=1, H=1, T=16, D=64, beta=1.0, p=2.0, dtype=1):
+    from block_sparse_attention_tra_gb300 import bsa
+
+    return bsa.tra_forward_raw(q, k, v, o, B, H, T, D, beta, p, dtype, 0)
+
+
+def nsa(lib, q=P, k=P, v=P, idx=P, o=P, lse=None, B=1, Hq=16, Hkv=1, T=128, D=128, bs=64, S=4):
+    from block_sparse_attention_tra_gb300 import bsa
+
+    return bsa.nsa_select_forward_raw(q, k, v, idx, o, lse, B, Hq, Hkv, T, D, bs, S, 0)
+
+
+def test_tra_argument_errors(lib):
+    assert tra(lib, q=None) == 1
+    assert tra(lib, o=None) == 1
+    assert tra(lib, dtype=7) == 3
+    assert tra(lib, B=0) == 2
+    assert tra(lib, T=0) == 2
+    assert tra(lib, T=-5) == 2
+    assert tra(lib, D=96) == 4
+    assert tra(lib, D=32) == 4
+    assert tra(lib, p=0.0) == 4
+    assert tra(lib, p=-1.0) == 4
+    assert tra(lib, p=float("nan")) == 4
+    assert tra(lib, beta=float("inf")) == 4
+    assert tra(lib, q=P + 8) == 7
+    assert tra(lib, B=1 << 20, H=1 << 12, T=1 << 10, D=128) == 2  # B*H*T*D >= 2^40
+
+
+def test_nsa_argument_errors(lib):
+    assert nsa(lib, idx=None) == 1
+    assert nsa(lib, v=None) == 1
+    assert nsa(lib, Hq=24, Hkv=16) == 2  # not a multiple
+    assert nsa(lib, T=100) == 2  # T % block_size
+    assert nsa(lib, S=0) == 2
+    assert nsa(lib, S=33) == 2
+    assert nsa(lib, D=96) == 4
+    assert nsa(lib, bs=32, T=128) == 4
+    assert nsa(lib, Hq=32, Hkv=1) == 4  # group of 32 heads
+    assert nsa(lib, k=P + 4) == 7
+    assert nsa(lib, idx=P + 2) == 7
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the no-device path")
+def test_valid_arguments_without_a_device_report_device_error(lib):
+    assert tra(lib) == 6
+    assert nsa(lib) == 6
+
+
+def test_binding_has_no_cpu_path():
+    import torch
+
+    from block_sparse_attention_tra_gb300 import BsaError, nsa_select_forward, tra_forward
+
+    x = torch.zeros(1, 1, 8, 64)
+    with pytest.raises(BsaError):
+        tra_forward(x, x, x, 1.0, 2.0)
+    idx = torch.zeros(1, 1, 64, 1, dtype=torch.int32)
+    xb = torch.zeros(1, 16, 64, 64, dtype=torch.bfloat16)
+    with pytest.raises(BsaError):
+        nsa_select_forward(xb, xb[:, :1], xb[:, :1], idx)

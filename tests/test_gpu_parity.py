@@ -1,0 +1,238 @@
+"""GPU parity: the CUDA library (through the C ABI) against the float64 oracle
+on the same seeded inputs.
+
+Bars (written here, from the method's precision):
+* bf16 inputs: max|gpu - ref| <= 2e-2 * max|ref| over the compared outputs;
+* fp32 inputs: max|gpu - ref| <= 1e-4 * max|ref|;
+* NSA lse: |gpu - ref| <= 1e-2 on rows with a valid key; exactly -1e9 on
+  empty rows; an empty row's output is exactly 0.
+
+Small cases compare every output and span several tiles plus a ragged tail;
+the full workloads run in the launch configuration the benchmark times and
+are compared on sampled rows that the oracle computes one by one.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from block_sparse_attention_tra_gb300 import bsa, workloads
+from oracle import nsa as onsa
+from oracle import tra as otra
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL = 2e-2
+F32_TOL = 1e-4
+LSE_TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_sparse_attention_tra_gb300 import build
+
+    build.build()
+    bsa.load_library()
+    torch.cuda.set_device(0)
+    yield
+    assert bsa.device_error() == 0
+
+
+def f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def rel_err(gpu, ref):
+    return float(np.abs(gpu - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
+
+
+def run_tra(q, k, v, beta, p):
+    out = bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), beta, p)
+    torch.cuda.synchronize()
+    return f64(out)
+
+
+# ----------------------------------------------------------------- TRA, full compare
+
+TRA_SMALL = [
+    # (B, H, T, D, beta, p, dtype)
+    (1, 2, 256, 64, 1.0, 2.0, "f32"),     # the fp32 workload itself
+    (1, 1, 1, 64, 1.0, 2.0, "f32"),
+    (2, 1, 130, 128, 0.5, 1.5, "f32"),    # ragged, general power
+    (1, 2, 77, 64, -0.5, 1.0, "f32"),     # beta < 0 reading
+    (1, 2, 384, 128, 1.0, 2.0, "bf16"),   # 3 row tiles
+    (1, 2, 300, 128, 1.0, 2.0, "bf16"),   # ragged tail
+    (1, 2, 333, 64, 2.0, 1.5, "bf16"),    # general power, D = 64
+    (1, 1, 1, 64, 1.0, 2.0, "bf16"),      # T = 1
+    (1, 1, 129, 128, 0.0, 1.0, "bf16"),   # p = 1, beta = 0: causal ReLU attention
+    (2, 1, 200, 64, -1.0, 2.0, "bf16"),   # beta < 0 reading
+    (1, 2, 257, 128, 0.7, 3.7, "bf16"),   # another general power
+    (3, 5, 640, 64, 1.0, 2.0, "bf16"),    # many (b, h), 5 row tiles
+]
+
+
+@pytest.mark.parametrize("B,H,T,D,beta,p,dtype", TRA_SMALL)
+def test_tra_small_full_output(B, H, T, D, beta, p, dtype):
+    q, k, v = workloads.tra_inputs(B, H, T, D, dtype, seed=T + D)
+    gpu = run_tra(q, k, v, beta, p)
+    ref = otra.tra_forward(f64(q), f64(k), f64(v), beta, p)
+    tol = F32_TOL if dtype == "f32" else BF16_TOL
+    err = rel_err(gpu, ref)
+    assert err <= tol, f"max err {err:.3e} of max|ref| (tol {tol})"
+
+
+def test_tra_huge_beta_only_row0():
+    q, k, v = workloads.tra_inputs(2, 2, 256, 64, "bf16", seed=3)
+    gpu = run_tra(q, k, v, 1e6, 2.0)
+    assert np.all(gpu[:, :, 1:] == 0.0)
+    s = np.einsum("bhd,bhd->bh", f64(q)[:, :, 0], f64(k)[:, :, 0])
+    ref0 = (np.maximum(s, 0) ** 2)[..., None] * f64(v)[:, :, 0]
+    assert rel_err(gpu[:, :, 0], ref0) <= BF16_TOL
+
+
+def test_tra_repeatable_and_stream():
+    q, k, v = workloads.tra_inputs(1, 4, 512, 128, "bf16", seed=9)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    a = bsa.tra_forward(q, k, v, 1.0, 2.0)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b = bsa.tra_forward(q, k, v, 1.0, 2.0, stream=s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)  # deterministic: no atomics, fixed order
+
+
+def test_tra_out_of_place_canary():
+    """Writes only [B, H, T, D]: guard bands around out stay untouched."""
+    B, H, T, D = 1, 2, 200, 64
+    q, k, v = workloads.tra_inputs(B, H, T, D, "bf16", seed=5)
+    n = B * H * T * D
+    buf = torch.full((n + 2 * 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[4096:4096 + n].view(B, H, T, D)
+    bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), 1.0, 2.0, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:4096] == 7.0) and torch.all(buf[4096 + n:] == 7.0)
+
+
+# ----------------------------------------------------- TRA, full workloads, sampled rows
+
+def _sample_rows(B, H, T, n, seed):
+    r = np.random.default_rng(seed)
+    rows = {(0, 0, 0), (B - 1, H - 1, T - 1), (0, H - 1, 127), (B - 1, 0, 128), (0, 0, T // 2)}
+    while len(rows) < n:
+        rows.add((int(r.integers(B)), int(r.integers(H)), int(r.integers(T))))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", ["tra_bf16_B4_H16_T4096_D128", "tra_bf16_B2_H32_T8192_D64",
+                                  "tra_f32_B1_H2_T256_D64"])
+def test_tra_full_workload_sampled_rows(name):
+    w = workloads.TRA_WORKLOADS[name]
+    q, k, v = workloads.workload_inputs(w)
+    gpu = run_tra(q, k, v, w.beta, w.p) if w.T <= 256 else None
+    if gpu is None:
+        out = bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), w.beta, w.p)
+        torch.cuda.synchronize()
+    rows = _sample_rows(w.B, w.H, w.T, 96, seed=1)
+    got, ref = [], []
+    by_bh = {}
+    for (b, h, i) in rows:
+        by_bh.setdefault((b, h), []).append(i)
+    for (b, h), iis in by_bh.items():
+        sub = [(0, 0, i) for i in iis]
+        r = otra.tra_rows(f64(q[b:b + 1, h:h + 1]), f64(k[b:b + 1, h:h + 1]), f64(v[b:b + 1, h:h + 1]),
+                          w.beta, w.p, sub)
+        ref.append(r)
+        if gpu is not None:
+            got.append(gpu[b, h, iis])
+        else:
+            got.append(f64(out[b, h, iis]))
+    got, ref = np.concatenate(got), np.concatenate(ref)
+    tol = F32_TOL if w.dtype == "f32" else BF16_TOL
+    err = rel_err(got, ref)
+    assert err <= tol, f"max err {err:.3e} of max|ref| (tol {tol})"
+
+
+# ------------------------------------------------------------------------- NSA
+
+def run_nsa(q, k, v, idx):
+    out, lse = bsa.nsa_select_forward(q.cuda(), k.cuda(), v.cuda(), idx.cuda(), 64, return_lse=True)
+    torch.cuda.synchronize()
+    return f64(out), f64(lse)
+
+
+def check_nsa(gpu_o, gpu_l, ref_o, ref_l):
+    err = rel_err(gpu_o, ref_o)
+    assert err <= BF16_TOL, f"out: max err {err:.3e} of max|ref|"
+    empty = ref_l == -1e9
+    assert np.all(gpu_l[empty] == -1e9)
+    assert np.all(gpu_o[np.broadcast_to(empty[..., None], gpu_o.shape)] == 0.0)
+    if np.any(~empty):
+        lerr = float(np.abs(gpu_l[~empty] - ref_l[~empty]).max())
+        assert lerr <= LSE_TOL, f"lse: max abs err {lerr:.3e}"
+
+
+NSA_SMALL = [
+    # (B, Hq, Hkv, T, D, S)
+    (1, 16, 1, 512, 128, 16),
+    (2, 32, 2, 384, 128, 4),
+    (1, 32, 2, 1024, 64, 8),
+    (1, 8, 2, 256, 128, 4),    # G = 4 (rows 4..15 of the MMA padded)
+    (1, 16, 1, 64, 128, 1),    # one block, S = 1
+    (1, 16, 4, 320, 64, 32),   # G = 4, S = 32
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,T,D,S", NSA_SMALL)
+def test_nsa_small_full_output(B, Hq, Hkv, T, D, S):
+    q, k, v, idx = workloads.nsa_inputs(B, Hq, Hkv, T, D, 64, S, seed=T + S)
+    go, gl = run_nsa(q, k, v, idx)
+    ro, rl = onsa.nsa_select_forward(f64(q), f64(k), f64(v), idx.numpy(), 64)
+    check_nsa(go, gl, ro, rl)
+
+
+def test_nsa_padding_future_and_out_of_range_slots():
+    B, Hq, Hkv, T, D, S = 1, 16, 1, 256, 128, 4
+    q, k, v, idx = workloads.nsa_inputs(B, Hq, Hkv, T, D, 64, S, seed=21)
+    idx[0, 0, 10:20, :] = -1                # empty rows
+    idx[0, 0, 30:40, 0] = 3                 # a future block only
+    idx[0, 0, 30:40, 1:] = -1
+    idx[0, 0, 100:110, 2] = 2               # future block next to valid ones
+    go, gl = run_nsa(q, k, v, idx)
+    ro, rl = onsa.nsa_select_forward(f64(q), f64(k), f64(v), idx.numpy(), 64)
+    check_nsa(go, gl, ro, rl)
+    assert np.all(gl[0, :, 10:20] == -1e9) and np.all(go[0, :, 10:20] == 0)
+
+
+def test_nsa_without_lse_matches():
+    q, k, v, idx = workloads.nsa_inputs(1, 16, 1, 256, 128, 64, 4, seed=2)
+    a = bsa.nsa_select_forward(q.cuda(), k.cuda(), v.cuda(), idx.cuda(), 64)
+    b, _ = bsa.nsa_select_forward(q.cuda(), k.cuda(), v.cuda(), idx.cuda(), 64, return_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name", list(workloads.NSA_WORKLOADS))
+def test_nsa_full_workload_sampled_rows(name):
+    w = workloads.NSA_WORKLOADS[name]
+    q, k, v, idx = workloads.workload_inputs(w)
+    out, lse = bsa.nsa_select_forward(q.cuda(), k.cuda(), v.cuda(), idx.cuda(), w.block_size, return_lse=True)
+    torch.cuda.synchronize()
+    r = np.random.default_rng(3)
+    rows = {(0, 0, 0), (0, 0, 63), (0, 0, 64), (w.B - 1, w.Hkv - 1, w.T - 1), (0, w.Hkv - 1, 1000)}
+    while len(rows) < 64:
+        rows.add((int(r.integers(w.B)), int(r.integers(w.Hkv)), int(r.integers(w.T))))
+    rows = sorted(rows)
+    G = w.G
+    got_o, got_l, ref_o, ref_l = [], [], [], []
+    for (b, g, i) in rows:
+        toks = onsa.selected_tokens(idx[b, g, i].numpy(), i, w.block_size)
+        o1, l1 = onsa.softmax_attend(f64(q[b, g * G:(g + 1) * G, i]), f64(k[b, g, toks]), f64(v[b, g, toks]),
+                                     w.D ** -0.5)
+        ref_o.append(o1)
+        ref_l.append(l1)
+        got_o.append(f64(out[b, g * G:(g + 1) * G, i]))
+        got_l.append(f64(lse[b, g * G:(g + 1) * G, i]))
+    check_nsa(np.stack(got_o), np.stack(got_l), np.stack(ref_o), np.stack(ref_l))

@@ -474,13 +474,17 @@ def test_planted_nsa_mistakes_are_caught(golden, monkeypatch):
         assert not pins(), bad.__name__
     monkeypatch.setattr(nsa, "selected_tokens", good_sel)
 
-    good_one = nsa._one_query
+    good_one = nsa.softmax_attend
 
-    def no_scale(qg, kk, vv, toks, scale):
-        return good_one(qg, kk, vv, toks, 1.0)
+    def no_scale(qg, ks, vs, scale):
+        return good_one(qg, ks, vs, 1.0)
 
-    for bad in (no_scale,):
-        monkeypatch.setattr(nsa, "_one_query", bad)
+    def no_max_shift_lse(qg, ks, vs, scale):
+        o, l = good_one(qg, ks, vs, scale)
+        return o, l - (np.asarray(qg) @ np.asarray(ks).T * scale).max(axis=1) if len(ks) else l
+
+    for bad in (no_scale, no_max_shift_lse):
+        monkeypatch.setattr(nsa, "softmax_attend", bad)
         assert not pins(), bad.__name__
-    monkeypatch.setattr(nsa, "_one_query", good_one)
+    monkeypatch.setattr(nsa, "softmax_attend", good_one)
     assert pins()
