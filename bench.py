@@ -95,6 +95,9 @@ class ClockSampler:
                  "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.time()  # the first sample takes a moment; start the load after it
+            while not self.lines and time.time() - t0 < 5.0 and self.proc.poll() is None:
+                time.sleep(0.02)
         except OSError:
             self.proc = None
         return self
@@ -201,10 +204,12 @@ def roofline_for(w, ms_per_launch, pk, sustained: bool):
             "unique_bytes_per_launch": w.unique_bytes}
 
 
-def time_resident(fn, steps, warmup, world, flush=None):
+def time_resident(fn, steps, warmup, world, flush=None, soak_s=0.0):
     """Device time (ms) of `steps` launches with inputs resident.  Without a
     flush the launches run back to back between two events; with a flush each
-    launch is bracketed by its own events and the flush runs outside them."""
+    launch is bracketed by its own events and the flush runs outside them.
+    `soak_s` seconds of further untimed launches follow, so that a clock
+    sampler running around the call sees the GPU under this load."""
     import torch
 
     for _ in range(warmup):
@@ -231,6 +236,12 @@ def time_resident(fn, steps, warmup, world, flush=None):
             evs.append((a, b))
         torch.cuda.synchronize()
         total = sum(a.elapsed_time(b) for a, b in evs)
+    if soak_s > 0:
+        t0 = time.time()
+        while time.time() - t0 < soak_s:
+            for _ in range(8):
+                fn()
+            torch.cuda.synchronize()
     barrier(world)
     return total
 
@@ -259,7 +270,7 @@ def run_ours(args):
 
     # ---- device-resident timing of the headline workload
     with ClockSampler(device.index) as cs:
-        total_ms = time_resident(fn, args.steps, args.warmup, world)
+        total_ms = time_resident(fn, args.steps, args.warmup, world, soak_s=args.clock_soak)
     total_ms = reduce_max(total_ms, world, device)
     ms = total_ms / args.steps
     flops_all = w.flops * world
@@ -438,6 +449,8 @@ def main(argv=None):
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--clock-soak", type=float, default=1.5,
+                    help="seconds of untimed launches after the timed region, under the clock sampler")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     res = run_reference(args) if args.impl == "reference" else run_ours(args)
