@@ -38,6 +38,30 @@ def tra_forward(q, k, v, beta, p):
     return out
 
 
+def tra_backward(q, k, v, dout, beta, p):
+    """Scalar loops of the TRA backward; returns (dq, dk, dv) nested lists."""
+    B, H, T, D = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
+    z = lambda: [[[[0.0] * D for _ in range(T)] for _ in range(H)] for _ in range(B)]  # noqa: E731
+    dq, dk, dv = z(), z(), z()
+    for b in range(B):
+        for h in range(H):
+            for i in range(T):
+                t = beta * math.sqrt(2.0 * math.log(i + 1) / D)
+                for j in range(i + 1):
+                    s = sum(q[b][h][i][d] * k[b][h][j][d] for d in range(D))
+                    x = s - t
+                    if x <= 0.0:
+                        continue
+                    w = x ** p
+                    gw = p * x ** (p - 1.0)
+                    dw = sum(dout[b][h][i][d] * v[b][h][j][d] for d in range(D))
+                    for d in range(D):
+                        dv[b][h][j][d] += w * dout[b][h][i][d]
+                        dq[b][h][i][d] += dw * gw * k[b][h][j][d]
+                        dk[b][h][j][d] += dw * gw * q[b][h][i][d]
+    return dq, dk, dv
+
+
 def nsa_select_forward(q, k, v, block_idx, block_size):
     """q [B][Hq][T][D], k/v [B][Hkv][T][D], block_idx [B][Hkv][T][S] ->
     (out [B][Hq][T][D], lse [B][Hq][T])."""

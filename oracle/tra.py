@@ -105,7 +105,67 @@ def tra_rows(q, k, v, beta: float, p: float, rows) -> np.ndarray:
     return res
 
 
+def relu_power_grad(x: np.ndarray, p: float) -> np.ndarray:
+    """Derivative of ``ReLU(x)**p``: ``p * x**(p-1)`` where ``x > 0``, else 0.
+
+    The page's backward kernels use the same convention at the kink: the
+    derivative is 0 for ``x <= 0`` (p == 1 branch: ``where(qk_thresh > 0, 1,
+    0)``; general branch: ``where(qk_relu > 0, ...)``)."""
+    if not p > 0:
+        raise ValueError("relu power p must be > 0")
+    out = np.zeros_like(x, dtype=np.float64)
+    pos = x > 0
+    out[pos] = float(p) * np.power(x[pos], float(p) - 1.0)
+    return out
+
+
+def tra_backward(q, k, v, dout, beta: float, p: float, block: int = 256):
+    """Gradients ``(dq, dk, dv)`` of ``sum(out * dout)`` for the TRA forward.
+
+    Page "triton_threshold_attention.py", ``ThresholdRelaFunction.backward``
+    and the kernels ``_threshold_rela_bwd_kernel_dq`` / ``_dkv``: with
+    ``x_ij = q_i.k_j - tau(i)`` over the causal pairs ``j <= i``,
+
+        W_ij  = ReLU(x_ij)^p,          dV_j = sum_i W_ij dout_i,
+        dA_ij = (dout_i . v_j) * p ReLU(x_ij)^(p-1),
+        dQ_i  = sum_j dA_ij k_j,        dK_j = sum_i dA_ij q_i.
+
+    tau does not depend on q or k, and neither beta nor p receives a
+    gradient (the page returns None for both).  Masked pairs contribute
+    nothing (same reading as the forward).
+    """
+    q, k, v = _check(q, k, v)
+    dout = np.asarray(dout, dtype=np.float64)
+    if dout.shape != q.shape:
+        raise ValueError("dout must have the shape of q")
+    B, H, T, D = q.shape
+    t = tau(T, beta, D)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            for i0 in range(0, T, block):
+                i1 = min(T, i0 + block)
+                x = q[b, h, i0:i1] @ k[b, h, :i1].T - t[i0:i1, None]  # [rows, keys]
+                keep = np.arange(i1)[None, :] <= np.arange(i0, i1)[:, None]
+                w = np.where(keep, relu_power(x, p), 0.0)
+                g = np.where(keep, relu_power_grad(x, p), 0.0)
+                da = (dout[b, h, i0:i1] @ v[b, h, :i1].T) * g
+                dv[b, h, :i1] += w.T @ dout[b, h, i0:i1]
+                dq[b, h, i0:i1] += da @ k[b, h, :i1]
+                dk[b, h, :i1] += da.T @ q[b, h, i0:i1]
+    return dq, dk, dv
+
+
 def tra_flops(B: int, H: int, T: int, D: int) -> int:
     """Algorithmic FLOPs of one causal TRA forward: two multiply-adds of length
     D (one for q_i.k_j, one for w_ij v_j) per causally valid pair (i, j<=i)."""
     return 4 * D * B * H * (T * (T + 1) // 2)
+
+
+def tra_backward_flops(B: int, H: int, T: int, D: int) -> int:
+    """Algorithmic FLOPs of one causal TRA backward: per causal pair four
+    multiply-adds of length D (dout_i.v_j, dV_j += W dout_i, dQ_i += dA k_j,
+    dK_j += dA q_i) plus the recomputed score q_i.k_j."""
+    return 10 * D * B * H * (T * (T + 1) // 2)

@@ -488,3 +488,82 @@ def test_planted_nsa_mistakes_are_caught(golden, monkeypatch):
         assert not pins(), bad.__name__
     monkeypatch.setattr(nsa, "softmax_attend", good_one)
     assert pins()
+
+
+# ------------------------------------------------------------- TRA backward
+
+def _torch_tra(q, k, v, beta, p):
+    """TRA forward written with torch fp64 ops, differentiated by autograd."""
+    T, D = q.shape[-2], q.shape[-1]
+    i = torch.arange(T, dtype=torch.float64)
+    tau = beta * torch.sqrt(2.0 * torch.log(i + 1.0) / D)
+    x = q @ k.transpose(-1, -2) - tau[:, None]
+    keep = torch.tril(torch.ones(T, T, dtype=torch.bool))
+    w = torch.where(keep & (x > 0), torch.relu(x) ** p, torch.zeros_like(x))
+    return w @ v
+
+
+@pytest.mark.parametrize("p", [1.0, 2.0, 1.5, 3.7])
+@pytest.mark.parametrize("beta", [0.0, 0.8])
+def test_tra_backward_matches_torch_autograd(p, beta):
+    q, k, v = rand_tra(2, 2, 37, 8, seed=20)
+    do = rng(21).standard_normal(q.shape)
+    dq, dk, dv = tra.tra_backward(q, k, v, do, beta, p, block=16)
+    qt, kt, vt = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+    out = _torch_tra(qt, kt, vt, beta, p)
+    gq, gk, gv = torch.autograd.grad((out * torch.tensor(do)).sum(), (qt, kt, vt))
+    np.testing.assert_allclose(dq, gq.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, gk.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, gv.numpy(), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("p", [2.0, 1.5, 3.7])
+def test_tra_backward_finite_differences(p):
+    """Central differences of L = sum(out * dout) (p > 1: L is C^1)."""
+    q, k, v = rand_tra(1, 1, 9, 4, seed=22)
+    do = rng(23).standard_normal(q.shape)
+    beta = 0.3
+    dq, dk, dv = tra.tra_backward(q, k, v, do, beta, p)
+
+    def L(qq, kk, vv):
+        return float((tra.tra_forward(qq, kk, vv, beta, p) * do).sum())
+
+    h = 1e-6
+    r = rng(24)
+    for grad, which in ((dq, 0), (dk, 1), (dv, 2)):
+        for _ in range(12):
+            idx = tuple(int(r.integers(n)) for n in q.shape)
+            args = [q.copy(), k.copy(), v.copy()]
+            args[which][idx] += h
+            lp = L(*args)
+            args[which][idx] -= 2 * h
+            lm = L(*args)
+            assert grad[idx] == pytest.approx((lp - lm) / (2 * h), rel=1e-5, abs=1e-7)
+
+
+def test_tra_backward_brute_agrees():
+    q, k, v = rand_tra(1, 2, 11, 3, seed=25)
+    do = rng(26).standard_normal(q.shape)
+    for p, beta in ((2.0, 0.5), (1.5, 0.0), (1.0, -0.4)):
+        got = tra.tra_backward(q, k, v, do, beta, p, block=4)
+        want = brute.tra_backward(q.tolist(), k.tolist(), v.tolist(), do.tolist(), beta, p)
+        for g, w_ in zip(got, want):
+            np.testing.assert_allclose(g, np.array(w_), rtol=1e-11, atol=1e-12)
+
+
+def test_tra_backward_textbook_beta0_p1():
+    """beta = 0, p = 1: W = tril(ReLU(QK^T)), dV = W^T dO,
+    dS = (dO V^T) * tril(QK^T > 0), dQ = dS K, dK = dS^T Q."""
+    q, k, v = rand_tra(1, 1, 30, 6, seed=27)
+    do = rng(28).standard_normal(q.shape)
+    dq, dk, dv = tra.tra_backward(q, k, v, do, 0.0, 1.0)
+    s = q[0, 0] @ k[0, 0].T
+    w = np.tril(np.maximum(s, 0))
+    ds = np.tril((s > 0).astype(float)) * (do[0, 0] @ v[0, 0].T)
+    np.testing.assert_allclose(dv[0, 0], w.T @ do[0, 0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dq[0, 0], ds @ k[0, 0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dk[0, 0], ds.T @ q[0, 0], rtol=1e-12, atol=1e-12)
+
+
+def test_tra_backward_flops_count():
+    assert tra.tra_backward_flops(1, 1, 3, 2) == 10 * 2 * 6
