@@ -3,7 +3,7 @@
 The epilogue splits x = 2^e * m (m in [1, 2)) with integer bit operations
 and approximates log2(m) by a degree-4 polynomial in m, fitted here by least
 squares on Chebyshev nodes of [1, 2] (a near-minimax fit).  Run this script
-to regenerate the constants in ``tra_log2_poly.h``; it prints the header and
+to regenerate the constants LOG2_C0..LOG2_C4 of ``tra_bf16.cu``; it prints the header and
 the maximum absolute error of the fit in float64 and when evaluated in
 float32 Horner form.
 """
@@ -34,4 +34,4 @@ if __name__ == "__main__":
     e64 = np.abs(np.polyval(c[::-1], mt) - np.log2(mt)).max()
     e32 = np.abs(eval_f32(c, mt).astype(np.float64) - np.log2(mt)).max()
     print("// log2(m) ~= sum_k LOG2_POLY[k] * m^k on [1, 2); max |err| %.2e (f64), %.2e (f32 Horner)" % (e64, e32))
-    print("constexpr float LOG2_POLY[%d] = {%s};" % (DEG + 1, ", ".join("%.9ef" % v for v in c)))
+    print("constexpr float " + ", ".join("LOG2_C%d = %.9ef" % (k, v) for k, v in enumerate(c)) + ";")

@@ -9,13 +9,13 @@
 //
 // Gather, not scan: each selected block is fetched as one 64-token K tile and
 // one V tile by TMA (box 64 x 64 of a [B*Hkv, T, D] tensor map, 128-byte
-// swizzle) into a 4-stage ring.  The G heads of the group are the 16 rows of
-// mma.sync.m16n8k16 (rows >= G are zero).  Four consumer warps split every
-// 64-token block into 16-token slices, each keeping its own online-softmax
-// state (running max m, partial sum l, 16 x D accumulator); at the end of a
-// query the four states are merged through shared memory.  A fifth warp is the
-// TMA producer.  The grid is persistent: CTA c takes query groups
-// c, c + gridDim.x, ...
+// swizzle) into a 2-stage ring per CTA.  The G heads of the group are the 16
+// rows of mma.sync.m16n8k16 (rows >= G are zero).  Four consumer warps split
+// every 64-token block into 16-token slices, each keeping its own online-
+// softmax state (running max m, partial sum l, 16 x D accumulator); at the end
+// of a query the four states are merged through shared memory.  A fifth warp
+// is the TMA producer.  The grid is persistent with two CTAs per SM: CTA c
+// takes query groups c, c + gridDim.x, ...
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -25,7 +25,7 @@ namespace {
 constexpr int NSA_BS = 64;        // tokens per selected block
 constexpr int NSA_CONSUMERS = 4;  // consumer warps (16 tokens each)
 constexpr int NSA_THREADS = (NSA_CONSUMERS + 1) * 32;
-constexpr int NSA_NS = 4;         // K/V stages
+constexpr int NSA_NS = 2;         // K/V stages per CTA (two CTAs per SM)
 constexpr int NSA_NQ = 2;         // Q stages
 
 template <int D>
@@ -84,7 +84,7 @@ __device__ __forceinline__ bool slot_live(int blk, int i, int n_blk) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(NSA_THREADS, 1)
+__global__ void __launch_bounds__(NSA_THREADS, 2)
     nsa_select_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const int32_t* __restrict__ block_idx,
                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int Hq, int Hkv, int G, int T,
@@ -240,30 +240,38 @@ __global__ void __launch_bounds__(NSA_THREADS, 1)
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: tok0 <= i
-        const float al0 = ex2f(m0 - mn0), al1 = ex2f(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
+        // Lazy rescale: keep the running max unless a new score exceeds it
+        // by more than 8 (log2 units) in some row of the warp; exp2(s - m)
+        // then stays below 2^8 and the accumulator is rescaled only rarely.
+        // The first live slice always rescales (m = -inf).
+        if (__any_sync(0xffffffffu, mx0 > m0 + 8.0f || mx1 > m1 + 8.0f)) {
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: tok0 <= i
+          const float al0 = ex2f(m0 - mn0), al1 = ex2f(m1 - mn1);
+          m0 = mn0;
+          m1 = mn1;
+          l0 *= al0;
+          l1 *= al1;
+#pragma unroll
+          for (int j = 0; j < D / 8; ++j) {
+            acc[j][0] *= al0;
+            acc[j][1] *= al0;
+            acc[j][2] *= al1;
+            acc[j][3] *= al1;
+          }
+        }
         uint32_t pa[4];
         float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const float p0 = ex2f(sc[j][0] - mn0), p1 = ex2f(sc[j][1] - mn0);
-          const float p2 = ex2f(sc[j][2] - mn1), p3 = ex2f(sc[j][3] - mn1);
+          const float p0 = ex2f(sc[j][0] - m0), p1 = ex2f(sc[j][1] - m0);
+          const float p2 = ex2f(sc[j][2] - m1), p3 = ex2f(sc[j][3] - m1);
           rs0 += p0 + p1;
           rs1 += p2 + p3;
           pa[2 * j + 0] = pack_bf16x2(p0, p1);  // row g,     k = 8j + 2t
           pa[2 * j + 1] = pack_bf16x2(p2, p3);  // row g + 8, k = 8j + 2t
         }
-        l0 = l0 * al0 + rs0;
-        l1 = l1 * al1 + rs1;
-#pragma unroll
-        for (int j = 0; j < D / 8; ++j) {
-          acc[j][0] *= al0;
-          acc[j][1] *= al0;
-          acc[j][2] *= al1;
-          acc[j][3] *= al1;
-        }
+        l0 += rs0;
+        l1 += rs1;
         // ---- O += P V over this slice (k = 16 tokens)
         {
           const int vrow = 16 * warp + 8 * (mat & 1) + mrow;  // token row
@@ -353,7 +361,7 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return ERR_DEVICE;
   const long long nq = static_cast<long long>(B) * Hkv * T;
-  const long long grid = nq < sms ? nq : sms;
+  const long long grid = nq < 2 * sms ? nq : 2 * sms;  // two CTAs per SM
   const float scale_log2 = (1.0f / sqrtf(static_cast<float>(D))) * 1.4426950408889634f;
   kern<<<static_cast<unsigned>(grid), NSA_THREADS, L::ALLOC, stream>>>(
       mq, mk, mv, idx, static_cast<__nv_bfloat16*>(out), lse, Hq, Hkv, Hq / Hkv, T, S, nq, scale_log2);

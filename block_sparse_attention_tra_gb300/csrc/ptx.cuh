@@ -74,6 +74,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// True once another CTA has recorded a device error (waits give up early).
+__device__ __forceinline__ bool device_error_raised() {
+  return *reinterpret_cast<volatile unsigned int*>(&g_device_error) != 0u;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (and records a device error) if it never does.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {

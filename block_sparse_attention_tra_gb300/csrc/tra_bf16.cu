@@ -6,24 +6,37 @@
 //     out_i = sum_{j <= i} ReLU(q_i . k_j - tau(i))^p v_j,
 //     tau(i) = beta * sqrt(2 ln(i+1) / D),
 // causal and unnormalised, no 1/sqrt(D) factor.  The page's kernel walks every
-// key tile for every query tile; this one visits only key tiles at or below
-// the diagonal and masks the diagonal tile per element.
+// key tile for every query tile; these visit only key tiles at or below the
+// diagonal and mask the diagonal tile per element.
 //
-// One CTA owns 256 query rows of one (b, h) as two 128-row tiles Q0, Q1 that
-// share every K/V tile brought in by TMA:
-//   warp 8      TMA producer: Q0, Q1 once, then K and V tiles (128 keys x D)
-//               into two smem rings (128-byte swizzled 64-column panels).
-//   warp 9      MMA issuer (one thread).  Per key tile n the tensor pipe runs
-//                 ... PV0(n), QK0(n+1), PV1(n), QK1(n+1), PV0(n+1) ...
-//               where QKt(n): S_t = Q_t K_n^T into TMEM (fp32, 128 columns),
-//               PVt(n): O_t += P_t V_n with P_t read from TMEM.  Each epilogue
-//               warpgroup therefore has two MMAs' time to turn S_t into P_t.
-//   warps 0-3   epilogue of Q0, warps 4-7 epilogue of Q1: thread r owns query
-//               row r (TMEM lane r).  It loads its 128 scores, masks the
-//               diagonal tile, subtracts tau(i) in fp32, takes ReLU^p, rounds
-//               to bf16 and writes P over the consumed score columns; at the
-//               end it reads O_t (fp32) and stores it as bf16.
-// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// Shared by both kernels: Q/K/V tiles (128 rows x D, 128-byte swizzled
+// 64-column panels) arrive by TMA; S = Q K^T (M=128, N=128, K=D; both
+// operands K-major in smem) and O += P V (M=128, N=D, K=128; P read straight
+// from TMEM, V an MN-major smem operand) run on tcgen05 with fp32 TMEM
+// accumulators, issued by one thread; an epilogue thread owns one query row
+// (one TMEM lane): it loads its scores, subtracts tau(i) in fp32, applies
+// ReLU^p, masks the diagonal tile, rounds to bf16 and writes P over the
+// consumed score columns in two halves, so the P V MMA can start on the
+// first 64 keys while the second half is still being computed.
+//
+// Two CTA organisations, chosen by the power class:
+//
+// * p = 1 or 2 (cheap epilogue, tensor-bound): "pair" kernel.  A CTA owns 256
+//   query rows of one (b, h) as two 128-row tiles Q0, Q1 sharing every K/V
+//   tile (half the K/V smem traffic per FLOP).  The tensor pipe runs
+//     ... PV0(n), QK0(n+1), PV1(n), QK1(n+1), PV0(n+1) ...
+//   and epilogue warpgroup t (warps 4t..4t+3) serves tile Q_t, so each has
+//   two MMA durations to turn S_t into P_t.  TMEM: S0, S1, O0, O1.
+//
+// * general p (x^p = exp2(p log2 x): two MUFU operations per score, which
+//   outweigh the tensor work at small D): "round-robin" kernel.  A CTA owns
+//   one 128-row tile; NB = 3 score buffers in TMEM are filled by QK(n) for
+//   n = k mod 3 and served by three epilogue warpgroups, so twelve epilogue
+//   warps share the MUFU units while the tensor pipe runs ahead.  TMEM:
+//   S0, S1, S2, O.
+//
+// CTAs are numbered longest-first (the most causal key tiles first); the
+// hardware block scheduler then balances the causal load across SMs.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -33,27 +46,22 @@ namespace {
 constexpr int BM = 128;                 // query rows per tile
 constexpr int BN = 128;                 // keys per tile
 constexpr int PANEL_BYTES = 128 * 128;  // 128 rows x 128 B (64 bf16) swizzle panel
-constexpr int NUM_THREADS = 320;        // 2 epilogue warpgroups + TMA warp + MMA warp
-constexpr int TMA_WARP = 8;
-constexpr int MMA_WARP = 9;
-
-template <int D>
-struct Layout {
-  static constexpr int NP = D / 64;              // 64-column panels per tile
-  static constexpr int TILE = NP * PANEL_BYTES;  // one 128 x D bf16 tile
-  static constexpr int NS = (D == 128) ? 2 : 4;  // stages per K ring and per V ring
-  static constexpr int Q_OFF = 0;                // Q0, Q1
-  static constexpr int K_OFF = Q_OFF + 2 * TILE;
-  static constexpr int V_OFF = K_OFF + NS * TILE;
-  static constexpr int BAR_OFF = V_OFF + NS * TILE;
-  // q_full | k_full[NS] | k_empty[NS] | v_full[NS] | v_empty[NS] | s_full[2] | p_full[2] | o_full[2]
-  static constexpr int NBAR = 1 + 4 * NS + 6;
-  static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int BYTES = TPTR_OFF + 16;
-  static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024 B
-};
-
 constexpr uint32_t TMEM_COLS = 512;
+
+// General power: pairs (of 16 per 32 columns) whose log2 is evaluated on the
+// FMA pipe by a polynomial instead of the MUFU lg2 (the MUFU unit, shared by
+// lg2 and ex2, bounds the general path).
+#ifndef BSA_EMU_LOG2_PAIRS
+#define BSA_EMU_LOG2_PAIRS 0
+#endif
+constexpr int EMU_LOG2_PAIRS = BSA_EMU_LOG2_PAIRS;
+static_assert(EMU_LOG2_PAIRS >= 0 && EMU_LOG2_PAIRS <= 16, "pairs per 16");
+
+// log2(m) ~= sum_k LOG2_Ck m^k for m in [1, 2): degree-4 least-squares fit
+// on Chebyshev nodes (fit_log2.py); max |error| 1.0e-4, i.e. a relative error
+// <= p * ln2 * 1e-4 in the weight, well below its bf16 rounding (2^-9).
+constexpr float LOG2_C0 = -2.505614662e+00f, LOG2_C1 = 4.049616893e+00f, LOG2_C2 = -2.099402281e+00f,
+                LOG2_C3 = 6.355111165e-01f, LOG2_C4 = -8.001087691e-02f;
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -77,9 +85,38 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   return r;
 }
 
+// Round two non-negative fp32 weights to bf16 (nearest, ties away from zero)
+// and pack them, with integer adds and a byte permute on the ALU pipe instead
+// of the conversion unit, which the general path keeps busy with lg2/ex2.
+#ifndef BSA_INT_PACK
+#define BSA_INT_PACK 0
+#endif
+__device__ __forceinline__ uint32_t pack_bf16x2_alu(float lo, float hi) {
+#if BSA_INT_PACK
+  const uint32_t a = __float_as_uint(lo) + 0x8000u, b = __float_as_uint(hi) + 0x8000u;
+  return __byte_perm(a, b, 0x7632);
+#else
+  return pack_bf16x2(lo, hi);
+#endif
+}
+
+// p * log2(x) on the FMA/ALU pipes: x = 2^e m with m in [1, 2) taken from
+// the bits, log2(m) from the LOG2_Ck polynomial with p folded into pc[].
+// Any x <= 0 (the ReLU's zeros) returns -inf, so that exp2 of it is 0.
+__device__ __forceinline__ float p_log2_poly(float x, float p, const float (&pc)[5]) {
+  const uint32_t b = __float_as_uint(x);
+  const float m = __uint_as_float((b & 0x007fffffu) | 0x3f800000u);
+  const float e = __uint_as_float((b >> 23) | 0x4b000000u) - (8388608.0f + 127.0f);
+  float acc = fmaf(pc[4], m, pc[3]);
+  acc = fmaf(acc, m, pc[2]);
+  acc = fmaf(acc, m, pc[1]);
+  acc = fmaf(acc, m, pc[0]);
+  return x > 0.0f ? fmaf(p, e, acc) : -INFINITY;
+}
+
 // Weights of two adjacent keys from their scores: ReLU(s - tau)^p, bf16x2.
-template <int PC>
-__device__ __forceinline__ uint32_t weights2(float s0, float s1, float tau, float p) {
+template <int PC, bool EMU>
+__device__ __forceinline__ uint32_t weights2(float s0, float s1, float tau, float p, const float (&pc)[5]) {
   const float x0 = s0 - tau, x1 = s1 - tau;
   if constexpr (PC == POW_ONE) {
     return relu_pack(x0, x1);
@@ -87,22 +124,30 @@ __device__ __forceinline__ uint32_t weights2(float s0, float s1, float tau, floa
     const uint32_t h = relu_pack(x0, x1);
     return mul_bf16x2(h, h);
   } else {
-    // x^p = exp2(p log2 x); lg2(0) = -inf and ex2(-inf) = 0 give ReLU's zero.
-    const float w0 = ex2_approx(p * lg2_approx(fmaxf(x0, 0.0f)));
-    const float w1 = ex2_approx(p * lg2_approx(fmaxf(x1, 0.0f)));
-    return pack_bf16x2(w0, w1);
+    // x^p = exp2(p log2 x); log2 of the ReLU's zeros is -inf and ex2 of it 0.
+    float y0, y1;
+    if constexpr (EMU) {
+      y0 = p_log2_poly(x0, p, pc);
+      y1 = p_log2_poly(x1, p, pc);
+    } else {
+      y0 = p * lg2_approx(fmaxf(x0, 0.0f));
+      y1 = p * lg2_approx(fmaxf(x1, 0.0f));
+    }
+    return pack_bf16x2_alu(ex2_approx(y0), ex2_approx(y1));
   }
 }
 
-// Turn 64 scores (columns c0 .. c0+63 of the tile) into 32 packed weights and
-// store them to TMEM columns c0/2 .. c0/2+31 of the same buffer.
+// 32 scores (tile columns c0 .. c0+31) -> 16 packed weights, stored to TMEM
+// columns c0/2 .. c0/2+15 of the same buffer (already-consumed scores).
 template <int PC>
-__device__ __forceinline__ void epilogue_half(const uint32_t (&s)[64], uint32_t tS, int c0, float tau, float p,
-                                              bool diag, int key0, int row) {
-  uint32_t pk[32];
+__device__ __forceinline__ void epilogue_quarter(const uint32_t (&s)[32], uint32_t tS, int c0, float tau, float p,
+                                                 const float (&pc)[5], bool diag, int key0, int row) {
+  uint32_t pk[16];
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    uint32_t w = weights2<PC>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), tau, p);
+  for (int e = 0; e < 16; ++e) {
+    const bool emu = e >= 16 - EMU_LOG2_PAIRS;
+    uint32_t w = emu ? weights2<PC, true>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), tau, p, pc)
+                     : weights2<PC, false>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), tau, p, pc);
     if (diag) {
       const int key = key0 + c0 + 2 * e;  // keys key, key + 1
       if (key > row) w = 0u;
@@ -110,27 +155,161 @@ __device__ __forceinline__ void epilogue_half(const uint32_t (&s)[64], uint32_t 
     }
     pk[e] = w;
   }
-  uint32_t lo[16], hi[16];
-#pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    lo[e] = pk[e];
-    hi[e] = pk[16 + e];
-  }
-  tmem_st16(tS + c0 / 2, lo);
-  tmem_st16(tS + c0 / 2 + 16, hi);
+  tmem_st16(tS + c0 / 2, pk);
 }
 
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
-  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-  tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+// One 128-key score tile of this thread's row -> P, in four software-
+// pipelined quarters; arrives on p_half after keys 0..63 and on p_full after
+// all 128 (one arrival per warp).
+template <int PC, bool SPLIT = true>
+__device__ __forceinline__ void epilogue_tile(uint32_t tS, float tau, float p, const float (&pc)[5], bool diag,
+                                              int key0, int row, int lane, uint64_t* p_half, uint64_t* p_full) {
+  uint32_t a[32], b[32];
+  tmem_ld32(tS, a);
+  tmem_wait_ld();
+  tmem_ld32(tS + 32, b);
+  epilogue_quarter<PC>(a, tS, 0, tau, p, pc, diag, key0, row);
+  tmem_wait_ld();
+  tmem_ld32(tS + 64, a);
+  epilogue_quarter<PC>(b, tS, 32, tau, p, pc, diag, key0, row);
+  if constexpr (SPLIT) {
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(p_half);
+  }
+  tmem_wait_ld();
+  tmem_ld32(tS + 96, b);
+  epilogue_quarter<PC>(a, tS, 64, tau, p, pc, diag, key0, row);
+  tmem_wait_ld();
+  epilogue_quarter<PC>(b, tS, 96, tau, p, pc, diag, key0, row);
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(p_full);
 }
+
+// O columns [c*32, c*32+32) of this thread's row: TMEM fp32 -> bf16 -> HBM.
+__device__ __forceinline__ void store_o_chunk(uint32_t tO, int c, __nv_bfloat16* orow, bool in_range) {
+  uint32_t ov[32];
+  tmem_ld32(tO + c * 32, ov);
+  tmem_wait_ld();
+  if (in_range) {
+    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+    for (int vq = 0; vq < 4; ++vq) {
+      uint4 u;
+      u.x = pack_bf16x2(__uint_as_float(ov[8 * vq + 0]), __uint_as_float(ov[8 * vq + 1]));
+      u.y = pack_bf16x2(__uint_as_float(ov[8 * vq + 2]), __uint_as_float(ov[8 * vq + 3]));
+      u.z = pack_bf16x2(__uint_as_float(ov[8 * vq + 4]), __uint_as_float(ov[8 * vq + 5]));
+      u.w = pack_bf16x2(__uint_as_float(ov[8 * vq + 6]), __uint_as_float(ov[8 * vq + 7]));
+      dst[vq] = u;
+    }
+  }
+}
+
+__device__ __forceinline__ float tau_of_row(int row, float beta, int D) {
+  return beta * sqrtf(2.0f * logf(static_cast<float>(row + 1)) / static_cast<float>(D));
+}
+
+// S_tmem = Q K^T over D: D/16 MMAs of K=16 (32 bytes of each 128-byte row).
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t sQ, uint32_t sK) {
+  constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * PANEL_BYTES + (kk & 3) * 32;
+    mma_ss(tS, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024), IDESC_QK,
+           kk > 0 ? 1u : 0u);
+  }
+}
+
+// O_tmem += P V for keys [16*kk0, 16*kk1) of the tile (P from TMEM).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t sV, int kk0, int kk1, bool first) {
+  constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 0, 1);  // P (TMEM), V MN-major
+  constexpr int NP = D / 64;
+#pragma unroll
+  for (int kk = kk0; kk < kk1; ++kk) {
+    const uint64_t bdesc = smem_desc_sw128(sV + kk * 16 * 128, NP > 1 ? PANEL_BYTES : 1024, 1024);
+    mma_ts(tO, tP + kk * 8, bdesc, IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+  }
+}
+
+// Producer body shared by both kernels: Q tiles, then K(n), V(n) for
+// n = 0..nlast into NS-stage rings.  On a timed-out wait it drains what it
+// has issued before returning.
+template <int NP, int TILE, int NS>
+__device__ __forceinline__ void produce(uint8_t* smem, int q_off, int k_off, int v_off, int nq, int qrow0, int bh,
+                                        int nlast, const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                        const CUtensorMap* tmV, uint64_t* q_full, uint64_t* k_full,
+                                        uint64_t* k_empty, uint64_t* v_full, uint64_t* v_empty) {
+  tma_prefetch_desc(tmQ);
+  tma_prefetch_desc(tmK);
+  tma_prefetch_desc(tmV);
+  mbar_arrive_expect_tx(q_full, nq * TILE);
+  for (int qt = 0; qt < nq; ++qt) {
+#pragma unroll
+    for (int pnl = 0; pnl < NP; ++pnl)
+      tma_load_3d(smem + q_off + qt * TILE + pnl * PANEL_BYTES, tmQ, q_full, 64 * pnl, qrow0 + qt * BM, bh);
+  }
+  bool ok = true;
+  int nk = 0, nv = 0;  // K / V tiles issued
+  for (int n = 0; n <= nlast; ++n) {
+    const int s = n % NS;
+    const uint32_t ph = (n / NS) & 1;
+    if (!(ok = mbar_wait(&k_empty[s], ph ^ 1))) break;
+    mbar_arrive_expect_tx(&k_full[s], TILE);
+#pragma unroll
+    for (int pnl = 0; pnl < NP; ++pnl)
+      tma_load_3d(smem + k_off + s * TILE + pnl * PANEL_BYTES, tmK, &k_full[s], 64 * pnl, n * BN, bh);
+    nk = n + 1;
+    if (!(ok = mbar_wait(&v_empty[s], ph ^ 1))) break;
+    mbar_arrive_expect_tx(&v_full[s], TILE);
+#pragma unroll
+    for (int pnl = 0; pnl < NP; ++pnl)
+      tma_load_3d(smem + v_off + s * TILE + pnl * PANEL_BYTES, tmV, &v_full[s], 64 * pnl, n * BN, bh);
+    nv = n + 1;
+  }
+  if (!ok) {
+    // Drain: never leave the CTA with a bulk copy still landing in its smem.
+    mbar_wait(q_full, 0);
+    for (int n = (nk > NS ? nk - NS : 0); n < nk; ++n) mbar_wait(&k_full[n % NS], (n / NS) & 1);
+    for (int n = (nv > NS ? nv - NS : 0); n < nv; ++n) mbar_wait(&v_full[n % NS], (n / NS) & 1);
+  }
+}
+
+// ============================================================ pair kernel (p = 1, 2)
+
+template <int D>
+struct PairLayout {
+  static constexpr int NP = D / 64;
+  static constexpr int TILE = NP * PANEL_BYTES;
+  static constexpr int NS = (D == 128) ? 2 : 4;
+  static constexpr int Q_OFF = 0;  // Q0, Q1
+  static constexpr int K_OFF = Q_OFF + 2 * TILE;
+  static constexpr int V_OFF = K_OFF + NS * TILE;
+  static constexpr int BAR_OFF = V_OFF + NS * TILE;
+  // q_full | k_full[NS] | k_empty[NS] | v_full[NS] | v_empty[NS] | s_full[2] | p_half[2] | p_full[2] |
+  // o_full[2] | mma_done
+  static constexpr int NBAR = 1 + 4 * NS + 8 + 1;
+  static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int ALLOC = TPTR_OFF + 16 + 1024;
+};
+constexpr int PAIR_THREADS = 320;  // 2 epilogue warpgroups + TMA warp + MMA warp
+#ifndef BSA_PAIR_SPLIT_P
+#define BSA_PAIR_SPLIT_P 1
+#endif
+constexpr bool PAIR_SPLIT_P = BSA_PAIR_SPLIT_P;  // hand P over in two halves
+constexpr int PAIR_TMA_WARP = 8;
+constexpr int PAIR_MMA_WARP = 9;
 
 template <int D, int PC>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    tra_bf16_tcgen05_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                            const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out, int BH,
-                            int T, int nQ, int nPair, float beta, float p) {
-  using L = Layout<D>;
+__global__ void __launch_bounds__(PAIR_THREADS, 1)
+    tra_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out, int BH, int T,
+                         int nQ, int nPair, float beta, float p) {
+  using L = PairLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -140,18 +319,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* v_full = k_empty + L::NS;
   uint64_t* v_empty = v_full + L::NS;
   uint64_t* s_full = v_empty + L::NS;  // [2], one per query tile
-  uint64_t* p_full = s_full + 2;       // [2]
+  uint64_t* p_half = s_full + 2;       // [2]
+  uint64_t* p_full = p_half + 2;       // [2]
   uint64_t* o_full = p_full + 2;       // [2]
+  uint64_t* mma_done = o_full + 2;
   uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // Longest-first order: the first BH CTAs take the last (longest) tile pair.
+  // Longest-first: the first BH CTAs take the last (longest) tile pair.
   const int t = nPair - 1 - static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
-  const bool has1 = (2 * t + 1) < nQ;     // second query tile exists
-  const int nmax0 = 2 * t;                // last key tile of Q0 (its diagonal)
+  const bool has1 = (2 * t + 1) < nQ;  // second query tile exists
+  const int nmax0 = 2 * t;             // last key tile of Q0 (its diagonal)
   const int nmax1 = has1 ? 2 * t + 1 : -1;
   const int nlast = has1 ? nmax1 : nmax0;
 
@@ -165,12 +345,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
+      mbar_init(&p_half[b], 4);
       mbar_init(&p_full[b], 4);
       mbar_init(&o_full[b], 1);
     }
+    mbar_init(mma_done, 1);
     fence_barrier_init();
   }
-  if (warp == MMA_WARP) {
+  if (warp == PAIR_MMA_WARP) {
     tmem_alloc(tptr, TMEM_COLS);
     tmem_relinquish();
   }
@@ -179,74 +361,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tptr;
 
-  if (warp == TMA_WARP) {
-    // ------------------------------------------------------------ producer
+  if (warp == PAIR_TMA_WARP) {
+    if (lane == 0)
+      produce<L::NP, L::TILE, L::NS>(smem, L::Q_OFF, L::K_OFF, L::V_OFF, has1 ? 2 : 1, 2 * t * BM, bh, nlast, &tmQ,
+                                     &tmK, &tmV, q_full, k_full, k_empty, v_full, v_empty);
+  } else if (warp == PAIR_MMA_WARP) {
     if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(q_full, (has1 ? 2 : 1) * L::TILE);
-      for (int qt = 0; qt < (has1 ? 2 : 1); ++qt) {
-        uint8_t* sQ = smem + L::Q_OFF + qt * L::TILE;
-#pragma unroll
-        for (int pnl = 0; pnl < L::NP; ++pnl)
-          tma_load_3d(sQ + pnl * PANEL_BYTES, &tmQ, q_full, 64 * pnl, (2 * t + qt) * BM, bh);
-      }
-      bool ok = true;
-      int nk = 0, nv = 0;  // K / V tiles issued
-      for (int n = 0; n <= nlast; ++n) {
-        const int s = n % L::NS;
-        const uint32_t ph = (n / L::NS) & 1;
-        if (!(ok = mbar_wait(&k_empty[s], ph ^ 1))) break;
-        uint8_t* sK = smem + L::K_OFF + s * L::TILE;
-        mbar_arrive_expect_tx(&k_full[s], L::TILE);
-#pragma unroll
-        for (int pnl = 0; pnl < L::NP; ++pnl)
-          tma_load_3d(sK + pnl * PANEL_BYTES, &tmK, &k_full[s], 64 * pnl, n * BN, bh);
-        ++nk;
-        if (!(ok = mbar_wait(&v_empty[s], ph ^ 1))) break;
-        uint8_t* sV = smem + L::V_OFF + s * L::TILE;
-        mbar_arrive_expect_tx(&v_full[s], L::TILE);
-#pragma unroll
-        for (int pnl = 0; pnl < L::NP; ++pnl)
-          tma_load_3d(sV + pnl * PANEL_BYTES, &tmV, &v_full[s], 64 * pnl, n * BN, bh);
-        ++nv;
-      }
-      if (!ok) {
-        // Drain: never leave the CTA with a bulk copy still landing in its smem.
-        mbar_wait(q_full, 0);
-        for (int n = (nk > L::NS ? nk - L::NS : 0); n < nk; ++n) mbar_wait(&k_full[n % L::NS], (n / L::NS) & 1);
-        for (int n = (nv > L::NS ? nv - L::NS : 0); n < nv; ++n) mbar_wait(&v_full[n % L::NS], (n / L::NS) & 1);
-      }
-    }
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
-      constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 0, 1);   // P (TMEM), V MN-major
       const uint32_t sQ0 = smem_u32(smem + L::Q_OFF);
-
       auto qk = [&](int qt, int n) {
-        const uint32_t sQ = sQ0 + qt * L::TILE;
-        const uint32_t sK = smem_u32(smem + L::K_OFF + (n % L::NS) * L::TILE);
-        const uint32_t tS = tmem + qt * BN;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * PANEL_BYTES + (kk & 3) * 32;
-          mma_ss(tS, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024), IDESC_QK,
-                 kk > 0 ? 1u : 0u);
-        }
+        issue_qk<D>(tmem + qt * BN, sQ0 + qt * L::TILE, smem_u32(smem + L::K_OFF + (n % L::NS) * L::TILE));
         mma_commit(&s_full[qt]);
       };
-      auto pv = [&](int qt, int n) {
+      // PVt(n) in two halves: keys 0..63 as soon as that half of P is there.
+      auto pv = [&](int qt, int n) -> bool {
         const uint32_t sV = smem_u32(smem + L::V_OFF + (n % L::NS) * L::TILE);
-        const uint32_t tP = tmem + qt * BN;
-        const uint32_t tO = tmem + 2 * BN + qt * D;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bdesc = smem_desc_sw128(sV + kk * 16 * 128, L::NP > 1 ? PANEL_BYTES : 1024, 1024);
-          mma_ts(tO, tP + kk * 8, bdesc, IDESC_PV, (n > 0 || kk > 0) ? 1u : 0u);
-        }
+        const uint32_t tP = tmem + qt * BN, tO = tmem + 2 * BN + qt * D;
+        if (!mbar_wait(PAIR_SPLIT_P ? &p_half[qt] : &p_full[qt], n & 1) ||
+            !mbar_wait(&v_full[n % L::NS], (n / L::NS) & 1))
+          return false;
+        tc_fence_after();
+        issue_pv<D>(tO, tP, sV, 0, BN / 32, n == 0);
+        if (!mbar_wait(&p_full[qt], n & 1)) return false;
+        tc_fence_after();
+        issue_pv<D>(tO, tP, sV, BN / 32, BN / 16, false);
+        return true;
       };
 
       bool ok = mbar_wait(q_full, 0) && mbar_wait(&k_full[0], 0);
@@ -257,15 +395,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mma_commit(&k_empty[0]);
       }
       for (int n = 0; n <= nlast && ok; ++n) {
-        const int s = n % L::NS;
-        const uint32_t vph = (n / L::NS) & 1;
         const int n1 = n + 1;
         const bool next_k = n1 <= nlast;
         // tile 0: PV0(n), then QK0(n+1)
         if (n <= nmax0) {
-          if (!(ok = mbar_wait(&p_full[0], n & 1) && mbar_wait(&v_full[s], vph))) break;
-          tc_fence_after();
-          pv(0, n);
+          if (!(ok = pv(0, n))) break;
           if (n == nmax0) mma_commit(&o_full[0]);
         }
         if (next_k) {
@@ -275,75 +409,188 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         // tile 1: PV1(n), then QK1(n+1)
         if (has1) {
-          if (!(ok = mbar_wait(&p_full[1], n & 1) && mbar_wait(&v_full[s], vph))) break;
-          tc_fence_after();
-          pv(1, n);
+          if (!(ok = pv(1, n))) break;
           if (n == nmax1) mma_commit(&o_full[1]);
         }
-        mma_commit(&v_empty[s]);
+        mma_commit(&v_empty[n % L::NS]);
         if (next_k) {
           if (has1 && n1 <= nmax1) qk(1, n1);
           mma_commit(&k_empty[n1 % L::NS]);
         }
       }
+      // Commits arrive in issue order: once this one has landed, every
+      // barrier arrival of this CTA's MMAs has too, and smem may be released.
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0);
     }
   } else {
-    // ------------------------------------------------------------ epilogue
     const int qt = warp >> 2;  // query tile of this warpgroup
     const int wq = warp & 3;   // TMEM lane quarter
     const int nmax = qt == 0 ? nmax0 : nmax1;
-    const int r = wq * 32 + lane;
-    const int row = (2 * t + qt) * BM + r;
-    const float tau = beta * sqrtf(2.0f * logf(static_cast<float>(row + 1)) / static_cast<float>(D));
+    const int row = (2 * t + qt) * BM + wq * 32 + lane;
+    const float tau = tau_of_row(row, beta, D);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t tS = lane_base + qt * BN;
+    const float pc[5] = {p * LOG2_C0, p * LOG2_C1, p * LOG2_C2, p * LOG2_C3, p * LOG2_C4};
     bool ok = true;
     for (int n = 0; n <= nmax; ++n) {
       if (!(ok = mbar_wait(&s_full[qt], n & 1))) break;
       tc_fence_after();
-      const bool diag = (n == nmax);
-      const int key0 = n * BN;
-      uint32_t sa[64], sb[64];
-      tmem_ld64(tS, sa);
-      tmem_wait_ld();
-      tmem_ld64(tS + 64, sb);
-      epilogue_half<PC>(sa, tS, 0, tau, p, diag, key0, row);
-      tmem_wait_ld();
-      epilogue_half<PC>(sb, tS, 64, tau, p, diag, key0, row);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[qt]);
+      epilogue_tile<PC, PAIR_SPLIT_P>(tS, tau, p, pc, n == nmax, n * BN, row, lane, &p_half[qt], &p_full[qt]);
     }
-    if (ok && nmax >= 0) ok = mbar_wait(&o_full[qt], 0);
-    if (ok && nmax >= 0) {
+    if (ok && nmax >= 0 && mbar_wait(&o_full[qt], 0)) {
       tc_fence_after();
       __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * T + row) * D;
-      const uint32_t tO = lane_base + 2 * BN + qt * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(tO + c * 32, ov);
-        tmem_wait_ld();
-        if (row < T) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int vq = 0; vq < 4; ++vq) {
-            uint4 u;
-            u.x = pack_bf16x2(__uint_as_float(ov[8 * vq + 0]), __uint_as_float(ov[8 * vq + 1]));
-            u.y = pack_bf16x2(__uint_as_float(ov[8 * vq + 2]), __uint_as_float(ov[8 * vq + 3]));
-            u.z = pack_bf16x2(__uint_as_float(ov[8 * vq + 4]), __uint_as_float(ov[8 * vq + 5]));
-            u.w = pack_bf16x2(__uint_as_float(ov[8 * vq + 6]), __uint_as_float(ov[8 * vq + 7]));
-            dst[vq] = u;
-          }
-        }
-      }
+      for (int c = 0; c < D / 32; ++c) store_o_chunk(lane_base + 2 * BN + qt * D, c, orow, row < T);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == MMA_WARP) {
+  if (warp == PAIR_MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ===================================================== round-robin kernel (general p)
+
+constexpr int RR_NB = 3;                          // score buffers = epilogue warpgroups
+constexpr int RR_THREADS = RR_NB * 128 + 64;      // + TMA warp + MMA warp
+constexpr int RR_TMA_WARP = RR_NB * 4;
+constexpr int RR_MMA_WARP = RR_NB * 4 + 1;
+
+template <int D>
+struct RrLayout {
+  static constexpr int NP = D / 64;
+  static constexpr int TILE = NP * PANEL_BYTES;
+  static constexpr int NS = (D == 128) ? 3 : 6;  // >= RR_NB: QK runs RR_NB tiles ahead of PV
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + TILE;
+  static constexpr int V_OFF = K_OFF + NS * TILE;
+  static constexpr int BAR_OFF = V_OFF + NS * TILE;
+  // q_full | k_full[NS] | k_empty[NS] | v_full[NS] | v_empty[NS] | s_full[NB] | p_half[NB] | p_full[NB] |
+  // o_full | mma_done
+  static constexpr int NBAR = 1 + 4 * NS + 3 * RR_NB + 2;
+  static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int ALLOC = TPTR_OFF + 16 + 1024;
+};
+
+template <int D, int PC>
+__global__ void __launch_bounds__(RR_THREADS, 1)
+    tra_bf16_rr_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out, int BH, int T,
+                       int nQ, float beta, float p) {
+  using L = RrLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + L::NS;
+  uint64_t* v_full = k_empty + L::NS;
+  uint64_t* v_empty = v_full + L::NS;
+  uint64_t* s_full = v_empty + L::NS;  // [NB]
+  uint64_t* p_half = s_full + RR_NB;   // [NB]
+  uint64_t* p_full = p_half + RR_NB;   // [NB]
+  uint64_t* o_full = p_full + RR_NB;
+  uint64_t* mma_done = o_full + 1;
+  uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m = nQ - 1 - static_cast<int>(blockIdx.x) / BH;  // longest first
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int nmax = m;  // key tiles 0..m (BN == BM)
+  constexpr uint32_t O_COL = RR_NB * BN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < L::NS; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int b = 0; b < RR_NB; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_half[b], 4);
+      mbar_init(&p_full[b], 4);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == RR_MMA_WARP) {
+    tmem_alloc(tptr, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tptr;
+
+  if (warp == RR_TMA_WARP) {
+    if (lane == 0)
+      produce<L::NP, L::TILE, L::NS>(smem, L::Q_OFF, L::K_OFF, L::V_OFF, 1, m * BM, bh, nmax, &tmQ, &tmK, &tmV,
+                                     q_full, k_full, k_empty, v_full, v_empty);
+  } else if (warp == RR_MMA_WARP) {
+    if (lane == 0) {
+      const uint32_t sQ = smem_u32(smem + L::Q_OFF);
+      auto qk = [&](int n) -> bool {
+        if (!mbar_wait(&k_full[n % L::NS], (n / L::NS) & 1)) return false;
+        tc_fence_after();
+        issue_qk<D>(tmem + (n % RR_NB) * BN, sQ, smem_u32(smem + L::K_OFF + (n % L::NS) * L::TILE));
+        mma_commit(&s_full[n % RR_NB]);
+        mma_commit(&k_empty[n % L::NS]);
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0);
+      for (int n = 0; n < RR_NB && n <= nmax && ok; ++n) ok = qk(n);
+      for (int n = 0; n <= nmax && ok; ++n) {
+        const int b = n % RR_NB;
+        const uint32_t ph = (n / RR_NB) & 1;
+        const uint32_t sV = smem_u32(smem + L::V_OFF + (n % L::NS) * L::TILE);
+        if (!(ok = mbar_wait(&p_half[b], ph) && mbar_wait(&v_full[n % L::NS], (n / L::NS) & 1))) break;
+        tc_fence_after();
+        issue_pv<D>(tmem + O_COL, tmem + b * BN, sV, 0, BN / 32, n == 0);
+        if (!(ok = mbar_wait(&p_full[b], ph))) break;
+        tc_fence_after();
+        issue_pv<D>(tmem + O_COL, tmem + b * BN, sV, BN / 32, BN / 16, false);
+        mma_commit(&v_empty[n % L::NS]);
+        if (n + RR_NB <= nmax) ok = qk(n + RR_NB);  // reuses buffer b after PV(n) in issue order
+      }
+      if (ok) mma_commit(o_full);
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0);
+    }
+  } else {
+    const int wg = warp >> 2;  // epilogue warpgroup: key tiles n = wg mod NB
+    const int wq = warp & 3;   // TMEM lane quarter
+    const int row = m * BM + wq * 32 + lane;
+    const float tau = tau_of_row(row, beta, D);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t tS = lane_base + wg * BN;
+    const float pc[5] = {p * LOG2_C0, p * LOG2_C1, p * LOG2_C2, p * LOG2_C3, p * LOG2_C4};
+    bool ok = true;
+    for (int n = wg; n <= nmax; n += RR_NB) {
+      if (!(ok = mbar_wait(&s_full[wg], (n / RR_NB) & 1))) break;
+      tc_fence_after();
+      epilogue_tile<PC>(tS, tau, p, pc, n == nmax, n * BN, row, lane, &p_half[wg], &p_full[wg]);
+    }
+    // O: 32-column chunk c is stored by warpgroup c mod NB.
+    if (ok && mbar_wait(o_full, 0)) {
+      tc_fence_after();
+      __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * T + row) * D;
+      for (int c = wg; c < D / 32; c += RR_NB) store_o_chunk(lane_base + O_COL, c, orow, row < T);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == RR_MMA_WARP) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -351,18 +598,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 template <int D, int PC>
-int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* out, int BH, int T,
-           float beta, float p, cudaStream_t stream) {
-  using L = Layout<D>;
-  auto kern = tra_bf16_tcgen05_kernel<D, PC>;
+int launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* out, int BH, int T,
+                float beta, float p, cudaStream_t stream) {
+  using L = PairLayout<D>;
+  auto kern = tra_bf16_pair_kernel<D, PC>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
     return ERR_LAUNCH;
   const int nQ = (T + BM - 1) / BM;
   const int nPair = (nQ + 1) / 2;
   const long long grid = static_cast<long long>(nPair) * BH;
   if (grid > 0x7fffffffLL) return ERR_SHAPE;
-  kern<<<static_cast<unsigned>(grid), NUM_THREADS, L::ALLOC, stream>>>(
+  kern<<<static_cast<unsigned>(grid), PAIR_THREADS, L::ALLOC, stream>>>(
       mq, mk, mv, static_cast<__nv_bfloat16*>(out), BH, T, nQ, nPair, beta, p);
+  return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
+}
+
+template <int D>
+int launch_rr(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* out, int BH, int T,
+              float beta, float p, cudaStream_t stream) {
+  using L = RrLayout<D>;
+  auto kern = tra_bf16_rr_kernel<D, POW_GENERAL>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
+    return ERR_LAUNCH;
+  const int nQ = (T + BM - 1) / BM;
+  const long long grid = static_cast<long long>(nQ) * BH;
+  if (grid > 0x7fffffffLL) return ERR_SHAPE;
+  kern<<<static_cast<unsigned>(grid), RR_THREADS, L::ALLOC, stream>>>(
+      mq, mk, mv, static_cast<__nv_bfloat16*>(out), BH, T, nQ, beta, p);
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
 
@@ -380,14 +642,14 @@ int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int 
   if (st != OK) return st;
   const int pc = power_class(p);
   if (D == 128) {
-    if (pc == POW_TWO) return launch<128, POW_TWO>(mq, mk, mv, out, BH, T, beta, p, stream);
-    if (pc == POW_ONE) return launch<128, POW_ONE>(mq, mk, mv, out, BH, T, beta, p, stream);
-    return launch<128, POW_GENERAL>(mq, mk, mv, out, BH, T, beta, p, stream);
+    if (pc == POW_TWO) return launch_pair<128, POW_TWO>(mq, mk, mv, out, BH, T, beta, p, stream);
+    if (pc == POW_ONE) return launch_pair<128, POW_ONE>(mq, mk, mv, out, BH, T, beta, p, stream);
+    return launch_rr<128>(mq, mk, mv, out, BH, T, beta, p, stream);
   }
   if (D == 64) {
-    if (pc == POW_TWO) return launch<64, POW_TWO>(mq, mk, mv, out, BH, T, beta, p, stream);
-    if (pc == POW_ONE) return launch<64, POW_ONE>(mq, mk, mv, out, BH, T, beta, p, stream);
-    return launch<64, POW_GENERAL>(mq, mk, mv, out, BH, T, beta, p, stream);
+    if (pc == POW_TWO) return launch_pair<64, POW_TWO>(mq, mk, mv, out, BH, T, beta, p, stream);
+    if (pc == POW_ONE) return launch_pair<64, POW_ONE>(mq, mk, mv, out, BH, T, beta, p, stream);
+    return launch_rr<64>(mq, mk, mv, out, BH, T, beta, p, stream);
   }
   return ERR_UNSUPPORTED;
 }

@@ -70,6 +70,9 @@ TRA_SMALL = [
     (2, 1, 200, 64, -1.0, 2.0, "bf16"),   # beta < 0 reading
     (1, 2, 257, 128, 0.7, 3.7, "bf16"),   # another general power
     (3, 5, 640, 64, 1.0, 2.0, "bf16"),    # many (b, h), 5 row tiles
+    (1, 2, 200, 64, 0.5, 0.25, "bf16"),   # p < 1: ReLU zeros must stay exactly 0
+    (1, 1, 256, 128, 1.0, 15.0, "bf16"),  # large power (the page's p=15 example)
+    (2, 3, 1000, 64, 2.0, 1.5, "bf16"),   # persistent grid: more items than one pass
 ]
 
 

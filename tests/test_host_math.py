@@ -1,0 +1,56 @@
+"""CPU checks of host-side arithmetic the kernels rely on.
+
+* The general-power epilogue of the bf16 TRA kernel evaluates p*log2(x) for
+  part of the elements with integer bit operations and a degree-4 polynomial
+  (constants LOG2_C0..LOG2_C4 in ``csrc/tra_bf16.cu``).  Here the same steps
+  are replayed in float32 numpy and checked against numpy's log2 over a wide
+  range, including the zero / denormal cases that must flush the weight to 0.
+"""
+
+import os
+import re
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "block_sparse_attention_tra_gb300", "csrc", "tra_bf16.cu")
+
+
+def coefficients():
+    txt = open(SRC).read()
+    c = [float(re.search(r"LOG2_C%d = ([-+0-9.e]+)f" % k, txt).group(1)) for k in range(5)]
+    return np.array(c, dtype=np.float32)
+
+
+def p_log2_poly(r, p):
+    """float32 replay of p_log2_poly() in tra_bf16.cu."""
+    c = coefficients()
+    pc = (np.float32(p) * c).astype(np.float32)
+    r = np.asarray(r, dtype=np.float32)
+    b = r.view(np.uint32)
+    m = ((b & np.uint32(0x007FFFFF)) | np.uint32(0x3F800000)).view(np.float32)
+    e = ((b >> np.uint32(23)) | np.uint32(0x4B000000)).view(np.float32) - np.float32(8388608.0 + 127.0)
+    acc = (pc[4] * m + pc[3]).astype(np.float32)
+    acc = (acc * m + pc[2]).astype(np.float32)
+    acc = (acc * m + pc[1]).astype(np.float32)
+    acc = (acc * m + pc[0]).astype(np.float32)
+    y = (np.float32(p) * e + acc).astype(np.float32)
+    return np.where(r > 0, y, np.float32(-np.inf)).astype(np.float32)
+
+
+def test_log2_polynomial_error_bound():
+    r = np.geomspace(1e-37, 1e37, 2_000_001).astype(np.float32)
+    for p in (1.5, 3.7, 0.25):
+        got = p_log2_poly(r, p).astype(np.float64)
+        want = p * np.log2(r.astype(np.float64))
+        # 1.0e-4 from the fit plus float32 rounding of p*e (|p*e| <= ~100)
+        tol = p * 1.05e-4 + np.abs(want) * 2 ** -23
+        assert np.all(np.abs(got - want) <= tol)
+
+
+def test_log2_polynomial_relu_zeros_give_zero_weight():
+    """x <= 0 must give -inf (weight exactly 0) whatever p is."""
+    for p in (1.5, 0.25, 0.01):
+        y = p_log2_poly(np.array([0.0, -0.0, -1.0, -3e38], dtype=np.float32), p)
+        assert np.all(np.isneginf(y))
+        assert np.all(np.exp2(y.astype(np.float64)) == 0.0)
