@@ -21,6 +21,8 @@ from .bsa import (  # noqa: F401
     nsa_select_forward,
     nsa_select_forward_raw,
     status_string,
+    tra_backward,
+    tra_backward_raw,
     tra_forward,
     tra_forward_raw,
 )
@@ -32,6 +34,8 @@ __all__ = [
     "load_library",
     "tra_forward",
     "tra_forward_raw",
+    "tra_backward",
+    "tra_backward_raw",
     "nsa_select_forward",
     "nsa_select_forward_raw",
     "status_string",

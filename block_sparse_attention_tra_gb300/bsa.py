@@ -55,6 +55,8 @@ def load_library():
     lib.tra_forward.restype = i32
     lib.nsa_select_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.nsa_select_forward.restype = i32
+    lib.tra_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, vp]
+    lib.tra_backward.restype = i32
     lib.bsa_status_string.argtypes = [i32]
     lib.bsa_status_string.restype = ctypes.c_char_p
     lib.bsa_version.argtypes = []
@@ -83,6 +85,12 @@ def _check(status: int, what: str):
 def tra_forward_raw(q, k, v, out, B, H, T, D, beta, p, dtype, stream=0) -> int:
     """Direct C call with integer device pointers; returns the bsa_status."""
     return load_library().tra_forward(q, k, v, out, B, H, T, D, float(beta), float(p), int(dtype), stream)
+
+
+def tra_backward_raw(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, dtype, stream=0) -> int:
+    """Direct C call with integer device pointers; returns the bsa_status."""
+    return load_library().tra_backward(q, k, v, dout, dq, dk, dv, B, H, T, D, float(beta), float(p), int(dtype),
+                                       stream)
 
 
 def nsa_select_forward_raw(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, block_size, S,
@@ -133,6 +141,28 @@ def tra_forward(q, k, v, beta: float, p: float = 2.0, out=None, stream=None):
                          beta, p, _dtype_code(q), _stream_handle(stream))
     _check(st, "tra_forward")
     return out
+
+
+def tra_backward(q, k, v, dout, beta: float, p: float = 2.0, stream=None):
+    """Gradients ``(dq, dk, dv)`` of the threshold rectified attention
+    forward for the upstream gradient ``dout``; bf16 CUDA tensors
+    ``[B, H, T, D]``.  Scores are recomputed; runs on ``stream`` (default:
+    torch's current stream) without synchronising."""
+    import torch
+
+    if q.device.type != "cuda":
+        raise BsaError("tra_backward takes CUDA tensors (no CPU path)")
+    if not (q.shape == k.shape == v.shape == dout.shape) or q.dim() != 4:
+        raise BsaError("q, k, v, dout must share one shape [B, H, T, D]", 2)
+    if not (q.dtype == k.dtype == v.dtype == dout.dtype):
+        raise BsaError("q, k, v, dout must share one dtype", 3)
+    q, k, v, dout = q.contiguous(), k.contiguous(), v.contiguous(), dout.contiguous()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    B, H, T, D = q.shape
+    st = tra_backward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                          dv.data_ptr(), B, H, T, D, beta, p, _dtype_code(q), _stream_handle(stream))
+    _check(st, "tra_backward")
+    return dq, dk, dv
 
 
 def nsa_select_forward(q, k, v, block_idx, block_size: int = 64, out=None, lse=None,

@@ -81,6 +81,26 @@ int tra_forward(const void* q, const void* k, const void* v, void* out, int B, i
   return launch_tra_bf16(q, k, v, out, B, H, T, D, beta, p, stream);
 }
 
+int tra_backward(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv, int B,
+                 int H, int T, int D, float beta, float p, int dtype, cudaStream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || dout == nullptr || dq == nullptr || dk == nullptr ||
+      dv == nullptr)
+    return BSA_ERR_NULLPTR;
+  if (dtype != BSA_F32 && dtype != BSA_BF16) return BSA_ERR_DTYPE;
+  if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
+  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (dtype != BSA_BF16) return BSA_ERR_UNSUPPORTED;
+  if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f)) return BSA_ERR_UNSUPPORTED;
+  const void* ptrs[7] = {q, k, v, dout, dq, dk, dv};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return BSA_ERR_ALIGN;
+  const int dvs = check_device();
+  if (dvs != OK) return dvs;
+  return launch_tra_bwd_bf16(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, stream);
+}
+
 int nsa_select_forward(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out, float* lse,
                        int B, int Hq, int Hkv, int T, int D, int block_size, int S, cudaStream_t stream) {
   if (q == nullptr || k == nullptr || v == nullptr || block_idx == nullptr || out == nullptr)
@@ -120,7 +140,8 @@ const char* bsa_status_string(int status) {
 int bsa_version(void) { return 100; }
 
 int bsa_device_error(void) {
-  const unsigned codes[3] = {tra_bf16_device_error(), tra_f32_device_error(), nsa_device_error()};
+  const unsigned codes[4] = {tra_bf16_device_error(), tra_f32_device_error(), nsa_device_error(),
+                             tra_bwd_device_error()};
   unsigned worst = 0;
   for (unsigned c : codes) {
     if (c == 0xffffffffu) return -1;

@@ -34,6 +34,10 @@ int launch_tra_f32(const float* q, const float* k, const float* v, float* out, i
 int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int D,
                     float beta, float p, cudaStream_t stream);
 
+// Threshold rectified attention backward (dq, dk, dv), bf16 tcgen05 kernels.
+int launch_tra_bwd_bf16(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv,
+                        int B, int H, int T, int D, float beta, float p, cudaStream_t stream);
+
 // NSA selection attention, bf16 kernel.
 int launch_nsa_select(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out,
                       float* lse, int B, int Hq, int Hkv, int T, int D, int block_size, int S,
@@ -44,6 +48,7 @@ int launch_nsa_select(const void* q, const void* k, const void* v, const int32_t
 unsigned int tra_bf16_device_error();
 unsigned int tra_f32_device_error();
 unsigned int nsa_device_error();
+unsigned int tra_bwd_device_error();
 
 // Power class of the TRA epilogue: p == 1, p == 2, or the general exp2/log2 path.
 enum PowerClass : int { POW_GENERAL = 0, POW_ONE = 1, POW_TWO = 2 };

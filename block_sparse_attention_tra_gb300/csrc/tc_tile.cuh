@@ -1,0 +1,78 @@
+// tc_tile.cuh -- 128 x 128 tile building blocks on tcgen05 shared by the
+// threshold-attention forward and backward kernels.
+//
+// Tiles of 128 rows x D bf16 live in shared memory as D/64 panels of 128 rows
+// x 128 bytes, written by TMA with 128-byte swizzle (1024-byte aligned).  One
+// such tile serves both as a K-major operand (rows = M or N, D along K) and
+// as an MN-major operand (rows along K, D along N).
+#pragma once
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace bsa {
+namespace tile {
+
+constexpr int ROWS = 128;               // rows of a tile (and keys/queries per MMA tile)
+constexpr int PANEL_BYTES = 128 * 128;  // 128 rows x 128 B (64 bf16) swizzle panel
+
+// C_tmem[128 x 128] = A[128 x D] * B[128 x D]^T, both K-major tiles in smem:
+// D/16 MMAs of K = 16 (32 bytes of each 128-byte row).
+template <int D>
+__device__ __forceinline__ void mma_abt(uint32_t tC, uint32_t sA, uint32_t sB) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(ROWS, ROWS, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * PANEL_BYTES + (kk & 3) * 32;
+    mma_ss(tC, smem_desc_sw128(sA + off, 16, 1024), smem_desc_sw128(sB + off, 16, 1024), IDESC, kk > 0 ? 1u : 0u);
+  }
+}
+
+// C_tmem[128 x D] (+)= P_tmem[128 x 128] * B[128 x D] for the K range
+// [16*kk0, 16*kk1): P is bf16 packed two per TMEM column, B an MN-major tile
+// in smem (its rows run along K).  `first` starts a new accumulation.
+template <int D>
+__device__ __forceinline__ void mma_tmem_a(uint32_t tC, uint32_t tP, uint32_t sB, int kk0, int kk1, bool first) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(ROWS, D, 0, 1);
+  constexpr int NP = D / 64;
+#pragma unroll
+  for (int kk = kk0; kk < kk1; ++kk) {
+    const uint64_t bdesc = smem_desc_sw128(sB + kk * 16 * 128, NP > 1 ? PANEL_BYTES : 1024, 1024);
+    mma_ts(tC, tP + kk * 8, bdesc, IDESC, (!first || kk > 0) ? 1u : 0u);
+  }
+}
+
+// Columns [c*32, c*32+32) of this thread's TMEM lane (fp32) -> bf16 -> 64
+// bytes of global memory at dst (skipped when !in_range).
+__device__ __forceinline__ void store_row_chunk(uint32_t tC, int c, __nv_bfloat16* row, bool in_range) {
+  uint32_t v[32];
+  tmem_ld32(tC + c * 32, v);
+  tmem_wait_ld();
+  if (in_range) {
+    uint4* dst = reinterpret_cast<uint4*>(row + c * 32);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 u;
+      u.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+      u.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+      u.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+      u.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+      dst[q] = u;
+    }
+  }
+}
+
+// tau(i) = beta * sqrt(2 ln(i+1) / D), in fp32 as the page computes it.
+__device__ __forceinline__ float tau_of_row(int row, float beta, int D) {
+  return beta * sqrtf(2.0f * logf(static_cast<float>(row + 1)) / static_cast<float>(D));
+}
+
+// Load the D/64 panels of tile row block `row0` of head `bh` into smem.
+template <int D>
+__device__ __forceinline__ void tma_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int row0, int bh) {
+#pragma unroll
+  for (int pnl = 0; pnl < D / 64; ++pnl) tma_load_3d(dst + pnl * PANEL_BYTES, map, bar, 64 * pnl, row0, bh);
+}
+
+}  // namespace tile
+}  // namespace bsa

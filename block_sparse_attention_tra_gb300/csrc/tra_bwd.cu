@@ -1,0 +1,412 @@
+// tra_bwd.cu -- threshold rectified attention backward, bf16 in / fp32
+// accumulate, on tcgen05 tensor cores.
+//
+// Method: page "triton_threshold_attention.py", ThresholdRelaFunction.backward
+// with _threshold_rela_bwd_kernel_dq and _threshold_rela_bwd_kernel_dkv: with
+// x_ij = q_i.k_j - tau(i) over the causal pairs j <= i,
+//     W_ij  = ReLU(x_ij)^p                       dV_j = sum_i W_ij dO_i
+//     dA_ij = (dO_i . v_j) p ReLU(x_ij)^(p-1)     dK_j = sum_i dA_ij q_i
+//                                                dQ_i = sum_j dA_ij k_j
+// (derivative 0 where x <= 0, as on the page; beta and p get no gradient).
+// Like the page, two kernels: one per key tile for dK and dV, one per query
+// tile for dQ; both recompute the scores instead of storing W.
+//
+// dK/dV kernel, one CTA per 128-key tile n of one (b, h), looping over the
+// query tiles m >= n: S^T = K_n Q_m^T and dP^T = V_n dO_m^T into TMEM; the
+// epilogue (thread = key row, tau per query column from a shared table) turns
+// them into W^T and dA^T (bf16, written over the consumed columns); then
+// dV += W^T dO_m and dK += dA^T Q_m with the A operand read from TMEM.
+// TMEM: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D,256+2D).
+//
+// dQ kernel, one CTA per 128-row query tile m, looping over key tiles n <= m:
+// S = Q_m K_n^T and dP = dO_m V_n^T; the epilogue (thread = query row) forms
+// dA; then dQ += dA K_n.  TMEM: S [0,128), dP [128,256), dQ [256,256+D).
+//
+// Both: warp 4 = TMA producer, warp 5 = single-thread MMA issuer, warps 0-3 =
+// epilogue; every wait is bounded.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tc_tile.cuh"
+
+namespace bsa {
+namespace {
+
+using tile::PANEL_BYTES;
+constexpr int BT = tile::ROWS;  // 128 rows per query tile and per key tile
+constexpr int BWD_THREADS = 192;
+constexpr int EPI_WARPS = 4;
+constexpr int TMA_WARP = 4;
+constexpr int MMA_WARP = 5;
+constexpr uint32_t TMEM_COLS = 512;
+
+__device__ __forceinline__ float ex2a(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2a(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_WARPS * 32)); }
+
+// ReLU(x)^p and its derivative (0 for x <= 0).
+template <int PC>
+__device__ __forceinline__ void weight_and_grad(float x, float p, float& w, float& g) {
+  const float r = fmaxf(x, 0.0f);
+  if constexpr (PC == POW_ONE) {
+    w = r;
+    g = x > 0.0f ? 1.0f : 0.0f;
+  } else if constexpr (PC == POW_TWO) {
+    w = r * r;
+    g = 2.0f * r;
+  } else {
+    const float l = lg2a(r);  // -inf for r = 0
+    w = ex2a(p * l);
+    g = x > 0.0f ? p * ex2a((p - 1.0f) * l) : 0.0f;
+  }
+}
+
+template <int D>
+struct BwdLayout {
+  static constexpr int NP = D / 64;
+  static constexpr int TILE = NP * PANEL_BYTES;
+  static constexpr int NS = (D == 128) ? 2 : 4;  // ring stages, each two tiles
+  static constexpr int RES_OFF = 0;              // two resident tiles
+  static constexpr int RING_OFF = 2 * TILE;
+  static constexpr int TAU_OFF = RING_OFF + NS * 2 * TILE;  // float[2][128]
+  static constexpr int BAR_OFF = TAU_OFF + 2 * BT * 4;
+  // res_full | ring_full[NS] | ring_empty[NS] | s_full | p_full | acc_full | mma_done
+  static constexpr int NBAR = 1 + 2 * NS + 4;
+  static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int ALLOC = TPTR_OFF + 16 + 1024;
+};
+
+struct BwdBars {
+  uint64_t *res_full, *ring_full, *ring_empty, *s_full, *p_full, *acc_full, *mma_done;
+};
+
+template <int D>
+__device__ __forceinline__ BwdBars bwd_bars(uint8_t* smem) {
+  using L = BwdLayout<D>;
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  BwdBars r;
+  r.res_full = b;
+  r.ring_full = b + 1;
+  r.ring_empty = r.ring_full + L::NS;
+  r.s_full = r.ring_empty + L::NS;
+  r.p_full = r.s_full + 1;
+  r.acc_full = r.p_full + 1;
+  r.mma_done = r.acc_full + 1;
+  return r;
+}
+
+template <int D>
+__device__ __forceinline__ void bwd_setup(uint8_t* smem, const BwdBars& B, uint32_t* tptr, int warp) {
+  using L = BwdLayout<D>;
+  if (threadIdx.x == 0) {
+    mbar_init(B.res_full, 1);
+    for (int s = 0; s < L::NS; ++s) {
+      mbar_init(&B.ring_full[s], 1);
+      mbar_init(&B.ring_empty[s], 1);
+    }
+    mbar_init(B.s_full, 1);
+    mbar_init(B.p_full, EPI_WARPS);
+    mbar_init(B.acc_full, 1);
+    mbar_init(B.mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(tptr, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+
+__device__ __forceinline__ void bwd_teardown(uint32_t tmem, int warp) {
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// Producer: two resident tiles (rows res_row of maps r0, r1), then for
+// j = 0..count-1 two ring tiles (rows (first + j) * 128 of maps g0, g1).
+template <int D>
+__device__ __forceinline__ void bwd_produce(uint8_t* smem, const BwdBars& B, const CUtensorMap* r0,
+                                            const CUtensorMap* r1, int res_row, const CUtensorMap* g0,
+                                            const CUtensorMap* g1, int first, int count, int bh) {
+  using L = BwdLayout<D>;
+  tma_prefetch_desc(r0);
+  tma_prefetch_desc(r1);
+  tma_prefetch_desc(g0);
+  tma_prefetch_desc(g1);
+  mbar_arrive_expect_tx(B.res_full, 2 * L::TILE);
+  tile::tma_tile<D>(smem + L::RES_OFF, r0, B.res_full, res_row, bh);
+  tile::tma_tile<D>(smem + L::RES_OFF + L::TILE, r1, B.res_full, res_row, bh);
+  int issued = 0;
+  bool ok = true;
+  for (int j = 0; j < count; ++j) {
+    const int s = j % L::NS;
+    if (!(ok = mbar_wait(&B.ring_empty[s], ((j / L::NS) & 1) ^ 1))) break;
+    uint8_t* dst = smem + L::RING_OFF + s * 2 * L::TILE;
+    mbar_arrive_expect_tx(&B.ring_full[s], 2 * L::TILE);
+    tile::tma_tile<D>(dst, g0, &B.ring_full[s], (first + j) * BT, bh);
+    tile::tma_tile<D>(dst + L::TILE, g1, &B.ring_full[s], (first + j) * BT, bh);
+    issued = j + 1;
+  }
+  if (!ok) {  // drain what is still landing before the CTA may exit
+    mbar_wait(B.res_full, 0);
+    for (int j = (issued > L::NS ? issued - L::NS : 0); j < issued; ++j)
+      mbar_wait(&B.ring_full[j % L::NS], (j / L::NS) & 1);
+  }
+}
+
+// ---------------------------------------------------------------- dK / dV
+
+template <int D, int PC>
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    tra_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                        __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int T, int nT,
+                        float beta, float p) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const BwdBars B = bwd_bars<D>(smem);
+  uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
+  float* tau_s = reinterpret_cast<float*>(smem + L::TAU_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = static_cast<int>(blockIdx.x) / BH;  // key tile; n = 0 has the most query tiles
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int nq = nT - n;  // query tiles m = n .. nT-1
+  constexpr uint32_t ST = 0, DPT = BT, DV = 2 * BT, DK = 2 * BT + D;
+
+  bwd_setup<D>(smem, B, tptr, warp);
+  const uint32_t tmem = *tptr;
+
+  if (warp == TMA_WARP) {
+    if (lane == 0) bwd_produce<D>(smem, B, &tmK, &tmV, n * BT, &tmQ, &tmDO, n, nq, bh);
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      const uint32_t sK = smem_u32(smem + L::RES_OFF), sV = sK + L::TILE;
+      bool ok = mbar_wait(B.res_full, 0);
+      for (int j = 0; j < nq && ok; ++j) {
+        const int s = j % L::NS;
+        const uint32_t sQ = smem_u32(smem + L::RING_OFF + s * 2 * L::TILE), sDO = sQ + L::TILE;
+        if (!(ok = mbar_wait(&B.ring_full[s], (j / L::NS) & 1))) break;
+        tc_fence_after();
+        tile::mma_abt<D>(tmem + ST, sK, sQ);   // S^T  = K_n Q_m^T
+        tile::mma_abt<D>(tmem + DPT, sV, sDO); // dP^T = V_n dO_m^T
+        mma_commit(B.s_full);
+        if (!(ok = mbar_wait(B.p_full, j & 1))) break;
+        tc_fence_after();
+        tile::mma_tmem_a<D>(tmem + DV, tmem + ST, sDO, 0, BT / 16, j == 0);  // dV += W^T dO_m
+        tile::mma_tmem_a<D>(tmem + DK, tmem + DPT, sQ, 0, BT / 16, j == 0);  // dK += dA^T Q_m
+        mma_commit(&B.ring_empty[s]);
+      }
+      if (ok) mma_commit(B.acc_full);
+      mma_commit(B.mma_done);
+      mbar_wait(B.mma_done, 0);
+    }
+  } else {
+    const int r = warp * 32 + lane;  // key row within the tile
+    const int key = n * BT + r;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    bool ok = true;
+    for (int j = 0; j < nq && ok; ++j) {
+      const int m = n + j;
+      float* tau_m = tau_s + (j & 1) * BT;
+      tau_m[r] = tile::tau_of_row(m * BT + r, beta, D);  // tau of query column r
+      epi_sync();
+      if (!(ok = mbar_wait(B.s_full, j & 1))) break;
+      tc_fence_after();
+      const bool diag = (m == n);
+#pragma unroll 1
+      for (int c = 0; c < BT / 32; ++c) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32(lane_base + ST + 32 * c, sv);
+        tmem_ld32(lane_base + DPT + 32 * c, dp);
+        tmem_wait_ld();
+        uint32_t wpk[16], apk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float w0, g0, w1, g1;
+          const int i0 = 32 * c + 2 * e;  // query column within the tile
+          weight_and_grad<PC>(__uint_as_float(sv[2 * e]) - tau_m[i0], p, w0, g0);
+          weight_and_grad<PC>(__uint_as_float(sv[2 * e + 1]) - tau_m[i0 + 1], p, w1, g1);
+          float a0 = __uint_as_float(dp[2 * e]) * g0, a1 = __uint_as_float(dp[2 * e + 1]) * g1;
+          if (diag) {  // causal: key r <= query column
+            if (i0 < r) w0 = a0 = 0.0f;
+            if (i0 + 1 < r) w1 = a1 = 0.0f;
+          }
+          wpk[e] = pack_bf16x2(w0, w1);
+          apk[e] = pack_bf16x2(a0, a1);
+        }
+        tmem_st16(lane_base + ST + 16 * c, wpk);
+        tmem_st16(lane_base + DPT + 16 * c, apk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.p_full);
+    }
+    if (ok && mbar_wait(B.acc_full, 0)) {
+      tc_fence_after();
+      const size_t rowoff = (static_cast<size_t>(bh) * T + key) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        tile::store_row_chunk(lane_base + DV, c, dv + rowoff, key < T);
+        tile::store_row_chunk(lane_base + DK, c, dk + rowoff, key < T);
+      }
+    }
+  }
+  bwd_teardown(tmem, warp);
+}
+
+// ---------------------------------------------------------------------- dQ
+
+template <int D, int PC>
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    tra_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                      __nv_bfloat16* __restrict__ dq, int BH, int T, int nT, float beta, float p) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const BwdBars B = bwd_bars<D>(smem);
+  uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = nT - 1 - static_cast<int>(blockIdx.x) / BH;  // longest first
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  constexpr uint32_t S = 0, DP = BT, DQ = 2 * BT;
+
+  bwd_setup<D>(smem, B, tptr, warp);
+  const uint32_t tmem = *tptr;
+
+  if (warp == TMA_WARP) {
+    if (lane == 0) bwd_produce<D>(smem, B, &tmQ, &tmDO, m * BT, &tmK, &tmV, 0, m + 1, bh);
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      const uint32_t sQ = smem_u32(smem + L::RES_OFF), sDO = sQ + L::TILE;
+      bool ok = mbar_wait(B.res_full, 0);
+      for (int n = 0; n <= m && ok; ++n) {
+        const int s = n % L::NS;
+        const uint32_t sK = smem_u32(smem + L::RING_OFF + s * 2 * L::TILE), sV = sK + L::TILE;
+        if (!(ok = mbar_wait(&B.ring_full[s], (n / L::NS) & 1))) break;
+        tc_fence_after();
+        tile::mma_abt<D>(tmem + S, sQ, sK);    // S  = Q_m K_n^T
+        tile::mma_abt<D>(tmem + DP, sDO, sV);  // dP = dO_m V_n^T
+        mma_commit(B.s_full);
+        if (!(ok = mbar_wait(B.p_full, n & 1))) break;
+        tc_fence_after();
+        tile::mma_tmem_a<D>(tmem + DQ, tmem + S, sK, 0, BT / 16, n == 0);  // dQ += dA K_n
+        mma_commit(&B.ring_empty[s]);
+      }
+      if (ok) mma_commit(B.acc_full);
+      mma_commit(B.mma_done);
+      mbar_wait(B.mma_done, 0);
+    }
+  } else {
+    const int r = warp * 32 + lane;
+    const int row = m * BT + r;
+    const float tau = tile::tau_of_row(row, beta, D);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    bool ok = true;
+    for (int n = 0; n <= m && ok; ++n) {
+      if (!(ok = mbar_wait(B.s_full, n & 1))) break;
+      tc_fence_after();
+      const bool diag = (n == m);
+#pragma unroll 1
+      for (int c = 0; c < BT / 32; ++c) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32(lane_base + S + 32 * c, sv);
+        tmem_ld32(lane_base + DP + 32 * c, dp);
+        tmem_wait_ld();
+        uint32_t apk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float w0, g0, w1, g1;
+          weight_and_grad<PC>(__uint_as_float(sv[2 * e]) - tau, p, w0, g0);
+          weight_and_grad<PC>(__uint_as_float(sv[2 * e + 1]) - tau, p, w1, g1);
+          float a0 = __uint_as_float(dp[2 * e]) * g0, a1 = __uint_as_float(dp[2 * e + 1]) * g1;
+          if (diag) {  // causal: key column <= query row r
+            const int kc = 32 * c + 2 * e;
+            if (kc > r) a0 = 0.0f;
+            if (kc + 1 > r) a1 = 0.0f;
+          }
+          apk[e] = pack_bf16x2(a0, a1);
+        }
+        tmem_st16(lane_base + S + 16 * c, apk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.p_full);
+    }
+    if (ok && mbar_wait(B.acc_full, 0)) {
+      tc_fence_after();
+      __nv_bfloat16* dst = dq + (static_cast<size_t>(bh) * T + row) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tile::store_row_chunk(lane_base + DQ, c, dst, row < T);
+    }
+  }
+  bwd_teardown(tmem, warp);
+}
+
+template <int D, int PC>
+int launch_bwd(const CUtensorMap* maps, void* dq, void* dk, void* dv, int BH, int T, float beta, float p,
+               cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  auto k1 = tra_bwd_dkdv_kernel<D, PC>;
+  auto k2 = tra_bwd_dq_kernel<D, PC>;
+  if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess ||
+      cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
+    return ERR_LAUNCH;
+  const int nT = (T + BT - 1) / BT;
+  const long long grid = static_cast<long long>(nT) * BH;
+  if (grid > 0x7fffffffLL) return ERR_SHAPE;
+  k1<<<static_cast<unsigned>(grid), BWD_THREADS, L::ALLOC, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), BH, T,
+      nT, beta, p);
+  if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
+  k2<<<static_cast<unsigned>(grid), BWD_THREADS, L::ALLOC, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dq), BH, T, nT, beta, p);
+  return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
+}
+
+}  // namespace
+
+int launch_tra_bwd_bf16(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv,
+                        int B, int H, int T, int D, float beta, float p, cudaStream_t stream) {
+  const int BH = B * H;
+  CUtensorMap maps[4];
+  const uint64_t rs = static_cast<uint64_t>(D) * 2, hs = rs * T;
+  const void* src[4] = {q, k, v, dout};
+  for (int i = 0; i < 4; ++i) {
+    const int st = encode_tmap_3d(&maps[i], src[i], D, T, BH, rs, hs, 64, BT, 1);
+    if (st != OK) return st;
+  }
+  const int pc = power_class(p);
+  if (D == 128) {
+    if (pc == POW_TWO) return launch_bwd<128, POW_TWO>(maps, dq, dk, dv, BH, T, beta, p, stream);
+    if (pc == POW_ONE) return launch_bwd<128, POW_ONE>(maps, dq, dk, dv, BH, T, beta, p, stream);
+    return launch_bwd<128, POW_GENERAL>(maps, dq, dk, dv, BH, T, beta, p, stream);
+  }
+  if (D == 64) {
+    if (pc == POW_TWO) return launch_bwd<64, POW_TWO>(maps, dq, dk, dv, BH, T, beta, p, stream);
+    if (pc == POW_ONE) return launch_bwd<64, POW_ONE>(maps, dq, dk, dv, BH, T, beta, p, stream);
+    return launch_bwd<64, POW_GENERAL>(maps, dq, dk, dv, BH, T, beta, p, stream);
+  }
+  return ERR_UNSUPPORTED;
+}
+
+unsigned int tra_bwd_device_error() { return read_and_clear_device_error(); }
+
+}  // namespace bsa

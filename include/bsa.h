@@ -95,6 +95,35 @@ BSA_API int tra_forward(const void* q, const void* k, const void* v, void* out,
                         int dtype, cudaStream_t stream);
 
 /*
+ * tra_backward -- gradients of the threshold rectified attention forward.
+ *
+ * Defined on the page "triton_threshold_attention.py": ThresholdRelaFunction
+ * .backward with the kernels _threshold_rela_bwd_kernel_dq and
+ * _threshold_rela_bwd_kernel_dkv.  With x_ij = q_i . k_j - tau(i) over the
+ * causal pairs j <= i and dout the gradient of out:
+ *
+ *   W_ij  = ReLU(x_ij)^p                    dv_j = sum_i W_ij dout_i
+ *   dA_ij = (dout_i . v_j) p ReLU(x_ij)^(p-1)   (0 where x_ij <= 0)
+ *   dq_i  = sum_j dA_ij k_j                 dk_j = sum_i dA_ij q_i
+ *
+ * beta and p receive no gradient (as on the page).  Scores are recomputed
+ * (nothing is saved by tra_forward).  Two kernel launches on `stream`: one
+ * per key tile for dk and dv, one per query tile for dq.
+ *
+ *   q, k, v, dout       : [B, H, T, D] bf16 inputs (dout = dL/d out).
+ *   dq, dk, dv          : [B, H, T, D] bf16 outputs (fp32 accumulation);
+ *                         they must not alias the inputs or each other.
+ *   B, H, T, D, beta, p : as for tra_forward.
+ *   dtype               : BSA_BF16 (BSA_F32 returns BSA_ERR_UNSUPPORTED).
+ *
+ * Errors: as for tra_forward.
+ */
+BSA_API int tra_backward(const void* q, const void* k, const void* v,
+                         const void* dout, void* dq, void* dk, void* dv,
+                         int B, int H, int T, int D, float beta, float p,
+                         int dtype, cudaStream_t stream);
+
+/*
  * nsa_select_forward -- NSA selection-branch attention forward (bf16).
  *
  * Defined on the page "nsa_selection_kernel.py" (openbox-llm): module
