@@ -158,6 +158,31 @@ def tra_backward(q, k, v, dout, beta: float, p: float, block: int = 256):
     return dq, dk, dv
 
 
+def l2_normalize(x, eps: float = 1e-12) -> np.ndarray:
+    """Rows scaled to unit L2 norm along the last axis: ``x / max(||x||, eps)``
+    (the page calls ``torch.nn.functional.normalize(x, p=2, dim=-1)``, whose
+    default eps is 1e-12)."""
+    x = np.asarray(x, dtype=np.float64)
+    n = np.sqrt((x * x).sum(axis=-1, keepdims=True))
+    return x / np.maximum(n, eps)
+
+
+def tra_diff_forward(q1, q2, k1, k2, v, beta: float, lam: float, p: float, normalize: bool = True,
+                     block: int = 256) -> np.ndarray:
+    """Threshold differential attention (page "triton_threshold_attention.py",
+    ``differential_threshold_rela_triton``):
+
+        out = TRA(q1, k1, v) - clamp(lam, 0, 1) * TRA(q2, k2, v),
+
+    with q1, k1, q2, k2 first L2-normalised row by row when ``normalize``
+    (cosine-similarity scores).  Both TRA terms share beta, p and v.
+    """
+    if normalize:
+        q1, q2, k1, k2 = (l2_normalize(a) for a in (q1, q2, k1, k2))
+    lam_c = min(max(float(lam), 0.0), 1.0)
+    return tra_forward(q1, k1, v, beta, p, block) - lam_c * tra_forward(q2, k2, v, beta, p, block)
+
+
 def tra_flops(B: int, H: int, T: int, D: int) -> int:
     """Algorithmic FLOPs of one causal TRA forward: two multiply-adds of length
     D (one for q_i.k_j, one for w_ij v_j) per causally valid pair (i, j<=i)."""

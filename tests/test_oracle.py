@@ -567,3 +567,48 @@ def test_tra_backward_textbook_beta0_p1():
 
 def test_tra_backward_flops_count():
     assert tra.tra_backward_flops(1, 1, 3, 2) == 10 * 2 * 6
+
+
+# ----------------------------------------------------------- differential TRA
+
+def test_l2_normalize_matches_torch():
+    x = rng(30).standard_normal((2, 3, 7, 5))
+    x[0, 0, 0] = 0.0  # zero row stays zero (eps)
+    want = torch.nn.functional.normalize(torch.from_numpy(x), p=2, dim=-1).numpy()
+    np.testing.assert_allclose(tra.l2_normalize(x), want, rtol=1e-14, atol=1e-300)
+
+
+def test_tra_diff_special_cases():
+    q1, k1, v = rand_tra(1, 2, 40, 8, seed=31)
+    q2, k2, _ = rand_tra(1, 2, 40, 8, seed=32)
+    beta, p = 0.2, 2.0
+    base = tra.tra_forward(tra.l2_normalize(q1), tra.l2_normalize(k1), v, beta, p)
+    # lambda = 0 (and below 0, clamped) leaves the first term
+    np.testing.assert_allclose(tra.tra_diff_forward(q1, q2, k1, k2, v, beta, 0.0, p), base, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(tra.tra_diff_forward(q1, q2, k1, k2, v, beta, -3.0, p), base, rtol=1e-13, atol=1e-13)
+    # lambda >= 1 clamps to 1; equal streams cancel
+    np.testing.assert_allclose(tra.tra_diff_forward(q1, q1, k1, k1, v, beta, 1.0, p), 0.0, atol=1e-12)
+    np.testing.assert_allclose(tra.tra_diff_forward(q1, q2, k1, k2, v, beta, 7.0, p),
+                               tra.tra_diff_forward(q1, q2, k1, k2, v, beta, 1.0, p), rtol=1e-13, atol=1e-13)
+    # normalisation: positive row scalings of q or k change nothing
+    sc = np.abs(rng(33).standard_normal(q1.shape[:-1] + (1,))) + 0.1
+    np.testing.assert_allclose(tra.tra_diff_forward(q1 * sc, q2, k1, k2 / sc, v, beta, 0.4, p),
+                               tra.tra_diff_forward(q1, q2, k1, k2, v, beta, 0.4, p), rtol=1e-11, atol=1e-12)
+    # without normalisation it is the plain difference of two TRAs
+    want = tra.tra_forward(q1, k1, v, beta, p) - 0.4 * tra.tra_forward(q2, k2, v, beta, p)
+    np.testing.assert_allclose(tra.tra_diff_forward(q1, q2, k1, k2, v, beta, 0.4, p, normalize=False), want,
+                               rtol=1e-13, atol=1e-13)
+
+
+def test_tra_diff_normalised_scores_are_cosines():
+    """With normalisation and beta = 0, p = 1, row 0 is max(cos(q1_0, k1_0), 0) v_0
+    minus lambda times the same for stream 2."""
+    q1, k1, v = rand_tra(1, 1, 5, 6, seed=34)
+    q2, k2, _ = rand_tra(1, 1, 5, 6, seed=35)
+    out = tra.tra_diff_forward(q1, q2, k1, k2, v, 0.0, 0.25, 1.0)
+
+    def cos(a, b):
+        return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b)))
+
+    want = max(cos(q1[0, 0, 0], k1[0, 0, 0]), 0) * v[0, 0, 0] - 0.25 * max(cos(q2[0, 0, 0], k2[0, 0, 0]), 0) * v[0, 0, 0]
+    np.testing.assert_allclose(out[0, 0, 0], want, rtol=1e-12, atol=1e-14)
