@@ -23,6 +23,8 @@ from .bsa import (  # noqa: F401
     status_string,
     tra_backward,
     tra_backward_raw,
+    tra_diff_forward,
+    tra_diff_forward_raw,
     tra_forward,
     tra_forward_raw,
 )
@@ -36,6 +38,8 @@ __all__ = [
     "tra_forward_raw",
     "tra_backward",
     "tra_backward_raw",
+    "tra_diff_forward",
+    "tra_diff_forward_raw",
     "nsa_select_forward",
     "nsa_select_forward_raw",
     "status_string",

@@ -26,6 +26,7 @@ _STATUS = {
     5: "BSA_ERR_LAUNCH",
     6: "BSA_ERR_DEVICE",
     7: "BSA_ERR_ALIGN",
+    8: "BSA_ERR_MEMORY",
 }
 
 
@@ -57,6 +58,8 @@ def load_library():
     lib.nsa_select_forward.restype = i32
     lib.tra_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, vp]
     lib.tra_backward.restype = i32
+    lib.tra_diff_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, f32, i32, i32, vp]
+    lib.tra_diff_forward.restype = i32
     lib.bsa_status_string.argtypes = [i32]
     lib.bsa_status_string.restype = ctypes.c_char_p
     lib.bsa_version.argtypes = []
@@ -91,6 +94,12 @@ def tra_backward_raw(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, dtype, stre
     """Direct C call with integer device pointers; returns the bsa_status."""
     return load_library().tra_backward(q, k, v, dout, dq, dk, dv, B, H, T, D, float(beta), float(p), int(dtype),
                                        stream)
+
+
+def tra_diff_forward_raw(q1, q2, k1, k2, v, out, B, H, T, D, beta, lam, p, normalize, dtype, stream=0) -> int:
+    """Direct C call with integer device pointers; returns the bsa_status."""
+    return load_library().tra_diff_forward(q1, q2, k1, k2, v, out, B, H, T, D, float(beta), float(lam), float(p),
+                                           int(bool(normalize)), int(dtype), stream)
 
 
 def nsa_select_forward_raw(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, block_size, S,
@@ -163,6 +172,31 @@ def tra_backward(q, k, v, dout, beta: float, p: float = 2.0, stream=None):
                           dv.data_ptr(), B, H, T, D, beta, p, _dtype_code(q), _stream_handle(stream))
     _check(st, "tra_backward")
     return dq, dk, dv
+
+
+def tra_diff_forward(q1, q2, k1, k2, v, beta: float, lam: float, p: float = 2.0, normalize: bool = True,
+                     out=None, stream=None):
+    """Threshold differential attention on bf16 CUDA tensors ``[B, H, T, D]``:
+    ``TRA(n(q1), n(k1), v) - clamp(lam, 0, 1) * TRA(n(q2), n(k2), v)`` with
+    ``n`` the row-wise L2 normalisation when ``normalize``."""
+    import torch
+
+    ts = (q1, q2, k1, k2, v)
+    if q1.device.type != "cuda":
+        raise BsaError("tra_diff_forward takes CUDA tensors (no CPU path)")
+    if any(t.shape != q1.shape for t in ts) or q1.dim() != 4:
+        raise BsaError("q1, q2, k1, k2, v must share one shape [B, H, T, D]", 2)
+    if any(t.dtype != q1.dtype for t in ts):
+        raise BsaError("q1, q2, k1, k2, v must share one dtype", 3)
+    q1, q2, k1, k2, v = (t.contiguous() for t in ts)
+    if out is None:
+        out = torch.empty_like(q1)
+    B, H, T, D = q1.shape
+    st = tra_diff_forward_raw(q1.data_ptr(), q2.data_ptr(), k1.data_ptr(), k2.data_ptr(), v.data_ptr(),
+                              out.data_ptr(), B, H, T, D, beta, lam, p, normalize, _dtype_code(q1),
+                              _stream_handle(stream))
+    _check(st, "tra_diff_forward")
+    return out
 
 
 def nsa_select_forward(q, k, v, block_idx, block_size: int = 64, out=None, lse=None,

@@ -101,6 +101,34 @@ int tra_backward(const void* q, const void* k, const void* v, const void* dout, 
   return launch_tra_bwd_bf16(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, stream);
 }
 
+int tra_diff_forward(const void* q1, const void* q2, const void* k1, const void* k2, const void* v, void* out, int B,
+                     int H, int T, int D, float beta, float lambda, float p, int normalize, int dtype,
+                     cudaStream_t stream) {
+  if (q1 == nullptr || q2 == nullptr || k1 == nullptr || k2 == nullptr || v == nullptr || out == nullptr)
+    return BSA_ERR_NULLPTR;
+  if (dtype != BSA_F32 && dtype != BSA_BF16) return BSA_ERR_DTYPE;
+  if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
+  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (dtype != BSA_BF16) return BSA_ERR_UNSUPPORTED;
+  if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f) || isnan(lambda)) return BSA_ERR_UNSUPPORTED;
+  const void* ptrs[6] = {q1, q2, k1, k2, v, out};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return BSA_ERR_ALIGN;
+  const int dvs = check_device();
+  if (dvs != OK) return dvs;
+  if (!normalize) return launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, nullptr, stream);
+  // Normalisation factors of every row of q1, k1, q2, k2 (T padded to a
+  // multiple of 128): a stream-ordered temporary, released on the same stream.
+  float* inv = nullptr;
+  const size_t bytes = tra_diff_scratch_bytes(B, H, T);
+  if (cudaMallocAsync(reinterpret_cast<void**>(&inv), bytes, stream) != cudaSuccess) return BSA_ERR_MEMORY;
+  const int st = launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, inv, stream);
+  if (cudaFreeAsync(inv, stream) != cudaSuccess && st == OK) return BSA_ERR_MEMORY;
+  return st;
+}
+
 int nsa_select_forward(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out, float* lse,
                        int B, int Hq, int Hkv, int T, int D, int block_size, int S, cudaStream_t stream) {
   if (q == nullptr || k == nullptr || v == nullptr || block_idx == nullptr || out == nullptr)
@@ -133,6 +161,7 @@ const char* bsa_status_string(int status) {
     case BSA_ERR_LAUNCH: return "CUDA kernel launch failed";
     case BSA_ERR_DEVICE: return "no usable sm_103 device or CUDA driver entry point";
     case BSA_ERR_ALIGN: return "a tensor pointer is not suitably aligned";
+    case BSA_ERR_MEMORY: return "scratch memory could not be allocated or released";
     default: return "unknown bsa_status";
   }
 }
@@ -140,8 +169,8 @@ const char* bsa_status_string(int status) {
 int bsa_version(void) { return 100; }
 
 int bsa_device_error(void) {
-  const unsigned codes[4] = {tra_bf16_device_error(), tra_f32_device_error(), nsa_device_error(),
-                             tra_bwd_device_error()};
+  const unsigned codes[5] = {tra_bf16_device_error(), tra_f32_device_error(), nsa_device_error(),
+                             tra_bwd_device_error(), tra_diff_device_error()};
   unsigned worst = 0;
   for (unsigned c : codes) {
     if (c == 0xffffffffu) return -1;

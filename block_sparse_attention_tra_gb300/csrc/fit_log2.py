@@ -3,7 +3,7 @@
 The epilogue splits x = 2^e * m (m in [1, 2)) with integer bit operations
 and approximates log2(m) by a degree-4 polynomial in m, fitted here by least
 squares on Chebyshev nodes of [1, 2] (a near-minimax fit).  Run this script
-to regenerate the constants LOG2_C0..LOG2_C4 of ``tra_bf16.cu``; it prints the header and
+to regenerate the constants LOG2_C0..LOG2_C4 of ``tra_math.cuh``; it prints the header and
 the maximum absolute error of the fit in float64 and when evaluated in
 float32 Horner form.
 """

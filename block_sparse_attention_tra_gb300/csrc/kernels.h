@@ -18,6 +18,7 @@ enum Status : int {
   ERR_LAUNCH = 5,
   ERR_DEVICE = 6,
   ERR_ALIGN = 7,
+  ERR_MEMORY = 8,
 };
 
 // Encode a rank-3 bf16 (or other 2-byte) tensor map with 128-byte swizzle.
@@ -38,6 +39,15 @@ int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int 
 int launch_tra_bwd_bf16(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv,
                         int B, int H, int T, int D, float beta, float p, cudaStream_t stream);
 
+// Threshold differential attention (fused two-stream kernel).  inv_norm is a
+// float scratch buffer of tra_diff_scratch_bytes(B, H, T) bytes (256-byte
+// aligned) for the row normalisation factors, or null to skip the
+// normalisation.
+size_t tra_diff_scratch_bytes(int B, int H, int T);
+int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const void* k2, const void* v, void* out,
+                         int B, int H, int T, int D, float beta, float lam, float p, float* inv_norm,
+                         cudaStream_t stream);
+
 // NSA selection attention, bf16 kernel.
 int launch_nsa_select(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out,
                       float* lse, int B, int Hq, int Hkv, int T, int D, int block_size, int S,
@@ -49,6 +59,7 @@ unsigned int tra_bf16_device_error();
 unsigned int tra_f32_device_error();
 unsigned int nsa_device_error();
 unsigned int tra_bwd_device_error();
+unsigned int tra_diff_device_error();
 
 // Power class of the TRA epilogue: p == 1, p == 2, or the general exp2/log2 path.
 enum PowerClass : int { POW_GENERAL = 0, POW_ONE = 1, POW_TWO = 2 };

@@ -17,7 +17,7 @@ namespace bsa {
 // ~1 s at the GB300 boost clock; no wait in a healthy launch comes close.
 constexpr long long BSA_WAIT_LIMIT_CYCLES = 2000000000LL;
 
-enum : unsigned { BSA_DEVERR_NONE = 0, BSA_DEVERR_TIMEOUT = 1 };
+enum : unsigned { BSA_DEVERR_NONE = 0, BSA_DEVERR_TIMEOUT = 1, BSA_DEVERR_LAYOUT = 2 };
 
 // Device error word of this translation unit (each kernel file has its own;
 // the host reads and clears them through bsa_device_error()).
@@ -124,6 +124,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+// Untiled bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0),
+// completing on `bar` like a tensor copy.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 
 // --------------------------------------------------------------- tcgen05

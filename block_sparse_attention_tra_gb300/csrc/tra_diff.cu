@@ -1,0 +1,403 @@
+// tra_diff.cu -- threshold differential attention forward (bf16, tcgen05).
+//
+// Method: page "triton_threshold_attention.py", differential_threshold_rela_
+// triton: optionally L2-normalise q1, k1, q2, k2 row by row, then
+//     out = TRA(q1, k1, v) - clamp(lambda, 0, 1) * TRA(q2, k2, v)
+// with both threshold-attention terms sharing beta, p and v.
+//
+// Fused: one CTA owns 128 query rows of one (b, h) and runs the two score
+// streams side by side.  Stream t has its own Q_t (resident) and K_t tiles,
+// both streams share each V tile, and both P V products accumulate into ONE
+// TMEM accumulator O: the second stream's weights are multiplied by
+// -clamp(lambda, 0, 1) before they are rounded, so O ends up holding the
+// difference and V is read once for both streams.
+//   warp 8      TMA producer (Q0, Q1 once; K0+K1 and V tiles in rings).
+//   warp 9      MMA issuer: ... PV0(n), QK0(n+1), PV1(n), QK1(n+1) ...
+//   warps 4t..  epilogue of stream t (thread = query row).
+// TMEM: S0 [0,128), S1 [128,256), O [256,256+D).
+//
+// Normalisation does not rewrite q or k: with r(x) = 1 / max(||x||, 1e-12)
+// the normalised score is s_ij r(q_i) r(k_j).  A pre-pass kernel writes r()
+// of every row of q1, k1, q2, k2 into a float scratch buffer [4, B*H, Tp]
+// (Tp = T rounded up to 128, zero past T); the producer copies the 2 x 128
+// factors of each key tile (k1 and k2 rows) into a small shared-memory ring
+// of its own (bulk copies), and the epilogue scales each score by
+// r(q_i) r(k_j) before subtracting tau.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tc_tile.cuh"
+#include "tra_math.cuh"
+
+namespace bsa {
+namespace {
+
+using tile::PANEL_BYTES;
+constexpr int BT = tile::ROWS;
+constexpr int DIFF_THREADS = 320;
+constexpr int DIFF_TMA_WARP = 8;
+constexpr int DIFF_MMA_WARP = 9;
+
+template <int D>
+struct DiffLayout {
+  static constexpr int NP = D / 64;
+  static constexpr int TILE = NP * PANEL_BYTES;
+  static constexpr int NSK0 = (D == 128) ? 2 : 3;  // K of stream 0 (needed first in each step)
+  static constexpr int NSK1 = (D == 128) ? 1 : 3;  // K of stream 1
+  static constexpr int NSV = (D == 128) ? 2 : 3;   // V (shared by both streams)
+  static constexpr int NSR = 2;                    // key-factor ring (k1 and k2 rows of one key tile)
+  static constexpr int RK_BYTES = BT * 4;
+  static constexpr int Q_OFF = 0;                  // Q0, Q1
+  static constexpr int K0_OFF = 2 * TILE;
+  static constexpr int K1_OFF = K0_OFF + NSK0 * TILE;
+  static constexpr int V_OFF = K1_OFF + NSK1 * TILE;
+  static constexpr int RK_OFF = V_OFF + NSV * TILE;
+  static constexpr int BAR_OFF = RK_OFF + NSR * 2 * RK_BYTES;
+  // q_full | k0 full/empty | k1 full/empty | v full/empty | rk full/empty | s_full[2] | p_full[2] | o_full |
+  // mma_done
+  static constexpr int NBAR = 1 + 2 * (NSK0 + NSK1 + NSV + NSR) + 6;
+  static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int ALLOC = TPTR_OFF + 16;  // the dynamic smem base is 1024-byte aligned
+  static_assert(ALLOC <= 232448, "shared memory budget");
+};
+
+// A ring of NS single-tile stages with full/empty barriers.
+struct Ring {
+  uint64_t* full;
+  uint64_t* empty;
+  int off, ns;
+  __device__ __forceinline__ int stage(int n) const { return n % ns; }
+  __device__ __forceinline__ uint32_t phase(int n) const { return (n / ns) & 1; }
+};
+
+// 1 / max(||row||_2, 1e-12) for every row of the four inputs into
+// inv[which][bh][Tp] (0 for the padding rows t >= T); one warp per row, fp32
+// accumulation of the squared bf16 elements.
+__global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* __restrict__ a0,
+                                                           const __nv_bfloat16* __restrict__ a1,
+                                                           const __nv_bfloat16* __restrict__ a2,
+                                                           const __nv_bfloat16* __restrict__ a3,
+                                                           float* __restrict__ inv, int BH, int T, int Tp, int D) {
+  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long rows_p = static_cast<long long>(BH) * Tp;
+  if (gw >= 4 * rows_p) return;
+  const int which = static_cast<int>(gw / rows_p);
+  const long long rem = gw - static_cast<long long>(which) * rows_p;
+  const long long bh = rem / Tp;
+  const int t = static_cast<int>(rem - bh * Tp);
+  if (t >= T) {
+    if (lane == 0) inv[gw] = 0.0f;
+    return;
+  }
+  const __nv_bfloat16* src = which == 0 ? a0 : which == 1 ? a1 : which == 2 ? a2 : a3;
+  const __nv_bfloat16* x = src + (bh * T + t) * D;
+  float acc = 0.0f;
+  for (int d = lane * 2; d < D; d += 64) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(x + d));
+    acc = fmaf(f.x, f.x, acc);
+    acc = fmaf(f.y, f.y, acc);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) inv[gw] = 1.0f / fmaxf(sqrtf(acc), 1e-12f);
+}
+
+// 32 scores of stream t -> 16 packed weights (scaled by `wscale` when
+// SCALE_W), over the consumed score columns.  With NORM the scores are first
+// multiplied by rq * rk[col] (the normalisation of row and key).
+template <int PC, bool NORM, bool SCALE_W>
+__device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t tS, int c0, float tau, float p,
+                                             const float (&pc)[5], float rq, const float (&rk)[32], uint32_t wscale,
+                                             bool diag, int key0, int row) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    float s0 = __uint_as_float(s[2 * e]), s1 = __uint_as_float(s[2 * e + 1]);
+    if constexpr (NORM) {
+      s0 *= rq * rk[2 * e];
+      s1 *= rq * rk[2 * e + 1];
+    }
+    const bool emu = e >= 16 - EMU_LOG2_PAIRS;
+    uint32_t w = emu ? weights2<PC, true>(s0, s1, tau, p, pc) : weights2<PC, false>(s0, s1, tau, p, pc);
+    if constexpr (SCALE_W) w = mul_bf16x2(w, wscale);
+    if (diag) {
+      const int key = key0 + c0 + 2 * e;
+      if (key > row) w = 0u;
+      else if (key + 1 > row) w &= 0x0000ffffu;
+    }
+    pk[e] = w;
+  }
+  tmem_st16(tS + c0 / 2, pk);
+}
+
+template <int D, int PC, bool NORM>
+__global__ void __launch_bounds__(DIFF_THREADS, 1)
+    tra_diff_kernel(const __grid_constant__ CUtensorMap tmQ0, const __grid_constant__ CUtensorMap tmQ1,
+                    const __grid_constant__ CUtensorMap tmK0, const __grid_constant__ CUtensorMap tmK1,
+                    const __grid_constant__ CUtensorMap tmV, const float* __restrict__ inv_norm,
+                    __nv_bfloat16* __restrict__ out, int BH, int T, int nQ, float beta, float p, float lam) {
+  const int Tp = nQ * BT;  // row stride of the normalisation buffer
+  using L = DiffLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  // The swizzled tiles need a 1024-byte aligned base (the layout has no slack
+  // to round it up); refuse to run rather than compute garbage.
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) record_device_error(BSA_DEVERR_LAYOUT);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* q_full = bars;
+  uint64_t* b1 = bars + 1;
+  const Ring rk0{b1, b1 + L::NSK0, L::K0_OFF, L::NSK0};
+  b1 += 2 * L::NSK0;
+  const Ring rk1{b1, b1 + L::NSK1, L::K1_OFF, L::NSK1};
+  b1 += 2 * L::NSK1;
+  const Ring rv{b1, b1 + L::NSV, L::V_OFF, L::NSV};
+  b1 += 2 * L::NSV;
+  const Ring rr{b1, b1 + L::NSR, L::RK_OFF, L::NSR};
+  b1 += 2 * L::NSR;
+  uint64_t* s_full = b1;  // [2]
+  uint64_t* p_full = s_full + 2;                                    // [2]
+  uint64_t* o_full = p_full + 2;
+  uint64_t* mma_done = o_full + 1;
+  uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = nQ - 1 - static_cast<int>(blockIdx.x) / BH;  // longest first
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int nmax = m;
+  constexpr uint32_t O_COL = 2 * BT;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2 * (L::NSK0 + L::NSK1 + L::NSV); ++i) mbar_init(bars + 1 + i, 1);
+    for (int i = 0; i < L::NSR; ++i) {
+      mbar_init(&rr.full[i], 1);
+      mbar_init(&rr.empty[i], 8);  // four warps of each stream's epilogue
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], 4);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == DIFF_MMA_WARP) {
+    tmem_alloc(tptr, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tptr;
+
+  if (warp == DIFF_TMA_WARP) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ0);
+      tma_prefetch_desc(&tmQ1);
+      tma_prefetch_desc(&tmK0);
+      tma_prefetch_desc(&tmK1);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(q_full, 2 * L::TILE);
+      tile::tma_tile<D>(smem + L::Q_OFF, &tmQ0, q_full, m * BT, bh);
+      tile::tma_tile<D>(smem + L::Q_OFF + L::TILE, &tmQ1, q_full, m * BT, bh);
+      bool ok = true;
+      int issued[3] = {0, 0, 0};
+      const Ring* rings[3] = {&rk0, &rk1, &rv};
+      const CUtensorMap* maps[3] = {&tmK0, &tmK1, &tmV};
+      int issued_rk = 0;
+      for (int n = 0; n <= nmax && ok; ++n) {
+        if constexpr (NORM) {  // key factors of the k1 and k2 rows of key tile n
+          if (!(ok = mbar_wait(&rr.empty[rr.stage(n)], rr.phase(n) ^ 1))) break;
+          mbar_arrive_expect_tx(&rr.full[rr.stage(n)], 2 * L::RK_BYTES);
+          uint8_t* dst = smem + rr.off + rr.stage(n) * 2 * L::RK_BYTES;
+          // inv_norm rows [q1 | k1 | q2 | k2]: k1 = 1, k2 = 3
+          bulk_load(dst, inv_norm + (1LL * BH + bh) * Tp + n * BT, L::RK_BYTES, &rr.full[rr.stage(n)]);
+          bulk_load(dst + L::RK_BYTES, inv_norm + (3LL * BH + bh) * Tp + n * BT, L::RK_BYTES, &rr.full[rr.stage(n)]);
+          issued_rk = n + 1;
+        }
+        for (int r = 0; r < 3; ++r) {
+          const Ring& R = *rings[r];
+          if (!(ok = mbar_wait(&R.empty[R.stage(n)], R.phase(n) ^ 1))) break;
+          mbar_arrive_expect_tx(&R.full[R.stage(n)], L::TILE);
+          tile::tma_tile<D>(smem + R.off + R.stage(n) * L::TILE, maps[r], &R.full[R.stage(n)], n * BT, bh);
+          issued[r] = n + 1;
+        }
+      }
+      if (!ok) {  // drain: never leave with a bulk copy still landing
+        mbar_wait(q_full, 0);
+        for (int n = (issued_rk > L::NSR ? issued_rk - L::NSR : 0); n < issued_rk; ++n)
+          mbar_wait(&rr.full[rr.stage(n)], rr.phase(n));
+        for (int r = 0; r < 3; ++r) {
+          const Ring& R = *rings[r];
+          for (int n = (issued[r] > R.ns ? issued[r] - R.ns : 0); n < issued[r]; ++n)
+            mbar_wait(&R.full[R.stage(n)], R.phase(n));
+        }
+      }
+    }
+  } else if (warp == DIFF_MMA_WARP) {
+    if (lane == 0) {
+      const uint32_t sQ = smem_u32(smem + L::Q_OFF);
+      // QKt(n): S_t = Q_t K_t(n)^T, then release K_t(n).
+      auto qk = [&](int t, int n) -> bool {
+        const Ring& R = t == 0 ? rk0 : rk1;
+        if (!mbar_wait(&R.full[R.stage(n)], R.phase(n))) return false;
+        tc_fence_after();
+        tile::mma_abt<D>(tmem + t * BT, sQ + t * L::TILE, smem_u32(smem + R.off + R.stage(n) * L::TILE));
+        mma_commit(&s_full[t]);
+        mma_commit(&R.empty[R.stage(n)]);
+        return true;
+      };
+      // PVt(n): O += P_t V(n) (stream 1's P already carries -lambda).
+      auto pv = [&](int t, int n) -> bool {
+        if (!mbar_wait(&p_full[t], n & 1) || !mbar_wait(&rv.full[rv.stage(n)], rv.phase(n))) return false;
+        tc_fence_after();
+        const uint32_t sV = smem_u32(smem + rv.off + rv.stage(n) * L::TILE);
+        tile::mma_tmem_a<D>(tmem + O_COL, tmem + t * BT, sV, 0, BT / 16, t == 0 && n == 0);
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0) && qk(0, 0) && qk(1, 0);
+      for (int n = 0; n <= nmax && ok; ++n) {
+        const int n1 = n + 1;
+        if (!(ok = pv(0, n))) break;
+        if (n1 <= nmax && !(ok = qk(0, n1))) break;
+        if (!(ok = pv(1, n))) break;
+        mma_commit(&rv.empty[rv.stage(n)]);
+        if (n1 <= nmax && !(ok = qk(1, n1))) break;
+      }
+      if (ok) mma_commit(o_full);
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0);
+    }
+  } else {
+    const int t = warp >> 2, wq = warp & 3;
+    const int row = m * BT + wq * 32 + lane;
+    const float tau = tile::tau_of_row(row, beta, D);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t tS = lane_base + t * BT;
+    const float pc[5] = {p * LOG2_C0, p * LOG2_C1, p * LOG2_C2, p * LOG2_C3, p * LOG2_C4};
+    const float lc = fminf(fmaxf(lam, 0.0f), 1.0f);
+    const uint32_t wscale = pack_bf16x2(-lc, -lc);
+    // inv_norm: [q1 | k1 | q2 | k2] x [B*H] x [Tp], zero past T
+    const float rq = NORM ? inv_norm[(static_cast<long long>(t == 0 ? 0 : 2) * BH + bh) * Tp + row] : 1.0f;
+    bool ok = true;
+    for (int n = 0; n <= nmax; ++n) {
+      if (!(ok = mbar_wait(&s_full[t], n & 1))) break;
+      tc_fence_after();
+      const bool diag = (n == nmax);
+      // Key normalisation factors of this tile (stream t's half of the stage).
+      const float* rk_tile =
+          reinterpret_cast<const float*>(smem + rr.off + rr.stage(n) * 2 * L::RK_BYTES + t * L::RK_BYTES);
+      if (NORM && !(ok = mbar_wait(&rr.full[rr.stage(n)], rr.phase(n)))) break;
+#pragma unroll 1
+      for (int c = 0; c < BT / 32; ++c) {
+        float rk[32];
+        if constexpr (NORM) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(rk_tile + 32 * c + j);
+            rk[j] = f.x;
+            rk[j + 1] = f.y;
+            rk[j + 2] = f.z;
+            rk[j + 3] = f.w;
+          }
+        }
+        uint32_t sv[32];
+        tmem_ld32(tS + 32 * c, sv);
+        tmem_wait_ld();
+        if (t == 0)
+          diff_quarter<PC, NORM, false>(sv, tS, 32 * c, tau, p, pc, rq, rk, wscale, diag, n * BT, row);
+        else
+          diff_quarter<PC, NORM, true>(sv, tS, 32 * c, tau, p, pc, rq, rk, wscale, diag, n * BT, row);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&p_full[t]);
+        if constexpr (NORM) mbar_arrive(&rr.empty[rr.stage(n)]);  // done with the key factors
+      }
+    }
+    if (ok && mbar_wait(o_full, 0)) {
+      tc_fence_after();
+      __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * T + row) * D;
+      for (int c = t; c < D / 32; c += 2) tile::store_row_chunk(lane_base + O_COL, c, orow, row < T);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == DIFF_MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int PC, bool NORM>
+int launch_diff_kernel(const CUtensorMap* maps, const float* inv, void* out, int BH, int T, float beta, float p,
+                       float lam, cudaStream_t stream) {
+  using L = DiffLayout<D>;
+  auto kern = tra_diff_kernel<D, PC, NORM>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
+    return ERR_LAUNCH;
+  const int nQ = (T + BT - 1) / BT;
+  const long long grid = static_cast<long long>(nQ) * BH;
+  if (grid > 0x7fffffffLL) return ERR_SHAPE;
+  kern<<<static_cast<unsigned>(grid), DIFF_THREADS, L::ALLOC, stream>>>(
+      maps[0], maps[1], maps[2], maps[3], maps[4], inv, static_cast<__nv_bfloat16*>(out), BH, T, nQ, beta, p, lam);
+  return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
+}
+
+template <int D, bool NORM>
+int dispatch_pc(const CUtensorMap* maps, const float* inv, void* out, int BH, int T, float beta, float p, float lam,
+                cudaStream_t stream) {
+  const int pc = power_class(p);
+  if (pc == POW_TWO) return launch_diff_kernel<D, POW_TWO, NORM>(maps, inv, out, BH, T, beta, p, lam, stream);
+  if (pc == POW_ONE) return launch_diff_kernel<D, POW_ONE, NORM>(maps, inv, out, BH, T, beta, p, lam, stream);
+  return launch_diff_kernel<D, POW_GENERAL, NORM>(maps, inv, out, BH, T, beta, p, lam, stream);
+}
+
+}  // namespace
+
+size_t tra_diff_scratch_bytes(int B, int H, int T) {
+  const size_t Tp = ((static_cast<size_t>(T) + BT - 1) / BT) * BT;
+  return 4 * sizeof(float) * static_cast<size_t>(B) * H * Tp;
+}
+
+int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const void* k2, const void* v, void* out,
+                         int B, int H, int T, int D, float beta, float lam, float p, float* inv_norm,
+                         cudaStream_t stream) {
+  const int BH = B * H;
+  CUtensorMap maps[5];
+  const uint64_t rs = static_cast<uint64_t>(D) * 2, hs = rs * T;
+  const void* src[5] = {q1, q2, k1, k2, v};
+  for (int i = 0; i < 5; ++i) {
+    const int st = encode_tmap_3d(&maps[i], src[i], D, T, BH, rs, hs, 64, BT, 1);
+    if (st != OK) return st;
+  }
+  const bool norm = inv_norm != nullptr;
+  if (norm) {
+    const int Tp = ((T + BT - 1) / BT) * BT;
+    const long long threads = 4LL * BH * Tp * 32;
+    const long long blocks = (threads + 255) / 256;
+    if (blocks > 0x7fffffffLL) return ERR_SHAPE;
+    row_inv_norm_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(q1), static_cast<const __nv_bfloat16*>(k1),
+        static_cast<const __nv_bfloat16*>(q2), static_cast<const __nv_bfloat16*>(k2), inv_norm, BH, T, Tp, D);
+    if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
+  }
+  if (D == 128)
+    return norm ? dispatch_pc<128, true>(maps, inv_norm, out, BH, T, beta, p, lam, stream)
+                : dispatch_pc<128, false>(maps, inv_norm, out, BH, T, beta, p, lam, stream);
+  if (D == 64)
+    return norm ? dispatch_pc<64, true>(maps, inv_norm, out, BH, T, beta, p, lam, stream)
+                : dispatch_pc<64, false>(maps, inv_norm, out, BH, T, beta, p, lam, stream);
+  return ERR_UNSUPPORTED;
+}
+
+unsigned int tra_diff_device_error() { return read_and_clear_device_error(); }
+
+}  // namespace bsa

@@ -13,9 +13,10 @@
  *   framework allocator) on the current device.  Tensors are dense, contiguous
  *   and row-major in the shapes given below; there are no stride arguments.
  *   q, k, v and out start on a 16-byte boundary.
- * - The library allocates no device memory and never synchronises: work is
- *   enqueued on `stream` (0 = legacy default stream) and the call returns
- *   after the launch.  Its only state is a device error word per kernel file,
+ * - The library never synchronises: work is enqueued on `stream` (0 = legacy
+ *   default stream) and the call returns after the launch.  It allocates no
+ *   device memory, except tra_diff_forward with normalize != 0, which takes a
+ *   small temporary through the stream-ordered allocator (documented there).  Its only state is a device error word per kernel file,
  *   written only when a bounded wait times out (see bsa_device_error).  Inputs must stay valid and
  *   unmodified, and outputs untouched by others, until that work completes.
  * - A call returns a bsa_status.  Argument errors are detected on the host
@@ -58,7 +59,9 @@ typedef enum {
                               non-finite beta)                               */
   BSA_ERR_LAUNCH = 5,      /* the CUDA launch failed (cudaGetLastError)       */
   BSA_ERR_DEVICE = 6,      /* no usable sm_100-family device / driver entry   */
-  BSA_ERR_ALIGN = 7        /* a tensor pointer is not 16-byte aligned         */
+  BSA_ERR_ALIGN = 7,       /* a tensor pointer is not 16-byte aligned         */
+  BSA_ERR_MEMORY = 8       /* a temporary scratch buffer could not be
+                              allocated or released (tra_diff_forward)       */
 } bsa_status;
 
 /*
@@ -124,6 +127,39 @@ BSA_API int tra_backward(const void* q, const void* k, const void* v,
                          int dtype, cudaStream_t stream);
 
 /*
+ * tra_diff_forward -- threshold differential attention forward.
+ *
+ * Defined on the page "triton_threshold_attention.py":
+ * differential_threshold_rela_triton.  With n(x) = x / max(||x||_2, 1e-12)
+ * applied row by row when `normalize` is non-zero (identity otherwise):
+ *
+ *   out = TRA(n(q1), n(k1), v) - clamp(lambda, 0, 1) * TRA(n(q2), n(k2), v)
+ *
+ * where TRA is tra_forward's map with the same beta and p.  One fused kernel
+ * runs both score streams on the same query tile, shares each V tile and
+ * accumulates both P.V products into one accumulator.  With normalize, a
+ * pre-pass kernel first computes 1/max(||row||, 1e-12) of every row of q1,
+ * k1, q2, k2 into a temporary of 16 * B * H * Tp bytes (Tp = T rounded up to
+ * a multiple of 128) taken with
+ * cudaMallocAsync on `stream` and returned with cudaFreeAsync on `stream`
+ * (the device's default memory pool); without normalize nothing is
+ * allocated.
+ *
+ *   q1, q2, k1, k2, v, out : [B, H, T, D] bf16 (out may not alias inputs).
+ *   B, H, T, D, beta, p    : as for tra_forward.
+ *   lambda                 : any non-NaN value; clamped to [0, 1].
+ *   dtype                  : BSA_BF16 (BSA_F32 returns BSA_ERR_UNSUPPORTED).
+ *
+ * Errors: as for tra_forward, plus BSA_ERR_MEMORY if the temporary cannot be
+ * allocated or released.
+ */
+BSA_API int tra_diff_forward(const void* q1, const void* q2, const void* k1,
+                             const void* k2, const void* v, void* out,
+                             int B, int H, int T, int D, float beta,
+                             float lambda, float p, int normalize, int dtype,
+                             cudaStream_t stream);
+
+/*
  * nsa_select_forward -- NSA selection-branch attention forward (bf16).
  *
  * Defined on the page "nsa_selection_kernel.py" (openbox-llm): module
@@ -168,8 +204,10 @@ BSA_API int bsa_version(void);
  * Every wait inside the kernels (on a TMA arrival, an MMA completion or a
  * sibling warp) is bounded to about one second; a wait that runs out records
  * code 1 here and the kernel winds down instead of hanging (its outputs are
- * then unspecified).  Returns 0 when no kernel has timed out since the last
- * call, 1 after a timeout, -1 if the words could not be read.  Synchronises
+ * then unspecified); a kernel that finds its shared memory misaligned records
+ * code 2 and does nothing.  Returns 0 when no kernel has failed since the
+ * last call, else the largest code recorded, -1 if the words could not be
+ * read.  Synchronises
  * with the current device (cudaMemcpyFromSymbol); not for the hot path.
  */
 BSA_API int bsa_device_error(void);

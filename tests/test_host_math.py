@@ -2,7 +2,7 @@
 
 * The general-power epilogue of the bf16 TRA kernel evaluates p*log2(x) for
   part of the elements with integer bit operations and a degree-4 polynomial
-  (constants LOG2_C0..LOG2_C4 in ``csrc/tra_bf16.cu``).  Here the same steps
+  (constants LOG2_C0..LOG2_C4 in ``csrc/tra_math.cuh``).  Here the same steps
   are replayed in float32 numpy and checked against numpy's log2 over a wide
   range, including the zero / denormal cases that must flush the weight to 0.
 """
@@ -13,7 +13,7 @@ import re
 import numpy as np
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SRC = os.path.join(ROOT, "block_sparse_attention_tra_gb300", "csrc", "tra_bf16.cu")
+SRC = os.path.join(ROOT, "block_sparse_attention_tra_gb300", "csrc", "tra_math.cuh")
 
 
 def coefficients():
@@ -23,7 +23,7 @@ def coefficients():
 
 
 def p_log2_poly(r, p):
-    """float32 replay of p_log2_poly() in tra_bf16.cu."""
+    """float32 replay of p_log2_poly() in tra_math.cuh."""
     c = coefficients()
     pc = (np.float32(p) * c).astype(np.float32)
     r = np.asarray(r, dtype=np.float32)
