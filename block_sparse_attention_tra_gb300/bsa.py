@@ -27,6 +27,7 @@ _STATUS = {
     6: "BSA_ERR_DEVICE",
     7: "BSA_ERR_ALIGN",
     8: "BSA_ERR_MEMORY",
+    9: "BSA_ERR_SCRATCH_LIMIT",
 }
 
 
@@ -60,6 +61,9 @@ def load_library():
     lib.tra_backward.restype = i32
     lib.tra_diff_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, f32, i32, i32, vp]
     lib.tra_diff_forward.restype = i32
+    lib.tra_diff_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, f32, i32, i32,
+                                             vp]
+    lib.tra_diff_forward_noalloc.restype = i32
     lib.bsa_status_string.argtypes = [i32]
     lib.bsa_status_string.restype = ctypes.c_char_p
     lib.bsa_version.argtypes = []
@@ -100,6 +104,15 @@ def tra_diff_forward_raw(q1, q2, k1, k2, v, out, B, H, T, D, beta, lam, p, norma
     """Direct C call with integer device pointers; returns the bsa_status."""
     return load_library().tra_diff_forward(q1, q2, k1, k2, v, out, B, H, T, D, float(beta), float(lam), float(p),
                                            int(bool(normalize)), int(dtype), stream)
+
+
+def tra_diff_forward_noalloc_raw(q1, q2, k1, k2, v, out, B, H, T, D, beta, lam, p, normalize, dtype,
+                                 stream=0) -> int:
+    """Direct call of the allocation-free differential entry point (for
+    callers that cannot allocate device memory during the call: scratch lives
+    in a fixed library-held device array); returns the bsa_status."""
+    return load_library().tra_diff_forward_noalloc(q1, q2, k1, k2, v, out, B, H, T, D, float(beta), float(lam),
+                                                   float(p), int(bool(normalize)), int(dtype), stream)
 
 
 def nsa_select_forward_raw(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, block_size, S,

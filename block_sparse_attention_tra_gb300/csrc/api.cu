@@ -101,6 +101,26 @@ int tra_backward(const void* q, const void* k, const void* v, const void* dout, 
   return launch_tra_bwd_bf16(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, stream);
 }
 
+// Argument checks of tra_diff_forward_noalloc (the same checks, in the same
+// order, as tra_diff_forward).
+static int check_diff_args(const void* q1, const void* q2, const void* k1, const void* k2, const void* v,
+                           const void* out, int B, int H, int T, int D, float beta, float lambda, float p,
+                           int dtype) {
+  if (q1 == nullptr || q2 == nullptr || k1 == nullptr || k2 == nullptr || v == nullptr || out == nullptr)
+    return BSA_ERR_NULLPTR;
+  if (dtype != BSA_F32 && dtype != BSA_BF16) return BSA_ERR_DTYPE;
+  if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
+  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (dtype != BSA_BF16) return BSA_ERR_UNSUPPORTED;
+  if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f) || isnan(lambda)) return BSA_ERR_UNSUPPORTED;
+  const void* ptrs[6] = {q1, q2, k1, k2, v, out};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return BSA_ERR_ALIGN;
+  return BSA_OK;
+}
+
 int tra_diff_forward(const void* q1, const void* q2, const void* k1, const void* k2, const void* v, void* out, int B,
                      int H, int T, int D, float beta, float lambda, float p, int normalize, int dtype,
                      cudaStream_t stream) {
@@ -127,6 +147,17 @@ int tra_diff_forward(const void* q1, const void* q2, const void* k1, const void*
   const int st = launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, inv, stream);
   if (cudaFreeAsync(inv, stream) != cudaSuccess && st == OK) return BSA_ERR_MEMORY;
   return st;
+}
+
+int tra_diff_forward_noalloc(const void* q1, const void* q2, const void* k1, const void* k2, const void* v,
+                             void* out, int B, int H, int T, int D, float beta, float lambda, float p, int normalize,
+                             int dtype, cudaStream_t stream) {
+  const int chk = check_diff_args(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, dtype);
+  if (chk != BSA_OK) return chk;
+  if (normalize && !tra_diff_noalloc_fits(B, H, T)) return BSA_ERR_SCRATCH_LIMIT;
+  const int dvs = check_device();
+  if (dvs != OK) return dvs;
+  return launch_tra_diff_noalloc_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, normalize != 0, stream);
 }
 
 int nsa_select_forward(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out, float* lse,
@@ -162,6 +193,8 @@ const char* bsa_status_string(int status) {
     case BSA_ERR_DEVICE: return "no usable sm_103 device or CUDA driver entry point";
     case BSA_ERR_ALIGN: return "a tensor pointer is not suitably aligned";
     case BSA_ERR_MEMORY: return "scratch memory could not be allocated or released";
+    case BSA_ERR_SCRATCH_LIMIT:
+      return "the problem needs more scratch than the fixed buffer of the allocation-free entry point holds";
     default: return "unknown bsa_status";
   }
 }

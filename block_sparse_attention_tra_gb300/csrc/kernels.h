@@ -19,6 +19,7 @@ enum Status : int {
   ERR_DEVICE = 6,
   ERR_ALIGN = 7,
   ERR_MEMORY = 8,
+  ERR_SCRATCH_LIMIT = 9,
 };
 
 // Encode a rank-3 bf16 (or other 2-byte) tensor map with 128-byte swizzle.
@@ -47,6 +48,14 @@ size_t tra_diff_scratch_bytes(int B, int H, int T);
 int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const void* k2, const void* v, void* out,
                          int B, int H, int T, int D, float beta, float lam, float p, float* inv_norm,
                          cudaStream_t stream);
+
+// Allocation-free variant: the normalisation factors go to a fixed device
+// array of TRA_DIFF_NOALLOC_MAX_ROWS rows per input (see tra_diff.cu).
+constexpr long long TRA_DIFF_NOALLOC_MAX_ROWS = 1LL << 20;
+bool tra_diff_noalloc_fits(int B, int H, int T);
+int launch_tra_diff_noalloc_bf16(const void* q1, const void* q2, const void* k1, const void* k2, const void* v,
+                                 void* out, int B, int H, int T, int D, float beta, float lam, float p,
+                                 bool normalize, cudaStream_t stream);
 
 // NSA selection attention, bf16 kernel.
 int launch_nsa_select(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out,

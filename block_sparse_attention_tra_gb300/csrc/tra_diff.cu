@@ -23,6 +23,8 @@
 // factors of each key tile (k1 and k2 rows) into a small shared-memory ring
 // of its own (bulk copies), and the epilogue scales each score by
 // r(q_i) r(k_j) before subtracting tau.
+#include <mutex>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc_tile.cuh"
@@ -396,6 +398,50 @@ int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const v
     return norm ? dispatch_pc<64, true>(maps, inv_norm, out, BH, T, beta, p, lam, stream)
                 : dispatch_pc<64, false>(maps, inv_norm, out, BH, T, beta, p, lam, stream);
   return ERR_UNSUPPORTED;
+}
+
+// ------------------------------------------------ allocation-free entry point
+//
+// Fixed scratch for tra_diff_forward_noalloc: the normalisation factors of at
+// most TRA_DIFF_NOALLOC_MAX_ROWS padded (b, h, t) rows of each of q1, k1, q2,
+// k2 (16 MiB of device memory on every GPU that loads the library, held until
+// the process exits).  In host code the name below is only a stand-in for the
+// device symbol; its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) float g_noalloc_inv_norm[4 * TRA_DIFF_NOALLOC_MAX_ROWS];
+
+namespace {
+// Device address of g_noalloc_inv_norm on the current device, looked up once
+// per device (with that device current) and cached.
+int noalloc_scratch(float** out) {
+  constexpr int MAX_DEVICES = 64;
+  static std::mutex mu;
+  static float* cache[MAX_DEVICES] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_inv_norm) != cudaSuccess || ptr == nullptr) return ERR_DEVICE;
+    cache[dev] = static_cast<float*>(ptr);
+  }
+  *out = cache[dev];
+  return OK;
+}
+}  // namespace
+
+bool tra_diff_noalloc_fits(int B, int H, int T) {
+  return tra_diff_scratch_bytes(B, H, T) <= sizeof(float) * 4 * static_cast<size_t>(TRA_DIFF_NOALLOC_MAX_ROWS);
+}
+
+int launch_tra_diff_noalloc_bf16(const void* q1, const void* q2, const void* k1, const void* k2, const void* v,
+                                 void* out, int B, int H, int T, int D, float beta, float lam, float p,
+                                 bool normalize, cudaStream_t stream) {
+  if (!normalize) return launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lam, p, nullptr, stream);
+  if (!tra_diff_noalloc_fits(B, H, T)) return ERR_SCRATCH_LIMIT;
+  float* scratch = nullptr;
+  const int st = noalloc_scratch(&scratch);
+  if (st != OK) return st;
+  return launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lam, p, scratch, stream);
 }
 
 unsigned int tra_diff_device_error() { return read_and_clear_device_error(); }

@@ -60,8 +60,10 @@ typedef enum {
   BSA_ERR_LAUNCH = 5,      /* the CUDA launch failed (cudaGetLastError)       */
   BSA_ERR_DEVICE = 6,      /* no usable sm_100-family device / driver entry   */
   BSA_ERR_ALIGN = 7,       /* a tensor pointer is not 16-byte aligned         */
-  BSA_ERR_MEMORY = 8       /* a temporary scratch buffer could not be
+  BSA_ERR_MEMORY = 8,      /* a temporary scratch buffer could not be
                               allocated or released (tra_diff_forward)       */
+  BSA_ERR_SCRATCH_LIMIT = 9 /* the problem needs more scratch than the fixed
+                              buffer of tra_diff_forward_noalloc holds        */
 } bsa_status;
 
 /*
@@ -158,6 +160,42 @@ BSA_API int tra_diff_forward(const void* q1, const void* q2, const void* k1,
                              int B, int H, int T, int D, float beta,
                              float lambda, float p, int normalize, int dtype,
                              cudaStream_t stream);
+
+/*
+ * tra_diff_forward_noalloc -- tra_diff_forward without any allocation.
+ *
+ * The source pages have no counterpart to this entry point; it exists for
+ * callers that cannot allocate device memory from inside the call: code whose
+ * device memory is owned by its own allocator (a framework that reserves the
+ * GPU up front and accounts for every byte), or code on a latency-critical
+ * path that must not wait on the CUDA allocator.  It computes exactly what
+ * tra_diff_forward computes, with the same arguments, rules and errors, but
+ * the row normalisation factors go to a fixed scratch array that the library
+ * holds in device memory (16 MiB on every GPU that loads the library, until
+ * the process exits) instead of a temporary from cudaMallocAsync.  It calls
+ * no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Limit: with normalize != 0 the problem must satisfy
+ *   B * H * Tp <= 1,048,576   (Tp = T rounded up to a multiple of 128);
+ * larger problems return BSA_ERR_SCRATCH_LIMIT before anything is enqueued.
+ * Without normalize no scratch is used and there is no such limit.
+ *
+ * Set-up: the first call on a device looks up the device address of the
+ * array (cudaGetSymbolAddress, with that device current) and caches it; make
+ * that first call before any stream capture on that device.
+ *
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents.  Each call rewrites every entry it reads before reading it,
+ * so nothing needs clearing, but calls whose work overlaps on the GPU (for
+ * example on two streams at once) race on the array and give undefined
+ * results: serialise them.
+ */
+BSA_API int tra_diff_forward_noalloc(const void* q1, const void* q2,
+                                     const void* k1, const void* k2,
+                                     const void* v, void* out, int B, int H,
+                                     int T, int D, float beta, float lambda,
+                                     float p, int normalize, int dtype,
+                                     cudaStream_t stream);
 
 /*
  * nsa_select_forward -- NSA selection-branch attention forward (bf16).
