@@ -367,6 +367,28 @@ def run_ours(args):
                      "tflops": round(w2.flops * world / (t * 1e-3) / 1e12, 3),
                      "roofline": roofline_for(w2, t, pk, sustained=False), "l2": "flushed between launches"}
             sec.append(entry)
+        # The widened rows on the headline shape: training backward and the
+        # fused differential forward (two score streams, with normalisation).
+        del dev, out
+        torch.cuda.empty_cache()
+        wb = workloads.TRA_WORKLOADS[DEFAULT_WORKLOAD]
+        qb, kb, vb = (t.to(device) for t in workloads.workload_inputs(wb))
+        gen = torch.Generator(device="cpu").manual_seed(1)
+        dob = torch.randn(qb.shape, generator=gen).to(torch.bfloat16).to(device)
+        q2b = torch.randn(qb.shape, generator=gen).to(torch.bfloat16).to(device)
+        k2b = torch.randn(qb.shape, generator=gen).to(torch.bfloat16).to(device)
+        n = max(3, args.steps // 2)
+        extra = [
+            ("tra_backward", lambda: bsa.tra_backward(qb, kb, vb, dob, wb.beta, wb.p), 10 * wb.flops // 4),
+            ("tra_diff_forward(normalize=1, lambda=0.5)",
+             lambda: bsa.tra_diff_forward(qb, q2b, kb, k2b, vb, wb.beta, 0.5, wb.p, normalize=True), 2 * wb.flops),
+        ]
+        for label, f, flops in extra:
+            t = reduce_max(time_resident(f, n, 3, world, flush=flush), world, device) / n
+            sec.append({"workload": f"{label} on {wb.name}", "ms_per_launch": round(t, 4),
+                        "tflops": round(flops * world / (t * 1e-3) / 1e12, 3),
+                        "frac_of_bf16_peak": round(flops / (t * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
+                        "algorithmic_flops": flops, "l2": "flushed between launches"})
         result["secondary"] = sec
 
     if args.cpu_baseline and rank == 0 and world == 1:
@@ -466,6 +488,43 @@ def run_reference(args):
     }
 
 
+def run_op(args):
+    """Time one of the widened ops (TRA backward, fused differential forward)
+    on a TRA workload; prints a JSON line of the same metric.  Used for the
+    per-kernel measurements and ncu captures of those rows."""
+    import torch
+
+    from block_sparse_attention_tra_gb300 import bsa, build, workloads
+
+    torch.cuda.set_device(0)
+    build.build()
+    bsa.load_library()
+    pk = peaks()
+    w = workloads.TRA_WORKLOADS[args.workload]
+    q, k, v = (t.cuda() for t in workloads.workload_inputs(w))
+    gen = torch.Generator().manual_seed(1)
+    extra = [torch.randn(q.shape, generator=gen).to(torch.bfloat16).cuda() for _ in range(2)]
+    if args.op == "backward":
+        fn = lambda: bsa.tra_backward(q, k, v, extra[0], w.beta, w.p)  # noqa: E731
+        flops = 10 * w.flops // 4
+        launches = 2
+    else:
+        fn = lambda: bsa.tra_diff_forward(q, extra[0], k, extra[1], v, w.beta, 0.5, w.p, normalize=True)  # noqa: E731
+        flops = 2 * w.flops
+        launches = 2
+    with ClockSampler(0) as cs:
+        total = time_resident(fn, args.steps, args.warmup, 1, soak_s=args.clock_soak)
+    ms = total / args.steps
+    value = flops / (ms * 1e-3) / 1e12
+    return {"metric": METRIC, "op": args.op, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic", "config": workload_config(w, 1),
+            "roofline": {"bound": "tensor", "achieved": round(value, 2), "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(value / pk["bf16_tflops"], 4),
+                         "algorithmic_flops_per_step": flops},
+            "gpu_launches": launches * args.steps, "clocks": cs.summary()}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -473,6 +532,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--op", choices=["forward", "backward", "diff"], default="forward",
+                    help="forward (the headline path), or one widened op timed on its own")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -480,7 +541,12 @@ def main(argv=None):
                     help="seconds of untimed launches after the timed region, under the clock sampler")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
-    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.impl == "reference":
+        res = run_reference(args)
+    elif args.op != "forward":
+        res = run_op(args)
+    else:
+        res = run_ours(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 

@@ -4,6 +4,8 @@
 // returns an error without touching the device.
 #include <math.h>
 
+#include <mutex>
+
 #include "../../include/bsa.h"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -29,6 +31,30 @@ EncodeTiledFn encode_fn() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The library's own stream-ordered memory pool on `dev`, created on first use.
+// Its release threshold keeps freed temporaries mapped, so repeated calls
+// recycle the same memory instead of mapping it again each time; the
+// caller's default pool is left untouched.
+cudaMemPool_t scratch_pool(int dev) {
+  constexpr int MAX_DEVICES = 64;
+  static std::mutex mu;
+  static cudaMemPool_t pools[MAX_DEVICES] = {};
+  if (dev < 0 || dev >= MAX_DEVICES) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (pools[dev] == nullptr) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = 1ull << 30;  // keep up to 1 GiB of freed temporaries mapped
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    pools[dev] = pool;
+  }
+  return pools[dev];
+}
 
 // The kernels are built for sm_103a only; refuse other devices up front
 // instead of failing inside the launch.
@@ -143,7 +169,11 @@ int tra_diff_forward(const void* q1, const void* q2, const void* k1, const void*
   // multiple of 128): a stream-ordered temporary, released on the same stream.
   float* inv = nullptr;
   const size_t bytes = tra_diff_scratch_bytes(B, H, T);
-  if (cudaMallocAsync(reinterpret_cast<void**>(&inv), bytes, stream) != cudaSuccess) return BSA_ERR_MEMORY;
+  int dev = 0;
+  cudaMemPool_t pool = cudaGetDevice(&dev) == cudaSuccess ? scratch_pool(dev) : nullptr;
+  if (pool == nullptr) return BSA_ERR_MEMORY;
+  if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&inv), bytes, pool, stream) != cudaSuccess)
+    return BSA_ERR_MEMORY;
   const int st = launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, inv, stream);
   if (cudaFreeAsync(inv, stream) != cudaSuccess && st == OK) return BSA_ERR_MEMORY;
   return st;

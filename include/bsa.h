@@ -142,10 +142,11 @@ BSA_API int tra_backward(const void* q, const void* k, const void* v,
  * accumulates both P.V products into one accumulator.  With normalize, a
  * pre-pass kernel first computes 1/max(||row||, 1e-12) of every row of q1,
  * k1, q2, k2 into a temporary of 16 * B * H * Tp bytes (Tp = T rounded up to
- * a multiple of 128) taken with
- * cudaMallocAsync on `stream` and returned with cudaFreeAsync on `stream`
- * (the device's default memory pool); without normalize nothing is
- * allocated.
+ * a multiple of 128) taken with cudaMallocFromPoolAsync on `stream` and
+ * returned with cudaFreeAsync on `stream`, from a memory pool the library
+ * creates on the device at first use (it keeps up to 1 GiB of freed
+ * temporaries mapped; the caller's default pool is not touched); without
+ * normalize nothing is allocated.
  *
  *   q1, q2, k1, k2, v, out : [B, H, T, D] bf16 (out may not alias inputs).
  *   B, H, T, D, beta, p    : as for tra_forward.
@@ -172,7 +173,7 @@ BSA_API int tra_diff_forward(const void* q1, const void* q2, const void* k1,
  * tra_diff_forward computes, with the same arguments, rules and errors, but
  * the row normalisation factors go to a fixed scratch array that the library
  * holds in device memory (16 MiB on every GPU that loads the library, until
- * the process exits) instead of a temporary from cudaMallocAsync.  It calls
+ * the process exits) instead of a temporary from a memory pool.  It calls
  * no cudaMalloc, cudaFree or other allocating routine.
  *
  * Limit: with normalize != 0 the problem must satisfy
