@@ -9,6 +9,9 @@ path computes, written in float64 numpy from the source pages:
 * ``oracle.nsa``   -- NSA selection-branch attention, from the page
   "nsa_selection_kernel.py" (module docstring "The operation" and the
   ground-truth function ``selection_forward_reference``).
+* ``oracle.fsa``   -- the same NSA selection forward in the page's block-outer
+  split-K form (per-(query, block) softmax partials and a log-sum-exp
+  combine), from the page's FSA forward section.
 * ``oracle.brute`` -- scalar pure-Python loops of both, for tiny inputs only.
 
 It is test infrastructure.  Only ``tests/``, ``__graft_entry__.smoke()`` and
@@ -22,6 +25,6 @@ closed forms, hand-worked fixtures, textbook/library special cases and
 invariants (``tests/test_oracle.py``); none is "parity unpinned".
 """
 
-from . import brute, nsa, tra  # noqa: F401
+from . import brute, fsa, nsa, tra  # noqa: F401
 
-__all__ = ["tra", "nsa", "brute"]
+__all__ = ["tra", "nsa", "fsa", "brute"]

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import brute, nsa, tra
+from oracle import brute, fsa, nsa, tra
 from block_sparse_attention_tra_gb300 import workloads
 
 
@@ -612,3 +612,133 @@ def test_tra_diff_normalised_scores_are_cosines():
 
     want = max(cos(q1[0, 0, 0], k1[0, 0, 0]), 0) * v[0, 0, 0] - 0.25 * max(cos(q2[0, 0, 0], k2[0, 0, 0]), 0) * v[0, 0, 0]
     np.testing.assert_allclose(out[0, 0, 0], want, rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------- NSA block-outer (FSA) split-K form
+
+def _fsa_handworked_inputs(golden):
+    rows = golden("nsa_uniform_handworked.txt")
+    T, D, bs = 8, 4, 2
+    q = np.zeros((1, 2, T, D))
+    k = rng(9).standard_normal((1, 1, T, D))
+    v = np.array([[j, 2 * j, -j, 1] for j in range(T)], dtype=np.float64).reshape(1, 1, T, D)
+    idx = np.array([[int(r[1]), int(r[2])] for r in rows]).reshape(1, 1, T, 2)
+    return q, k, v, idx, bs
+
+
+def test_fsa_partials_handworked_fixture(golden):
+    q, k, v, idx, bs = _fsa_handworked_inputs(golden)
+    want = {(int(r[0]), int(r[1])): (float(r[2]), [float(x) for x in r[3:7]])
+            for r in golden("fsa_partials_handworked.txt")}
+    parts = fsa.fsa_partials(q, k, v, idx, bs)
+    assert {(i, j) for (_, _, i, j) in parts} == set(want)
+    for (b, h, i, j), (m, l, acc) in parts.items():
+        n, a = want[(i, j)]
+        np.testing.assert_array_equal(m, 0.0)
+        np.testing.assert_allclose(l, n, rtol=0, atol=1e-15)
+        for g in range(2):
+            np.testing.assert_allclose(acc[g], a, rtol=0, atol=1e-14)
+    lists = fsa.block_query_lists(idx, bs)
+    assert lists[(0, 0, 1)] == [(2, 0), (3, 0), (7, 1)]  # i=3 lists block 1 twice: first slot
+    out, lse = fsa.nsa_select_forward_fsa(q, k, v, idx, bs)
+    for r in golden("nsa_uniform_handworked.txt"):
+        i, n = int(r[0]), int(r[7])
+        np.testing.assert_allclose(out[0, :, i], np.broadcast_to([float(x) for x in r[3:7]], (2, 4)), atol=1e-14)
+        assert np.all(lse[0, :, i] == pytest.approx(-1e9 if n == 0 else math.log(n), abs=1e-14))
+
+
+def test_fsa_single_token_partial_is_the_key():
+    """The pair (i = j*bs, block j) sees one token: m = its score, l = 1, acc = its v."""
+    B, Hq, Hkv, T, D, bs = 1, 4, 2, 32, 8, 8
+    q, k, v = rand_nsa(B, Hq, Hkv, T, D, seed=31)
+    idx = -np.ones((B, Hkv, T, 1), dtype=np.int64)
+    idx[..., 0] = (np.arange(T) // bs)[None, None, :]
+    parts = fsa.fsa_partials(q, k, v, idx, bs)
+    for (b, h, i, j), (m, l, acc) in parts.items():
+        if i % bs:
+            continue
+        for g in range(2):
+            np.testing.assert_allclose(m[g], q[b, 2 * h + g, i] @ k[b, h, i] / math.sqrt(D), rtol=1e-13)
+            np.testing.assert_allclose(acc[g], v[b, h, i], rtol=1e-13)
+        np.testing.assert_allclose(l, 1.0, rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("G,D,bs,S", [(1, 8, 4, 3), (2, 6, 8, 4), (4, 8, 6, 5)])
+def test_fsa_equals_query_outer_oracle(G, D, bs, S):
+    """The split-K partials + log-sum-exp combine equal one softmax over the
+    union of the selected causal tokens (query-outer oracle), including
+    padding, duplicates, future-only rows and empty rows."""
+    B, Hkv, T = 2, 2, 6 * bs
+    q, k, v = rand_nsa(B, Hkv * G, Hkv, T, D, seed=40 + G)
+    g = torch.Generator().manual_seed(7 + G)
+    idx = workloads.selection_indices(B, Hkv, T, bs, S, g).numpy().astype(np.int64)
+    idx[0, 1, 3:7, 1] = idx[0, 1, 3:7, 0]  # duplicates
+    idx[1, 0, bs:2 * bs, :] = -1  # empty rows
+    idx[1, 1, 2, 0] = 5  # a wholly future block next to valid ones
+    idx[1, 1, 3, :] = -1
+    idx[1, 1, 3, 0] = 4  # future-only row
+    out, lse = fsa.nsa_select_forward_fsa(q, k, v, idx, bs)
+    ref, ref_lse = nsa.nsa_select_forward(q, k, v, idx, bs)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-12)
+    dense = nsa.nsa_select_dense(q, k, v, idx, bs)
+    np.testing.assert_allclose(out, dense, rtol=1e-10, atol=1e-12)
+
+
+def test_fsa_combine_is_shift_invariant():
+    """Adding a constant to one pair's local max and scaling its l and acc by
+    exp(-constant) describes the same softmax: the combine must not change."""
+    B, Hq, Hkv, T, D, bs, S = 1, 2, 1, 32, 8, 8, 3
+    q, k, v = rand_nsa(B, Hq, Hkv, T, D, seed=33)
+    g = torch.Generator().manual_seed(8)
+    idx = workloads.selection_indices(B, Hkv, T, bs, S, g).numpy()
+    parts = fsa.fsa_partials(q, k, v, idx, bs)
+    rows = {}
+    for (b, h, i, j), p in parts.items():
+        rows.setdefault((b, h, i), []).append(p)
+    for (b, h, i), ps in rows.items():
+        def combine(ps):
+            m = np.stack([p[0] for p in ps])
+            w = np.exp(m - m.max(axis=0))
+            L = (w * np.stack([p[1] for p in ps])).sum(axis=0)
+            return (w[:, :, None] * np.stack([p[2] for p in ps])).sum(axis=0) / L[:, None]
+        c = 3.25
+        shifted = [(ps[0][0] + c, ps[0][1] * math.exp(-c), ps[0][2] * math.exp(-c))] + ps[1:]
+        np.testing.assert_allclose(combine(shifted), combine(ps), rtol=1e-12, atol=1e-14)
+
+
+def test_planted_fsa_mistakes_are_caught(golden, monkeypatch):
+    good = fsa.fsa_partials
+
+    def pins():
+        try:
+            test_fsa_partials_handworked_fixture(golden)
+            test_fsa_equals_query_outer_oracle(2, 6, 8, 4)
+        except AssertionError:
+            return False
+        return True
+
+    assert pins()
+
+    def no_causal(q, k, v, block_idx, block_size):
+        q, k, v, idx = nsa._check(q, k, v, block_idx, block_size)
+        G = q.shape[1] // k.shape[1]
+        scale = q.shape[-1] ** -0.5
+        parts = {}
+        for (b, h, j), pairs in fsa.block_query_lists(idx, block_size).items():
+            toks = np.arange(j * block_size, (j + 1) * block_size)
+            for i, _ in pairs:
+                sc = (q[b, h * G:(h + 1) * G, i] @ k[b, h, toks].T) * scale
+                m = sc.max(axis=1)
+                p = np.exp(sc - m[:, None])
+                parts[(b, h, i, j)] = (m, p.sum(axis=1), p @ v[b, h, toks])
+        return parts
+
+    def unshifted_l(*a):
+        return {key: (m, l * np.exp(m), acc) for key, (m, l, acc) in good(*a).items()}
+
+    for bad in (no_causal, unshifted_l):
+        monkeypatch.setattr(fsa, "fsa_partials", bad)
+        assert not pins(), bad.__name__
+    monkeypatch.setattr(fsa, "fsa_partials", good)
+    assert pins()
