@@ -42,6 +42,7 @@ KERNEL_SOURCES = {
     "tra": "block_sparse_attention_tra_gb300/csrc/tra_bf16.cu",
     "tra_f32": "block_sparse_attention_tra_gb300/csrc/tra_f32.cu",
     "nsa": "block_sparse_attention_tra_gb300/csrc/nsa_select.cu",
+    "fsa": "block_sparse_attention_tra_gb300/csrc/nsa_fsa.cu",
 }
 
 
@@ -196,7 +197,7 @@ def workload_config(w, world):
             "l2": "no flush (unique K/V stays in L2 by design; gathered bytes counted)", "parallelism": par}
 
 
-def roofline_for(w, ms_per_launch, pk, sustained: bool):
+def roofline_for(w, ms_per_launch, pk, sustained: bool, fsa: bool = False):
     from block_sparse_attention_tra_gb300 import workloads
 
     if isinstance(w, workloads.TraWorkload):
@@ -210,12 +211,19 @@ def roofline_for(w, ms_per_launch, pk, sustained: bool):
                 "traffic": ncu_traffic("tra", w.name), "kernel": "tra_bf16_tcgen05_kernel",
                 "algorithmic_flops_per_launch": w.flops}
     achieved = w.algorithmic_bytes / (ms_per_launch * 1e-3) / 1e9
-    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": round(achieved / pk["hbm_gbs"], 4), "peak_kind": "copy bandwidth of " + pk["source"],
-            "traffic": ncu_traffic("nsa", w.name), "kernel": "nsa_select_kernel",
-            "algorithmic_bytes_per_launch": w.algorithmic_bytes,
-            "tflops": round(w.flops / (ms_per_launch * 1e-3) / 1e12, 2),
-            "unique_bytes_per_launch": w.unique_bytes}
+    r = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+         "frac": round(achieved / pk["hbm_gbs"], 4), "peak_kind": "copy bandwidth of " + pk["source"],
+         "traffic": ncu_traffic("fsa" if fsa else "nsa", ("fsa:" if fsa else "") + w.name),
+         "kernel": "fsa_blockouter_kernel + fsa_combine_kernel" if fsa else "nsa_select_kernel",
+         "algorithmic_bytes_per_launch": w.algorithmic_bytes,
+         "tflops": round(w.flops / (ms_per_launch * 1e-3) / 1e12, 2),
+         "unique_bytes_per_launch": w.unique_bytes}
+    if fsa:
+        # The split-K form also writes and re-reads its fp32 partials
+        # (m, l and a D-vector per (query, selected block, head)).
+        parts = w.B * w.Hq * w.T * w.S * (w.D + 2) * 4
+        r["partial_bytes_written_and_read"] = 2 * parts
+    return r
 
 
 def time_resident(fn, steps, warmup, world, flush=None, soak_s=0.0):
@@ -367,6 +375,21 @@ def run_ours(args):
                      "tflops": round(w2.flops * world / (t * 1e-3) / 1e12, 3),
                      "roofline": roofline_for(w2, t, pk, sustained=False), "l2": "flushed between launches"}
             sec.append(entry)
+            if isinstance(w2, workloads.NsaWorkload):
+                # The same selection through the block-outer split-K form
+                # (six launches: list build, block pass, combine).
+                q2, k2, v2, idx2 = dev
+                ws = torch.empty(bsa.nsa_select_fsa_workspace_size(w2.B, w2.Hq, w2.Hkv, w2.T, w2.D,
+                                                                   w2.block_size, w2.S),
+                                 dtype=torch.uint8, device=device)
+                f = lambda: bsa.nsa_select_forward_fsa(q2, k2, v2, idx2, w2.block_size, out=out,  # noqa: E731
+                                                       lse=lse, workspace=ws)
+                t = reduce_max(time_resident(f, n, 3, world, flush=flush), world, device) / n
+                sec.append({"workload": f"nsa_select_forward_fsa on {w2.name}", "ms_per_launch": round(t, 4),
+                            "tflops": round(w2.flops * world / (t * 1e-3) / 1e12, 3),
+                            "roofline": roofline_for(w2, t, pk, sustained=False, fsa=True),
+                            "gpu_launches_per_call": 6, "l2": "flushed between launches"})
+                del ws, q2, k2, v2, idx2, f
         # The widened rows on the headline shape: training backward and the
         # fused differential forward (two score streams, with normalisation).
         del dev, out
@@ -489,8 +512,9 @@ def run_reference(args):
 
 
 def run_op(args):
-    """Time one of the widened ops (TRA backward, fused differential forward)
-    on a TRA workload; prints a JSON line of the same metric.  Used for the
+    """Time one of the widened ops (TRA backward or the fused differential
+    forward on a TRA workload; the block-outer split-K NSA form on an NSA
+    workload); prints a JSON line of the same metric.  Used for the
     per-kernel measurements and ncu captures of those rows."""
     import torch
 
@@ -500,6 +524,24 @@ def run_op(args):
     build.build()
     bsa.load_library()
     pk = peaks()
+    if args.op == "fsa":
+        w = workloads.NSA_WORKLOADS[args.workload]
+        q, k, v, idx = (t.cuda() for t in workloads.workload_inputs(w))
+        out = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, w.T), dtype=torch.float32, device=q.device)
+        ws = torch.empty(bsa.nsa_select_fsa_workspace_size(w.B, w.Hq, w.Hkv, w.T, w.D, w.block_size, w.S),
+                         dtype=torch.uint8, device=q.device)
+        fn = lambda: bsa.nsa_select_forward_fsa(q, k, v, idx, w.block_size, out=out, lse=lse,  # noqa: E731
+                                                workspace=ws)
+        with ClockSampler(0) as cs:
+            total = time_resident(fn, args.steps, args.warmup, 1, soak_s=args.clock_soak)
+        ms = total / args.steps
+        value = w.flops / (ms * 1e-3) / 1e12
+        return {"metric": METRIC, "op": args.op, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+                "higher_is_better": True, "dtype": "bf16", "data": "synthetic", "config": workload_config(w, 1),
+                "roofline": roofline_for(w, ms, pk, sustained=False, fsa=True),
+                "gpu_launches": 6 * args.steps, "clocks": cs.summary()}
     w = workloads.TRA_WORKLOADS[args.workload]
     q, k, v = (t.cuda() for t in workloads.workload_inputs(w))
     gen = torch.Generator().manual_seed(1)
@@ -532,7 +574,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--op", choices=["forward", "backward", "diff"], default="forward",
+    ap.add_argument("--op", choices=["forward", "backward", "diff", "fsa"], default="forward",
                     help="forward (the headline path), or one widened op timed on its own")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")

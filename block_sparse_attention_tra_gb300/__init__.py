@@ -8,6 +8,9 @@ kernel for sm_103a behind a C ABI (``include/bsa.h``, ``libbsa.so``):
   causal and unnormalised (page "triton_threshold_attention.py").
 * ``nsa_select_forward`` -- NSA selection-branch attention over gathered key
   blocks, GQA, causal, scaled softmax (page "nsa_selection_kernel.py").
+* ``nsa_select_forward_fsa`` -- the same result in the page's block-outer
+  split-K form: each selected block's K/V read once, per-pair softmax
+  partials, a log-sum-exp combine.
 
 The binding in ``bsa`` only marshals arguments; every step runs in the CUDA
 library, which is loaded on first use and must be built (``build.build()``).
@@ -19,7 +22,10 @@ from .bsa import (  # noqa: F401
     library_path,
     load_library,
     nsa_select_forward,
+    nsa_select_forward_fsa,
+    nsa_select_forward_fsa_raw,
     nsa_select_forward_raw,
+    nsa_select_fsa_workspace_size,
     status_string,
     tra_backward,
     tra_backward_raw,
@@ -42,5 +48,8 @@ __all__ = [
     "tra_diff_forward_raw",
     "nsa_select_forward",
     "nsa_select_forward_raw",
+    "nsa_select_forward_fsa",
+    "nsa_select_forward_fsa_raw",
+    "nsa_select_fsa_workspace_size",
     "status_string",
 ]

@@ -64,6 +64,11 @@ def load_library():
     lib.tra_diff_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, f32, i32, i32,
                                              vp]
     lib.tra_diff_forward_noalloc.restype = i32
+    lib.nsa_select_fsa_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.nsa_select_fsa_workspace_size.restype = ctypes.c_size_t
+    lib.nsa_select_forward_fsa.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp,
+                                           ctypes.c_size_t, vp]
+    lib.nsa_select_forward_fsa.restype = i32
     lib.bsa_status_string.argtypes = [i32]
     lib.bsa_status_string.restype = ctypes.c_char_p
     lib.bsa_version.argtypes = []
@@ -120,6 +125,18 @@ def nsa_select_forward_raw(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, block
     """Direct C call with integer device pointers; returns the bsa_status."""
     return load_library().nsa_select_forward(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D,
                                              block_size, S, stream)
+
+
+def nsa_select_fsa_workspace_size(B, Hq, Hkv, T, D, block_size, S) -> int:
+    """Bytes of workspace ``nsa_select_forward_fsa`` needs (0 = sizes not accepted)."""
+    return int(load_library().nsa_select_fsa_workspace_size(B, Hq, Hkv, T, D, block_size, S))
+
+
+def nsa_select_forward_fsa_raw(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, block_size, S, workspace,
+                               workspace_bytes, stream=0) -> int:
+    """Direct C call with integer device pointers; returns the bsa_status."""
+    return load_library().nsa_select_forward_fsa(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, block_size, S,
+                                                 workspace, int(workspace_bytes), stream)
 
 
 def _stream_handle(stream):
@@ -241,4 +258,40 @@ def nsa_select_forward(q, k, v, block_idx, block_size: int = 64, out=None, lse=N
                                 out.data_ptr(), lse.data_ptr() if lse is not None else None,
                                 B, Hq, Hkv, T, D, block_size, S, _stream_handle(stream))
     _check(st, "nsa_select_forward")
+    return (out, lse) if return_lse else out
+
+
+def nsa_select_forward_fsa(q, k, v, block_idx, block_size: int = 64, out=None, lse=None,
+                           return_lse: bool = False, workspace=None, stream=None):
+    """NSA selection forward in the block-outer split-K form (same arguments
+    and result as ``nsa_select_forward``).  ``workspace`` is a uint8 CUDA
+    tensor of at least ``nsa_select_fsa_workspace_size(...)`` bytes; one is
+    allocated when it is None.  It stays in use until the stream's work is
+    done."""
+    import torch
+
+    if q.device.type != "cuda":
+        raise BsaError("nsa_select_forward_fsa takes CUDA tensors (no CPU path)")
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or block_idx.dim() != 4:
+        raise BsaError("q [B,Hq,T,D], k/v [B,Hkv,T,D], block_idx [B,Hkv,T,S] expected", 2)
+    if not (q.dtype == k.dtype == v.dtype == torch.bfloat16):
+        raise BsaError("nsa_select_forward_fsa takes bfloat16 q, k, v", 3)
+    B, Hq, T, D = q.shape
+    Hkv = k.shape[1]
+    S = block_idx.shape[-1]
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    idx = block_idx.to(torch.int32).contiguous()
+    need = nsa_select_fsa_workspace_size(B, Hq, Hkv, T, D, block_size, S)
+    if need == 0:
+        raise BsaError("nsa_select_forward_fsa: sizes not accepted", 2)
+    if workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, T), device=q.device, dtype=torch.float32)
+    st = nsa_select_forward_fsa_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), idx.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr() if lse is not None else None, B, Hq, Hkv, T, D, block_size, S,
+                                    workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    _check(st, "nsa_select_forward_fsa")
     return (out, lse) if return_lse else out

@@ -56,6 +56,33 @@ cudaMemPool_t scratch_pool(int dev) {
   return pools[dev];
 }
 
+// Sizes and parameters of the NSA selection entry points (pointers aside).
+int check_nsa_shape(int B, int Hq, int Hkv, int T, int D, int block_size, int S) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || D < 1 || block_size < 1 || S < 1) return BSA_ERR_SHAPE;
+  if (Hq % Hkv != 0) return BSA_ERR_SHAPE;
+  if (T % block_size != 0) return BSA_ERR_SHAPE;
+  if (S > 32) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * Hq * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * Hq > 0x7fffffffLL || static_cast<long long>(B) * Hkv * T * S >= (1LL << 40))
+    return BSA_ERR_SHAPE;
+  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (block_size != 64) return BSA_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16) return BSA_ERR_UNSUPPORTED;
+  return BSA_OK;
+}
+
+int check_nsa_args(const void* q, const void* k, const void* v, const int32_t* block_idx, const void* out,
+                   const float* lse, int B, int Hq, int Hkv, int T, int D, int block_size, int S) {
+  if (q == nullptr || k == nullptr || v == nullptr || block_idx == nullptr || out == nullptr)
+    return BSA_ERR_NULLPTR;
+  const int sh = check_nsa_shape(B, Hq, Hkv, T, D, block_size, S);
+  if (sh != BSA_OK) return sh;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_idx) & 3u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return BSA_ERR_ALIGN;
+  return BSA_OK;
+}
+
 // The kernels are built for sm_103a only; refuse other devices up front
 // instead of failing inside the launch.
 int check_device() {
@@ -192,24 +219,33 @@ int tra_diff_forward_noalloc(const void* q1, const void* q2, const void* k1, con
 
 int nsa_select_forward(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out, float* lse,
                        int B, int Hq, int Hkv, int T, int D, int block_size, int S, cudaStream_t stream) {
-  if (q == nullptr || k == nullptr || v == nullptr || block_idx == nullptr || out == nullptr)
-    return BSA_ERR_NULLPTR;
-  if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || D < 1 || block_size < 1 || S < 1) return BSA_ERR_SHAPE;
-  if (Hq % Hkv != 0) return BSA_ERR_SHAPE;
-  if (T % block_size != 0) return BSA_ERR_SHAPE;
-  if (S > 32) return BSA_ERR_SHAPE;
-  if (static_cast<long long>(B) * Hq * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
-  if (static_cast<long long>(B) * Hq > 0x7fffffffLL || static_cast<long long>(B) * Hkv * T * S >= (1LL << 40))
-    return BSA_ERR_SHAPE;
-  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
-  if (block_size != 64) return BSA_ERR_UNSUPPORTED;
-  if (Hq / Hkv > 16) return BSA_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(block_idx) & 3u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
-    return BSA_ERR_ALIGN;
+  const int chk = check_nsa_args(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, block_size, S);
+  if (chk != BSA_OK) return chk;
   const int dv = check_device();
   if (dv != OK) return dv;
   return launch_nsa_select(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, block_size, S, stream);
+}
+
+size_t nsa_select_fsa_workspace_size(int B, int Hq, int Hkv, int T, int D, int block_size, int S) {
+  if (check_nsa_shape(B, Hq, Hkv, T, D, block_size, S) != BSA_OK) return 0;
+  // The partial rows are indexed with 32-bit integers inside the kernels.
+  if (static_cast<long long>(B) * Hq * T * S >= (1LL << 31)) return 0;
+  return nsa_fsa_workspace_bytes(B, Hq, Hkv, T, D, S);
+}
+
+int nsa_select_forward_fsa(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out,
+                           float* lse, int B, int Hq, int Hkv, int T, int D, int block_size, int S, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  const int chk = check_nsa_args(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, block_size, S);
+  if (chk != BSA_OK) return chk;
+  if (workspace == nullptr) return BSA_ERR_NULLPTR;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BSA_ERR_ALIGN;
+  const size_t need = nsa_select_fsa_workspace_size(B, Hq, Hkv, T, D, block_size, S);
+  if (need == 0) return BSA_ERR_SHAPE;
+  if (workspace_bytes < need) return BSA_ERR_SCRATCH_LIMIT;
+  const int dv = check_device();
+  if (dv != OK) return dv;
+  return launch_nsa_fsa(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, S, workspace, stream);
 }
 
 const char* bsa_status_string(int status) {
@@ -224,7 +260,7 @@ const char* bsa_status_string(int status) {
     case BSA_ERR_ALIGN: return "a tensor pointer is not suitably aligned";
     case BSA_ERR_MEMORY: return "scratch memory could not be allocated or released";
     case BSA_ERR_SCRATCH_LIMIT:
-      return "the problem needs more scratch than the fixed buffer of the allocation-free entry point holds";
+      return "the problem needs more scratch than the fixed buffer or the caller's workspace holds";
     default: return "unknown bsa_status";
   }
 }
@@ -232,8 +268,8 @@ const char* bsa_status_string(int status) {
 int bsa_version(void) { return 100; }
 
 int bsa_device_error(void) {
-  const unsigned codes[5] = {tra_bf16_device_error(), tra_f32_device_error(), nsa_device_error(),
-                             tra_bwd_device_error(), tra_diff_device_error()};
+  const unsigned codes[6] = {tra_bf16_device_error(), tra_f32_device_error(), nsa_device_error(),
+                             tra_bwd_device_error(), tra_diff_device_error(), nsa_fsa_device_error()};
   unsigned worst = 0;
   for (unsigned c : codes) {
     if (c == 0xffffffffu) return -1;

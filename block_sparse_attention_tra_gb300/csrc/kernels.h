@@ -62,6 +62,13 @@ int launch_nsa_select(const void* q, const void* k, const void* v, const int32_t
                       float* lse, int B, int Hq, int Hkv, int T, int D, int block_size, int S,
                       cudaStream_t stream);
 
+// NSA selection attention, block-outer split-K form with a log-sum-exp
+// combine (nsa_fsa.cu).  `workspace` holds nsa_fsa_workspace_bytes(...) bytes,
+// 256-byte aligned; block_size is 64.
+size_t nsa_fsa_workspace_bytes(int B, int Hq, int Hkv, int T, int D, int S);
+int launch_nsa_fsa(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out, float* lse,
+                   int B, int Hq, int Hkv, int T, int D, int S, void* workspace, cudaStream_t stream);
+
 // Read-and-clear of each kernel file's device error word (0 = none,
 // 1 = a bounded wait timed out; 0xffffffff = the read itself failed).
 unsigned int tra_bf16_device_error();
@@ -69,6 +76,7 @@ unsigned int tra_f32_device_error();
 unsigned int nsa_device_error();
 unsigned int tra_bwd_device_error();
 unsigned int tra_diff_device_error();
+unsigned int nsa_fsa_device_error();
 
 // Power class of the TRA epilogue: p == 1, p == 2, or the general exp2/log2 path.
 enum PowerClass : int { POW_GENERAL = 0, POW_ONE = 1, POW_TWO = 2 };

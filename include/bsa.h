@@ -7,6 +7,10 @@
  *   tra_forward         threshold rectified attention (TRA)
  *   nsa_select_forward  NSA selection-branch attention
  *
+ * plus the TRA backward, the differential TRA and the NSA selection forward
+ * in the page's block-outer split-K form (nsa_select_forward_fsa, which works
+ * in a caller-provided workspace).
+ *
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Every tensor pointer is caller-owned DEVICE memory (cudaMalloc or a
@@ -230,6 +234,58 @@ BSA_API int nsa_select_forward(const void* q, const void* k, const void* v,
                                const int32_t* block_idx, void* out, float* lse,
                                int B, int Hq, int Hkv, int T, int D,
                                int block_size, int S, cudaStream_t stream);
+
+/*
+ * nsa_select_forward_fsa -- the same NSA selection forward in the block-outer
+ * split-K form (bf16).
+ *
+ * Defined on the page "nsa_selection_kernel.py" (openbox-llm), FSA forward
+ * section (_selection_fwd_blockouter_kernel, selection_forward_fsa).  Every
+ * selected key block's K/V is read once: for each (query i, live block j of
+ * its row) pair and head h of the group, a softmax partial over the block's
+ * tokens t <= i,
+ *
+ *   m = max_t s_t,   l = sum_t exp(s_t - m),   acc = sum_t exp(s_t - m) v_t,
+ *
+ * (s_t as in nsa_select_forward) is written to the workspace, and a
+ * log-sum-exp combine per (b, h, i) gives
+ *
+ *   out = sum_j w_j acc_j / sum_j w_j l_j,   w_j = exp(m_j - max_j m_j),
+ *   lse = max_j m_j + ln sum_j w_j l_j,
+ *
+ * which is the same softmax over the union of the selected causal tokens as
+ * nsa_select_forward computes (out = 0, lse = -1e9 for a row with no pair).
+ * A live slot holds 0 <= j < T / block_size with j * block_size <= i.
+ *
+ * Arguments, shapes, dtypes, preconditions (distinct entries per row) and
+ * errors are those of nsa_select_forward, plus:
+ *   workspace       : caller-owned device memory of at least
+ *                     nsa_select_fsa_workspace_size(...) bytes, 256-byte
+ *                     aligned; overwritten, and in use until the work on
+ *                     `stream` completes (one workspace per concurrent call).
+ *   workspace_bytes : its size.
+ * Extra errors: BSA_ERR_NULLPTR (workspace NULL), BSA_ERR_ALIGN (workspace
+ * not 256-byte aligned), BSA_ERR_SCRATCH_LIMIT (workspace_bytes too small),
+ * BSA_ERR_SHAPE (B * Hq * T * S >= 2^31).
+ *
+ * nsa_select_fsa_workspace_size returns the bytes of workspace needed for
+ * these sizes, or 0 if nsa_select_forward_fsa does not accept them; it is
+ * host only and touches no device.
+ *
+ * The work is six kernel launches on `stream`: the inverted selection lists
+ * are built on the device (count, scan, fill), then the block-outer pass and
+ * the combine.  The workspace holds B * Hq * T * S * (D + 2) floats of
+ * partials plus the lists (about 4.4 GB at B=2, Hq=32, T=8192, S=16, D=128).
+ */
+BSA_API size_t nsa_select_fsa_workspace_size(int B, int Hq, int Hkv, int T,
+                                             int D, int block_size, int S);
+BSA_API int nsa_select_forward_fsa(const void* q, const void* k,
+                                   const void* v, const int32_t* block_idx,
+                                   void* out, float* lse, int B, int Hq,
+                                   int Hkv, int T, int D, int block_size,
+                                   int S, void* workspace,
+                                   size_t workspace_bytes,
+                                   cudaStream_t stream);
 
 /* Static, NUL-terminated description of a bsa_status value (never NULL). */
 BSA_API const char* bsa_status_string(int status);

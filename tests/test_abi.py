@@ -123,3 +123,34 @@ def test_backward_and_diff_argument_errors(lib):
     assert bsa.tra_diff_forward_raw(P, P, P, P, P, P, 0, 1, 16, 64, 1.0, 0.5, 2.0, 1, 1, 0) == 2
     assert bsa.tra_diff_forward_raw(P, P, P, P, P, P, 1, 1, 16, 64, 1.0, float("nan"), 2.0, 1, 1, 0) == 4
     assert bsa.tra_diff_forward_raw(P, P, P, P, P, P, 1, 1, 16, 64, 1.0, 0.5, -2.0, 1, 1, 0) == 4
+
+
+def test_fsa_workspace_size_and_argument_errors(lib):
+    from block_sparse_attention_tra_gb300 import bsa
+
+    ws = bsa.nsa_select_fsa_workspace_size
+    B, Hq, Hkv, T, D, S = 2, 32, 2, 8192, 128, 16
+    need = ws(B, Hq, Hkv, T, D, 64, S)
+    partials = B * Hq * T * S * (D + 2) * 4
+    assert partials <= need <= partials + B * Hkv * T * S * 4 + (1 << 22)
+    assert need % 256 == 0
+    assert ws(B, Hq, Hkv, T, 64, 64, S) < need
+    assert ws(B, Hq, Hkv, T, 96, 64, S) == 0  # head dim
+    assert ws(B, Hq, Hkv, 100, D, 64, S) == 0  # T % block_size
+    assert ws(B, 24, 16, T, D, 64, S) == 0  # Hq % Hkv
+    assert ws(B, Hq, Hkv, T, D, 64, 33) == 0
+    assert ws(64, 64, 4, 32768, D, 64, 32) == 0  # B*Hq*T*S >= 2^31: 32-bit partial rows
+
+    def fsa(q=P, idx=P, lse=None, work=P * 64, nbytes=1 << 40, B=1, Hq=16, Hkv=1, T=128, D=128, bs=64, S=4):
+        return bsa.nsa_select_forward_fsa_raw(q, P, P, idx, P, lse, B, Hq, Hkv, T, D, bs, S, work, nbytes, 0)
+
+    assert fsa(q=None) == 1
+    assert fsa(work=None) == 1
+    assert fsa(work=P * 64 + 16) == 7  # workspace not 256-byte aligned
+    assert fsa(idx=P + 2) == 7
+    assert fsa(T=100) == 2
+    assert fsa(D=96) == 4
+    assert fsa(Hq=32, Hkv=1) == 4
+    assert fsa(nbytes=ws(1, 16, 1, 128, 128, 64, 4) - 1) == 9  # workspace too small
+    if not __import__("torch").cuda.is_available():
+        assert fsa(nbytes=ws(1, 16, 1, 128, 128, 64, 4)) == 6  # valid: no device here
