@@ -110,6 +110,19 @@ int encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
   return r == CUDA_SUCCESS ? OK : ERR_SHAPE;
 }
 
+int sm_count() {
+  constexpr int MAX_DEVICES = 64;
+  static int counts[MAX_DEVICES] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return 0;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
 }  // namespace bsa
 
 using namespace bsa;

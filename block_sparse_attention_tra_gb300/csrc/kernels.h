@@ -28,6 +28,10 @@ int encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
                    uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
                    uint32_t box2);
 
+// Streaming multiprocessors of the current device (cached per device; 0 if
+// the query fails).  Persistent kernels size their grids with it.
+int sm_count();
+
 // Threshold rectified attention, fp32 CUDA-core kernel.
 int launch_tra_f32(const float* q, const float* k, const float* v, float* out, int B, int H, int T, int D,
                    float beta, float p, cudaStream_t stream);

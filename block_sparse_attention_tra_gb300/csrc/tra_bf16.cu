@@ -21,9 +21,10 @@
 //
 // Two CTA organisations, chosen by the power class:
 //
-// * p = 1 or 2 (cheap epilogue, tensor-bound): "pair" kernel.  A CTA owns 256
-//   query rows of one (b, h) as two 128-row tiles Q0, Q1 sharing every K/V
-//   tile (half the K/V smem traffic per FLOP).  The tensor pipe runs
+// * p = 1 or 2 (cheap epilogue, tensor-bound): "pair" kernel.  A work item is
+//   256 query rows of one (b, h) as two 128-row tiles Q0, Q1 sharing every
+//   K/V tile (half the K/V smem traffic per FLOP); one persistent CTA per SM
+//   walks a list of items.  The tensor pipe runs
 //     ... PV0(n), QK0(n+1), PV1(n), QK1(n+1), PV0(n+1) ...
 //   and epilogue warpgroup t (warps 4t..4t+3) serves tile Q_t, so each has
 //   two MMA durations to turn S_t into P_t.  TMEM: S0, S1, O0, O1.
@@ -51,16 +52,19 @@ constexpr uint32_t TMEM_COLS = 512;
 
 // 32 scores (tile columns c0 .. c0+31) -> 16 packed weights, stored to TMEM
 // columns c0/2 .. c0/2+15 of the same buffer (already-consumed scores).
-template <int PC>
-__device__ __forceinline__ void epilogue_quarter(const uint32_t (&s)[32], uint32_t tS, int c0, float tau, float p,
-                                                 const float (&pc)[5], bool diag, int key0, int row) {
+// DIAG: the tile holds the diagonal, mask keys after the row (a compile-time
+// flag, so that the other tiles carry no masking instructions at all).
+// EMU: the last EMU_LOG2_PAIRS pairs take log2 on the FMA pipe (p >= 1 only).
+template <int PC, bool EMU, bool DIAG>
+__device__ __forceinline__ void epilogue_quarter(const uint32_t (&s)[32], uint32_t tS, int c0, const PowParams& wp,
+                                                 int key0, int row) {
   uint32_t pk[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
-    const bool emu = e >= 16 - EMU_LOG2_PAIRS;
-    uint32_t w = emu ? weights2<PC, true>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), tau, p, pc)
-                     : weights2<PC, false>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), tau, p, pc);
-    if (diag) {
+    const bool emu = EMU && e >= 16 - EMU_LOG2_PAIRS;
+    uint32_t w = emu ? weights2<PC, true>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp)
+                     : weights2<PC, false>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp);
+    if constexpr (DIAG) {
       const int key = key0 + c0 + 2 * e;  // keys key, key + 1
       if (key > row) w = 0u;
       else if (key + 1 > row) w &= 0x0000ffffu;
@@ -73,17 +77,17 @@ __device__ __forceinline__ void epilogue_quarter(const uint32_t (&s)[32], uint32
 // One 128-key score tile of this thread's row -> P, in four software-
 // pipelined quarters; arrives on p_half after keys 0..63 and on p_full after
 // all 128 (one arrival per warp).
-template <int PC, bool SPLIT = true>
-__device__ __forceinline__ void epilogue_tile(uint32_t tS, float tau, float p, const float (&pc)[5], bool diag,
-                                              int key0, int row, int lane, uint64_t* p_half, uint64_t* p_full) {
+template <int PC, bool EMU, bool SPLIT, bool DIAG>
+__device__ __forceinline__ void epilogue_tile(uint32_t tS, const PowParams& wp, int key0, int row, int lane,
+                                              uint64_t* p_half, uint64_t* p_full) {
   uint32_t a[32], b[32];
   tmem_ld32(tS, a);
   tmem_wait_ld();
   tmem_ld32(tS + 32, b);
-  epilogue_quarter<PC>(a, tS, 0, tau, p, pc, diag, key0, row);
+  epilogue_quarter<PC, EMU, DIAG>(a, tS, 0, wp, key0, row);
   tmem_wait_ld();
   tmem_ld32(tS + 64, a);
-  epilogue_quarter<PC>(b, tS, 32, tau, p, pc, diag, key0, row);
+  epilogue_quarter<PC, EMU, DIAG>(b, tS, 32, wp, key0, row);
   if constexpr (SPLIT) {
     tmem_wait_st();
     tc_fence_before();
@@ -92,9 +96,9 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tS, float tau, float p, c
   }
   tmem_wait_ld();
   tmem_ld32(tS + 96, b);
-  epilogue_quarter<PC>(a, tS, 64, tau, p, pc, diag, key0, row);
+  epilogue_quarter<PC, EMU, DIAG>(a, tS, 64, wp, key0, row);
   tmem_wait_ld();
-  epilogue_quarter<PC>(b, tS, 96, tau, p, pc, diag, key0, row);
+  epilogue_quarter<PC, EMU, DIAG>(b, tS, 96, wp, key0, row);
   tmem_wait_st();
   tc_fence_before();
   __syncwarp();
@@ -192,6 +196,14 @@ __device__ __forceinline__ void produce(uint8_t* smem, int q_off, int k_off, int
 }
 
 // ============================================================ pair kernel (p = 1, 2)
+//
+// Persistent: grid = min(items, SMs).  An item is one (pair index t, bh): the
+// query tiles 2t and 2t+1 of head bh.  Items are numbered longest first and
+// CTA c of G takes, in round r, item r*G + c (r even) or r*G + G-1-c (r odd);
+// this snake order spreads the causal load within ~1% of even for the
+// benchmark shapes.  Every role walks the same item sequence, so no queue is
+// needed; barrier phases are running counts across items, and the next
+// item's Q, K and V loads and QK products overlap the current item's tail.
 
 template <int D>
 struct PairLayout {
@@ -202,9 +214,9 @@ struct PairLayout {
   static constexpr int K_OFF = Q_OFF + 2 * TILE;
   static constexpr int V_OFF = K_OFF + NS * TILE;
   static constexpr int BAR_OFF = V_OFF + NS * TILE;
-  // q_full | k_full[NS] | k_empty[NS] | v_full[NS] | v_empty[NS] | s_full[2] | p_half[2] | p_full[2] |
-  // o_full[2] | mma_done
-  static constexpr int NBAR = 1 + 4 * NS + 8 + 1;
+  // q_full[2] | q_empty[2] | k_full[NS] | k_empty[NS] | v_full[NS] | v_empty[NS] | s_full[2] | p_half[2] |
+  // p_full[2] | o_full[2] | o_empty[2] | mma_done
+  static constexpr int NBAR = 4 + 4 * NS + 10 + 1;
   static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
   static constexpr int ALLOC = TPTR_OFF + 16 + 1024;
 };
@@ -216,50 +228,65 @@ constexpr bool PAIR_SPLIT_P = BSA_PAIR_SPLIT_P;  // hand P over in two halves
 constexpr int PAIR_TMA_WARP = 8;
 constexpr int PAIR_MMA_WARP = 9;
 
+// Item of round r for this CTA (false once the CTA has no more items).
+struct PairItem {
+  int t, bh, nmax0, nmax1, nlast;
+  bool has1;
+};
+__device__ __forceinline__ bool pair_item(int r, int nItems, int BH, int nPair, int nQ, PairItem& it) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const long long k = static_cast<long long>(r) * G + ((r & 1) ? G - 1 - c : c);
+  if (k >= nItems) return false;
+  it.t = nPair - 1 - static_cast<int>(k / BH);
+  it.bh = static_cast<int>(k % BH);
+  it.has1 = (2 * it.t + 1) < nQ;  // second query tile exists
+  it.nmax0 = 2 * it.t;            // last key tile of Q0 (its diagonal)
+  it.nmax1 = it.has1 ? 2 * it.t + 1 : -1;
+  it.nlast = it.has1 ? it.nmax1 : it.nmax0;
+  return true;
+}
+
 template <int D, int PC>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
     tra_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out, int BH, int T,
-                         int nQ, int nPair, float beta, float p) {
+                         int nQ, int nPair, int nItems, float beta, float p) {
   using L = PairLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
+  uint64_t* q_full = bars;               // [2], one per query tile
+  uint64_t* q_empty = q_full + 2;        // [2]
+  uint64_t* k_full = q_empty + 2;
   uint64_t* k_empty = k_full + L::NS;
   uint64_t* v_full = k_empty + L::NS;
   uint64_t* v_empty = v_full + L::NS;
-  uint64_t* s_full = v_empty + L::NS;  // [2], one per query tile
-  uint64_t* p_half = s_full + 2;       // [2]
-  uint64_t* p_full = p_half + 2;       // [2]
-  uint64_t* o_full = p_full + 2;       // [2]
-  uint64_t* mma_done = o_full + 2;
+  uint64_t* s_full = v_empty + L::NS;    // [2]
+  uint64_t* p_half = s_full + 2;         // [2]
+  uint64_t* p_full = p_half + 2;         // [2]
+  uint64_t* o_full = p_full + 2;         // [2]
+  uint64_t* o_empty = o_full + 2;        // [2]
+  uint64_t* mma_done = o_empty + 2;
   uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Longest-first: the first BH CTAs take the last (longest) tile pair.
-  const int t = nPair - 1 - static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
-  const bool has1 = (2 * t + 1) < nQ;  // second query tile exists
-  const int nmax0 = 2 * t;             // last key tile of Q0 (its diagonal)
-  const int nmax1 = has1 ? 2 * t + 1 : -1;
-  const int nlast = has1 ? nmax1 : nmax0;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&q_full[b], 1);
+      mbar_init(&q_empty[b], 1);
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_half[b], 4);
+      mbar_init(&p_full[b], 4);
+      mbar_init(&o_full[b], 1);
+      mbar_init(&o_empty[b], 4);
+    }
     for (int s = 0; s < L::NS; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_half[b], 4);
-      mbar_init(&p_full[b], 4);
-      mbar_init(&o_full[b], 1);
     }
     mbar_init(mma_done, 1);
     fence_barrier_init();
@@ -272,63 +299,129 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tptr;
+  PairItem it;
 
   if (warp == PAIR_TMA_WARP) {
-    if (lane == 0)
-      produce<L::NP, L::TILE, L::NS>(smem, L::Q_OFF, L::K_OFF, L::V_OFF, has1 ? 2 : 1, 2 * t * BM, bh, nlast, &tmQ,
-                                     &tmK, &tmV, q_full, k_full, k_empty, v_full, v_empty);
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      bool ok = true;
+      int g = 0;                // K/V tiles issued so far (ring position)
+      int uq[2] = {0, 0};       // items so far that used query tile qt
+      int nk = 0, nv = 0;
+      for (int r = 0; ok && pair_item(r, nItems, BH, nPair, nQ, it); ++r) {
+        for (int qt = 0; qt < (it.has1 ? 2 : 1); ++qt) {
+          // The previous user of this Q buffer has finished its last QK.
+          if (uq[qt] > 0 && !(ok = mbar_wait(&q_empty[qt], (uq[qt] - 1) & 1))) break;
+          mbar_arrive_expect_tx(&q_full[qt], L::TILE);
+#pragma unroll
+          for (int pnl = 0; pnl < L::NP; ++pnl)
+            tma_load_3d(smem + L::Q_OFF + qt * L::TILE + pnl * PANEL_BYTES, &tmQ, &q_full[qt], 64 * pnl,
+                        (2 * it.t + qt) * BM, it.bh);
+          ++uq[qt];
+        }
+        for (int n = 0; ok && n <= it.nlast; ++n, ++g) {
+          const int s = g % L::NS;
+          const uint32_t ph = (g / L::NS) & 1;
+          if (!(ok = mbar_wait(&k_empty[s], ph ^ 1))) break;
+          mbar_arrive_expect_tx(&k_full[s], L::TILE);
+#pragma unroll
+          for (int pnl = 0; pnl < L::NP; ++pnl)
+            tma_load_3d(smem + L::K_OFF + s * L::TILE + pnl * PANEL_BYTES, &tmK, &k_full[s], 64 * pnl, n * BN,
+                        it.bh);
+          nk = g + 1;
+          if (!(ok = mbar_wait(&v_empty[s], ph ^ 1))) break;
+          mbar_arrive_expect_tx(&v_full[s], L::TILE);
+#pragma unroll
+          for (int pnl = 0; pnl < L::NP; ++pnl)
+            tma_load_3d(smem + L::V_OFF + s * L::TILE + pnl * PANEL_BYTES, &tmV, &v_full[s], 64 * pnl, n * BN,
+                        it.bh);
+          nv = g + 1;
+        }
+      }
+      if (!ok) {
+        // Drain: never leave the CTA with a bulk copy still landing in its smem.
+        for (int qt = 0; qt < 2; ++qt)
+          if (uq[qt] > 0) mbar_wait(&q_full[qt], (uq[qt] - 1) & 1);
+        for (int n = (nk > L::NS ? nk - L::NS : 0); n < nk; ++n) mbar_wait(&k_full[n % L::NS], (n / L::NS) & 1);
+        for (int n = (nv > L::NS ? nv - L::NS : 0); n < nv; ++n) mbar_wait(&v_full[n % L::NS], (n / L::NS) & 1);
+      }
+    }
   } else if (warp == PAIR_MMA_WARP) {
     if (lane == 0) {
       const uint32_t sQ0 = smem_u32(smem + L::Q_OFF);
-      auto qk = [&](int qt, int n) {
-        issue_qk<D>(tmem + qt * BN, sQ0 + qt * L::TILE, smem_u32(smem + L::K_OFF + (n % L::NS) * L::TILE));
+      int g = 0;               // K/V ring position of the item's key tile 0
+      int cs[2] = {0, 0};      // score tiles so far per query tile (s_full / p_half / p_full phase)
+      int uq[2] = {0, 0};      // items so far per query tile (q_full / o_full / o_empty phase)
+      bool ok = true;
+      auto qk = [&](int qt, int gi) {
+        issue_qk<D>(tmem + qt * BN, sQ0 + qt * L::TILE, smem_u32(smem + L::K_OFF + (gi % L::NS) * L::TILE));
         mma_commit(&s_full[qt]);
       };
       // PVt(n) in two halves: keys 0..63 as soon as that half of P is there.
-      auto pv = [&](int qt, int n) -> bool {
-        const uint32_t sV = smem_u32(smem + L::V_OFF + (n % L::NS) * L::TILE);
+      auto pv = [&](int qt, int n, int gi) -> bool {
+        const uint32_t sV = smem_u32(smem + L::V_OFF + (gi % L::NS) * L::TILE);
         const uint32_t tP = tmem + qt * BN, tO = tmem + 2 * BN + qt * D;
-        if (!mbar_wait(PAIR_SPLIT_P ? &p_half[qt] : &p_full[qt], n & 1) ||
-            !mbar_wait(&v_full[n % L::NS], (n / L::NS) & 1))
+        const uint32_t ph = cs[qt] & 1;
+        if (!mbar_wait(PAIR_SPLIT_P ? &p_half[qt] : &p_full[qt], ph) ||
+            !mbar_wait(&v_full[gi % L::NS], (gi / L::NS) & 1))
           return false;
+        // The first P V of an item overwrites O: the epilogue has read the last one.
+        if (n == 0 && uq[qt] > 0 && !mbar_wait(&o_empty[qt], (uq[qt] - 1) & 1)) return false;
         tc_fence_after();
         issue_pv<D>(tO, tP, sV, 0, BN / 32, n == 0);
-        if (!mbar_wait(&p_full[qt], n & 1)) return false;
+        if (!mbar_wait(&p_full[qt], ph)) return false;
         tc_fence_after();
         issue_pv<D>(tO, tP, sV, BN / 32, BN / 16, false);
+        ++cs[qt];
         return true;
       };
 
-      bool ok = mbar_wait(q_full, 0) && mbar_wait(&k_full[0], 0);
-      if (ok) {
+      for (int r = 0; ok && pair_item(r, nItems, BH, nPair, nQ, it); ++r) {
+        if (!(ok = mbar_wait(&k_full[g % L::NS], (g / L::NS) & 1) && mbar_wait(&q_full[0], uq[0] & 1))) break;
         tc_fence_after();
-        qk(0, 0);
-        if (has1) qk(1, 0);
-        mma_commit(&k_empty[0]);
-      }
-      for (int n = 0; n <= nlast && ok; ++n) {
-        const int n1 = n + 1;
-        const bool next_k = n1 <= nlast;
-        // tile 0: PV0(n), then QK0(n+1)
-        if (n <= nmax0) {
-          if (!(ok = pv(0, n))) break;
-          if (n == nmax0) mma_commit(&o_full[0]);
-        }
-        if (next_k) {
-          if (!(ok = mbar_wait(&k_full[n1 % L::NS], (n1 / L::NS) & 1))) break;
+        qk(0, g);
+        if (it.nmax0 == 0) mma_commit(&q_empty[0]);
+        if (it.has1) {
+          if (!(ok = mbar_wait(&q_full[1], uq[1] & 1))) break;
           tc_fence_after();
-          if (n1 <= nmax0) qk(0, n1);
+          qk(1, g);
         }
-        // tile 1: PV1(n), then QK1(n+1)
-        if (has1) {
-          if (!(ok = pv(1, n))) break;
-          if (n == nmax1) mma_commit(&o_full[1]);
+        mma_commit(&k_empty[g % L::NS]);
+        for (int n = 0; n <= it.nlast && ok; ++n) {
+          const int n1 = n + 1, gn = g + n, gn1 = g + n1;
+          const bool next_k = n1 <= it.nlast;
+          // tile 0: PV0(n), then QK0(n+1)
+          if (n <= it.nmax0) {
+            if (!(ok = pv(0, n, gn))) break;
+            if (n == it.nmax0) mma_commit(&o_full[0]);
+          }
+          if (next_k) {
+            if (!(ok = mbar_wait(&k_full[gn1 % L::NS], (gn1 / L::NS) & 1))) break;
+            tc_fence_after();
+            if (n1 <= it.nmax0) {
+              qk(0, gn1);
+              if (n1 == it.nmax0) mma_commit(&q_empty[0]);
+            }
+          }
+          // tile 1: PV1(n), then QK1(n+1)
+          if (it.has1) {
+            if (!(ok = pv(1, n, gn))) break;
+            if (n == it.nmax1) mma_commit(&o_full[1]);
+          }
+          mma_commit(&v_empty[gn % L::NS]);
+          if (next_k) {
+            if (it.has1 && n1 <= it.nmax1) {
+              qk(1, gn1);
+              if (n1 == it.nmax1) mma_commit(&q_empty[1]);
+            }
+            mma_commit(&k_empty[gn1 % L::NS]);
+          }
         }
-        mma_commit(&v_empty[n % L::NS]);
-        if (next_k) {
-          if (has1 && n1 <= nmax1) qk(1, n1);
-          mma_commit(&k_empty[n1 % L::NS]);
-        }
+        g += it.nlast + 1;
+        ++uq[0];
+        if (it.has1) ++uq[1];
       }
       // Commits arrive in issue order: once this one has landed, every
       // barrier arrival of this CTA's MMAs has too, and smem may be released.
@@ -338,23 +431,32 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   } else {
     const int qt = warp >> 2;  // query tile of this warpgroup
     const int wq = warp & 3;   // TMEM lane quarter
-    const int nmax = qt == 0 ? nmax0 : nmax1;
-    const int row = (2 * t + qt) * BM + wq * 32 + lane;
-    const float tau = tau_of_row(row, beta, D);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t tS = lane_base + qt * BN;
-    const float pc[5] = {p * LOG2_C0, p * LOG2_C1, p * LOG2_C2, p * LOG2_C3, p * LOG2_C4};
+    int cs = 0, uq = 0;
     bool ok = true;
-    for (int n = 0; n <= nmax; ++n) {
-      if (!(ok = mbar_wait(&s_full[qt], n & 1))) break;
+    for (int r = 0; ok && pair_item(r, nItems, BH, nPair, nQ, it); ++r) {
+      if (qt == 1 && !it.has1) continue;
+      const int nmax = qt == 0 ? it.nmax0 : it.nmax1;
+      const int row = (2 * it.t + qt) * BM + wq * 32 + lane;
+      const PowParams wp = pow_params(tau_of_row(row, beta, D), p);
+      for (int n = 0; n <= nmax; ++n, ++cs) {
+        if (!(ok = mbar_wait(&s_full[qt], cs & 1))) break;
+        tc_fence_after();
+        if (n == nmax)
+          epilogue_tile<PC, false, PAIR_SPLIT_P, true>(tS, wp, n * BN, row, lane, &p_half[qt], &p_full[qt]);
+        else
+          epilogue_tile<PC, false, PAIR_SPLIT_P, false>(tS, wp, n * BN, row, lane, &p_half[qt], &p_full[qt]);
+      }
+      if (!ok || !(ok = mbar_wait(&o_full[qt], uq & 1))) break;
       tc_fence_after();
-      epilogue_tile<PC, PAIR_SPLIT_P>(tS, tau, p, pc, n == nmax, n * BN, row, lane, &p_half[qt], &p_full[qt]);
-    }
-    if (ok && nmax >= 0 && mbar_wait(&o_full[qt], 0)) {
-      tc_fence_after();
-      __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * T + row) * D;
+      __nv_bfloat16* orow = out + (static_cast<size_t>(it.bh) * T + row) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) store_o_chunk(lane_base + 2 * BN + qt * D, c, orow, row < T);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_empty[qt]);
+      ++uq;
     }
   }
 
@@ -390,7 +492,7 @@ struct RrLayout {
   static constexpr int ALLOC = TPTR_OFF + 16 + 1024;
 };
 
-template <int D, int PC>
+template <int D, int PC, bool EMU>
 __global__ void __launch_bounds__(RR_THREADS, 1)
     tra_bf16_rr_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out, int BH, int T,
@@ -482,15 +584,17 @@ __global__ void __launch_bounds__(RR_THREADS, 1)
     const int wg = warp >> 2;  // epilogue warpgroup: key tiles n = wg mod NB
     const int wq = warp & 3;   // TMEM lane quarter
     const int row = m * BM + wq * 32 + lane;
-    const float tau = tau_of_row(row, beta, D);
+    const PowParams wp = pow_params(tau_of_row(row, beta, D), p);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t tS = lane_base + wg * BN;
-    const float pc[5] = {p * LOG2_C0, p * LOG2_C1, p * LOG2_C2, p * LOG2_C3, p * LOG2_C4};
     bool ok = true;
     for (int n = wg; n <= nmax; n += RR_NB) {
       if (!(ok = mbar_wait(&s_full[wg], (n / RR_NB) & 1))) break;
       tc_fence_after();
-      epilogue_tile<PC>(tS, tau, p, pc, n == nmax, n * BN, row, lane, &p_half[wg], &p_full[wg]);
+      if (n == nmax)
+        epilogue_tile<PC, EMU, true, true>(tS, wp, n * BN, row, lane, &p_half[wg], &p_full[wg]);
+      else
+        epilogue_tile<PC, EMU, true, false>(tS, wp, n * BN, row, lane, &p_half[wg], &p_full[wg]);
     }
     // O: 32-column chunk c is stored by warpgroup c mod NB.
     if (ok && mbar_wait(o_full, 0)) {
@@ -518,10 +622,13 @@ int launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
     return ERR_LAUNCH;
   const int nQ = (T + BM - 1) / BM;
   const int nPair = (nQ + 1) / 2;
-  const long long grid = static_cast<long long>(nPair) * BH;
-  if (grid > 0x7fffffffLL) return ERR_SHAPE;
-  kern<<<static_cast<unsigned>(grid), PAIR_THREADS, L::ALLOC, stream>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16*>(out), BH, T, nQ, nPair, beta, p);
+  const long long items = static_cast<long long>(nPair) * BH;
+  if (items > 0x7fffffffLL) return ERR_SHAPE;
+  const int sms = sm_count();
+  if (sms <= 0) return ERR_DEVICE;
+  const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
+  kern<<<grid, PAIR_THREADS, L::ALLOC, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(out), BH, T, nQ, nPair,
+                                                 static_cast<int>(items), beta, p);
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
 
@@ -529,7 +636,9 @@ template <int D>
 int launch_rr(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* out, int BH, int T,
               float beta, float p, cudaStream_t stream) {
   using L = RrLayout<D>;
-  auto kern = tra_bf16_rr_kernel<D, POW_GENERAL>;
+  // The FMA-pipe log2 is exact on the ReLU's zeros only for p >= 1.
+  auto kern = (EMU_LOG2_PAIRS > 0 && p >= 1.0f) ? tra_bf16_rr_kernel<D, POW_GENERAL, true>
+                                                : tra_bf16_rr_kernel<D, POW_GENERAL, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
     return ERR_LAUNCH;
   const int nQ = (T + BM - 1) / BM;

@@ -107,10 +107,10 @@ __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* 
 // 32 scores of stream t -> 16 packed weights (scaled by `wscale` when
 // SCALE_W), over the consumed score columns.  With NORM the scores are first
 // multiplied by rq * rk[col] (the normalisation of row and key).
-template <int PC, bool NORM, bool SCALE_W>
-__device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t tS, int c0, float tau, float p,
-                                             const float (&pc)[5], float rq, const float (&rk)[32], uint32_t wscale,
-                                             bool diag, int key0, int row) {
+// DIAG (compile time): the tile holds the diagonal, mask keys after the row.
+template <int PC, bool NORM, bool SCALE_W, bool DIAG>
+__device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t tS, int c0, const PowParams& wp,
+                                             float rq, const float (&rk)[32], uint32_t wscale, int key0, int row) {
   uint32_t pk[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
@@ -119,10 +119,9 @@ __device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t t
       s0 *= rq * rk[2 * e];
       s1 *= rq * rk[2 * e + 1];
     }
-    const bool emu = e >= 16 - EMU_LOG2_PAIRS;
-    uint32_t w = emu ? weights2<PC, true>(s0, s1, tau, p, pc) : weights2<PC, false>(s0, s1, tau, p, pc);
+    uint32_t w = weights2<PC, false>(s0, s1, wp);
     if constexpr (SCALE_W) w = mul_bf16x2(w, wscale);
-    if (diag) {
+    if constexpr (DIAG) {
       const int key = key0 + c0 + 2 * e;
       if (key > row) w = 0u;
       else if (key + 1 > row) w &= 0x0000ffffu;
@@ -279,7 +278,7 @@ __global__ void __launch_bounds__(DIFF_THREADS, 1)
     const float tau = tile::tau_of_row(row, beta, D);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t tS = lane_base + t * BT;
-    const float pc[5] = {p * LOG2_C0, p * LOG2_C1, p * LOG2_C2, p * LOG2_C3, p * LOG2_C4};
+    const PowParams wp = pow_params(tau, p);
     const float lc = fminf(fmaxf(lam, 0.0f), 1.0f);
     const uint32_t wscale = pack_bf16x2(-lc, -lc);
     // inv_norm: [q1 | k1 | q2 | k2] x [B*H] x [Tp], zero past T
@@ -309,10 +308,17 @@ __global__ void __launch_bounds__(DIFF_THREADS, 1)
         uint32_t sv[32];
         tmem_ld32(tS + 32 * c, sv);
         tmem_wait_ld();
-        if (t == 0)
-          diff_quarter<PC, NORM, false>(sv, tS, 32 * c, tau, p, pc, rq, rk, wscale, diag, n * BT, row);
-        else
-          diff_quarter<PC, NORM, true>(sv, tS, 32 * c, tau, p, pc, rq, rk, wscale, diag, n * BT, row);
+        if (t == 0) {
+          if (diag)
+            diff_quarter<PC, NORM, false, true>(sv, tS, 32 * c, wp, rq, rk, wscale, n * BT, row);
+          else
+            diff_quarter<PC, NORM, false, false>(sv, tS, 32 * c, wp, rq, rk, wscale, n * BT, row);
+        } else {
+          if (diag)
+            diff_quarter<PC, NORM, true, true>(sv, tS, 32 * c, wp, rq, rk, wscale, n * BT, row);
+          else
+            diff_quarter<PC, NORM, true, false>(sv, tS, 32 * c, wp, rq, rk, wscale, n * BT, row);
+        }
       }
       tmem_wait_st();
       tc_fence_before();

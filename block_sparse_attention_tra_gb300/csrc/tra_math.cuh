@@ -1,6 +1,6 @@
 // tra_math.cuh -- the threshold-attention weight ReLU(s - tau)^p in the
 // epilogue registers: power classes p = 1, p = 2 and general p through
-// exp2(p log2 x), with an optional FMA-pipe log2 for part of the elements.
+// exp2(p log2 x), with an FMA-pipe log2 for part of the elements when p >= 1.
 // Shared by the forward kernels (plain and differential).
 #pragma once
 
@@ -10,9 +10,8 @@
 namespace bsa {
 namespace {
 
-// General power: pairs (of 16 per 32 columns) whose log2 is evaluated on the
-// FMA pipe by a polynomial instead of the MUFU lg2 (the MUFU unit, shared by
-// lg2 and ex2, bounds the general path).
+// General power with p >= 1: pairs (of 16 per 32 columns) whose log2 is
+// evaluated on the FMA pipe by a polynomial instead of the MUFU lg2.
 #ifndef BSA_EMU_LOG2_PAIRS
 #define BSA_EMU_LOG2_PAIRS 0
 #endif
@@ -62,39 +61,85 @@ __device__ __forceinline__ uint32_t pack_bf16x2_alu(float lo, float hi) {
 #endif
 }
 
-// p * log2(x) on the FMA/ALU pipes: x = 2^e m with m in [1, 2) taken from
-// the bits, log2(m) from the LOG2_Ck polynomial with p folded into pc[].
-// Any x <= 0 (the ReLU's zeros) returns -inf, so that exp2 of it is 0.
-__device__ __forceinline__ float p_log2_poly(float x, float p, const float (&pc)[5]) {
-  const uint32_t b = __float_as_uint(x);
-  const float m = __uint_as_float((b & 0x007fffffu) | 0x3f800000u);
-  const float e = __uint_as_float((b >> 23) | 0x4b000000u) - (8388608.0f + 127.0f);
-  float acc = fmaf(pc[4], m, pc[3]);
-  acc = fmaf(acc, m, pc[2]);
-  acc = fmaf(acc, m, pc[1]);
-  acc = fmaf(acc, m, pc[0]);
-  return x > 0.0f ? fmaf(p, e, acc) : -INFINITY;
+// Two fp32 values in one 64-bit register (lo = first) and the packed
+// f32x2 arithmetic of the sm_100 family: one instruction for both keys of a
+// pair on the FMA pipe.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// Per-row constants of the weight: tau and p (and p * LOG2_Ck) duplicated
+// into both halves of a packed pair.
+struct PowParams {
+  uint64_t tau2, p2, pc2[5];
+};
+__device__ __forceinline__ PowParams pow_params(float tau, float p) {
+  PowParams w;
+  w.tau2 = f2_pack(tau, tau);
+  w.p2 = f2_pack(p, p);
+  const float c[5] = {LOG2_C0, LOG2_C1, LOG2_C2, LOG2_C3, LOG2_C4};
+#pragma unroll
+  for (int k = 0; k < 5; ++k) w.pc2[k] = f2_pack(p * c[k], p * c[k]);
+  return w;
+}
+
+// p * log2(x) of two non-negative x on the FMA/ALU pipes: x = 2^e m with
+// m in [1, 2) taken from the bits, log2(m) from the LOG2_Ck polynomial with p
+// folded into pc2.  x = 0 reads as e = -127, m = 1, i.e. about -127 p, whose
+// exp2 flushes to 0 for p >= 1: callers use this path only when p >= 1.
+__device__ __forceinline__ uint64_t p_log2_poly2(float x0, float x1, const PowParams& w) {
+  const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
+  const uint64_t m = f2_pack(__uint_as_float((b0 & 0x007fffffu) | 0x3f800000u),
+                             __uint_as_float((b1 & 0x007fffffu) | 0x3f800000u));
+  const float bias = 8388608.0f + 127.0f;
+  const uint64_t e = f2_sub(f2_pack(__uint_as_float((b0 >> 23) | 0x4b000000u), __uint_as_float((b1 >> 23) | 0x4b000000u)),
+                            f2_pack(bias, bias));
+  uint64_t acc = f2_fma(w.pc2[4], m, w.pc2[3]);
+  acc = f2_fma(acc, m, w.pc2[2]);
+  acc = f2_fma(acc, m, w.pc2[1]);
+  acc = f2_fma(acc, m, w.pc2[0]);
+  return f2_fma(w.p2, e, acc);
 }
 
 // Weights of two adjacent keys from their scores: ReLU(s - tau)^p, bf16x2.
+// EMU: p * log2 on the FMA pipe (requires p >= 1), else on the MUFU unit.
 template <int PC, bool EMU>
-__device__ __forceinline__ uint32_t weights2(float s0, float s1, float tau, float p, const float (&pc)[5]) {
-  const float x0 = s0 - tau, x1 = s1 - tau;
+__device__ __forceinline__ uint32_t weights2(float s0, float s1, const PowParams& w) {
+  float x0, x1;
+  f2_unpack(f2_sub(f2_pack(s0, s1), w.tau2), x0, x1);
   if constexpr (PC == POW_ONE) {
     return relu_pack(x0, x1);
   } else if constexpr (PC == POW_TWO) {
     const uint32_t h = relu_pack(x0, x1);
     return mul_bf16x2(h, h);
   } else {
-    // x^p = exp2(p log2 x); log2 of the ReLU's zeros is -inf and ex2 of it 0.
+    // x^p = exp2(p log2 x); the ReLU's zeros give log2 = -inf (MUFU) or about
+    // -127 p (polynomial, p >= 1), and exp2 of either is 0.
+    x0 = fmaxf(x0, 0.0f);
+    x1 = fmaxf(x1, 0.0f);
+    const uint64_t y = EMU ? p_log2_poly2(x0, x1, w) : f2_mul(f2_pack(lg2_approx(x0), lg2_approx(x1)), w.p2);
     float y0, y1;
-    if constexpr (EMU) {
-      y0 = p_log2_poly(x0, p, pc);
-      y1 = p_log2_poly(x1, p, pc);
-    } else {
-      y0 = p * lg2_approx(fmaxf(x0, 0.0f));
-      y1 = p * lg2_approx(fmaxf(x1, 0.0f));
-    }
+    f2_unpack(y, y0, y1);
     return pack_bf16x2_alu(ex2_approx(y0), ex2_approx(y1));
   }
 }

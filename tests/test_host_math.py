@@ -1,10 +1,11 @@
 """CPU checks of host-side arithmetic the kernels rely on.
 
-* The general-power epilogue of the bf16 TRA kernel evaluates p*log2(x) for
-  part of the elements with integer bit operations and a degree-4 polynomial
-  (constants LOG2_C0..LOG2_C4 in ``csrc/tra_math.cuh``).  Here the same steps
-  are replayed in float32 numpy and checked against numpy's log2 over a wide
-  range, including the zero / denormal cases that must flush the weight to 0.
+* The general-power epilogue of the bf16 TRA kernel can evaluate p*log2(x)
+  for part of the elements with integer bit operations and a degree-4
+  polynomial (constants LOG2_C0..LOG2_C4 in ``csrc/tra_math.cuh``), when
+  p >= 1.  Here the same steps are replayed in float32 numpy and checked
+  against numpy's log2 over a wide range, including the ReLU zeros whose
+  weight must flush to 0.
 """
 
 import os
@@ -22,8 +23,9 @@ def coefficients():
     return np.array(c, dtype=np.float32)
 
 
-def p_log2_poly(r, p):
-    """float32 replay of p_log2_poly() in tra_math.cuh."""
+def p_log2_poly2(r, p):
+    """float32 replay of p_log2_poly2() in tra_math.cuh (inputs are the ReLU's
+    outputs, so r >= 0)."""
     c = coefficients()
     pc = (np.float32(p) * c).astype(np.float32)
     r = np.asarray(r, dtype=np.float32)
@@ -34,23 +36,27 @@ def p_log2_poly(r, p):
     acc = (acc * m + pc[2]).astype(np.float32)
     acc = (acc * m + pc[1]).astype(np.float32)
     acc = (acc * m + pc[0]).astype(np.float32)
-    y = (np.float32(p) * e + acc).astype(np.float32)
-    return np.where(r > 0, y, np.float32(-np.inf)).astype(np.float32)
+    return (np.float32(p) * e + acc).astype(np.float32)
 
 
 def test_log2_polynomial_error_bound():
     r = np.geomspace(1e-37, 1e37, 2_000_001).astype(np.float32)
-    for p in (1.5, 3.7, 0.25):
-        got = p_log2_poly(r, p).astype(np.float64)
+    for p in (1.5, 3.7, 1.0):
+        got = p_log2_poly2(r, p).astype(np.float64)
         want = p * np.log2(r.astype(np.float64))
         # 1.0e-4 from the fit plus float32 rounding of p*e (|p*e| <= ~100)
         tol = p * 1.05e-4 + np.abs(want) * 2 ** -23
         assert np.all(np.abs(got - want) <= tol)
 
 
-def test_log2_polynomial_relu_zeros_give_zero_weight():
-    """x <= 0 must give -inf (weight exactly 0) whatever p is."""
-    for p in (1.5, 0.25, 0.01):
-        y = p_log2_poly(np.array([0.0, -0.0, -1.0, -3e38], dtype=np.float32), p)
-        assert np.all(np.isneginf(y))
-        assert np.all(np.exp2(y.astype(np.float64)) == 0.0)
+def test_log2_polynomial_relu_zeros_give_zero_weight_for_p_at_least_one():
+    """A ReLU zero (x = +0) reads as about -127 p: for p >= 1 its exp2 is below
+    the smallest normal float, which ex2.approx.ftz flushes to exactly 0.  (The
+    kernels use this path only when p >= 1.)"""
+    smallest_normal = np.float64(2.0) ** -126
+    for p in (1.0, 1.5, 3.7, 15.0):
+        y = p_log2_poly2(np.array([0.0], dtype=np.float32), p).astype(np.float64)
+        assert np.all(np.exp2(y) < smallest_normal)
+    # Below p = 1 the same bits would give a tiny non-zero weight: excluded.
+    y = p_log2_poly2(np.array([0.0], dtype=np.float32), 0.5).astype(np.float64)
+    assert np.exp2(y) >= smallest_normal
