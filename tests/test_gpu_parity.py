@@ -72,7 +72,7 @@ TRA_SMALL = [
     (3, 5, 640, 64, 1.0, 2.0, "bf16"),    # many (b, h), 5 row tiles
     (1, 2, 200, 64, 0.5, 0.25, "bf16"),   # p < 1: ReLU zeros must stay exactly 0
     (1, 1, 256, 128, 1.0, 15.0, "bf16"),  # large power (the page's p=15 example)
-    (2, 3, 1000, 64, 2.0, 1.5, "bf16"),   # persistent grid: more items than one pass
+    (2, 3, 1000, 64, 2.0, 1.5, "bf16"),   # general power, ragged, 8 row tiles
 ]
 
 
@@ -84,6 +84,29 @@ def test_tra_small_full_output(B, H, T, D, beta, p, dtype):
     tol = F32_TOL if dtype == "f32" else BF16_TOL
     err = rel_err(gpu, ref)
     assert err <= tol, f"max err {err:.3e} of max|ref| (tol {tol})"
+
+
+# The bf16 kernels are persistent (one CTA per SM walking a list of items).
+# Hundreds of heads with short sequences give every CTA several items of one
+# to three key tiles, so the handoffs between items (Q buffer, O accumulator,
+# barrier phases across items) run many times per CTA.
+TRA_MANY_ITEMS = [
+    # (B, H, T, D, beta, p)
+    (4, 100, 256, 64, 2.0, 1.5),    # round-robin kernel, two O accumulators
+    (2, 100, 384, 128, 1.0, 1.5),   # round-robin kernel, one O accumulator
+    (4, 100, 256, 64, 1.0, 2.0),    # pair kernel
+    (2, 100, 384, 128, 1.0, 2.0),   # pair kernel, odd tile count (items without a second tile)
+    (3, 70, 130, 64, 0.5, 0.25),    # p < 1, ragged two-tile items
+]
+
+
+@pytest.mark.parametrize("B,H,T,D,beta,p", TRA_MANY_ITEMS)
+def test_tra_many_short_items_per_cta(B, H, T, D, beta, p):
+    q, k, v = workloads.tra_inputs(B, H, T, D, "bf16", seed=H + T)
+    gpu = run_tra(q, k, v, beta, p)
+    ref = otra.tra_forward(f64(q), f64(k), f64(v), beta, p)
+    err = rel_err(gpu, ref)
+    assert err <= BF16_TOL, f"max err {err:.3e} of max|ref| (tol {BF16_TOL})"
 
 
 def test_tra_huge_beta_only_row0():
