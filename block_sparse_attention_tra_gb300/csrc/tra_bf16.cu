@@ -29,15 +29,13 @@
 //   and epilogue warpgroup t (warps 4t..4t+3) serves tile Q_t, so each has
 //   two MMA durations to turn S_t into P_t.  TMEM: S0, S1, O0, O1.
 //
-// * general p (x^p = exp2(p log2 x): two MUFU operations per score, which
-//   outweigh the tensor work at small D): "round-robin" kernel.  A CTA owns
-//   one 128-row tile; NB = 3 score buffers in TMEM are filled by QK(n) for
+// * general p (x^p = exp2(p log2 x), an epilogue several times heavier than
+//   the tensor work at small D): "round-robin" kernel.  A CTA owns one
+//   128-row tile; NB = 3 score buffers in TMEM are filled by QK(n) for
 //   n = k mod 3 and served by three epilogue warpgroups, so twelve epilogue
-//   warps share the MUFU units while the tensor pipe runs ahead.  TMEM:
-//   S0, S1, S2, O.
-//
-// CTAs are numbered longest-first (the most causal key tiles first); the
-// hardware block scheduler then balances the causal load across SMs.
+//   warps work while the tensor pipe runs ahead.  TMEM: S0, S1, S2, O.  Its
+//   CTAs are numbered longest-first (the most causal key tiles first) and the
+//   hardware block scheduler balances the causal load across SMs.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tra_math.cuh"
