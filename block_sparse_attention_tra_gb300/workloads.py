@@ -116,6 +116,10 @@ NSA_WORKLOADS = {
     for w in [
         NsaWorkload("nsa_bf16_B2_Hq32_Hkv2_T8192_D128", 2, 32, 2, 8192, 128, 64, 16),
         NsaWorkload("nsa_bf16_B1_Hq64_Hkv4_T32768_D128", 1, 64, 4, 32768, 128, 64, 16),
+        # A quarter of the T=8192 workload (half the groups, half the length):
+        # small enough for multi-pass profiler captures of the split-K form,
+        # whose workspace is 1.1 GB here instead of 4.4 GB.
+        NsaWorkload("nsa_bf16_B1_Hq32_Hkv2_T4096_D128", 1, 32, 2, 4096, 128, 64, 16),
     ]
 }
 
