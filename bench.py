@@ -36,7 +36,8 @@ if ROOT not in sys.path:
 
 METRIC = "causal fwd TFLOP/s & % of dense BF16 tensor peak (threshold attn; NSA select)"
 DEFAULT_WORKLOAD = "tra_bf16_B4_H16_T4096_D128"
-SECONDARY = ["tra_bf16_B2_H32_T8192_D64", "nsa_bf16_B2_Hq32_Hkv2_T8192_D128", "nsa_bf16_B1_Hq64_Hkv4_T32768_D128"]
+SECONDARY = ["tra_bf16_B2_H32_T8192_D64", "nsa_bf16_B2_Hq32_Hkv2_T8192_D128", "nsa_bf16_B1_Hq64_Hkv4_T32768_D128",
+             "nsa_bf16_B2_Hq32_Hkv2_T8192_D32_bs32"]
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = {
     "tra": "block_sparse_attention_tra_gb300/csrc/tra_bf16.cu",
@@ -213,8 +214,9 @@ def roofline_for(w, ms_per_launch, pk, sustained: bool, fsa: bool = False):
     achieved = w.algorithmic_bytes / (ms_per_launch * 1e-3) / 1e9
     r = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
          "frac": round(achieved / pk["hbm_gbs"], 4), "peak_kind": "copy bandwidth of " + pk["source"],
-         "traffic": ncu_traffic("fsa" if fsa else "nsa", ("fsa:" if fsa else "") + w.name),
-         "kernel": "fsa_blockouter_kernel + fsa_combine_kernel" if fsa else "nsa_select_kernel",
+            "traffic": ncu_traffic("fsa" if fsa else "nsa", ("fsa:" if fsa else "") + w.name),
+         "kernel": ("fsa_blockouter_kernel + fsa_combine_kernel" if fsa else
+                    "nsa_select_kernel" if (w.block_size == 64 and w.D in (64, 128)) else "nsa_general_kernel"),
          "algorithmic_bytes_per_launch": w.algorithmic_bytes,
          "tflops": round(w.flops / (ms_per_launch * 1e-3) / 1e12, 2),
          "unique_bytes_per_launch": w.unique_bytes}
@@ -375,7 +377,7 @@ def run_ours(args):
                      "tflops": round(w2.flops * world / (t * 1e-3) / 1e12, 3),
                      "roofline": roofline_for(w2, t, pk, sustained=False), "l2": "flushed between launches"}
             sec.append(entry)
-            if isinstance(w2, workloads.NsaWorkload):
+            if isinstance(w2, workloads.NsaWorkload) and w2.block_size == 64 and w2.D in (64, 128):
                 # The same selection through the block-outer split-K form
                 # (six launches: list build, block pass, combine).
                 q2, k2, v2, idx2 = dev

@@ -65,11 +65,14 @@ int check_nsa_shape(int B, int Hq, int Hkv, int T, int D, int block_size, int S)
   if (static_cast<long long>(B) * Hq * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * Hq > 0x7fffffffLL || static_cast<long long>(B) * Hkv * T * S >= (1LL << 40))
     return BSA_ERR_SHAPE;
-  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
-  if (block_size != 64) return BSA_ERR_UNSUPPORTED;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128) return BSA_ERR_UNSUPPORTED;
   if (Hq / Hkv > 16) return BSA_ERR_UNSUPPORTED;
   return BSA_OK;
 }
+
+// The split-K form is built for 64-token blocks of 64 or 128 dims.
+bool fsa_shape_supported(int D, int block_size) { return block_size == 64 && (D == 64 || D == 128); }
 
 int check_nsa_args(const void* q, const void* k, const void* v, const int32_t* block_idx, const void* out,
                    const float* lse, int B, int Hq, int Hkv, int T, int D, int block_size, int S) {
@@ -240,7 +243,7 @@ int nsa_select_forward(const void* q, const void* k, const void* v, const int32_
 }
 
 size_t nsa_select_fsa_workspace_size(int B, int Hq, int Hkv, int T, int D, int block_size, int S) {
-  if (check_nsa_shape(B, Hq, Hkv, T, D, block_size, S) != BSA_OK) return 0;
+  if (check_nsa_shape(B, Hq, Hkv, T, D, block_size, S) != BSA_OK || !fsa_shape_supported(D, block_size)) return 0;
   // The partial rows are indexed with 32-bit integers inside the kernels.
   if (static_cast<long long>(B) * Hq * T * S >= (1LL << 31)) return 0;
   return nsa_fsa_workspace_bytes(B, Hq, Hkv, T, D, S);
@@ -251,6 +254,7 @@ int nsa_select_forward_fsa(const void* q, const void* k, const void* v, const in
                            size_t workspace_bytes, cudaStream_t stream) {
   const int chk = check_nsa_args(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, block_size, S);
   if (chk != BSA_OK) return chk;
+  if (!fsa_shape_supported(D, block_size)) return BSA_ERR_UNSUPPORTED;
   if (workspace == nullptr) return BSA_ERR_NULLPTR;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BSA_ERR_ALIGN;
   const size_t need = nsa_select_fsa_workspace_size(B, Hq, Hkv, T, D, block_size, S);

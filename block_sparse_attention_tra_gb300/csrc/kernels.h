@@ -66,6 +66,11 @@ int launch_nsa_select(const void* q, const void* k, const void* v, const int32_t
                       float* lse, int B, int Hq, int Hkv, int T, int D, int block_size, int S,
                       cudaStream_t stream);
 
+// NSA selection attention for any accepted head dim and block size (cp.async
+// + mma.sync kernel); launch_nsa_select hands other shapes to it.
+int launch_nsa_general(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out, float* lse,
+                       int B, int Hq, int Hkv, int T, int D, int block_size, int S, cudaStream_t stream);
+
 // NSA selection attention, block-outer split-K form with a log-sum-exp
 // combine (nsa_fsa.cu).  `workspace` holds nsa_fsa_workspace_bytes(...) bytes,
 // 256-byte aligned; block_size is 64.

@@ -17,6 +17,7 @@
 // is the TMA producer.  The grid is persistent with two CTAs per SM: CTA c
 // takes query groups c, c + gridDim.x, ...
 #include "kernels.h"
+#include "mma_sync.cuh"
 #include "ptx.cuh"
 
 namespace bsa {
@@ -46,29 +47,6 @@ struct NsaLayout {
   static constexpr int ALLOC = BYTES + 1024;
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ float ex2f(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NSA_CONSUMERS * 32)); }
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a panel of
@@ -372,7 +350,10 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
 
 int launch_nsa_select(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out, float* lse,
                       int B, int Hq, int Hkv, int T, int D, int block_size, int S, cudaStream_t stream) {
-  if (block_size != NSA_BS) return ERR_UNSUPPORTED;
+  // The TMA kernel serves 64-token blocks of 64 or 128 dims; every other
+  // accepted shape runs the general kernel.
+  if (block_size != NSA_BS || (D != 64 && D != 128))
+    return launch_nsa_general(q, k, v, block_idx, out, lse, B, Hq, Hkv, T, D, block_size, S, stream);
   const int G = Hq / Hkv;
   if (G < 1 || G > 16) return ERR_UNSUPPORTED;
   CUtensorMap mq, mk, mv;

@@ -120,6 +120,8 @@ NSA_WORKLOADS = {
         # small enough for multi-pass profiler captures of the split-K form,
         # whose workspace is 1.1 GB here instead of 4.4 GB.
         NsaWorkload("nsa_bf16_B1_Hq32_Hkv2_T4096_D128", 1, 32, 2, 4096, 128, 64, 16),
+        # Smaller head dim and blocks (the general kernel's shapes).
+        NsaWorkload("nsa_bf16_B2_Hq32_Hkv2_T8192_D32_bs32", 2, 32, 2, 8192, 32, 32, 16),
     ]
 }
 

@@ -222,7 +222,11 @@ BSA_API int tra_diff_forward_noalloc(const void* q1, const void* q2,
  *                distinct (the page's reference treats a repeated block as
  *                selected once; this kernel would count it twice).
  *   lse        : [B, Hq, T] fp32, or NULL to skip it.
- *   D          : 128 or 64.   block_size : 64.   1 <= S <= 32.
+ *   D          : 16, 32, 64 or 128 (the page: a power of two <= 128).
+ *   block_size : 16, 32, 64 or 128 (the page: >= 16; its tiles need a power
+ *                of two).  64-token blocks of 64 or 128 dims run a TMA kernel,
+ *                every other shape a cp.async one; results agree either way.
+ *   1 <= S <= 32.
  *   T          : multiple of block_size.   Hq % Hkv == 0, 1 <= Hq / Hkv <= 16.
  *   stream     : CUDA stream the kernel is enqueued on.
  *
@@ -258,7 +262,8 @@ BSA_API int nsa_select_forward(const void* q, const void* k, const void* v,
  * A live slot holds 0 <= j < T / block_size with j * block_size <= i.
  *
  * Arguments, shapes, dtypes, preconditions (distinct entries per row) and
- * errors are those of nsa_select_forward, plus:
+ * errors are those of nsa_select_forward (but only block_size 64 with D 64 or
+ * 128 is built: other shapes return BSA_ERR_UNSUPPORTED), plus:
  *   workspace       : caller-owned device memory of at least
  *                     nsa_select_fsa_workspace_size(...) bytes, 256-byte
  *                     aligned; overwritten, and in use until the work on

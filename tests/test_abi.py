@@ -86,7 +86,9 @@ def test_nsa_argument_errors(lib):
     assert nsa(lib, S=0) == 2
     assert nsa(lib, S=33) == 2
     assert nsa(lib, D=96) == 4
-    assert nsa(lib, bs=32, T=128) == 4
+    assert nsa(lib, D=8) == 4
+    assert nsa(lib, bs=48, T=192) == 4  # block sizes 16, 32, 64, 128 only
+    assert nsa(lib, bs=256, T=256) == 4
     assert nsa(lib, Hq=32, Hkv=1) == 4  # group of 32 heads
     assert nsa(lib, k=P + 4) == 7
     assert nsa(lib, idx=P + 2) == 7
@@ -96,6 +98,9 @@ def test_nsa_argument_errors(lib):
 def test_valid_arguments_without_a_device_report_device_error(lib):
     assert tra(lib) == 6
     assert nsa(lib) == 6
+    for D in (16, 32, 64, 128):
+        for bs in (16, 32, 64, 128):
+            assert nsa(lib, D=D, bs=bs, T=256) == 6
 
 
 def test_binding_has_no_cpu_path():
@@ -150,6 +155,9 @@ def test_fsa_workspace_size_and_argument_errors(lib):
     assert fsa(idx=P + 2) == 7
     assert fsa(T=100) == 2
     assert fsa(D=96) == 4
+    assert fsa(D=32) == 4  # the split-K form is built for 64-token blocks of 64 or 128 dims
+    assert fsa(bs=32) == 4
+    assert ws(B, Hq, Hkv, T, 32, 64, S) == 0
     assert fsa(Hq=32, Hkv=1) == 4
     assert fsa(nbytes=ws(1, 16, 1, 128, 128, 64, 4) - 1) == 9  # workspace too small
     if not __import__("torch").cuda.is_available():

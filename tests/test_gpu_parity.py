@@ -219,6 +219,43 @@ def test_nsa_small_full_output(B, Hq, Hkv, T, D, S):
     check_nsa(go, gl, ro, rl)
 
 
+# Head dims and block sizes served by the general kernel (cp.async + mma.sync);
+# (64 / 128, 64) above run the TMA kernel.
+NSA_SHAPES = [
+    # (B, Hq, Hkv, T, D, block_size, S)
+    (1, 16, 1, 256, 16, 16, 8),
+    (2, 8, 2, 384, 32, 32, 5),
+    (1, 16, 2, 512, 64, 128, 4),
+    (1, 16, 1, 512, 128, 128, 3),
+    (1, 4, 4, 320, 128, 16, 16),    # G = 1, many small blocks
+    (2, 12, 4, 256, 32, 64, 6),     # G = 3, D = 32 with 64-token blocks
+    (1, 16, 1, 192, 16, 64, 32),    # S = 32
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,T,D,bs,S", NSA_SHAPES)
+def test_nsa_head_dims_and_block_sizes(B, Hq, Hkv, T, D, bs, S):
+    q, k, v, idx = workloads.nsa_inputs(B, Hq, Hkv, T, D, bs, S, seed=T + D + bs)
+    out, lse = bsa.nsa_select_forward(q.cuda(), k.cuda(), v.cuda(), idx.cuda(), bs, return_lse=True)
+    torch.cuda.synchronize()
+    ro, rl = onsa.nsa_select_forward(f64(q), f64(k), f64(v), idx.numpy(), bs)
+    check_nsa(f64(out), f64(lse), ro, rl)
+
+
+def test_nsa_general_padding_future_and_empty_rows():
+    B, Hq, Hkv, T, D, bs, S = 1, 8, 1, 256, 32, 32, 4
+    q, k, v, idx = workloads.nsa_inputs(B, Hq, Hkv, T, D, bs, S, seed=23)
+    idx[0, 0, 10:20, :] = -1                # empty rows
+    idx[0, 0, 30:40, 0] = 3                 # a future block only (tokens 96..127)
+    idx[0, 0, 30:40, 1:] = -1
+    idx[0, 0, 100:110, 3] = 7               # future block next to valid ones
+    out, lse = bsa.nsa_select_forward(q.cuda(), k.cuda(), v.cuda(), idx.cuda(), bs, return_lse=True)
+    torch.cuda.synchronize()
+    ro, rl = onsa.nsa_select_forward(f64(q), f64(k), f64(v), idx.numpy(), bs)
+    check_nsa(f64(out), f64(lse), ro, rl)
+    assert np.all(f64(lse)[0, :, 10:20] == -1e9) and np.all(f64(out)[0, :, 10:20] == 0)
+
+
 def test_nsa_padding_future_and_out_of_range_slots():
     B, Hq, Hkv, T, D, S = 1, 16, 1, 256, 128, 4
     q, k, v, idx = workloads.nsa_inputs(B, Hq, Hkv, T, D, 64, S, seed=21)
