@@ -32,6 +32,7 @@ from .bsa import (  # noqa: F401
     tra_diff_forward,
     tra_diff_forward_raw,
     tra_forward,
+    tra_forward_ex_raw,
     tra_forward_raw,
 )
 
@@ -42,6 +43,7 @@ __all__ = [
     "load_library",
     "tra_forward",
     "tra_forward_raw",
+    "tra_forward_ex_raw",
     "tra_backward",
     "tra_backward_raw",
     "tra_diff_forward",

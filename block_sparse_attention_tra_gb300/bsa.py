@@ -16,6 +16,7 @@ _LIB = None
 
 BSA_F32 = 0
 BSA_BF16 = 1
+BSA_TRA_SQRT_HALF_POWERS = 1  # tra_forward_ex flag: p = k + 1/2 as x^k sqrt(x)
 
 _STATUS = {
     0: "BSA_OK",
@@ -55,6 +56,8 @@ def load_library():
     vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.tra_forward.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, vp]
     lib.tra_forward.restype = i32
+    lib.tra_forward_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, i32, vp]
+    lib.tra_forward_ex.restype = i32
     lib.nsa_select_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.nsa_select_forward.restype = i32
     lib.tra_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, vp]
@@ -97,6 +100,12 @@ def _check(status: int, what: str):
 def tra_forward_raw(q, k, v, out, B, H, T, D, beta, p, dtype, stream=0) -> int:
     """Direct C call with integer device pointers; returns the bsa_status."""
     return load_library().tra_forward(q, k, v, out, B, H, T, D, float(beta), float(p), int(dtype), stream)
+
+
+def tra_forward_ex_raw(q, k, v, out, B, H, T, D, beta, p, dtype, flags, stream=0) -> int:
+    """Direct C call of tra_forward_ex with integer device pointers."""
+    return load_library().tra_forward_ex(q, k, v, out, B, H, T, D, float(beta), float(p), int(dtype), int(flags),
+                                         stream)
 
 
 def tra_backward_raw(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, dtype, stream=0) -> int:
@@ -157,12 +166,14 @@ def _dtype_code(t):
     raise BsaError(f"unsupported dtype {t.dtype}", 3)
 
 
-def tra_forward(q, k, v, beta: float, p: float = 2.0, out=None, stream=None):
+def tra_forward(q, k, v, beta: float, p: float = 2.0, out=None, stream=None, sqrt_half_powers: bool = False):
     """Threshold rectified attention forward on CUDA tensors ``[B, H, T, D]``.
 
     ``out = ReLU(q k^T - tau(i))^p v`` with ``tau(i) = beta sqrt(2 ln(i+1)/D)``,
     causal, unnormalised; float32 or bfloat16 in, same dtype out.  Runs on
     ``stream`` (default: torch's current stream) without synchronising.
+    ``sqrt_half_powers``: evaluate p = 0.5, 1.5, 2.5, 3.5 as x^k sqrt(x)
+    (``tra_forward_ex`` with ``BSA_TRA_SQRT_HALF_POWERS``).
     """
     if q.device.type != "cuda":
         raise BsaError("tra_forward takes CUDA tensors (no CPU path)")
@@ -176,8 +187,12 @@ def tra_forward(q, k, v, beta: float, p: float = 2.0, out=None, stream=None):
 
         out = torch.empty_like(q)
     B, H, T, D = q.shape
-    st = tra_forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T, D,
-                         beta, p, _dtype_code(q), _stream_handle(stream))
+    if sqrt_half_powers:
+        st = tra_forward_ex_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T, D, beta, p,
+                                _dtype_code(q), BSA_TRA_SQRT_HALF_POWERS, _stream_handle(stream))
+    else:
+        st = tra_forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T, D,
+                             beta, p, _dtype_code(q), _stream_handle(stream))
     _check(st, "tra_forward")
     return out
 

@@ -134,6 +134,12 @@ extern "C" {
 
 int tra_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int D, float beta,
                 float p, int dtype, cudaStream_t stream) {
+  return tra_forward_ex(q, k, v, out, B, H, T, D, beta, p, dtype, 0, stream);
+}
+
+int tra_forward_ex(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int D, float beta,
+                   float p, int dtype, int flags, cudaStream_t stream) {
+  if ((flags & ~BSA_TRA_SQRT_HALF_POWERS) != 0) return BSA_ERR_UNSUPPORTED;
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return BSA_ERR_NULLPTR;
   if (dtype != BSA_F32 && dtype != BSA_BF16) return BSA_ERR_DTYPE;
   if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
@@ -147,7 +153,7 @@ int tra_forward(const void* q, const void* k, const void* v, void* out, int B, i
   if (dtype == BSA_F32)
     return launch_tra_f32(static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
                           static_cast<float*>(out), B, H, T, D, beta, p, stream);
-  return launch_tra_bf16(q, k, v, out, B, H, T, D, beta, p, stream);
+  return launch_tra_bf16(q, k, v, out, B, H, T, D, beta, p, (flags & BSA_TRA_SQRT_HALF_POWERS) != 0, stream);
 }
 
 int tra_backward(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv, int B,

@@ -36,9 +36,10 @@ int sm_count();
 int launch_tra_f32(const float* q, const float* k, const float* v, float* out, int B, int H, int T, int D,
                    float beta, float p, cudaStream_t stream);
 
-// Threshold rectified attention, bf16 tcgen05 kernel.
+// Threshold rectified attention, bf16 tcgen05 kernel.  sqrt_half_powers:
+// p = k + 1/2 (k = 0..3) runs as x^k sqrt(x) instead of exp2(p log2 x).
 int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int D,
-                    float beta, float p, cudaStream_t stream);
+                    float beta, float p, bool sqrt_half_powers, cudaStream_t stream);
 
 // Threshold rectified attention backward (dq, dk, dv), bf16 tcgen05 kernels.
 int launch_tra_bwd_bf16(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv,
@@ -87,9 +88,17 @@ unsigned int tra_bwd_device_error();
 unsigned int tra_diff_device_error();
 unsigned int nsa_fsa_device_error();
 
-// Power class of the TRA epilogue: p == 1, p == 2, or the general exp2/log2 path.
-enum PowerClass : int { POW_GENERAL = 0, POW_ONE = 1, POW_TWO = 2 };
+// Power class of the TRA epilogue: p == 1, p == 2, or the general exp2/log2
+// path; and, on request only, p = k + 1/2 (k = 0..3) as x^k sqrt(x).
+enum PowerClass : int { POW_GENERAL = 0, POW_ONE = 1, POW_TWO = 2, POW_HALF0 = 3, POW_HALF3 = 6 };
 
 inline int power_class(float p) { return p == 1.0f ? POW_ONE : (p == 2.0f ? POW_TWO : POW_GENERAL); }
+
+// POW_HALF0 + k for p = k + 1/2 with k in 0..3, else -1.
+inline int half_power_class(float p) {
+  for (int k = 0; k <= POW_HALF3 - POW_HALF0; ++k)
+    if (p == static_cast<float>(k) + 0.5f) return POW_HALF0 + k;
+  return -1;
+}
 
 }  // namespace bsa

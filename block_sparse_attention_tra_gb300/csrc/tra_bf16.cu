@@ -649,8 +649,22 @@ int launch_rr(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& m
 
 }  // namespace
 
+// Half powers (on request): the pair kernel, whose two epilogue warpgroups
+// suffice for a one-MUFU-operation weight.
+template <int D>
+int launch_half(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* out, int BH, int T,
+                float beta, float p, int hc, cudaStream_t stream) {
+  switch (hc) {
+    case POW_HALF0: return launch_pair<D, POW_HALF0>(mq, mk, mv, out, BH, T, beta, p, stream);
+    case POW_HALF0 + 1: return launch_pair<D, POW_HALF0 + 1>(mq, mk, mv, out, BH, T, beta, p, stream);
+    case POW_HALF0 + 2: return launch_pair<D, POW_HALF0 + 2>(mq, mk, mv, out, BH, T, beta, p, stream);
+    case POW_HALF3: return launch_pair<D, POW_HALF3>(mq, mk, mv, out, BH, T, beta, p, stream);
+    default: return ERR_UNSUPPORTED;
+  }
+}
+
 int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int D,
-                    float beta, float p, cudaStream_t stream) {
+                    float beta, float p, bool sqrt_half_powers, cudaStream_t stream) {
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
   const uint64_t rs = static_cast<uint64_t>(D) * 2;  // row stride in bytes
@@ -660,6 +674,12 @@ int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int 
   if (st == OK) st = encode_tmap_3d(&mv, v, D, T, BH, rs, hs, 64, BN, 1);
   if (st != OK) return st;
   const int pc = power_class(p);
+  const int hc = sqrt_half_powers ? half_power_class(p) : -1;
+  if (hc >= 0) {
+    if (D == 128) return launch_half<128>(mq, mk, mv, out, BH, T, beta, p, hc, stream);
+    if (D == 64) return launch_half<64>(mq, mk, mv, out, BH, T, beta, p, hc, stream);
+    return ERR_UNSUPPORTED;
+  }
   if (D == 128) {
     if (pc == POW_TWO) return launch_pair<128, POW_TWO>(mq, mk, mv, out, BH, T, beta, p, stream);
     if (pc == POW_ONE) return launch_pair<128, POW_ONE>(mq, mk, mv, out, BH, T, beta, p, stream);

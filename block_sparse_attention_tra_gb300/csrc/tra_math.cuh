@@ -1,6 +1,7 @@
 // tra_math.cuh -- the threshold-attention weight ReLU(s - tau)^p in the
-// epilogue registers: power classes p = 1, p = 2 and general p through
-// exp2(p log2 x), with an FMA-pipe log2 for part of the elements when p >= 1.
+// epilogue registers: power classes p = 1, p = 2, general p through
+// exp2(p log2 x) (with an FMA-pipe log2 for part of the elements when
+// p >= 1), and, on request, p = k + 1/2 as x^k sqrt(x).
 // Shared by the forward kernels (plain and differential).
 #pragma once
 
@@ -27,6 +28,11 @@ constexpr float LOG2_C0 = -2.505614662e+00f, LOG2_C1 = 4.049616893e+00f, LOG2_C2
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float y;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 __device__ __forceinline__ float lg2_approx(float x) {
@@ -132,6 +138,18 @@ __device__ __forceinline__ uint32_t weights2(float s0, float s1, const PowParams
   } else if constexpr (PC == POW_TWO) {
     const uint32_t h = relu_pack(x0, x1);
     return mul_bf16x2(h, h);
+  } else if constexpr (PC >= POW_HALF0) {
+    // p = k + 1/2: x^p = x^k sqrt(x), one MUFU operation per score; the
+    // ReLU's zeros give sqrt(0) = 0 exactly.
+    x0 = fmaxf(x0, 0.0f);
+    x1 = fmaxf(x1, 0.0f);
+    uint64_t r = f2_pack(sqrt_approx(x0), sqrt_approx(x1));
+    const uint64_t x = f2_pack(x0, x1);
+#pragma unroll
+    for (int j = 0; j < PC - POW_HALF0; ++j) r = f2_mul(r, x);
+    float r0, r1;
+    f2_unpack(r, r0, r1);
+    return pack_bf16x2_alu(r0, r1);
   } else {
     // x^p = exp2(p log2 x); the ReLU's zeros give log2 = -inf (MUFU) or about
     // -127 p (polynomial, p >= 1), and exp2 of either is 0.

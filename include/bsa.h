@@ -103,6 +103,30 @@ BSA_API int tra_forward(const void* q, const void* k, const void* v, void* out,
                         int B, int H, int T, int D, float beta, float p,
                         int dtype, cudaStream_t stream);
 
+/* Flags of tra_forward_ex. */
+typedef enum {
+  /* p = k + 1/2 with k in 0..3 (0.5, 1.5, 2.5, 3.5) is evaluated as
+     x^k * sqrt(x): one square root per score instead of exp2(p * log2 x). */
+  BSA_TRA_SQRT_HALF_POWERS = 1
+} bsa_tra_flags;
+
+/*
+ * tra_forward_ex -- tra_forward with evaluation flags.
+ *
+ * Same method, arguments, layout, rules and errors as tra_forward, plus
+ * `flags`, a bitwise OR of bsa_tra_flags (0 = exactly tra_forward; unknown
+ * bits return BSA_ERR_UNSUPPORTED).  With BSA_TRA_SQRT_HALF_POWERS and
+ * dtype BSA_BF16, a half-integer p from 0.5 to 3.5 runs x^k * sqrt(x) on the
+ * pair kernel; the result is the same map ReLU(.)^p within rounding (the
+ * square root is correct to about one float ulp).  Other p, and dtype
+ * BSA_F32, are computed exactly as tra_forward computes them.  The page
+ * evaluates every non-integer power through exp and log, which tra_forward
+ * follows; this option is an equivalent evaluation for half-integer powers.
+ */
+BSA_API int tra_forward_ex(const void* q, const void* k, const void* v,
+                           void* out, int B, int H, int T, int D, float beta,
+                           float p, int dtype, int flags, cudaStream_t stream);
+
 /*
  * tra_backward -- gradients of the threshold rectified attention forward.
  *

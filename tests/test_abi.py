@@ -162,3 +162,17 @@ def test_fsa_workspace_size_and_argument_errors(lib):
     assert fsa(nbytes=ws(1, 16, 1, 128, 128, 64, 4) - 1) == 9  # workspace too small
     if not __import__("torch").cuda.is_available():
         assert fsa(nbytes=ws(1, 16, 1, 128, 128, 64, 4)) == 6  # valid: no device here
+
+
+def test_tra_forward_ex_flags(lib):
+    from block_sparse_attention_tra_gb300 import bsa
+
+    def ex(flags, p=1.5, D=64):
+        return bsa.tra_forward_ex_raw(P, P, P, P, 1, 1, 16, D, 1.0, p, 1, flags, 0)
+
+    assert ex(2) == 4 and ex(-1) == 4  # unknown flag bits
+    assert ex(1, D=96) == 4
+    assert ex(1, p=0.0) == 4
+    assert bsa.tra_forward_ex_raw(None, P, P, P, 1, 1, 16, 64, 1.0, 1.5, 1, 1, 0) == 1
+    if not __import__("torch").cuda.is_available():
+        assert ex(0) == 6 and ex(1) == 6 and ex(1, p=2.0) == 6

@@ -109,6 +109,30 @@ def test_tra_many_short_items_per_cta(B, H, T, D, beta, p):
     assert err <= BF16_TOL, f"max err {err:.3e} of max|ref| (tol {BF16_TOL})"
 
 
+# Half-integer powers evaluated as x^k sqrt(x) (tra_forward_ex flag): the same
+# map, so the same oracle and bar; other powers must match tra_forward bit
+# for bit.
+@pytest.mark.parametrize("p,D,T", [(1.5, 64, 333), (0.5, 128, 300), (2.5, 64, 640), (3.5, 128, 257)])
+def test_tra_sqrt_half_powers(p, D, T):
+    q, k, v = workloads.tra_inputs(2, 3, T, D, "bf16", seed=T + D)
+    gpu = f64(bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), 1.0, p, sqrt_half_powers=True))
+    ref = otra.tra_forward(f64(q), f64(k), f64(v), 1.0, p)
+    err = rel_err(gpu, ref)
+    assert err <= BF16_TOL, f"max err {err:.3e} of max|ref|"
+    # and it agrees with the exp/log evaluation far inside the bar
+    plain = f64(bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), 1.0, p))
+    assert rel_err(gpu, plain) <= BF16_TOL / 4
+
+
+@pytest.mark.parametrize("p", [2.0, 1.7, 1.0])
+def test_tra_sqrt_flag_leaves_other_powers_alone(p):
+    q, k, v = workloads.tra_inputs(1, 4, 384, 64, "bf16", seed=5)
+    a = bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), 1.0, p, sqrt_half_powers=True)
+    b = bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), 1.0, p)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
 def test_tra_huge_beta_only_row0():
     q, k, v = workloads.tra_inputs(2, 2, 256, 64, "bf16", seed=3)
     gpu = run_tra(q, k, v, 1e6, 2.0)
