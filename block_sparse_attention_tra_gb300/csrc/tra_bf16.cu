@@ -19,23 +19,15 @@
 // consumed score columns in two halves, so the P V MMA can start on the
 // first 64 keys while the second half is still being computed.
 //
-// Two CTA organisations, chosen by the power class:
-//
-// * p = 1 or 2 (cheap epilogue, tensor-bound): "pair" kernel.  A work item is
-//   256 query rows of one (b, h) as two 128-row tiles Q0, Q1 sharing every
-//   K/V tile (half the K/V smem traffic per FLOP); one persistent CTA per SM
-//   walks a list of items.  The tensor pipe runs
+// One organisation for every power class, the persistent "pair" kernel: a
+// work item is 256 query rows of one (b, h) as two 128-row tiles Q0, Q1
+// sharing every K/V tile (half the K/V smem traffic per FLOP); one CTA per SM
+// walks a list of items.  The tensor pipe runs
 //     ... PV0(n), QK0(n+1), PV1(n), QK1(n+1), PV0(n+1) ...
-//   and epilogue warpgroup t (warps 4t..4t+3) serves tile Q_t, so each has
-//   two MMA durations to turn S_t into P_t.  TMEM: S0, S1, O0, O1.
-//
-// * general p (x^p = exp2(p log2 x), an epilogue several times heavier than
-//   the tensor work at small D): "round-robin" kernel.  A CTA owns one
-//   128-row tile; NB = 3 score buffers in TMEM are filled by QK(n) for
-//   n = k mod 3 and served by three epilogue warpgroups, so twelve epilogue
-//   warps work while the tensor pipe runs ahead.  TMEM: S0, S1, S2, O.  Its
-//   CTAs are numbered longest-first (the most causal key tiles first) and the
-//   hardware block scheduler balances the causal load across SMs.
+// and epilogue warpgroup t (warps 4t..4t+3) serves tile Q_t, so each has two
+// MMA durations to turn S_t into P_t.  TMEM: S0, S1, O0, O1.  The power class
+// (p = 1, p = 2, general p through exp2(p log2 x), or on request a half
+// power as x^k sqrt(x)) only changes the epilogue arithmetic.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tra_math.cuh"
@@ -52,16 +44,13 @@ constexpr uint32_t TMEM_COLS = 512;
 // columns c0/2 .. c0/2+15 of the same buffer (already-consumed scores).
 // DIAG: the tile holds the diagonal, mask keys after the row (a compile-time
 // flag, so that the other tiles carry no masking instructions at all).
-// EMU: the last EMU_LOG2_PAIRS pairs take log2 on the FMA pipe (p >= 1 only).
-template <int PC, bool EMU, bool DIAG>
+template <int PC, bool DIAG>
 __device__ __forceinline__ void epilogue_quarter(const uint32_t (&s)[32], uint32_t tS, int c0, const PowParams& wp,
                                                  int key0, int row) {
   uint32_t pk[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
-    const bool emu = EMU && e >= 16 - EMU_LOG2_PAIRS;
-    uint32_t w = emu ? weights2<PC, true>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp)
-                     : weights2<PC, false>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp);
+    uint32_t w = weights2<PC>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp);
     if constexpr (DIAG) {
       const int key = key0 + c0 + 2 * e;  // keys key, key + 1
       if (key > row) w = 0u;
@@ -75,17 +64,17 @@ __device__ __forceinline__ void epilogue_quarter(const uint32_t (&s)[32], uint32
 // One 128-key score tile of this thread's row -> P, in four software-
 // pipelined quarters; arrives on p_half after keys 0..63 and on p_full after
 // all 128 (one arrival per warp).
-template <int PC, bool EMU, bool SPLIT, bool DIAG>
+template <int PC, bool SPLIT, bool DIAG>
 __device__ __forceinline__ void epilogue_tile(uint32_t tS, const PowParams& wp, int key0, int row, int lane,
                                               uint64_t* p_half, uint64_t* p_full) {
   uint32_t a[32], b[32];
   tmem_ld32(tS, a);
   tmem_wait_ld();
   tmem_ld32(tS + 32, b);
-  epilogue_quarter<PC, EMU, DIAG>(a, tS, 0, wp, key0, row);
+  epilogue_quarter<PC, DIAG>(a, tS, 0, wp, key0, row);
   tmem_wait_ld();
   tmem_ld32(tS + 64, a);
-  epilogue_quarter<PC, EMU, DIAG>(b, tS, 32, wp, key0, row);
+  epilogue_quarter<PC, DIAG>(b, tS, 32, wp, key0, row);
   if constexpr (SPLIT) {
     tmem_wait_st();
     tc_fence_before();
@@ -94,9 +83,9 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tS, const PowParams& wp, 
   }
   tmem_wait_ld();
   tmem_ld32(tS + 96, b);
-  epilogue_quarter<PC, EMU, DIAG>(a, tS, 64, wp, key0, row);
+  epilogue_quarter<PC, DIAG>(a, tS, 64, wp, key0, row);
   tmem_wait_ld();
-  epilogue_quarter<PC, EMU, DIAG>(b, tS, 96, wp, key0, row);
+  epilogue_quarter<PC, DIAG>(b, tS, 96, wp, key0, row);
   tmem_wait_st();
   tc_fence_before();
   __syncwarp();
@@ -442,9 +431,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         if (!(ok = mbar_wait(&s_full[qt], cs & 1))) break;
         tc_fence_after();
         if (n == nmax)
-          epilogue_tile<PC, false, PAIR_SPLIT_P, true>(tS, wp, n * BN, row, lane, &p_half[qt], &p_full[qt]);
+          epilogue_tile<PC, PAIR_SPLIT_P, true>(tS, wp, n * BN, row, lane, &p_half[qt], &p_full[qt]);
         else
-          epilogue_tile<PC, false, PAIR_SPLIT_P, false>(tS, wp, n * BN, row, lane, &p_half[qt], &p_full[qt]);
+          epilogue_tile<PC, PAIR_SPLIT_P, false>(tS, wp, n * BN, row, lane, &p_half[qt], &p_full[qt]);
       }
       if (!ok || !(ok = mbar_wait(&o_full[qt], uq & 1))) break;
       tc_fence_after();
@@ -461,150 +450,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == PAIR_MMA_WARP) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
-  }
-}
-
-// ===================================================== round-robin kernel (general p)
-
-constexpr int RR_NB = 3;                          // score buffers = epilogue warpgroups
-constexpr int RR_THREADS = RR_NB * 128 + 64;      // + TMA warp + MMA warp
-constexpr int RR_TMA_WARP = RR_NB * 4;
-constexpr int RR_MMA_WARP = RR_NB * 4 + 1;
-
-template <int D>
-struct RrLayout {
-  static constexpr int NP = D / 64;
-  static constexpr int TILE = NP * PANEL_BYTES;
-  static constexpr int NS = (D == 128) ? 3 : 6;  // >= RR_NB: QK runs RR_NB tiles ahead of PV
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + TILE;
-  static constexpr int V_OFF = K_OFF + NS * TILE;
-  static constexpr int BAR_OFF = V_OFF + NS * TILE;
-  // q_full | k_full[NS] | k_empty[NS] | v_full[NS] | v_empty[NS] | s_full[NB] | p_half[NB] | p_full[NB] |
-  // o_full | mma_done
-  static constexpr int NBAR = 1 + 4 * NS + 3 * RR_NB + 2;
-  static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int ALLOC = TPTR_OFF + 16 + 1024;
-};
-
-template <int D, int PC, bool EMU>
-__global__ void __launch_bounds__(RR_THREADS, 1)
-    tra_bf16_rr_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out, int BH, int T,
-                       int nQ, float beta, float p) {
-  using L = RrLayout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = k_full + L::NS;
-  uint64_t* v_full = k_empty + L::NS;
-  uint64_t* v_empty = v_full + L::NS;
-  uint64_t* s_full = v_empty + L::NS;  // [NB]
-  uint64_t* p_half = s_full + RR_NB;   // [NB]
-  uint64_t* p_full = p_half + RR_NB;   // [NB]
-  uint64_t* o_full = p_full + RR_NB;
-  uint64_t* mma_done = o_full + 1;
-  uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int m = nQ - 1 - static_cast<int>(blockIdx.x) / BH;  // longest first
-  const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int nmax = m;  // key tiles 0..m (BN == BM)
-  constexpr uint32_t O_COL = RR_NB * BN;
-
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < L::NS; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
-    }
-    for (int b = 0; b < RR_NB; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_half[b], 4);
-      mbar_init(&p_full[b], 4);
-    }
-    mbar_init(o_full, 1);
-    mbar_init(mma_done, 1);
-    fence_barrier_init();
-  }
-  if (warp == RR_MMA_WARP) {
-    tmem_alloc(tptr, TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tptr;
-
-  if (warp == RR_TMA_WARP) {
-    if (lane == 0)
-      produce<L::NP, L::TILE, L::NS>(smem, L::Q_OFF, L::K_OFF, L::V_OFF, 1, m * BM, bh, nmax, &tmQ, &tmK, &tmV,
-                                     q_full, k_full, k_empty, v_full, v_empty);
-  } else if (warp == RR_MMA_WARP) {
-    if (lane == 0) {
-      const uint32_t sQ = smem_u32(smem + L::Q_OFF);
-      auto qk = [&](int n) -> bool {
-        if (!mbar_wait(&k_full[n % L::NS], (n / L::NS) & 1)) return false;
-        tc_fence_after();
-        issue_qk<D>(tmem + (n % RR_NB) * BN, sQ, smem_u32(smem + L::K_OFF + (n % L::NS) * L::TILE));
-        mma_commit(&s_full[n % RR_NB]);
-        mma_commit(&k_empty[n % L::NS]);
-        return true;
-      };
-      bool ok = mbar_wait(q_full, 0);
-      for (int n = 0; n < RR_NB && n <= nmax && ok; ++n) ok = qk(n);
-      for (int n = 0; n <= nmax && ok; ++n) {
-        const int b = n % RR_NB;
-        const uint32_t ph = (n / RR_NB) & 1;
-        const uint32_t sV = smem_u32(smem + L::V_OFF + (n % L::NS) * L::TILE);
-        if (!(ok = mbar_wait(&p_half[b], ph) && mbar_wait(&v_full[n % L::NS], (n / L::NS) & 1))) break;
-        tc_fence_after();
-        issue_pv<D>(tmem + O_COL, tmem + b * BN, sV, 0, BN / 32, n == 0);
-        if (!(ok = mbar_wait(&p_full[b], ph))) break;
-        tc_fence_after();
-        issue_pv<D>(tmem + O_COL, tmem + b * BN, sV, BN / 32, BN / 16, false);
-        mma_commit(&v_empty[n % L::NS]);
-        if (n + RR_NB <= nmax) ok = qk(n + RR_NB);  // reuses buffer b after PV(n) in issue order
-      }
-      if (ok) mma_commit(o_full);
-      mma_commit(mma_done);
-      mbar_wait(mma_done, 0);
-    }
-  } else {
-    const int wg = warp >> 2;  // epilogue warpgroup: key tiles n = wg mod NB
-    const int wq = warp & 3;   // TMEM lane quarter
-    const int row = m * BM + wq * 32 + lane;
-    const PowParams wp = pow_params(tau_of_row(row, beta, D), p);
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t tS = lane_base + wg * BN;
-    bool ok = true;
-    for (int n = wg; n <= nmax; n += RR_NB) {
-      if (!(ok = mbar_wait(&s_full[wg], (n / RR_NB) & 1))) break;
-      tc_fence_after();
-      if (n == nmax)
-        epilogue_tile<PC, EMU, true, true>(tS, wp, n * BN, row, lane, &p_half[wg], &p_full[wg]);
-      else
-        epilogue_tile<PC, EMU, true, false>(tS, wp, n * BN, row, lane, &p_half[wg], &p_full[wg]);
-    }
-    // O: 32-column chunk c is stored by warpgroup c mod NB.
-    if (ok && mbar_wait(o_full, 0)) {
-      tc_fence_after();
-      __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * T + row) * D;
-      for (int c = wg; c < D / 32; c += RR_NB) store_o_chunk(lane_base + O_COL, c, orow, row < T);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == RR_MMA_WARP) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -630,27 +475,7 @@ int launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
 
-template <int D>
-int launch_rr(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* out, int BH, int T,
-              float beta, float p, cudaStream_t stream) {
-  using L = RrLayout<D>;
-  // The FMA-pipe log2 is exact on the ReLU's zeros only for p >= 1.
-  auto kern = (EMU_LOG2_PAIRS > 0 && p >= 1.0f) ? tra_bf16_rr_kernel<D, POW_GENERAL, true>
-                                                : tra_bf16_rr_kernel<D, POW_GENERAL, false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
-    return ERR_LAUNCH;
-  const int nQ = (T + BM - 1) / BM;
-  const long long grid = static_cast<long long>(nQ) * BH;
-  if (grid > 0x7fffffffLL) return ERR_SHAPE;
-  kern<<<static_cast<unsigned>(grid), RR_THREADS, L::ALLOC, stream>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16*>(out), BH, T, nQ, beta, p);
-  return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
-}
-
-}  // namespace
-
-// Half powers (on request): the pair kernel, whose two epilogue warpgroups
-// suffice for a one-MUFU-operation weight.
+// Half powers (on request).
 template <int D>
 int launch_half(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* out, int BH, int T,
                 float beta, float p, int hc, cudaStream_t stream) {
@@ -662,6 +487,8 @@ int launch_half(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
     default: return ERR_UNSUPPORTED;
   }
 }
+
+}  // namespace
 
 int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int D,
                     float beta, float p, bool sqrt_half_powers, cudaStream_t stream) {
@@ -683,12 +510,12 @@ int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int 
   if (D == 128) {
     if (pc == POW_TWO) return launch_pair<128, POW_TWO>(mq, mk, mv, out, BH, T, beta, p, stream);
     if (pc == POW_ONE) return launch_pair<128, POW_ONE>(mq, mk, mv, out, BH, T, beta, p, stream);
-    return launch_rr<128>(mq, mk, mv, out, BH, T, beta, p, stream);
+    return launch_pair<128, POW_GENERAL>(mq, mk, mv, out, BH, T, beta, p, stream);
   }
   if (D == 64) {
     if (pc == POW_TWO) return launch_pair<64, POW_TWO>(mq, mk, mv, out, BH, T, beta, p, stream);
     if (pc == POW_ONE) return launch_pair<64, POW_ONE>(mq, mk, mv, out, BH, T, beta, p, stream);
-    return launch_rr<64>(mq, mk, mv, out, BH, T, beta, p, stream);
+    return launch_pair<64, POW_GENERAL>(mq, mk, mv, out, BH, T, beta, p, stream);
   }
   return ERR_UNSUPPORTED;
 }

@@ -119,7 +119,7 @@ __device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t t
       s0 *= rq * rk[2 * e];
       s1 *= rq * rk[2 * e + 1];
     }
-    uint32_t w = weights2<PC, false>(s0, s1, wp);
+    uint32_t w = weights2<PC>(s0, s1, wp);
     if constexpr (SCALE_W) w = mul_bf16x2(w, wscale);
     if constexpr (DIAG) {
       const int key = key0 + c0 + 2 * e;

@@ -86,16 +86,16 @@ def test_tra_small_full_output(B, H, T, D, beta, p, dtype):
     assert err <= tol, f"max err {err:.3e} of max|ref| (tol {tol})"
 
 
-# The bf16 kernels are persistent (one CTA per SM walking a list of items).
+# The bf16 kernel is persistent (one CTA per SM walking a list of items).
 # Hundreds of heads with short sequences give every CTA several items of one
 # to three key tiles, so the handoffs between items (Q buffer, O accumulator,
 # barrier phases across items) run many times per CTA.
 TRA_MANY_ITEMS = [
     # (B, H, T, D, beta, p)
-    (4, 100, 256, 64, 2.0, 1.5),    # round-robin kernel, two O accumulators
-    (2, 100, 384, 128, 1.0, 1.5),   # round-robin kernel, one O accumulator
-    (4, 100, 256, 64, 1.0, 2.0),    # pair kernel
-    (2, 100, 384, 128, 1.0, 2.0),   # pair kernel, odd tile count (items without a second tile)
+    (4, 100, 256, 64, 2.0, 1.5),    # general power
+    (2, 100, 384, 128, 1.0, 1.5),   # general power, odd tile count (items without a second tile)
+    (4, 100, 256, 64, 1.0, 2.0),    # p = 2
+    (2, 100, 384, 128, 1.0, 2.0),   # p = 2, odd tile count
     (3, 70, 130, 64, 0.5, 0.25),    # p < 1, ragged two-tile items
 ]
 
