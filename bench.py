@@ -404,8 +404,8 @@ def run_ours(args):
         k2b = torch.randn(qb.shape, generator=gen).to(torch.bfloat16).to(device)
         n = max(3, args.steps // 2)
         extra = [
-            ("tra_backward", lambda: bsa.tra_backward(qb, kb, vb, dob, wb.beta, wb.p), 10 * wb.flops // 4),
-            ("tra_diff_forward(normalize=1, lambda=0.5)",
+            ("tra_backward", wb.name, lambda: bsa.tra_backward(qb, kb, vb, dob, wb.beta, wb.p), 10 * wb.flops // 4),
+            ("tra_diff_forward(normalize=1, lambda=0.5)", wb.name,
              lambda: bsa.tra_diff_forward(qb, q2b, kb, k2b, vb, wb.beta, 0.5, wb.p, normalize=True), 2 * wb.flops),
         ]
         # The half-power variant on the T=8192 general-power workload (p = 1.5
@@ -413,11 +413,11 @@ def run_ours(args):
         w3 = workloads.TRA_WORKLOADS["tra_bf16_B2_H32_T8192_D64"]
         q3, k3, v3 = (t.to(device) for t in workloads.workload_inputs(w3))
         o3 = torch.empty_like(q3)
-        extra.append((f"tra_forward(sqrt_half_powers) on {w3.name}",
+        extra.append(("tra_forward(sqrt_half_powers)", w3.name,
                       lambda: bsa.tra_forward(q3, k3, v3, w3.beta, w3.p, out=o3, sqrt_half_powers=True), w3.flops))
-        for label, f, flops in extra:
+        for label, wname, f, flops in extra:
             t = reduce_max(time_resident(f, n, 3, world, flush=flush), world, device) / n
-            sec.append({"workload": f"{label} on {wb.name}", "ms_per_launch": round(t, 4),
+            sec.append({"workload": f"{label} on {wname}", "ms_per_launch": round(t, 4),
                         "tflops": round(flops * world / (t * 1e-3) / 1e12, 3),
                         "frac_of_bf16_peak": round(flops / (t * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
                         "algorithmic_flops": flops, "l2": "flushed between launches"})
