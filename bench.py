@@ -209,7 +209,7 @@ def roofline_for(w, ms_per_launch, pk, sustained: bool, fsa: bool = False):
         return {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4) if peak else None,
                 "peak_kind": ("sustained" if sustained else "burst") + " bf16 of " + pk["source"],
-                "traffic": ncu_traffic("tra", w.name), "kernel": "tra_bf16_tcgen05_kernel",
+                "traffic": ncu_traffic("tra", w.name), "kernel": "tra_bf16_pair_kernel (persistent, tcgen05)",
                 "algorithmic_flops_per_launch": w.flops}
     achieved = w.algorithmic_bytes / (ms_per_launch * 1e-3) / 1e9
     r = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
