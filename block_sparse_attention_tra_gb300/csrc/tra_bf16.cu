@@ -22,10 +22,12 @@
 // One organisation for every power class, the persistent "pair" kernel: a
 // work item is 256 query rows of one (b, h) as two 128-row tiles Q0, Q1
 // sharing every K/V tile (half the K/V smem traffic per FLOP); one CTA per SM
-// walks a list of items.  The tensor pipe runs
-//     ... PV0(n), QK0(n+1), PV1(n), QK1(n+1), PV0(n+1) ...
-// and epilogue warpgroup t (warps 4t..4t+3) serves tile Q_t, so each has two
-// MMA durations to turn S_t into P_t.  TMEM: S0, S1, O0, O1.  The power class
+// walks a list of items.  For each tile t the tensor pipe runs
+//     ... PV_t(n), QK_t(n+1), PV_t(n+1) ...
+// and epilogue warpgroup t (warps 4t..4t+3) turns S_t into P_t.  For p = 1
+// and p = 2 each tile has its own MMA-issuing thread; for the other powers
+// one thread issues both tiles' MMAs in turn (PairCfg).  TMEM: S0, S1, O0,
+// O1.  The power class
 // (p = 1, p = 2, general p through exp2(p log2 x), or on request a half
 // power as x^k sqrt(x)) only changes the epilogue arithmetic.
 #include "kernels.h"
@@ -202,18 +204,28 @@ struct PairLayout {
   static constexpr int V_OFF = K_OFF + NS * TILE;
   static constexpr int BAR_OFF = V_OFF + NS * TILE;
   // q_full[2] | q_empty[2] | k_full[NS] | k_empty[NS] | v_full[NS] | v_empty[NS] | s_full[2] | p_half[2] |
-  // p_full[2] | o_full[2] | o_empty[2] | mma_done
-  static constexpr int NBAR = 4 + 4 * NS + 10 + 1;
+  // p_full[2] | o_full[2] | o_empty[2] | mma_done[2]
+  static constexpr int NBAR = 4 + 4 * NS + 10 + 2;
   static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
   static constexpr int ALLOC = TPTR_OFF + 16 + 1024;
 };
-constexpr int PAIR_THREADS = 320;  // 2 epilogue warpgroups + TMA warp + MMA warp
+// MMA issuers: a single thread sustains only about one tcgen05.mma per ~70
+// cycles whatever N is (measured), which cannot keep the tensor pipe fed
+// when the epilogue is light (p = 1, 2): there each query tile gets its own
+// issuing warp.  With a heavy epilogue (general and half powers) one issuer
+// serving both tiles in turn is faster: it keeps the two epilogue
+// warpgroups half a step apart, so one of them is always computing.
+template <int PC>
+struct PairCfg {
+  static constexpr int ISSUERS = (PC == POW_ONE || PC == POW_TWO) ? 2 : 1;
+  static constexpr int THREADS = 256 + 32 + 32 * ISSUERS;  // epilogue warpgroups, TMA warp, MMA warp(s)
+};
 #ifndef BSA_PAIR_SPLIT_P
 #define BSA_PAIR_SPLIT_P 1
 #endif
 constexpr bool PAIR_SPLIT_P = BSA_PAIR_SPLIT_P;  // hand P over in two halves
 constexpr int PAIR_TMA_WARP = 8;
-constexpr int PAIR_MMA_WARP = 9;
+constexpr int PAIR_MMA_WARP = 9;  // first MMA warp (allocates TMEM)
 
 // Item of round r for this CTA (false once the CTA has no more items).
 struct PairItem {
@@ -234,7 +246,7 @@ __device__ __forceinline__ bool pair_item(int r, int nItems, int BH, int nPair, 
 }
 
 template <int D, int PC>
-__global__ void __launch_bounds__(PAIR_THREADS, 1)
+__global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
     tra_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out, int BH, int T,
                          int nQ, int nPair, int nItems, float beta, float p) {
@@ -253,7 +265,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   uint64_t* p_full = p_half + 2;         // [2]
   uint64_t* o_full = p_full + 2;         // [2]
   uint64_t* o_empty = o_full + 2;        // [2]
-  uint64_t* mma_done = o_empty + 2;
+  uint64_t* mma_done = o_empty + 2;     // [2]
   uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
 
   const int warp = threadIdx.x >> 5;
@@ -271,11 +283,12 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     }
     for (int s = 0; s < L::NS; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
+      mbar_init(&k_empty[s], PairCfg<PC>::ISSUERS);  // one release per issuer per use
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&v_empty[s], PairCfg<PC>::ISSUERS);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
     fence_barrier_init();
   }
   if (warp == PAIR_MMA_WARP) {
@@ -335,7 +348,77 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         for (int n = (nv > L::NS ? nv - L::NS : 0); n < nv; ++n) mbar_wait(&v_full[n % L::NS], (n / L::NS) & 1);
       }
     }
+  } else if (warp >= PAIR_MMA_WARP && PairCfg<PC>::ISSUERS == 2) {
+    // Issuer qt serves query tile qt: per key tile n, P V(n) and then
+    // QK(n+1), on the items and K/V ring positions the producer walks.  Every
+    // ring use takes two arrivals on k_empty / v_empty: one commit from each
+    // issuer, or two from the one issuer whose tile alone reads that key tile
+    // (Q1's diagonal tile; every key tile of an item without Q1).  An issuer
+    // arrives for a use only after waiting for that use's load, so an arrival
+    // can never count toward the previous phase.
+    const int qt = warp - PAIR_MMA_WARP;
+    if (lane == 0) {
+      const uint32_t sQ = smem_u32(smem + L::Q_OFF + qt * L::TILE);
+      const uint32_t tS = tmem + qt * BN, tO = tmem + 2 * BN + qt * D;
+      int g = 0;   // K/V ring position of the item's key tile 0
+      int cs = 0;  // score tiles so far (s_full / p_half / p_full phase)
+      int uq = 0;  // items so far for this query tile (q_full / o_full / o_empty phase)
+      bool ok = true;
+      for (int r = 0; ok && pair_item(r, nItems, BH, nPair, nQ, it); ++r) {
+        if (qt == 1 && !it.has1) {
+          g += it.nlast + 1;
+          continue;
+        }
+        const int nmax = qt == 0 ? it.nmax0 : it.nmax1;
+        const bool alone_all = !it.has1;  // Q0 alone reads every key tile of the item
+        auto release = [&](uint64_t* empty, int n) {
+          mma_commit(empty);
+          if (alone_all || (qt == 1 && n == it.nlast)) mma_commit(empty);
+        };
+        auto qk = [&](int n) -> bool {
+          const int gi = g + n;
+          if (!mbar_wait(&k_full[gi % L::NS], (gi / L::NS) & 1)) return false;
+          tc_fence_after();
+          issue_qk<D>(tS, sQ, smem_u32(smem + L::K_OFF + (gi % L::NS) * L::TILE));
+          mma_commit(&s_full[qt]);
+          release(&k_empty[gi % L::NS], n);
+          if (n == nmax) mma_commit(&q_empty[qt]);
+          return true;
+        };
+        if (!(ok = mbar_wait(&q_full[qt], uq & 1) && qk(0))) break;
+        for (int n = 0; n <= nmax; ++n, ++cs) {
+          // P V(n) in two halves: keys 0..63 as soon as that half of P is there.
+          const int gi = g + n;
+          const uint32_t sV = smem_u32(smem + L::V_OFF + (gi % L::NS) * L::TILE);
+          const uint32_t ph = cs & 1;
+          if (!(ok = mbar_wait(PAIR_SPLIT_P ? &p_half[qt] : &p_full[qt], ph) &&
+                     mbar_wait(&v_full[gi % L::NS], (gi / L::NS) & 1)))
+            break;
+          // The first P V of an item overwrites O: the epilogue has read the last one.
+          if (n == 0 && uq > 0 && !(ok = mbar_wait(&o_empty[qt], (uq - 1) & 1))) break;
+          tc_fence_after();
+          issue_pv<D>(tO, tS, sV, 0, BN / 32, n == 0);
+          if (!(ok = mbar_wait(&p_full[qt], ph))) break;
+          tc_fence_after();
+          issue_pv<D>(tO, tS, sV, BN / 32, BN / 16, false);
+          release(&v_empty[gi % L::NS], n);
+          if (n == nmax)
+            mma_commit(&o_full[qt]);
+          else if (!(ok = qk(n + 1)))
+            break;
+        }
+        g += it.nlast + 1;
+        ++uq;
+      }
+      // Commits arrive in issue order: once this one has landed, every
+      // barrier arrival of this thread's MMAs has too, and smem may be released.
+      mma_commit(&mma_done[qt]);
+      mbar_wait(&mma_done[qt], 0);
+    }
   } else if (warp == PAIR_MMA_WARP) {
+    // One issuer for both tiles, in the order PV0(n), QK0(n+1), PV1(n),
+    // QK1(n+1); each ring use is released by one commit once both tiles'
+    // products on it have been issued.
     if (lane == 0) {
       const uint32_t sQ0 = smem_u32(smem + L::Q_OFF);
       int g = 0;               // K/V ring position of the item's key tile 0
@@ -412,8 +495,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
       }
       // Commits arrive in issue order: once this one has landed, every
       // barrier arrival of this CTA's MMAs has too, and smem may be released.
-      mma_commit(mma_done);
-      mbar_wait(mma_done, 0);
+      mma_commit(&mma_done[0]);
+      mbar_wait(&mma_done[0], 0);
     }
   } else {
     const int qt = warp >> 2;  // query tile of this warpgroup
@@ -470,7 +553,7 @@ int launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
   const int sms = sm_count();
   if (sms <= 0) return ERR_DEVICE;
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-  kern<<<grid, PAIR_THREADS, L::ALLOC, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(out), BH, T, nQ, nPair,
+  kern<<<grid, PairCfg<PC>::THREADS, L::ALLOC, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(out), BH, T, nQ, nPair,
                                                  static_cast<int>(items), beta, p);
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
