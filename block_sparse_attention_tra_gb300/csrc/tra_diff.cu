@@ -7,14 +7,18 @@
 //
 // Fused: one CTA owns 128 query rows of one (b, h) and runs the two score
 // streams side by side.  Stream t has its own Q_t (resident) and K_t tiles,
-// both streams share each V tile, and both P V products accumulate into ONE
-// TMEM accumulator O: the second stream's weights are multiplied by
-// -clamp(lambda, 0, 1) before they are rounded, so O ends up holding the
-// difference and V is read once for both streams.
-//   warp 8      TMA producer (Q0, Q1 once; K0+K1 and V tiles in rings).
-//   warp 9      MMA issuer: ... PV0(n), QK0(n+1), PV1(n), QK1(n+1) ...
+// both streams share each V tile (loaded once), and stream t accumulates
+// P_t V into its own TMEM accumulator O_t; the store epilogue writes
+// O_0 - clamp(lambda, 0, 1) O_1 from fp32.
+//   warp 8      TMA producer (Q0, Q1 once; K0, K1 and V tiles in rings).
+//   warp 9(+10) MMA issuer(s): per stream ... PV_t(n), QK_t(n+1) ...; at
+//               D=64 with p = 1, 2 each stream has its own issuing warp (one
+//               thread issues only about one tcgen05.mma per ~70 cycles);
+//               otherwise warp 9 serves both streams in turn (at D=128 the
+//               single-stage K1 ring keeps the streams in step anyway, and
+//               two issuers measured slower).
 //   warps 4t..  epilogue of stream t (thread = query row).
-// TMEM: S0 [0,128), S1 [128,256), O [256,256+D).
+// TMEM: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
 //
 // Normalisation does not rewrite q or k: with r(x) = 1 / max(||x||, 1e-12)
 // the normalised score is s_ij r(q_i) r(k_j).  A pre-pass kernel writes r()
@@ -35,9 +39,13 @@ namespace {
 
 using tile::PANEL_BYTES;
 constexpr int BT = tile::ROWS;
-constexpr int DIFF_THREADS = 320;
 constexpr int DIFF_TMA_WARP = 8;
-constexpr int DIFF_MMA_WARP = 9;
+constexpr int DIFF_MMA_WARP = 9;  // first MMA warp (allocates TMEM)
+template <int D, int PC>
+struct DiffCfg {
+  static constexpr int ISSUERS = (D == 64 && (PC == POW_ONE || PC == POW_TWO)) ? 2 : 1;
+  static constexpr int THREADS = 256 + 32 + 32 * ISSUERS;
+};
 
 template <int D>
 struct DiffLayout {
@@ -54,9 +62,9 @@ struct DiffLayout {
   static constexpr int V_OFF = K1_OFF + NSK1 * TILE;
   static constexpr int RK_OFF = V_OFF + NSV * TILE;
   static constexpr int BAR_OFF = RK_OFF + NSR * 2 * RK_BYTES;
-  // q_full | k0 full/empty | k1 full/empty | v full/empty | rk full/empty | s_full[2] | p_full[2] | o_full |
-  // mma_done
-  static constexpr int NBAR = 1 + 2 * (NSK0 + NSK1 + NSV + NSR) + 6;
+  // q_full | k0 full/empty | k1 full/empty | v full/empty | rk full/empty | s_full[2] | p_full[2] | o_full[2] |
+  // mma_done[2]
+  static constexpr int NBAR = 1 + 2 * (NSK0 + NSK1 + NSV + NSR) + 8;
   static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
   static constexpr int ALLOC = TPTR_OFF + 16;  // the dynamic smem base is 1024-byte aligned
   static_assert(ALLOC <= 232448, "shared memory budget");
@@ -104,13 +112,13 @@ __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* 
   if (lane == 0) inv[gw] = 1.0f / fmaxf(sqrtf(acc), 1e-12f);
 }
 
-// 32 scores of stream t -> 16 packed weights (scaled by `wscale` when
-// SCALE_W), over the consumed score columns.  With NORM the scores are first
-// multiplied by rq * rk[col] (the normalisation of row and key).
+// 32 scores of stream t -> 16 packed weights over the consumed score
+// columns.  With NORM the scores are first multiplied by rq * rk[col] (the
+// normalisation of row and key).
 // DIAG (compile time): the tile holds the diagonal, mask keys after the row.
-template <int PC, bool NORM, bool SCALE_W, bool DIAG>
+template <int PC, bool NORM, bool DIAG>
 __device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t tS, int c0, const PowParams& wp,
-                                             float rq, const float (&rk)[32], uint32_t wscale, int key0, int row) {
+                                             float rq, const float (&rk)[32], int key0, int row) {
   uint32_t pk[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
@@ -120,7 +128,6 @@ __device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t t
       s1 *= rq * rk[2 * e + 1];
     }
     uint32_t w = weights2<PC>(s0, s1, wp);
-    if constexpr (SCALE_W) w = mul_bf16x2(w, wscale);
     if constexpr (DIAG) {
       const int key = key0 + c0 + 2 * e;
       if (key > row) w = 0u;
@@ -132,7 +139,7 @@ __device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t t
 }
 
 template <int D, int PC, bool NORM>
-__global__ void __launch_bounds__(DIFF_THREADS, 1)
+__global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
     tra_diff_kernel(const __grid_constant__ CUtensorMap tmQ0, const __grid_constant__ CUtensorMap tmQ1,
                     const __grid_constant__ CUtensorMap tmK0, const __grid_constant__ CUtensorMap tmK1,
                     const __grid_constant__ CUtensorMap tmV, const float* __restrict__ inv_norm,
@@ -160,19 +167,20 @@ __global__ void __launch_bounds__(DIFF_THREADS, 1)
   b1 += 2 * L::NSR;
   uint64_t* s_full = b1;  // [2]
   uint64_t* p_full = s_full + 2;                                    // [2]
-  uint64_t* o_full = p_full + 2;
-  uint64_t* mma_done = o_full + 1;
+  uint64_t* o_full = p_full + 2;                                    // [2]
+  uint64_t* mma_done = o_full + 2;                                  // [2]
   uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = nQ - 1 - static_cast<int>(blockIdx.x) / BH;  // longest first
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int nmax = m;
-  constexpr uint32_t O_COL = 2 * BT;
+  constexpr uint32_t O_COL = 2 * BT;  // O0; O1 at O_COL + D
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < 2 * (L::NSK0 + L::NSK1 + L::NSV); ++i) mbar_init(bars + 1 + i, 1);
+    for (int i = 0; i < L::NSV; ++i) mbar_init(&rv.empty[i], 2);  // released once per stream
     for (int i = 0; i < L::NSR; ++i) {
       mbar_init(&rr.full[i], 1);
       mbar_init(&rr.empty[i], 8);  // four warps of each stream's epilogue
@@ -181,8 +189,10 @@ __global__ void __launch_bounds__(DIFF_THREADS, 1)
       mbar_init(&s_full[b], 1);
       mbar_init(&p_full[b], 4);
     }
-    mbar_init(o_full, 1);
-    mbar_init(mma_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&o_full[b], 1);
+      mbar_init(&mma_done[b], 1);
+    }
     fence_barrier_init();
   }
   if (warp == DIFF_MMA_WARP) {
@@ -238,7 +248,13 @@ __global__ void __launch_bounds__(DIFF_THREADS, 1)
         }
       }
     }
-  } else if (warp == DIFF_MMA_WARP) {
+  } else if (warp >= DIFF_MMA_WARP) {
+    // Issuer j serves streams T0 .. T0 + NT - 1, per key tile n in the order
+    // PV_t(n), QK_t(n+1).  Each V use is released once per stream, after the
+    // stream's P V on it (and so after its wait for that V load).
+    constexpr int NT = 3 - DiffCfg<D, PC>::ISSUERS;
+    const int j = warp - DIFF_MMA_WARP;
+    const int T0 = NT == 1 ? j : 0;
     if (lane == 0) {
       const uint32_t sQ = smem_u32(smem + L::Q_OFF);
       // QKt(n): S_t = Q_t K_t(n)^T, then release K_t(n).
@@ -251,26 +267,30 @@ __global__ void __launch_bounds__(DIFF_THREADS, 1)
         mma_commit(&R.empty[R.stage(n)]);
         return true;
       };
-      // PVt(n): O += P_t V(n) (stream 1's P already carries -lambda).
+      // PVt(n): O_t += P_t V(n), then release V(n) for this stream.
       auto pv = [&](int t, int n) -> bool {
         if (!mbar_wait(&p_full[t], n & 1) || !mbar_wait(&rv.full[rv.stage(n)], rv.phase(n))) return false;
         tc_fence_after();
         const uint32_t sV = smem_u32(smem + rv.off + rv.stage(n) * L::TILE);
-        tile::mma_tmem_a<D>(tmem + O_COL, tmem + t * BT, sV, 0, BT / 16, t == 0 && n == 0);
+        tile::mma_tmem_a<D>(tmem + O_COL + t * D, tmem + t * BT, sV, 0, BT / 16, n == 0);
+        mma_commit(&rv.empty[rv.stage(n)]);
         return true;
       };
-      bool ok = mbar_wait(q_full, 0) && qk(0, 0) && qk(1, 0);
+      bool ok = mbar_wait(q_full, 0);
+#pragma unroll
+      for (int i = 0; i < NT; ++i) ok = ok && qk(T0 + i, 0);
       for (int n = 0; n <= nmax && ok; ++n) {
-        const int n1 = n + 1;
-        if (!(ok = pv(0, n))) break;
-        if (n1 <= nmax && !(ok = qk(0, n1))) break;
-        if (!(ok = pv(1, n))) break;
-        mma_commit(&rv.empty[rv.stage(n)]);
-        if (n1 <= nmax && !(ok = qk(1, n1))) break;
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+          if (!(ok = pv(T0 + i, n) && (n == nmax || qk(T0 + i, n + 1)))) break;
+        }
       }
-      if (ok) mma_commit(o_full);
-      mma_commit(mma_done);
-      mbar_wait(mma_done, 0);
+      if (ok) {
+#pragma unroll
+        for (int i = 0; i < NT; ++i) mma_commit(&o_full[T0 + i]);
+      }
+      mma_commit(&mma_done[j]);
+      mbar_wait(&mma_done[j], 0);
     }
   } else {
     const int t = warp >> 2, wq = warp & 3;
@@ -280,7 +300,6 @@ __global__ void __launch_bounds__(DIFF_THREADS, 1)
     const uint32_t tS = lane_base + t * BT;
     const PowParams wp = pow_params(tau, p);
     const float lc = fminf(fmaxf(lam, 0.0f), 1.0f);
-    const uint32_t wscale = pack_bf16x2(-lc, -lc);
     // inv_norm: [q1 | k1 | q2 | k2] x [B*H] x [Tp], zero past T
     const float rq = NORM ? inv_norm[(static_cast<long long>(t == 0 ? 0 : 2) * BH + bh) * Tp + row] : 1.0f;
     bool ok = true;
@@ -308,17 +327,10 @@ __global__ void __launch_bounds__(DIFF_THREADS, 1)
         uint32_t sv[32];
         tmem_ld32(tS + 32 * c, sv);
         tmem_wait_ld();
-        if (t == 0) {
-          if (diag)
-            diff_quarter<PC, NORM, false, true>(sv, tS, 32 * c, wp, rq, rk, wscale, n * BT, row);
-          else
-            diff_quarter<PC, NORM, false, false>(sv, tS, 32 * c, wp, rq, rk, wscale, n * BT, row);
-        } else {
-          if (diag)
-            diff_quarter<PC, NORM, true, true>(sv, tS, 32 * c, wp, rq, rk, wscale, n * BT, row);
-          else
-            diff_quarter<PC, NORM, true, false>(sv, tS, 32 * c, wp, rq, rk, wscale, n * BT, row);
-        }
+        if (diag)
+          diff_quarter<PC, NORM, true>(sv, tS, 32 * c, wp, rq, rk, n * BT, row);
+        else
+          diff_quarter<PC, NORM, false>(sv, tS, 32 * c, wp, rq, rk, n * BT, row);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -328,10 +340,27 @@ __global__ void __launch_bounds__(DIFF_THREADS, 1)
         if constexpr (NORM) mbar_arrive(&rr.empty[rr.stage(n)]);  // done with the key factors
       }
     }
-    if (ok && mbar_wait(o_full, 0)) {
+    if (ok && mbar_wait(&o_full[0], 0) && mbar_wait(&o_full[1], 0)) {
       tc_fence_after();
       __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * T + row) * D;
-      for (int c = t; c < D / 32; c += 2) tile::store_row_chunk(lane_base + O_COL, c, orow, row < T);
+      // out = O0 - clamp(lambda, 0, 1) O1; stream t's warpgroup writes every other 32-column chunk.
+      for (int c = t; c < D / 32; c += 2) {
+        uint32_t o0[32], o1[32];
+        tmem_ld32(lane_base + O_COL + c * 32, o0);
+        tmem_ld32(lane_base + O_COL + D + c * 32, o1);
+        tmem_wait_ld();
+        if (row < T) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = fmaf(-lc, __uint_as_float(o1[8 * q + e]), __uint_as_float(o0[8 * q + e]));
+            dst[q] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                                pack_bf16x2(f[6], f[7]));
+          }
+        }
+      }
     }
   }
 
@@ -354,7 +383,7 @@ int launch_diff_kernel(const CUtensorMap* maps, const float* inv, void* out, int
   const int nQ = (T + BT - 1) / BT;
   const long long grid = static_cast<long long>(nQ) * BH;
   if (grid > 0x7fffffffLL) return ERR_SHAPE;
-  kern<<<static_cast<unsigned>(grid), DIFF_THREADS, L::ALLOC, stream>>>(
+  kern<<<static_cast<unsigned>(grid), DiffCfg<D, PC>::THREADS, L::ALLOC, stream>>>(
       maps[0], maps[1], maps[2], maps[3], maps[4], inv, static_cast<__nv_bfloat16*>(out), BH, T, nQ, beta, p, lam);
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
