@@ -22,8 +22,17 @@
 // S = Q_m K_n^T and dP = dO_m V_n^T; the epilogue (thread = query row) forms
 // dA; then dQ += dA K_n.  TMEM: S [0,128), dP [128,256), dQ [256,256+D).
 //
-// Both: warp 4 = TMA producer, warp 5 = single-thread MMA issuer, warps 0-3 =
-// epilogue; every wait is bounded.
+// Both kernels produce each 128 x 128 score (and gradient) tile in two
+// 64-column halves h that behave like two tiles: the epilogue turns half h
+// into bf16 while the other half's products run, and the products that read
+// half h (dV, dK; dQ) start as soon as it is done.  Two threads issue the
+// MMAs (one thread sustains only about one tcgen05.mma per ~70 cycles):
+//   dK/dV: warp 5 issues S^T_h and dV (its A operand, W^T, lives in S^T's
+//          columns), warp 6 issues dP^T_h and dK (dA^T in dP^T's columns);
+//   dQ:    warp 5 issues S_h and dQ (dA is written over S), warp 6 dP_h.
+// Each issuer's own MMAs overwrite a half only after the products that read
+// it (same thread, in order).  Warp 4 = TMA producer, warps 0-3 = epilogue;
+// every wait is bounded.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc_tile.cuh"
@@ -33,10 +42,10 @@ namespace {
 
 using tile::PANEL_BYTES;
 constexpr int BT = tile::ROWS;  // 128 rows per query tile and per key tile
-constexpr int BWD_THREADS = 192;
+constexpr int BWD_THREADS = 224;
 constexpr int EPI_WARPS = 4;
 constexpr int TMA_WARP = 4;
-constexpr int MMA_WARP = 5;
+constexpr int MMA_WARP = 5;  // first of the two MMA-issuing warps (allocates TMEM)
 constexpr uint32_t TMEM_COLS = 512;
 
 __device__ __forceinline__ float ex2a(float x) {
@@ -49,7 +58,6 @@ __device__ __forceinline__ float lg2a(float x) {
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_WARPS * 32)); }
 
 // ReLU(x)^p and its derivative (0 for x <= 0).
 template <int PC>
@@ -77,14 +85,14 @@ struct BwdLayout {
   static constexpr int RING_OFF = 2 * TILE;
   static constexpr int TAU_OFF = RING_OFF + NS * 2 * TILE;  // float[2][128]
   static constexpr int BAR_OFF = TAU_OFF + 2 * BT * 4;
-  // res_full | ring_full[NS] | ring_empty[NS] | s_full | p_full | acc_full | mma_done
-  static constexpr int NBAR = 1 + 2 * NS + 4;
+  // res_full | ring_full[NS] | ring_empty[NS] | s_full[2] | p_full[2] | acc_full | mma_done[2] | tau_full[2]
+  static constexpr int NBAR = 1 + 2 * NS + 9;
   static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
   static constexpr int ALLOC = TPTR_OFF + 16 + 1024;
 };
 
 struct BwdBars {
-  uint64_t *res_full, *ring_full, *ring_empty, *s_full, *p_full, *acc_full, *mma_done;
+  uint64_t *res_full, *ring_full, *ring_empty, *s_full, *p_full, *acc_full, *mma_done, *tau_full;
 };
 
 template <int D>
@@ -95,26 +103,30 @@ __device__ __forceinline__ BwdBars bwd_bars(uint8_t* smem) {
   r.res_full = b;
   r.ring_full = b + 1;
   r.ring_empty = r.ring_full + L::NS;
-  r.s_full = r.ring_empty + L::NS;
-  r.p_full = r.s_full + 1;
-  r.acc_full = r.p_full + 1;
-  r.mma_done = r.acc_full + 1;
+  r.s_full = r.ring_empty + L::NS;  // [2], per half
+  r.p_full = r.s_full + 2;          // [2], per half
+  r.acc_full = r.p_full + 2;
+  r.mma_done = r.acc_full + 1;      // [2], per issuer
+  r.tau_full = r.mma_done + 2;      // [2], per tau buffer
   return r;
 }
 
 template <int D>
-__device__ __forceinline__ void bwd_setup(uint8_t* smem, const BwdBars& B, uint32_t* tptr, int warp) {
+__device__ __forceinline__ void bwd_setup(uint8_t* smem, const BwdBars& B, uint32_t* tptr, int warp, int acc_count) {
   using L = BwdLayout<D>;
   if (threadIdx.x == 0) {
     mbar_init(B.res_full, 1);
     for (int s = 0; s < L::NS; ++s) {
       mbar_init(&B.ring_full[s], 1);
-      mbar_init(&B.ring_empty[s], 1);
+      mbar_init(&B.ring_empty[s], 2);  // one release per issuer
     }
-    mbar_init(B.s_full, 1);
-    mbar_init(B.p_full, EPI_WARPS);
-    mbar_init(B.acc_full, 1);
-    mbar_init(B.mma_done, 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&B.s_full[h], 2);  // both issuers' products of half h
+      mbar_init(&B.p_full[h], EPI_WARPS);
+      mbar_init(&B.mma_done[h], 1);
+      mbar_init(&B.tau_full[h], EPI_WARPS);
+    }
+    mbar_init(B.acc_full, acc_count);
     fence_barrier_init();
   }
   if (warp == MMA_WARP) {
@@ -133,6 +145,21 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem, int warp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// C_tmem[128 x 64] = A[128 x D] B_h[64 x D]^T: the score half h of a tile,
+// B_h being rows 64h .. 64h+63 of a K-major 128-row smem tile (8 KB into
+// each 128-byte-swizzled panel, a whole number of swizzle atoms).
+template <int D>
+__device__ __forceinline__ void mma_abt_half(uint32_t tC, uint32_t sA, uint32_t sB, int h) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(BT, 64, 0, 0);
+  const uint32_t sBh = sB + static_cast<uint32_t>(h) * 64u * 128u;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * PANEL_BYTES + (kk & 3) * 32;
+    mma_ss(tC, smem_desc_sw128(sA + off, 16, 1024), smem_desc_sw128(sBh + off, 16, 1024), IDESC,
+           kk > 0 ? 1u : 0u);
   }
 }
 
@@ -188,74 +215,102 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const int nq = nT - n;  // query tiles m = n .. nT-1
   constexpr uint32_t ST = 0, DPT = BT, DV = 2 * BT, DK = 2 * BT + D;
 
-  bwd_setup<D>(smem, B, tptr, warp);
+  bwd_setup<D>(smem, B, tptr, warp, 2);
   const uint32_t tmem = *tptr;
 
   if (warp == TMA_WARP) {
     if (lane == 0) bwd_produce<D>(smem, B, &tmK, &tmV, n * BT, &tmQ, &tmDO, n, nq, bh);
-  } else if (warp == MMA_WARP) {
+  } else if (warp == MMA_WARP || warp == MMA_WARP + 1) {
+    // Issuer X (warp 5): S^T_h = K_n Q_m[h]^T and dV += W^T_h dO_m[h];
+    // issuer Y (warp 6): dP^T_h = V_n dO_m[h]^T and dK += dA^T_h Q_m[h].
+    // Per query tile j: acc(j, 0), score(j+1, 0), acc(j, 1), score(j+1, 1).
+    const int is = warp - MMA_WARP;
     if (lane == 0) {
-      const uint32_t sK = smem_u32(smem + L::RES_OFF), sV = sK + L::TILE;
-      bool ok = mbar_wait(B.res_full, 0);
+      const uint32_t sRes = smem_u32(smem + L::RES_OFF) + (is == 0 ? 0u : static_cast<uint32_t>(L::TILE));
+      const uint32_t tScore = tmem + (is == 0 ? ST : DPT), tAcc = tmem + (is == 0 ? DV : DK);
+      auto slot = [&](int j) { return smem_u32(smem + L::RING_OFF + (j % L::NS) * 2 * L::TILE); };  // Q_j | dO_j
+      auto score = [&](int j, int h) {
+        mma_abt_half<D>(tScore + 64 * h, sRes, slot(j) + (is == 0 ? 0u : static_cast<uint32_t>(L::TILE)), h);
+        mma_commit(&B.s_full[h]);
+      };
+      auto acc = [&](int j, int h) {
+        tile::mma_tmem_a<D>(tAcc, tScore + 32 * h, slot(j) + (is == 0 ? static_cast<uint32_t>(L::TILE) : 0u),
+                            4 * h, 4 * h + 4, j == 0 && h == 0);
+      };
+      bool ok = mbar_wait(B.res_full, 0) && mbar_wait(&B.ring_full[0], 0);
+      if (ok) {
+        tc_fence_after();
+        score(0, 0);
+        score(0, 1);
+      }
       for (int j = 0; j < nq && ok; ++j) {
-        const int s = j % L::NS;
-        const uint32_t sQ = smem_u32(smem + L::RING_OFF + s * 2 * L::TILE), sDO = sQ + L::TILE;
-        if (!(ok = mbar_wait(&B.ring_full[s], (j / L::NS) & 1))) break;
-        tc_fence_after();
-        tile::mma_abt<D>(tmem + ST, sK, sQ);   // S^T  = K_n Q_m^T
-        tile::mma_abt<D>(tmem + DPT, sV, sDO); // dP^T = V_n dO_m^T
-        mma_commit(B.s_full);
-        if (!(ok = mbar_wait(B.p_full, j & 1))) break;
-        tc_fence_after();
-        tile::mma_tmem_a<D>(tmem + DV, tmem + ST, sDO, 0, BT / 16, j == 0);  // dV += W^T dO_m
-        tile::mma_tmem_a<D>(tmem + DK, tmem + DPT, sQ, 0, BT / 16, j == 0);  // dK += dA^T Q_m
-        mma_commit(&B.ring_empty[s]);
+        const bool more = j + 1 < nq;
+        for (int h = 0; h < 2; ++h) {
+          if (!(ok = mbar_wait(&B.p_full[h], j & 1))) break;
+          tc_fence_after();
+          acc(j, h);
+          if (h == 1) mma_commit(&B.ring_empty[j % L::NS]);  // Q_j, dO_j read by every product issued so far
+          if (more) {
+            if (h == 0 && !(ok = mbar_wait(&B.ring_full[(j + 1) % L::NS], ((j + 1) / L::NS) & 1))) break;
+            tc_fence_after();
+            score(j + 1, h);
+          }
+        }
       }
       if (ok) mma_commit(B.acc_full);
-      mma_commit(B.mma_done);
-      mbar_wait(B.mma_done, 0);
+      mma_commit(&B.mma_done[is]);
+      mbar_wait(&B.mma_done[is], 0);
     }
-  } else {
+  } else if (warp < EPI_WARPS) {
     const int r = warp * 32 + lane;  // key row within the tile
     const int key = n * BT + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     bool ok = true;
     for (int j = 0; j < nq && ok; ++j) {
       const int m = n + j;
+      // Double-buffered tau table: a warp writes buffer j&1 for step j only
+      // after every warp arrived for step j-1 (so all have finished step j-2,
+      // the buffer's previous user); the barrier wait is bounded.
       float* tau_m = tau_s + (j & 1) * BT;
       tau_m[r] = tile::tau_of_row(m * BT + r, beta, D);  // tau of query column r
-      epi_sync();
-      if (!(ok = mbar_wait(B.s_full, j & 1))) break;
-      tc_fence_after();
-      const bool diag = (m == n);
-#pragma unroll 1
-      for (int c = 0; c < BT / 32; ++c) {
-        uint32_t sv[32], dp[32];
-        tmem_ld32(lane_base + ST + 32 * c, sv);
-        tmem_ld32(lane_base + DPT + 32 * c, dp);
-        tmem_wait_ld();
-        uint32_t wpk[16], apk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float w0, g0, w1, g1;
-          const int i0 = 32 * c + 2 * e;  // query column within the tile
-          weight_and_grad<PC>(__uint_as_float(sv[2 * e]) - tau_m[i0], p, w0, g0);
-          weight_and_grad<PC>(__uint_as_float(sv[2 * e + 1]) - tau_m[i0 + 1], p, w1, g1);
-          float a0 = __uint_as_float(dp[2 * e]) * g0, a1 = __uint_as_float(dp[2 * e + 1]) * g1;
-          if (diag) {  // causal: key r <= query column
-            if (i0 < r) w0 = a0 = 0.0f;
-            if (i0 + 1 < r) w1 = a1 = 0.0f;
-          }
-          wpk[e] = pack_bf16x2(w0, w1);
-          apk[e] = pack_bf16x2(a0, a1);
-        }
-        tmem_st16(lane_base + ST + 16 * c, wpk);
-        tmem_st16(lane_base + DPT + 16 * c, apk);
-      }
-      tmem_wait_st();
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(B.p_full);
+      if (lane == 0) mbar_arrive(&B.tau_full[j & 1]);
+      if (!(ok = mbar_wait(&B.tau_full[j & 1], (j >> 1) & 1))) break;
+      const bool diag = (m == n);
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = mbar_wait(&B.s_full[h], j & 1))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 2 * h; c < 2 * h + 2; ++c) {
+          uint32_t sv[32], dp[32];
+          tmem_ld32(lane_base + ST + 32 * c, sv);
+          tmem_ld32(lane_base + DPT + 32 * c, dp);
+          tmem_wait_ld();
+          uint32_t wpk[16], apk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float w0, g0, w1, g1;
+            const int i0 = 32 * c + 2 * e;  // query column within the tile
+            weight_and_grad<PC>(__uint_as_float(sv[2 * e]) - tau_m[i0], p, w0, g0);
+            weight_and_grad<PC>(__uint_as_float(sv[2 * e + 1]) - tau_m[i0 + 1], p, w1, g1);
+            float a0 = __uint_as_float(dp[2 * e]) * g0, a1 = __uint_as_float(dp[2 * e + 1]) * g1;
+            if (diag) {  // causal: key r <= query column
+              if (i0 < r) w0 = a0 = 0.0f;
+              if (i0 + 1 < r) w1 = a1 = 0.0f;
+            }
+            wpk[e] = pack_bf16x2(w0, w1);
+            apk[e] = pack_bf16x2(a0, a1);
+          }
+          // half h packs into its own first 32 columns (already-consumed scores)
+          const int pc = 64 * h + 16 * (c - 2 * h);
+          tmem_st16(lane_base + ST + pc, wpk);
+          tmem_st16(lane_base + DPT + pc, apk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.p_full[h]);
+      }
     }
     if (ok && mbar_wait(B.acc_full, 0)) {
       tc_fence_after();
@@ -287,68 +342,86 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const int bh = static_cast<int>(blockIdx.x) % BH;
   constexpr uint32_t S = 0, DP = BT, DQ = 2 * BT;
 
-  bwd_setup<D>(smem, B, tptr, warp);
+  bwd_setup<D>(smem, B, tptr, warp, 1);
   const uint32_t tmem = *tptr;
 
   if (warp == TMA_WARP) {
     if (lane == 0) bwd_produce<D>(smem, B, &tmQ, &tmDO, m * BT, &tmK, &tmV, 0, m + 1, bh);
-  } else if (warp == MMA_WARP) {
+  } else if (warp == MMA_WARP || warp == MMA_WARP + 1) {
+    // Issuer X (warp 5): S_h = Q_m K_n[h]^T and dQ += dA_h K_n[h] (dA over S);
+    // issuer Y (warp 6): dP_h = dO_m V_n[h]^T, re-issued for the next key tile
+    // once the epilogue has read half h.
+    const int is = warp - MMA_WARP;
     if (lane == 0) {
-      const uint32_t sQ = smem_u32(smem + L::RES_OFF), sDO = sQ + L::TILE;
-      bool ok = mbar_wait(B.res_full, 0);
-      for (int n = 0; n <= m && ok; ++n) {
-        const int s = n % L::NS;
-        const uint32_t sK = smem_u32(smem + L::RING_OFF + s * 2 * L::TILE), sV = sK + L::TILE;
-        if (!(ok = mbar_wait(&B.ring_full[s], (n / L::NS) & 1))) break;
+      const uint32_t sRes = smem_u32(smem + L::RES_OFF) + (is == 0 ? 0u : static_cast<uint32_t>(L::TILE));
+      const uint32_t tScore = tmem + (is == 0 ? S : DP);
+      auto slot = [&](int j) { return smem_u32(smem + L::RING_OFF + (j % L::NS) * 2 * L::TILE); };  // K_j | V_j
+      auto score = [&](int j, int h) {
+        mma_abt_half<D>(tScore + 64 * h, sRes, slot(j) + (is == 0 ? 0u : static_cast<uint32_t>(L::TILE)), h);
+        mma_commit(&B.s_full[h]);
+      };
+      bool ok = mbar_wait(B.res_full, 0) && mbar_wait(&B.ring_full[0], 0);
+      if (ok) {
         tc_fence_after();
-        tile::mma_abt<D>(tmem + S, sQ, sK);    // S  = Q_m K_n^T
-        tile::mma_abt<D>(tmem + DP, sDO, sV);  // dP = dO_m V_n^T
-        mma_commit(B.s_full);
-        if (!(ok = mbar_wait(B.p_full, n & 1))) break;
-        tc_fence_after();
-        tile::mma_tmem_a<D>(tmem + DQ, tmem + S, sK, 0, BT / 16, n == 0);  // dQ += dA K_n
-        mma_commit(&B.ring_empty[s]);
+        score(0, 0);
+        score(0, 1);
       }
-      if (ok) mma_commit(B.acc_full);
-      mma_commit(B.mma_done);
-      mbar_wait(B.mma_done, 0);
+      for (int j = 0; j <= m && ok; ++j) {
+        const bool more = j < m;
+        for (int h = 0; h < 2; ++h) {
+          if (!(ok = mbar_wait(&B.p_full[h], j & 1))) break;
+          tc_fence_after();
+          if (is == 0) tile::mma_tmem_a<D>(tmem + DQ, tmem + S + 32 * h, slot(j), 4 * h, 4 * h + 4, j == 0 && h == 0);
+          if (h == 1) mma_commit(&B.ring_empty[j % L::NS]);  // K_j, V_j read by every product issued so far
+          if (more) {
+            if (h == 0 && !(ok = mbar_wait(&B.ring_full[(j + 1) % L::NS], ((j + 1) / L::NS) & 1))) break;
+            tc_fence_after();
+            score(j + 1, h);
+          }
+        }
+      }
+      if (ok && is == 0) mma_commit(B.acc_full);
+      mma_commit(&B.mma_done[is]);
+      mbar_wait(&B.mma_done[is], 0);
     }
-  } else {
+  } else if (warp < EPI_WARPS) {
     const int r = warp * 32 + lane;
     const int row = m * BT + r;
     const float tau = tile::tau_of_row(row, beta, D);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     bool ok = true;
     for (int n = 0; n <= m && ok; ++n) {
-      if (!(ok = mbar_wait(B.s_full, n & 1))) break;
-      tc_fence_after();
       const bool diag = (n == m);
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = mbar_wait(&B.s_full[h], n & 1))) break;
+        tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < BT / 32; ++c) {
-        uint32_t sv[32], dp[32];
-        tmem_ld32(lane_base + S + 32 * c, sv);
-        tmem_ld32(lane_base + DP + 32 * c, dp);
-        tmem_wait_ld();
-        uint32_t apk[16];
+        for (int c = 2 * h; c < 2 * h + 2; ++c) {
+          uint32_t sv[32], dp[32];
+          tmem_ld32(lane_base + S + 32 * c, sv);
+          tmem_ld32(lane_base + DP + 32 * c, dp);
+          tmem_wait_ld();
+          uint32_t apk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float w0, g0, w1, g1;
-          weight_and_grad<PC>(__uint_as_float(sv[2 * e]) - tau, p, w0, g0);
-          weight_and_grad<PC>(__uint_as_float(sv[2 * e + 1]) - tau, p, w1, g1);
-          float a0 = __uint_as_float(dp[2 * e]) * g0, a1 = __uint_as_float(dp[2 * e + 1]) * g1;
-          if (diag) {  // causal: key column <= query row r
-            const int kc = 32 * c + 2 * e;
-            if (kc > r) a0 = 0.0f;
-            if (kc + 1 > r) a1 = 0.0f;
+          for (int e = 0; e < 16; ++e) {
+            float w0, g0, w1, g1;
+            weight_and_grad<PC>(__uint_as_float(sv[2 * e]) - tau, p, w0, g0);
+            weight_and_grad<PC>(__uint_as_float(sv[2 * e + 1]) - tau, p, w1, g1);
+            float a0 = __uint_as_float(dp[2 * e]) * g0, a1 = __uint_as_float(dp[2 * e + 1]) * g1;
+            if (diag) {  // causal: key column <= query row r
+              const int kc = 32 * c + 2 * e;
+              if (kc > r) a0 = 0.0f;
+              if (kc + 1 > r) a1 = 0.0f;
+            }
+            apk[e] = pack_bf16x2(a0, a1);
           }
-          apk[e] = pack_bf16x2(a0, a1);
+          tmem_st16(lane_base + S + 64 * h + 16 * (c - 2 * h), apk);
         }
-        tmem_st16(lane_base + S + 16 * c, apk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.p_full[h]);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(B.p_full);
     }
     if (ok && mbar_wait(B.acc_full, 0)) {
       tc_fence_after();

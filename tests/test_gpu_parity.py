@@ -89,13 +89,18 @@ def test_tra_small_full_output(B, H, T, D, beta, p, dtype):
 # The bf16 kernel is persistent (one CTA per SM walking a list of items).
 # Hundreds of heads with short sequences give every CTA several items of one
 # to three key tiles, so the handoffs between items (Q buffer, O accumulator,
-# barrier phases across items) run many times per CTA.
+# barrier phases across items) run many times per CTA.  For p = 1 and 2 each
+# query tile has its own MMA-issuing thread; items without a second tile (odd
+# tile count) and the second tile's diagonal key tile are the ring uses that
+# one issuer releases twice.
 TRA_MANY_ITEMS = [
     # (B, H, T, D, beta, p)
     (4, 100, 256, 64, 2.0, 1.5),    # general power
     (2, 100, 384, 128, 1.0, 1.5),   # general power, odd tile count (items without a second tile)
     (4, 100, 256, 64, 1.0, 2.0),    # p = 2
     (2, 100, 384, 128, 1.0, 2.0),   # p = 2, odd tile count
+    (2, 100, 384, 64, 1.0, 1.0),    # p = 1, D = 64, odd tile count
+    (4, 64, 200, 128, 0.5, 1.0),    # p = 1, ragged two-tile items
     (3, 70, 130, 64, 0.5, 0.25),    # p < 1, ragged two-tile items
 ]
 
