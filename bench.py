@@ -228,6 +228,27 @@ def roofline_for(w, ms_per_launch, pk, sustained: bool, fsa: bool = False):
     return r
 
 
+# MUFU results per clock per SM on GB300 (sm_103a), measured with a one-CTA-
+# per-SM throughput loop: lg2.approx.f32 16, ex2.approx.f32 32, sqrt.approx.f32 16.
+MUFU_PER_CLK = {"lg2": 16.0, "ex2": 32.0, "sqrt": 16.0}
+
+
+def sfu_roofline(w, ms_per_launch, sm_mhz, ops):
+    """Special-function roofline of a TRA power class that evaluates `ops`
+    (MUFU operation names) once per causal pair: the time the MUFU units of
+    all SMs need at the sampled SM clock, as a fraction of the measured time."""
+    if not sm_mhz:
+        return None
+    import torch
+
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    pairs = w.B * w.H * (w.T * (w.T + 1) // 2)
+    clk_per_pair = sum(1.0 / MUFU_PER_CLK[o] for o in ops)
+    min_ms = pairs * clk_per_pair / sms / (sm_mhz * 1e6) * 1e3
+    return {"bound": "sfu", "ops_per_pair": list(ops), "results_per_clk_per_sm": {o: MUFU_PER_CLK[o] for o in ops},
+            "pairs": pairs, "sm_mhz": sm_mhz, "min_ms": round(min_ms, 4), "frac": round(min_ms / ms_per_launch, 4)}
+
+
 def time_resident(fn, steps, warmup, world, flush=None, soak_s=0.0):
     """Device time (ms) of `steps` launches with inputs resident.  Without a
     flush the launches run back to back between two events; with a flush each
@@ -360,6 +381,7 @@ def run_ours(args):
             flush_buf.fill_(1.0)
 
         sec = []
+        sfu_clock = None
         for name in SECONDARY:
             del dev, out
             torch.cuda.empty_cache()
@@ -373,7 +395,7 @@ def run_ours(args):
             # TRA inputs larger than L2 need no flush (back-to-back launches, as
             # for the headline); the NSA gather's unique K/V fits L2, so those
             # launches are flushed.
-            big = isinstance(w2, workloads.TraWorkload) and w2.io_bytes > 2 * L2_BYTES
+            big = isinstance(w2, workloads.TraWorkload) and w2.io_bytes > L2_BYTES
             with ClockSampler(device.index) as cs2:
                 t = time_resident(f, n, 3, world, flush=None if big else flush, soak_s=min(args.clock_soak, 1.0))
             t = reduce_max(t, world, device) / n
@@ -382,6 +404,10 @@ def run_ours(args):
                      "roofline": roofline_for(w2, t, pk, sustained=False),
                      "l2": ("no flush: inputs %d MB > 129 MB L2" % (w2.io_bytes // 2**20)) if big
                      else "flushed between launches"}
+            if isinstance(w2, workloads.TraWorkload) and w2.dtype == "bf16" and w2.p not in (1.0, 2.0):
+                # general power: one lg2 and one ex2 per causal pair (exp2(p log2 x))
+                entry["sfu"] = sfu_roofline(w2, t, entry["clocks"]["sm_mhz"], ("lg2", "ex2"))
+                sfu_clock = entry["clocks"]["sm_mhz"]
             sec.append(entry)
             if isinstance(w2, workloads.NsaWorkload) and w2.block_size == 64 and w2.D in (64, 128):
                 # The same selection through the block-outer split-K form
@@ -431,6 +457,9 @@ def run_ours(args):
                         "tflops": round(flops * world / (t * 1e-3) / 1e12, 3),
                         "frac_of_bf16_peak": round(flops / (t * 1e-3) / 1e12 / pk["bf16_tflops"], 4),
                         "algorithmic_flops": flops, "l2": "no flush: inputs and outputs > 129 MB L2"})
+            if label.startswith("tra_forward(sqrt_half_powers)"):
+                # p = 1.5 as x sqrt(x): one sqrt per causal pair (clock of the exp/log line's run)
+                sec[-1]["sfu"] = sfu_roofline(w3, t, sfu_clock, ("sqrt",))
         result["secondary"] = sec
 
     if args.cpu_baseline and rank == 0 and world == 1:

@@ -80,36 +80,70 @@ struct Ring {
 };
 
 // 1 / max(||row||_2, 1e-12) for every row of the four inputs into
-// inv[which][bh][Tp] (0 for the padding rows t >= T); one warp per row, fp32
-// accumulation of the squared bf16 elements.
+// inv[which][bh][Tp] (0 for the padding rows t >= T).  Eight threads per row,
+// eight rows per warp and pass (two groups of four, whose 16-byte loads are
+// all issued before any arithmetic), fp32 sums of the squared bf16 elements;
+// the warps stride over the rows, and every lane takes part in every shuffle
+// (rows past the end contribute zeros and store nothing).
+__device__ __forceinline__ float sumsq_bf16x8(const uint4& u) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  float acc = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+    acc = fmaf(lo, lo, acc);
+    acc = fmaf(hi, hi, acc);
+  }
+  return acc;
+}
+
+template <int D>
 __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* __restrict__ a0,
                                                            const __nv_bfloat16* __restrict__ a1,
                                                            const __nv_bfloat16* __restrict__ a2,
                                                            const __nv_bfloat16* __restrict__ a3,
-                                                           float* __restrict__ inv, int BH, int T, int Tp, int D) {
-  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+                                                           float* __restrict__ inv, int BH, int T, int Tp) {
+  constexpr int CH = D / 64;  // 16-byte chunks per lane per row
+  const int lane = threadIdx.x & 31, sub = lane & 7;
   const long long rows_p = static_cast<long long>(BH) * Tp;
-  if (gw >= 4 * rows_p) return;
-  const int which = static_cast<int>(gw / rows_p);
-  const long long rem = gw - static_cast<long long>(which) * rows_p;
-  const long long bh = rem / Tp;
-  const int t = static_cast<int>(rem - bh * Tp);
-  if (t >= T) {
-    if (lane == 0) inv[gw] = 0.0f;
-    return;
-  }
-  const __nv_bfloat16* src = which == 0 ? a0 : which == 1 ? a1 : which == 2 ? a2 : a3;
-  const __nv_bfloat16* x = src + (bh * T + t) * D;
-  float acc = 0.0f;
-  for (int d = lane * 2; d < D; d += 64) {
-    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(x + d));
-    acc = fmaf(f.x, f.x, acc);
-    acc = fmaf(f.y, f.y, acc);
-  }
+  const long long total = 4 * rows_p;
+  const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long base = warp0 * 8; base < total; base += nwarps * 8) {
+    long long row[2];
+    bool live[2];
+    uint4 u[2][CH];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) inv[gw] = 1.0f / fmaxf(sqrtf(acc), 1e-12f);
+    for (int g = 0; g < 2; ++g) {
+      row[g] = base + 4 * g + (lane >> 3);
+      live[g] = false;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) u[g][c] = make_uint4(0u, 0u, 0u, 0u);
+      if (row[g] < total) {
+        const int which = static_cast<int>(row[g] / rows_p);
+        const long long rem = row[g] - static_cast<long long>(which) * rows_p;
+        const long long bh = rem / Tp;
+        const int t = static_cast<int>(rem - bh * Tp);
+        live[g] = t < T;
+        if (live[g]) {
+          const __nv_bfloat16* src = which == 0 ? a0 : which == 1 ? a1 : which == 2 ? a2 : a3;
+          const uint4* x = reinterpret_cast<const uint4*>(src + (bh * T + t) * D);
+#pragma unroll
+          for (int c = 0; c < CH; ++c) u[g][c] = x[sub + 8 * c];
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) acc += sumsq_bf16x8(u[g][c]);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+      if (sub == 0 && row[g] < total) inv[row[g]] = live[g] ? 1.0f / fmaxf(sqrtf(acc), 1e-12f) : 0.0f;
+    }
+  }
 }
 
 // 32 scores of stream t -> 16 packed weights over the consumed score
@@ -407,6 +441,7 @@ size_t tra_diff_scratch_bytes(int B, int H, int T) {
 int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const void* k2, const void* v, void* out,
                          int B, int H, int T, int D, float beta, float lam, float p, float* inv_norm,
                          cudaStream_t stream) {
+  if (D != 64 && D != 128) return ERR_UNSUPPORTED;
   const int BH = B * H;
   CUtensorMap maps[5];
   const uint64_t rs = static_cast<uint64_t>(D) * 2, hs = rs * T;
@@ -418,12 +453,19 @@ int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const v
   const bool norm = inv_norm != nullptr;
   if (norm) {
     const int Tp = ((T + BT - 1) / BT) * BT;
-    const long long threads = 4LL * BH * Tp * 32;
-    const long long blocks = (threads + 255) / 256;
-    if (blocks > 0x7fffffffLL) return ERR_SHAPE;
-    row_inv_norm_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(q1), static_cast<const __nv_bfloat16*>(k1),
-        static_cast<const __nv_bfloat16*>(q2), static_cast<const __nv_bfloat16*>(k2), inv_norm, BH, T, Tp, D);
+    const long long rows = 4LL * BH * Tp;  // 64 rows per 256-thread block per pass
+    const int sms = sm_count();
+    if (sms <= 0) return ERR_DEVICE;
+    const long long want = (rows + 63) / 64, cap = 8LL * sms;
+    const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
+    const auto* a0 = static_cast<const __nv_bfloat16*>(q1);
+    const auto* a1 = static_cast<const __nv_bfloat16*>(k1);
+    const auto* a2 = static_cast<const __nv_bfloat16*>(q2);
+    const auto* a3 = static_cast<const __nv_bfloat16*>(k2);
+    if (D == 128)
+      row_inv_norm_kernel<128><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv_norm, BH, T, Tp);
+    else
+      row_inv_norm_kernel<64><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv_norm, BH, T, Tp);
     if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
   }
   if (D == 128)
