@@ -9,11 +9,11 @@
 // key tile for every query tile; these visit only key tiles at or below the
 // diagonal and mask the diagonal tile per element.
 //
-// Shared by both kernels: Q/K/V tiles (128 rows x D, 128-byte swizzled
-// 64-column panels) arrive by TMA; S = Q K^T (M=128, N=128, K=D; both
-// operands K-major in smem) and O += P V (M=128, N=D, K=128; P read straight
-// from TMEM, V an MN-major smem operand) run on tcgen05 with fp32 TMEM
-// accumulators, issued by one thread; an epilogue thread owns one query row
+// Q/K/V tiles (128 rows x D, 128-byte swizzled 64-column panels) arrive by
+// TMA; S = Q K^T (M=128, N=128, K=D; both operands K-major in smem) and
+// O += P V (M=128, N=D, K=128; P read straight from TMEM, V an MN-major smem
+// operand) run on tcgen05 with fp32 TMEM accumulators, each tile's MMAs
+// issued by a single thread; an epilogue thread owns one query row
 // (one TMEM lane): it loads its scores, subtracts tau(i) in fp32, applies
 // ReLU^p, masks the diagonal tile, rounds to bf16 and writes P over the
 // consumed score columns in two halves, so the P V MMA can start on the
@@ -32,14 +32,15 @@
 // power as x^k sqrt(x)) only changes the epilogue arithmetic.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tc_tile.cuh"
 #include "tra_math.cuh"
 
 namespace bsa {
 namespace {
 
-constexpr int BM = 128;                 // query rows per tile
-constexpr int BN = 128;                 // keys per tile
-constexpr int PANEL_BYTES = 128 * 128;  // 128 rows x 128 B (64 bf16) swizzle panel
+using tile::PANEL_BYTES;                // 128 rows x 128 B (64 bf16) swizzle panel
+constexpr int BM = tile::ROWS;          // query rows per tile
+constexpr int BN = tile::ROWS;          // keys per tile
 constexpr uint32_t TMEM_COLS = 512;
 
 // 32 scores (tile columns c0 .. c0+31) -> 16 packed weights, stored to TMEM
@@ -92,96 +93,6 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tS, const PowParams& wp, 
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(p_full);
-}
-
-// O columns [c*32, c*32+32) of this thread's row: TMEM fp32 -> bf16 -> HBM.
-__device__ __forceinline__ void store_o_chunk(uint32_t tO, int c, __nv_bfloat16* orow, bool in_range) {
-  uint32_t ov[32];
-  tmem_ld32(tO + c * 32, ov);
-  tmem_wait_ld();
-  if (in_range) {
-    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-    for (int vq = 0; vq < 4; ++vq) {
-      uint4 u;
-      u.x = pack_bf16x2(__uint_as_float(ov[8 * vq + 0]), __uint_as_float(ov[8 * vq + 1]));
-      u.y = pack_bf16x2(__uint_as_float(ov[8 * vq + 2]), __uint_as_float(ov[8 * vq + 3]));
-      u.z = pack_bf16x2(__uint_as_float(ov[8 * vq + 4]), __uint_as_float(ov[8 * vq + 5]));
-      u.w = pack_bf16x2(__uint_as_float(ov[8 * vq + 6]), __uint_as_float(ov[8 * vq + 7]));
-      dst[vq] = u;
-    }
-  }
-}
-
-__device__ __forceinline__ float tau_of_row(int row, float beta, int D) {
-  return beta * sqrtf(2.0f * logf(static_cast<float>(row + 1)) / static_cast<float>(D));
-}
-
-// S_tmem = Q K^T over D: D/16 MMAs of K=16 (32 bytes of each 128-byte row).
-template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t sQ, uint32_t sK) {
-  constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * PANEL_BYTES + (kk & 3) * 32;
-    mma_ss(tS, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024), IDESC_QK,
-           kk > 0 ? 1u : 0u);
-  }
-}
-
-// O_tmem += P V for keys [16*kk0, 16*kk1) of the tile (P from TMEM).
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t sV, int kk0, int kk1, bool first) {
-  constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 0, 1);  // P (TMEM), V MN-major
-  constexpr int NP = D / 64;
-#pragma unroll
-  for (int kk = kk0; kk < kk1; ++kk) {
-    const uint64_t bdesc = smem_desc_sw128(sV + kk * 16 * 128, NP > 1 ? PANEL_BYTES : 1024, 1024);
-    mma_ts(tO, tP + kk * 8, bdesc, IDESC_PV, (!first || kk > 0) ? 1u : 0u);
-  }
-}
-
-// Producer body shared by both kernels: Q tiles, then K(n), V(n) for
-// n = 0..nlast into NS-stage rings.  On a timed-out wait it drains what it
-// has issued before returning.
-template <int NP, int TILE, int NS>
-__device__ __forceinline__ void produce(uint8_t* smem, int q_off, int k_off, int v_off, int nq, int qrow0, int bh,
-                                        int nlast, const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                                        const CUtensorMap* tmV, uint64_t* q_full, uint64_t* k_full,
-                                        uint64_t* k_empty, uint64_t* v_full, uint64_t* v_empty) {
-  tma_prefetch_desc(tmQ);
-  tma_prefetch_desc(tmK);
-  tma_prefetch_desc(tmV);
-  mbar_arrive_expect_tx(q_full, nq * TILE);
-  for (int qt = 0; qt < nq; ++qt) {
-#pragma unroll
-    for (int pnl = 0; pnl < NP; ++pnl)
-      tma_load_3d(smem + q_off + qt * TILE + pnl * PANEL_BYTES, tmQ, q_full, 64 * pnl, qrow0 + qt * BM, bh);
-  }
-  bool ok = true;
-  int nk = 0, nv = 0;  // K / V tiles issued
-  for (int n = 0; n <= nlast; ++n) {
-    const int s = n % NS;
-    const uint32_t ph = (n / NS) & 1;
-    if (!(ok = mbar_wait(&k_empty[s], ph ^ 1))) break;
-    mbar_arrive_expect_tx(&k_full[s], TILE);
-#pragma unroll
-    for (int pnl = 0; pnl < NP; ++pnl)
-      tma_load_3d(smem + k_off + s * TILE + pnl * PANEL_BYTES, tmK, &k_full[s], 64 * pnl, n * BN, bh);
-    nk = n + 1;
-    if (!(ok = mbar_wait(&v_empty[s], ph ^ 1))) break;
-    mbar_arrive_expect_tx(&v_full[s], TILE);
-#pragma unroll
-    for (int pnl = 0; pnl < NP; ++pnl)
-      tma_load_3d(smem + v_off + s * TILE + pnl * PANEL_BYTES, tmV, &v_full[s], 64 * pnl, n * BN, bh);
-    nv = n + 1;
-  }
-  if (!ok) {
-    // Drain: never leave the CTA with a bulk copy still landing in its smem.
-    mbar_wait(q_full, 0);
-    for (int n = (nk > NS ? nk - NS : 0); n < nk; ++n) mbar_wait(&k_full[n % NS], (n / NS) & 1);
-    for (int n = (nv > NS ? nv - NS : 0); n < nv; ++n) mbar_wait(&v_full[n % NS], (n / NS) & 1);
-  }
 }
 
 // ============================================================ pair kernel (p = 1, 2)
@@ -379,7 +290,7 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
           const int gi = g + n;
           if (!mbar_wait(&k_full[gi % L::NS], (gi / L::NS) & 1)) return false;
           tc_fence_after();
-          issue_qk<D>(tS, sQ, smem_u32(smem + L::K_OFF + (gi % L::NS) * L::TILE));
+          tile::mma_abt<D>(tS, sQ, smem_u32(smem + L::K_OFF + (gi % L::NS) * L::TILE));
           mma_commit(&s_full[qt]);
           release(&k_empty[gi % L::NS], n);
           if (n == nmax) mma_commit(&q_empty[qt]);
@@ -397,10 +308,10 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
           // The first P V of an item overwrites O: the epilogue has read the last one.
           if (n == 0 && uq > 0 && !(ok = mbar_wait(&o_empty[qt], (uq - 1) & 1))) break;
           tc_fence_after();
-          issue_pv<D>(tO, tS, sV, 0, BN / 32, n == 0);
+          tile::mma_tmem_a<D>(tO, tS, sV, 0, BN / 32, n == 0);
           if (!(ok = mbar_wait(&p_full[qt], ph))) break;
           tc_fence_after();
-          issue_pv<D>(tO, tS, sV, BN / 32, BN / 16, false);
+          tile::mma_tmem_a<D>(tO, tS, sV, BN / 32, BN / 16, false);
           release(&v_empty[gi % L::NS], n);
           if (n == nmax)
             mma_commit(&o_full[qt]);
@@ -426,7 +337,7 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
       int uq[2] = {0, 0};      // items so far per query tile (q_full / o_full / o_empty phase)
       bool ok = true;
       auto qk = [&](int qt, int gi) {
-        issue_qk<D>(tmem + qt * BN, sQ0 + qt * L::TILE, smem_u32(smem + L::K_OFF + (gi % L::NS) * L::TILE));
+        tile::mma_abt<D>(tmem + qt * BN, sQ0 + qt * L::TILE, smem_u32(smem + L::K_OFF + (gi % L::NS) * L::TILE));
         mma_commit(&s_full[qt]);
       };
       // PVt(n) in two halves: keys 0..63 as soon as that half of P is there.
@@ -440,10 +351,10 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
         // The first P V of an item overwrites O: the epilogue has read the last one.
         if (n == 0 && uq[qt] > 0 && !mbar_wait(&o_empty[qt], (uq[qt] - 1) & 1)) return false;
         tc_fence_after();
-        issue_pv<D>(tO, tP, sV, 0, BN / 32, n == 0);
+        tile::mma_tmem_a<D>(tO, tP, sV, 0, BN / 32, n == 0);
         if (!mbar_wait(&p_full[qt], ph)) return false;
         tc_fence_after();
-        issue_pv<D>(tO, tP, sV, BN / 32, BN / 16, false);
+        tile::mma_tmem_a<D>(tO, tP, sV, BN / 32, BN / 16, false);
         ++cs[qt];
         return true;
       };
@@ -509,7 +420,7 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
       if (qt == 1 && !it.has1) continue;
       const int nmax = qt == 0 ? it.nmax0 : it.nmax1;
       const int row = (2 * it.t + qt) * BM + wq * 32 + lane;
-      const PowParams wp = pow_params(tau_of_row(row, beta, D), p);
+      const PowParams wp = pow_params(tile::tau_of_row(row, beta, D), p);
       for (int n = 0; n <= nmax; ++n, ++cs) {
         if (!(ok = mbar_wait(&s_full[qt], cs & 1))) break;
         tc_fence_after();
@@ -522,7 +433,7 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
       tc_fence_after();
       __nv_bfloat16* orow = out + (static_cast<size_t>(it.bh) * T + row) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) store_o_chunk(lane_base + 2 * BN + qt * D, c, orow, row < T);
+      for (int c = 0; c < D / 32; ++c) tile::store_row_chunk(lane_base + 2 * BN + qt * D, c, orow, row < T);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_empty[qt]);
