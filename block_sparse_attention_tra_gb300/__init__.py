@@ -11,6 +11,8 @@ kernel for sm_103a behind a C ABI (``include/bsa.h``, ``libbsa.so``):
 * ``nsa_select_forward_fsa`` -- the same result in the page's block-outer
   split-K form: each selected block's K/V read once, per-pair softmax
   partials, a log-sum-exp combine.
+* ``tra_forward_host`` -- ``tra_forward`` on host tensors, streamed through
+  the GPU in chunks of heads with overlapped copies.
 
 The binding in ``bsa`` only marshals arguments; every step runs in the CUDA
 library, which is loaded on first use and must be built (``build.build()``).
@@ -33,6 +35,9 @@ from .bsa import (  # noqa: F401
     tra_diff_forward_raw,
     tra_forward,
     tra_forward_ex_raw,
+    tra_forward_host,
+    tra_forward_host_raw,
+    tra_forward_host_workspace_size,
     tra_forward_raw,
 )
 
@@ -44,6 +49,9 @@ __all__ = [
     "tra_forward",
     "tra_forward_raw",
     "tra_forward_ex_raw",
+    "tra_forward_host",
+    "tra_forward_host_raw",
+    "tra_forward_host_workspace_size",
     "tra_backward",
     "tra_backward_raw",
     "tra_diff_forward",

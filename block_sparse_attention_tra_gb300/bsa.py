@@ -58,6 +58,10 @@ def load_library():
     lib.tra_forward.restype = i32
     lib.tra_forward_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, i32, vp]
     lib.tra_forward_ex.restype = i32
+    lib.tra_forward_host_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.tra_forward_host_workspace_size.restype = ctypes.c_size_t
+    lib.tra_forward_host.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, vp, ctypes.c_size_t, vp]
+    lib.tra_forward_host.restype = i32
     lib.nsa_select_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.nsa_select_forward.restype = i32
     lib.tra_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, vp]
@@ -106,6 +110,17 @@ def tra_forward_ex_raw(q, k, v, out, B, H, T, D, beta, p, dtype, flags, stream=0
     """Direct C call of tra_forward_ex with integer device pointers."""
     return load_library().tra_forward_ex(q, k, v, out, B, H, T, D, float(beta), float(p), int(dtype), int(flags),
                                          stream)
+
+
+def tra_forward_host_workspace_size(B, H, T, D, dtype) -> int:
+    """Device bytes tra_forward_host needs for its workspace (0 if the arguments are rejected)."""
+    return int(load_library().tra_forward_host_workspace_size(B, H, T, D, int(dtype)))
+
+
+def tra_forward_host_raw(q, k, v, out, B, H, T, D, beta, p, dtype, workspace, workspace_bytes, stream=0) -> int:
+    """Direct C call of tra_forward_host: integer HOST pointers for q, k, v, out and a device workspace."""
+    return load_library().tra_forward_host(q, k, v, out, B, H, T, D, float(beta), float(p), int(dtype), workspace,
+                                           int(workspace_bytes), stream)
 
 
 def tra_backward_raw(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, dtype, stream=0) -> int:
@@ -194,6 +209,43 @@ def tra_forward(q, k, v, beta: float, p: float = 2.0, out=None, stream=None, sqr
         st = tra_forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T, D,
                              beta, p, _dtype_code(q), _stream_handle(stream))
     _check(st, "tra_forward")
+    return out
+
+
+def tra_forward_host(q, k, v, beta: float, p: float = 2.0, out=None, workspace=None, stream=None):
+    """Threshold rectified attention forward on CPU tensors ``[B, H, T, D]``
+    (float32 or bfloat16; page-locked tensors, e.g. ``t.pin_memory()``, let the
+    copies overlap the kernels).  The library streams chunks of heads through
+    the GPU (``tra_forward_host``); ``workspace`` is a uint8 CUDA tensor of at
+    least ``tra_forward_host_workspace_size`` bytes (allocated if None).  The
+    call is asynchronous on ``stream`` (default: torch's current stream):
+    keep q, k, v, out and the workspace alive, and synchronise ``stream``,
+    before reading ``out`` or releasing them (the library's copies run on
+    its own streams, which torch's allocators do not see)."""
+    import torch
+
+    if q.device.type != "cpu" or k.device.type != "cpu" or v.device.type != "cpu":
+        raise BsaError("tra_forward_host takes host (CPU) tensors")
+    if not (q.shape == k.shape == v.shape) or q.dim() != 4:
+        raise BsaError("q, k, v must share one shape [B, H, T, D]", 2)
+    if not (q.dtype == k.dtype == v.dtype):
+        raise BsaError("q, k, v must share one dtype", 3)
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if out.device.type != "cpu" or out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise BsaError("out must be a contiguous CPU tensor shaped and typed like q", 2)
+    B, H, T, D = q.shape
+    dt = _dtype_code(q)
+    need = tra_forward_host_workspace_size(B, H, T, D, dt)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+        if isinstance(stream, torch.cuda.Stream):
+            workspace.record_stream(stream)  # not reused before `stream` passes this call
+    st = tra_forward_host_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, T, D, beta, p, dt,
+                              workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                              _stream_handle(stream))
+    _check(st, "tra_forward_host")
     return out
 
 

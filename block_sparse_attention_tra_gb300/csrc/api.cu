@@ -156,6 +156,29 @@ int tra_forward_ex(const void* q, const void* k, const void* v, void* out, int B
   return launch_tra_bf16(q, k, v, out, B, H, T, D, beta, p, (flags & BSA_TRA_SQRT_HALF_POWERS) != 0, stream);
 }
 
+size_t tra_forward_host_workspace_size(int B, int H, int T, int D, int dtype) {
+  if (dtype != BSA_F32 && dtype != BSA_BF16) return 0;
+  if (B < 1 || H < 1 || T < 1 || (D != 64 && D != 128)) return 0;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL || static_cast<long long>(B) * H * T * D >= (1LL << 40)) return 0;
+  return tra_host_workspace_bytes(static_cast<long long>(B) * H, T, D, dtype == BSA_F32 ? 4 : 2);
+}
+
+int tra_forward_host(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int D, float beta,
+                     float p, int dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || workspace == nullptr) return BSA_ERR_NULLPTR;
+  if (dtype != BSA_F32 && dtype != BSA_BF16) return BSA_ERR_DTYPE;
+  if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
+  if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
+  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f)) return BSA_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BSA_ERR_ALIGN;
+  if (workspace_bytes < tra_forward_host_workspace_size(B, H, T, D, dtype)) return BSA_ERR_SCRATCH_LIMIT;
+  const int dv = check_device();
+  if (dv != OK) return dv;
+  return launch_tra_host(q, k, v, out, B, H, T, D, beta, p, dtype == BSA_F32, workspace, stream);
+}
+
 int tra_backward(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv, int B,
                  int H, int T, int D, float beta, float p, int dtype, cudaStream_t stream) {
   if (q == nullptr || k == nullptr || v == nullptr || dout == nullptr || dq == nullptr || dk == nullptr ||

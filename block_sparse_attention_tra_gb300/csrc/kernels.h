@@ -76,6 +76,14 @@ int launch_nsa_general(const void* q, const void* k, const void* v, const int32_
 // combine (nsa_fsa.cu).  `workspace` holds nsa_fsa_workspace_bytes(...) bytes,
 // 256-byte aligned; block_size is 64.
 size_t nsa_fsa_workspace_bytes(int B, int Hq, int Hkv, int T, int D, int S);
+
+// Threshold attention on host-resident tensors, streamed through the GPU in
+// chunks of heads with overlapped copies (tra_host.cu).  `workspace` holds
+// tra_host_workspace_bytes(...) bytes of 256-byte aligned device memory.
+int tra_host_chunk_heads(long long BH);
+size_t tra_host_workspace_bytes(long long BH, int T, int D, int elsize);
+int launch_tra_host(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int D, float beta,
+                    float p, bool f32, void* workspace, cudaStream_t stream);
 int launch_nsa_fsa(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out, float* lse,
                    int B, int Hq, int Hkv, int T, int D, int S, void* workspace, cudaStream_t stream);
 

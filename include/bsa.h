@@ -7,21 +7,25 @@
  *   tra_forward         threshold rectified attention (TRA)
  *   nsa_select_forward  NSA selection-branch attention
  *
- * plus the TRA backward, the differential TRA and the NSA selection forward
+ * plus the TRA backward, the differential TRA, the NSA selection forward
  * in the page's block-outer split-K form (nsa_select_forward_fsa, which works
- * in a caller-provided workspace).
+ * in a caller-provided workspace) and tra_forward_host, which takes host
+ * buffers and streams them through the GPU.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Every tensor pointer is caller-owned DEVICE memory (cudaMalloc or a
- *   framework allocator) on the current device.  Tensors are dense, contiguous
+ *   framework allocator) on the current device, except the host tensors of
+ *   tra_forward_host.  Tensors are dense, contiguous
  *   and row-major in the shapes given below; there are no stride arguments.
  *   q, k, v and out start on a 16-byte boundary.
  * - The library never synchronises: work is enqueued on `stream` (0 = legacy
  *   default stream) and the call returns after the launch.  It allocates no
  *   device memory, except tra_diff_forward with normalize != 0, which takes a
- *   small temporary through the stream-ordered allocator (documented there).  Its only state is a device error word per kernel file,
- *   written only when a bounded wait times out (see bsa_device_error).  Inputs must stay valid and
+ *   small temporary through the stream-ordered allocator (documented there).
+ *   Its state is a device error word per kernel file, written only when a
+ *   bounded wait times out (see bsa_device_error), and the streams and
+ *   events tra_forward_host creates on its first call on a device.  Inputs must stay valid and
  *   unmodified, and outputs untouched by others, until that work completes.
  * - A call returns a bsa_status.  Argument errors are detected on the host
  *   before anything is enqueued and leave every buffer untouched.  A launch
@@ -126,6 +130,37 @@ typedef enum {
 BSA_API int tra_forward_ex(const void* q, const void* k, const void* v,
                            void* out, int B, int H, int T, int D, float beta,
                            float p, int dtype, int flags, cudaStream_t stream);
+
+/*
+ * tra_forward_host -- tra_forward on tensors in host memory.
+ *
+ * Same method, arguments, layout, rules and errors as tra_forward, except
+ * that q, k, v (read) and out (written) are HOST pointers.  The (b, h) heads
+ * are streamed through the GPU in about eight chunks: the host-to-device
+ * copies of one chunk, the kernel of the previous chunk and the
+ * device-to-host copy of the one before overlap on three library streams
+ * (created on the first call on a device and kept for the process).  For the
+ * copies to overlap, the host buffers should be page-locked (cudaHostAlloc
+ * or cudaHostRegister); pageable buffers give the same result with the
+ * copies serialised.  The call is asynchronous with respect to `stream`:
+ * work already queued on `stream` comes first, and out is complete when
+ * `stream` reaches the point after the call (synchronize `stream` before
+ * reading out or reusing q, k, v, out or the workspace).
+ *
+ *   workspace, workspace_bytes : caller-owned device memory, 256-byte
+ *       aligned, at least tra_forward_host_workspace_size(B, H, T, D, dtype)
+ *       bytes (three stages of q, k, v and out for one chunk of heads).
+ *
+ * Errors: those of tra_forward, plus BSA_ERR_NULLPTR for a NULL workspace,
+ * BSA_ERR_ALIGN for a misaligned workspace and BSA_ERR_SCRATCH_LIMIT for a
+ * workspace that is too small.  Host pointers need no particular alignment.
+ */
+BSA_API size_t tra_forward_host_workspace_size(int B, int H, int T, int D,
+                                               int dtype);
+BSA_API int tra_forward_host(const void* q, const void* k, const void* v,
+                             void* out, int B, int H, int T, int D,
+                             float beta, float p, int dtype, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * tra_backward -- gradients of the threshold rectified attention forward.

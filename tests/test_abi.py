@@ -176,3 +176,26 @@ def test_tra_forward_ex_flags(lib):
     assert bsa.tra_forward_ex_raw(None, P, P, P, 1, 1, 16, 64, 1.0, 1.5, 1, 1, 0) == 1
     if not __import__("torch").cuda.is_available():
         assert ex(0) == 6 and ex(1) == 6 and ex(1, p=2.0) == 6
+
+
+def test_tra_forward_host_workspace_and_argument_errors(lib):
+    from block_sparse_attention_tra_gb300 import bsa
+
+    # three stages of q, k, v, out for one chunk of ceil(B*H / 8) heads
+    assert bsa.tra_forward_host_workspace_size(4, 16, 4096, 128, 1) == 3 * 4 * 8 * 4096 * 128 * 2
+    assert bsa.tra_forward_host_workspace_size(1, 3, 100, 64, 0) == 3 * 4 * ((1 * 100 * 64 * 4 + 255) // 256 * 256)
+    assert bsa.tra_forward_host_workspace_size(1, 1, 16, 32, 1) == 0     # D
+    assert bsa.tra_forward_host_workspace_size(1, 1, 16, 64, 7) == 0     # dtype
+    assert bsa.tra_forward_host_workspace_size(0, 1, 16, 64, 1) == 0     # B
+    ws, need = 1 << 20, bsa.tra_forward_host_workspace_size(1, 1, 16, 64, 1)
+
+    def call(q=P, k=P, v=P, o=P, B=1, H=1, T=16, D=64, beta=1.0, p=2.0, dtype=1, w=ws, nbytes=need):
+        return bsa.tra_forward_host_raw(q, k, v, o, B, H, T, D, beta, p, dtype, w, nbytes, 0)
+
+    assert call(q=None) == 1 and call(w=None) == 1
+    assert call(dtype=5) == 3
+    assert call(B=0) == 2 and call(T=0) == 2
+    assert call(D=96) == 4 and call(p=0.0) == 4 and call(beta=float("nan")) == 4
+    assert call(w=ws + 16) == 7                      # workspace not 256-byte aligned
+    assert call(nbytes=need - 1) == 9                # workspace too small
+    assert call() == 6                               # valid arguments, no device here

@@ -328,3 +328,39 @@ def test_nsa_full_workload_sampled_rows(name):
         got_o.append(f64(out[b, g * G:(g + 1) * G, i]))
         got_l.append(f64(lse[b, g * G:(g + 1) * G, i]))
     check_nsa(np.stack(got_o), np.stack(got_l), np.stack(ref_o), np.stack(ref_l))
+
+
+# tra_forward_host: host tensors streamed through the GPU in chunks of heads.
+# Each head is computed by the same kernel as on the device path, so the
+# result is bit-identical to tra_forward on device copies of the inputs.
+@pytest.mark.parametrize("B,H,T,D,p,dtype,pinned", [
+    (2, 5, 300, 64, 2.0, "bf16", True),     # 10 heads -> 5 chunks of 2 (more chunks than stages)
+    (1, 2, 256, 128, 1.5, "bf16", True),    # 2 chunks, fewer than the 3 stages
+    (3, 8, 1000, 128, 1.0, "bf16", False),  # pageable host memory, 8 chunks of 3
+    (1, 3, 130, 64, 2.0, "f32", True),      # fp32 path
+])
+def test_tra_forward_host_matches_device_path(B, H, T, D, p, dtype, pinned):
+    import torch
+
+    q, k, v = workloads.tra_inputs(B, H, T, D, dtype, seed=B * H + T)
+    want = bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), 0.7, p)
+    hq, hk, hv = (t.pin_memory() if pinned else t.clone() for t in (q, k, v))
+    out = torch.empty(q.shape, dtype=q.dtype, pin_memory=pinned)
+    got = bsa.tra_forward_host(hq, hk, hv, 0.7, p, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want.cpu())
+
+
+def test_tra_forward_host_reuses_workspace():
+    import torch
+
+    B, H, T, D = 2, 4, 512, 128
+    ws = torch.empty(bsa.tra_forward_host_workspace_size(B, H, T, D, 1), dtype=torch.uint8, device="cuda")
+    outs, pinned = [], []
+    ins = [workloads.tra_inputs(B, H, T, D, "bf16", seed=s) for s in (1, 2)]
+    for q, k, v in ins:  # back to back on one stream and one workspace, no sync in between
+        pinned.append([t.pin_memory() for t in (q, k, v)])  # alive until the copies have run
+        outs.append(bsa.tra_forward_host(*pinned[-1], 1.0, 2.0, workspace=ws))
+    torch.cuda.synchronize()
+    for (q, k, v), got in zip(ins, outs):
+        assert torch.equal(got, bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), 1.0, 2.0).cpu())
