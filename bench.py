@@ -43,6 +43,7 @@ KERNEL_SOURCES = {
     "tra": "block_sparse_attention_tra_gb300/csrc/tra_bf16.cu",
     "tra_f32": "block_sparse_attention_tra_gb300/csrc/tra_f32.cu",
     "nsa": "block_sparse_attention_tra_gb300/csrc/nsa_select.cu",
+    "nsa_general": "block_sparse_attention_tra_gb300/csrc/nsa_general.cu",
     "fsa": "block_sparse_attention_tra_gb300/csrc/nsa_fsa.cu",
 }
 
@@ -212,11 +213,13 @@ def roofline_for(w, ms_per_launch, pk, sustained: bool, fsa: bool = False):
                 "traffic": ncu_traffic("tra", w.name), "kernel": "tra_bf16_pair_kernel (persistent, tcgen05)",
                 "algorithmic_flops_per_launch": w.flops}
     achieved = w.algorithmic_bytes / (ms_per_launch * 1e-3) / 1e9
+    general = not (w.block_size == 64 and w.D in (64, 128))  # shapes the general kernel serves
+    kind = "fsa" if fsa else "nsa_general" if general else "nsa"
     r = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
          "frac": round(achieved / pk["hbm_gbs"], 4), "peak_kind": "copy bandwidth of " + pk["source"],
-            "traffic": ncu_traffic("fsa" if fsa else "nsa", ("fsa:" if fsa else "") + w.name),
+         "traffic": ncu_traffic(kind, ("fsa:" if fsa else "") + w.name),
          "kernel": ("fsa_blockouter_kernel + fsa_combine_kernel" if fsa else
-                    "nsa_select_kernel" if (w.block_size == 64 and w.D in (64, 128)) else "nsa_general_kernel"),
+                    "nsa_general_kernel" if general else "nsa_select_kernel"),
          "algorithmic_bytes_per_launch": w.algorithmic_bytes,
          "tflops": round(w.flops / (ms_per_launch * 1e-3) / 1e12, 2),
          "unique_bytes_per_launch": w.unique_bytes}
