@@ -201,8 +201,10 @@ BSA_API int tra_backward(const void* q, const void* k, const void* v,
  *   out = TRA(n(q1), n(k1), v) - clamp(lambda, 0, 1) * TRA(n(q2), n(k2), v)
  *
  * where TRA is tra_forward's map with the same beta and p.  One fused kernel
- * runs both score streams on the same query tile, shares each V tile and
- * accumulates both P.V products into one accumulator.  With normalize, a
+ * runs both score streams on the same query tile and shares each V tile;
+ * each stream accumulates its P.V product in fp32 and the two are combined
+ * (first minus clamp(lambda, 0, 1) times second) before the bf16 store.
+ * With normalize, a
  * pre-pass kernel first computes 1/max(||row||, 1e-12) of every row of q1,
  * k1, q2, k2 into a temporary of 16 * B * H * Tp bytes (Tp = T rounded up to
  * a multiple of 128) taken with cudaMallocFromPoolAsync on `stream` and
