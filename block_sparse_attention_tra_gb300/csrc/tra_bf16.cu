@@ -302,8 +302,17 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
           const int gi = g + n;
           const uint32_t sV = smem_u32(smem + L::V_OFF + (gi % L::NS) * L::TILE);
           const uint32_t ph = cs & 1;
-          if (!(ok = mbar_wait(PAIR_SPLIT_P ? &p_half[qt] : &p_full[qt], ph) &&
-                     mbar_wait(&v_full[gi % L::NS], (gi / L::NS) & 1)))
+          // V(n) has usually landed long before P: then only the P barrier
+          // sits between the epilogue and the P V issue.  With p = 1 (the
+          // lightest epilogue) and with the four-stage D = 64 ring V is
+          // waited for first (measured fastest there); otherwise, if V has
+          // not landed yet (two-stage D = 128 ring), P is waited for first.
+          constexpr bool V_FIRST = PC == POW_ONE || D == 64;
+          uint64_t* vb = &v_full[gi % L::NS];
+          const uint32_t vph = (gi / L::NS) & 1;
+          const bool v_in = V_FIRST ? mbar_wait(vb, vph) : mbar_test(vb, vph);
+          if (V_FIRST && !(ok = v_in)) break;
+          if (!(ok = mbar_wait(PAIR_SPLIT_P ? &p_half[qt] : &p_full[qt], ph) && (v_in || mbar_wait(vb, vph))))
             break;
           // The first P V of an item overwrites O: the epilogue has read the last one.
           if (n == 0 && uq > 0 && !(ok = mbar_wait(&o_empty[qt], (uq - 1) & 1))) break;
@@ -345,8 +354,10 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
         const uint32_t sV = smem_u32(smem + L::V_OFF + (gi % L::NS) * L::TILE);
         const uint32_t tP = tmem + qt * BN, tO = tmem + 2 * BN + qt * D;
         const uint32_t ph = cs[qt] & 1;
-        if (!mbar_wait(PAIR_SPLIT_P ? &p_half[qt] : &p_full[qt], ph) ||
-            !mbar_wait(&v_full[gi % L::NS], (gi / L::NS) & 1))
+        uint64_t* vb = &v_full[gi % L::NS];  // V usually landed long before P (see the per-tile issuer)
+        const uint32_t vph = (gi / L::NS) & 1;
+        const bool v_in = mbar_test(vb, vph);
+        if (!mbar_wait(PAIR_SPLIT_P ? &p_half[qt] : &p_full[qt], ph) || !(v_in || mbar_wait(vb, vph)))
           return false;
         // The first P V of an item overwrites O: the epilogue has read the last one.
         if (n == 0 && uq[qt] > 0 && !mbar_wait(&o_empty[qt], (uq[qt] - 1) & 1)) return false;
