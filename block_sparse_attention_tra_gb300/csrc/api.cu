@@ -113,6 +113,20 @@ int encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
   return r == CUDA_SUCCESS ? OK : ERR_SHAPE;
 }
 
+int encode_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t stride1_bytes,
+                      uint32_t box0, uint32_t box1) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return ERR_DEVICE;
+  const cuuint64_t dims[2] = {d0, d1};
+  const cuuint64_t strides[1] = {stride1_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? OK : ERR_SHAPE;
+}
+
 int sm_count() {
   constexpr int MAX_DEVICES = 64;
   static int counts[MAX_DEVICES] = {};

@@ -27,6 +27,10 @@ enum Status : int {
 int encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                    uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
                    uint32_t box2);
+// Rank-2 fp32 tensor map (d0 innermost), 128-byte swizzle: used for TMA
+// stores of fp32 rows from shared memory.
+int encode_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t stride1_bytes,
+                      uint32_t box0, uint32_t box1);
 
 // Streaming multiprocessors of the current device (cached per device; 0 if
 // the query fails).  Persistent kernels size their grids with it.

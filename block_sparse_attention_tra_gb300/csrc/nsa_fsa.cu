@@ -50,6 +50,9 @@ constexpr int FSA_MMA_WARP = 12;
 constexpr int FSA_THREADS = 13 * 32;
 constexpr int FSA_STG_STRIDE = 272;    // staging row: 64 floats + 16 bytes of skew
 constexpr int FSA_STG_WARP = 32 * FSA_STG_STRIDE;
+constexpr int FSA_TSTG_BUF = 32 * 128;  // TMA-store stage: 32 rows x 32 floats, 128-byte swizzled
+constexpr int FSA_TSTG_WARP = 2 * FSA_TSTG_BUF;  // two stages per warp (8 KB, 1 KB aligned)
+static_assert(FSA_TSTG_WARP <= FSA_STG_WARP, "the TMA-store stages reuse the staging area");
 constexpr int PANEL = 128 * 128;       // 128 rows x 128 B swizzle panel
 
 template <int D>
@@ -173,9 +176,14 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-template <int D>
+// TMA_OUT (G = 8 or 16): the acc rows of each query (G consecutive partial
+// rows) leave through a 128-byte-swizzled shared-memory stage and one TMA
+// tensor store per query and 32-column chunk (tmAcc: fp32 [rows, D], box
+// 32 x G); otherwise through the skewed staging area and 16-byte stores.
+template <int D, bool TMA_OUT>
 __global__ void __launch_bounds__(FSA_THREADS, 1)
     fsa_blockouter_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                          const __grid_constant__ CUtensorMap tmAcc,
                           const __nv_bfloat16* __restrict__ q, const int* __restrict__ list,
                           const int4* __restrict__ items, const int* __restrict__ meta, float* __restrict__ acc,
                           float* __restrict__ pm, float* __restrict__ pl, int G, int Hq, int Hkv, int T, int S,
@@ -315,6 +323,8 @@ __global__ void __launch_bounds__(FSA_THREADS, 1)
     const uint32_t tS = lane_base + L::S_COL + w * FSA_BS, tO = lane_base + L::O_COL + w * D;
     const float sl2 = scale * 1.4426950408889634f;  // scale * log2(e)
     const uint32_t stg_u = smem_u32(smem + L::STG_OFF + warp * FSA_STG_WARP);
+    const uint32_t tstg = smem_u32(smem + L::STG_OFF + warp * FSA_TSTG_WARP);  // 1 KB aligned (TMA_OUT)
+    int tsc = 0;  // 32-column chunks staged so far (TMA_OUT: selects the stage)
     for (int t = w, n = 0; t < nt; t += 2, ++n) {
       const int slot = t * qpt + qi;
       const bool valid = qi < qpt && slot < npairs;
@@ -364,41 +374,81 @@ __global__ void __launch_bounds__(FSA_THREADS, 1)
       }
       if (!mbar_wait(&o_full[w], n & 1)) break;
       tc_fence_after();
-      // acc row -> HBM, 64 columns at a time through a skewed staging area so
-      // that every global store instruction writes two contiguous 256-byte rows.
-#pragma unroll 1
-      for (int h = 0; h < D / 64; ++h) {
-        uint32_t oa[32], ob[32];
-        tmem_ld32(tO + h * 64, oa);
-        tmem_ld32(tO + h * 64 + 32, ob);
-        tmem_wait_ld();
-        if (h == D / 64 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&o_empty[w]);
-        }
+      if constexpr (TMA_OUT) {
+        // First partial row of each query of this warp (lanes k * G), or -1.
+        int qrow[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t a = stg_u + lane * FSA_STG_STRIDE + c * 16;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(oa[4 * c]), "r"(oa[4 * c + 1]),
-                       "r"(oa[4 * c + 2]), "r"(oa[4 * c + 3]) : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a + 128), "r"(ob[4 * c]), "r"(ob[4 * c + 1]),
-                       "r"(ob[4 * c + 2]), "r"(ob[4 * c + 3]) : "memory");
+        for (int k = 0; k < 4; ++k) qrow[k] = __shfl_sync(0xffffffffu, prow, (k * G) & 31);
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c, ++tsc) {
+          const uint32_t buf = tstg + (tsc & 1) * FSA_TSTG_BUF;
+          // The store issued two chunks ago read this stage: let it finish reading.
+          if (tsc >= 2 && lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          uint32_t ov[32];
+          tmem_ld32(tO + c * 32, ov);
+          tmem_wait_ld();
+          if (c == D / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_empty[w]);
+          }
+#pragma unroll
+          for (int x = 0; x < 8; ++x)
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(buf + lane * 128 + ((x ^ (lane & 7)) << 4)),
+                         "r"(ov[4 * x]), "r"(ov[4 * x + 1]), "r"(ov[4 * x + 2]), "r"(ov[4 * x + 3])
+                         : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (k * G < 32 && qrow[k] >= 0) tma_store_2d(&tmAcc, buf + k * G * 128, c * 32, qrow[k]);
+            bulk_commit();
+          }
         }
-        __syncwarp();
+      } else {
+        // acc row -> HBM, 64 columns at a time through a skewed staging area so
+        // that every global store instruction writes two contiguous 256-byte rows.
+#pragma unroll 1
+        for (int h = 0; h < D / 64; ++h) {
+          uint32_t oa[32], ob[32];
+          tmem_ld32(tO + h * 64, oa);
+          tmem_ld32(tO + h * 64 + 32, ob);
+          tmem_wait_ld();
+          if (h == D / 64 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_empty[w]);
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t a = stg_u + lane * FSA_STG_STRIDE + c * 16;
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(oa[4 * c]), "r"(oa[4 * c + 1]),
+                         "r"(oa[4 * c + 2]), "r"(oa[4 * c + 3]) : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a + 128), "r"(ob[4 * c]), "r"(ob[4 * c + 1]),
+                         "r"(ob[4 * c + 2]), "r"(ob[4 * c + 3]) : "memory");
+          }
+          __syncwarp();
 #pragma unroll 4
-        for (int k = 0; k < 16; ++k) {
-          const int rr = 2 * k + (lane >> 4), ch = lane & 15;
-          const int orow = __shfl_sync(0xffffffffu, prow, rr);
-          uint4 v4;
-          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(v4.x), "=r"(v4.y), "=r"(v4.z), "=r"(v4.w)
-                       : "r"(stg_u + rr * FSA_STG_STRIDE + ch * 16));
-          if (orow >= 0)
-            *reinterpret_cast<uint4*>(acc + static_cast<size_t>(orow) * D + h * 64 + ch * 4) = v4;
+          for (int k = 0; k < 16; ++k) {
+            const int rr = 2 * k + (lane >> 4), ch = lane & 15;
+            const int orow = __shfl_sync(0xffffffffu, prow, rr);
+            uint4 v4;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(v4.x), "=r"(v4.y), "=r"(v4.z), "=r"(v4.w)
+                         : "r"(stg_u + rr * FSA_STG_STRIDE + ch * 16));
+            if (orow >= 0)
+              *reinterpret_cast<uint4*>(acc + static_cast<size_t>(orow) * D + h * 64 + ch * 4) = v4;
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
+    }
+    // Never leave the CTA while a tensor store still reads its stage.
+    if constexpr (TMA_OUT) {
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
   }
 
@@ -544,13 +594,22 @@ int launch_fsa(const void* q, const void* k, const void* v, const int32_t* block
   fsa_scan_kernel<<<1, SCAN_THREADS, 0, stream>>>(cnt, off, items, meta, static_cast<int>(pl.NB), pl.qch);
   fsa_pairs_kernel<true><<<grid_for(pl.slots, 256), 256, 0, stream>>>(block_idx, cnt, list, pl.slots, T, S, n_blk);
 
-  auto kern = fsa_blockouter_kernel<D>;
+  // G = 8 or 16: each query's G partial rows are contiguous, so they leave by
+  // TMA tensor stores (fp32 [rows, D] map, 32 x G boxes).
+  const bool tma_out = G == 8 || G == 16;
+  CUtensorMap macc = mk;  // unused unless tma_out
+  if (tma_out) {
+    st = encode_tmap_2d_f32(&macc, acc, D, static_cast<uint64_t>(pl.rows), static_cast<uint64_t>(D) * 4, 32,
+                            static_cast<uint32_t>(G));
+    if (st != OK) return st;
+  }
+  auto kern = tma_out ? fsa_blockouter_kernel<D, true> : fsa_blockouter_kernel<D, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
     return ERR_LAUNCH;
   if (pl.max_items > 0x7fffffffLL) return ERR_SHAPE;
   kern<<<static_cast<unsigned>(pl.max_items), FSA_THREADS, L::ALLOC, stream>>>(
-      mk, mv, static_cast<const __nv_bfloat16*>(q), list, items, meta, acc, pmv, plv, G, Hq, Hkv, T, S, n_blk,
-      1.0f / sqrtf(static_cast<float>(D)));
+      mk, mv, macc, static_cast<const __nv_bfloat16*>(q), list, items, meta, acc, pmv, plv, G, Hq, Hkv, T, S,
+      n_blk, 1.0f / sqrtf(static_cast<float>(D)));
 
   const long long warps = static_cast<long long>(B) * Hq * T;
   const long long blocks = (warps * 32 + 255) / 256;
