@@ -68,6 +68,8 @@ FSA_SMALL = [
     (1, 6, 2, 256, 128, 5),     # G = 3: 42 queries, rows 126, 127 idle
     (1, 16, 1, 64, 128, 1),     # one block, S = 1
     (1, 16, 4, 320, 64, 32),    # S = 32
+    (1, 16, 2, 384, 128, 6),    # G = 8: 16 queries per M tile, TMA stores of 8-row boxes
+    (2, 8, 1, 256, 64, 4),      # G = 8, D = 64
 ]
 
 
