@@ -67,6 +67,54 @@ __device__ __forceinline__ float tau_of_row(int row, float beta, int D) {
   return beta * sqrtf(2.0f * logf(static_cast<float>(row + 1)) / static_cast<float>(D));
 }
 
+// Block order of the non-persistent kernels: the BH (b, h) heads split into
+// G groups whose sizes differ by at most one (the first BH % G groups hold one
+// head more); inside a group the tile rank goes first (rank 0 = the longest
+// item) and the group's heads round-robin, so the CTAs resident at one time
+// stream the tiles of a few heads, which stay in L2, instead of touching every
+// head at once.  Block idx in [0, BH * nT) maps onto every (rank, bh) once.
+struct HeadItem {
+  int rank, bh;
+};
+__device__ __forceinline__ HeadItem head_group_item(int idx, int BH, int nT, int G) {
+  const int b = BH / G, r = BH % G;
+  const int big = (b + 1) * nT;  // items of each of the first r groups
+  int h0, hg, i;
+  if (idx < r * big) {
+    const int g = idx / big;
+    h0 = g * (b + 1);
+    hg = b + 1;
+    i = idx - g * big;
+  } else {
+    const int i2 = idx - r * big;
+    const int g = i2 / (b * nT);
+    h0 = r * (b + 1) + g * b;
+    hg = b;
+    i = i2 - g * b * nT;
+  }
+  return {i / hg, h0 + i % hg};
+}
+
+#ifndef BSA_HEAD_GROUP_MB
+#define BSA_HEAD_GROUP_MB 32  // L2 bytes (MB) a group of heads streams; 0 = one group
+#endif
+
+// Number of head groups G for head_group_item.  A group holds the heads whose
+// streamed tiles (stream_bytes per head) fill about BSA_HEAD_GROUP_MB of L2,
+// but at least enough heads that the group's work, spread over `slots`
+// resident CTAs, is twice its longest item: heads * nT (nT + 1) / 2 tile
+// steps >= 2 * slots * nT.  The longest items start when their group does, so
+// a smaller last group would leave the GPU idle behind them.
+inline int head_groups(int BH, int nT, long long stream_bytes, int slots) {
+  if (BSA_HEAD_GROUP_MB <= 0 || stream_bytes <= 0 || BH < 2) return 1;
+  long long hg = (static_cast<long long>(BSA_HEAD_GROUP_MB) << 20) / stream_bytes;
+  const long long hmin = (4LL * slots + nT) / (nT + 1);  // ceil(4 slots / (nT + 1))
+  if (hg < hmin) hg = hmin;
+  if (hg < 1) hg = 1;
+  const long long g = BH / hg;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
 // Load the D/64 panels of tile row block `row0` of head `bh` into smem.
 template <int D>
 __device__ __forceinline__ void tma_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int row0, int bh) {

@@ -47,9 +47,6 @@ constexpr int EPI_WARPS = 4;
 constexpr int TMA_WARP = 4;
 constexpr int MMA_WARP = 5;  // first of the two MMA-issuing warps (allocates TMEM)
 constexpr uint32_t TMEM_COLS = 512;
-#ifndef BSA_BWD_GROUP_MB
-#define BSA_BWD_GROUP_MB 32  // L2 bytes (MB) a block-order group of heads streams; 0 = no grouping
-#endif
 
 __device__ __forceinline__ float ex2a(float x) {
   float y;
@@ -198,22 +195,6 @@ __device__ __forceinline__ void bwd_produce(uint8_t* smem, const BwdBars& B, con
   }
 }
 
-// Block order: the (b, h) heads in groups of HG; inside a group the tile rank
-// goes first (rank 0 = the longest item) and the heads round-robin, so the
-// CTAs resident at one time stream the K/V (or Q/dO) tiles of a few heads,
-// which stay in L2, instead of touching every head at once.  The hardware's
-// dynamic block scheduling keeps the load balanced across group boundaries.
-struct BwdItem {
-  int rank, bh;
-};
-__device__ __forceinline__ BwdItem bwd_item(int idx, int BH, int nT, int HG) {
-  const int g = idx / (HG * nT);
-  const int h0 = g * HG;
-  const int hg = min(HG, BH - h0);
-  const int r = idx - g * HG * nT;
-  return {r / hg, h0 + r % hg};
-}
-
 // ---------------------------------------------------------------- dK / dV
 
 template <int D, int PC>
@@ -221,7 +202,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     tra_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                         __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int T, int nT,
-                        int HG, float beta, float p) {
+                        int G, float beta, float p) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -229,7 +210,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
   float* tau_s = reinterpret_cast<float*>(smem + L::TAU_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const BwdItem item = bwd_item(static_cast<int>(blockIdx.x), BH, nT, HG);
+  const tile::HeadItem item = tile::head_group_item(static_cast<int>(blockIdx.x), BH, nT, G);
   const int n = item.rank;  // key tile; n = 0 has the most query tiles
   const int bh = item.bh;
   const int nq = nT - n;  // query tiles m = n .. nT-1
@@ -351,14 +332,14 @@ template <int D, int PC>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     tra_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                      __nv_bfloat16* __restrict__ dq, int BH, int T, int nT, int HG, float beta, float p) {
+                      __nv_bfloat16* __restrict__ dq, int BH, int T, int nT, int G, float beta, float p) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const BwdBars B = bwd_bars<D>(smem);
   uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const BwdItem item = bwd_item(static_cast<int>(blockIdx.x), BH, nT, HG);
+  const tile::HeadItem item = tile::head_group_item(static_cast<int>(blockIdx.x), BH, nT, G);
   const int m = nT - 1 - item.rank;  // longest first
   const int bh = item.bh;
   constexpr uint32_t S = 0, DP = BT, DQ = 2 * BT;
@@ -466,18 +447,14 @@ int launch_bwd(const CUtensorMap* maps, void* dq, void* dk, void* dv, int BH, in
   const int nT = (T + BT - 1) / BT;
   const long long grid = static_cast<long long>(nT) * BH;
   if (grid > 0x7fffffffLL) return ERR_SHAPE;
-  // Heads per block-order group: the streamed tiles of a group (two bf16
-  // tensors of T x D per head) fill about BSA_BWD_GROUP_MB of L2.
-  const long long per_head = 4LL * T * D;
-  long long hg = BSA_BWD_GROUP_MB > 0 ? (static_cast<long long>(BSA_BWD_GROUP_MB) << 20) / per_head : BH;
-  hg = hg < 1 ? 1 : hg > BH ? BH : hg;
-  const int HG = static_cast<int>(hg);
+  // two streamed bf16 tensors of T x D per head; one resident CTA per SM
+  const int G = tile::head_groups(BH, nT, 4LL * T * D, sm_count());
   k1<<<static_cast<unsigned>(grid), BWD_THREADS, L::ALLOC, stream>>>(
       maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), BH, T,
-      nT, HG, beta, p);
+      nT, G, beta, p);
   if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
   k2<<<static_cast<unsigned>(grid), BWD_THREADS, L::ALLOC, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dq), BH, T, nT, HG, beta, p);
+      maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dq), BH, T, nT, G, beta, p);
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
 

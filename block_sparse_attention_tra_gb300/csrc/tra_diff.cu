@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
     tra_diff_kernel(const __grid_constant__ CUtensorMap tmQ0, const __grid_constant__ CUtensorMap tmQ1,
                     const __grid_constant__ CUtensorMap tmK0, const __grid_constant__ CUtensorMap tmK1,
                     const __grid_constant__ CUtensorMap tmV, const float* __restrict__ inv_norm,
-                    __nv_bfloat16* __restrict__ out, int BH, int T, int nQ, float beta, float p, float lam) {
+                    __nv_bfloat16* __restrict__ out, int BH, int T, int nQ, int G, float beta, float p, float lam) {
   const int Tp = nQ * BT;  // row stride of the normalisation buffer
   using L = DiffLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -206,8 +206,9 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
   uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m = nQ - 1 - static_cast<int>(blockIdx.x) / BH;  // longest first
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const tile::HeadItem item = tile::head_group_item(static_cast<int>(blockIdx.x), BH, nQ, G);
+  const int m = nQ - 1 - item.rank;  // longest first
+  const int bh = item.bh;
   const int nmax = m;
   constexpr uint32_t O_COL = 2 * BT;  // O0; O1 at O_COL + D
 
@@ -417,8 +418,11 @@ int launch_diff_kernel(const CUtensorMap* maps, const float* inv, void* out, int
   const int nQ = (T + BT - 1) / BT;
   const long long grid = static_cast<long long>(nQ) * BH;
   if (grid > 0x7fffffffLL) return ERR_SHAPE;
+  // K1, K2, V: three streamed bf16 tensors per head; one resident CTA per SM
+  const int G = tile::head_groups(BH, nQ, 6LL * T * D, sm_count());
   kern<<<static_cast<unsigned>(grid), DiffCfg<D, PC>::THREADS, L::ALLOC, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], maps[4], inv, static_cast<__nv_bfloat16*>(out), BH, T, nQ, beta, p, lam);
+      maps[0], maps[1], maps[2], maps[3], maps[4], inv, static_cast<__nv_bfloat16*>(out), BH, T, nQ, G, beta, p,
+      lam);
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
 
