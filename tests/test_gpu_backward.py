@@ -74,3 +74,20 @@ def test_tra_backward_full_workload_sampled_heads():
             gpu = f64(g[sl])
             err = float(np.abs(gpu - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
             assert err <= TOL, f"{name} head ({b},{h}): max err {err:.3e} of max|ref|"
+
+
+def test_tra_backward_head_groups_cover_every_head():
+    # At the bench shape the blocks run in head groups of unequal size (64
+    # heads in three groups).  Each output row is computed by one CTA with the
+    # same arithmetic whatever the block order, so the full call must equal
+    # single-head calls (one group each) bit for bit on every head.
+    w = workloads.TRA_WORKLOADS["tra_bf16_B4_H16_T4096_D128"]
+    q, k, v = (t.cuda() for t in workloads.workload_inputs(w))
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).cuda()
+    full = bsa.tra_backward(q, k, v, do, w.beta, w.p)
+    for b in range(w.B):
+        for h in range(w.H):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            one = bsa.tra_backward(q[sl], k[sl], v[sl], do[sl], w.beta, w.p)
+            for name, a, c in zip(("dq", "dk", "dv"), full, one):
+                assert torch.equal(a[sl], c), f"{name} head ({b},{h}) differs from its single-head call"

@@ -87,3 +87,19 @@ def test_tra_diff_full_workload_sampled_heads():
                                     normalize=True)
         err = float(np.abs(f64(out[sl]) - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
         assert err <= TOL, f"head ({b},{h}): max err {err:.3e} of max|ref|"
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+def test_tra_diff_head_groups_cover_every_head(normalize):
+    # At the bench shape the blocks run in head groups of unequal size (64
+    # heads in three groups).  Each output row is computed by one CTA with the
+    # same arithmetic whatever the block order (and the row norms per row), so
+    # the full call must equal single-head calls bit for bit on every head.
+    w = workloads.TRA_WORKLOADS["tra_bf16_B4_H16_T4096_D128"]
+    q1, q2, k1, k2, v = (t.cuda() for t in inputs(w.B, w.H, w.T, w.D, seed=5))
+    full = bsa.tra_diff_forward(q1, q2, k1, k2, v, w.beta, 0.5, w.p, normalize=normalize)
+    for b in range(w.B):
+        for h in range(w.H):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            one = bsa.tra_diff_forward(q1[sl], q2[sl], k1[sl], k2[sl], v[sl], w.beta, 0.5, w.p, normalize=normalize)
+            assert torch.equal(full[sl], one), f"head ({b},{h}) differs from its single-head call"

@@ -159,6 +159,22 @@ def test_tra_repeatable_and_stream():
     assert torch.equal(a, b)  # deterministic: no atomics, fixed order
 
 
+@pytest.mark.parametrize("name", ["tra_bf16_B4_H16_T4096_D128", "tra_bf16_B2_H32_T8192_D64"])
+def test_tra_full_workload_matches_single_heads(name):
+    # The persistent pair kernel deals the items of all heads over the SMs in
+    # a snake order; each query tile is computed by one CTA with the same
+    # arithmetic whatever the schedule, so the full-size call must equal
+    # single-head calls (a handful of items each) bit for bit on every head.
+    w = workloads.TRA_WORKLOADS[name]
+    q, k, v = (t.cuda() for t in workloads.workload_inputs(w))
+    full = bsa.tra_forward(q, k, v, w.beta, w.p)
+    for b in range(w.B):
+        for h in range(w.H):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            one = bsa.tra_forward(q[sl], k[sl], v[sl], w.beta, w.p)
+            assert torch.equal(full[sl], one), f"head ({b},{h}) differs from its single-head call"
+
+
 def test_tra_out_of_place_canary():
     """Writes only [B, H, T, D]: guard bands around out stay untouched."""
     B, H, T, D = 1, 2, 200, 64
