@@ -567,7 +567,7 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) q,k,v; no dataset)",
-        "config": {"workload": w.name, "sample": "bounded per step; see cpu_baseline.sample"},
+        "config": dict(workload_config(w, world), sample="bounded per step; see cpu_baseline.sample"),
         "cpu_baseline": cb,
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,

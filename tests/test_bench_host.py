@@ -90,3 +90,7 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle"
+    # the same workload description as the GPU arm's line, plus the sample note
+    for key, val in {"workload": "tra_f32_B1_H2_T256_D64", "B": 1, "H": 2, "T": 256, "D": 64}.items():
+        assert d["config"][key] == val
+    assert "sample" in d["config"]
