@@ -130,14 +130,16 @@ def _dtype(name: str) -> torch.dtype:
     return {"f32": torch.float32, "bf16": torch.bfloat16}[name]
 
 
-def tra_inputs(B: int, H: int, T: int, D: int, dtype: str = "bf16", seed: int = 0):
-    """``(q, k, v)`` CPU tensors ``[B, H, T, D]`` of the TRA recipe."""
-    g = torch.Generator().manual_seed(seed)
+def tra_inputs(B: int, H: int, T: int, D: int, dtype: str = "bf16", seed: int = 0, device: str = "cpu"):
+    """``(q, k, v)`` tensors ``[B, H, T, D]`` of the TRA recipe, drawn on
+    ``device`` (CPU by default; a CUDA device draws its own seeded stream,
+    for inputs too large to draw on the host)."""
+    g = torch.Generator(device=device).manual_seed(seed)
     shape = (B, H, T, D)
     sc = float(D) ** -0.25
-    q = (torch.randn(shape, generator=g) * sc).to(_dtype(dtype))
-    k = (torch.randn(shape, generator=g) * sc).to(_dtype(dtype))
-    v = torch.randn(shape, generator=g).to(_dtype(dtype))
+    q = (torch.randn(shape, generator=g, device=device) * sc).to(_dtype(dtype))
+    k = (torch.randn(shape, generator=g, device=device) * sc).to(_dtype(dtype))
+    v = torch.randn(shape, generator=g, device=device).to(_dtype(dtype))
     return q.contiguous(), k.contiguous(), v.contiguous()
 
 
@@ -170,13 +172,17 @@ def selection_indices(B: int, Hkv: int, T: int, block_size: int, S: int,
 
 
 def nsa_inputs(B: int, Hq: int, Hkv: int, T: int, D: int, block_size: int, S: int,
-               seed: int = 0):
-    """``(q, k, v, block_idx)`` CPU tensors of the NSA recipe (bf16 / int32)."""
-    g = torch.Generator().manual_seed(seed)
-    q = torch.randn((B, Hq, T, D), generator=g).to(torch.bfloat16).contiguous()
-    k = torch.randn((B, Hkv, T, D), generator=g).to(torch.bfloat16).contiguous()
-    v = torch.randn((B, Hkv, T, D), generator=g).to(torch.bfloat16).contiguous()
-    idx = selection_indices(B, Hkv, T, block_size, S, g)
+               seed: int = 0, device: str = "cpu"):
+    """``(q, k, v, block_idx)`` of the NSA recipe (bf16 / int32).  q, k, v
+    are drawn on ``device`` (CPU by default); block_idx is always drawn on
+    the host (with the same generator on CPU, a CPU generator of the same
+    seed otherwise)."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    q = torch.randn((B, Hq, T, D), generator=g, device=device).to(torch.bfloat16).contiguous()
+    k = torch.randn((B, Hkv, T, D), generator=g, device=device).to(torch.bfloat16).contiguous()
+    v = torch.randn((B, Hkv, T, D), generator=g, device=device).to(torch.bfloat16).contiguous()
+    gi = g if torch.device(device).type == "cpu" else torch.Generator().manual_seed(seed)
+    idx = selection_indices(B, Hkv, T, block_size, S, gi)
     return q, k, v, idx
 
 
