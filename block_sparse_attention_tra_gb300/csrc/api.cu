@@ -4,6 +4,7 @@
 // returns an error without touching the device.
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/bsa.h"
@@ -129,15 +130,15 @@ int encode_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
 
 int sm_count() {
   constexpr int MAX_DEVICES = 64;
-  static int counts[MAX_DEVICES] = {};
+  static std::atomic<int> counts[MAX_DEVICES] = {};  // 0 = not read yet; callers may race, all store one value
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return 0;
-  if (counts[dev] == 0) {
-    int n = 0;
+  int n = counts[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    counts[dev] = n;
+    counts[dev].store(n, std::memory_order_relaxed);
   }
-  return counts[dev];
+  return n;
 }
 
 }  // namespace bsa
@@ -213,8 +214,7 @@ int tra_backward(const void* q, const void* k, const void* v, const void* dout, 
   return launch_tra_bwd_bf16(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, stream);
 }
 
-// Argument checks of tra_diff_forward_noalloc (the same checks, in the same
-// order, as tra_diff_forward).
+// Argument checks of tra_diff_forward and tra_diff_forward_noalloc.
 static int check_diff_args(const void* q1, const void* q2, const void* k1, const void* k2, const void* v,
                            const void* out, int B, int H, int T, int D, float beta, float lambda, float p,
                            int dtype) {
@@ -236,18 +236,8 @@ static int check_diff_args(const void* q1, const void* q2, const void* k1, const
 int tra_diff_forward(const void* q1, const void* q2, const void* k1, const void* k2, const void* v, void* out, int B,
                      int H, int T, int D, float beta, float lambda, float p, int normalize, int dtype,
                      cudaStream_t stream) {
-  if (q1 == nullptr || q2 == nullptr || k1 == nullptr || k2 == nullptr || v == nullptr || out == nullptr)
-    return BSA_ERR_NULLPTR;
-  if (dtype != BSA_F32 && dtype != BSA_BF16) return BSA_ERR_DTYPE;
-  if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
-  if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
-  if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
-  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
-  if (dtype != BSA_BF16) return BSA_ERR_UNSUPPORTED;
-  if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f) || isnan(lambda)) return BSA_ERR_UNSUPPORTED;
-  const void* ptrs[6] = {q1, q2, k1, k2, v, out};
-  for (const void* ptr : ptrs)
-    if (!aligned16(ptr)) return BSA_ERR_ALIGN;
+  const int chk = check_diff_args(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, dtype);
+  if (chk != BSA_OK) return chk;
   const int dvs = check_device();
   if (dvs != OK) return dvs;
   if (!normalize) return launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, nullptr, stream);
