@@ -33,7 +33,8 @@ int encode_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
                       uint32_t box0, uint32_t box1);
 
 // Streaming multiprocessors of the current device (cached per device; 0 if
-// the query fails).  Persistent kernels size their grids with it.
+// the query fails).  Persistent kernels size their grids with it, the
+// head-grouped block orders their group sizes.
 int sm_count();
 
 // Threshold rectified attention, fp32 CUDA-core kernel.
