@@ -236,9 +236,16 @@ __global__ void __launch_bounds__(FSA_THREADS, 1)
   const uint32_t tmem = *tptr;
 
   if (warp >= FSA_PROD_WARP0 && warp < FSA_MMA_WARP) {
-    // ---- Q gather: thread r copies row r (query r / G, head r % G) of every tile.
+    // ---- Q gather.  Thread r resolves row r (query r / G, head r % G) of each
+    // tile; the copies go row by row, CPR consecutive lanes taking the 16-byte
+    // chunks of one row, so that a warp instruction reads whole rows (two at
+    // D = 128, four at D = 64) instead of one chunk of 32 different rows.
+    constexpr int CPR = D / 8;      // 16-byte chunks per row
+    constexpr int RPI = 32 / CPR;   // rows per warp instruction
     const int r = threadIdx.x - FSA_PROD_WARP0 * 32;
     const int qi = r / G, g = r % G;
+    const int row0 = r & ~31;       // first row of this warp
+    const int c = lane % CPR;       // this lane's chunk of every row it copies
     const size_t head_row0 = (static_cast<size_t>(b) * Hq + static_cast<size_t>(hkv) * G + g) * T;
     bool ok = true;
     int issued = 0;
@@ -248,12 +255,16 @@ __global__ void __launch_bounds__(FSA_THREADS, 1)
       const int slot = t * qpt + qi;
       const bool valid = qi < qpt && slot < npairs;
       const int i = valid ? (list[first + slot] >> 5) : 0;
-      const __nv_bfloat16* src = q + (head_row0 + i) * D;
-      const uint32_t dst = smem_u32(smem + L::Q_OFF + st * L::Q_TILE) + r * 128;
+      const unsigned long long src = reinterpret_cast<unsigned long long>(q + (head_row0 + i) * D);
+      const uint32_t tile = smem_u32(smem + L::Q_OFF + st * L::Q_TILE);
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint32_t cc = c & 7;
-        cp_async16(dst + (c >> 3) * PANEL + ((cc ^ (r & 7)) << 4), src + c * 8, valid ? 16u : 0u);
+      for (int k = 0; k < 32 / RPI; ++k) {
+        const int from = k * RPI + lane / CPR;  // lane holding the row copied now
+        const int rr = row0 + from;
+        const unsigned long long rsrc = __shfl_sync(0xffffffffu, src, from);
+        const bool rvalid = __shfl_sync(0xffffffffu, valid, from);
+        const uint32_t dst = tile + rr * 128 + (c >> 3) * PANEL + (((c & 7) ^ (rr & 7)) << 4);
+        cp_async16(dst, reinterpret_cast<const __nv_bfloat16*>(rsrc) + c * 8, rvalid ? 16u : 0u);
       }
       cp_async_commit();
       issued = t + 1;
