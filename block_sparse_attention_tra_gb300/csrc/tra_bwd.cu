@@ -22,6 +22,9 @@
 // S = Q_m K_n^T and dP = dO_m V_n^T; the epilogue (thread = query row) forms
 // dA; then dQ += dA K_n.  TMEM: S [0,128), dP [128,256), dQ [256,256+D).
 //
+// Both grids number their blocks in head groups (tile::head_group_item): the
+// CTAs resident at one time stream the tiles of a few heads, which stay in L2.
+//
 // Both kernels produce each 128 x 128 score (and gradient) tile in two
 // 64-column halves h that behave like two tiles: the epilogue turns half h
 // into bf16 while the other half's products run, and the products that read

@@ -19,6 +19,8 @@
 //               two issuers measured slower).
 //   warps 4t..  epilogue of stream t (thread = query row).
 // TMEM: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// The grid numbers its blocks in head groups (tile::head_group_item), so the
+// CTAs resident at one time stream the K/V tiles of a few heads from L2.
 //
 // Normalisation does not rewrite q or k: with r(x) = 1 / max(||x||, 1e-12)
 // the normalised score is s_ij r(q_i) r(k_j).  A pre-pass kernel writes r()
