@@ -146,6 +146,19 @@ def dist_info():
     return rank, world, local
 
 
+def clocks_rejected(c: dict) -> bool:
+    """A timed region is not a valid measurement when the GPU throttled for
+    hardware or thermal reasons, or when its SM clock sat well below the
+    maximum with no reason given (a clock left locked by an earlier user).
+    sw_power_cap is normal under a dense tensor load and is kept."""
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    reasons = set(c.get("reasons") or [])
+    if bad & reasons:
+        return True
+    mhz, mx = c.get("sm_mhz"), c.get("sm_max_mhz")
+    return bool(mhz and mx and mhz < 0.8 * mx and not (reasons - {"unsampled"}))
+
+
 def reduce_max(value: float, world: int, device=None) -> float:
     """Max of a float over all ranks (identity for a single process)."""
     if world == 1:
@@ -316,9 +329,17 @@ def run_ours(args):
     out = torch.empty_like(dev[0])
     fn = launcher(w, dev, out)
 
-    # ---- device-resident timing of the headline workload
+    # ---- device-resident timing of the headline workload; a region whose
+    # clocks show throttling (on any rank) is measured once more
     with ClockSampler(device.index) as cs:
         total_ms = time_resident(fn, args.steps, args.warmup, world, soak_s=args.clock_soak)
+    clocks = cs.summary()
+    remeasured = reduce_max(1.0 if clocks_rejected(clocks) else 0.0, world, device) > 0
+    if remeasured:
+        rejected = clocks
+        with ClockSampler(device.index) as cs:
+            total_ms = time_resident(fn, args.steps, args.warmup, world, soak_s=args.clock_soak)
+        clocks = dict(cs.summary(), remeasured_after=rejected)
     total_ms = reduce_max(total_ms, world, device)
     ms = total_ms / args.steps
     flops_all = w.flops * world
@@ -385,7 +406,7 @@ def run_ours(args):
                          "kernels)" if isinstance(w, workloads.TraWorkload) else
                          "pinned host -> device copies, nsa_select_forward, device -> host copy")},
         "gpu_launches": args.steps,
-        "clocks": cs.summary(),
+        "clocks": clocks,
     }
 
     # ---- secondary workloads (measured, reported beside the headline)

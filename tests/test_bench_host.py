@@ -94,3 +94,18 @@ def test_reference_arm_prints_one_json_line():
     for key, val in {"workload": "tra_f32_B1_H2_T256_D64", "B": 1, "H": 2, "T": 256, "D": 64}.items():
         assert d["config"][key] == val
     assert "sample" in d["config"]
+
+
+def test_clock_records_that_reject_a_measurement():
+    import bench
+
+    # a power cap under a dense tensor load is normal and kept
+    assert not bench.clocks_rejected({"sm_mhz": 1927.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]})
+    assert not bench.clocks_rejected({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []})
+    # hardware or thermal slowdowns are rejected
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert bench.clocks_rejected({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [r, "sw_power_cap"]})
+    # clocks stuck well below the maximum with no reason: a leftover clock lock
+    assert bench.clocks_rejected({"sm_mhz": 1200.0, "sm_max_mhz": 2070.0, "reasons": []})
+    # no samples (no nvidia-smi): nothing to judge
+    assert not bench.clocks_rejected({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]})
