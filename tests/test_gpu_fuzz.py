@@ -3,7 +3,8 @@
 The parity files check chosen shapes; these draw sizes, powers and group
 sizes from a fixed seed so that many combinations of tile counts, ragged
 tails, work items per CTA and MMA-issuer organisations (one issuer for the
-general and half powers, one per query tile for p = 1, 2) are exercised.
+general and half powers, one per query tile for p = 1, 2) are exercised, for
+the forwards, the backward and the differential forward.
 Bars: bf16 max|gpu - ref| <= 2e-2 * max|ref|, fp32 <= 1e-4 * max|ref|;
 NSA lse within 1e-2 on rows with a valid key; the host-buffer path must be
 bit-identical to the device path.
@@ -95,3 +96,43 @@ def test_tra_host_random_shapes(B, H, T, D):
     want = bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), 0.8, 2.0)
     torch.cuda.synchronize()
     assert torch.equal(got, want.cpu())
+
+
+# Backward and differential forward: a second seeded stream, so the cases
+# above stay as they are.  The backward draws p >= 1 only: for p < 1 the
+# gradient p x^(p-1) is unbounded as x -> 0+, and an element-wise bar
+# relative to max|ref| would then judge the rounding of x itself.
+_rng2 = np.random.default_rng(20261203)
+BWD_CASES = [(int(_rng2.integers(1, 3)), int(_rng2.integers(1, 4)), int(_rng2.integers(1, 600)),
+              int(_rng2.choice([64, 128])), round(float(_rng2.uniform(-0.5, 2.0)), 3),
+              float(_rng2.choice([1.0, 2.0, 1.5, 2.5, 3.0]))) for _ in range(8)]
+DIFF_CASES = [(int(_rng2.integers(1, 3)), int(_rng2.integers(1, 4)), int(_rng2.integers(1, 600)),
+               int(_rng2.choice([64, 128])), round(float(_rng2.uniform(-0.3, 1.0)), 3),
+               round(float(_rng2.uniform(-0.5, 1.5)), 3), float(_rng2.choice([1.0, 2.0, 1.5, 0.7])),
+               bool(_rng2.integers(0, 2))) for _ in range(8)]
+
+
+@pytest.mark.parametrize("B,H,T,D,beta,p", BWD_CASES)
+def test_tra_backward_random_shapes(B, H, T, D, beta, p):
+    q, k, v = workloads.tra_inputs(B, H, T, D, "bf16", seed=T * 7 + D)
+    do = torch.randn((B, H, T, D), generator=torch.Generator().manual_seed(T + 1)).to(torch.bfloat16)
+    grads = bsa.tra_backward(q.cuda(), k.cuda(), v.cuda(), do.cuda(), beta, p)
+    torch.cuda.synchronize()
+    refs = otra.tra_backward(f64(q), f64(k), f64(v), f64(do), beta, p)
+    for name, g, ref in zip(("dq", "dk", "dv"), grads, refs):
+        err = rel_err(f64(g), ref)
+        assert err <= 2e-2, f"{name}: max err {err:.3e} of max|ref|"
+
+
+@pytest.mark.parametrize("B,H,T,D,beta,lam,p,norm", DIFF_CASES)
+def test_tra_diff_random_shapes(B, H, T, D, beta, lam, p, norm):
+    q1, k1, v = workloads.tra_inputs(B, H, T, D, "bf16", seed=T * 5 + D)
+    q2, k2, _ = workloads.tra_inputs(B, H, T, D, "bf16", seed=T * 5 + D + 1)
+    out = bsa.tra_diff_forward(q1.cuda(), q2.cuda(), k1.cuda(), k2.cuda(), v.cuda(), beta, lam, p, normalize=norm)
+    torch.cuda.synchronize()
+    ref = otra.tra_diff_forward(f64(q1), f64(q2), f64(k1), f64(k2), f64(v), beta, lam, p, normalize=norm)
+    if float(np.abs(ref).max()) == 0.0:  # every score under its threshold: the output is exactly zero
+        assert float(out.abs().max()) == 0.0
+        return
+    err = rel_err(f64(out), ref)
+    assert err <= 2e-2, f"max err {err:.3e} of max|ref|"
