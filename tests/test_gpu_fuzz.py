@@ -112,6 +112,33 @@ DIFF_CASES = [(int(_rng2.integers(1, 3)), int(_rng2.integers(1, 4)), int(_rng2.i
                bool(_rng2.integers(0, 2))) for _ in range(8)]
 
 
+# NSA selection for head dims and block sizes other than (D in {64, 128},
+# 64-token blocks): the general query-outer kernel.
+NSA_GEN_CASES = []
+for _ in range(8):
+    bs = int(_rng2.choice([16, 32, 64, 128]))
+    D = int(_rng2.choice([16, 32, 64, 128]))
+    if bs == 64 and D in (64, 128):
+        D = 32  # that pair runs on the TMA kernel, covered above
+    G, Hkv = int(_rng2.choice([1, 3, 8, 16])), int(_rng2.integers(1, 3))
+    NSA_GEN_CASES.append((int(_rng2.integers(1, 3)), G * Hkv, Hkv, bs * int(_rng2.integers(1, 12)), D, bs,
+                          int(_rng2.integers(1, 17))))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,T,D,bs,S", NSA_GEN_CASES)
+def test_nsa_general_random_shapes(B, Hq, Hkv, T, D, bs, S):
+    q, k, v, idx = workloads.nsa_inputs(B, Hq, Hkv, T, D, bs, S, seed=Hq * 10 + T + S + D)
+    ro, rl = onsa.nsa_select_forward(f64(q), f64(k), f64(v), idx.numpy(), bs)
+    o, lse = bsa.nsa_select_forward(q.cuda(), k.cuda(), v.cuda(), idx.cuda(), bs, return_lse=True)
+    torch.cuda.synchronize()
+    err = rel_err(f64(o), ro)
+    assert err <= 2e-2, f"max err {err:.3e} of max|ref|"
+    gl, valid = f64(lse), rl != -1e9
+    assert np.all(gl[~valid] == -1e9)
+    if np.any(valid):
+        assert float(np.abs(gl[valid] - rl[valid]).max()) <= 1e-2
+
+
 @pytest.mark.parametrize("B,H,T,D,beta,p", BWD_CASES)
 def test_tra_backward_random_shapes(B, H, T, D, beta, p):
     q, k, v = workloads.tra_inputs(B, H, T, D, "bf16", seed=T * 7 + D)
