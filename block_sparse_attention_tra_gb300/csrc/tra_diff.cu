@@ -83,7 +83,7 @@ struct Ring {
 
 // 1 / max(||row||_2, 1e-12) for every row of the four inputs into
 // inv[which][bh][Tp] (0 for the padding rows t >= T).  Eight threads per row,
-// eight rows per warp and pass (two groups of four, whose 16-byte loads are
+// sixteen rows per warp and pass (four groups of four, whose 16-byte loads are
 // all issued before any arithmetic), fp32 sums of the squared bf16 elements;
 // the warps stride over the rows, and every lane takes part in every shuffle
 // (rows past the end contribute zeros and store nothing).
@@ -99,33 +99,47 @@ __device__ __forceinline__ float sumsq_bf16x8(const uint4& u) {
   return acc;
 }
 
-template <int D>
+constexpr int NORM_NG = 4;  // groups of four rows per warp and pass
+
+// Row index -> (input, head, position).  Idx is 32-bit when the four inputs'
+// padded rows fit (no 64-bit division), 64-bit otherwise.
+template <typename Idx>
+__device__ __forceinline__ void norm_row(long long row, long long rows_p, int Tp, int& which, long long& bh, int& t) {
+  const Idx r = static_cast<Idx>(row), rp = static_cast<Idx>(rows_p);
+  which = static_cast<int>(r / rp);
+  const Idx rem = r - static_cast<Idx>(which) * rp;
+  const Idx b = rem / static_cast<Idx>(Tp);
+  bh = static_cast<long long>(b);
+  t = static_cast<int>(rem - b * static_cast<Idx>(Tp));
+}
+
+template <int D, typename Idx>
 __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* __restrict__ a0,
                                                            const __nv_bfloat16* __restrict__ a1,
                                                            const __nv_bfloat16* __restrict__ a2,
                                                            const __nv_bfloat16* __restrict__ a3,
                                                            float* __restrict__ inv, int BH, int T, int Tp) {
   constexpr int CH = D / 64;  // 16-byte chunks per lane per row
+  constexpr int NG = NORM_NG;
   const int lane = threadIdx.x & 31, sub = lane & 7;
   const long long rows_p = static_cast<long long>(BH) * Tp;
   const long long total = 4 * rows_p;
   const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  for (long long base = warp0 * 8; base < total; base += nwarps * 8) {
-    long long row[2];
-    bool live[2];
-    uint4 u[2][CH];
+  for (long long base = warp0 * 4 * NG; base < total; base += nwarps * 4 * NG) {
+    long long row[NG];
+    bool live[NG];
+    uint4 u[NG][CH];
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
+    for (int g = 0; g < NG; ++g) {
       row[g] = base + 4 * g + (lane >> 3);
       live[g] = false;
 #pragma unroll
       for (int c = 0; c < CH; ++c) u[g][c] = make_uint4(0u, 0u, 0u, 0u);
       if (row[g] < total) {
-        const int which = static_cast<int>(row[g] / rows_p);
-        const long long rem = row[g] - static_cast<long long>(which) * rows_p;
-        const long long bh = rem / Tp;
-        const int t = static_cast<int>(rem - bh * Tp);
+        int which, t;
+        long long bh;
+        norm_row<Idx>(row[g], rows_p, Tp, which, bh, t);
         live[g] = t < T;
         if (live[g]) {
           const __nv_bfloat16* src = which == 0 ? a0 : which == 1 ? a1 : which == 2 ? a2 : a3;
@@ -136,7 +150,7 @@ __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* 
       }
     }
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
+    for (int g = 0; g < NG; ++g) {
       float acc = 0.0f;
 #pragma unroll
       for (int c = 0; c < CH; ++c) acc += sumsq_bf16x8(u[g][c]);
@@ -459,19 +473,24 @@ int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const v
   const bool norm = inv_norm != nullptr;
   if (norm) {
     const int Tp = ((T + BT - 1) / BT) * BT;
-    const long long rows = 4LL * BH * Tp;  // 64 rows per 256-thread block per pass
+    const long long rows = 4LL * BH * Tp;  // 32 * NORM_NG rows per 256-thread block per pass
     const int sms = sm_count();
     if (sms <= 0) return ERR_DEVICE;
-    const long long want = (rows + 63) / 64, cap = 8LL * sms;
+    const long long want = (rows + 32 * NORM_NG - 1) / (32 * NORM_NG), cap = 8LL * sms;
     const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
     const auto* a0 = static_cast<const __nv_bfloat16*>(q1);
     const auto* a1 = static_cast<const __nv_bfloat16*>(k1);
     const auto* a2 = static_cast<const __nv_bfloat16*>(q2);
     const auto* a3 = static_cast<const __nv_bfloat16*>(k2);
-    if (D == 128)
-      row_inv_norm_kernel<128><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv_norm, BH, T, Tp);
+    const bool idx32 = rows < (1LL << 32);  // every row index (and the division by Tp) fits 32 bits
+    if (D == 128 && idx32)
+      row_inv_norm_kernel<128, uint32_t><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv_norm, BH, T, Tp);
+    else if (D == 128)
+      row_inv_norm_kernel<128, unsigned long long><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv_norm, BH, T, Tp);
+    else if (idx32)
+      row_inv_norm_kernel<64, uint32_t><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv_norm, BH, T, Tp);
     else
-      row_inv_norm_kernel<64><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv_norm, BH, T, Tp);
+      row_inv_norm_kernel<64, unsigned long long><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv_norm, BH, T, Tp);
     if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
   }
   if (D == 128)
