@@ -5,13 +5,13 @@
 
 A step is one pass of the whole threshold-rectified-attention (TRA) path --
 tau table, Q K^T, causal mask, threshold and power, W V, store -- fused in one
-kernel launch, over one batch of synthetic input of the workload (default:
-bf16 B=4 H=16 T=4096 D=128, beta=1, p=2).  Inputs are resident in HBM when the
-timed region starts; the inputs plus output (268 MB) are larger than the
+kernel launch, over one batch of synthetic input of the workload.  Inputs are resident in HBM when the
+timed region starts; the inputs plus output (256 MB) are larger than the
 129 MB L2, so no flush is done between steps of the headline workload.  The
-secondary workloads (the T=8192 general-power TRA and both NSA selection
-workloads) are measured in the same run with an L2 flush between iterations
-and reported under ``secondary``.
+default workload is the T=8192 one: bf16 B=2 H=32 T=8192 D=64, beta=2 and the
+general power p=1.5 on the exp/log path.  The secondary workloads (the
+B=4 H=16 T=4096 D=128 p=2 TRA and the NSA selection workloads) are measured
+in the same run and reported under ``secondary``.
 
 Multi-GPU (torchrun): every rank runs the same workload on its own GPU with no
 collective on the data path (the work is independent per (batch, head));
@@ -35,9 +35,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "causal fwd TFLOP/s & % of dense BF16 tensor peak (threshold attn; NSA select)"
-DEFAULT_WORKLOAD = "tra_bf16_B4_H16_T4096_D128"
-SECONDARY = ["tra_bf16_B2_H32_T8192_D64", "nsa_bf16_B2_Hq32_Hkv2_T8192_D128", "nsa_bf16_B1_Hq64_Hkv4_T32768_D128",
+DEFAULT_WORKLOAD = "tra_bf16_B2_H32_T8192_D64"
+SECONDARY = ["tra_bf16_B4_H16_T4096_D128", "nsa_bf16_B2_Hq32_Hkv2_T8192_D128", "nsa_bf16_B1_Hq64_Hkv4_T32768_D128",
              "nsa_bf16_B2_Hq32_Hkv2_T8192_D32_bs32"]
+# Shape of the widened rows' lines (training backward, differential forward).
+WIDENED_WORKLOAD = "tra_bf16_B4_H16_T4096_D128"
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = {
     "tra": "block_sparse_attention_tra_gb300/csrc/tra_bf16.cu",
@@ -212,6 +214,31 @@ def workload_config(w, world):
             "l2": "no flush (unique K/V stays in L2 by design; gathered bytes counted)", "parallelism": par}
 
 
+def measure_l2_read_gbs(device, mb: int = 48, reps: int = 40):
+    """L2 read bandwidth of this GPU, measured here: the library's streaming-
+    read probe (16-byte loads that skip L1, four CTAs per SM) over a buffer of
+    `mb` MB that the 129 MB L2 holds, read once to warm it and then `reps`
+    times between CUDA events.  Returns (GB/s, description)."""
+    import torch
+
+    from block_sparse_attention_tra_gb300 import bsa
+
+    buf = torch.ones(mb * 2**20 // 4, dtype=torch.float32, device=device)
+    sink = torch.zeros(1, dtype=torch.int32, device=device)
+    best = 0.0
+    for _ in range(3):
+        bsa.read_probe(buf, 2, sink)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        bsa.read_probe(buf, reps, sink)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, mb * 2**20 * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    how = (f"bsa_read_probe: {mb} MB L2-resident buffer read {reps} times per launch with 16-byte L1-bypassing "
+           f"loads, 4 CTAs/SM, best of 3, CUDA events")
+    return round(best, 1), how
+
+
 def roofline_for(w, ms_per_launch, pk, sustained: bool, fsa: bool = False):
     from block_sparse_attention_tra_gb300 import workloads
 
@@ -228,14 +255,23 @@ def roofline_for(w, ms_per_launch, pk, sustained: bool, fsa: bool = False):
     achieved = w.algorithmic_bytes / (ms_per_launch * 1e-3) / 1e9
     general = not (w.block_size == 64 and w.D in (64, 128))  # shapes the general kernel serves
     kind = "fsa" if fsa else "nsa_general" if general else "nsa"
-    r = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-         "frac": round(achieved / pk["hbm_gbs"], 4), "peak_kind": "copy bandwidth of " + pk["source"],
-         "traffic": ncu_traffic(kind, ("fsa:" if fsa else "") + w.name),
-         "kernel": ("fsa_blockouter_kernel + fsa_combine_kernel" if fsa else
-                    "nsa_general_kernel" if general else "nsa_select_kernel"),
-         "algorithmic_bytes_per_launch": w.algorithmic_bytes,
-         "tflops": round(w.flops / (ms_per_launch * 1e-3) / 1e12, 2),
-         "unique_bytes_per_launch": w.unique_bytes}
+    common = {"traffic": ncu_traffic(kind, ("fsa:" if fsa else "") + w.name),
+              "kernel": ("fsa_blockouter_kernel + fsa_combine_kernel" if fsa else
+                         "nsa_general_kernel" if general else "nsa_select_kernel"),
+              "algorithmic_bytes_per_launch": w.algorithmic_bytes,
+              "tflops": round(w.flops / (ms_per_launch * 1e-3) / 1e12, 2),
+              "unique_bytes_per_launch": w.unique_bytes,
+              "hbm": {"peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                      "peak_kind": "copy bandwidth of " + pk["source"]}}
+    if pk.get("l2_read_gbs") and not fsa:
+        # The gathered K/V (the bulk of the algorithmic bytes) is served from
+        # L2: the unique K/V fits it, and DRAM reads stay near the unique bytes.
+        r = {"bound": "l2", "achieved": round(achieved, 1), "peak": pk["l2_read_gbs"], "unit": "GB/s",
+             "frac": round(achieved / pk["l2_read_gbs"], 4), "peak_kind": pk["l2_how"]}
+    else:
+        r = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+             "frac": round(achieved / pk["hbm_gbs"], 4), "peak_kind": "copy bandwidth of " + pk["source"]}
+    r.update(common)
     if fsa:
         # The split-K form also writes and re-reads its fp32 partials
         # (m, l and a D-vector per (query, selected block, head)).
@@ -418,6 +454,8 @@ def run_ours(args):
 
         sec = []
         sfu_clock = None
+        pk["l2_read_gbs"], pk["l2_how"] = measure_l2_read_gbs(device)
+        result["l2_read_gbs_measured"] = {"value": pk["l2_read_gbs"], "how": pk["l2_how"]}
         for name in SECONDARY:
             del dev, out
             torch.cuda.empty_cache()
@@ -464,7 +502,7 @@ def run_ours(args):
         # fused differential forward (two score streams, with normalisation).
         del dev, out
         torch.cuda.empty_cache()
-        wb = workloads.TRA_WORKLOADS[DEFAULT_WORKLOAD]
+        wb = workloads.TRA_WORKLOADS[WIDENED_WORKLOAD]
         qb, kb, vb = (t.to(device) for t in workloads.workload_inputs(wb))
         gen = torch.Generator(device="cpu").manual_seed(1)
         dob = torch.randn(qb.shape, generator=gen).to(torch.bfloat16).to(device)
@@ -509,56 +547,78 @@ def run_ours(args):
 
 # ------------------------------------------------------------ CPU oracle leg
 
-def cpu_baseline(w, host, budget_s=15.0):
-    """Time the float64 oracle on the host cores on a bounded sample of the
-    same workload: whole (b, h) heads (TRA) or query rows (NSA), until about
-    `budget_s` seconds have passed.  Returns the metric in the same unit."""
+def oracle_units(w, host, n, seed=0):
+    """Run the float64 oracle on the first ``n`` units of the workload --
+    whole (b, h) heads for TRA, seeded random query groups for NSA -- and
+    return the algorithmic FLOPs of that work (4 D per causal pair and head)."""
     import numpy as np
 
     from block_sparse_attention_tra_gb300 import workloads
     from oracle import nsa as onsa
     from oracle import tra as otra
 
-    cores = len(os.sched_getaffinity(0))
     if isinstance(w, workloads.TraWorkload):
         q, k, v = host
-        done, flops, heads = 0.0, 0, 0
-        t0 = time.perf_counter()
-        for b in range(w.B):
-            for h in range(w.H):
-                qq = q[b:b + 1, h:h + 1].double().numpy()
-                kk = k[b:b + 1, h:h + 1].double().numpy()
-                vv = v[b:b + 1, h:h + 1].double().numpy()
-                otra.tra_forward(qq, kk, vv, w.beta, w.p)
-                flops += otra.tra_flops(1, 1, w.T, w.D)
-                heads += 1
-                done = time.perf_counter() - t0
-                if done >= budget_s:
-                    break
-            if done >= budget_s:
-                break
-        return {"value": round(flops / done / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                "sample": f"{heads} of {w.B * w.H} (b,h) heads of {w.name}, float64 numpy/BLAS, {done:.1f} s"}
+        flops = 0
+        for u in range(n):
+            b, h = divmod(u % (w.B * w.H), w.H)
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            otra.tra_forward(q[sl].double().numpy(), k[sl].double().numpy(), v[sl].double().numpy(), w.beta, w.p)
+            flops += otra.tra_flops(1, 1, w.T, w.D)
+        return flops
     q, k, v, idx = host
     G = w.G
-    rng = np.random.default_rng(0)
-    t0 = time.perf_counter()
-    n, pairs = 0, 0
-    while time.perf_counter() - t0 < budget_s:
+    rng = np.random.default_rng(seed)
+    pairs = 0
+    for _ in range(n):
         b, g, i = int(rng.integers(w.B)), int(rng.integers(w.Hkv)), int(rng.integers(w.T))
         toks = onsa.selected_tokens(idx[b, g, i].numpy(), i, w.block_size)
         onsa.softmax_attend(q[b, g * G:(g + 1) * G, i].double().numpy(), k[b, g, toks].double().numpy(),
                             v[b, g, toks].double().numpy(), w.D ** -0.5)
-        n += 1
         pairs += toks.size
+    return 4 * G * w.D * pairs
+
+
+def oracle_sample_size(w, host, budget_s):
+    """Units of work (heads or query groups) the oracle gets through in about
+    ``budget_s`` seconds on this host, from one timed calibration call."""
+    from block_sparse_attention_tra_gb300 import workloads
+
+    probe = 1 if isinstance(w, workloads.TraWorkload) else 64
+    t0 = time.perf_counter()
+    oracle_units(w, host, probe, seed=1)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    return max(1, int(budget_s / dt * probe))
+
+
+def unit_name(w, n):
+    from block_sparse_attention_tra_gb300 import workloads
+
+    if isinstance(w, workloads.TraWorkload):
+        return f"{n} of {w.B * w.H} (b,h) heads of {w.name}"
+    return f"{n} seeded random query groups (G={w.G} heads each) of {w.name}"
+
+
+def cpu_baseline(w, host, budget_s=15.0):
+    """Time the float64 oracle on the host cores on a bounded sample of the
+    same workload (whole heads for TRA, query groups for NSA), about
+    ``budget_s`` seconds of work.  Returns the metric in the same unit."""
+    cores = len(os.sched_getaffinity(0))
+    n = oracle_sample_size(w, host, budget_s)
+    t0 = time.perf_counter()
+    flops = oracle_units(w, host, n)
     done = time.perf_counter() - t0
-    return {"value": round(4 * G * w.D * pairs / done / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
-            "kind": "oracle", "sample": f"{n} random query groups of {w.name}, float64 numpy, {done:.1f} s"}
+    return {"value": round(flops / done / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{unit_name(w, n)}, float64 numpy/BLAS, {done:.1f} s"}
 
 
 def run_reference(args):
-    """The reference arm: the float64 CPU oracle, timed on the host cores on a
-    bounded sample of the same workload (rank 0 only)."""
+    """The reference arm: the float64 CPU oracle on the host cores (rank 0
+    only).  Every step runs the same bounded sample of the workload (whole
+    heads for TRA, query groups for NSA), sized once before the warm-up so
+    that the whole run takes a few minutes; ``ms_per_step`` is the measured
+    time of that sampled work and ``value`` its FLOPs over that time --
+    nothing is scaled up to the full workload."""
     rank, world, _ = dist_info()
     if rank != 0:
         return None
@@ -566,31 +626,39 @@ def run_reference(args):
 
     w = workloads.TRA_WORKLOADS.get(args.workload) or workloads.NSA_WORKLOADS[args.workload]
     host = workloads.workload_inputs(w)
-    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    per_step = min(6.0, max(1.0, 150.0 / max(1, args.steps + args.warmup)))
+    n = oracle_sample_size(w, host, per_step)
     for _ in range(args.warmup):
-        cpu_baseline(w, host, budget_s=min(2.0, per_step))
-    vals = [cpu_baseline(w, host, budget_s=per_step) for _ in range(args.steps)]
-    value = statistics.median(v["value"] for v in vals)
-    cb = dict(vals[0])
-    cb["value"] = value
-    flops_per_step = w.flops
+        oracle_units(w, host, n)
+    times, flops = [], 0
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        flops = oracle_units(w, host, n)
+        times.append(time.perf_counter() - t0)
+    total_s = time.perf_counter() - t_all
+    ms = total_s / args.steps * 1e3
+    value = flops / (ms * 1e-3) / 1e12
+    cores = len(os.sched_getaffinity(0))
     return {
         "impl": "reference",
         "metric": METRIC,
-        "value": value,
+        "value": round(value, 6),
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(flops_per_step / (value * 1e12) * 1e3, 3) if value else None,
+        "ms_per_step": round(ms, 3),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) q,k,v; no dataset)",
-        "config": dict(workload_config(w, world), sample="bounded per step; see cpu_baseline.sample"),
-        "cpu_baseline": cb,
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "config": workload_config(w, world),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": (f"each step: {unit_name(w, n)} ({flops:.4g} FLOP), float64 numpy/BLAS; "
+                                    f"median step {statistics.median(times):.2f} s")},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
 

@@ -8,6 +8,7 @@ raise.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -49,7 +50,25 @@ def load_library():
     global _LIB
     if _LIB is not None:
         return _LIB
-    path = library_path()
+    _LIB = open_library(library_path())
+    return _LIB
+
+
+@contextlib.contextmanager
+def using_library(path):
+    """Route every call of this module, inside the ``with`` block, to the
+    library at ``path`` (e.g. the debug build, ``libbsa_debug.so``)."""
+    global _LIB
+    saved = load_library()
+    _LIB = open_library(path)
+    try:
+        yield _LIB
+    finally:
+        _LIB = saved
+
+
+def open_library(path):
+    """Open a build of the library at ``path`` and declare its C signatures."""
     if not os.path.exists(path):
         raise BsaError(f"{path} is not built; run block_sparse_attention_tra_gb300.build.build()")
     lib = ctypes.CDLL(path)
@@ -82,7 +101,12 @@ def load_library():
     lib.bsa_version.restype = i32
     lib.bsa_device_error.argtypes = []
     lib.bsa_device_error.restype = i32
-    _LIB = lib
+    lib.bsa_selftest_wait_timeout.argtypes = [ctypes.c_longlong, vp, vp]
+    lib.bsa_selftest_wait_timeout.restype = i32
+    lib.bsa_selftest_log2.argtypes = [vp, vp, vp, i32, vp]
+    lib.bsa_selftest_log2.restype = i32
+    lib.bsa_read_probe.argtypes = [vp, ctypes.c_size_t, i32, vp, vp]
+    lib.bsa_read_probe.restype = i32
     return lib
 
 
@@ -362,3 +386,37 @@ def nsa_select_forward_fsa(q, k, v, block_idx, block_size: int = 64, out=None, l
                                     workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
     _check(st, "nsa_select_forward_fsa")
     return (out, lse) if return_lse else out
+
+
+def selftest_wait_timeout(limit_cycles: int = 100000, stream=None) -> int:
+    """Run the bounded-wait expiry self test (a wait on an mbarrier nothing
+    arrives on, with a short limit).  Returns the kernel's result word: 0 when
+    the wait gave up as designed.  The timeout is also recorded in the device
+    error word that ``device_error()`` reads and clears."""
+    import torch
+
+    res = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _check(load_library().bsa_selftest_wait_timeout(int(limit_cycles), res.data_ptr(), _stream_handle(stream)),
+           "bsa_selftest_wait_timeout")
+    return int(res.item())
+
+
+def selftest_log2(x, stream=None):
+    """The epilogue's FMA-pipe log2 and CUDA's log2f on the same float32
+    device tensor; returns ``(y_fma, y_ref)``."""
+    import torch
+
+    if not (x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()):
+        raise BsaError("selftest_log2 needs a contiguous float32 CUDA tensor")
+    y_fma, y_ref = torch.empty_like(x), torch.empty_like(x)
+    _check(load_library().bsa_selftest_log2(x.data_ptr(), y_fma.data_ptr(), y_ref.data_ptr(), x.numel(),
+                                            _stream_handle(stream)), "bsa_selftest_log2")
+    return y_fma, y_ref
+
+
+def read_probe(buf, reps: int, sink, stream=None):
+    """Enqueue the streaming-read probe over the bytes of CUDA tensor ``buf``
+    (``reps`` passes); ``sink`` is a 1-element int32 CUDA tensor."""
+    nbytes = buf.numel() * buf.element_size()
+    _check(load_library().bsa_read_probe(buf.data_ptr(), nbytes - nbytes % 16, int(reps), sink.data_ptr(),
+                                         _stream_handle(stream)), "bsa_read_probe")

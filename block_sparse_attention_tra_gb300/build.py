@@ -19,6 +19,11 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbsa.so")
+# The debug build: the same sources compiled with -DBSA_DEBUG, whose kernels
+# check every gather index and TMA coordinate and report a violation through
+# the device error word (code 3) instead of touching memory out of bounds.
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libbsa_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
@@ -41,9 +46,13 @@ def _newest(paths):
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
-    """Compile and link; returns the path of ``libbsa.so``."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, extra_flags=None, debug: bool = False) -> str:
+    """Compile and link; returns the path of ``libbsa.so`` (``libbsa_debug.so``
+    with ``debug=True``)."""
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    if debug:
+        extra_flags = list(extra_flags or []) + ["-DBSA_DEBUG"]
+    os.makedirs(build_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = sorted(glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))
                      + glob.glob(os.path.join(ROOT, "include", "*.h")))
@@ -52,7 +61,7 @@ def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
     flags = NVCC_FLAGS + list(extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         if (not force and os.path.exists(obj)
                 and os.path.getmtime(obj) >= max(os.path.getmtime(src), hdr_time)):
             return obj
@@ -68,16 +77,16 @@ def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, min(len(sources), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, sources))
-    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < _newest(objs):
-        tmp = LIB + ".tmp"
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < _newest(objs):
+        tmp = lib + ".tmp"
         cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -204,13 +204,16 @@ int tra_backward(const void* q, const void* k, const void* v, const void* dout, 
   if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
   if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
-  if (dtype != BSA_BF16) return BSA_ERR_UNSUPPORTED;
   if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f)) return BSA_ERR_UNSUPPORTED;
   const void* ptrs[7] = {q, k, v, dout, dq, dk, dv};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return BSA_ERR_ALIGN;
   const int dvs = check_device();
   if (dvs != OK) return dvs;
+  if (dtype == BSA_F32)
+    return launch_tra_bwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                              static_cast<const float*>(v), static_cast<const float*>(dout), static_cast<float*>(dq),
+                              static_cast<float*>(dk), static_cast<float*>(dv), B, H, T, D, beta, p, stream);
   return launch_tra_bwd_bf16(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, stream);
 }
 
@@ -225,7 +228,6 @@ static int check_diff_args(const void* q1, const void* q2, const void* k1, const
   if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
   if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
-  if (dtype != BSA_BF16) return BSA_ERR_UNSUPPORTED;
   if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f) || isnan(lambda)) return BSA_ERR_UNSUPPORTED;
   const void* ptrs[6] = {q1, q2, k1, k2, v, out};
   for (const void* ptr : ptrs)
@@ -240,6 +242,11 @@ int tra_diff_forward(const void* q1, const void* q2, const void* k1, const void*
   if (chk != BSA_OK) return chk;
   const int dvs = check_device();
   if (dvs != OK) return dvs;
+  if (dtype == BSA_F32)  // no scratch: the fp32 kernel folds the normalisation into its scores
+    return launch_tra_diff_f32(static_cast<const float*>(q1), static_cast<const float*>(q2),
+                               static_cast<const float*>(k1), static_cast<const float*>(k2),
+                               static_cast<const float*>(v), static_cast<float*>(out), B, H, T, D, beta, lambda, p,
+                               normalize != 0, stream);
   if (!normalize) return launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, nullptr, stream);
   // Normalisation factors of every row of q1, k1, q2, k2 (T padded to a
   // multiple of 128): a stream-ordered temporary, released on the same stream.
@@ -260,6 +267,14 @@ int tra_diff_forward_noalloc(const void* q1, const void* q2, const void* k1, con
                              int dtype, cudaStream_t stream) {
   const int chk = check_diff_args(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, dtype);
   if (chk != BSA_OK) return chk;
+  if (dtype == BSA_F32) {  // the fp32 kernel uses no scratch at all
+    const int dvs = check_device();
+    if (dvs != OK) return dvs;
+    return launch_tra_diff_f32(static_cast<const float*>(q1), static_cast<const float*>(q2),
+                               static_cast<const float*>(k1), static_cast<const float*>(k2),
+                               static_cast<const float*>(v), static_cast<float*>(out), B, H, T, D, beta, lambda, p,
+                               normalize != 0, stream);
+  }
   if (normalize && !tra_diff_noalloc_fits(B, H, T)) return BSA_ERR_SCRATCH_LIMIT;
   const int dvs = check_device();
   if (dvs != OK) return dvs;
@@ -317,9 +332,39 @@ const char* bsa_status_string(int status) {
 
 int bsa_version(void) { return 100; }
 
+int bsa_selftest_wait_timeout(long long limit_cycles, int* result, cudaStream_t stream) {
+  if (result == nullptr) return BSA_ERR_NULLPTR;
+  if (limit_cycles < 1 || limit_cycles > 100000000LL) return BSA_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(result) & 3u) != 0) return BSA_ERR_ALIGN;
+  const int dv = check_device();
+  if (dv != OK) return dv;
+  return launch_selftest_wait_timeout(limit_cycles, result, stream);
+}
+
+int bsa_selftest_log2(const float* x, float* y_fma, float* y_ref, int n, cudaStream_t stream) {
+  if (x == nullptr || y_fma == nullptr || y_ref == nullptr) return BSA_ERR_NULLPTR;
+  if (n < 1) return BSA_ERR_SHAPE;
+  const uintptr_t mis = (reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y_fma) |
+                         reinterpret_cast<uintptr_t>(y_ref)) & 3u;
+  if (mis != 0) return BSA_ERR_ALIGN;
+  const int dv = check_device();
+  if (dv != OK) return dv;
+  return launch_selftest_log2(x, y_fma, y_ref, n, stream);
+}
+
+int bsa_read_probe(const void* buf, size_t bytes, int reps, unsigned int* sink, cudaStream_t stream) {
+  if (buf == nullptr || sink == nullptr) return BSA_ERR_NULLPTR;
+  if (bytes < 16 || bytes % 16 != 0 || bytes > (1ull << 40) || reps < 1 || reps > 100000) return BSA_ERR_SHAPE;
+  if (!aligned16(buf) || (reinterpret_cast<uintptr_t>(sink) & 3u) != 0) return BSA_ERR_ALIGN;
+  const int dv = check_device();
+  if (dv != OK) return dv;
+  return launch_read_probe(buf, static_cast<long long>(bytes), reps, sink, stream);
+}
+
 int bsa_device_error(void) {
-  const unsigned codes[6] = {tra_bf16_device_error(), tra_f32_device_error(), nsa_device_error(),
-                             tra_bwd_device_error(), tra_diff_device_error(), nsa_fsa_device_error()};
+  const unsigned codes[7] = {tra_bf16_device_error(), tra_f32_device_error(), nsa_device_error(),
+                             tra_bwd_device_error(), tra_diff_device_error(), nsa_fsa_device_error(),
+                             selftest_device_error()};
   unsigned worst = 0;
   for (unsigned c : codes) {
     if (c == 0xffffffffu) return -1;

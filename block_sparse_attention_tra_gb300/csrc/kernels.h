@@ -50,6 +50,14 @@ int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int 
 int launch_tra_bwd_bf16(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv,
                         int B, int H, int T, int D, float beta, float p, cudaStream_t stream);
 
+// fp32 forms of the backward and of the differential forward (CUDA-core FFMA
+// kernels, tra_f32_ext.cu); the differential one needs no scratch memory.
+int launch_tra_bwd_f32(const float* q, const float* k, const float* v, const float* dout, float* dq, float* dk,
+                       float* dv, int B, int H, int T, int D, float beta, float p, cudaStream_t stream);
+int launch_tra_diff_f32(const float* q1, const float* q2, const float* k1, const float* k2, const float* v,
+                        float* out, int B, int H, int T, int D, float beta, float lam, float p, bool normalize,
+                        cudaStream_t stream);
+
 // Threshold differential attention (fused two-stream kernel).  inv_norm is a
 // float scratch buffer of tra_diff_scratch_bytes(B, H, T) bytes (256-byte
 // aligned) for the row normalisation factors, or null to skip the
@@ -92,6 +100,14 @@ int launch_tra_host(const void* q, const void* k, const void* v, void* out, int 
 int launch_nsa_fsa(const void* q, const void* k, const void* v, const int32_t* block_idx, void* out, float* lse,
                    int B, int Hq, int Hkv, int T, int D, int S, void* workspace, cudaStream_t stream);
 
+// Self tests (selftest.cu): the bounded wait's expiry branch (result = 0 when
+// the wait gave up, 1 if it unexpectedly completed) and the FMA-pipe log2
+// beside CUDA's log2f.
+int launch_selftest_wait_timeout(long long limit_cycles, int* result, cudaStream_t stream);
+int launch_selftest_log2(const float* x, float* y_fma, float* y_ref, int n, cudaStream_t stream);
+// Streaming read of a device buffer `reps` times (L2 / HBM read-rate probe).
+int launch_read_probe(const void* buf, long long bytes, int reps, unsigned int* sink, cudaStream_t stream);
+
 // Read-and-clear of each kernel file's device error word (0 = none,
 // 1 = a bounded wait timed out; 0xffffffff = the read itself failed).
 unsigned int tra_bf16_device_error();
@@ -100,12 +116,21 @@ unsigned int nsa_device_error();
 unsigned int tra_bwd_device_error();
 unsigned int tra_diff_device_error();
 unsigned int nsa_fsa_device_error();
+unsigned int selftest_device_error();
 
 // Power class of the TRA epilogue: p == 1, p == 2, or the general exp2/log2
 // path; and, on request only, p = k + 1/2 (k = 0..3) as x^k sqrt(x).
-enum PowerClass : int { POW_GENERAL = 0, POW_ONE = 1, POW_TWO = 2, POW_HALF0 = 3, POW_HALF3 = 6 };
+// POW_GENERAL_MIX is the general path with part of the log2 evaluations on
+// the FMA pipe instead of the MUFU unit (tra_math.cuh); it serves
+// 1 <= p <= POW_MIX_MAX_P, where its exact zeros and its accuracy hold.
+enum PowerClass : int { POW_GENERAL = 0, POW_ONE = 1, POW_TWO = 2, POW_HALF0 = 3, POW_HALF3 = 6, POW_GENERAL_MIX = 7 };
+constexpr float POW_MIX_MAX_P = 64.0f;
 
-inline int power_class(float p) { return p == 1.0f ? POW_ONE : (p == 2.0f ? POW_TWO : POW_GENERAL); }
+inline int power_class(float p) {
+  if (p == 1.0f) return POW_ONE;
+  if (p == 2.0f) return POW_TWO;
+  return (p >= 1.0f && p <= POW_MIX_MAX_P) ? POW_GENERAL_MIX : POW_GENERAL;
+}
 
 // POW_HALF0 + k for p = k + 1/2 with k in 0..3, else -1.
 inline int half_power_class(float p) {

@@ -35,6 +35,7 @@
 #include <algorithm>
 
 #include "kernels.h"
+#include "nsa_slots.cuh"
 #include "ptx.cuh"
 
 namespace bsa {
@@ -98,10 +99,12 @@ __global__ void fsa_pairs_kernel(const int32_t* __restrict__ block_idx, int* __r
     const long long row = e / S;  // (bh, i)
     const int i = static_cast<int>(row % T);
     if (!slot_live(blk, i, n_blk)) continue;
+    // Set semantics: a block listed again later in the row forms no second pair.
+    if (!nsa_first_occurrence(block_idx + row * S, static_cast<int>(e - row * S), blk)) continue;
     const long long bh = row / T;
     int* c = counter + bh * n_blk + blk;
     if constexpr (FILL) {
-      const int pos = atomicAdd(c, 1);
+      const int pos = debug_index(atomicAdd(c, 1), 0, static_cast<int>(n_slots));
       list[pos] = i * 32 + static_cast<int>(e % S);
     } else {
       atomicAdd(c, 1);
@@ -254,7 +257,7 @@ __global__ void __launch_bounds__(FSA_THREADS, 1)
       if (t >= FSA_NQS && !(ok = mbar_wait(&q_empty[st], ((t / FSA_NQS) - 1) & 1))) break;
       const int slot = t * qpt + qi;
       const bool valid = qi < qpt && slot < npairs;
-      const int i = valid ? (list[first + slot] >> 5) : 0;
+      const int i = valid ? debug_index(list[first + slot] >> 5, 0, T) : 0;
       const unsigned long long src = reinterpret_cast<unsigned long long>(q + (head_row0 + i) * D);
       const uint32_t tile = smem_u32(smem + L::Q_OFF + st * L::Q_TILE);
 #pragma unroll
@@ -283,6 +286,7 @@ __global__ void __launch_bounds__(FSA_THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      debug_check(j >= 0 && j < n_blk);
       mbar_arrive_expect_tx(kv_full, 2 * L::KV_TILE);
 #pragma unroll
       for (int pnl = 0; pnl < L::NP; ++pnl) {
@@ -492,16 +496,14 @@ __global__ void __launch_bounds__(256) fsa_combine_kernel(const int32_t* __restr
   const int i = static_cast<int>((wid / G) % T);
   const long long bh = wid / (static_cast<long long>(G) * T);
   const long long srow = (bh * T + i) * S;  // first slot of (b, hkv, i)
-  bool live = false;
+  // The slots that formed a pair (the first occurrence of each causal block).
+  const unsigned mask = nsa_live_slots(block_idx + srow, S, i, n_blk, FSA_BS).live;
+  const bool live = (mask >> lane) & 1u;
   float m = -INFINITY, l = 0.0f;
-  if (lane < S) {
-    live = slot_live(block_idx[srow + lane], i, n_blk);
-    if (live) {
-      m = pm[(srow + lane) * G + g];
-      l = pl[(srow + lane) * G + g];
-    }
+  if (live) {
+    m = pm[(srow + lane) * G + g];
+    l = pl[(srow + lane) * G + g];
   }
-  const unsigned mask = __ballot_sync(0xffffffffu, live);
   float M = m;
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, d));

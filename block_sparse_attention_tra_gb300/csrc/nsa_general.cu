@@ -20,6 +20,7 @@
 // padded to D + 8 elements so that ldmatrix reads are free of bank conflicts.
 #include "kernels.h"
 #include "mma_sync.cuh"
+#include "nsa_slots.cuh"
 #include "ptx.cuh"
 
 namespace bsa {
@@ -42,10 +43,6 @@ struct GenLayout {
   static constexpr int BYTES = ML_OFF + GEN_WARPS * 16 * 2 * 4;
 };
 
-__device__ __forceinline__ bool gen_slot_live(int blk, int i, int n_blk, int bs) {
-  return blk >= 0 && blk < n_blk && blk * bs <= i;
-}
-
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -56,19 +53,21 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 __device__ __forceinline__ void gen_sync() { asm volatile("bar.sync 1, %0;" ::"n"(GEN_THREADS)); }
 
-// Walks the 16-token chunks of one query's live blocks in slot order.  A warp
-// takes chunks warp, warp + 4, ...; `tok0` is the chunk's first token.
+// Walks the 16-token chunks of one query's live blocks (nsa_slots.cuh) in
+// slot order.  A warp takes chunks warp, warp + 4, ...; `tok0` is the chunk's
+// first token.  Every lane of the warp steps it alike.
 struct ChunkIter {
-  const int32_t* sel;
-  int S, i, n_blk, bs;
+  SlotRow row;
+  int i, bs;
   int s, c, nc;  // slot, chunk in block, chunks of that block (causal part only)
   int tok0;
   bool valid;
 
   __device__ __forceinline__ void seek_slot() {  // from slot s onwards, c = 0
-    for (; s < S; ++s) {
-      const int blk = __ldg(sel + s);
-      if (!gen_slot_live(blk, i, n_blk, bs)) continue;
+    const uint32_t rest = s < 32 ? row.live & ~((1u << s) - 1u) : 0u;
+    if (rest != 0u) {
+      s = __ffs(rest) - 1;
+      const int blk = nsa_slot_block(row, s);
       const int first = blk * bs;
       const int last = min(first + bs - 1, i);
       nc = (last - first) / GEN_CHUNK + 1;
@@ -125,8 +124,9 @@ __global__ void __launch_bounds__(GEN_THREADS)
     // ---- Q rows of the group into smem (row r = head hkv * G + r)
     for (int e = threadIdx.x; e < G * CPR; e += GEN_THREADS) {
       const int r = e / CPR, c = e % CPR;
+      const int hq = debug_index(hkv * G + r, 0, Hq);
       const uint4 val = *reinterpret_cast<const uint4*>(
-          q + ((static_cast<size_t>(b) * Hq + hkv * G + r) * T + i) * D + c * 8);
+          q + ((static_cast<size_t>(b) * Hq + hq) * T + debug_index(i, 0, T)) * D + c * 8);
       *reinterpret_cast<uint4*>(smem + L::Q_OFF + r * L::RB + c * 16) = val;
     }
     gen_sync();
@@ -148,13 +148,13 @@ __global__ void __launch_bounds__(GEN_THREADS)
       const uint32_t dk = sKV + buf * 2 * 16 * L::RB, dv = dk + 16 * L::RB;
       for (int e = lane; e < 16 * CPR; e += 32) {
         const int r = e / CPR, c = e % CPR;
-        const size_t off = static_cast<size_t>(tok0 + r) * D + c * 8;
+        const size_t off = static_cast<size_t>(debug_index(tok0 + r, 0, T)) * D + c * 8;
         cp_async16(dk + r * L::RB + c * 16, kb + off);
         cp_async16(dv + r * L::RB + c * 16, vb + off);
       }
     };
 
-    ChunkIter cur{block_idx + qg * S, S, i, n_blk, bs, 0, 0, 0, 0, false};
+    ChunkIter cur{nsa_live_slots(block_idx + qg * S, S, i, n_blk, bs), i, bs, 0, 0, 0, 0, false};
     cur.seek_slot();
     cur.advance(warp);
     ChunkIter nxt = cur;

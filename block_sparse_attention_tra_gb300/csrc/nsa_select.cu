@@ -18,6 +18,7 @@
 // takes query groups c, c + gridDim.x, ...
 #include "kernels.h"
 #include "mma_sync.cuh"
+#include "nsa_slots.cuh"
 #include "ptx.cuh"
 
 namespace bsa {
@@ -53,12 +54,6 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
 // 128-byte rows written by TMA with 128-byte swizzle (1024-byte aligned).
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
-// Is slot value `blk` a block this query reads?  Negative = padding; blocks
-// past the end or wholly after query i contribute nothing and are skipped.
-__device__ __forceinline__ bool slot_live(int blk, int i, int n_blk) {
-  return blk >= 0 && blk < n_blk && blk * NSA_BS <= i;
 }
 
 template <int D>
@@ -100,30 +95,36 @@ __global__ void __launch_bounds__(NSA_THREADS, 2)
 
   if (warp == NSA_CONSUMERS) {
     // ---------------------------------------------------------------- producer
+    // The whole warp walks the queries (it computes each row's live slots
+    // together); lane 0 waits on the ring and issues the copies.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      int kv_it = 0, q_it = 0;
-      bool ok = true;
-      for (long long qg = blockIdx.x; qg < n_queries && ok; qg += gridDim.x) {
-        const int i = static_cast<int>(qg % T);
-        const long long bg = qg / T;  // b * Hkv + hkv
-        const int b = static_cast<int>(bg / Hkv), hkv = static_cast<int>(bg % Hkv);
-        const int qs = q_it % NSA_NQ;
-        if (!(ok = mbar_wait(&q_empty[qs], ((q_it / NSA_NQ) & 1) ^ 1))) break;
+    }
+    int kv_it = 0, q_it = 0;
+    bool ok = true;
+    for (long long qg = blockIdx.x; qg < n_queries && ok; qg += gridDim.x) {
+      const int i = static_cast<int>(qg % T);
+      const long long bg = qg / T;  // b * Hkv + hkv
+      const int b = static_cast<int>(bg / Hkv), hkv = static_cast<int>(bg % Hkv);
+      const int qs = q_it % NSA_NQ;
+      if (lane == 0 && (ok = mbar_wait(&q_empty[qs], ((q_it / NSA_NQ) & 1) ^ 1))) {
+        debug_check(i >= 0 && i < T && bg >= 0 && bg < n_queries / T);
         mbar_arrive_expect_tx(&q_full[qs], static_cast<uint32_t>(L::NP * G * 128));
         uint8_t* sQ = smem + L::Q_OFF + qs * L::Q_TILE;
 #pragma unroll
         for (int pnl = 0; pnl < L::NP; ++pnl)
           tma_load_3d(sQ + pnl * L::Q_PANEL, &tmQ, &q_full[qs], 64 * pnl, i, b * Hq + hkv * G);
-        ++q_it;
-        const int32_t* sel = block_idx + qg * S;
-        for (int s = 0; s < S; ++s) {
-          const int blk = __ldg(sel + s);
-          if (!slot_live(blk, i, n_blk)) continue;
-          const int st = kv_it % NSA_NS;
-          if (!(ok = mbar_wait(&kv_empty[st], ((kv_it / NSA_NS) & 1) ^ 1))) break;
+      }
+      if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+      ++q_it;
+      const SlotRow row = nsa_live_slots(block_idx + qg * S, S, i, n_blk, NSA_BS);
+      for (uint32_t m = row.live; m != 0u && ok; m &= m - 1u) {
+        const int blk = nsa_slot_block(row, __ffs(m) - 1);
+        const int st = kv_it % NSA_NS;
+        if (lane == 0 && (ok = mbar_wait(&kv_empty[st], ((kv_it / NSA_NS) & 1) ^ 1))) {
+          debug_check(blk >= 0 && blk < n_blk && blk * NSA_BS <= i);
           mbar_arrive_expect_tx(&kv_full[st], 2 * L::KV_TILE);
           uint8_t* sK = smem + L::KV_OFF + st * 2 * L::KV_TILE;
           uint8_t* sV = sK + L::KV_TILE;
@@ -132,10 +133,12 @@ __global__ void __launch_bounds__(NSA_THREADS, 2)
             tma_load_3d(sK + pnl * L::KV_PANEL, &tmK, &kv_full[st], 64 * pnl, blk * NSA_BS, static_cast<int>(bg));
             tma_load_3d(sV + pnl * L::KV_PANEL, &tmV, &kv_full[st], 64 * pnl, blk * NSA_BS, static_cast<int>(bg));
           }
-          ++kv_it;
         }
+        if ((ok = __shfl_sync(0xffffffffu, ok, 0))) ++kv_it;
       }
-      // Drain whatever is still landing before the CTA may exit.
+    }
+    // Drain whatever is still landing before the CTA may exit.
+    if (lane == 0) {
       for (int n = (kv_it > NSA_NS ? kv_it - NSA_NS : 0); n < kv_it; ++n)
         mbar_wait(&kv_full[n % NSA_NS], (n / NSA_NS) & 1);
       for (int n = (q_it > NSA_NQ ? q_it - NSA_NQ : 0); n < q_it; ++n) mbar_wait(&q_full[n % NSA_NQ], (n / NSA_NQ) & 1);
@@ -176,10 +179,9 @@ __global__ void __launch_bounds__(NSA_THREADS, 2)
 #pragma unroll
     for (int j = 0; j < D / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
 
-    const int32_t* sel = block_idx + qg * S;
-    for (int s = 0; s < S; ++s) {
-      const int blk = __ldg(sel + s);
-      if (!slot_live(blk, i, n_blk)) continue;
+    const SlotRow row = nsa_live_slots(block_idx + qg * S, S, i, n_blk, NSA_BS);
+    for (uint32_t msk = row.live; msk != 0u; msk &= msk - 1u) {
+      const int blk = nsa_slot_block(row, __ffs(msk) - 1);
       const int st = kv_it % NSA_NS;
       if (ok) ok = mbar_wait(&kv_full[st], (kv_it / NSA_NS) & 1);
       ++kv_it;

@@ -17,7 +17,7 @@ namespace bsa {
 // ~1 s at the GB300 boost clock; no wait in a healthy launch comes close.
 constexpr long long BSA_WAIT_LIMIT_CYCLES = 2000000000LL;
 
-enum : unsigned { BSA_DEVERR_NONE = 0, BSA_DEVERR_TIMEOUT = 1, BSA_DEVERR_LAYOUT = 2 };
+enum : unsigned { BSA_DEVERR_NONE = 0, BSA_DEVERR_TIMEOUT = 1, BSA_DEVERR_LAYOUT = 2, BSA_DEVERR_BOUNDS = 3 };
 
 // Device error word of this translation unit (each kernel file has its own;
 // the host reads and clears them through bsa_device_error()).
@@ -38,6 +38,34 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 __device__ __forceinline__ void record_device_error(unsigned code) {
   atomicCAS(&g_device_error, 0u, code);
+}
+
+// Debug builds (compiled with -DBSA_DEBUG) check every gather index and
+// every TMA coordinate against its tensor before the access.  A failed check
+// records BSA_DEVERR_BOUNDS (3) in the device error word -- no trap, no
+// assert -- and the access goes ahead on a clamped, in-range index (a TMA
+// copy with an out-of-range coordinate only reads fill values, so those are
+// recorded and left alone).  Release builds compile the checks away.
+__device__ __forceinline__ void debug_check(bool ok) {
+#ifdef BSA_DEBUG
+  if (!ok) record_device_error(BSA_DEVERR_BOUNDS);
+#else
+  (void)ok;
+#endif
+}
+// `v` if lo <= v < hi; otherwise (debug builds only) records the violation and returns lo.
+template <typename I>
+__device__ __forceinline__ I debug_index(I v, I lo, I hi) {
+#ifdef BSA_DEBUG
+  if (v < lo || v >= hi) {
+    record_device_error(BSA_DEVERR_BOUNDS);
+    return lo;
+  }
+#else
+  (void)lo;
+  (void)hi;
+#endif
+  return v;
 }
 
 // ----------------------------------------------------------------- mbarrier
@@ -92,9 +120,10 @@ __device__ __forceinline__ bool device_error_raised() {
   return *reinterpret_cast<volatile unsigned int*>(&g_device_error) != 0u;
 }
 
-// Bounded wait for the phase with the given parity to complete.  Returns
-// false (and records a device error) if it never does.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait for the phase with the given parity to complete, giving up
+// after about `limit_cycles` SM clocks.  Returns false (and records a device
+// error) if it never does.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit_cycles) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const long long t0 = clock64();
@@ -105,11 +134,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     // Another CTA already timed out: give up at once instead of waiting a
     // full period per CTA.
     if (*reinterpret_cast<volatile unsigned int*>(&g_device_error) != 0u) return false;
-    if (clock64() - t0 > BSA_WAIT_LIMIT_CYCLES) {
+    if (clock64() - t0 > limit_cycles) {
       record_device_error(BSA_DEVERR_TIMEOUT);
       return false;
     }
   }
+}
+
+// The wait every kernel uses: bounded to BSA_WAIT_LIMIT_CYCLES.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_bounded(bar, parity, BSA_WAIT_LIMIT_CYCLES);
 }
 
 // -------------------------------------------------------------------- TMA

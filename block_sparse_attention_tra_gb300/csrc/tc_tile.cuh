@@ -17,14 +17,19 @@ constexpr int ROWS = 128;               // rows of a tile (and keys/queries per 
 constexpr int PANEL_BYTES = 128 * 128;  // 128 rows x 128 B (64 bf16) swizzle panel
 
 // C_tmem[128 x 128] = A[128 x D] * B[128 x D]^T, both K-major tiles in smem:
-// D/16 MMAs of K = 16 (32 bytes of each 128-byte row).
+// D/16 MMAs of K = 16 (32 bytes of each 128-byte row).  `leader`: the one
+// thread that issues; a converged warp computes the descriptors together
+// (warp-uniform values) and only the leader issues -- measured to issue a
+// tcgen05.mma every ~32 cycles, against ~48 for a lone thread that builds
+// its own descriptors.
 template <int D>
-__device__ __forceinline__ void mma_abt(uint32_t tC, uint32_t sA, uint32_t sB) {
+__device__ __forceinline__ void mma_abt(uint32_t tC, uint32_t sA, uint32_t sB, bool leader = true) {
   constexpr uint32_t IDESC = idesc_bf16_f32(ROWS, ROWS, 0, 0);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk >> 2) * PANEL_BYTES + (kk & 3) * 32;
-    mma_ss(tC, smem_desc_sw128(sA + off, 16, 1024), smem_desc_sw128(sB + off, 16, 1024), IDESC, kk > 0 ? 1u : 0u);
+    const uint64_t a = smem_desc_sw128(sA + off, 16, 1024), b = smem_desc_sw128(sB + off, 16, 1024);
+    if (leader) mma_ss(tC, a, b, IDESC, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -32,13 +37,14 @@ __device__ __forceinline__ void mma_abt(uint32_t tC, uint32_t sA, uint32_t sB) {
 // [16*kk0, 16*kk1): P is bf16 packed two per TMEM column, B an MN-major tile
 // in smem (its rows run along K).  `first` starts a new accumulation.
 template <int D>
-__device__ __forceinline__ void mma_tmem_a(uint32_t tC, uint32_t tP, uint32_t sB, int kk0, int kk1, bool first) {
+__device__ __forceinline__ void mma_tmem_a(uint32_t tC, uint32_t tP, uint32_t sB, int kk0, int kk1, bool first,
+                                           bool leader = true) {
   constexpr uint32_t IDESC = idesc_bf16_f32(ROWS, D, 0, 1);
   constexpr int NP = D / 64;
 #pragma unroll
   for (int kk = kk0; kk < kk1; ++kk) {
     const uint64_t bdesc = smem_desc_sw128(sB + kk * 16 * 128, NP > 1 ? PANEL_BYTES : 1024, 1024);
-    mma_ts(tC, tP + kk * 8, bdesc, IDESC, (!first || kk > 0) ? 1u : 0u);
+    if (leader) mma_ts(tC, tP + kk * 8, bdesc, IDESC, (!first || kk > 0) ? 1u : 0u);
   }
 }
 

@@ -53,7 +53,10 @@ __device__ __forceinline__ void epilogue_quarter(const uint32_t (&s)[32], uint32
   uint32_t pk[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
-    uint32_t w = weights2<PC>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp);
+    // (unrolled: the choice of log2 unit per pair is made at compile time)
+    uint32_t w = (PC == POW_GENERAL_MIX && mix_pair_on_fma(e))
+                     ? weights2<PC, true>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp)
+                     : weights2<PC, false>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp);
     if constexpr (DIAG) {
       const int key = key0 + c0 + 2 * e;  // keys key, key + 1
       if (key > row) w = 0u;
@@ -135,6 +138,19 @@ struct PairCfg {
 #define BSA_PAIR_SPLIT_P 1
 #endif
 constexpr bool PAIR_SPLIT_P = BSA_PAIR_SPLIT_P;  // hand P over in two halves
+// MMA issue: with a converged warp walking the issue loop (one elected lane
+// issuing), tcgen05.mma issues every ~32 cycles against ~48 for a lone
+// thread that builds its own descriptors (measured); that matters where the
+// MMAs are short (the N = 64 P V products of D = 64) and measured slower at
+// D = 128, where every MMA already runs 64 cycles.  0: never, 1: D = 64
+// only, 2: always.
+#ifndef BSA_PAIR_CONVERGED_ISSUE
+#define BSA_PAIR_CONVERGED_ISSUE 1
+#endif
+template <int D>
+constexpr bool pair_converged_issue() {
+  return BSA_PAIR_CONVERGED_ISSUE == 2 || (BSA_PAIR_CONVERGED_ISSUE == 1 && D == 64);
+}
 constexpr int PAIR_TMA_WARP = 8;
 constexpr int PAIR_MMA_WARP = 9;  // first MMA warp (allocates TMEM)
 
@@ -225,6 +241,7 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
         for (int qt = 0; qt < (it.has1 ? 2 : 1); ++qt) {
           // The previous user of this Q buffer has finished its last QK.
           if (uq[qt] > 0 && !(ok = mbar_wait(&q_empty[qt], (uq[qt] - 1) & 1))) break;
+          debug_check((2 * it.t + qt) < nQ && it.bh >= 0 && it.bh < BH);
           mbar_arrive_expect_tx(&q_full[qt], L::TILE);
 #pragma unroll
           for (int pnl = 0; pnl < L::NP; ++pnl)
@@ -236,6 +253,7 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
           const int s = g % L::NS;
           const uint32_t ph = (g / L::NS) & 1;
           if (!(ok = mbar_wait(&k_empty[s], ph ^ 1))) break;
+          debug_check(n >= 0 && n < nQ && n <= it.nlast);
           mbar_arrive_expect_tx(&k_full[s], L::TILE);
 #pragma unroll
           for (int pnl = 0; pnl < L::NP; ++pnl)
@@ -266,9 +284,14 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
     // issuer, or two from the one issuer whose tile alone reads that key tile
     // (Q1's diagonal tile; every key tile of an item without Q1).  An issuer
     // arrives for a use only after waiting for that use's load, so an arrival
-    // can never count toward the previous phase.
+    // can never count toward the previous phase.  The whole warp walks the
+    // loop (or only the elected lane, see pair_converged_issue); one elected
+    // lane issues the MMAs and commits.  Every lane waits on its own, so the
+    // lanes can part only when a wait gives up, and nothing after that needs
+    // them together.
     const int qt = warp - PAIR_MMA_WARP;
-    if (lane == 0) {
+    const bool leader = elect_one();
+    if (pair_converged_issue<D>() || leader) {
       const uint32_t sQ = smem_u32(smem + L::Q_OFF + qt * L::TILE);
       const uint32_t tS = tmem + qt * BN, tO = tmem + 2 * BN + qt * D;
       int g = 0;   // K/V ring position of the item's key tile 0
@@ -283,17 +306,19 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
         const int nmax = qt == 0 ? it.nmax0 : it.nmax1;
         const bool alone_all = !it.has1;  // Q0 alone reads every key tile of the item
         auto release = [&](uint64_t* empty, int n) {
-          mma_commit(empty);
-          if (alone_all || (qt == 1 && n == it.nlast)) mma_commit(empty);
+          if (leader) {
+            mma_commit(empty);
+            if (alone_all || (qt == 1 && n == it.nlast)) mma_commit(empty);
+          }
         };
         auto qk = [&](int n) -> bool {
           const int gi = g + n;
           if (!mbar_wait(&k_full[gi % L::NS], (gi / L::NS) & 1)) return false;
           tc_fence_after();
-          tile::mma_abt<D>(tS, sQ, smem_u32(smem + L::K_OFF + (gi % L::NS) * L::TILE));
-          mma_commit(&s_full[qt]);
+          tile::mma_abt<D>(tS, sQ, smem_u32(smem + L::K_OFF + (gi % L::NS) * L::TILE), leader);
+          if (leader) mma_commit(&s_full[qt]);
           release(&k_empty[gi % L::NS], n);
-          if (n == nmax) mma_commit(&q_empty[qt]);
+          if (leader && n == nmax) mma_commit(&q_empty[qt]);
           return true;
         };
         if (!(ok = mbar_wait(&q_full[qt], uq & 1) && qk(0))) break;
@@ -312,42 +337,51 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
           const uint32_t vph = (gi / L::NS) & 1;
           const bool v_in = V_FIRST ? mbar_wait(vb, vph) : mbar_test(vb, vph);
           if (V_FIRST && !(ok = v_in)) break;
-          if (!(ok = mbar_wait(PAIR_SPLIT_P ? &p_half[qt] : &p_full[qt], ph) && (v_in || mbar_wait(vb, vph))))
+          if (!(ok = mbar_wait(PAIR_SPLIT_P ? &p_half[qt] : &p_full[qt], ph) &&
+                     (v_in || mbar_wait(vb, vph))))
             break;
           // The first P V of an item overwrites O: the epilogue has read the last one.
           if (n == 0 && uq > 0 && !(ok = mbar_wait(&o_empty[qt], (uq - 1) & 1))) break;
           tc_fence_after();
-          tile::mma_tmem_a<D>(tO, tS, sV, 0, BN / 32, n == 0);
+          tile::mma_tmem_a<D>(tO, tS, sV, 0, BN / 32, n == 0, leader);
           if (!(ok = mbar_wait(&p_full[qt], ph))) break;
           tc_fence_after();
-          tile::mma_tmem_a<D>(tO, tS, sV, BN / 32, BN / 16, false);
+          tile::mma_tmem_a<D>(tO, tS, sV, BN / 32, BN / 16, false, leader);
           release(&v_empty[gi % L::NS], n);
-          if (n == nmax)
-            mma_commit(&o_full[qt]);
-          else if (!(ok = qk(n + 1)))
+          if (n == nmax) {
+            if (leader) mma_commit(&o_full[qt]);
+          } else if (!(ok = qk(n + 1))) {
             break;
+          }
         }
         g += it.nlast + 1;
         ++uq;
       }
       // Commits arrive in issue order: once this one has landed, every
       // barrier arrival of this thread's MMAs has too, and smem may be released.
-      mma_commit(&mma_done[qt]);
+      if (leader) mma_commit(&mma_done[qt]);
       mbar_wait(&mma_done[qt], 0);
     }
   } else if (warp == PAIR_MMA_WARP) {
     // One issuer for both tiles, in the order PV0(n), QK0(n+1), PV1(n),
     // QK1(n+1); each ring use is released by one commit once both tiles'
-    // products on it have been issued.
-    if (lane == 0) {
+    // products on it have been issued.  The whole warp walks the loop (or
+    // only the elected lane, see pair_converged_issue); one elected lane
+    // issues and commits.
+    const bool leader = elect_one();
+    if (pair_converged_issue<D>() || leader) {
       const uint32_t sQ0 = smem_u32(smem + L::Q_OFF);
       int g = 0;               // K/V ring position of the item's key tile 0
       int cs[2] = {0, 0};      // score tiles so far per query tile (s_full / p_half / p_full phase)
       int uq[2] = {0, 0};      // items so far per query tile (q_full / o_full / o_empty phase)
       bool ok = true;
+      auto commit = [&](uint64_t* bar) {
+        if (leader) mma_commit(bar);
+      };
       auto qk = [&](int qt, int gi) {
-        tile::mma_abt<D>(tmem + qt * BN, sQ0 + qt * L::TILE, smem_u32(smem + L::K_OFF + (gi % L::NS) * L::TILE));
-        mma_commit(&s_full[qt]);
+        tile::mma_abt<D>(tmem + qt * BN, sQ0 + qt * L::TILE, smem_u32(smem + L::K_OFF + (gi % L::NS) * L::TILE),
+                         leader);
+        commit(&s_full[qt]);
       };
       // PVt(n) in two halves: keys 0..63 as soon as that half of P is there.
       auto pv = [&](int qt, int n, int gi) -> bool {
@@ -362,53 +396,54 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
         // The first P V of an item overwrites O: the epilogue has read the last one.
         if (n == 0 && uq[qt] > 0 && !mbar_wait(&o_empty[qt], (uq[qt] - 1) & 1)) return false;
         tc_fence_after();
-        tile::mma_tmem_a<D>(tO, tP, sV, 0, BN / 32, n == 0);
+        tile::mma_tmem_a<D>(tO, tP, sV, 0, BN / 32, n == 0, leader);
         if (!mbar_wait(&p_full[qt], ph)) return false;
         tc_fence_after();
-        tile::mma_tmem_a<D>(tO, tP, sV, BN / 32, BN / 16, false);
+        tile::mma_tmem_a<D>(tO, tP, sV, BN / 32, BN / 16, false, leader);
         ++cs[qt];
         return true;
       };
 
       for (int r = 0; ok && pair_item(r, nItems, BH, nPair, nQ, it); ++r) {
-        if (!(ok = mbar_wait(&k_full[g % L::NS], (g / L::NS) & 1) && mbar_wait(&q_full[0], uq[0] & 1))) break;
+        if (!(ok = mbar_wait(&k_full[g % L::NS], (g / L::NS) & 1) && mbar_wait(&q_full[0], uq[0] & 1)))
+          break;
         tc_fence_after();
         qk(0, g);
-        if (it.nmax0 == 0) mma_commit(&q_empty[0]);
+        if (it.nmax0 == 0) commit(&q_empty[0]);
         if (it.has1) {
           if (!(ok = mbar_wait(&q_full[1], uq[1] & 1))) break;
           tc_fence_after();
           qk(1, g);
         }
-        mma_commit(&k_empty[g % L::NS]);
+        commit(&k_empty[g % L::NS]);
         for (int n = 0; n <= it.nlast && ok; ++n) {
           const int n1 = n + 1, gn = g + n, gn1 = g + n1;
           const bool next_k = n1 <= it.nlast;
           // tile 0: PV0(n), then QK0(n+1)
           if (n <= it.nmax0) {
             if (!(ok = pv(0, n, gn))) break;
-            if (n == it.nmax0) mma_commit(&o_full[0]);
+            if (n == it.nmax0) commit(&o_full[0]);
           }
           if (next_k) {
             if (!(ok = mbar_wait(&k_full[gn1 % L::NS], (gn1 / L::NS) & 1))) break;
             tc_fence_after();
             if (n1 <= it.nmax0) {
               qk(0, gn1);
-              if (n1 == it.nmax0) mma_commit(&q_empty[0]);
+              if (n1 == it.nmax0) commit(&q_empty[0]);
             }
           }
           // tile 1: PV1(n), then QK1(n+1)
           if (it.has1) {
             if (!(ok = pv(1, n, gn))) break;
-            if (n == it.nmax1) mma_commit(&o_full[1]);
+            if (n == it.nmax1) commit(&o_full[1]);
           }
-          mma_commit(&v_empty[gn % L::NS]);
+          commit(&v_empty[gn % L::NS]);
           if (next_k) {
             if (it.has1 && n1 <= it.nmax1) {
               qk(1, gn1);
-              if (n1 == it.nmax1) mma_commit(&q_empty[1]);
+              if (n1 == it.nmax1) commit(&q_empty[1]);
             }
-            mma_commit(&k_empty[gn1 % L::NS]);
+            commit(&k_empty[gn1 % L::NS]);
           }
         }
         g += it.nlast + 1;
@@ -417,7 +452,7 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
       }
       // Commits arrive in issue order: once this one has landed, every
       // barrier arrival of this CTA's MMAs has too, and smem may be released.
-      mma_commit(&mma_done[0]);
+      commit(&mma_done[0]);
       mbar_wait(&mma_done[0], 0);
     }
   } else {
@@ -515,11 +550,13 @@ int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int 
   if (D == 128) {
     if (pc == POW_TWO) return launch_pair<128, POW_TWO>(mq, mk, mv, out, BH, T, beta, p, stream);
     if (pc == POW_ONE) return launch_pair<128, POW_ONE>(mq, mk, mv, out, BH, T, beta, p, stream);
+    if (pc == POW_GENERAL_MIX) return launch_pair<128, POW_GENERAL_MIX>(mq, mk, mv, out, BH, T, beta, p, stream);
     return launch_pair<128, POW_GENERAL>(mq, mk, mv, out, BH, T, beta, p, stream);
   }
   if (D == 64) {
     if (pc == POW_TWO) return launch_pair<64, POW_TWO>(mq, mk, mv, out, BH, T, beta, p, stream);
     if (pc == POW_ONE) return launch_pair<64, POW_ONE>(mq, mk, mv, out, BH, T, beta, p, stream);
+    if (pc == POW_GENERAL_MIX) return launch_pair<64, POW_GENERAL_MIX>(mq, mk, mv, out, BH, T, beta, p, stream);
     return launch_pair<64, POW_GENERAL>(mq, mk, mv, out, BH, T, beta, p, stream);
   }
   return ERR_UNSUPPORTED;

@@ -177,6 +177,7 @@ __device__ __forceinline__ void bwd_produce(uint8_t* smem, const BwdBars& B, con
   tma_prefetch_desc(r1);
   tma_prefetch_desc(g0);
   tma_prefetch_desc(g1);
+  debug_check(res_row >= 0 && first >= 0 && bh >= 0);
   mbar_arrive_expect_tx(B.res_full, 2 * L::TILE);
   tile::tma_tile<D>(smem + L::RES_OFF, r0, B.res_full, res_row, bh);
   tile::tma_tile<D>(smem + L::RES_OFF + L::TILE, r1, B.res_full, res_row, bh);
@@ -223,7 +224,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const uint32_t tmem = *tptr;
 
   if (warp == TMA_WARP) {
-    if (lane == 0) bwd_produce<D>(smem, B, &tmK, &tmV, n * BT, &tmQ, &tmDO, n, nq, bh);
+    if (lane == 0) {
+      debug_check(bh >= 0 && bh < BH && n * BT < T && (n + nq - 1) * BT < T);
+      bwd_produce<D>(smem, B, &tmK, &tmV, n * BT, &tmQ, &tmDO, n, nq, bh);
+    }
   } else if (warp == MMA_WARP || warp == MMA_WARP + 1) {
     // Issuer X (warp 5): S^T_h = K_n Q_m[h]^T and dV += W^T_h dO_m[h];
     // issuer Y (warp 6): dP^T_h = V_n dO_m[h]^T and dK += dA^T_h Q_m[h].
@@ -351,7 +355,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const uint32_t tmem = *tptr;
 
   if (warp == TMA_WARP) {
-    if (lane == 0) bwd_produce<D>(smem, B, &tmQ, &tmDO, m * BT, &tmK, &tmV, 0, m + 1, bh);
+    if (lane == 0) {
+      debug_check(bh >= 0 && bh < BH && m * BT < T);
+      bwd_produce<D>(smem, B, &tmQ, &tmDO, m * BT, &tmK, &tmV, 0, m + 1, bh);
+    }
   } else if (warp == MMA_WARP || warp == MMA_WARP + 1) {
     // Issuer X (warp 5): S_h = Q_m K_n[h]^T and dQ += dA_h K_n[h] (dA over S);
     // issuer Y (warp 6): dP_h = dO_m V_n[h]^T, re-issued for the next key tile

@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
       tma_prefetch_desc(&tmK0);
       tma_prefetch_desc(&tmK1);
       tma_prefetch_desc(&tmV);
+      debug_check(m >= 0 && m * BT < T && bh >= 0 && bh < BH);
       mbar_arrive_expect_tx(q_full, 2 * L::TILE);
       tile::tma_tile<D>(smem + L::Q_OFF, &tmQ0, q_full, m * BT, bh);
       tile::tma_tile<D>(smem + L::Q_OFF + L::TILE, &tmQ1, q_full, m * BT, bh);

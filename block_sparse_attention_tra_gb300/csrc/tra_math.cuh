@@ -2,6 +2,16 @@
 // epilogue registers: power classes p = 1, p = 2, general p through
 // exp2(p log2 x), and, on request, p = k + 1/2 as x^k sqrt(x).
 // Shared by the forward kernels (plain and differential).
+//
+// The general path's log2 runs on two units.  MUFU lg2 issues at half the
+// ex2 rate (16 against 32 results per clock and SM), so with one lg2 and one
+// ex2 per score it bounds the epilogue.  POW_GENERAL_MIX evaluates log2 of
+// a share of the scores on the FMA pipe instead: x = 2^e m with m in [1, 2)
+// taken from the float's exponent and mantissa fields (one funnel shift and
+// one LOP3), log2 m from a degree-5 minimax polynomial (Remez exchange fit,
+// block_sparse_attention_tra_gb300/log2_poly.py; max error 1.6e-5 evaluated
+// in float32) by Horner's rule on packed f32x2 FMAs, with p folded into the
+// coefficients.  exp2 stays on MUFU for every score.
 #pragma once
 
 #include "kernels.h"
@@ -58,20 +68,69 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// log2(m) ~= sum_k LOG2_M[k] m^k on m in [1, 2): the Remez minimax fit of
+// log2(1 + t) on t in [0, 1) (through 0 at t = 0), written in m = 1 + t.
+constexpr int LOG2_DEG = 5;
+__device__ constexpr float LOG2_M[LOG2_DEG + 1] = {-2.811879280e+00f, 5.131084173e+00f, -3.603921890e+00f,
+                                                  1.666528133e+00f, -4.281965043e-01f, 4.638536892e-02f};
+constexpr float EXP_FIELD_BIAS = 8388735.0f;  // 2^23 + 127: float of (0x4B000000 | e_field) minus this = e
+
 // Per-row constants of the weight: tau and p duplicated into both halves of
-// a packed pair.
+// a packed pair; for POW_GENERAL_MIX also p times the log2 coefficients and
+// the exponent-field bias.
 struct PowParams {
   uint64_t tau2, p2;
+  uint64_t lc[LOG2_DEG + 1];
+  uint64_t ebias2;
 };
 __device__ __forceinline__ PowParams pow_params(float tau, float p) {
   PowParams w;
   w.tau2 = f2_pack(tau, tau);
   w.p2 = f2_pack(p, p);
+#pragma unroll
+  for (int k = 0; k <= LOG2_DEG; ++k) w.lc[k] = f2_pack(p * LOG2_M[k], p * LOG2_M[k]);
+  w.ebias2 = f2_pack(EXP_FIELD_BIAS, EXP_FIELD_BIAS);
   return w;
 }
 
+// p log2(x0), p log2(x1) for x >= 0 on the FMA pipe (x = 0 gives -127 p, and
+// exp2 of it flushes to 0 for p >= 1).
+__device__ __forceinline__ uint64_t p_log2_fma(float x0, float x1, const PowParams& w) {
+  const uint32_t i0 = __float_as_uint(x0), i1 = __float_as_uint(x1);
+  // mantissa with a zero exponent field: m in [1, 2)
+  const uint64_t m = f2_pack(__uint_as_float((i0 & 0x007fffffu) | 0x3f800000u),
+                             __uint_as_float((i1 & 0x007fffffu) | 0x3f800000u));
+  // 0x4B000000 | exponent field (x >= 0: the sign bit is 0), as a float 2^23 + field
+  const uint64_t ef = f2_sub(f2_pack(__uint_as_float(__funnelshift_r(i0, 0x00258000u, 23)),
+                                     __uint_as_float(__funnelshift_r(i1, 0x00258000u, 23))),
+                             w.ebias2);
+  uint64_t r = w.lc[LOG2_DEG];
+#pragma unroll
+  for (int k = LOG2_DEG - 1; k >= 0; --k) r = f2_fma(r, m, w.lc[k]);
+  return f2_fma(ef, w.p2, r);
+}
+
+// Which pairs of a 16-pair quarter take the FMA-pipe log2 under
+// POW_GENERAL_MIX: BSA_MIX_MUFU_PAIRS of 16 stay on MUFU lg2, spread evenly.
+// (Measured on the T=8192 D=64 and T=4096 D=128 p = 1.5 workloads: 12 is
+// fastest on both; more FMA-pipe pairs are slower, since the packed f32x2
+// FMAs, LOP3 and funnel shifts of the polynomial path all run at half rate.)
+#ifndef BSA_MIX_MUFU_PAIRS
+#define BSA_MIX_MUFU_PAIRS 12
+#endif
+__host__ __device__ constexpr bool mix_pair_on_fma(int e) {
+  return ((e % 16) * BSA_MIX_MUFU_PAIRS) % 16 >= BSA_MIX_MUFU_PAIRS;
+}
+
 // Weights of two adjacent keys from their scores: ReLU(s - tau)^p, bf16x2.
-template <int PC>
+// FMA_LOG2 (POW_GENERAL_MIX only): this pair's log2 runs on the FMA pipe.
+template <int PC, bool FMA_LOG2 = false>
 __device__ __forceinline__ uint32_t weights2(float s0, float s1, const PowParams& w) {
   float x0, x1;
   f2_unpack(f2_sub(f2_pack(s0, s1), w.tau2), x0, x1);
@@ -80,7 +139,18 @@ __device__ __forceinline__ uint32_t weights2(float s0, float s1, const PowParams
   } else if constexpr (PC == POW_TWO) {
     const uint32_t h = relu_pack(x0, x1);
     return mul_bf16x2(h, h);
-  } else if constexpr (PC >= POW_HALF0) {
+  } else if constexpr (PC == POW_GENERAL_MIX) {
+    x0 = fmaxf(x0, 0.0f);
+    x1 = fmaxf(x1, 0.0f);
+    uint64_t y;
+    if constexpr (FMA_LOG2)
+      y = p_log2_fma(x0, x1, w);
+    else
+      y = f2_mul(f2_pack(lg2_approx(x0), lg2_approx(x1)), w.p2);
+    float y0, y1;
+    f2_unpack(y, y0, y1);
+    return pack_bf16x2(ex2_approx(y0), ex2_approx(y1));
+  } else if constexpr (PC >= POW_HALF0 && PC <= POW_HALF3) {
     // p = k + 1/2: x^p = x^k sqrt(x), one MUFU operation per score; the
     // ReLU's zeros give sqrt(0) = 0 exactly.
     x0 = fmaxf(x0, 0.0f);

@@ -279,9 +279,9 @@ BSA_API int tra_diff_forward_noalloc(const void* q1, const void* q2,
  *
  *   q, out     : [B, Hq, T, D] bf16.      k, v : [B, Hkv, T, D] bf16.
  *   block_idx  : [B, Hkv, T, S] int32, shared by the G heads of a group;
- *                -1 = padding.  The non-negative entries of one row must be
- *                distinct (the page's reference treats a repeated block as
- *                selected once; this kernel would count it twice).
+ *                -1 = padding.  A row is read as a set, as the page's
+ *                reference does: a block listed more than once is selected
+ *                once, and the order of the slots does not matter.
  *   lse        : [B, Hq, T] fp32, or NULL to skip it.
  *   D          : 16, 32, 64 or 128 (the page: a power of two <= 128).
  *   block_size : 16, 32, 64 or 128 (the page: >= 16; its tiles need a power
@@ -320,10 +320,12 @@ BSA_API int nsa_select_forward(const void* q, const void* k, const void* v,
  *
  * which is the same softmax over the union of the selected causal tokens as
  * nsa_select_forward computes (out = 0, lse = -1e9 for a row with no pair).
- * A live slot holds 0 <= j < T / block_size with j * block_size <= i.
+ * A live slot holds 0 <= j < T / block_size with j * block_size <= i, and
+ * is the first slot of its row that holds j (set semantics: a repeated block
+ * forms one pair).
  *
- * Arguments, shapes, dtypes, preconditions (distinct entries per row) and
- * errors are those of nsa_select_forward (but only block_size 64 with D 64 or
+ * Arguments, shapes, dtypes, preconditions and errors are those of
+ * nsa_select_forward (but only block_size 64 with D 64 or
  * 128 is built: other shapes return BSA_ERR_UNSUPPORTED), plus:
  *   workspace       : caller-owned device memory of at least
  *                     nsa_select_fsa_workspace_size(...) bytes, 256-byte
@@ -372,6 +374,49 @@ BSA_API int bsa_version(void);
  * with the current device (cudaMemcpyFromSymbol); not for the hot path.
  */
 BSA_API int bsa_device_error(void);
+
+/*
+ * Self tests: device code paths the attention calls reach only in rare
+ * conditions, run on their own so that a test can check them on the GPU.
+ * The pages have no counterpart of these; they serve this library's tests.
+ *
+ * bsa_selftest_wait_timeout -- one thread of a one-CTA kernel waits, with a
+ * limit of `limit_cycles` SM clocks (1 .. 1e8), on an mbarrier that nothing
+ * arrives on, through the same bounded wait every kernel uses.  The wait
+ * gives up, records code 1 in the library's device error word (read it with
+ * bsa_device_error) and writes 0 to *result (1 would mean the wait completed,
+ * which cannot happen); the kernel then returns.  No copy or tensor-core
+ * operation is in flight, so the context stays usable.  `result` is a device
+ * int (4-byte aligned).  Errors: BSA_ERR_NULLPTR, BSA_ERR_SHAPE (limit out of
+ * range), BSA_ERR_ALIGN, BSA_ERR_DEVICE, BSA_ERR_LAUNCH.
+ *
+ * bsa_selftest_log2 -- for n floats x (device memory), writes the
+ * general-power epilogue's FMA-pipe log2 (exponent/mantissa split and a
+ * degree-5 minimax polynomial, the path POW_GENERAL_MIX uses for part of the
+ * scores) to y_fma and CUDA's log2f to y_ref.  Inputs are meant to be
+ * non-negative finite floats.  Errors: BSA_ERR_NULLPTR, BSA_ERR_SHAPE (n < 1),
+ * BSA_ERR_ALIGN (a pointer not 4-byte aligned), BSA_ERR_DEVICE,
+ * BSA_ERR_LAUNCH.
+ */
+BSA_API int bsa_selftest_wait_timeout(long long limit_cycles, int* result,
+                                      cudaStream_t stream);
+BSA_API int bsa_selftest_log2(const float* x, float* y_fma, float* y_ref,
+                              int n, cudaStream_t stream);
+
+/*
+ * bsa_read_probe -- a measurement helper, not part of the method (the pages
+ * have no counterpart): reads `bytes` (a multiple of 16, at most 2^40) of
+ * device memory at `buf` (16-byte aligned) `reps` times (1 .. 100000) with
+ * 16-byte loads that bypass L1, over a grid of four CTAs per SM, and XORs
+ * what it read into the device word *sink (4-byte aligned).  Timed with CUDA
+ * events on `stream`, bytes * reps / time is the read bandwidth of wherever
+ * the buffer lives: for a buffer that fits in L2 and was read once before,
+ * the L2 read bandwidth that the NSA selection gathers are served from.
+ * Errors: BSA_ERR_NULLPTR, BSA_ERR_SHAPE, BSA_ERR_ALIGN, BSA_ERR_DEVICE,
+ * BSA_ERR_LAUNCH.
+ */
+BSA_API int bsa_read_probe(const void* buf, size_t bytes, int reps,
+                           unsigned int* sink, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -121,7 +121,8 @@ def test_backward_and_diff_argument_errors(lib):
     from block_sparse_attention_tra_gb300 import bsa
 
     assert bsa.tra_backward_raw(P, P, P, None, P, P, P, 1, 1, 16, 64, 1.0, 2.0, 1, 0) == 1
-    assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 64, 1.0, 2.0, 0, 0) == 4  # f32 not built
+    assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 64, 1.0, 2.0, 7, 0) == 3  # not a bsa_dtype
+    assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 96, 1.0, 2.0, 0, 0) == 4  # f32, D = 96
     assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 96, 1.0, 2.0, 1, 0) == 4
     assert bsa.tra_backward_raw(P, P, P, P, P + 2, P, P, 1, 1, 16, 64, 1.0, 2.0, 1, 0) == 7
     assert bsa.tra_diff_forward_raw(P, P, None, P, P, P, 1, 1, 16, 64, 1.0, 0.5, 2.0, 1, 1, 0) == 1

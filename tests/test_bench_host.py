@@ -89,11 +89,14 @@ def test_reference_arm_prints_one_json_line():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] == 0
-    assert d["cpu_baseline"]["kind"] == "oracle"
-    # the same workload description as the GPU arm's line, plus the sample note
-    for key, val in {"workload": "tra_f32_B1_H2_T256_D64", "B": 1, "H": 2, "T": 256, "D": 64}.items():
-        assert d["config"][key] == val
-    assert "sample" in d["config"]
+    assert d["cpu_baseline"]["kind"] == "oracle" and "sample" in d["cpu_baseline"]
+    # exactly the GPU arm's workload description (the sample note lives under cpu_baseline)
+    import bench
+    from block_sparse_attention_tra_gb300 import workloads
+
+    assert d["config"] == bench.workload_config(workloads.TRA_WORKLOADS["tra_f32_B1_H2_T256_D64"], 1)
+    # the step time is the measured time of the sampled work: steps x ms_per_step is the timed region
+    assert d["ms_per_step"] > 0 and d["value"] == d["cpu_baseline"]["value"]
 
 
 def test_clock_records_that_reject_a_measurement():

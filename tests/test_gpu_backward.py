@@ -91,3 +91,57 @@ def test_tra_backward_head_groups_cover_every_head():
             one = bsa.tra_backward(q[sl], k[sl], v[sl], do[sl], w.beta, w.p)
             for name, a, c in zip(("dq", "dk", "dv"), full, one):
                 assert torch.equal(a[sl], c), f"{name} head ({b},{h}) differs from its single-head call"
+
+
+# fp32 inputs: the CUDA-core FFMA kernels, against the oracle at the fp32 bar.
+F32_TOL = 1e-4
+F32_CASES = [
+    # (B, H, T, D, beta, p)
+    (1, 2, 256, 64, 1.0, 2.0),
+    (2, 1, 200, 128, 0.5, 1.5),   # ragged, general power
+    (1, 2, 130, 64, 0.0, 1.0),    # p = 1
+    (1, 1, 1, 128, 1.0, 2.0),     # T = 1
+    (1, 1, 320, 64, -0.5, 3.7),   # beta < 0 reading, large power
+]
+
+
+@pytest.mark.parametrize("B,H,T,D,beta,p", F32_CASES)
+def test_tra_backward_f32(B, H, T, D, beta, p):
+    q, k, v = workloads.tra_inputs(B, H, T, D, "f32", seed=T + D)
+    do = torch.randn((B, H, T, D), generator=torch.Generator().manual_seed(T + 1))
+    dq, dk, dv = bsa.tra_backward(q.cuda(), k.cuda(), v.cuda(), do.cuda(), beta, p)
+    torch.cuda.synchronize()
+    assert dq.dtype == torch.float32
+    rq, rk, rv = otra.tra_backward(f64(q), f64(k), f64(v), f64(do), beta, p)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        err = float(np.abs(f64(got) - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
+        assert err <= F32_TOL, f"{name}: max err {err:.3e} of max|ref|"
+
+
+def _clean_seed(B, H, T, D, beta, gap):
+    """First seed whose causal scores all keep |q.k - tau| >= gap (bf16 inputs)."""
+    t = otra.tau(T, beta, D)
+    keep = np.tril(np.ones((T, T), dtype=bool))
+    for seed in range(500):
+        q, k, v = workloads.tra_inputs(B, H, T, D, "bf16", seed=seed)
+        x = np.einsum("bhid,bhjd->bhij", f64(q), f64(k)) - t[None, None, :, None]
+        if np.all(np.abs(x[..., keep]) >= gap):
+            return seed, (q, k, v)
+    raise AssertionError("no clean seed")
+
+
+@pytest.mark.parametrize("p", [0.5, 0.75])
+def test_tra_backward_power_below_one(p):
+    # For p < 1 the derivative p x^(p-1) grows without bound as x -> 0+, so a
+    # score that sits within rounding of the threshold makes any two correct
+    # evaluations disagree.  The inputs are chosen so that no causal score
+    # lies within 5e-4 of tau; there the bf16 bar applies as for every power.
+    B, H, T, D, beta = 1, 1, 80, 64, 1.0
+    seed, (q, k, v) = _clean_seed(B, H, T, D, beta, 5e-4)
+    do = torch.randn((B, H, T, D), generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16)
+    dq, dk, dv = bsa.tra_backward(q.cuda(), k.cuda(), v.cuda(), do.cuda(), beta, p)
+    torch.cuda.synchronize()
+    rq, rk, rv = otra.tra_backward(f64(q), f64(k), f64(v), f64(do), beta, p)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        err = float(np.abs(f64(got) - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
+        assert err <= TOL, f"{name}: max err {err:.3e} of max|ref|"

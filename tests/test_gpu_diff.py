@@ -103,3 +103,35 @@ def test_tra_diff_head_groups_cover_every_head(normalize):
             sl = (slice(b, b + 1), slice(h, h + 1))
             one = bsa.tra_diff_forward(q1[sl], q2[sl], k1[sl], k2[sl], v[sl], w.beta, 0.5, w.p, normalize=normalize)
             assert torch.equal(full[sl], one), f"head ({b},{h}) differs from its single-head call"
+
+
+# fp32 inputs: the CUDA-core FFMA kernel (normalisation folded into the
+# scores, no scratch), at the fp32 bar.
+F32_TOL = 1e-4
+F32_CASES = [
+    # (B, H, T, D, beta, lam, p, normalize)
+    (1, 2, 256, 64, 0.0, 0.5, 2.0, True),
+    (2, 1, 200, 128, 0.2, 0.8, 1.5, True),   # ragged, general power
+    (1, 2, 130, 64, 0.5, 0.3, 1.0, False),
+    (1, 1, 1, 128, 1.0, 0.5, 2.0, True),
+    (1, 1, 320, 64, 0.1, 1.5, 2.0, False),   # lambda clamps to 1
+]
+
+
+@pytest.mark.parametrize("B,H,T,D,beta,lam,p,norm", F32_CASES)
+def test_tra_diff_f32(B, H, T, D, beta, lam, p, norm):
+    q1, k1, v = workloads.tra_inputs(B, H, T, D, "f32", seed=T + D)
+    q2, k2, _ = workloads.tra_inputs(B, H, T, D, "f32", seed=T + D + 1)
+    ts = [t.cuda() for t in (q1, q2, k1, k2, v)]
+    out = bsa.tra_diff_forward(*ts, beta, lam, p, normalize=norm)
+    torch.cuda.synchronize()
+    assert out.dtype == torch.float32
+    ref = otra.tra_diff_forward(f64(q1), f64(q2), f64(k1), f64(k2), f64(v), beta, lam, p, normalize=norm)
+    err = float(np.abs(f64(out) - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
+    assert err <= F32_TOL, f"max err {err:.3e} of max|ref|"
+    # the allocation-free entry point runs the same fp32 kernel (it needs no scratch)
+    out2 = torch.empty_like(out)
+    st = bsa.tra_diff_forward_noalloc_raw(*(t.data_ptr() for t in ts), out2.data_ptr(), B, H, T, D, beta, lam, p,
+                                          norm, bsa.BSA_F32, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == 0 and torch.equal(out, out2)

@@ -73,6 +73,12 @@ TRA_SMALL = [
     (1, 2, 200, 64, 0.5, 0.25, "bf16"),   # p < 1: ReLU zeros must stay exactly 0
     (1, 1, 256, 128, 1.0, 15.0, "bf16"),  # large power (the page's p=15 example)
     (2, 3, 1000, 64, 2.0, 1.5, "bf16"),   # general power, ragged, 8 row tiles
+    # general powers p >= 1 take part of their log2 on the FMA pipe
+    (1, 2, 300, 128, 2.0, 1.5, "bf16"),   # D = 128, ragged
+    (1, 2, 257, 64, 1.0, 1.0001, "bf16"), # just above p = 1 (zeros must stay exact)
+    (1, 1, 256, 64, 2.0, 64.0, "bf16"),   # the largest power of that path (weights stay finite)
+    (1, 1, 256, 64, 2.0, 70.0, "bf16"),   # above it: MUFU log2 for every score
+    (1, 2, 384, 128, -1.0, 2.7, "bf16"),  # beta < 0 reading
 ]
 
 
@@ -173,6 +179,25 @@ def test_tra_full_workload_matches_single_heads(name):
             sl = (slice(b, b + 1), slice(h, h + 1))
             one = bsa.tra_forward(q[sl], k[sl], v[sl], w.beta, w.p)
             assert torch.equal(full[sl], one), f"head ({b},{h}) differs from its single-head call"
+
+
+@pytest.mark.parametrize("name,heads", [
+    ("tra_bf16_B4_H16_T4096_D128", [(0, 0), (1, 7), (3, 15)]),
+    ("tra_bf16_B2_H32_T8192_D64", [(0, 0), (0, 19), (1, 31)]),
+])
+def test_tra_full_workload_full_heads(name, heads):
+    # The benchmark workloads in the benchmark's launch configuration (one call
+    # over every head); three whole (b, h) heads against the float64 oracle,
+    # every row of them.
+    w = workloads.TRA_WORKLOADS[name]
+    q, k, v = workloads.workload_inputs(w)
+    out = bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), w.beta, w.p)
+    torch.cuda.synchronize()
+    for b, h in heads:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = otra.tra_forward(f64(q[sl]), f64(k[sl]), f64(v[sl]), w.beta, w.p)
+        err = rel_err(f64(out[sl]), ref)
+        assert err <= BF16_TOL, f"head ({b},{h}): max err {err:.3e} of max|ref|"
 
 
 def test_tra_out_of_place_canary():

@@ -15,9 +15,10 @@ import pytest
 import torch
 
 from block_sparse_attention_tra_gb300 import bsa, workloads
+from oracle import tra as otra
 
 pytestmark = pytest.mark.gpu
-TOL = 2e-2  # the bf16 bar used by every parity test here
+TOL = 2e-2  # the bf16 bar used by every parity test here (oracle comparison)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -48,16 +49,23 @@ def _noalloc(ts, out, beta, lam, p, normalize=True):
 
 @pytest.mark.parametrize("shape,beta,lam,p", [((1, 2, 384, 128), 0.0, 0.5, 2.0), ((2, 2, 300, 64), 0.1, 0.7, 1.5)])
 def test_noalloc_matches_regular_entry_point_twice(shape, beta, lam, p):
+    # Both entry points run the same pre-pass and the same kernel on the same
+    # factors; only where the factors live differs, so the outputs must agree
+    # bit for bit -- on the first call and on the second, which finds the
+    # array filled by the first.
     for call, seed in enumerate((11, 12)):  # two calls in a row, different data
         ts = _inputs(*shape, seed=seed + 7 * shape[2])
         want = bsa.tra_diff_forward(*ts, beta, lam, p, normalize=True)
         out = torch.full_like(ts[0], float("nan"))
         assert _noalloc(ts, out, beta, lam, p) == 0
         torch.cuda.synchronize()
-        got, ref = out.double().cpu().numpy(), want.double().cpu().numpy()
-        assert np.all(np.isfinite(got)), f"call {call}: output not written"
-        err = float(np.abs(got - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
-        assert err <= TOL, f"call {call}: max err {err:.3e} of max|ref|"
+        assert torch.equal(out, want), f"call {call}: differs from tra_diff_forward"
+        if call == 1:
+            # and against the float64 oracle, within the bf16 bar
+            h = [t.double().cpu().numpy() for t in ts]
+            ref = otra.tra_diff_forward(*h, beta, lam, p, normalize=True)
+            err = float(np.abs(out.double().cpu().numpy() - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
+            assert err <= TOL, f"max err {err:.3e} of max|ref|"
 
 
 def test_noalloc_without_normalisation_and_limit():
@@ -66,8 +74,7 @@ def test_noalloc_without_normalisation_and_limit():
     out = torch.empty_like(ts[0])
     assert _noalloc(ts, out, 0.0, 0.5, 2.0, normalize=False) == 0
     torch.cuda.synchronize()
-    err = float((out.double() - want.double()).abs().max()) / float(want.double().abs().max())
-    assert err <= TOL
+    assert torch.equal(out, want)
     # B*H*Tp beyond the fixed array: refused before anything is enqueued
     big = 1 << 20  # rows of the fixed array
     P = ts[0].data_ptr()
