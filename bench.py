@@ -286,19 +286,31 @@ MUFU_PER_CLK = {"lg2": 16.0, "ex2": 32.0, "sqrt": 16.0}
 
 
 def sfu_roofline(w, ms_per_launch, sm_mhz, ops):
-    """Special-function roofline of a TRA power class that evaluates `ops`
-    (MUFU operation names) once per causal pair: the time the MUFU units of
-    all SMs need at the sampled SM clock, as a fraction of the measured time."""
+    """Special-function roofline of a TRA power class: `ops` maps each MUFU
+    operation name to how many it evaluates per causal pair (the general
+    power with part of its log2 on the FMA pipe uses 12/16 of an lg2).  The
+    time the MUFU units of all SMs need at the sampled SM clock, as a fraction
+    of the measured time."""
     if not sm_mhz:
         return None
     import torch
 
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     pairs = w.B * w.H * (w.T * (w.T + 1) // 2)
-    clk_per_pair = sum(1.0 / MUFU_PER_CLK[o] for o in ops)
+    clk_per_pair = sum(n / MUFU_PER_CLK[o] for o, n in ops.items())
     min_ms = pairs * clk_per_pair / sms / (sm_mhz * 1e6) * 1e3
-    return {"bound": "sfu", "ops_per_pair": list(ops), "results_per_clk_per_sm": {o: MUFU_PER_CLK[o] for o in ops},
+    return {"bound": "sfu", "ops_per_pair": dict(ops), "results_per_clk_per_sm": {o: MUFU_PER_CLK[o] for o in ops},
             "pairs": pairs, "sm_mhz": sm_mhz, "min_ms": round(min_ms, 4), "frac": round(min_ms / ms_per_launch, 4)}
+
+
+def sfu_ops(w):
+    """MUFU operations per causal pair of the power class tra_forward picks
+    for this workload's p (None for p = 1, 2: no MUFU work)."""
+    if w.dtype != "bf16" or w.p in (1.0, 2.0):
+        return None
+    if 1.0 <= w.p <= 64.0:  # part of log2 on the FMA pipe: 12 of every 16 score pairs on MUFU lg2
+        return {"lg2": 12 / 16, "ex2": 1.0}
+    return {"lg2": 1.0, "ex2": 1.0}
 
 
 def time_resident(fn, steps, warmup, world, flush=None, soak_s=0.0):
@@ -444,6 +456,9 @@ def run_ours(args):
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
+    if isinstance(w, workloads.TraWorkload) and sfu_ops(w):
+        # the general power's epilogue is bounded by the MUFU unit, not the tensor pipe
+        result["sfu"] = sfu_roofline(w, ms, clocks.get("sm_mhz"), sfu_ops(w))
 
     # ---- secondary workloads (measured, reported beside the headline)
     if not args.no_secondary:
@@ -453,7 +468,7 @@ def run_ours(args):
             flush_buf.fill_(1.0)
 
         sec = []
-        sfu_clock = None
+        sfu_clock = clocks.get("sm_mhz")
         pk["l2_read_gbs"], pk["l2_how"] = measure_l2_read_gbs(device)
         result["l2_read_gbs_measured"] = {"value": pk["l2_read_gbs"], "how": pk["l2_how"]}
         for name in SECONDARY:
@@ -478,10 +493,9 @@ def run_ours(args):
                      "roofline": roofline_for(w2, t, pk, sustained=False),
                      "l2": ("no flush: inputs %d MB > 129 MB L2" % (w2.io_bytes // 2**20)) if big
                      else "flushed between launches"}
-            if isinstance(w2, workloads.TraWorkload) and w2.dtype == "bf16" and w2.p not in (1.0, 2.0):
-                # general power: one lg2 and one ex2 per causal pair (exp2(p log2 x))
-                entry["sfu"] = sfu_roofline(w2, t, entry["clocks"]["sm_mhz"], ("lg2", "ex2"))
-                sfu_clock = entry["clocks"]["sm_mhz"]
+            if isinstance(w2, workloads.TraWorkload) and sfu_ops(w2):
+                # general power: exp2(p log2 x), an ex2 and (part of) an lg2 per causal pair
+                entry["sfu"] = sfu_roofline(w2, t, entry["clocks"]["sm_mhz"], sfu_ops(w2))
             sec.append(entry)
             if isinstance(w2, workloads.NsaWorkload) and w2.block_size == 64 and w2.D in (64, 128):
                 # The same selection through the block-outer split-K form
@@ -533,7 +547,7 @@ def run_ours(args):
                         "algorithmic_flops": flops, "l2": "no flush: inputs and outputs > 129 MB L2"})
             if label.startswith("tra_forward(sqrt_half_powers)"):
                 # p = 1.5 as x sqrt(x): one sqrt per causal pair (clock of the exp/log line's run)
-                sec[-1]["sfu"] = sfu_roofline(w3, t, sfu_clock, ("sqrt",))
+                sec[-1]["sfu"] = sfu_roofline(w3, t, sfu_clock, {"sqrt": 1.0})
         result["secondary"] = sec
 
     if args.cpu_baseline and rank == 0 and world == 1:

@@ -129,9 +129,12 @@ struct PairLayout {
 // issuing warp.  With a heavy epilogue (general and half powers) one issuer
 // serving both tiles in turn is faster: it keeps the two epilogue
 // warpgroups half a step apart, so one of them is always computing.
+#ifndef BSA_PAIR_GENERAL_ISSUERS
+#define BSA_PAIR_GENERAL_ISSUERS 1
+#endif
 template <int PC>
 struct PairCfg {
-  static constexpr int ISSUERS = (PC == POW_ONE || PC == POW_TWO) ? 2 : 1;
+  static constexpr int ISSUERS = (PC == POW_ONE || PC == POW_TWO) ? 2 : BSA_PAIR_GENERAL_ISSUERS;
   static constexpr int THREADS = 256 + 32 + 32 * ISSUERS;  // epilogue warpgroups, TMA warp, MMA warp(s)
 };
 #ifndef BSA_PAIR_SPLIT_P

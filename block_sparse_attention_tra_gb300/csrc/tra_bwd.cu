@@ -155,15 +155,28 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tmem, int warp) {
 // B_h being rows 64h .. 64h+63 of a K-major 128-row smem tile (8 KB into
 // each 128-byte-swizzled panel, a whole number of swizzle atoms).
 template <int D>
-__device__ __forceinline__ void mma_abt_half(uint32_t tC, uint32_t sA, uint32_t sB, int h) {
+__device__ __forceinline__ void mma_abt_half(uint32_t tC, uint32_t sA, uint32_t sB, int h, bool leader) {
   constexpr uint32_t IDESC = idesc_bf16_f32(BT, 64, 0, 0);
   const uint32_t sBh = sB + static_cast<uint32_t>(h) * 64u * 128u;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk >> 2) * PANEL_BYTES + (kk & 3) * 32;
-    mma_ss(tC, smem_desc_sw128(sA + off, 16, 1024), smem_desc_sw128(sBh + off, 16, 1024), IDESC,
-           kk > 0 ? 1u : 0u);
+    const uint64_t a = smem_desc_sw128(sA + off, 16, 1024), b = smem_desc_sw128(sBh + off, 16, 1024);
+    if (leader) mma_ss(tC, a, b, IDESC, kk > 0 ? 1u : 0u);
   }
+}
+
+// MMA issue: one elected lane issues.  At D = 64 the whole warp walks the
+// issue loop with it (the descriptors are then warp-uniform values), which
+// issues the short N = 64 products faster (B2 H32 T8192 D64 p=2: 2.38 ->
+// 2.19 ms); at D = 128 that measured 5% slower than the elected lane
+// walking it alone.  0: never, 1: D = 64 only, 2: always.
+#ifndef BSA_BWD_CONVERGED_ISSUE
+#define BSA_BWD_CONVERGED_ISSUE 1
+#endif
+template <int D>
+constexpr bool bwd_converged_issue() {
+  return BSA_BWD_CONVERGED_ISSUE == 2 || (BSA_BWD_CONVERGED_ISSUE == 1 && D == 64);
 }
 
 // Producer: two resident tiles (rows res_row of maps r0, r1), then for
@@ -233,17 +246,22 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // issuer Y (warp 6): dP^T_h = V_n dO_m[h]^T and dK += dA^T_h Q_m[h].
     // Per query tile j: acc(j, 0), score(j+1, 0), acc(j, 1), score(j+1, 1).
     const int is = warp - MMA_WARP;
-    if (lane == 0) {
+    const bool leader = elect_one();
+    if (bwd_converged_issue<D>() || leader) {
       const uint32_t sRes = smem_u32(smem + L::RES_OFF) + (is == 0 ? 0u : static_cast<uint32_t>(L::TILE));
       const uint32_t tScore = tmem + (is == 0 ? ST : DPT), tAcc = tmem + (is == 0 ? DV : DK);
       auto slot = [&](int j) { return smem_u32(smem + L::RING_OFF + (j % L::NS) * 2 * L::TILE); };  // Q_j | dO_j
+      auto mma_commit = [&](uint64_t* bar) {
+        if (leader) bsa::mma_commit(bar);
+      };
       auto score = [&](int j, int h) {
-        mma_abt_half<D>(tScore + 64 * h, sRes, slot(j) + (is == 0 ? 0u : static_cast<uint32_t>(L::TILE)), h);
+        mma_abt_half<D>(tScore + 64 * h, sRes, slot(j) + (is == 0 ? 0u : static_cast<uint32_t>(L::TILE)), h,
+                        leader);
         mma_commit(&B.s_full[h]);
       };
       auto acc = [&](int j, int h) {
         tile::mma_tmem_a<D>(tAcc, tScore + 32 * h, slot(j) + (is == 0 ? static_cast<uint32_t>(L::TILE) : 0u),
-                            4 * h, 4 * h + 4, j == 0 && h == 0);
+                            4 * h, 4 * h + 4, j == 0 && h == 0, leader);
       };
       bool ok = mbar_wait(B.res_full, 0) && mbar_wait(&B.ring_full[0], 0);
       if (ok) {
@@ -364,12 +382,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // issuer Y (warp 6): dP_h = dO_m V_n[h]^T, re-issued for the next key tile
     // once the epilogue has read half h.
     const int is = warp - MMA_WARP;
-    if (lane == 0) {
+    const bool leader = elect_one();
+    if (bwd_converged_issue<D>() || leader) {
       const uint32_t sRes = smem_u32(smem + L::RES_OFF) + (is == 0 ? 0u : static_cast<uint32_t>(L::TILE));
       const uint32_t tScore = tmem + (is == 0 ? S : DP);
       auto slot = [&](int j) { return smem_u32(smem + L::RING_OFF + (j % L::NS) * 2 * L::TILE); };  // K_j | V_j
+      auto mma_commit = [&](uint64_t* bar) {
+        if (leader) bsa::mma_commit(bar);
+      };
       auto score = [&](int j, int h) {
-        mma_abt_half<D>(tScore + 64 * h, sRes, slot(j) + (is == 0 ? 0u : static_cast<uint32_t>(L::TILE)), h);
+        mma_abt_half<D>(tScore + 64 * h, sRes, slot(j) + (is == 0 ? 0u : static_cast<uint32_t>(L::TILE)), h,
+                        leader);
         mma_commit(&B.s_full[h]);
       };
       bool ok = mbar_wait(B.res_full, 0) && mbar_wait(&B.ring_full[0], 0);
@@ -383,7 +406,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         for (int h = 0; h < 2; ++h) {
           if (!(ok = mbar_wait(&B.p_full[h], j & 1))) break;
           tc_fence_after();
-          if (is == 0) tile::mma_tmem_a<D>(tmem + DQ, tmem + S + 32 * h, slot(j), 4 * h, 4 * h + 4, j == 0 && h == 0);
+          if (is == 0)
+            tile::mma_tmem_a<D>(tmem + DQ, tmem + S + 32 * h, slot(j), 4 * h, 4 * h + 4, j == 0 && h == 0, leader);
           if (h == 1) mma_commit(&B.ring_empty[j % L::NS]);  // K_j, V_j read by every product issued so far
           if (more) {
             if (h == 0 && !(ok = mbar_wait(&B.ring_full[(j + 1) % L::NS], ((j + 1) / L::NS) & 1))) break;

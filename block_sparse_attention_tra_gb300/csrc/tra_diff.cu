@@ -307,14 +307,21 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
     constexpr int NT = 3 - DiffCfg<D, PC>::ISSUERS;
     const int j = warp - DIFF_MMA_WARP;
     const int T0 = NT == 1 ? j : 0;
-    if (lane == 0) {
+    // The whole warp walks the issue loop at D = 64 (short N = 64 P V
+    // products; descriptors are then warp-uniform values) and one elected
+    // lane issues; at D = 128 the elected lane walks it alone.
+    const bool leader = elect_one();
+    if (D == 64 || leader) {
       const uint32_t sQ = smem_u32(smem + L::Q_OFF);
+      auto mma_commit = [&](uint64_t* bar) {
+        if (leader) bsa::mma_commit(bar);
+      };
       // QKt(n): S_t = Q_t K_t(n)^T, then release K_t(n).
       auto qk = [&](int t, int n) -> bool {
         const Ring& R = t == 0 ? rk0 : rk1;
         if (!mbar_wait(&R.full[R.stage(n)], R.phase(n))) return false;
         tc_fence_after();
-        tile::mma_abt<D>(tmem + t * BT, sQ + t * L::TILE, smem_u32(smem + R.off + R.stage(n) * L::TILE));
+        tile::mma_abt<D>(tmem + t * BT, sQ + t * L::TILE, smem_u32(smem + R.off + R.stage(n) * L::TILE), leader);
         mma_commit(&s_full[t]);
         mma_commit(&R.empty[R.stage(n)]);
         return true;
@@ -324,7 +331,7 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
         if (!mbar_wait(&p_full[t], n & 1) || !mbar_wait(&rv.full[rv.stage(n)], rv.phase(n))) return false;
         tc_fence_after();
         const uint32_t sV = smem_u32(smem + rv.off + rv.stage(n) * L::TILE);
-        tile::mma_tmem_a<D>(tmem + O_COL + t * D, tmem + t * BT, sV, 0, BT / 16, n == 0);
+        tile::mma_tmem_a<D>(tmem + O_COL + t * D, tmem + t * BT, sV, 0, BT / 16, n == 0, leader);
         mma_commit(&rv.empty[rv.stage(n)]);
         return true;
       };
