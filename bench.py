@@ -308,8 +308,8 @@ def sfu_ops(w):
     for this workload's p (None for p = 1, 2: no MUFU work)."""
     if w.dtype != "bf16" or w.p in (1.0, 2.0):
         return None
-    if 1.0 <= w.p <= 64.0:  # part of log2 on the FMA pipe: 12 of every 16 score pairs on MUFU lg2
-        return {"lg2": 12 / 16, "ex2": 1.0}
+    if 1.0 <= w.p <= 64.0:  # part of log2 on the FMA pipe: 10 of every 16 score pairs on MUFU lg2
+        return {"lg2": 10 / 16, "ex2": 1.0}
     return {"lg2": 1.0, "ex2": 1.0}
 
 

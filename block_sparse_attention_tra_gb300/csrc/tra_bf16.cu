@@ -47,14 +47,14 @@ constexpr uint32_t TMEM_COLS = 512;
 // columns c0/2 .. c0/2+15 of the same buffer (already-consumed scores).
 // DIAG: the tile holds the diagonal, mask keys after the row (a compile-time
 // flag, so that the other tiles carry no masking instructions at all).
-template <int PC, bool DIAG>
+template <int PC, bool DIAG, int MUFU_PAIRS>
 __device__ __forceinline__ void epilogue_quarter(const uint32_t (&s)[32], uint32_t tS, int c0, const PowParams& wp,
                                                  int key0, int row) {
   uint32_t pk[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     // (unrolled: the choice of log2 unit per pair is made at compile time)
-    uint32_t w = (PC == POW_GENERAL_MIX && mix_pair_on_fma(e))
+    uint32_t w = (PC == POW_GENERAL_MIX && mix_pair_on_fma<MUFU_PAIRS>(e))
                      ? weights2<PC, true>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp)
                      : weights2<PC, false>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp);
     if constexpr (DIAG) {
@@ -70,17 +70,17 @@ __device__ __forceinline__ void epilogue_quarter(const uint32_t (&s)[32], uint32
 // One 128-key score tile of this thread's row -> P, in four software-
 // pipelined quarters; arrives on p_half after keys 0..63 and on p_full after
 // all 128 (one arrival per warp).
-template <int PC, bool SPLIT, bool DIAG>
+template <int PC, bool SPLIT, bool DIAG, int MP>
 __device__ __forceinline__ void epilogue_tile(uint32_t tS, const PowParams& wp, int key0, int row, int lane,
                                               uint64_t* p_half, uint64_t* p_full) {
   uint32_t a[32], b[32];
   tmem_ld32(tS, a);
   tmem_wait_ld();
   tmem_ld32(tS + 32, b);
-  epilogue_quarter<PC, DIAG>(a, tS, 0, wp, key0, row);
+  epilogue_quarter<PC, DIAG, MP>(a, tS, 0, wp, key0, row);
   tmem_wait_ld();
   tmem_ld32(tS + 64, a);
-  epilogue_quarter<PC, DIAG>(b, tS, 32, wp, key0, row);
+  epilogue_quarter<PC, DIAG, MP>(b, tS, 32, wp, key0, row);
   if constexpr (SPLIT) {
     tmem_wait_st();
     tc_fence_before();
@@ -89,9 +89,36 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tS, const PowParams& wp, 
   }
   tmem_wait_ld();
   tmem_ld32(tS + 96, b);
-  epilogue_quarter<PC, DIAG>(a, tS, 64, wp, key0, row);
+  epilogue_quarter<PC, DIAG, MP>(a, tS, 64, wp, key0, row);
   tmem_wait_ld();
-  epilogue_quarter<PC, DIAG>(b, tS, 96, wp, key0, row);
+  epilogue_quarter<PC, DIAG, MP>(b, tS, 96, wp, key0, row);
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(p_full);
+}
+
+// Two of a tile's four score quarters (q = half and half + 2) for one of the
+// two warps that share a TMEM lane quarter.  P of quarter q lands in TMEM
+// columns 16q .. 16q+15, inside quarter q / 2's scores, which may belong to
+// the other warp: both warps load their first quarter before either stores
+// (named barrier `bar_id`, 64 threads).  Quarters 0 and 1 make up P's first
+// half (p_half: one arrival per warp), all four the whole of it (p_full).
+template <int PC, bool DIAG, int MP>
+__device__ __forceinline__ void epilogue_two_quarters(uint32_t tS, const PowParams& wp, int key0, int row, int lane,
+                                                      int half, int bar_id, uint64_t* p_half, uint64_t* p_full) {
+  uint32_t a[32];
+  tmem_ld32(tS + 32 * half, a);
+  tmem_wait_ld();
+  asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+  epilogue_quarter<PC, DIAG, MP>(a, tS, 32 * half, wp, key0, row);
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(p_half);
+  tmem_ld32(tS + 32 * (half + 2), a);
+  tmem_wait_ld();
+  epilogue_quarter<PC, DIAG, MP>(a, tS, 32 * (half + 2), wp, key0, row);
   tmem_wait_st();
   tc_fence_before();
   __syncwarp();
@@ -132,10 +159,23 @@ struct PairLayout {
 #ifndef BSA_PAIR_GENERAL_ISSUERS
 #define BSA_PAIR_GENERAL_ISSUERS 1
 #endif
+// Epilogue warpgroups per query tile for the general powers (1 or 2).  With
+// two, warps w and w + 8 share a TMEM lane quarter of one tile and take its
+// score quarters {0, 2} and {1, 3}: four epilogue warps per SMSP instead of
+// two hide more of the MUFU and TMEM-load latency (B2 H32 T8192 D64 p=1.5
+// 0.803 -> 0.783 ms, and 0.733 ms with more of log2 on the FMA pipe; B4 H16
+// T4096 D128 p=1.5 0.239 -> 0.229 ms), at 80-96 registers per thread.
+#ifndef BSA_PAIR_GENERAL_EPI_WG
+#define BSA_PAIR_GENERAL_EPI_WG 2
+#endif
 template <int PC>
 struct PairCfg {
-  static constexpr int ISSUERS = (PC == POW_ONE || PC == POW_TWO) ? 2 : BSA_PAIR_GENERAL_ISSUERS;
-  static constexpr int THREADS = 256 + 32 + 32 * ISSUERS;  // epilogue warpgroups, TMA warp, MMA warp(s)
+  static constexpr bool GENERAL = !(PC == POW_ONE || PC == POW_TWO);
+  static constexpr int ISSUERS = GENERAL ? BSA_PAIR_GENERAL_ISSUERS : 2;
+  static constexpr int EPI_WG = GENERAL ? BSA_PAIR_GENERAL_EPI_WG : 1;
+  static constexpr int TMA_WARP = 8 * EPI_WG;
+  static constexpr int MMA_WARP = TMA_WARP + 1;  // first MMA warp (allocates TMEM)
+  static constexpr int THREADS = 256 * EPI_WG + 32 + 32 * ISSUERS;  // epilogue warpgroups, TMA warp, MMA warp(s)
 };
 #ifndef BSA_PAIR_SPLIT_P
 #define BSA_PAIR_SPLIT_P 1
@@ -154,8 +194,6 @@ template <int D>
 constexpr bool pair_converged_issue() {
   return BSA_PAIR_CONVERGED_ISSUE == 2 || (BSA_PAIR_CONVERGED_ISSUE == 1 && D == 64);
 }
-constexpr int PAIR_TMA_WARP = 8;
-constexpr int PAIR_MMA_WARP = 9;  // first MMA warp (allocates TMEM)
 
 // Item of round r for this CTA (false once the CTA has no more items).
 struct PairItem {
@@ -181,6 +219,9 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
                          const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out, int BH, int T,
                          int nQ, int nPair, int nItems, float beta, float p) {
   using L = PairLayout<D>;
+  using Cfg = PairCfg<PC>;
+  constexpr int PAIR_TMA_WARP = Cfg::TMA_WARP;
+  constexpr int PAIR_MMA_WARP = Cfg::MMA_WARP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -206,10 +247,10 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
       mbar_init(&q_full[b], 1);
       mbar_init(&q_empty[b], 1);
       mbar_init(&s_full[b], 1);
-      mbar_init(&p_half[b], 4);
-      mbar_init(&p_full[b], 4);
+      mbar_init(&p_half[b], 4 * Cfg::EPI_WG);
+      mbar_init(&p_full[b], 4 * Cfg::EPI_WG);
       mbar_init(&o_full[b], 1);
-      mbar_init(&o_empty[b], 4);
+      mbar_init(&o_empty[b], 4 * Cfg::EPI_WG);
     }
     for (int s = 0; s < L::NS; ++s) {
       mbar_init(&k_full[s], 1);
@@ -459,8 +500,9 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
       mbar_wait(&mma_done[0], 0);
     }
   } else {
-    const int qt = warp >> 2;  // query tile of this warpgroup
-    const int wq = warp & 3;   // TMEM lane quarter
+    const int qt = (warp >> 2) & 1;  // query tile of this warpgroup
+    const int wq = warp & 3;         // TMEM lane quarter
+    const int half = warp >> 3;      // with two warpgroups per tile: score quarters {0, 2} or {1, 3}
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t tS = lane_base + qt * BN;
     int cs = 0, uq = 0;
@@ -473,16 +515,27 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
       for (int n = 0; n <= nmax; ++n, ++cs) {
         if (!(ok = mbar_wait(&s_full[qt], cs & 1))) break;
         tc_fence_after();
-        if (n == nmax)
-          epilogue_tile<PC, PAIR_SPLIT_P, true>(tS, wp, n * BN, row, lane, &p_half[qt], &p_full[qt]);
-        else
-          epilogue_tile<PC, PAIR_SPLIT_P, false>(tS, wp, n * BN, row, lane, &p_half[qt], &p_full[qt]);
+        constexpr int MP = mix_mufu_pairs<D>();
+        if constexpr (Cfg::EPI_WG == 2) {
+          const int bar_id = 1 + qt * 4 + wq;  // the two warps sharing this lane quarter
+          if (n == nmax)
+            epilogue_two_quarters<PC, true, MP>(tS, wp, n * BN, row, lane, half, bar_id, &p_half[qt], &p_full[qt]);
+          else
+            epilogue_two_quarters<PC, false, MP>(tS, wp, n * BN, row, lane, half, bar_id, &p_half[qt], &p_full[qt]);
+        } else {
+          if (n == nmax)
+            epilogue_tile<PC, PAIR_SPLIT_P, true, MP>(tS, wp, n * BN, row, lane, &p_half[qt], &p_full[qt]);
+          else
+            epilogue_tile<PC, PAIR_SPLIT_P, false, MP>(tS, wp, n * BN, row, lane, &p_half[qt], &p_full[qt]);
+        }
       }
       if (!ok || !(ok = mbar_wait(&o_full[qt], uq & 1))) break;
       tc_fence_after();
       __nv_bfloat16* orow = out + (static_cast<size_t>(it.bh) * T + row) * D;
+      constexpr int CPW = D / 32 / Cfg::EPI_WG;  // 32-column chunks of O this warp stores
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) tile::store_row_chunk(lane_base + 2 * BN + qt * D, c, orow, row < T);
+      for (int c = 0; c < CPW; ++c)
+        tile::store_row_chunk(lane_base + 2 * BN + qt * D, half * CPW + c, orow, row < T);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_empty[qt]);

@@ -117,15 +117,24 @@ __device__ __forceinline__ uint64_t p_log2_fma(float x0, float x1, const PowPara
 }
 
 // Which pairs of a 16-pair quarter take the FMA-pipe log2 under
-// POW_GENERAL_MIX: BSA_MIX_MUFU_PAIRS of 16 stay on MUFU lg2, spread evenly.
-// (Measured on the T=8192 D=64 and T=4096 D=128 p = 1.5 workloads: 12 is
-// fastest on both; more FMA-pipe pairs are slower, since the packed f32x2
-// FMAs, LOP3 and funnel shifts of the polynomial path all run at half rate.)
-#ifndef BSA_MIX_MUFU_PAIRS
-#define BSA_MIX_MUFU_PAIRS 12
+// POW_GENERAL_MIX: M of every 16 stay on MUFU lg2, spread evenly.  M is
+// chosen per head dim (measured on the T=8192 D=64 and the T=4096 D=128
+// p = 1.5 workloads with two epilogue warpgroups per query tile); more
+// FMA-pipe pairs than that are slower, since the packed f32x2 FMAs, LOP3 and
+// funnel shifts of the polynomial path all run at half rate.
+#ifndef BSA_MIX_MUFU_PAIRS_D64
+#define BSA_MIX_MUFU_PAIRS_D64 10
 #endif
+#ifndef BSA_MIX_MUFU_PAIRS_D128
+#define BSA_MIX_MUFU_PAIRS_D128 10
+#endif
+template <int D>
+__host__ __device__ constexpr int mix_mufu_pairs() {
+  return D == 64 ? BSA_MIX_MUFU_PAIRS_D64 : BSA_MIX_MUFU_PAIRS_D128;
+}
+template <int M>
 __host__ __device__ constexpr bool mix_pair_on_fma(int e) {
-  return ((e % 16) * BSA_MIX_MUFU_PAIRS) % 16 >= BSA_MIX_MUFU_PAIRS;
+  return ((e % 16) * M) % 16 >= M;
 }
 
 // Weights of two adjacent keys from their scores: ReLU(s - tau)^p, bf16x2.
