@@ -14,8 +14,9 @@
 // causal tokens of its live blocks are cut into 16-token chunks (block sizes
 // are multiples of 16, so a chunk never straddles two blocks) and dealt to
 // the warps round-robin.  Each warp brings its chunks' K and V rows into its
-// own ring of shared-memory stages with cp.async (two chunks deep), computes
-// S = Q K^T, an
+// own double-buffered shared memory with cp.async (deeper rings measured
+// slower: the shared memory they take costs more resident CTAs per SM than the
+// extra chunks in flight give back), computes S = Q K^T, an
 // online softmax with lazy rescaling and O += P V in registers; the four
 // states are merged through shared memory at the end of the query.  Rows are
 // padded to D + 8 elements so that ldmatrix reads are free of bank conflicts.
@@ -31,27 +32,13 @@ constexpr int GEN_WARPS = 4;
 constexpr int GEN_THREADS = GEN_WARPS * 32;
 constexpr int GEN_CHUNK = 16;  // tokens per chunk
 
-// Chunks in each warp's cp.async ring (the chunk being computed and NST - 1
-// in flight behind it).  Deeper rings for the small head dims measured slower
-// (B2 Hq32 Hkv2 T8192 D32 bs32: 2 stages 0.451 ms, 3: 0.497, 4: 0.549, 6:
-// 0.667): the shared memory they take costs more resident CTAs per SM than
-// the extra chunks in flight per warp give back.
-#ifndef BSA_GEN_STAGES
-#define BSA_GEN_STAGES 2
-#endif
-template <int D>
-constexpr int gen_stages() {
-  return BSA_GEN_STAGES;
-}
-
 template <int D>
 struct GenLayout {
-  static constexpr int NST = gen_stages<D>();
   static constexpr int RS = D + 8;                       // padded row (bf16 elements)
   static constexpr int RB = RS * 2;                      // padded row in bytes
   static constexpr int Q_OFF = 0;                        // [16][RS] bf16
-  static constexpr int KV_OFF = Q_OFF + 16 * RB;         // [warp][stage][K|V][16][RS]
-  static constexpr int KV_WARP = NST * 2 * 16 * RB;
+  static constexpr int KV_OFF = Q_OFF + 16 * RB;         // [warp][buf][K|V][16][RS]
+  static constexpr int KV_WARP = 2 * 2 * 16 * RB;
   static constexpr int CST = D + 4;                      // combine row stride (floats)
   static constexpr int C_OFF = KV_OFF + GEN_WARPS * KV_WARP;             // fp32 [4][16][CST]
   static constexpr int ML_OFF = C_OFF + GEN_WARPS * 16 * CST * 4;        // fp32 [4][16][2]
@@ -169,27 +156,19 @@ __global__ void __launch_bounds__(GEN_THREADS)
       }
     };
 
-    // `cur` walks the chunks this warp computes, `ld` the ones it loads,
-    // NST - 1 chunks ahead; every iteration commits one cp.async group (empty
-    // once `ld` has run out), so waiting until at most NST - 1 groups are
-    // pending always means the current chunk has landed.
     ChunkIter cur{nsa_live_slots(block_idx + qg * S, S, i, n_blk, bs), i, bs, 0, 0, 0, 0, false};
     cur.seek_slot();
     cur.advance(warp);
-    ChunkIter ld = cur;
-#pragma unroll
-    for (int st = 0; st < L::NST - 1; ++st) {
-      if (ld.valid) load_chunk(ld.tok0, st);
-      cp_async_commit();
-      ld.advance(GEN_WARPS);
-    }
+    ChunkIter nxt = cur;
+    nxt.advance(GEN_WARPS);
+    if (cur.valid) load_chunk(cur.tok0, 0);
+    cp_async_commit();
     for (int it = 0; cur.valid; ++it) {
-      if (ld.valid) load_chunk(ld.tok0, (it + L::NST - 1) % L::NST);
+      if (nxt.valid) load_chunk(nxt.tok0, (it + 1) & 1);
       cp_async_commit();
-      ld.advance(GEN_WARPS);
-      cp_async_wait<L::NST - 1>();  // this chunk's copies have landed
+      cp_async_wait<1>();  // this chunk's copies have landed
       __syncwarp();
-      const uint32_t sK = sKV + (it % L::NST) * 2 * 16 * L::RB, sV = sK + 16 * L::RB;
+      const uint32_t sK = sKV + (it & 1) * 2 * 16 * L::RB, sV = sK + 16 * L::RB;
       const int tok0 = cur.tok0;
 
       // ---- S = Q K^T for tokens tok0 .. tok0+15 (two n8 tiles)
@@ -279,8 +258,9 @@ __global__ void __launch_bounds__(GEN_THREADS)
           mma16816(acc[2 * jj + 1], pa, v2, v3);
         }
       }
-      __syncwarp();  // this stage is refilled at the start of the next iteration
-      cur.advance(GEN_WARPS);
+      __syncwarp();  // the buffer is refilled two chunks later
+      cur = nxt;
+      nxt.advance(GEN_WARPS);
     }
     cp_async_wait<0>();
 

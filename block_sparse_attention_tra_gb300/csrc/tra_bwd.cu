@@ -45,10 +45,25 @@ namespace {
 
 using tile::PANEL_BYTES;
 constexpr int BT = tile::ROWS;  // 128 rows per query tile and per key tile
-constexpr int BWD_THREADS = 224;
-constexpr int EPI_WARPS = 4;
-constexpr int TMA_WARP = 4;
-constexpr int MMA_WARP = 5;  // first of the two MMA-issuing warps (allocates TMEM)
+// Epilogue warpgroups (1 or 2).  With two, warps w and w + 4 share a TMEM lane
+// quarter and take the two 32-column chunks of each score half, so every
+// SMSP runs two epilogue warps and one chunk's TMEM loads and arithmetic
+// overlap the other's.  Measured: B2 H32 T8192 D64 p=2 2.19 -> 2.10 ms,
+// p=1.5 3.69 -> 3.29 ms; B4 H16 T4096 D128 p=2 0.791 -> 0.816 ms (slower), so
+// D = 128 with p = 1 or 2 keeps one.  BSA_BWD_EPI_WG forces 1 or 2 (0: that
+// choice).
+#ifndef BSA_BWD_EPI_WG
+#define BSA_BWD_EPI_WG 0
+#endif
+template <int D, int PC>
+struct BwdCfg {
+  static constexpr bool LIGHT = (PC == POW_ONE || PC == POW_TWO) && D == 128;
+  static constexpr int EPI_WG = BSA_BWD_EPI_WG != 0 ? BSA_BWD_EPI_WG : (LIGHT ? 1 : 2);
+  static constexpr int EPI_WARPS = 4 * EPI_WG;
+  static constexpr int TMA_WARP = EPI_WARPS;
+  static constexpr int MMA_WARP = EPI_WARPS + 1;  // first of the two MMA-issuing warps (allocates TMEM)
+  static constexpr int THREADS = 32 * (EPI_WARPS + 3);
+};
 constexpr uint32_t TMEM_COLS = 512;
 
 __device__ __forceinline__ float ex2a(float x) {
@@ -115,7 +130,8 @@ __device__ __forceinline__ BwdBars bwd_bars(uint8_t* smem) {
 }
 
 template <int D>
-__device__ __forceinline__ void bwd_setup(uint8_t* smem, const BwdBars& B, uint32_t* tptr, int warp, int acc_count) {
+__device__ __forceinline__ void bwd_setup(uint8_t* smem, const BwdBars& B, uint32_t* tptr, int warp, int acc_count,
+                                          int epi_warps, int mma_warp) {
   using L = BwdLayout<D>;
   if (threadIdx.x == 0) {
     mbar_init(B.res_full, 1);
@@ -125,14 +141,14 @@ __device__ __forceinline__ void bwd_setup(uint8_t* smem, const BwdBars& B, uint3
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(&B.s_full[h], 2);  // both issuers' products of half h
-      mbar_init(&B.p_full[h], EPI_WARPS);
+      mbar_init(&B.p_full[h], epi_warps);
       mbar_init(&B.mma_done[h], 1);
-      mbar_init(&B.tau_full[h], EPI_WARPS);
+      mbar_init(&B.tau_full[h], epi_warps);
     }
     mbar_init(B.acc_full, acc_count);
     fence_barrier_init();
   }
-  if (warp == MMA_WARP) {
+  if (warp == mma_warp) {
     tmem_alloc(tptr, TMEM_COLS);
     tmem_relinquish();
   }
@@ -141,10 +157,10 @@ __device__ __forceinline__ void bwd_setup(uint8_t* smem, const BwdBars& B, uint3
   tc_fence_after();
 }
 
-__device__ __forceinline__ void bwd_teardown(uint32_t tmem, int warp) {
+__device__ __forceinline__ void bwd_teardown(uint32_t tmem, int warp, int mma_warp) {
   tc_fence_before();
   __syncthreads();
-  if (warp == MMA_WARP) {
+  if (warp == mma_warp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -215,7 +231,7 @@ __device__ __forceinline__ void bwd_produce(uint8_t* smem, const BwdBars& B, con
 // ---------------------------------------------------------------- dK / dV
 
 template <int D, int PC>
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+__global__ void __launch_bounds__(BwdCfg<D, PC>::THREADS, 1)
     tra_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                         __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int T, int nT,
@@ -233,7 +249,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const int nq = nT - n;  // query tiles m = n .. nT-1
   constexpr uint32_t ST = 0, DPT = BT, DV = 2 * BT, DK = 2 * BT + D;
 
-  bwd_setup<D>(smem, B, tptr, warp, 2);
+  using Cfg = BwdCfg<D, PC>;
+  constexpr int EPI_WG = Cfg::EPI_WG, EPI_WARPS = Cfg::EPI_WARPS, TMA_WARP = Cfg::TMA_WARP, MMA_WARP = Cfg::MMA_WARP;
+  bwd_setup<D>(smem, B, tptr, warp, 2, EPI_WARPS, MMA_WARP);
   const uint32_t tmem = *tptr;
 
   if (warp == TMA_WARP) {
@@ -288,9 +306,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_wait(&B.mma_done[is], 0);
     }
   } else if (warp < EPI_WARPS) {
-    const int r = warp * 32 + lane;  // key row within the tile
+    const int wq = warp & 3, grp = warp >> 2;  // TMEM lane quarter; chunk of each half (two warpgroups)
+    const int r = wq * 32 + lane;              // key row within the tile
     const int key = n * BT + r;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     bool ok = true;
     for (int j = 0; j < nq && ok; ++j) {
       const int m = n + j;
@@ -307,11 +326,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         if (!(ok = mbar_wait(&B.s_full[h], j & 1))) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 2 * h; c < 2 * h + 2; ++c) {
+        for (int c = 2 * h + (EPI_WG == 2 ? grp : 0); c < 2 * h + 2; c += EPI_WG) {
           uint32_t sv[32], dp[32];
           tmem_ld32(lane_base + ST + 32 * c, sv);
           tmem_ld32(lane_base + DPT + 32 * c, dp);
           tmem_wait_ld();
+          // Chunk 2h + 1 packs into chunk 2h's columns: with two warpgroups,
+          // both chunks are loaded before either warp stores.
+          if constexpr (EPI_WG == 2) asm volatile("bar.sync %0, 64;" ::"r"(1 + wq) : "memory");
           uint32_t wpk[16], apk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -341,20 +363,21 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (ok && mbar_wait(B.acc_full, 0)) {
       tc_fence_after();
       const size_t rowoff = (static_cast<size_t>(bh) * T + key) * D;
+      constexpr int CPW = D / 32 / EPI_WG;  // 32-column chunks of dK, dV this warp stores
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = grp * CPW; c < (grp + 1) * CPW; ++c) {
         tile::store_row_chunk(lane_base + DV, c, dv + rowoff, key < T);
         tile::store_row_chunk(lane_base + DK, c, dk + rowoff, key < T);
       }
     }
   }
-  bwd_teardown(tmem, warp);
+  bwd_teardown(tmem, warp, MMA_WARP);
 }
 
 // ---------------------------------------------------------------------- dQ
 
 template <int D, int PC>
-__global__ void __launch_bounds__(BWD_THREADS, 1)
+__global__ void __launch_bounds__(BwdCfg<D, PC>::THREADS, 1)
     tra_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                       __nv_bfloat16* __restrict__ dq, int BH, int T, int nT, int G, float beta, float p) {
@@ -369,7 +392,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const int bh = item.bh;
   constexpr uint32_t S = 0, DP = BT, DQ = 2 * BT;
 
-  bwd_setup<D>(smem, B, tptr, warp, 1);
+  using Cfg = BwdCfg<D, PC>;
+  constexpr int EPI_WG = Cfg::EPI_WG, EPI_WARPS = Cfg::EPI_WARPS, TMA_WARP = Cfg::TMA_WARP, MMA_WARP = Cfg::MMA_WARP;
+  bwd_setup<D>(smem, B, tptr, warp, 1, EPI_WARPS, MMA_WARP);
   const uint32_t tmem = *tptr;
 
   if (warp == TMA_WARP) {
@@ -421,10 +446,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_wait(&B.mma_done[is], 0);
     }
   } else if (warp < EPI_WARPS) {
-    const int r = warp * 32 + lane;
+    const int wq = warp & 3, grp = warp >> 2;  // TMEM lane quarter; chunk of each half (two warpgroups)
+    const int r = wq * 32 + lane;
     const int row = m * BT + r;
     const float tau = tile::tau_of_row(row, beta, D);
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     bool ok = true;
     for (int n = 0; n <= m && ok; ++n) {
       const bool diag = (n == m);
@@ -432,11 +458,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         if (!(ok = mbar_wait(&B.s_full[h], n & 1))) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 2 * h; c < 2 * h + 2; ++c) {
+        for (int c = 2 * h + (EPI_WG == 2 ? grp : 0); c < 2 * h + 2; c += EPI_WG) {
           uint32_t sv[32], dp[32];
           tmem_ld32(lane_base + S + 32 * c, sv);
           tmem_ld32(lane_base + DP + 32 * c, dp);
           tmem_wait_ld();
+          // Chunk 2h + 1 packs into chunk 2h's columns (see the dK/dV kernel).
+          if constexpr (EPI_WG == 2) asm volatile("bar.sync %0, 64;" ::"r"(1 + wq) : "memory");
           uint32_t apk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -462,11 +490,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (ok && mbar_wait(B.acc_full, 0)) {
       tc_fence_after();
       __nv_bfloat16* dst = dq + (static_cast<size_t>(bh) * T + row) * D;
+      constexpr int CPW = D / 32 / EPI_WG;  // 32-column chunks of dQ this warp stores
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) tile::store_row_chunk(lane_base + DQ, c, dst, row < T);
+      for (int c = grp * CPW; c < (grp + 1) * CPW; ++c) tile::store_row_chunk(lane_base + DQ, c, dst, row < T);
     }
   }
-  bwd_teardown(tmem, warp);
+  bwd_teardown(tmem, warp, MMA_WARP);
 }
 
 template <int D, int PC>
@@ -483,11 +512,11 @@ int launch_bwd(const CUtensorMap* maps, void* dq, void* dk, void* dv, int BH, in
   if (grid > 0x7fffffffLL) return ERR_SHAPE;
   // two streamed bf16 tensors of T x D per head; one resident CTA per SM
   const int G = tile::head_groups(BH, nT, 4LL * T * D, sm_count());
-  k1<<<static_cast<unsigned>(grid), BWD_THREADS, L::ALLOC, stream>>>(
+  k1<<<static_cast<unsigned>(grid), BwdCfg<D, PC>::THREADS, L::ALLOC, stream>>>(
       maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), BH, T,
       nT, G, beta, p);
   if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
-  k2<<<static_cast<unsigned>(grid), BWD_THREADS, L::ALLOC, stream>>>(
+  k2<<<static_cast<unsigned>(grid), BwdCfg<D, PC>::THREADS, L::ALLOC, stream>>>(
       maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dq), BH, T, nT, G, beta, p);
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
