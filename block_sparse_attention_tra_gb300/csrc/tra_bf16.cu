@@ -98,12 +98,6 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tS, const PowParams& wp, 
   if (lane == 0) mbar_arrive(p_full);
 }
 
-// Prefetch the second of the two quarters' scores under the first one's
-// arithmetic (costs 32 registers, where 18 warps per CTA cap a thread at 96).
-#ifndef BSA_PAIR_EPI_PREFETCH
-#define BSA_PAIR_EPI_PREFETCH 0
-#endif
-
 // Two of a tile's four score quarters (q = half and half + 2) for one of the
 // two warps that share a TMEM lane quarter.  P of quarter q lands in TMEM
 // columns 16q .. 16q+15, inside quarter q / 2's scores, which may belong to
@@ -117,25 +111,14 @@ __device__ __forceinline__ void epilogue_two_quarters(uint32_t tS, const PowPara
   tmem_ld32(tS + 32 * half, a);
   tmem_wait_ld();
   asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
-#if BSA_PAIR_EPI_PREFETCH
-  // The second quarter's scores (columns 64..127) are never written over by P
-  // (columns 0..63): load them now, under the first quarter's arithmetic.
-  uint32_t b[32];
-  tmem_ld32(tS + 32 * (half + 2), b);
-#endif
   epilogue_quarter<PC, DIAG, MP>(a, tS, 32 * half, wp, key0, row);
   tmem_wait_st();
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(p_half);
-#if BSA_PAIR_EPI_PREFETCH
-  tmem_wait_ld();
-  epilogue_quarter<PC, DIAG, MP>(b, tS, 32 * (half + 2), wp, key0, row);
-#else
   tmem_ld32(tS + 32 * (half + 2), a);
   tmem_wait_ld();
   epilogue_quarter<PC, DIAG, MP>(a, tS, 32 * (half + 2), wp, key0, row);
-#endif
   tmem_wait_st();
   tc_fence_before();
   __syncwarp();

@@ -55,10 +55,17 @@ constexpr int BT = tile::ROWS;  // 128 rows per query tile and per key tile
 #ifndef BSA_BWD_EPI_WG
 #define BSA_BWD_EPI_WG 0
 #endif
-template <int D, int PC>
+#ifndef BSA_BWD_DQ_EPI_WG
+#define BSA_BWD_DQ_EPI_WG BSA_BWD_EPI_WG
+#endif
+#ifndef BSA_BWD_DKDV_EPI_WG
+#define BSA_BWD_DKDV_EPI_WG BSA_BWD_EPI_WG
+#endif
+template <int D, int PC, bool DQ>
 struct BwdCfg {
   static constexpr bool LIGHT = (PC == POW_ONE || PC == POW_TWO) && D == 128;
-  static constexpr int EPI_WG = BSA_BWD_EPI_WG != 0 ? BSA_BWD_EPI_WG : (LIGHT ? 1 : 2);
+  static constexpr int FORCED = DQ ? BSA_BWD_DQ_EPI_WG : BSA_BWD_DKDV_EPI_WG;
+  static constexpr int EPI_WG = FORCED != 0 ? FORCED : (LIGHT ? 1 : 2);
   static constexpr int EPI_WARPS = 4 * EPI_WG;
   static constexpr int TMA_WARP = EPI_WARPS;
   static constexpr int MMA_WARP = EPI_WARPS + 1;  // first of the two MMA-issuing warps (allocates TMEM)
@@ -231,7 +238,7 @@ __device__ __forceinline__ void bwd_produce(uint8_t* smem, const BwdBars& B, con
 // ---------------------------------------------------------------- dK / dV
 
 template <int D, int PC>
-__global__ void __launch_bounds__(BwdCfg<D, PC>::THREADS, 1)
+__global__ void __launch_bounds__(BwdCfg<D, PC, false>::THREADS, 1)
     tra_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                         __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int T, int nT,
@@ -249,7 +256,7 @@ __global__ void __launch_bounds__(BwdCfg<D, PC>::THREADS, 1)
   const int nq = nT - n;  // query tiles m = n .. nT-1
   constexpr uint32_t ST = 0, DPT = BT, DV = 2 * BT, DK = 2 * BT + D;
 
-  using Cfg = BwdCfg<D, PC>;
+  using Cfg = BwdCfg<D, PC, false>;
   constexpr int EPI_WG = Cfg::EPI_WG, EPI_WARPS = Cfg::EPI_WARPS, TMA_WARP = Cfg::TMA_WARP, MMA_WARP = Cfg::MMA_WARP;
   bwd_setup<D>(smem, B, tptr, warp, 2, EPI_WARPS, MMA_WARP);
   const uint32_t tmem = *tptr;
@@ -377,7 +384,7 @@ __global__ void __launch_bounds__(BwdCfg<D, PC>::THREADS, 1)
 // ---------------------------------------------------------------------- dQ
 
 template <int D, int PC>
-__global__ void __launch_bounds__(BwdCfg<D, PC>::THREADS, 1)
+__global__ void __launch_bounds__(BwdCfg<D, PC, true>::THREADS, 1)
     tra_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                       __nv_bfloat16* __restrict__ dq, int BH, int T, int nT, int G, float beta, float p) {
@@ -392,7 +399,7 @@ __global__ void __launch_bounds__(BwdCfg<D, PC>::THREADS, 1)
   const int bh = item.bh;
   constexpr uint32_t S = 0, DP = BT, DQ = 2 * BT;
 
-  using Cfg = BwdCfg<D, PC>;
+  using Cfg = BwdCfg<D, PC, true>;
   constexpr int EPI_WG = Cfg::EPI_WG, EPI_WARPS = Cfg::EPI_WARPS, TMA_WARP = Cfg::TMA_WARP, MMA_WARP = Cfg::MMA_WARP;
   bwd_setup<D>(smem, B, tptr, warp, 1, EPI_WARPS, MMA_WARP);
   const uint32_t tmem = *tptr;
@@ -512,11 +519,11 @@ int launch_bwd(const CUtensorMap* maps, void* dq, void* dk, void* dv, int BH, in
   if (grid > 0x7fffffffLL) return ERR_SHAPE;
   // two streamed bf16 tensors of T x D per head; one resident CTA per SM
   const int G = tile::head_groups(BH, nT, 4LL * T * D, sm_count());
-  k1<<<static_cast<unsigned>(grid), BwdCfg<D, PC>::THREADS, L::ALLOC, stream>>>(
+  k1<<<static_cast<unsigned>(grid), BwdCfg<D, PC, false>::THREADS, L::ALLOC, stream>>>(
       maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), BH, T,
       nT, G, beta, p);
   if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
-  k2<<<static_cast<unsigned>(grid), BwdCfg<D, PC>::THREADS, L::ALLOC, stream>>>(
+  k2<<<static_cast<unsigned>(grid), BwdCfg<D, PC, true>::THREADS, L::ALLOC, stream>>>(
       maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dq), BH, T, nT, G, beta, p);
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
