@@ -237,12 +237,12 @@ __device__ __forceinline__ void bwd_produce(uint8_t* smem, const BwdBars& B, con
 
 // ---------------------------------------------------------------- dK / dV
 
+// dK/dV work of block `blk` (key tile, head): the body of the dK/dV kernel.
 template <int D, int PC>
-__global__ void __launch_bounds__(BwdCfg<D, PC, false>::THREADS, 1)
-    tra_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                        __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int T, int nT,
-                        int G, float beta, float p) {
+__device__ __forceinline__ void bwd_dkdv_block(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                               const CUtensorMap& tmDO, __nv_bfloat16* __restrict__ dk,
+                                               __nv_bfloat16* __restrict__ dv, int BH, int T, int nT, int G,
+                                               float beta, float p, int blk) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(BwdCfg<D, PC, false>::THREADS, 1)
   uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
   float* tau_s = reinterpret_cast<float*>(smem + L::TAU_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const tile::HeadItem item = tile::head_group_item(static_cast<int>(blockIdx.x), BH, nT, G);
+  const tile::HeadItem item = tile::head_group_item(blk, BH, nT, G);
   const int n = item.rank;  // key tile; n = 0 has the most query tiles
   const int bh = item.bh;
   const int nq = nT - n;  // query tiles m = n .. nT-1
@@ -383,18 +383,18 @@ __global__ void __launch_bounds__(BwdCfg<D, PC, false>::THREADS, 1)
 
 // ---------------------------------------------------------------------- dQ
 
+// dQ work of block `blk` (query tile, head): the body of the dQ kernel.
 template <int D, int PC>
-__global__ void __launch_bounds__(BwdCfg<D, PC, true>::THREADS, 1)
-    tra_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                      __nv_bfloat16* __restrict__ dq, int BH, int T, int nT, int G, float beta, float p) {
+__device__ __forceinline__ void bwd_dq_block(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                             const CUtensorMap& tmDO, __nv_bfloat16* __restrict__ dq, int BH, int T,
+                                             int nT, int G, float beta, float p, int blk) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const BwdBars B = bwd_bars<D>(smem);
   uint32_t* tptr = reinterpret_cast<uint32_t*>(smem + L::TPTR_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const tile::HeadItem item = tile::head_group_item(static_cast<int>(blockIdx.x), BH, nT, G);
+  const tile::HeadItem item = tile::head_group_item(blk, BH, nT, G);
   const int m = nT - 1 - item.rank;  // longest first
   const int bh = item.bh;
   constexpr uint32_t S = 0, DP = BT, DQ = 2 * BT;
@@ -506,26 +506,74 @@ __global__ void __launch_bounds__(BwdCfg<D, PC, true>::THREADS, 1)
 }
 
 template <int D, int PC>
+__global__ void __launch_bounds__(BwdCfg<D, PC, false>::THREADS, 1)
+    tra_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                        __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int T, int nT,
+                        int G, float beta, float p) {
+  bwd_dkdv_block<D, PC>(tmQ, tmK, tmV, tmDO, dk, dv, BH, T, nT, G, beta, p, static_cast<int>(blockIdx.x));
+}
+
+template <int D, int PC>
+__global__ void __launch_bounds__(BwdCfg<D, PC, true>::THREADS, 1)
+    tra_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                      __nv_bfloat16* __restrict__ dq, int BH, int T, int nT, int G, float beta, float p) {
+  bwd_dq_block<D, PC>(tmQ, tmK, tmV, tmDO, dq, BH, T, nT, G, beta, p, static_cast<int>(blockIdx.x));
+}
+
+// Both kinds of block in one grid: the dK/dV blocks first, then the dQ
+// blocks, which start on the SMs the dK/dV blocks' tail leaves free instead of
+// after the whole first launch has drained.
+template <int D, int PC>
+__global__ void __launch_bounds__(BwdCfg<D, PC, false>::THREADS, 1)
+    tra_bwd_both_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                        __nv_bfloat16* __restrict__ dq, __nv_bfloat16* __restrict__ dk,
+                        __nv_bfloat16* __restrict__ dv, int BH, int T, int nT, int G, float beta, float p) {
+  const int nk = nT * BH, b = static_cast<int>(blockIdx.x);
+  if (b < nk)
+    bwd_dkdv_block<D, PC>(tmQ, tmK, tmV, tmDO, dk, dv, BH, T, nT, G, beta, p, b);
+  else
+    bwd_dq_block<D, PC>(tmQ, tmK, tmV, tmDO, dq, BH, T, nT, G, beta, p, b - nk);
+}
+
+#ifndef BSA_BWD_ONE_GRID
+#define BSA_BWD_ONE_GRID 1
+#endif
+
+template <int D, int PC>
 int launch_bwd(const CUtensorMap* maps, void* dq, void* dk, void* dv, int BH, int T, float beta, float p,
                cudaStream_t stream) {
   using L = BwdLayout<D>;
-  auto k1 = tra_bwd_dkdv_kernel<D, PC>;
-  auto k2 = tra_bwd_dq_kernel<D, PC>;
-  if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess ||
-      cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
-    return ERR_LAUNCH;
   const int nT = (T + BT - 1) / BT;
   const long long grid = static_cast<long long>(nT) * BH;
-  if (grid > 0x7fffffffLL) return ERR_SHAPE;
+  if (2 * grid > 0x7fffffffLL) return ERR_SHAPE;
   // two streamed bf16 tensors of T x D per head; one resident CTA per SM
   const int G = tile::head_groups(BH, nT, 4LL * T * D, sm_count());
-  k1<<<static_cast<unsigned>(grid), BwdCfg<D, PC, false>::THREADS, L::ALLOC, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), BH, T,
-      nT, G, beta, p);
-  if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
-  k2<<<static_cast<unsigned>(grid), BwdCfg<D, PC, true>::THREADS, L::ALLOC, stream>>>(
-      maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dq), BH, T, nT, G, beta, p);
-  return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
+  constexpr bool ONE_GRID = BSA_BWD_ONE_GRID && BwdCfg<D, PC, false>::THREADS == BwdCfg<D, PC, true>::THREADS;
+  if constexpr (ONE_GRID) {
+    auto k = tra_bwd_both_kernel<D, PC>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
+      return ERR_LAUNCH;
+    k<<<static_cast<unsigned>(2 * grid), BwdCfg<D, PC, false>::THREADS, L::ALLOC, stream>>>(
+        maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
+        static_cast<__nv_bfloat16*>(dv), BH, T, nT, G, beta, p);
+    return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
+  } else {
+    auto k1 = tra_bwd_dkdv_kernel<D, PC>;
+    auto k2 = tra_bwd_dq_kernel<D, PC>;
+    if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess ||
+        cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
+      return ERR_LAUNCH;
+    k1<<<static_cast<unsigned>(grid), BwdCfg<D, PC, false>::THREADS, L::ALLOC, stream>>>(
+        maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), BH, T,
+        nT, G, beta, p);
+    if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
+    k2<<<static_cast<unsigned>(grid), BwdCfg<D, PC, true>::THREADS, L::ALLOC, stream>>>(
+        maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dq), BH, T, nT, G, beta, p);
+    return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
+  }
 }
 
 }  // namespace

@@ -137,6 +137,15 @@ __host__ __device__ constexpr bool mix_pair_on_fma(int e) {
   return ((e % 16) * M) % 16 >= M;
 }
 
+// p = 2: round x to bf16 and square in bf16 (0: two roundings, at most ~1.5
+// bf16 ulp per weight), or square in fp32 and round once (1: half an ulp, one
+// instruction more per key pair; measured 8.6% slower at B4 H16 T4096 D128
+// and 4% at B2 H32 T8192 D64, whose epilogues share the SMSPs with the MMA
+// issue).
+#ifndef BSA_POW2_SINGLE_ROUNDING
+#define BSA_POW2_SINGLE_ROUNDING 0
+#endif
+
 // Weights of two adjacent keys from their scores: ReLU(s - tau)^p, bf16x2.
 // FMA_LOG2 (POW_GENERAL_MIX only): this pair's log2 runs on the FMA pipe.
 template <int PC, bool FMA_LOG2 = false>
@@ -146,8 +155,14 @@ __device__ __forceinline__ uint32_t weights2(float s0, float s1, const PowParams
   if constexpr (PC == POW_ONE) {
     return relu_pack(x0, x1);
   } else if constexpr (PC == POW_TWO) {
-    const uint32_t h = relu_pack(x0, x1);
+#if BSA_POW2_SINGLE_ROUNDING
+    // x |x| is x^2 where x > 0 and negative elsewhere, so the ReLU of the
+    // conversion keeps exactly the positive part: one rounding, from fp32.
+    return relu_pack(x0 * fabsf(x0), x1 * fabsf(x1));
+#else
+    const uint32_t h = relu_pack(x0, x1);  // x rounded to bf16, then squared in bf16
     return mul_bf16x2(h, h);
+#endif
   } else if constexpr (PC == POW_GENERAL_MIX) {
     x0 = fmaxf(x0, 0.0f);
     x1 = fmaxf(x1, 0.0f);
