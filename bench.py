@@ -715,7 +715,7 @@ def run_op(args):
     if args.op == "backward":
         fn = lambda: bsa.tra_backward(q, k, v, extra[0], w.beta, w.p)  # noqa: E731
         flops = 10 * w.flops // 4
-        launches = 2
+        launches = 1  # dK/dV and dQ blocks in one grid
     else:
         fn = lambda: bsa.tra_diff_forward(q, extra[0], k, extra[1], v, w.beta, 0.5, w.p, normalize=True)  # noqa: E731
         flops = 2 * w.flops

@@ -160,7 +160,7 @@ int tra_forward_ex(const void* q, const void* k, const void* v, void* out, int B
   if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
-  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
   if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f)) return BSA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return BSA_ERR_ALIGN;
   const int dv = check_device();
@@ -173,7 +173,7 @@ int tra_forward_ex(const void* q, const void* k, const void* v, void* out, int B
 
 size_t tra_forward_host_workspace_size(int B, int H, int T, int D, int dtype) {
   if (dtype != BSA_F32 && dtype != BSA_BF16) return 0;
-  if (B < 1 || H < 1 || T < 1 || (D != 64 && D != 128)) return 0;
+  if (B < 1 || H < 1 || T < 1 || (D != 16 && D != 32 && D != 64 && D != 128)) return 0;
   if (static_cast<long long>(B) * H > 0x7fffffffLL || static_cast<long long>(B) * H * T * D >= (1LL << 40)) return 0;
   return tra_host_workspace_bytes(static_cast<long long>(B) * H, T, D, dtype == BSA_F32 ? 4 : 2);
 }
@@ -185,7 +185,7 @@ int tra_forward_host(const void* q, const void* k, const void* v, void* out, int
   if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
-  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
   if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f)) return BSA_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BSA_ERR_ALIGN;
   if (workspace_bytes < tra_forward_host_workspace_size(B, H, T, D, dtype)) return BSA_ERR_SCRATCH_LIMIT;

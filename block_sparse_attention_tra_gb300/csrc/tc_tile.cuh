@@ -68,6 +68,27 @@ __device__ __forceinline__ void store_row_chunk(uint32_t tC, int c, __nv_bfloat1
   }
 }
 
+// The first `ncols` (16 or 32) of the 32 columns [c*32, c*32+32) of this
+// thread's TMEM lane -> bf16 -> global memory at row + c*32 (skipped when
+// !in_range): the last, partial chunk of a row whose head dim is not a
+// multiple of 32.
+__device__ __forceinline__ void store_row_part(uint32_t tC, int c, __nv_bfloat16* row, bool in_range, int ncols) {
+  uint32_t v[32];
+  tmem_ld32(tC + c * 32, v);
+  tmem_wait_ld();
+  if (in_range) {
+    uint4* dst = reinterpret_cast<uint4*>(row + c * 32);
+    for (int q = 0; q < ncols / 8; ++q) {
+      uint4 u;
+      u.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+      u.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+      u.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+      u.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+      dst[q] = u;
+    }
+  }
+}
+
 // tau(i) = beta * sqrt(2 ln(i+1) / D), in fp32 as the page computes it.
 __device__ __forceinline__ float tau_of_row(int row, float beta, int D) {
   return beta * sqrtf(2.0f * logf(static_cast<float>(row + 1)) / static_cast<float>(D));

@@ -217,10 +217,11 @@ template <int D, int PC>
 __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
     tra_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out, int BH, int T,
-                         int nQ, int nPair, int nItems, float beta, float p) {
+                         int nQ, int nPair, int nItems, float beta, float p, int d_real) {
   using L = PairLayout<D>;
   using Cfg = PairCfg<PC>;
   constexpr int PAIR_TMA_WARP = Cfg::TMA_WARP;
+  const int dr = D == 128 ? D : d_real;  // tile width 128 serves head dim 128 alone
   constexpr int PAIR_MMA_WARP = Cfg::MMA_WARP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -511,7 +512,7 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
       if (qt == 1 && !it.has1) continue;
       const int nmax = qt == 0 ? it.nmax0 : it.nmax1;
       const int row = (2 * it.t + qt) * BM + wq * 32 + lane;
-      const PowParams wp = pow_params(tile::tau_of_row(row, beta, D), p);
+      const PowParams wp = pow_params(tile::tau_of_row(row, beta, dr), p);
       for (int n = 0; n <= nmax; ++n, ++cs) {
         if (!(ok = mbar_wait(&s_full[qt], cs & 1))) break;
         tc_fence_after();
@@ -531,11 +532,16 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
       }
       if (!ok || !(ok = mbar_wait(&o_full[qt], uq & 1))) break;
       tc_fence_after();
-      __nv_bfloat16* orow = out + (static_cast<size_t>(it.bh) * T + row) * D;
+      __nv_bfloat16* orow = out + (static_cast<size_t>(it.bh) * T + row) * dr;
       constexpr int CPW = D / 32 / Cfg::EPI_WG;  // 32-column chunks of O this warp stores
 #pragma unroll
-      for (int c = 0; c < CPW; ++c)
-        tile::store_row_chunk(lane_base + 2 * BN + qt * D, half * CPW + c, orow, row < T);
+      for (int c = 0; c < CPW; ++c) {
+        const int cc = half * CPW + c;
+        if (dr == D)
+          tile::store_row_chunk(lane_base + 2 * BN + qt * D, cc, orow, row < T);
+        else if (cc * 32 < dr)  // head dim below the tile width: only its columns
+          tile::store_row_part(lane_base + 2 * BN + qt * D, cc, orow, row < T, min(32, dr - cc * 32));
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_empty[qt]);
@@ -554,7 +560,7 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
 
 template <int D, int PC>
 int launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* out, int BH, int T,
-                float beta, float p, cudaStream_t stream) {
+                float beta, float p, cudaStream_t stream, int d_real = D) {
   using L = PairLayout<D>;
   auto kern = tra_bf16_pair_kernel<D, PC>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
@@ -567,21 +573,31 @@ int launch_pair(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
   if (sms <= 0) return ERR_DEVICE;
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
   kern<<<grid, PairCfg<PC>::THREADS, L::ALLOC, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(out), BH, T, nQ, nPair,
-                                                 static_cast<int>(items), beta, p);
+                                                 static_cast<int>(items), beta, p, d_real);
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
 
 // Half powers (on request).
 template <int D>
 int launch_half(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* out, int BH, int T,
-                float beta, float p, int hc, cudaStream_t stream) {
+                float beta, float p, int hc, cudaStream_t stream, int d_real) {
   switch (hc) {
-    case POW_HALF0: return launch_pair<D, POW_HALF0>(mq, mk, mv, out, BH, T, beta, p, stream);
-    case POW_HALF0 + 1: return launch_pair<D, POW_HALF0 + 1>(mq, mk, mv, out, BH, T, beta, p, stream);
-    case POW_HALF0 + 2: return launch_pair<D, POW_HALF0 + 2>(mq, mk, mv, out, BH, T, beta, p, stream);
-    case POW_HALF3: return launch_pair<D, POW_HALF3>(mq, mk, mv, out, BH, T, beta, p, stream);
+    case POW_HALF0: return launch_pair<D, POW_HALF0>(mq, mk, mv, out, BH, T, beta, p, stream, d_real);
+    case POW_HALF0 + 1: return launch_pair<D, POW_HALF0 + 1>(mq, mk, mv, out, BH, T, beta, p, stream, d_real);
+    case POW_HALF0 + 2: return launch_pair<D, POW_HALF0 + 2>(mq, mk, mv, out, BH, T, beta, p, stream, d_real);
+    case POW_HALF3: return launch_pair<D, POW_HALF3>(mq, mk, mv, out, BH, T, beta, p, stream, d_real);
     default: return ERR_UNSUPPORTED;
   }
+}
+
+// Every power class at tile width D for a head dim d_real <= D.
+template <int D>
+int launch_width(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* out, int BH, int T,
+                 float beta, float p, int pc, cudaStream_t stream, int d_real) {
+  if (pc == POW_TWO) return launch_pair<D, POW_TWO>(mq, mk, mv, out, BH, T, beta, p, stream, d_real);
+  if (pc == POW_ONE) return launch_pair<D, POW_ONE>(mq, mk, mv, out, BH, T, beta, p, stream, d_real);
+  if (pc == POW_GENERAL_MIX) return launch_pair<D, POW_GENERAL_MIX>(mq, mk, mv, out, BH, T, beta, p, stream, d_real);
+  return launch_pair<D, POW_GENERAL>(mq, mk, mv, out, BH, T, beta, p, stream, d_real);
 }
 
 }  // namespace
@@ -589,6 +605,7 @@ int launch_half(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
 int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int D,
                     float beta, float p, bool sqrt_half_powers, cudaStream_t stream) {
   const int BH = B * H;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return ERR_UNSUPPORTED;
   CUtensorMap mq, mk, mv;
   const uint64_t rs = static_cast<uint64_t>(D) * 2;  // row stride in bytes
   const uint64_t hs = rs * T;                        // (b, h) stride in bytes
@@ -598,24 +615,15 @@ int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int 
   if (st != OK) return st;
   const int pc = power_class(p);
   const int hc = sqrt_half_powers ? half_power_class(p) : -1;
-  if (hc >= 0) {
-    if (D == 128) return launch_half<128>(mq, mk, mv, out, BH, T, beta, p, hc, stream);
-    if (D == 64) return launch_half<64>(mq, mk, mv, out, BH, T, beta, p, hc, stream);
-    return ERR_UNSUPPORTED;
-  }
-  if (D == 128) {
-    if (pc == POW_TWO) return launch_pair<128, POW_TWO>(mq, mk, mv, out, BH, T, beta, p, stream);
-    if (pc == POW_ONE) return launch_pair<128, POW_ONE>(mq, mk, mv, out, BH, T, beta, p, stream);
-    if (pc == POW_GENERAL_MIX) return launch_pair<128, POW_GENERAL_MIX>(mq, mk, mv, out, BH, T, beta, p, stream);
-    return launch_pair<128, POW_GENERAL>(mq, mk, mv, out, BH, T, beta, p, stream);
-  }
-  if (D == 64) {
-    if (pc == POW_TWO) return launch_pair<64, POW_TWO>(mq, mk, mv, out, BH, T, beta, p, stream);
-    if (pc == POW_ONE) return launch_pair<64, POW_ONE>(mq, mk, mv, out, BH, T, beta, p, stream);
-    if (pc == POW_GENERAL_MIX) return launch_pair<64, POW_GENERAL_MIX>(mq, mk, mv, out, BH, T, beta, p, stream);
-    return launch_pair<64, POW_GENERAL>(mq, mk, mv, out, BH, T, beta, p, stream);
-  }
-  return ERR_UNSUPPORTED;
+  // Head dims 16 and 32 run at tile width 64: the TMA box of 64 columns reads
+  // zeros past the tensor's D columns, which change neither q.k nor P V, and
+  // only the D real columns of O are stored.
+  const int width = D <= 64 ? 64 : 128;
+  if (hc >= 0)
+    return width == 128 ? launch_half<128>(mq, mk, mv, out, BH, T, beta, p, hc, stream, D)
+                        : launch_half<64>(mq, mk, mv, out, BH, T, beta, p, hc, stream, D);
+  return width == 128 ? launch_width<128>(mq, mk, mv, out, BH, T, beta, p, pc, stream, D)
+                      : launch_width<64>(mq, mk, mv, out, BH, T, beta, p, pc, stream, D);
 }
 
 unsigned int tra_bf16_device_error() { return read_and_clear_device_error(); }

@@ -148,23 +148,27 @@ int launch(const float* q, const float* k, const float* v, float* out, int BH, i
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
 
+template <int D>
+int launch_d(const float* q, const float* k, const float* v, float* out, int BH, int T, float beta, float p,
+             cudaStream_t stream) {
+  const int pc = power_class(p);
+  if (pc == POW_TWO) return launch<D, POW_TWO>(q, k, v, out, BH, T, beta, p, stream);
+  if (pc == POW_ONE) return launch<D, POW_ONE>(q, k, v, out, BH, T, beta, p, stream);
+  return launch<D, POW_GENERAL>(q, k, v, out, BH, T, beta, p, stream);
+}
+
 }  // namespace
 
 int launch_tra_f32(const float* q, const float* k, const float* v, float* out, int B, int H, int T, int D,
                    float beta, float p, cudaStream_t stream) {
   const int BH = B * H;
-  const int pc = power_class(p);
-  if (D == 64) {
-    if (pc == POW_TWO) return launch<64, POW_TWO>(q, k, v, out, BH, T, beta, p, stream);
-    if (pc == POW_ONE) return launch<64, POW_ONE>(q, k, v, out, BH, T, beta, p, stream);
-    return launch<64, POW_GENERAL>(q, k, v, out, BH, T, beta, p, stream);
+  switch (D) {
+    case 16: return launch_d<16>(q, k, v, out, BH, T, beta, p, stream);
+    case 32: return launch_d<32>(q, k, v, out, BH, T, beta, p, stream);
+    case 64: return launch_d<64>(q, k, v, out, BH, T, beta, p, stream);
+    case 128: return launch_d<128>(q, k, v, out, BH, T, beta, p, stream);
+    default: return ERR_UNSUPPORTED;
   }
-  if (D == 128) {
-    if (pc == POW_TWO) return launch<128, POW_TWO>(q, k, v, out, BH, T, beta, p, stream);
-    if (pc == POW_ONE) return launch<128, POW_ONE>(q, k, v, out, BH, T, beta, p, stream);
-    return launch<128, POW_GENERAL>(q, k, v, out, BH, T, beta, p, stream);
-  }
-  return ERR_UNSUPPORTED;
 }
 
 unsigned int tra_f32_device_error() { return read_and_clear_device_error(); }

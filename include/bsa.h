@@ -92,7 +92,9 @@ typedef enum {
  *   q, k, v, out : [B, H, T, D], element type `dtype`; out has the input type
  *                  (the page casts its fp32 result back to the input dtype).
  *   B, H, T      : >= 1; B * H <= 2^31 - 1 and B*H*T*D < 2^40.
- *   D            : 64 or 128 (head dim).
+ *   D            : 16, 32, 64 or 128 (head dim; the page's kernel takes any
+ *                  power of two up to 128 as its BLOCK_D).  16 and 32 run the
+ *                  width-64 kernel on zero-filled columns.
  *   beta         : finite.      p : finite and > 0.
  *   dtype        : BSA_BF16 -- tensor-core (tcgen05) path, bf16 operands,
  *                  fp32 accumulation, weights rounded to bf16 before W.V;
@@ -100,7 +102,7 @@ typedef enum {
  *   stream       : CUDA stream the kernel is enqueued on.
  *
  * Errors: BSA_ERR_NULLPTR, BSA_ERR_SHAPE (sizes), BSA_ERR_DTYPE,
- * BSA_ERR_UNSUPPORTED (D not 64/128, p <= 0, non-finite beta/p),
+ * BSA_ERR_UNSUPPORTED (D not 16/32/64/128, p <= 0, non-finite beta/p),
  * BSA_ERR_ALIGN, BSA_ERR_DEVICE, BSA_ERR_LAUNCH.
  */
 BSA_API int tra_forward(const void* q, const void* k, const void* v, void* out,
@@ -175,16 +177,22 @@ BSA_API int tra_forward_host(const void* q, const void* k, const void* v,
  *   dq_i  = sum_j dA_ij k_j                 dk_j = sum_i dA_ij q_i
  *
  * beta and p receive no gradient (as on the page).  Scores are recomputed
- * (nothing is saved by tra_forward).  Two kernel launches on `stream`: one
- * per key tile for dk and dv, one per query tile for dq.
+ * (nothing is saved by tra_forward).  bf16: one launch on `stream` whose
+ * blocks compute dk and dv per key tile, then dq per query tile.  fp32: two
+ * launches (CUDA-core kernels, fp32 throughout, as the page computes).
  *
- *   q, k, v, dout       : [B, H, T, D] bf16 inputs (dout = dL/d out).
- *   dq, dk, dv          : [B, H, T, D] bf16 outputs (fp32 accumulation);
+ *   q, k, v, dout       : [B, H, T, D] inputs of `dtype` (dout = dL/d out).
+ *   dq, dk, dv          : [B, H, T, D] outputs of `dtype` (fp32 accumulation);
  *                         they must not alias the inputs or each other.
- *   B, H, T, D, beta, p : as for tra_forward.
- *   dtype               : BSA_BF16 (BSA_F32 returns BSA_ERR_UNSUPPORTED).
+ *   D                   : 64 or 128.
+ *   B, H, T, beta, p    : as for tra_forward.  For 0 < p < 1 the derivative
+ *                         p x^(p-1) grows without bound as x -> 0+, so a
+ *                         score within rounding of tau(i) makes dq and dk
+ *                         ill-conditioned (any two correct evaluations may
+ *                         differ there).
+ *   dtype               : BSA_BF16 or BSA_F32.
  *
- * Errors: as for tra_forward.
+ * Errors: as for tra_forward (BSA_ERR_UNSUPPORTED for D other than 64, 128).
  */
 BSA_API int tra_backward(const void* q, const void* k, const void* v,
                          const void* dout, void* dq, void* dk, void* dv,
@@ -204,19 +212,22 @@ BSA_API int tra_backward(const void* q, const void* k, const void* v,
  * runs both score streams on the same query tile and shares each V tile;
  * each stream accumulates its P.V product in fp32 and the two are combined
  * (first minus clamp(lambda, 0, 1) times second) before the bf16 store.
- * With normalize, a
- * pre-pass kernel first computes 1/max(||row||, 1e-12) of every row of q1,
+ * With normalize (bf16), a pre-pass kernel first computes 1/max(||row||, 1e-12) of every row of q1,
  * k1, q2, k2 into a temporary of 16 * B * H * Tp bytes (Tp = T rounded up to
  * a multiple of 128) taken with cudaMallocFromPoolAsync on `stream` and
  * returned with cudaFreeAsync on `stream`, from a memory pool the library
  * creates on the device at first use (it keeps up to 1 GiB of freed
  * temporaries mapped; the caller's default pool is not touched); without
- * normalize nothing is allocated.
+ * normalize nothing is allocated.  BSA_F32 runs one CUDA-core kernel that
+ * folds the two row norms into each score (q.k times both reciprocals) and
+ * allocates nothing in either mode.
  *
- *   q1, q2, k1, k2, v, out : [B, H, T, D] bf16 (out may not alias inputs).
- *   B, H, T, D, beta, p    : as for tra_forward.
+ *   q1, q2, k1, k2, v, out : [B, H, T, D] of `dtype` (out may not alias
+ *                            inputs).
+ *   D                      : 64 or 128.
+ *   B, H, T, beta, p       : as for tra_forward.
  *   lambda                 : any non-NaN value; clamped to [0, 1].
- *   dtype                  : BSA_BF16 (BSA_F32 returns BSA_ERR_UNSUPPORTED).
+ *   dtype                  : BSA_BF16 or BSA_F32.
  *
  * Errors: as for tra_forward, plus BSA_ERR_MEMORY if the temporary cannot be
  * allocated or released.

@@ -69,7 +69,8 @@ def test_tra_argument_errors(lib):
     assert tra(lib, T=0) == 2
     assert tra(lib, T=-5) == 2
     assert tra(lib, D=96) == 4
-    assert tra(lib, D=32) == 4
+    assert tra(lib, D=48) == 4
+    assert tra(lib, D=256) == 4
     assert tra(lib, p=0.0) == 4
     assert tra(lib, p=-1.0) == 4
     assert tra(lib, p=float("nan")) == 4
@@ -185,7 +186,7 @@ def test_tra_forward_host_workspace_and_argument_errors(lib):
     # three stages of q, k, v, out for one chunk of ceil(B*H / 8) heads
     assert bsa.tra_forward_host_workspace_size(4, 16, 4096, 128, 1) == 3 * 4 * 8 * 4096 * 128 * 2
     assert bsa.tra_forward_host_workspace_size(1, 3, 100, 64, 0) == 3 * 4 * ((1 * 100 * 64 * 4 + 255) // 256 * 256)
-    assert bsa.tra_forward_host_workspace_size(1, 1, 16, 32, 1) == 0     # D
+    assert bsa.tra_forward_host_workspace_size(1, 1, 16, 48, 1) == 0     # D
     assert bsa.tra_forward_host_workspace_size(1, 1, 16, 64, 7) == 0     # dtype
     assert bsa.tra_forward_host_workspace_size(0, 1, 16, 64, 1) == 0     # B
     ws, need = 1 << 20, bsa.tra_forward_host_workspace_size(1, 1, 16, 64, 1)

@@ -79,6 +79,12 @@ TRA_SMALL = [
     (1, 1, 256, 64, 2.0, 64.0, "bf16"),   # the largest power of that path (weights stay finite)
     (1, 1, 256, 64, 2.0, 70.0, "bf16"),   # above it: MUFU log2 for every score
     (1, 2, 384, 128, -1.0, 2.7, "bf16"),  # beta < 0 reading
+    # head dims 16 and 32 (the pair kernel at tile width 64, zero-filled columns)
+    (1, 2, 300, 32, 1.0, 2.0, "bf16"),
+    (2, 1, 257, 16, 0.5, 1.5, "bf16"),
+    (1, 3, 200, 32, 0.0, 1.0, "bf16"),
+    (1, 2, 130, 16, 1.0, 2.0, "f32"),
+    (1, 1, 200, 32, 0.5, 1.5, "f32"),
 ]
 
 
@@ -123,7 +129,7 @@ def test_tra_many_short_items_per_cta(B, H, T, D, beta, p):
 # Half-integer powers evaluated as x^k sqrt(x) (tra_forward_ex flag): the same
 # map, so the same oracle and bar; other powers must match tra_forward bit
 # for bit.
-@pytest.mark.parametrize("p,D,T", [(1.5, 64, 333), (0.5, 128, 300), (2.5, 64, 640), (3.5, 128, 257)])
+@pytest.mark.parametrize("p,D,T", [(1.5, 64, 333), (0.5, 128, 300), (2.5, 64, 640), (3.5, 128, 257), (1.5, 32, 200)])
 def test_tra_sqrt_half_powers(p, D, T):
     q, k, v = workloads.tra_inputs(2, 3, T, D, "bf16", seed=T + D)
     gpu = f64(bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), 1.0, p, sqrt_half_powers=True))
@@ -379,6 +385,7 @@ def test_nsa_full_workload_sampled_rows(name):
     (1, 2, 256, 128, 1.5, "bf16", True),    # 2 chunks, fewer than the 3 stages
     (3, 8, 1000, 128, 1.0, "bf16", False),  # pageable host memory, 8 chunks of 3
     (1, 3, 130, 64, 2.0, "f32", True),      # fp32 path
+    (2, 3, 200, 32, 1.5, "bf16", True),     # head dim 32
 ])
 def test_tra_forward_host_matches_device_path(B, H, T, D, p, dtype, pinned):
     import torch
