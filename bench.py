@@ -525,6 +525,8 @@ def run_ours(args):
         n = max(3, args.steps // 2)
         extra = [
             ("tra_backward", wb.name, lambda: bsa.tra_backward(qb, kb, vb, dob, wb.beta, wb.p), 10 * wb.flops // 4),
+            ("tra_backward(deterministic: two kernels)", wb.name,
+             lambda: bsa.tra_backward(qb, kb, vb, dob, wb.beta, wb.p, deterministic=True), 10 * wb.flops // 4),
             ("tra_diff_forward(normalize=1, lambda=0.5)", wb.name,
              lambda: bsa.tra_diff_forward(qb, q2b, kb, k2b, vb, wb.beta, 0.5, wb.p, normalize=True), 2 * wb.flops),
         ]
@@ -715,7 +717,7 @@ def run_op(args):
     if args.op == "backward":
         fn = lambda: bsa.tra_backward(q, k, v, extra[0], w.beta, w.p)  # noqa: E731
         flops = 10 * w.flops // 4
-        launches = 1  # dK/dV and dQ blocks in one grid
+        launches = 3  # dq accumulator zeroing, the fused kernel, dq conversion
     else:
         fn = lambda: bsa.tra_diff_forward(q, extra[0], k, extra[1], v, w.beta, 0.5, w.p, normalize=True)  # noqa: E731
         flops = 2 * w.flops

@@ -18,6 +18,7 @@ _LIB = None
 BSA_F32 = 0
 BSA_BF16 = 1
 BSA_TRA_SQRT_HALF_POWERS = 1  # tra_forward_ex flag: p = k + 1/2 as x^k sqrt(x)
+BSA_TRA_BWD_DETERMINISTIC = 1  # tra_backward_ex flag: the two-kernel bf16 backward (no scratch, bit-repeatable)
 
 _STATUS = {
     0: "BSA_OK",
@@ -85,6 +86,8 @@ def open_library(path):
     lib.nsa_select_forward.restype = i32
     lib.tra_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, vp]
     lib.tra_backward.restype = i32
+    lib.tra_backward_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, i32, i32, vp]
+    lib.tra_backward_ex.restype = i32
     lib.tra_diff_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, f32, i32, i32, vp]
     lib.tra_diff_forward.restype = i32
     lib.tra_diff_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, f32, i32, i32,
@@ -151,6 +154,12 @@ def tra_backward_raw(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, dtype, stre
     """Direct C call with integer device pointers; returns the bsa_status."""
     return load_library().tra_backward(q, k, v, dout, dq, dk, dv, B, H, T, D, float(beta), float(p), int(dtype),
                                        stream)
+
+
+def tra_backward_ex_raw(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, dtype, flags, stream=0) -> int:
+    """Direct C call of tra_backward_ex with integer device pointers; returns the bsa_status."""
+    return load_library().tra_backward_ex(q, k, v, dout, dq, dk, dv, B, H, T, D, float(beta), float(p), int(dtype),
+                                          int(flags), stream)
 
 
 def tra_diff_forward_raw(q1, q2, k1, k2, v, out, B, H, T, D, beta, lam, p, normalize, dtype, stream=0) -> int:
@@ -273,11 +282,13 @@ def tra_forward_host(q, k, v, beta: float, p: float = 2.0, out=None, workspace=N
     return out
 
 
-def tra_backward(q, k, v, dout, beta: float, p: float = 2.0, stream=None):
+def tra_backward(q, k, v, dout, beta: float, p: float = 2.0, stream=None, deterministic: bool = False):
     """Gradients ``(dq, dk, dv)`` of the threshold rectified attention
-    forward for the upstream gradient ``dout``; bf16 CUDA tensors
+    forward for the upstream gradient ``dout``; bf16 or fp32 CUDA tensors
     ``[B, H, T, D]``.  Scores are recomputed; runs on ``stream`` (default:
-    torch's current stream) without synchronising."""
+    torch's current stream) without synchronising.  bf16 runs the fused
+    kernel (dq summed in fp32 in a run-dependent order) unless
+    ``deterministic`` asks for the two-kernel form."""
     import torch
 
     if q.device.type != "cuda":
@@ -289,8 +300,9 @@ def tra_backward(q, k, v, dout, beta: float, p: float = 2.0, stream=None):
     q, k, v, dout = q.contiguous(), k.contiguous(), v.contiguous(), dout.contiguous()
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     B, H, T, D = q.shape
-    st = tra_backward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                          dv.data_ptr(), B, H, T, D, beta, p, _dtype_code(q), _stream_handle(stream))
+    st = tra_backward_ex_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), dq.data_ptr(),
+                             dk.data_ptr(), dv.data_ptr(), B, H, T, D, beta, p, _dtype_code(q),
+                             BSA_TRA_BWD_DETERMINISTIC if deterministic else 0, _stream_handle(stream))
     _check(st, "tra_backward")
     return dq, dk, dv
 

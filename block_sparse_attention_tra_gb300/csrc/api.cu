@@ -128,6 +128,20 @@ int encode_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
   return r == CUDA_SUCCESS ? OK : ERR_SHAPE;
 }
 
+int encode_tmap_3d_f32(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1, uint32_t box2) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return ERR_DEVICE;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {box0, box1, box2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? OK : ERR_SHAPE;
+}
+
 int sm_count() {
   constexpr int MAX_DEVICES = 64;
   static std::atomic<int> counts[MAX_DEVICES] = {};  // 0 = not read yet; callers may race, all store one value
@@ -194,8 +208,8 @@ int tra_forward_host(const void* q, const void* k, const void* v, void* out, int
   return launch_tra_host(q, k, v, out, B, H, T, D, beta, p, dtype == BSA_F32, workspace, stream);
 }
 
-int tra_backward(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv, int B,
-                 int H, int T, int D, float beta, float p, int dtype, cudaStream_t stream) {
+int tra_backward_ex(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv,
+                    int B, int H, int T, int D, float beta, float p, int dtype, int flags, cudaStream_t stream) {
   if (q == nullptr || k == nullptr || v == nullptr || dout == nullptr || dq == nullptr || dk == nullptr ||
       dv == nullptr)
     return BSA_ERR_NULLPTR;
@@ -205,6 +219,7 @@ int tra_backward(const void* q, const void* k, const void* v, const void* dout, 
   if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
   if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
   if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f)) return BSA_ERR_UNSUPPORTED;
+  if ((flags & ~BSA_TRA_BWD_DETERMINISTIC) != 0) return BSA_ERR_UNSUPPORTED;
   const void* ptrs[7] = {q, k, v, dout, dq, dk, dv};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return BSA_ERR_ALIGN;
@@ -214,7 +229,24 @@ int tra_backward(const void* q, const void* k, const void* v, const void* dout, 
     return launch_tra_bwd_f32(static_cast<const float*>(q), static_cast<const float*>(k),
                               static_cast<const float*>(v), static_cast<const float*>(dout), static_cast<float*>(dq),
                               static_cast<float*>(dk), static_cast<float*>(dv), B, H, T, D, beta, p, stream);
-  return launch_tra_bwd_bf16(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, stream);
+  if (flags & BSA_TRA_BWD_DETERMINISTIC)
+    return launch_tra_bwd_bf16(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, stream);
+  // fp32 dq accumulator: a stream-ordered temporary, released on the same stream.
+  float* acc = nullptr;
+  const size_t bytes = static_cast<size_t>(B) * H * T * D * sizeof(float);
+  int dev = 0;
+  cudaMemPool_t pool = cudaGetDevice(&dev) == cudaSuccess ? scratch_pool(dev) : nullptr;
+  if (pool == nullptr) return BSA_ERR_MEMORY;
+  if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&acc), bytes, pool, stream) != cudaSuccess)
+    return BSA_ERR_MEMORY;
+  const int st = launch_tra_bwd_fused_bf16(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, acc, stream);
+  if (cudaFreeAsync(acc, stream) != cudaSuccess && st == OK) return BSA_ERR_MEMORY;
+  return st;
+}
+
+int tra_backward(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv, int B,
+                 int H, int T, int D, float beta, float p, int dtype, cudaStream_t stream) {
+  return tra_backward_ex(q, k, v, dout, dq, dk, dv, B, H, T, D, beta, p, dtype, 0, stream);
 }
 
 // Argument checks of tra_diff_forward and tra_diff_forward_noalloc.

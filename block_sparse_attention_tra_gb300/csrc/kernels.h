@@ -31,6 +31,9 @@ int encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
 // stores of fp32 rows from shared memory.
 int encode_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t stride1_bytes,
                       uint32_t box0, uint32_t box1);
+// Rank-3 fp32 tensor map, 128-byte swizzle (TMA reduce-adds of fp32 boxes).
+int encode_tmap_3d_f32(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1, uint32_t box2);
 
 // Streaming multiprocessors of the current device (cached per device; 0 if
 // the query fails).  Persistent kernels size their grids with it, the
@@ -49,6 +52,15 @@ int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int 
 // Threshold rectified attention backward (dq, dk, dv), bf16 tcgen05 kernels.
 int launch_tra_bwd_bf16(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dv,
                         int B, int H, int T, int D, float beta, float p, cudaStream_t stream);
+
+// The same backward as one fused kernel: the scores and dP of each (key tile,
+// query tile) pair are computed once, dk and dv accumulate in tensor memory
+// and each pair's dq partial is added into dq_acc (fp32, B*H*T*D elements,
+// 16-byte aligned), which this call zeroes first and converts into dq last.
+// The order of those fp32 additions varies from run to run.
+int launch_tra_bwd_fused_bf16(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
+                              void* dv, int B, int H, int T, int D, float beta, float p, float* dq_acc,
+                              cudaStream_t stream);
 
 // fp32 forms of the backward and of the differential forward (CUDA-core FFMA
 // kernels, tra_f32_ext.cu); the differential one needs no scratch memory.

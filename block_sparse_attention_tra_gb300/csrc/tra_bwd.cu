@@ -39,6 +39,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc_tile.cuh"
+#include "tra_bwd_common.cuh"
 
 namespace bsa {
 namespace {
@@ -73,33 +74,7 @@ struct BwdCfg {
 };
 constexpr uint32_t TMEM_COLS = 512;
 
-__device__ __forceinline__ float ex2a(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float lg2a(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// ReLU(x)^p and its derivative (0 for x <= 0).
-template <int PC>
-__device__ __forceinline__ void weight_and_grad(float x, float p, float& w, float& g) {
-  const float r = fmaxf(x, 0.0f);
-  if constexpr (PC == POW_ONE) {
-    w = r;
-    g = x > 0.0f ? 1.0f : 0.0f;
-  } else if constexpr (PC == POW_TWO) {
-    w = r * r;
-    g = 2.0f * r;
-  } else {
-    const float l = lg2a(r);  // -inf for r = 0
-    w = ex2a(p * l);
-    g = x > 0.0f ? p * ex2a((p - 1.0f) * l) : 0.0f;
-  }
-}
+using bwd::weight_and_grad;
 
 template <int D>
 struct BwdLayout {

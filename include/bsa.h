@@ -177,9 +177,19 @@ BSA_API int tra_forward_host(const void* q, const void* k, const void* v,
  *   dq_i  = sum_j dA_ij k_j                 dk_j = sum_i dA_ij q_i
  *
  * beta and p receive no gradient (as on the page).  Scores are recomputed
- * (nothing is saved by tra_forward).  bf16: one launch on `stream` whose
- * blocks compute dk and dv per key tile, then dq per query tile.  fp32: two
- * launches (CUDA-core kernels, fp32 throughout, as the page computes).
+ * (nothing is saved by tra_forward).
+ *
+ * bf16: one fused kernel computes the scores and dout . v of every (key tile,
+ * query tile) pair once; dk and dv accumulate on chip, and each pair's dq
+ * partial is added (fp32) into a temporary of 4 * B * H * T * D bytes, taken
+ * with cudaMallocFromPoolAsync on `stream` from the library's memory pool
+ * (as tra_diff_forward's) and returned with cudaFreeAsync on `stream`; a
+ * zeroing kernel before and a conversion kernel after it run on `stream` too.  The
+ * order of the fp32 dq additions varies between runs, so dq may differ in
+ * its last bf16 bit from one run to the next; dk and dv do not.  For results
+ * that repeat bit for bit use tra_backward_ex with
+ * BSA_TRA_BWD_DETERMINISTIC.  fp32: two launches (CUDA-core kernels, fp32
+ * throughout, as the page computes; deterministic).
  *
  *   q, k, v, dout       : [B, H, T, D] inputs of `dtype` (dout = dL/d out).
  *   dq, dk, dv          : [B, H, T, D] outputs of `dtype` (fp32 accumulation);
@@ -192,12 +202,36 @@ BSA_API int tra_forward_host(const void* q, const void* k, const void* v,
  *                         differ there).
  *   dtype               : BSA_BF16 or BSA_F32.
  *
- * Errors: as for tra_forward (BSA_ERR_UNSUPPORTED for D other than 64, 128).
+ * Errors: as for tra_forward (BSA_ERR_UNSUPPORTED for D other than 64, 128),
+ * plus BSA_ERR_MEMORY if the bf16 temporary cannot be allocated or released.
  */
 BSA_API int tra_backward(const void* q, const void* k, const void* v,
                          const void* dout, void* dq, void* dk, void* dv,
                          int B, int H, int T, int D, float beta, float p,
                          int dtype, cudaStream_t stream);
+
+/* Flags of tra_backward_ex. */
+typedef enum {
+  /* bf16: the two-kernel form (one block per key tile for dk and dv, one per
+     query tile for dq, each producing the scores itself).  It allocates
+     nothing and repeats bit for bit; it does 14 D instead of 10 D tensor
+     FLOPs per causal pair. */
+  BSA_TRA_BWD_DETERMINISTIC = 1
+} bsa_tra_bwd_flags;
+
+/*
+ * tra_backward_ex -- tra_backward with evaluation flags.
+ *
+ * Same method, arguments, layout, rules and errors as tra_backward, plus
+ * `flags`, a bitwise OR of bsa_tra_bwd_flags (0 = exactly tra_backward;
+ * unknown bits return BSA_ERR_UNSUPPORTED).  BSA_TRA_BWD_DETERMINISTIC
+ * allocates nothing, so it never returns BSA_ERR_MEMORY.  fp32 ignores the
+ * flag (its kernels are deterministic and allocate nothing).
+ */
+BSA_API int tra_backward_ex(const void* q, const void* k, const void* v,
+                            const void* dout, void* dq, void* dk, void* dv,
+                            int B, int H, int T, int D, float beta, float p,
+                            int dtype, int flags, cudaStream_t stream);
 
 /*
  * tra_diff_forward -- threshold differential attention forward.
