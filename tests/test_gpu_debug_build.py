@@ -72,7 +72,12 @@ def test_tra_backward_and_diff_debug_build(debug_lib, T, D, p):
     q, k, v = (t.cuda() for t in workloads.tra_inputs(1, 2, T, D, "bf16", seed=T + 1))
     q2, k2, _ = (t.cuda() for t in workloads.tra_inputs(1, 2, T, D, "bf16", seed=T + 2))
     do = torch.randn(q.shape, generator=torch.Generator().manual_seed(T)).to(torch.bfloat16).cuda()
-    same(*both(debug_lib, lambda: bsa.tra_backward(q, k, v, do, 1.0, p)))
+    same(*both(debug_lib, lambda: bsa.tra_backward(q, k, v, do, 1.0, p, deterministic=True)))
+    # the fused kernel adds dq's fp32 partials in a run-dependent order: dk, dv bit for bit, dq within the bar
+    a, b = both(debug_lib, lambda: bsa.tra_backward(q, k, v, do, 1.0, p))
+    same(a[1:], b[1:])
+    ref = a[0].double()
+    assert float((b[0].double() - ref).abs().max()) <= 2e-2 * max(float(ref.abs().max()), 1e-30)
     same(*both(debug_lib, lambda: bsa.tra_diff_forward(q, q2, k, k2, v, 0.1, 0.5, p, normalize=True)))
 
 
