@@ -78,7 +78,9 @@ __device__ __forceinline__ void store_row_part(uint32_t tC, int c, __nv_bfloat16
   tmem_wait_ld();
   if (in_range) {
     uint4* dst = reinterpret_cast<uint4*>(row + c * 32);
-    for (int q = 0; q < ncols / 8; ++q) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // (static register indices; ncols / 8 of the four are stored)
+      if (q >= ncols / 8) break;
       uint4 u;
       u.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
       u.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));

@@ -67,6 +67,29 @@ __device__ __forceinline__ void epilogue_quarter(const uint32_t (&s)[32], uint32
   tmem_st16(tS + c0 / 2, pk);
 }
 
+// Half of a quarter: 16 scores of this thread's row, keys key0 + c0 ..
+// key0 + c0 + 15 (c0 a multiple of 16), into 8 packed P columns at tS +
+// c0 / 2.  Pair e of the half is pair e0 + e of its quarter (for the choice
+// of log2 unit).
+template <int PC, bool DIAG, int MUFU_PAIRS>
+__device__ __forceinline__ void epilogue_eighth(const uint32_t (&s)[16], uint32_t tS, int c0, int e0,
+                                                const PowParams& wp, int key0, int row) {
+  uint32_t pk[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    uint32_t w = (PC == POW_GENERAL_MIX && mix_pair_on_fma<MUFU_PAIRS>(e0 + e))
+                     ? weights2<PC, true>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp)
+                     : weights2<PC, false>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp);
+    if constexpr (DIAG) {
+      const int key = key0 + c0 + 2 * e;
+      if (key > row) w = 0u;
+      else if (key + 1 > row) w &= 0x0000ffffu;
+    }
+    pk[e] = w;
+  }
+  tmem_st8(tS + c0 / 2, pk);
+}
+
 // One 128-key score tile of this thread's row -> P, in four software-
 // pipelined quarters; arrives on p_half after keys 0..63 and on p_full after
 // all 128 (one arrival per warp).
@@ -104,25 +127,65 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tS, const PowParams& wp, 
 // the other warp: both warps load their first quarter before either stores
 // (named barrier `bar_id`, 64 threads).  Quarters 0 and 1 make up P's first
 // half (p_half: one arrival per warp), all four the whole of it (p_full).
-template <int PC, bool DIAG, int MP>
+//
+//
+// Half loads: each quarter is loaded in two 16-column halves, and the next
+// half's load is issued before the current half is turned into P, so its
+// latency overlaps that work (same 32 registers of scores).  Measured at
+// T=8192 D=64 p=1.5: 0.739 -> 0.715 ms; at D=128 p=1.5 1% slower, so
+// BSA_PAIR_HALF_LOADS = 1 (default) uses them at D = 64 only (0: never,
+// 2: always).
+#ifndef BSA_PAIR_HALF_LOADS
+#define BSA_PAIR_HALF_LOADS 1
+#endif
+template <int D>
+constexpr bool pair_half_loads() {
+  return BSA_PAIR_HALF_LOADS == 2 || (BSA_PAIR_HALF_LOADS == 1 && D == 64);
+}
+template <int PC, bool DIAG, int MP, bool HALF_LOADS>
 __device__ __forceinline__ void epilogue_two_quarters(uint32_t tS, const PowParams& wp, int key0, int row, int lane,
                                                       int half, int bar_id, uint64_t* p_half, uint64_t* p_full) {
-  uint32_t a[32];
-  tmem_ld32(tS + 32 * half, a);
-  tmem_wait_ld();
-  asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
-  epilogue_quarter<PC, DIAG, MP>(a, tS, 32 * half, wp, key0, row);
-  tmem_wait_st();
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(p_half);
-  tmem_ld32(tS + 32 * (half + 2), a);
-  tmem_wait_ld();
-  epilogue_quarter<PC, DIAG, MP>(a, tS, 32 * (half + 2), wp, key0, row);
-  tmem_wait_st();
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(p_full);
+  if constexpr (HALF_LOADS) {
+    const int c1 = 32 * half, c2 = 32 * (half + 2);  // this warp's quarters
+    uint32_t a[16], b[16];
+    tmem_ld16(tS + c1, a);
+    tmem_ld16(tS + c1 + 16, b);
+    tmem_wait_ld();
+    asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+    epilogue_eighth<PC, DIAG, MP>(a, tS, c1, 0, wp, key0, row);
+    tmem_ld16(tS + c2, a);  // P above went to columns c1 / 2 .., never c2 ..
+    epilogue_eighth<PC, DIAG, MP>(b, tS, c1 + 16, 8, wp, key0, row);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(p_half);
+    tmem_wait_ld();
+    tmem_ld16(tS + c2 + 16, b);
+    epilogue_eighth<PC, DIAG, MP>(a, tS, c2, 0, wp, key0, row);
+    tmem_wait_ld();
+    epilogue_eighth<PC, DIAG, MP>(b, tS, c2 + 16, 8, wp, key0, row);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(p_full);
+  } else {
+    uint32_t a[32];
+    tmem_ld32(tS + 32 * half, a);
+    tmem_wait_ld();
+    asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+    epilogue_quarter<PC, DIAG, MP>(a, tS, 32 * half, wp, key0, row);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(p_half);
+    tmem_ld32(tS + 32 * (half + 2), a);
+    tmem_wait_ld();
+    epilogue_quarter<PC, DIAG, MP>(a, tS, 32 * (half + 2), wp, key0, row);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(p_full);
+  }
 }
 
 // ============================================================ pair kernel (p = 1, 2)
@@ -519,10 +582,13 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
         constexpr int MP = mix_mufu_pairs<D>();
         if constexpr (Cfg::EPI_WG == 2) {
           const int bar_id = 1 + qt * 4 + wq;  // the two warps sharing this lane quarter
+          constexpr bool HL = pair_half_loads<D>();
           if (n == nmax)
-            epilogue_two_quarters<PC, true, MP>(tS, wp, n * BN, row, lane, half, bar_id, &p_half[qt], &p_full[qt]);
+            epilogue_two_quarters<PC, true, MP, HL>(tS, wp, n * BN, row, lane, half, bar_id, &p_half[qt],
+                                                    &p_full[qt]);
           else
-            epilogue_two_quarters<PC, false, MP>(tS, wp, n * BN, row, lane, half, bar_id, &p_half[qt], &p_full[qt]);
+            epilogue_two_quarters<PC, false, MP, HL>(tS, wp, n * BN, row, lane, half, bar_id, &p_half[qt],
+                                                     &p_full[qt]);
         } else {
           if (n == nmax)
             epilogue_tile<PC, PAIR_SPLIT_P, true, MP>(tS, wp, n * BN, row, lane, &p_half[qt], &p_full[qt]);
