@@ -217,7 +217,7 @@ int tra_backward_ex(const void* q, const void* k, const void* v, const void* dou
   if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
-  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
   if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f)) return BSA_ERR_UNSUPPORTED;
   if ((flags & ~BSA_TRA_BWD_DETERMINISTIC) != 0) return BSA_ERR_UNSUPPORTED;
   const void* ptrs[7] = {q, k, v, dout, dq, dk, dv};
@@ -259,7 +259,7 @@ static int check_diff_args(const void* q1, const void* q2, const void* k1, const
   if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
-  if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
   if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f) || isnan(lambda)) return BSA_ERR_UNSUPPORTED;
   const void* ptrs[6] = {q1, q2, k1, k2, v, out};
   for (const void* ptr : ptrs)

@@ -217,8 +217,9 @@ template <int D, int PC>
 __device__ __forceinline__ void bwd_dkdv_block(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                                const CUtensorMap& tmDO, __nv_bfloat16* __restrict__ dk,
                                                __nv_bfloat16* __restrict__ dv, int BH, int T, int nT, int G,
-                                               float beta, float p, int blk) {
+                                               float beta, float p, int blk, int d_real) {
   using L = BwdLayout<D>;
+  const int dr = D == 128 ? D : d_real;  // head dims 16, 32 run at width 64 on zero-filled columns
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const BwdBars B = bwd_bars<D>(smem);
@@ -299,7 +300,7 @@ __device__ __forceinline__ void bwd_dkdv_block(const CUtensorMap& tmQ, const CUt
       // after every warp arrived for step j-1 (so all have finished step j-2,
       // the buffer's previous user); the barrier wait is bounded.
       float* tau_m = tau_s + (j & 1) * BT;
-      tau_m[r] = tile::tau_of_row(m * BT + r, beta, D);  // tau of query column r
+      tau_m[r] = tile::tau_of_row(m * BT + r, beta, dr);  // tau of query column r
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.tau_full[j & 1]);
       if (!(ok = mbar_wait(&B.tau_full[j & 1], (j >> 1) & 1))) break;
@@ -344,12 +345,17 @@ __device__ __forceinline__ void bwd_dkdv_block(const CUtensorMap& tmQ, const CUt
     }
     if (ok && mbar_wait(B.acc_full, 0)) {
       tc_fence_after();
-      const size_t rowoff = (static_cast<size_t>(bh) * T + key) * D;
+      const size_t rowoff = (static_cast<size_t>(bh) * T + key) * dr;
       constexpr int CPW = D / 32 / EPI_WG;  // 32-column chunks of dK, dV this warp stores
 #pragma unroll
       for (int c = grp * CPW; c < (grp + 1) * CPW; ++c) {
-        tile::store_row_chunk(lane_base + DV, c, dv + rowoff, key < T);
-        tile::store_row_chunk(lane_base + DK, c, dk + rowoff, key < T);
+        if (dr == D) {
+          tile::store_row_chunk(lane_base + DV, c, dv + rowoff, key < T);
+          tile::store_row_chunk(lane_base + DK, c, dk + rowoff, key < T);
+        } else if (c * 32 < dr) {
+          tile::store_row_part(lane_base + DV, c, dv + rowoff, key < T, min(32, dr - c * 32));
+          tile::store_row_part(lane_base + DK, c, dk + rowoff, key < T, min(32, dr - c * 32));
+        }
       }
     }
   }
@@ -362,8 +368,9 @@ __device__ __forceinline__ void bwd_dkdv_block(const CUtensorMap& tmQ, const CUt
 template <int D, int PC>
 __device__ __forceinline__ void bwd_dq_block(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                              const CUtensorMap& tmDO, __nv_bfloat16* __restrict__ dq, int BH, int T,
-                                             int nT, int G, float beta, float p, int blk) {
+                                             int nT, int G, float beta, float p, int blk, int d_real) {
   using L = BwdLayout<D>;
+  const int dr = D == 128 ? D : d_real;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const BwdBars B = bwd_bars<D>(smem);
@@ -431,7 +438,7 @@ __device__ __forceinline__ void bwd_dq_block(const CUtensorMap& tmQ, const CUten
     const int wq = warp & 3, grp = warp >> 2;  // TMEM lane quarter; chunk of each half (two warpgroups)
     const int r = wq * 32 + lane;
     const int row = m * BT + r;
-    const float tau = tile::tau_of_row(row, beta, D);
+    const float tau = tile::tau_of_row(row, beta, dr);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     bool ok = true;
     for (int n = 0; n <= m && ok; ++n) {
@@ -471,10 +478,15 @@ __device__ __forceinline__ void bwd_dq_block(const CUtensorMap& tmQ, const CUten
     }
     if (ok && mbar_wait(B.acc_full, 0)) {
       tc_fence_after();
-      __nv_bfloat16* dst = dq + (static_cast<size_t>(bh) * T + row) * D;
+      __nv_bfloat16* dst = dq + (static_cast<size_t>(bh) * T + row) * dr;
       constexpr int CPW = D / 32 / EPI_WG;  // 32-column chunks of dQ this warp stores
 #pragma unroll
-      for (int c = grp * CPW; c < (grp + 1) * CPW; ++c) tile::store_row_chunk(lane_base + DQ, c, dst, row < T);
+      for (int c = grp * CPW; c < (grp + 1) * CPW; ++c) {
+        if (dr == D)
+          tile::store_row_chunk(lane_base + DQ, c, dst, row < T);
+        else if (c * 32 < dr)
+          tile::store_row_part(lane_base + DQ, c, dst, row < T, min(32, dr - c * 32));
+      }
     }
   }
   bwd_teardown(tmem, warp, MMA_WARP);
@@ -485,16 +497,17 @@ __global__ void __launch_bounds__(BwdCfg<D, PC, false>::THREADS, 1)
     tra_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                         __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int BH, int T, int nT,
-                        int G, float beta, float p) {
-  bwd_dkdv_block<D, PC>(tmQ, tmK, tmV, tmDO, dk, dv, BH, T, nT, G, beta, p, static_cast<int>(blockIdx.x));
+                        int G, float beta, float p, int d_real) {
+  bwd_dkdv_block<D, PC>(tmQ, tmK, tmV, tmDO, dk, dv, BH, T, nT, G, beta, p, static_cast<int>(blockIdx.x), d_real);
 }
 
 template <int D, int PC>
 __global__ void __launch_bounds__(BwdCfg<D, PC, true>::THREADS, 1)
     tra_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                      __nv_bfloat16* __restrict__ dq, int BH, int T, int nT, int G, float beta, float p) {
-  bwd_dq_block<D, PC>(tmQ, tmK, tmV, tmDO, dq, BH, T, nT, G, beta, p, static_cast<int>(blockIdx.x));
+                      __nv_bfloat16* __restrict__ dq, int BH, int T, int nT, int G, float beta, float p,
+                      int d_real) {
+  bwd_dq_block<D, PC>(tmQ, tmK, tmV, tmDO, dq, BH, T, nT, G, beta, p, static_cast<int>(blockIdx.x), d_real);
 }
 
 // Both kinds of block in one grid: the dK/dV blocks first, then the dQ
@@ -505,12 +518,13 @@ __global__ void __launch_bounds__(BwdCfg<D, PC, false>::THREADS, 1)
     tra_bwd_both_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                         __nv_bfloat16* __restrict__ dq, __nv_bfloat16* __restrict__ dk,
-                        __nv_bfloat16* __restrict__ dv, int BH, int T, int nT, int G, float beta, float p) {
+                        __nv_bfloat16* __restrict__ dv, int BH, int T, int nT, int G, float beta, float p,
+                        int d_real) {
   const int nk = nT * BH, b = static_cast<int>(blockIdx.x);
   if (b < nk)
-    bwd_dkdv_block<D, PC>(tmQ, tmK, tmV, tmDO, dk, dv, BH, T, nT, G, beta, p, b);
+    bwd_dkdv_block<D, PC>(tmQ, tmK, tmV, tmDO, dk, dv, BH, T, nT, G, beta, p, b, d_real);
   else
-    bwd_dq_block<D, PC>(tmQ, tmK, tmV, tmDO, dq, BH, T, nT, G, beta, p, b - nk);
+    bwd_dq_block<D, PC>(tmQ, tmK, tmV, tmDO, dq, BH, T, nT, G, beta, p, b - nk, d_real);
 }
 
 #ifndef BSA_BWD_ONE_GRID
@@ -519,13 +533,13 @@ __global__ void __launch_bounds__(BwdCfg<D, PC, false>::THREADS, 1)
 
 template <int D, int PC>
 int launch_bwd(const CUtensorMap* maps, void* dq, void* dk, void* dv, int BH, int T, float beta, float p,
-               cudaStream_t stream) {
+               int d_real, cudaStream_t stream) {
   using L = BwdLayout<D>;
   const int nT = (T + BT - 1) / BT;
   const long long grid = static_cast<long long>(nT) * BH;
   if (2 * grid > 0x7fffffffLL) return ERR_SHAPE;
   // two streamed bf16 tensors of T x D per head; one resident CTA per SM
-  const int G = tile::head_groups(BH, nT, 4LL * T * D, sm_count());
+  const int G = tile::head_groups(BH, nT, 4LL * T * d_real, sm_count());
   constexpr bool ONE_GRID = BSA_BWD_ONE_GRID && BwdCfg<D, PC, false>::THREADS == BwdCfg<D, PC, true>::THREADS;
   if constexpr (ONE_GRID) {
     auto k = tra_bwd_both_kernel<D, PC>;
@@ -533,7 +547,7 @@ int launch_bwd(const CUtensorMap* maps, void* dq, void* dk, void* dv, int BH, in
       return ERR_LAUNCH;
     k<<<static_cast<unsigned>(2 * grid), BwdCfg<D, PC, false>::THREADS, L::ALLOC, stream>>>(
         maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
-        static_cast<__nv_bfloat16*>(dv), BH, T, nT, G, beta, p);
+        static_cast<__nv_bfloat16*>(dv), BH, T, nT, G, beta, p, d_real);
     return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
   } else {
     auto k1 = tra_bwd_dkdv_kernel<D, PC>;
@@ -543,10 +557,10 @@ int launch_bwd(const CUtensorMap* maps, void* dq, void* dk, void* dv, int BH, in
       return ERR_LAUNCH;
     k1<<<static_cast<unsigned>(grid), BwdCfg<D, PC, false>::THREADS, L::ALLOC, stream>>>(
         maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), BH, T,
-        nT, G, beta, p);
+        nT, G, beta, p, d_real);
     if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
     k2<<<static_cast<unsigned>(grid), BwdCfg<D, PC, true>::THREADS, L::ALLOC, stream>>>(
-        maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dq), BH, T, nT, G, beta, p);
+        maps[0], maps[1], maps[2], maps[3], static_cast<__nv_bfloat16*>(dq), BH, T, nT, G, beta, p, d_real);
     return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
   }
 }
@@ -565,14 +579,14 @@ int launch_tra_bwd_bf16(const void* q, const void* k, const void* v, const void*
   }
   const int pc = power_class(p);
   if (D == 128) {
-    if (pc == POW_TWO) return launch_bwd<128, POW_TWO>(maps, dq, dk, dv, BH, T, beta, p, stream);
-    if (pc == POW_ONE) return launch_bwd<128, POW_ONE>(maps, dq, dk, dv, BH, T, beta, p, stream);
-    return launch_bwd<128, POW_GENERAL>(maps, dq, dk, dv, BH, T, beta, p, stream);
+    if (pc == POW_TWO) return launch_bwd<128, POW_TWO>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
+    if (pc == POW_ONE) return launch_bwd<128, POW_ONE>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
+    return launch_bwd<128, POW_GENERAL>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
   }
-  if (D == 64) {
-    if (pc == POW_TWO) return launch_bwd<64, POW_TWO>(maps, dq, dk, dv, BH, T, beta, p, stream);
-    if (pc == POW_ONE) return launch_bwd<64, POW_ONE>(maps, dq, dk, dv, BH, T, beta, p, stream);
-    return launch_bwd<64, POW_GENERAL>(maps, dq, dk, dv, BH, T, beta, p, stream);
+  if (D == 64 || D == 32 || D == 16) {  // 16 and 32 at width 64 on zero-filled columns
+    if (pc == POW_TWO) return launch_bwd<64, POW_TWO>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
+    if (pc == POW_ONE) return launch_bwd<64, POW_ONE>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
+    return launch_bwd<64, POW_GENERAL>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
   }
   return ERR_UNSUPPORTED;
 }

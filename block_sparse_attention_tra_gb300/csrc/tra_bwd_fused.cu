@@ -162,8 +162,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     tra_bwd_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                          const __grid_constant__ CUtensorMap tmDQ, __nv_bfloat16* __restrict__ dk,
-                         __nv_bfloat16* __restrict__ dv, int BH, int T, int nT, int G, float beta, float p) {
+                         __nv_bfloat16* __restrict__ dv, int BH, int T, int nT, int G, float beta, float p,
+                         int d_real) {
   using L = FusedLayout<D>;
+  // Head dims 16 and 32 run at tile width 64 on zero-filled columns (the
+  // tensor maps cover the real d_real columns); width 128 serves 128 alone.
+  const int dr = D == 128 ? D : d_real;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const FusedBars B = fused_bars<D>(smem);
@@ -301,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bar_sync(DRAIN_BAR, 128);
       if (issuer) {
         tma_reduce_add_3d(&tmDQ, sStg, 0, m * BT, bh);
-        tma_reduce_add_3d(&tmDQ, sStg + L::BOX_BYTES, 32, m * BT, bh);
+        if (dr > 32) tma_reduce_add_3d(&tmDQ, sStg + L::BOX_BYTES, 32, m * BT, bh);
         bulk_commit();
         bulk_wait_read<0>();
       }
@@ -334,7 +338,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int m = n + j;
       // Double-buffered tau table (as in the recompute kernels).
       float* tau_m = tau_s + (j & 1) * BT;
-      tau_m[r] = tile::tau_of_row(m * BT + r, beta, D);
+      tau_m[r] = tile::tau_of_row(m * BT + r, beta, dr);
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.tau_full[j & 1]);
       if (!(ok = mbar_wait(&B.tau_full[j & 1], (j >> 1) & 1))) break;
@@ -402,12 +406,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (ok && mbar_wait(B.acc_full, 0)) {
       tc_fence_after();
-      const size_t rowoff = (static_cast<size_t>(bh) * T + key) * D;
+      const size_t rowoff = (static_cast<size_t>(bh) * T + key) * dr;
       constexpr int CPW = D / 32 / 2;  // 32-column chunks of dK, dV this warp stores
 #pragma unroll
       for (int c = h * CPW; c < (h + 1) * CPW; ++c) {
-        tile::store_row_chunk(lane_base + L::TDV, c, dv + rowoff, key < T);
-        tile::store_row_chunk(lane_base + L::TDK, c, dk + rowoff, key < T);
+        if (dr == D) {
+          tile::store_row_chunk(lane_base + L::TDV, c, dv + rowoff, key < T);
+          tile::store_row_chunk(lane_base + L::TDK, c, dk + rowoff, key < T);
+        } else if (c * 32 < dr) {  // head dim below the tile width: only its columns
+          tile::store_row_part(lane_base + L::TDV, c, dv + rowoff, key < T, min(32, dr - c * 32));
+          tile::store_row_part(lane_base + L::TDK, c, dk + rowoff, key < T, min(32, dr - c * 32));
+        }
       }
     }
   }
@@ -441,29 +450,30 @@ __global__ void __launch_bounds__(256) tra_bwd_dq_convert_kernel(const float* __
 
 template <int D, int PC>
 int launch_fused(const CUtensorMap* maps, const CUtensorMap& mdq, void* dk, void* dv, int BH, int T, float beta,
-                 float p, cudaStream_t stream) {
+                 float p, int d_real, cudaStream_t stream) {
   using L = FusedLayout<D>;
   const int nT = (T + BT - 1) / BT;
   const long long grid = static_cast<long long>(nT) * BH;
   if (grid > 0x7fffffffLL) return ERR_SHAPE;
   // streamed per head: q and dO (bf16) and the dq accumulator (fp32)
-  const int G = tile::head_groups(BH, nT, 8LL * T * D, sm_count());
+  const int G = tile::head_groups(BH, nT, 8LL * T * d_real, sm_count());
   auto k = tra_bwd_fused_kernel<D, PC>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
     return ERR_LAUNCH;
   k<<<static_cast<unsigned>(grid), THREADS, L::ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], mdq,
                                                                 static_cast<__nv_bfloat16*>(dk),
-                                                                static_cast<__nv_bfloat16*>(dv), BH, T, nT, G, beta, p);
+                                                                static_cast<__nv_bfloat16*>(dv), BH, T, nT, G, beta, p,
+                                                                d_real);
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
 
 template <int D>
 int launch_fused_pc(const CUtensorMap* maps, const CUtensorMap& mdq, void* dk, void* dv, int BH, int T, float beta,
-                    float p, cudaStream_t stream) {
+                    float p, int d_real, cudaStream_t stream) {
   const int pc = power_class(p);
-  if (pc == POW_TWO) return launch_fused<D, POW_TWO>(maps, mdq, dk, dv, BH, T, beta, p, stream);
-  if (pc == POW_ONE) return launch_fused<D, POW_ONE>(maps, mdq, dk, dv, BH, T, beta, p, stream);
-  return launch_fused<D, POW_GENERAL>(maps, mdq, dk, dv, BH, T, beta, p, stream);
+  if (pc == POW_TWO) return launch_fused<D, POW_TWO>(maps, mdq, dk, dv, BH, T, beta, p, d_real, stream);
+  if (pc == POW_ONE) return launch_fused<D, POW_ONE>(maps, mdq, dk, dv, BH, T, beta, p, d_real, stream);
+  return launch_fused<D, POW_GENERAL>(maps, mdq, dk, dv, BH, T, beta, p, d_real, stream);
 }
 
 }  // namespace
@@ -471,7 +481,7 @@ int launch_fused_pc(const CUtensorMap* maps, const CUtensorMap& mdq, void* dk, v
 int launch_tra_bwd_fused_bf16(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
                               void* dv, int B, int H, int T, int D, float beta, float p, float* dq_acc,
                               cudaStream_t stream) {
-  if (D != 64 && D != 128) return ERR_UNSUPPORTED;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return ERR_UNSUPPORTED;
   const int BH = B * H;
   CUtensorMap maps[4], mdq;
   const uint64_t rs = static_cast<uint64_t>(D) * 2, hs = rs * T;
@@ -483,7 +493,7 @@ int launch_tra_bwd_fused_bf16(const void* q, const void* k, const void* v, const
   const int st = encode_tmap_3d_f32(&mdq, dq_acc, D, T, BH, static_cast<uint64_t>(D) * 4,
                                     static_cast<uint64_t>(D) * 4 * T, 32, BT, 1);
   if (st != OK) return st;
-  const size_t elems = static_cast<size_t>(BH) * T * D;  // a multiple of 64 (D is)
+  const size_t elems = static_cast<size_t>(BH) * T * D;  // a multiple of 16 (D is)
   const size_t n8 = elems / 8;
   const int sms = sm_count();
   size_t blocks = (n8 + 255) / 256;
@@ -492,8 +502,8 @@ int launch_tra_bwd_fused_bf16(const void* q, const void* k, const void* v, const
   tra_bwd_dq_zero_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(reinterpret_cast<uint4*>(dq_acc),
                                                                              elems / 4);
   if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
-  const int rc = D == 128 ? launch_fused_pc<128>(maps, mdq, dk, dv, BH, T, beta, p, stream)
-                          : launch_fused_pc<64>(maps, mdq, dk, dv, BH, T, beta, p, stream);
+  const int rc = D == 128 ? launch_fused_pc<128>(maps, mdq, dk, dv, BH, T, beta, p, D, stream)
+                          : launch_fused_pc<64>(maps, mdq, dk, dv, BH, T, beta, p, D, stream);
   if (rc != OK) return rc;
   tra_bwd_dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
       dq_acc, static_cast<__nv_bfloat16*>(dq), n8);

@@ -119,7 +119,9 @@ __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* 
                                                            const __nv_bfloat16* __restrict__ a2,
                                                            const __nv_bfloat16* __restrict__ a3,
                                                            float* __restrict__ inv, int BH, int T, int Tp) {
-  constexpr int CH = D / 64;  // 16-byte chunks per lane per row
+  // Row of D bf16 = D / 8 chunks of 16 bytes over the eight lanes of a row:
+  // lane `sub` takes chunks sub + 8c (none past the row for D = 16, 32).
+  constexpr int CH = (D + 63) / 64;
   constexpr int NG = NORM_NG;
   const int lane = threadIdx.x & 31, sub = lane & 7;
   const long long rows_p = static_cast<long long>(BH) * Tp;
@@ -145,7 +147,8 @@ __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* 
           const __nv_bfloat16* src = which == 0 ? a0 : which == 1 ? a1 : which == 2 ? a2 : a3;
           const uint4* x = reinterpret_cast<const uint4*>(src + (bh * T + t) * D);
 #pragma unroll
-          for (int c = 0; c < CH; ++c) u[g][c] = x[sub + 8 * c];
+          for (int c = 0; c < CH; ++c)
+            if (sub + 8 * c < D / 8) u[g][c] = x[sub + 8 * c];
         }
       }
     }
@@ -193,8 +196,10 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
     tra_diff_kernel(const __grid_constant__ CUtensorMap tmQ0, const __grid_constant__ CUtensorMap tmQ1,
                     const __grid_constant__ CUtensorMap tmK0, const __grid_constant__ CUtensorMap tmK1,
                     const __grid_constant__ CUtensorMap tmV, const float* __restrict__ inv_norm,
-                    __nv_bfloat16* __restrict__ out, int BH, int T, int nQ, int G, float beta, float p, float lam) {
+                    __nv_bfloat16* __restrict__ out, int BH, int T, int nQ, int G, float beta, float p, float lam,
+                    int d_real) {
   const int Tp = nQ * BT;  // row stride of the normalisation buffer
+  const int dr = D == 128 ? D : d_real;  // head dims 16, 32 run at width 64 on zero-filled columns
   using L = DiffLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
   } else {
     const int t = warp >> 2, wq = warp & 3;
     const int row = m * BT + wq * 32 + lane;
-    const float tau = tile::tau_of_row(row, beta, D);
+    const float tau = tile::tau_of_row(row, beta, dr);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t tS = lane_base + t * BT;
     const PowParams wp = pow_params(tau, p);
@@ -401,17 +406,19 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
     }
     if (ok && mbar_wait(&o_full[0], 0) && mbar_wait(&o_full[1], 0)) {
       tc_fence_after();
-      __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * T + row) * D;
+      __nv_bfloat16* orow = out + (static_cast<size_t>(bh) * T + row) * dr;
       // out = O0 - clamp(lambda, 0, 1) O1; stream t's warpgroup writes every other 32-column chunk.
-      for (int c = t; c < D / 32; c += 2) {
+      for (int c = t; c < D / 32 && c * 32 < dr; c += 2) {
         uint32_t o0[32], o1[32];
         tmem_ld32(lane_base + O_COL + c * 32, o0);
         tmem_ld32(lane_base + O_COL + D + c * 32, o1);
         tmem_wait_ld();
         if (row < T) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          const int nq = min(32, dr - c * 32) / 8;  // 16-byte stores of this chunk's real columns
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
+            if (q >= nq) break;
             float f[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = fmaf(-lc, __uint_as_float(o1[8 * q + e]), __uint_as_float(o0[8 * q + e]));
@@ -434,7 +441,7 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
 
 template <int D, int PC, bool NORM>
 int launch_diff_kernel(const CUtensorMap* maps, const float* inv, void* out, int BH, int T, float beta, float p,
-                       float lam, cudaStream_t stream) {
+                       float lam, int d_real, cudaStream_t stream) {
   using L = DiffLayout<D>;
   auto kern = tra_diff_kernel<D, PC, NORM>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
@@ -443,20 +450,30 @@ int launch_diff_kernel(const CUtensorMap* maps, const float* inv, void* out, int
   const long long grid = static_cast<long long>(nQ) * BH;
   if (grid > 0x7fffffffLL) return ERR_SHAPE;
   // K1, K2, V: three streamed bf16 tensors per head; one resident CTA per SM
-  const int G = tile::head_groups(BH, nQ, 6LL * T * D, sm_count());
+  const int G = tile::head_groups(BH, nQ, 6LL * T * d_real, sm_count());
   kern<<<static_cast<unsigned>(grid), DiffCfg<D, PC>::THREADS, L::ALLOC, stream>>>(
       maps[0], maps[1], maps[2], maps[3], maps[4], inv, static_cast<__nv_bfloat16*>(out), BH, T, nQ, G, beta, p,
-      lam);
+      lam, d_real);
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
 
 template <int D, bool NORM>
 int dispatch_pc(const CUtensorMap* maps, const float* inv, void* out, int BH, int T, float beta, float p, float lam,
-                cudaStream_t stream) {
+                int d_real, cudaStream_t stream) {
   const int pc = power_class(p);
-  if (pc == POW_TWO) return launch_diff_kernel<D, POW_TWO, NORM>(maps, inv, out, BH, T, beta, p, lam, stream);
-  if (pc == POW_ONE) return launch_diff_kernel<D, POW_ONE, NORM>(maps, inv, out, BH, T, beta, p, lam, stream);
-  return launch_diff_kernel<D, POW_GENERAL, NORM>(maps, inv, out, BH, T, beta, p, lam, stream);
+  if (pc == POW_TWO) return launch_diff_kernel<D, POW_TWO, NORM>(maps, inv, out, BH, T, beta, p, lam, d_real, stream);
+  if (pc == POW_ONE) return launch_diff_kernel<D, POW_ONE, NORM>(maps, inv, out, BH, T, beta, p, lam, d_real, stream);
+  return launch_diff_kernel<D, POW_GENERAL, NORM>(maps, inv, out, BH, T, beta, p, lam, d_real, stream);
+}
+
+// Row-norm pre-pass at the head dim D (the real one).
+template <int D>
+void launch_row_norms(unsigned blocks, const __nv_bfloat16* a0, const __nv_bfloat16* a1, const __nv_bfloat16* a2,
+                      const __nv_bfloat16* a3, float* inv, int BH, int T, int Tp, bool idx32, cudaStream_t stream) {
+  if (idx32)
+    row_inv_norm_kernel<D, uint32_t><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv, BH, T, Tp);
+  else
+    row_inv_norm_kernel<D, unsigned long long><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv, BH, T, Tp);
 }
 
 }  // namespace
@@ -469,7 +486,7 @@ size_t tra_diff_scratch_bytes(int B, int H, int T) {
 int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const void* k2, const void* v, void* out,
                          int B, int H, int T, int D, float beta, float lam, float p, float* inv_norm,
                          cudaStream_t stream) {
-  if (D != 64 && D != 128) return ERR_UNSUPPORTED;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return ERR_UNSUPPORTED;
   const int BH = B * H;
   CUtensorMap maps[5];
   const uint64_t rs = static_cast<uint64_t>(D) * 2, hs = rs * T;
@@ -491,23 +508,20 @@ int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const v
     const auto* a2 = static_cast<const __nv_bfloat16*>(q2);
     const auto* a3 = static_cast<const __nv_bfloat16*>(k2);
     const bool idx32 = rows < (1LL << 32);  // every row index (and the division by Tp) fits 32 bits
-    if (D == 128 && idx32)
-      row_inv_norm_kernel<128, uint32_t><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv_norm, BH, T, Tp);
-    else if (D == 128)
-      row_inv_norm_kernel<128, unsigned long long><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv_norm, BH, T, Tp);
-    else if (idx32)
-      row_inv_norm_kernel<64, uint32_t><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv_norm, BH, T, Tp);
-    else
-      row_inv_norm_kernel<64, unsigned long long><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv_norm, BH, T, Tp);
+    switch (D) {
+      case 128: launch_row_norms<128>(blocks, a0, a1, a2, a3, inv_norm, BH, T, Tp, idx32, stream); break;
+      case 64: launch_row_norms<64>(blocks, a0, a1, a2, a3, inv_norm, BH, T, Tp, idx32, stream); break;
+      case 32: launch_row_norms<32>(blocks, a0, a1, a2, a3, inv_norm, BH, T, Tp, idx32, stream); break;
+      default: launch_row_norms<16>(blocks, a0, a1, a2, a3, inv_norm, BH, T, Tp, idx32, stream); break;
+    }
     if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
   }
   if (D == 128)
-    return norm ? dispatch_pc<128, true>(maps, inv_norm, out, BH, T, beta, p, lam, stream)
-                : dispatch_pc<128, false>(maps, inv_norm, out, BH, T, beta, p, lam, stream);
-  if (D == 64)
-    return norm ? dispatch_pc<64, true>(maps, inv_norm, out, BH, T, beta, p, lam, stream)
-                : dispatch_pc<64, false>(maps, inv_norm, out, BH, T, beta, p, lam, stream);
-  return ERR_UNSUPPORTED;
+    return norm ? dispatch_pc<128, true>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream)
+                : dispatch_pc<128, false>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
+  // 64, and 16 or 32 at width 64 on zero-filled columns
+  return norm ? dispatch_pc<64, true>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream)
+              : dispatch_pc<64, false>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
 }
 
 // ------------------------------------------------ allocation-free entry point

@@ -382,34 +382,49 @@ int diff_pc(const float* q1, const float* q2, const float* k1, const float* k2, 
 
 }  // namespace
 
+namespace {
+
+template <int D>
+int bwd_pc(const float* q, const float* k, const float* v, const float* dout, float* dq, float* dk, float* dv, int BH,
+           int T, float beta, float p, cudaStream_t stream) {
+  const int pc = power_class(p);
+  if (pc == POW_TWO) return launch_bwd<D, POW_TWO>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
+  if (pc == POW_ONE) return launch_bwd<D, POW_ONE>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
+  return launch_bwd<D, POW_GENERAL>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
+}
+
+template <int D>
+int diff_norm(const float* q1, const float* q2, const float* k1, const float* k2, const float* v, float* out, int BH,
+              int T, float beta, float p, float lam, bool normalize, cudaStream_t stream) {
+  return normalize ? diff_pc<D, true>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, stream)
+                   : diff_pc<D, false>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, stream);
+}
+
+}  // namespace
+
 int launch_tra_bwd_f32(const float* q, const float* k, const float* v, const float* dout, float* dq, float* dk,
                        float* dv, int B, int H, int T, int D, float beta, float p, cudaStream_t stream) {
   const int BH = B * H;
-  const int pc = power_class(p);
-  if (D == 64) {
-    if (pc == POW_TWO) return launch_bwd<64, POW_TWO>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
-    if (pc == POW_ONE) return launch_bwd<64, POW_ONE>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
-    return launch_bwd<64, POW_GENERAL>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
+  switch (D) {
+    case 16: return bwd_pc<16>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
+    case 32: return bwd_pc<32>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
+    case 64: return bwd_pc<64>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
+    case 128: return bwd_pc<128>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
+    default: return ERR_UNSUPPORTED;
   }
-  if (D == 128) {
-    if (pc == POW_TWO) return launch_bwd<128, POW_TWO>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
-    if (pc == POW_ONE) return launch_bwd<128, POW_ONE>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
-    return launch_bwd<128, POW_GENERAL>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
-  }
-  return ERR_UNSUPPORTED;
 }
 
 int launch_tra_diff_f32(const float* q1, const float* q2, const float* k1, const float* k2, const float* v,
                         float* out, int B, int H, int T, int D, float beta, float lam, float p, bool normalize,
                         cudaStream_t stream) {
   const int BH = B * H;
-  if (D == 64)
-    return normalize ? diff_pc<64, true>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, stream)
-                     : diff_pc<64, false>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, stream);
-  if (D == 128)
-    return normalize ? diff_pc<128, true>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, stream)
-                     : diff_pc<128, false>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, stream);
-  return ERR_UNSUPPORTED;
+  switch (D) {
+    case 16: return diff_norm<16>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, normalize, stream);
+    case 32: return diff_norm<32>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, normalize, stream);
+    case 64: return diff_norm<64>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, normalize, stream);
+    case 128: return diff_norm<128>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, normalize, stream);
+    default: return ERR_UNSUPPORTED;
+  }
 }
 
 }  // namespace bsa

@@ -194,7 +194,8 @@ BSA_API int tra_forward_host(const void* q, const void* k, const void* v,
  *   q, k, v, dout       : [B, H, T, D] inputs of `dtype` (dout = dL/d out).
  *   dq, dk, dv          : [B, H, T, D] outputs of `dtype` (fp32 accumulation);
  *                         they must not alias the inputs or each other.
- *   D                   : 64 or 128.
+ *   D                   : 16, 32, 64 or 128 (16 and 32 run the width-64
+ *                         kernels on zero-filled columns).
  *   B, H, T, beta, p    : as for tra_forward.  For 0 < p < 1 the derivative
  *                         p x^(p-1) grows without bound as x -> 0+, so a
  *                         score within rounding of tau(i) makes dq and dk
@@ -202,7 +203,8 @@ BSA_API int tra_forward_host(const void* q, const void* k, const void* v,
  *                         differ there).
  *   dtype               : BSA_BF16 or BSA_F32.
  *
- * Errors: as for tra_forward (BSA_ERR_UNSUPPORTED for D other than 64, 128),
+ * Errors: as for tra_forward (BSA_ERR_UNSUPPORTED for D other than 16, 32,
+ * 64, 128),
  * plus BSA_ERR_MEMORY if the bf16 temporary cannot be allocated or released.
  */
 BSA_API int tra_backward(const void* q, const void* k, const void* v,
@@ -258,7 +260,7 @@ BSA_API int tra_backward_ex(const void* q, const void* k, const void* v,
  *
  *   q1, q2, k1, k2, v, out : [B, H, T, D] of `dtype` (out may not alias
  *                            inputs).
- *   D                      : 64 or 128.
+ *   D                      : 16, 32, 64 or 128 (as for tra_forward).
  *   B, H, T, beta, p       : as for tra_forward.
  *   lambda                 : any non-NaN value; clamped to [0, 1].
  *   dtype                  : BSA_BF16 or BSA_F32.

@@ -125,6 +125,8 @@ def test_backward_and_diff_argument_errors(lib):
     assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 64, 1.0, 2.0, 7, 0) == 3  # not a bsa_dtype
     assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 96, 1.0, 2.0, 0, 0) == 4  # f32, D = 96
     assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 96, 1.0, 2.0, 1, 0) == 4
+    assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 48, 1.0, 2.0, 1, 0) == 4
+    assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 8, 1.0, 2.0, 1, 0) == 4
     assert bsa.tra_backward_raw(P, P, P, P, P + 2, P, P, 1, 1, 16, 64, 1.0, 2.0, 1, 0) == 7
     assert bsa.tra_backward_ex_raw(P, P, P, P, P, P, P, 1, 1, 16, 64, 1.0, 2.0, 1, 2, 0) == 4  # unknown flag bit
     assert bsa.tra_backward_ex_raw(P, P, P, None, P, P, P, 1, 1, 16, 64, 1.0, 2.0, 1, 1, 0) == 1

@@ -41,6 +41,8 @@ CASES = [
     (1, 2, 640, 64, 1.0, 2.0),   # 5 tiles each way
     (1, 1, 384, 128, -0.5, 3.7), # beta < 0 reading, large power
     (2, 2, 1024, 128, 1.0, 2.0), # medium size
+    (1, 2, 300, 32, 1.0, 2.0),   # head dim 32 (width-64 tiles, zero-filled columns), ragged
+    (1, 1, 257, 16, 0.5, 1.5),   # head dim 16, general power
 ]
 
 
@@ -110,6 +112,8 @@ F32_CASES = [
     (1, 2, 130, 64, 0.0, 1.0),    # p = 1
     (1, 1, 1, 128, 1.0, 2.0),     # T = 1
     (1, 1, 320, 64, -0.5, 3.7),   # beta < 0 reading, large power
+    (1, 2, 150, 32, 1.0, 2.0),    # head dim 32
+    (1, 1, 100, 16, 0.5, 1.5),    # head dim 16
 ]
 
 

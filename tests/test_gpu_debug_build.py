@@ -67,7 +67,7 @@ def test_tra_forward_debug_build(debug_lib, B, H, T, D, beta, p, dtype):
     same(*both(debug_lib, lambda: bsa.tra_forward(q, k, v, beta, p)))
 
 
-@pytest.mark.parametrize("T,D,p", [(1, 64, 2.0), (300, 128, 2.0), (257, 64, 1.5)])
+@pytest.mark.parametrize("T,D,p", [(1, 64, 2.0), (300, 128, 2.0), (257, 64, 1.5), (200, 32, 2.0)])
 def test_tra_backward_and_diff_debug_build(debug_lib, T, D, p):
     q, k, v = (t.cuda() for t in workloads.tra_inputs(1, 2, T, D, "bf16", seed=T + 1))
     q2, k2, _ = (t.cuda() for t in workloads.tra_inputs(1, 2, T, D, "bf16", seed=T + 2))

@@ -47,6 +47,9 @@ CASES = [
     (1, 1, 384, 128, 0.5, -1.0, 2.0, False),  # lambda clamps to 0
     (2, 2, 1024, 128, 0.05, 0.5, 2.0, True),
     (2, 3, 500, 64, 0.3, 0.6, 1.0, False),  # D = 64, p = 1: one MMA issuer per stream
+    (1, 2, 300, 32, 0.2, 0.5, 2.0, True),   # head dim 32 (width-64 tiles, zero-filled columns)
+    (1, 1, 257, 16, 0.0, 0.7, 1.5, True),   # head dim 16, general power
+    (1, 2, 130, 32, 0.3, 0.4, 1.0, False),
 ]
 
 
@@ -115,6 +118,8 @@ F32_CASES = [
     (1, 2, 130, 64, 0.5, 0.3, 1.0, False),
     (1, 1, 1, 128, 1.0, 0.5, 2.0, True),
     (1, 1, 320, 64, 0.1, 1.5, 2.0, False),   # lambda clamps to 1
+    (1, 2, 150, 32, 0.2, 0.5, 2.0, True),    # head dim 32
+    (1, 1, 100, 16, 0.0, 0.6, 1.5, True),    # head dim 16
 ]
 
 
