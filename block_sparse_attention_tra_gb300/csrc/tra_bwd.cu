@@ -9,7 +9,11 @@
 //                                                dQ_i = sum_j dA_ij k_j
 // (derivative 0 where x <= 0, as on the page; beta and p get no gradient).
 // Like the page, two kernels: one per key tile for dK and dV, one per query
-// tile for dQ; both recompute the scores instead of storing W.
+// tile for dQ; both recompute the scores instead of storing W.  This is the
+// deterministic form (bit-repeatable, no scratch) behind
+// BSA_TRA_BWD_DETERMINISTIC; the default bf16 backward is the fused kernel of
+// tra_bwd_fused.cu, which produces the scores once per tile pair.  Head dims
+// 16 and 32 run the width-64 kernels on zero-filled columns.
 //
 // dK/dV kernel, one CTA per 128-key tile n of one (b, h), looping over the
 // query tiles m >= n: S^T = K_n Q_m^T and dP^T = V_n dO_m^T into TMEM; the
