@@ -88,8 +88,20 @@ struct ChunkIter {
       seek_slot();
     }
   }
+  // n steps at once: whole blocks are skipped instead of walked chunk by chunk.
   __device__ __forceinline__ void advance(int n) {
-    for (int k = 0; k < n && valid; ++k) step();
+    while (valid) {
+      const int left = nc - c;  // chunks of this block from c on
+      if (n < left) {
+        c += n;
+        tok0 += n * GEN_CHUNK;
+        return;
+      }
+      n -= left;
+      ++s;
+      seek_slot();
+      if (n == 0) return;
+    }
   }
 };
 
@@ -200,17 +212,31 @@ __global__ void __launch_bounds__(GEN_THREADS)
             for (int e = 0; e < 4; ++e) sc[j][e] += sd[j][e];
         }
       }
-      // ---- scale (log2 domain), causal mask, online softmax
+      // ---- scale (log2 domain), causal mask, online softmax.  Only the chunk
+      // holding token i has keys after it (a warp-uniform test).
       float mx0 = -INFINITY, mx1 = -INFINITY;
+      if (tok0 + GEN_CHUNK - 1 <= i) {
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < 2; ++j) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const bool ok_key = tok0 + 8 * j + 2 * t + e <= i;
-          sc[j][e] = ok_key ? sc[j][e] * scale_log2 : -INFINITY;
-          sc[j][2 + e] = ok_key ? sc[j][2 + e] * scale_log2 : -INFINITY;
-          mx0 = fmaxf(mx0, sc[j][e]);
-          mx1 = fmaxf(mx1, sc[j][2 + e]);
+          for (int e = 0; e < 2; ++e) {
+            sc[j][e] *= scale_log2;
+            sc[j][2 + e] *= scale_log2;
+            mx0 = fmaxf(mx0, sc[j][e]);
+            mx1 = fmaxf(mx1, sc[j][2 + e]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const bool ok_key = tok0 + 8 * j + 2 * t + e <= i;
+            sc[j][e] = ok_key ? sc[j][e] * scale_log2 : -INFINITY;
+            sc[j][2 + e] = ok_key ? sc[j][2 + e] * scale_log2 : -INFINITY;
+            mx0 = fmaxf(mx0, sc[j][e]);
+            mx1 = fmaxf(mx1, sc[j][2 + e]);
+          }
         }
       }
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
