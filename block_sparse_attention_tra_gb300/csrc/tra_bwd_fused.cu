@@ -36,7 +36,11 @@
 // ~5000 cycles per step against 2560 of tensor work.
 // Shared memory (D = 128): K_n, V_n resident; Q in two slots; dO in one slot
 // (dO_m's last reader, dV, finishes ~1500 tensor cycles before the next dP^T
-// needs dO_{m+1}); the dA^T operand; 32 KB of staging for the dQ boxes.
+// needs dO_{m+1}); the dA^T operand; 32 KB of staging for the dQ boxes.  At
+// D = 64, Q and dO have two slots each.  A trace there shows the MMA issuer
+// waiting ~2000 cycles per step for dO, but three or four slots measured
+// slower (B2 H32 T8192 p=2: 1.50 / 1.59 / 1.63 ms for 2 / 3 / 4): the wait is
+// the L2 serving the loads beside the dQ reduce-adds, not prefetch depth.
 //
 // Warps: 0-7 epilogue, 8-11 dQ drain, 12 TMA producer, 13 MMA issuer.  Every
 // mbarrier wait is bounded; the drain warps take each go/no-go decision
@@ -60,22 +64,27 @@ constexpr int MMA_WARP = 13;
 constexpr int THREADS = 14 * 32;
 constexpr int DRAIN_BAR = 1;  // named barrier of the drain warps
 
+#ifndef BSA_FBWD_SLOTS_D64
+#define BSA_FBWD_SLOTS_D64 2  // Q and dO slots at D = 64
+#endif
+
 template <int D>
 struct FusedLayout {
   static constexpr int TILE = D / 64 * PANEL_BYTES;
-  static constexpr int DO_SLOTS = D == 128 ? 1 : 2;
+  static constexpr int Q_SLOTS = D == 128 ? 2 : BSA_FBWD_SLOTS_D64;
+  static constexpr int DO_SLOTS = D == 128 ? 1 : BSA_FBWD_SLOTS_D64;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = TILE;
-  static constexpr int Q_OFF = 2 * TILE;                    // two slots
-  static constexpr int DO_OFF = Q_OFF + 2 * TILE;           // DO_SLOTS slots
+  static constexpr int Q_OFF = 2 * TILE;                    // Q_SLOTS slots
+  static constexpr int DO_OFF = Q_OFF + Q_SLOTS * TILE;     // DO_SLOTS slots
   static constexpr int DA_OFF = DO_OFF + DO_SLOTS * TILE;   // dA^T: 128 keys x 128 queries bf16, two panels
   static constexpr int STG_OFF = DA_OFF + 2 * PANEL_BYTES;  // two fp32 boxes of 128 rows x 32 columns
   static constexpr int BOX_BYTES = BT * 32 * 4;
   static constexpr int TAU_OFF = STG_OFF + 2 * BOX_BYTES;   // float[2][128]
   static constexpr int BAR_OFF = TAU_OFF + 2 * BT * 4;
-  // kv_full | q_full[2] | q_empty[2] | do_full[S] | do_empty[S] | s_full | p_full | w_ready | a_ready |
+  // kv_full | q_full[QS] | q_empty[QS] | do_full[S] | do_empty[S] | s_full | p_full | w_ready | a_ready |
   // dq_full | dq_empty | da_free | tau_full[2] | acc_full | mma_done
-  static constexpr int NBAR = 1 + 4 + 2 * DO_SLOTS + 7 + 2 + 2;
+  static constexpr int NBAR = 1 + 2 * Q_SLOTS + 2 * DO_SLOTS + 7 + 2 + 2;
   static constexpr int TPTR_OFF = BAR_OFF + NBAR * 8;
   static constexpr int ALLOC = TPTR_OFF + 16 + 1024;
   static_assert(ALLOC <= 232448, "shared memory");
@@ -96,8 +105,8 @@ __device__ __forceinline__ FusedBars fused_bars(uint8_t* smem) {
   FusedBars r;
   r.kv_full = b;
   r.q_full = b + 1;
-  r.q_empty = r.q_full + 2;
-  r.do_full = r.q_empty + 2;
+  r.q_empty = r.q_full + L::Q_SLOTS;
+  r.do_full = r.q_empty + L::Q_SLOTS;
   r.do_empty = r.do_full + L::DO_SLOTS;
   r.s_full = r.do_empty + L::DO_SLOTS;
   r.p_full = r.s_full + 1;
@@ -181,11 +190,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(B.kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < L::Q_SLOTS; ++s) {
       mbar_init(&B.q_full[s], 1);
       mbar_init(&B.q_empty[s], 1);
-      mbar_init(&B.tau_full[s], EPI_WARPS);
     }
+    for (int s = 0; s < 2; ++s) mbar_init(&B.tau_full[s], EPI_WARPS);
     for (int s = 0; s < L::DO_SLOTS; ++s) {
       mbar_init(&B.do_full[s], 1);
       mbar_init(&B.do_empty[s], 1);
@@ -213,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == TMA_WARP) {
     if (lane == 0) {
       debug_check(bh >= 0 && bh < BH && n * BT < T && (n + nq - 1) * BT < T);
-      bwd::produce<D, 2, L::DO_SLOTS>(smem + L::K_OFF, smem + L::V_OFF, B.kv_full, smem + L::Q_OFF, B.q_full,
+      bwd::produce<D, L::Q_SLOTS, L::DO_SLOTS>(smem + L::K_OFF, smem + L::V_OFF, B.kv_full, smem + L::Q_OFF, B.q_full,
                                       B.q_empty, smem + L::DO_OFF, B.do_full, B.do_empty, &tmK, &tmV, n * BT, &tmQ,
                                       &tmDO, n, nq, bh);
     }
@@ -225,10 +234,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       };
       const uint32_t sK = smem_u32(smem + L::K_OFF), sV = smem_u32(smem + L::V_OFF);
       const uint32_t sDA = smem_u32(smem + L::DA_OFF);
-      auto q_slot = [&](int j) { return smem_u32(smem + L::Q_OFF + (j & 1) * L::TILE); };
+      auto q_slot = [&](int j) { return smem_u32(smem + L::Q_OFF + (j % L::Q_SLOTS) * L::TILE); };
       // S^T = K_n Q_m^T of step j (into S, whose W^T of step j-1 dV has read, in issue order)
       auto scores = [&](int j) -> bool {
-        if (!mbar_wait(&B.q_full[j & 1], (j >> 1) & 1)) return false;
+        if (!mbar_wait(&B.q_full[j % L::Q_SLOTS], (j / L::Q_SLOTS) & 1)) return false;
         tc_fence_after();
         tile::mma_abt<D>(tmem + L::TS, sK, q_slot(j), leader);
         commit(B.s_full);
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         mma_dq<D>(tmem + L::TDQ, sDA, sK, leader);
         commit(B.dq_full);
         mma_dk<D>(tmem + L::TDK, sDA, sQ, j == 0, leader);
-        commit(&B.q_empty[j & 1]);
+        commit(&B.q_empty[j % L::Q_SLOTS]);
         commit(B.da_free);
       }
       if (ok) commit(B.acc_full);
