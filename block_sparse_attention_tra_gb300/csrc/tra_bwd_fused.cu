@@ -159,6 +159,14 @@ __device__ __forceinline__ void stage_box(uint8_t* box, int r, const uint32_t (&
         make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
 }
 
+// Who fills the epilogue's tau table: the drain warps at D = 64, two steps
+// ahead; at D = 128 (where the drain warps sit on the path to the next dP^T
+// and the change measured 1-3% slower) the epilogue warps, per step.
+template <int D>
+constexpr bool drain_fills_tau() {
+  return D == 64;
+}
+
 // MMA issue: a converged warp with an elected issuing lane at D = 64, the
 // elected lane alone at D = 128 (as in the recompute kernels).
 template <int D>
@@ -194,7 +202,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&B.q_full[s], 1);
       mbar_init(&B.q_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) mbar_init(&B.tau_full[s], EPI_WARPS);
+    for (int s = 0; s < 2; ++s) mbar_init(&B.tau_full[s], drain_fills_tau<D>() ? 4 : EPI_WARPS);
     for (int s = 0; s < L::DO_SLOTS; ++s) {
       mbar_init(&B.do_full[s], 1);
       mbar_init(&B.do_empty[s], 1);
@@ -285,6 +293,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* stg = smem + L::STG_OFF;
     const uint32_t sStg = smem_u32(stg);
     const bool issuer = warp == DRAIN_WARP && lane == 0;
+    // At D = 64 the drain warps also fill the epilogue's double-buffered tau table
+    // (tau(i) of the step's 128 query columns): steps 0 and 1 up front, step
+    // j + 2 once dQ of step j is done (the epilogue finished reading buffer
+    // j & 1 before it produced the dA of step j) and its TMEM released.  This
+    // keeps the tau evaluation (log, divide, square root) and a barrier of
+    // all eight epilogue warps off the epilogue's path (B2 H32 T8192 D64:
+    // p=2 1.50 -> 1.45 ms, p=1.5 2.17 -> 2.07 ms).
+    auto fill_tau = [&](int jj) {
+      if constexpr (drain_fills_tau<D>()) {
+        tau_s[(jj & 1) * BT + r] = tile::tau_of_row((n + jj) * BT + r, beta, dr);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.tau_full[jj & 1]);
+      }
+    };
+    fill_tau(0);
+    if (nq > 1) fill_tau(1);
     bool ok = true;
     for (int j = 0; j < nq; ++j) {
       const int m = n + j;
@@ -310,6 +334,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(B.dq_empty);
       }
+      // (after dQ's TMEM is released: at D = 128 the next dP^T waits for it)
+      if (j + 2 < nq) fill_tau(j + 2);
       fence_proxy_async_smem();
       bar_sync(DRAIN_BAR, 128);
       if (issuer) {
@@ -345,11 +371,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int j = 0; j < nq && ok; ++j) {
       const int m = n + j;
-      // Double-buffered tau table (as in the recompute kernels).
+      // Double-buffered tau table (a warp writes buffer j & 1 for step j only
+      // after every warp arrived for step j - 1, i.e. finished step j - 2).
       float* tau_m = tau_s + (j & 1) * BT;
-      tau_m[r] = tile::tau_of_row(m * BT + r, beta, dr);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B.tau_full[j & 1]);
+      if constexpr (!drain_fills_tau<D>()) {
+        tau_m[r] = tile::tau_of_row(m * BT + r, beta, dr);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.tau_full[j & 1]);
+      }
       if (!(ok = mbar_wait(&B.tau_full[j & 1], (j >> 1) & 1))) break;
       const bool diag = (m == n);
       // Part 1: W^T and g from S^T.
@@ -363,12 +392,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(lane_base + L::TS + q0, sv);
         tmem_wait_ld();
         uint32_t wpk[16];
+        float4 t4;
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int i0 = q0 + 2 * e;  // query column within the tile
+          if ((e & 1) == 0) t4 = *reinterpret_cast<const float4*>(tau_m + i0);  // tau of columns i0 .. i0+3
+          const float ta = (e & 1) ? t4.z : t4.x, tb = (e & 1) ? t4.w : t4.y;
           float w0, g0, w1, g1;
-          bwd::weight_and_grad<PC>(__uint_as_float(sv[2 * e]) - tau_m[i0], p, w0, g0);
-          bwd::weight_and_grad<PC>(__uint_as_float(sv[2 * e + 1]) - tau_m[i0 + 1], p, w1, g1);
+          bwd::weight_and_grad<PC>(__uint_as_float(sv[2 * e]) - ta, p, w0, g0);
+          bwd::weight_and_grad<PC>(__uint_as_float(sv[2 * e + 1]) - tb, p, w1, g1);
           if (diag) {  // causal: key r <= query column
             if (i0 < r) w0 = g0 = 0.0f;
             if (i0 + 1 < r) w1 = g1 = 0.0f;
