@@ -49,6 +49,7 @@
 #include "ptx.cuh"
 #include "tc_tile.cuh"
 #include "tra_bwd_common.cuh"
+#include "tra_math.cuh"
 
 namespace bsa {
 namespace {
@@ -159,12 +160,32 @@ __device__ __forceinline__ void stage_box(uint8_t* box, int r, const uint32_t (&
         make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
 }
 
+// tau(i) = beta sqrt(2 ln(i+1) / d) from the MUFU lg2 and sqrt approximations
+// (k2 = 2 ln 2 / d): within ~1e-7 relative of the correctly rounded value, at
+// a few instructions instead of the dozens of logf, a divide and sqrtf.
+// BSA_FBWD_FAST_TAU = 0 uses tile::tau_of_row instead.
+#ifndef BSA_FBWD_FAST_TAU
+#define BSA_FBWD_FAST_TAU 1
+#endif
+__device__ __forceinline__ float tau_fast(int row, float beta, float k2, int d) {
+#if BSA_FBWD_FAST_TAU
+  (void)d;
+  return beta * sqrt_approx(lg2_approx(static_cast<float>(row + 1)) * k2);
+#else
+  (void)k2;
+  return tile::tau_of_row(row, beta, d);
+#endif
+}
+
 // Who fills the epilogue's tau table: the drain warps at D = 64, two steps
 // ahead; at D = 128 (where the drain warps sit on the path to the next dP^T
 // and the change measured 1-3% slower) the epilogue warps, per step.
+#ifndef BSA_FBWD_DRAIN_TAU
+#define BSA_FBWD_DRAIN_TAU 1  // 1: D = 64 only; 2: every D
+#endif
 template <int D>
 constexpr bool drain_fills_tau() {
-  return D == 64;
+  return BSA_FBWD_DRAIN_TAU == 2 || (BSA_FBWD_DRAIN_TAU == 1 && D == 64);
 }
 
 // MMA issue: a converged warp with an elected issuing lane at D = 64, the
@@ -185,6 +206,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // Head dims 16 and 32 run at tile width 64 on zero-filled columns (the
   // tensor maps cover the real d_real columns); width 128 serves 128 alone.
   const int dr = D == 128 ? D : d_real;
+  const float k2 = 2.0f * 0.6931471805599453f / static_cast<float>(dr);  // 2 ln 2 / d
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const FusedBars B = fused_bars<D>(smem);
@@ -302,7 +324,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // p=2 1.50 -> 1.45 ms, p=1.5 2.17 -> 2.07 ms).
     auto fill_tau = [&](int jj) {
       if constexpr (drain_fills_tau<D>()) {
-        tau_s[(jj & 1) * BT + r] = tile::tau_of_row((n + jj) * BT + r, beta, dr);
+        tau_s[(jj & 1) * BT + r] = tau_fast((n + jj) * BT + r, beta, k2, dr);
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.tau_full[jj & 1]);
       }
@@ -375,7 +397,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // after every warp arrived for step j - 1, i.e. finished step j - 2).
       float* tau_m = tau_s + (j & 1) * BT;
       if constexpr (!drain_fills_tau<D>()) {
-        tau_m[r] = tile::tau_of_row(m * BT + r, beta, dr);
+        tau_m[r] = tau_fast(m * BT + r, beta, k2, dr);
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.tau_full[j & 1]);
       }
