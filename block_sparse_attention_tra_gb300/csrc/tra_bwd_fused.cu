@@ -177,6 +177,34 @@ __device__ __forceinline__ float tau_fast(int row, float beta, float k2, int d) 
 #endif
 }
 
+// W and g = p ReLU(x)^(p-1) of two scores at once for p = 1 and p = 2 on
+// packed f32x2 arithmetic (x = s - tau in one packed subtract; W = r r and
+// g = r + r in one packed multiply and add for p = 2), bit-identical to
+// bwd::weight_and_grad; other powers take the scalar form.
+template <int PC>
+__device__ __forceinline__ void weight_and_grad2(float s0, float s1, float t0, float t1, float p, float& w0,
+                                                 float& w1, uint64_t& g) {
+  if constexpr (PC == POW_TWO || PC == POW_ONE) {
+    float x0, x1;
+    f2_unpack(f2_sub(f2_pack(s0, s1), f2_pack(t0, t1)), x0, x1);
+    const float r0 = fmaxf(x0, 0.0f), r1 = fmaxf(x1, 0.0f);
+    const uint64_t r = f2_pack(r0, r1);
+    if constexpr (PC == POW_TWO) {
+      f2_unpack(f2_mul(r, r), w0, w1);
+      g = f2_add(r, r);
+    } else {
+      w0 = r0;
+      w1 = r1;
+      g = f2_pack(x0 > 0.0f ? 1.0f : 0.0f, x1 > 0.0f ? 1.0f : 0.0f);
+    }
+  } else {
+    float g0, g1;
+    bwd::weight_and_grad<PC>(s0 - t0, p, w0, g0);
+    bwd::weight_and_grad<PC>(s1 - t1, p, w1, g1);
+    g = f2_pack(g0, g1);
+  }
+}
+
 // Who fills the epilogue's tau table: the drain warps at D = 64, two steps
 // ahead; at D = 128 (where the drain warps sit on the path to the next dP^T
 // and the change measured 1-3% slower) the epilogue warps, per step.
@@ -406,7 +434,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Part 1: W^T and g from S^T.
       if (!(ok = mbar_wait(B.s_full, j & 1))) break;
       tc_fence_after();
-      float g[64];
+      uint64_t g[32];  // g of this warp's 64 query columns, two per register pair
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int q0 = 64 * h + 32 * c;
@@ -420,16 +448,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int i0 = q0 + 2 * e;  // query column within the tile
           if ((e & 1) == 0) t4 = *reinterpret_cast<const float4*>(tau_m + i0);  // tau of columns i0 .. i0+3
           const float ta = (e & 1) ? t4.z : t4.x, tb = (e & 1) ? t4.w : t4.y;
-          float w0, g0, w1, g1;
-          bwd::weight_and_grad<PC>(__uint_as_float(sv[2 * e]) - ta, p, w0, g0);
-          bwd::weight_and_grad<PC>(__uint_as_float(sv[2 * e + 1]) - tb, p, w1, g1);
+          float w0, w1;
+          uint64_t g2;
+          weight_and_grad2<PC>(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1]), ta, tb, p, w0, w1, g2);
           if (diag) {  // causal: key r <= query column
+            float g0, g1;
+            f2_unpack(g2, g0, g1);
             if (i0 < r) w0 = g0 = 0.0f;
             if (i0 + 1 < r) w1 = g1 = 0.0f;
+            g2 = f2_pack(g0, g1);
           }
           wpk[e] = pack_bf16x2(w0, w1);
-          g[32 * c + 2 * e] = g0;
-          g[32 * c + 2 * e + 1] = g1;
+          g[16 * c + e] = g2;
         }
         // packs into the half's own first 32 columns (already-consumed scores)
         tmem_st16(lane_base + L::TS + 64 * h + 16 * c, wpk);
@@ -451,9 +481,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_wait_ld();
         uint32_t apk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          apk[e] = pack_bf16x2(__uint_as_float(dp[2 * e]) * g[32 * c + 2 * e],
-                               __uint_as_float(dp[2 * e + 1]) * g[32 * c + 2 * e + 1]);
+        for (int e = 0; e < 16; ++e) {
+          float a0, a1;
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])), g[16 * c + e]), a0, a1);
+          apk[e] = pack_bf16x2(a0, a1);
+        }
         // row r, query columns q0 .. q0+31 = 16-byte chunks 4c .. 4c+3 of panel h
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
