@@ -216,11 +216,14 @@ constexpr bool drain_fills_tau() {
   return BSA_FBWD_DRAIN_TAU == 2 || (BSA_FBWD_DRAIN_TAU == 1 && D == 64);
 }
 
-// MMA issue: a converged warp with an elected issuing lane at D = 64, the
-// elected lane alone at D = 128 (as in the recompute kernels).
+// MMA issue: a converged warp with an elected issuing lane (at D = 128 the
+// elected lane alone was 0.5-1% slower).
+#ifndef BSA_FBWD_CONVERGED_ISSUE
+#define BSA_FBWD_CONVERGED_ISSUE 2  // 1: D = 64 only; 2: every D (D = 128 measured 0.5-1% faster)
+#endif
 template <int D>
 constexpr bool fused_converged_issue() {
-  return D == 64;
+  return BSA_FBWD_CONVERGED_ISSUE == 2 || (BSA_FBWD_CONVERGED_ISSUE == 1 && D == 64);
 }
 
 template <int D, int PC>
