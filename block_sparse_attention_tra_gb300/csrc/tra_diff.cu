@@ -166,21 +166,24 @@ __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* 
 }
 
 // 32 scores of stream t -> 16 packed weights over the consumed score
-// columns.  With NORM the scores are first multiplied by rq * rk[col] (the
-// normalisation of row and key).
+// columns.  With NORM the scores are scaled by rq * rk[col] (the normalisation
+// of row and key): x = s (rq rk) - tau in one packed multiply and one packed
+// fused multiply-add per key pair.
 // DIAG (compile time): the tile holds the diagonal, mask keys after the row.
 template <int PC, bool NORM, bool DIAG>
 __device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t tS, int c0, const PowParams& wp,
-                                             float rq, const float (&rk)[32], int key0, int row) {
+                                             uint64_t rq2, uint64_t ntau2, const float (&rk)[32], int key0,
+                                             int row) {
   uint32_t pk[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
-    float s0 = __uint_as_float(s[2 * e]), s1 = __uint_as_float(s[2 * e + 1]);
-    if constexpr (NORM) {
-      s0 *= rq * rk[2 * e];
-      s1 *= rq * rk[2 * e + 1];
-    }
-    uint32_t w = weights2<PC>(s0, s1, wp);
+    const uint64_t s2 = f2_pack(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]));
+    uint64_t x2;
+    if constexpr (NORM)
+      x2 = f2_fma(s2, f2_mul(rq2, f2_pack(rk[2 * e], rk[2 * e + 1])), ntau2);
+    else
+      x2 = f2_sub(s2, wp.tau2);
+    uint32_t w = weights2_x<PC>(x2, wp);
     if constexpr (DIAG) {
       const int key = key0 + c0 + 2 * e;
       if (key > row) w = 0u;
@@ -366,6 +369,7 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
     const float lc = fminf(fmaxf(lam, 0.0f), 1.0f);
     // inv_norm: [q1 | k1 | q2 | k2] x [B*H] x [Tp], zero past T
     const float rq = NORM ? inv_norm[(static_cast<long long>(t == 0 ? 0 : 2) * BH + bh) * Tp + row] : 1.0f;
+    const uint64_t rq2 = f2_pack(rq, rq), ntau2 = f2_pack(-tau, -tau);
     bool ok = true;
     for (int n = 0; n <= nmax; ++n) {
       if (!(ok = mbar_wait(&s_full[t], n & 1))) break;
@@ -375,8 +379,9 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
       const float* rk_tile =
           reinterpret_cast<const float*>(smem + rr.off + rr.stage(n) * 2 * L::RK_BYTES + t * L::RK_BYTES);
       if (NORM && !(ok = mbar_wait(&rr.full[rr.stage(n)], rr.phase(n)))) break;
-#pragma unroll 1
-      for (int c = 0; c < BT / 32; ++c) {
+      // Four 32-column chunks; each chunk's scores are loaded while the
+      // previous one is turned into weights (two buffers of 32 registers).
+      auto quarter = [&](const uint32_t (&sv)[32], int c) {
         float rk[32];
         if constexpr (NORM) {
 #pragma unroll
@@ -388,14 +393,24 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
             rk[j + 3] = f.w;
           }
         }
-        uint32_t sv[32];
-        tmem_ld32(tS + 32 * c, sv);
-        tmem_wait_ld();
         if (diag)
-          diff_quarter<PC, NORM, true>(sv, tS, 32 * c, wp, rq, rk, n * BT, row);
+          diff_quarter<PC, NORM, true>(sv, tS, 32 * c, wp, rq2, ntau2, rk, n * BT, row);
         else
-          diff_quarter<PC, NORM, false>(sv, tS, 32 * c, wp, rq, rk, n * BT, row);
-      }
+          diff_quarter<PC, NORM, false>(sv, tS, 32 * c, wp, rq2, ntau2, rk, n * BT, row);
+      };
+      uint32_t sa[32], sb[32];
+      tmem_ld32(tS, sa);
+      tmem_wait_ld();
+      tmem_ld32(tS + 32, sb);
+      quarter(sa, 0);  // P of chunk c lands in columns 16c .., already read
+      tmem_wait_ld();
+      tmem_ld32(tS + 64, sa);
+      quarter(sb, 1);
+      tmem_wait_ld();
+      tmem_ld32(tS + 96, sb);
+      quarter(sa, 2);
+      tmem_wait_ld();
+      quarter(sb, 3);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

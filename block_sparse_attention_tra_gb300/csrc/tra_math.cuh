@@ -151,12 +151,12 @@ __host__ __device__ constexpr bool mix_pair_on_fma(int e) {
 #define BSA_POW2_SINGLE_ROUNDING 0
 #endif
 
-// Weights of two adjacent keys from their scores: ReLU(s - tau)^p, bf16x2.
+// Weights of two adjacent keys from x = s - tau (packed): ReLU(x)^p, bf16x2.
 // FMA_LOG2 (POW_GENERAL_MIX only): this pair's log2 runs on the FMA pipe.
 template <int PC, bool FMA_LOG2 = false>
-__device__ __forceinline__ uint32_t weights2(float s0, float s1, const PowParams& w) {
+__device__ __forceinline__ uint32_t weights2_x(uint64_t x2, const PowParams& w) {
   float x0, x1;
-  f2_unpack(f2_sub(f2_pack(s0, s1), w.tau2), x0, x1);
+  f2_unpack(x2, x0, x1);
   if constexpr (PC == POW_ONE) {
     return relu_pack(x0, x1);
   } else if constexpr (PC == POW_TWO) {
@@ -200,6 +200,12 @@ __device__ __forceinline__ uint32_t weights2(float s0, float s1, const PowParams
     f2_unpack(y, y0, y1);
     return pack_bf16x2(ex2_approx(y0), ex2_approx(y1));
   }
+}
+
+// Weights of two adjacent keys from their scores: ReLU(s - tau)^p, bf16x2.
+template <int PC, bool FMA_LOG2 = false>
+__device__ __forceinline__ uint32_t weights2(float s0, float s1, const PowParams& w) {
+  return weights2_x<PC, FMA_LOG2>(f2_sub(f2_pack(s0, s1), w.tau2), w);
 }
 
 }  // namespace
