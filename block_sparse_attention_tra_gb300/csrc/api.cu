@@ -279,17 +279,21 @@ int tra_diff_forward(const void* q1, const void* q2, const void* k1, const void*
                                static_cast<const float*>(k1), static_cast<const float*>(k2),
                                static_cast<const float*>(v), static_cast<float*>(out), B, H, T, D, beta, lambda, p,
                                normalize != 0, stream);
-  if (!normalize) return launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, nullptr, stream);
+  if (!normalize)
+    return launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, nullptr, nullptr, stream);
   // Normalisation factors of every row of q1, k1, q2, k2 (T padded to a
-  // multiple of 128): a stream-ordered temporary, released on the same stream.
+  // multiple of 128) and normalised copies of k1 and k2: one stream-ordered
+  // temporary, released on the same stream.
   float* inv = nullptr;
-  const size_t bytes = tra_diff_scratch_bytes(B, H, T);
+  const size_t nbytes = (tra_diff_scratch_bytes(B, H, T) + 255) / 256 * 256;
+  const size_t bytes = nbytes + 2 * sizeof(uint16_t) * static_cast<size_t>(B) * H * T * D;
   int dev = 0;
   cudaMemPool_t pool = cudaGetDevice(&dev) == cudaSuccess ? scratch_pool(dev) : nullptr;
   if (pool == nullptr) return BSA_ERR_MEMORY;
   if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&inv), bytes, pool, stream) != cudaSuccess)
     return BSA_ERR_MEMORY;
-  const int st = launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, inv, stream);
+  const int st = launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, inv,
+                                      reinterpret_cast<uint8_t*>(inv) + nbytes, stream);
   if (cudaFreeAsync(inv, stream) != cudaSuccess && st == OK) return BSA_ERR_MEMORY;
   return st;
 }

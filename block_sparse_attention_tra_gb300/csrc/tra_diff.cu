@@ -113,12 +113,28 @@ __device__ __forceinline__ void norm_row(long long row, long long rows_p, int Tp
   t = static_cast<int>(rem - b * static_cast<Idx>(Tp));
 }
 
-template <int D, typename Idx>
+// x * r rounded to bf16, for the eight bf16 of a 16-byte chunk.
+__device__ __forceinline__ uint4 scale_bf16x8(const uint4& u, float r) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+    o[e] = pack_bf16x2(lo * r, hi * r);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// WRITE_K: the k1 and k2 rows (inputs 1 and 3) are also written normalised,
+// x / max(||x||, 1e-12) rounded to bf16 -- the page normalises q and k before
+// its kernel, in the input dtype -- into kn (k1 at kn, k2 at kn + B*H*T*D).
+template <int D, typename Idx, bool WRITE_K>
 __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* __restrict__ a0,
                                                            const __nv_bfloat16* __restrict__ a1,
                                                            const __nv_bfloat16* __restrict__ a2,
                                                            const __nv_bfloat16* __restrict__ a3,
-                                                           float* __restrict__ inv, int BH, int T, int Tp) {
+                                                           float* __restrict__ inv, __nv_bfloat16* __restrict__ kn,
+                                                           int BH, int T, int Tp) {
   // Row of D bf16 = D / 8 chunks of 16 bytes over the eight lanes of a row:
   // lane `sub` takes chunks sub + 8c (none past the row for D = 16, 32).
   constexpr int CH = (D + 63) / 64;
@@ -131,11 +147,15 @@ __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* 
   for (long long base = warp0 * 4 * NG; base < total; base += nwarps * 4 * NG) {
     long long row[NG];
     bool live[NG];
+    int which_g[NG];
+    long long src_off[NG];  // element offset of the row in its input
     uint4 u[NG][CH];
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
       row[g] = base + 4 * g + (lane >> 3);
       live[g] = false;
+      which_g[g] = 0;
+      src_off[g] = 0;
 #pragma unroll
       for (int c = 0; c < CH; ++c) u[g][c] = make_uint4(0u, 0u, 0u, 0u);
       if (row[g] < total) {
@@ -143,9 +163,11 @@ __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* 
         long long bh;
         norm_row<Idx>(row[g], rows_p, Tp, which, bh, t);
         live[g] = t < T;
+        which_g[g] = which;
+        src_off[g] = (bh * T + t) * D;
         if (live[g]) {
           const __nv_bfloat16* src = which == 0 ? a0 : which == 1 ? a1 : which == 2 ? a2 : a3;
-          const uint4* x = reinterpret_cast<const uint4*>(src + (bh * T + t) * D);
+          const uint4* x = reinterpret_cast<const uint4*>(src + src_off[g]);
 #pragma unroll
           for (int c = 0; c < CH; ++c)
             if (sub + 8 * c < D / 8) u[g][c] = x[sub + 8 * c];
@@ -160,17 +182,27 @@ __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* 
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
       acc += __shfl_xor_sync(0xffffffffu, acc, 2);
       acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-      if (sub == 0 && row[g] < total) inv[row[g]] = live[g] ? 1.0f / fmaxf(sqrtf(acc), 1e-12f) : 0.0f;
+      const float r = 1.0f / fmaxf(sqrtf(acc), 1e-12f);
+      if (sub == 0 && row[g] < total) inv[row[g]] = live[g] ? r : 0.0f;
+      if constexpr (WRITE_K) {
+        if (live[g] && (which_g[g] & 1)) {  // k1 or k2
+          uint4* y = reinterpret_cast<uint4*>(kn + (which_g[g] == 3 ? static_cast<long long>(BH) * T * D : 0LL) +
+                                              src_off[g]);
+#pragma unroll
+          for (int c = 0; c < CH; ++c)
+            if (sub + 8 * c < D / 8) y[sub + 8 * c] = scale_bf16x8(u[g][c], r);
+        }
+      }
     }
   }
 }
 
 // 32 scores of stream t -> 16 packed weights over the consumed score
-// columns.  With NORM the scores are scaled by rq * rk[col] (the normalisation
+// columns.  With NM = 1 the scores are scaled by rq * rk[col] (the normalisation
 // of row and key): x = s (rq rk) - tau in one packed multiply and one packed
 // fused multiply-add per key pair.
 // DIAG (compile time): the tile holds the diagonal, mask keys after the row.
-template <int PC, bool NORM, bool DIAG>
+template <int PC, int NM, bool DIAG>
 __device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t tS, int c0, const PowParams& wp,
                                              uint64_t rq2, uint64_t ntau2, const float (&rk)[32], int key0,
                                              int row) {
@@ -179,8 +211,10 @@ __device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t t
   for (int e = 0; e < 16; ++e) {
     const uint64_t s2 = f2_pack(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]));
     uint64_t x2;
-    if constexpr (NORM)
+    if constexpr (NM == 1)
       x2 = f2_fma(s2, f2_mul(rq2, f2_pack(rk[2 * e], rk[2 * e + 1])), ntau2);
+    else if constexpr (NM == 2)  // k already normalised: only the query's factor
+      x2 = f2_fma(s2, rq2, ntau2);
     else
       x2 = f2_sub(s2, wp.tau2);
     uint32_t w = weights2_x<PC>(x2, wp);
@@ -194,7 +228,7 @@ __device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t t
   tmem_st16(tS + c0 / 2, pk);
 }
 
-template <int D, int PC, bool NORM>
+template <int D, int PC, int NM>
 __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
     tra_diff_kernel(const __grid_constant__ CUtensorMap tmQ0, const __grid_constant__ CUtensorMap tmQ1,
                     const __grid_constant__ CUtensorMap tmK0, const __grid_constant__ CUtensorMap tmK1,
@@ -280,7 +314,7 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
       const CUtensorMap* maps[3] = {&tmK0, &tmK1, &tmV};
       int issued_rk = 0;
       for (int n = 0; n <= nmax && ok; ++n) {
-        if constexpr (NORM) {  // key factors of the k1 and k2 rows of key tile n
+        if constexpr (NM == 1) {  // key factors of the k1 and k2 rows of key tile n
           if (!(ok = mbar_wait(&rr.empty[rr.stage(n)], rr.phase(n) ^ 1))) break;
           mbar_arrive_expect_tx(&rr.full[rr.stage(n)], 2 * L::RK_BYTES);
           uint8_t* dst = smem + rr.off + rr.stage(n) * 2 * L::RK_BYTES;
@@ -368,7 +402,7 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
     const PowParams wp = pow_params(tau, p);
     const float lc = fminf(fmaxf(lam, 0.0f), 1.0f);
     // inv_norm: [q1 | k1 | q2 | k2] x [B*H] x [Tp], zero past T
-    const float rq = NORM ? inv_norm[(static_cast<long long>(t == 0 ? 0 : 2) * BH + bh) * Tp + row] : 1.0f;
+    const float rq = NM ? inv_norm[(static_cast<long long>(t == 0 ? 0 : 2) * BH + bh) * Tp + row] : 1.0f;
     const uint64_t rq2 = f2_pack(rq, rq), ntau2 = f2_pack(-tau, -tau);
     bool ok = true;
     for (int n = 0; n <= nmax; ++n) {
@@ -378,12 +412,12 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
       // Key normalisation factors of this tile (stream t's half of the stage).
       const float* rk_tile =
           reinterpret_cast<const float*>(smem + rr.off + rr.stage(n) * 2 * L::RK_BYTES + t * L::RK_BYTES);
-      if (NORM && !(ok = mbar_wait(&rr.full[rr.stage(n)], rr.phase(n)))) break;
+      if (NM == 1 && !(ok = mbar_wait(&rr.full[rr.stage(n)], rr.phase(n)))) break;
       // Four 32-column chunks; each chunk's scores are loaded while the
       // previous one is turned into weights (two buffers of 32 registers).
       auto quarter = [&](const uint32_t (&sv)[32], int c) {
         float rk[32];
-        if constexpr (NORM) {
+        if constexpr (NM == 1) {
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
             const float4 f = *reinterpret_cast<const float4*>(rk_tile + 32 * c + j);
@@ -394,9 +428,9 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
           }
         }
         if (diag)
-          diff_quarter<PC, NORM, true>(sv, tS, 32 * c, wp, rq2, ntau2, rk, n * BT, row);
+          diff_quarter<PC, NM, true>(sv, tS, 32 * c, wp, rq2, ntau2, rk, n * BT, row);
         else
-          diff_quarter<PC, NORM, false>(sv, tS, 32 * c, wp, rq2, ntau2, rk, n * BT, row);
+          diff_quarter<PC, NM, false>(sv, tS, 32 * c, wp, rq2, ntau2, rk, n * BT, row);
       };
       uint32_t sa[32], sb[32];
       tmem_ld32(tS, sa);
@@ -416,7 +450,7 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&p_full[t]);
-        if constexpr (NORM) mbar_arrive(&rr.empty[rr.stage(n)]);  // done with the key factors
+        if constexpr (NM == 1) mbar_arrive(&rr.empty[rr.stage(n)]);  // done with the key factors
       }
     }
     if (ok && mbar_wait(&o_full[0], 0) && mbar_wait(&o_full[1], 0)) {
@@ -454,11 +488,11 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
   }
 }
 
-template <int D, int PC, bool NORM>
+template <int D, int PC, int NM>
 int launch_diff_kernel(const CUtensorMap* maps, const float* inv, void* out, int BH, int T, float beta, float p,
                        float lam, int d_real, cudaStream_t stream) {
   using L = DiffLayout<D>;
-  auto kern = tra_diff_kernel<D, PC, NORM>;
+  auto kern = tra_diff_kernel<D, PC, NM>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
     return ERR_LAUNCH;
   const int nQ = (T + BT - 1) / BT;
@@ -472,23 +506,31 @@ int launch_diff_kernel(const CUtensorMap* maps, const float* inv, void* out, int
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
 
-template <int D, bool NORM>
+template <int D, int NM>
 int dispatch_pc(const CUtensorMap* maps, const float* inv, void* out, int BH, int T, float beta, float p, float lam,
                 int d_real, cudaStream_t stream) {
   const int pc = power_class(p);
-  if (pc == POW_TWO) return launch_diff_kernel<D, POW_TWO, NORM>(maps, inv, out, BH, T, beta, p, lam, d_real, stream);
-  if (pc == POW_ONE) return launch_diff_kernel<D, POW_ONE, NORM>(maps, inv, out, BH, T, beta, p, lam, d_real, stream);
-  return launch_diff_kernel<D, POW_GENERAL, NORM>(maps, inv, out, BH, T, beta, p, lam, d_real, stream);
+  if (pc == POW_TWO) return launch_diff_kernel<D, POW_TWO, NM>(maps, inv, out, BH, T, beta, p, lam, d_real, stream);
+  if (pc == POW_ONE) return launch_diff_kernel<D, POW_ONE, NM>(maps, inv, out, BH, T, beta, p, lam, d_real, stream);
+  return launch_diff_kernel<D, POW_GENERAL, NM>(maps, inv, out, BH, T, beta, p, lam, d_real, stream);
 }
 
 // Row-norm pre-pass at the head dim D (the real one).
 template <int D>
 void launch_row_norms(unsigned blocks, const __nv_bfloat16* a0, const __nv_bfloat16* a1, const __nv_bfloat16* a2,
-                      const __nv_bfloat16* a3, float* inv, int BH, int T, int Tp, bool idx32, cudaStream_t stream) {
-  if (idx32)
-    row_inv_norm_kernel<D, uint32_t><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv, BH, T, Tp);
-  else
-    row_inv_norm_kernel<D, unsigned long long><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv, BH, T, Tp);
+                      const __nv_bfloat16* a3, float* inv, __nv_bfloat16* kn, int BH, int T, int Tp, bool idx32,
+                      cudaStream_t stream) {
+  if (kn != nullptr) {
+    if (idx32)
+      row_inv_norm_kernel<D, uint32_t, true><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv, kn, BH, T, Tp);
+    else
+      row_inv_norm_kernel<D, unsigned long long, true><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv, kn, BH, T,
+                                                                                  Tp);
+  } else if (idx32) {
+    row_inv_norm_kernel<D, uint32_t, false><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv, kn, BH, T, Tp);
+  } else {
+    row_inv_norm_kernel<D, unsigned long long, false><<<blocks, 256, 0, stream>>>(a0, a1, a2, a3, inv, kn, BH, T, Tp);
+  }
 }
 
 }  // namespace
@@ -499,13 +541,17 @@ size_t tra_diff_scratch_bytes(int B, int H, int T) {
 }
 
 int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const void* k2, const void* v, void* out,
-                         int B, int H, int T, int D, float beta, float lam, float p, float* inv_norm,
+                         int B, int H, int T, int D, float beta, float lam, float p, float* inv_norm, void* knorm,
                          cudaStream_t stream) {
   if (D != 16 && D != 32 && D != 64 && D != 128) return ERR_UNSUPPORTED;
   const int BH = B * H;
   CUtensorMap maps[5];
   const uint64_t rs = static_cast<uint64_t>(D) * 2, hs = rs * T;
-  const void* src[5] = {q1, q2, k1, k2, v};
+  // with knorm, the kernel reads the normalised k copies the pre-pass writes there
+  const bool kn = inv_norm != nullptr && knorm != nullptr;
+  auto* kn1 = static_cast<__nv_bfloat16*>(knorm);
+  const void* src[5] = {q1, q2, kn ? static_cast<const void*>(kn1) : k1,
+                        kn ? static_cast<const void*>(kn1 + static_cast<size_t>(BH) * T * D) : k2, v};
   for (int i = 0; i < 5; ++i) {
     const int st = encode_tmap_3d(&maps[i], src[i], D, T, BH, rs, hs, 64, BT, 1);
     if (st != OK) return st;
@@ -523,20 +569,25 @@ int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const v
     const auto* a2 = static_cast<const __nv_bfloat16*>(q2);
     const auto* a3 = static_cast<const __nv_bfloat16*>(k2);
     const bool idx32 = rows < (1LL << 32);  // every row index (and the division by Tp) fits 32 bits
+    auto* kw = kn ? kn1 : nullptr;
     switch (D) {
-      case 128: launch_row_norms<128>(blocks, a0, a1, a2, a3, inv_norm, BH, T, Tp, idx32, stream); break;
-      case 64: launch_row_norms<64>(blocks, a0, a1, a2, a3, inv_norm, BH, T, Tp, idx32, stream); break;
-      case 32: launch_row_norms<32>(blocks, a0, a1, a2, a3, inv_norm, BH, T, Tp, idx32, stream); break;
-      default: launch_row_norms<16>(blocks, a0, a1, a2, a3, inv_norm, BH, T, Tp, idx32, stream); break;
+      case 128: launch_row_norms<128>(blocks, a0, a1, a2, a3, inv_norm, kw, BH, T, Tp, idx32, stream); break;
+      case 64: launch_row_norms<64>(blocks, a0, a1, a2, a3, inv_norm, kw, BH, T, Tp, idx32, stream); break;
+      case 32: launch_row_norms<32>(blocks, a0, a1, a2, a3, inv_norm, kw, BH, T, Tp, idx32, stream); break;
+      default: launch_row_norms<16>(blocks, a0, a1, a2, a3, inv_norm, kw, BH, T, Tp, idx32, stream); break;
     }
     if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
   }
-  if (D == 128)
-    return norm ? dispatch_pc<128, true>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream)
-                : dispatch_pc<128, false>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
+  const int nm = !norm ? 0 : kn ? 2 : 1;
+  if (D == 128) {
+    if (nm == 2) return dispatch_pc<128, 2>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
+    if (nm == 1) return dispatch_pc<128, 1>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
+    return dispatch_pc<128, 0>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
+  }
   // 64, and 16 or 32 at width 64 on zero-filled columns
-  return norm ? dispatch_pc<64, true>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream)
-              : dispatch_pc<64, false>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
+  if (nm == 2) return dispatch_pc<64, 2>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
+  if (nm == 1) return dispatch_pc<64, 1>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
+  return dispatch_pc<64, 0>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
 }
 
 // ------------------------------------------------ allocation-free entry point
@@ -575,12 +626,13 @@ bool tra_diff_noalloc_fits(int B, int H, int T) {
 int launch_tra_diff_noalloc_bf16(const void* q1, const void* q2, const void* k1, const void* k2, const void* v,
                                  void* out, int B, int H, int T, int D, float beta, float lam, float p,
                                  bool normalize, cudaStream_t stream) {
-  if (!normalize) return launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lam, p, nullptr, stream);
+  if (!normalize)
+    return launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lam, p, nullptr, nullptr, stream);
   if (!tra_diff_noalloc_fits(B, H, T)) return ERR_SCRATCH_LIMIT;
   float* scratch = nullptr;
   const int st = noalloc_scratch(&scratch);
   if (st != OK) return st;
-  return launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lam, p, scratch, stream);
+  return launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lam, p, scratch, nullptr, stream);
 }
 
 unsigned int tra_diff_device_error() { return read_and_clear_device_error(); }

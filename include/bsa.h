@@ -248,12 +248,16 @@ BSA_API int tra_backward_ex(const void* q, const void* k, const void* v,
  * runs both score streams on the same query tile and shares each V tile;
  * each stream accumulates its P.V product in fp32 and the two are combined
  * (first minus clamp(lambda, 0, 1) times second) before the bf16 store.
- * With normalize (bf16), a pre-pass kernel first computes 1/max(||row||, 1e-12) of every row of q1,
- * k1, q2, k2 into a temporary of 16 * B * H * Tp bytes (Tp = T rounded up to
- * a multiple of 128) taken with cudaMallocFromPoolAsync on `stream` and
- * returned with cudaFreeAsync on `stream`, from a memory pool the library
- * creates on the device at first use (it keeps up to 1 GiB of freed
- * temporaries mapped; the caller's default pool is not touched); without
+ * With normalize (bf16), a pre-pass kernel first computes 1/max(||row||, 1e-12)
+ * of every row of q1, k1, q2, k2 and writes bf16 copies of k1 and k2 with
+ * their rows normalised (as the page normalises q and k before its kernel);
+ * the kernel then reads those copies and scales each score by its query
+ * row's factor.  Both go to a temporary of 16 * B * H * Tp + 4 * B * H * T * D
+ * bytes (Tp = T rounded up to a multiple of 128; the factors rounded up to 256
+ * bytes) taken with cudaMallocFromPoolAsync on `stream` and returned with
+ * cudaFreeAsync on `stream`, from a memory pool the library creates on the
+ * device at first use (it keeps up to 1 GiB of freed temporaries mapped; the
+ * caller's default pool is not touched); without
  * normalize nothing is allocated.  BSA_F32 runs one CUDA-core kernel that
  * folds the two row norms into each score (q.k times both reciprocals) and
  * allocates nothing in either mode.
@@ -281,12 +285,18 @@ BSA_API int tra_diff_forward(const void* q1, const void* q2, const void* k1,
  * callers that cannot allocate device memory from inside the call: code whose
  * device memory is owned by its own allocator (a framework that reserves the
  * GPU up front and accounts for every byte), or code on a latency-critical
- * path that must not wait on the CUDA allocator.  It computes exactly what
- * tra_diff_forward computes, with the same arguments, rules and errors, but
- * the row normalisation factors go to a fixed scratch array that the library
+ * path that must not wait on the CUDA allocator.  It computes the same map
+ * as tra_diff_forward, with the same arguments, rules and errors, but the
+ * row normalisation factors go to a fixed scratch array that the library
  * holds in device memory (16 MiB on every GPU that loads the library, until
- * the process exits) instead of a temporary from a memory pool.  It calls
- * no cudaMalloc, cudaFree or other allocating routine.
+ * the process exits) instead of a temporary from a memory pool, and there is
+ * no room there for normalised copies of k1 and k2: with normalize the
+ * kernel scales each score by the key row's factor as well as the query
+ * row's, in fp32, instead of reading keys normalised and rounded to bf16.
+ * So with normalize the two entry points agree within bf16 rounding, not
+ * bit for bit (each is bit-repeatable on its own); without normalize they
+ * run the same kernel and agree exactly.  It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
  *
  * Limit: with normalize != 0 the problem must satisfy
  *   B * H * Tp <= 1,048,576   (Tp = T rounded up to a multiple of 128);

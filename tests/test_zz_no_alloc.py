@@ -6,8 +6,10 @@ that must not wait on the CUDA allocator.  For them the library offers a
 variant of the differential forward whose scratch (the row normalisation
 factors) lives in a fixed device array held by the library.  These tests call
 it through the C ABI, on buffers the test itself owns, and compare its output
-with the regular entry point's, on two calls in a row (the second call reuses
-the array the first one left filled).  The file is collected last on purpose.
+with the regular entry point's and the float64 oracle's, on two calls in a
+row (the second call reuses the array the first one left filled); without
+normalisation the two entry points run the same kernel and must agree bit for
+bit.  The file is collected last on purpose.
 """
 
 import numpy as np
@@ -49,23 +51,29 @@ def _noalloc(ts, out, beta, lam, p, normalize=True):
 
 @pytest.mark.parametrize("shape,beta,lam,p", [((1, 2, 384, 128), 0.0, 0.5, 2.0), ((2, 2, 300, 64), 0.1, 0.7, 1.5)])
 def test_noalloc_matches_regular_entry_point_twice(shape, beta, lam, p):
-    # Both entry points run the same pre-pass and the same kernel on the same
-    # factors; only where the factors live differs, so the outputs must agree
-    # bit for bit -- on the first call and on the second, which finds the
-    # array filled by the first.
+    # With normalisation the regular entry point reads keys normalised and
+    # rounded to bf16 (from its pool temporary), the allocation-free one folds
+    # the key factors into the scores in fp32 (its fixed array holds only the
+    # factors): both within the bf16 bar of the float64 oracle and of each
+    # other, each bit-repeatable -- on the first call and on the second, which
+    # finds the array filled by the first.
     for call, seed in enumerate((11, 12)):  # two calls in a row, different data
         ts = _inputs(*shape, seed=seed + 7 * shape[2])
         want = bsa.tra_diff_forward(*ts, beta, lam, p, normalize=True)
         out = torch.full_like(ts[0], float("nan"))
         assert _noalloc(ts, out, beta, lam, p) == 0
+        again = torch.full_like(ts[0], float("nan"))
+        assert _noalloc(ts, again, beta, lam, p) == 0
         torch.cuda.synchronize()
-        assert torch.equal(out, want), f"call {call}: differs from tra_diff_forward"
-        if call == 1:
-            # and against the float64 oracle, within the bf16 bar
-            h = [t.double().cpu().numpy() for t in ts]
-            ref = otra.tra_diff_forward(*h, beta, lam, p, normalize=True)
-            err = float(np.abs(out.double().cpu().numpy() - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
-            assert err <= TOL, f"max err {err:.3e} of max|ref|"
+        assert torch.equal(out, again), f"call {call}: not repeatable"
+        h = [t.double().cpu().numpy() for t in ts]
+        ref = otra.tra_diff_forward(*h, beta, lam, p, normalize=True)
+        scale = max(float(np.abs(ref).max()), 1e-30)
+        for name, got in (("noalloc", out), ("regular", want)):
+            err = float(np.abs(got.double().cpu().numpy() - ref).max()) / scale
+            assert err <= TOL, f"call {call}, {name}: max err {err:.3e} of max|ref|"
+        gap = float((out.double() - want.double()).abs().max()) / scale
+        assert gap <= TOL, f"call {call}: the two entry points differ by {gap:.3e} of max|ref|"
 
 
 def test_noalloc_without_normalisation_and_limit():
