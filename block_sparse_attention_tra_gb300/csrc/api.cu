@@ -281,20 +281,17 @@ int tra_diff_forward(const void* q1, const void* q2, const void* k1, const void*
                                normalize != 0, stream);
   if (!normalize)
     return launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, nullptr, nullptr, stream);
-  // Normalisation factors of every row of q1, k1, q2, k2 (T padded to a
-  // multiple of 128) and normalised copies of k1 and k2: one stream-ordered
-  // temporary, released on the same stream.
-  float* inv = nullptr;
-  const size_t nbytes = (tra_diff_scratch_bytes(B, H, T) + 255) / 256 * 256;
-  const size_t bytes = nbytes + 2 * sizeof(uint16_t) * static_cast<size_t>(B) * H * T * D;
+  // Normalised copies of k1 and k2 (the kernel takes the query rows' factors
+  // from its resident Q tiles): a stream-ordered temporary, released on the
+  // same stream.
+  void* kn = nullptr;
+  const size_t bytes = 2 * sizeof(uint16_t) * static_cast<size_t>(B) * H * T * D;
   int dev = 0;
   cudaMemPool_t pool = cudaGetDevice(&dev) == cudaSuccess ? scratch_pool(dev) : nullptr;
   if (pool == nullptr) return BSA_ERR_MEMORY;
-  if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&inv), bytes, pool, stream) != cudaSuccess)
-    return BSA_ERR_MEMORY;
-  const int st = launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, inv,
-                                      reinterpret_cast<uint8_t*>(inv) + nbytes, stream);
-  if (cudaFreeAsync(inv, stream) != cudaSuccess && st == OK) return BSA_ERR_MEMORY;
+  if (cudaMallocFromPoolAsync(&kn, bytes, pool, stream) != cudaSuccess) return BSA_ERR_MEMORY;
+  const int st = launch_tra_diff_bf16(q1, q2, k1, k2, v, out, B, H, T, D, beta, lambda, p, nullptr, kn, stream);
+  if (cudaFreeAsync(kn, stream) != cudaSuccess && st == OK) return BSA_ERR_MEMORY;
   return st;
 }
 

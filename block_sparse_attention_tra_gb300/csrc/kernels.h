@@ -73,10 +73,11 @@ int launch_tra_diff_f32(const float* q1, const float* q2, const float* k1, const
 // Threshold differential attention (fused two-stream kernel).  inv_norm is a
 // float scratch buffer of tra_diff_scratch_bytes(B, H, T) bytes (256-byte
 // aligned) for the row normalisation factors, or null to skip the
-// normalisation.  knorm (with inv_norm; 16-byte aligned, 2*B*H*T*D bf16) or
-// null: where the pre-pass writes normalised copies of k1 and k2 for the
-// kernel to read, leaving it only the query rows' factor to apply; without it
-// the kernel scales every score by both factors.
+// normalisation.  knorm (16-byte aligned, 2*B*H*T*D bf16) or null: where the
+// pre-pass writes normalised copies of k1 and k2 for the kernel to read; the
+// kernel then takes the query rows' factors from its Q tiles and inv_norm is
+// not used (it may be null).  Without knorm (and with inv_norm) the kernel
+// scales every score by both rows' factors from inv_norm.
 size_t tra_diff_scratch_bytes(int B, int H, int T);
 int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const void* k2, const void* v, void* out,
                          int B, int H, int T, int D, float beta, float lam, float p, float* inv_norm, void* knorm,

@@ -125,9 +125,10 @@ __device__ __forceinline__ uint4 scale_bf16x8(const uint4& u, float r) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// WRITE_K: the k1 and k2 rows (inputs 1 and 3) are also written normalised,
-// x / max(||x||, 1e-12) rounded to bf16 -- the page normalises q and k before
-// its kernel, in the input dtype -- into kn (k1 at kn, k2 at kn + B*H*T*D).
+// WRITE_K: only the k1 and k2 rows (inputs 1 and 3) are visited, and written
+// normalised, x / max(||x||, 1e-12) rounded to bf16 -- the page normalises q
+// and k before its kernel, in the input dtype -- into kn (k1 at kn, k2 at
+// kn + B*H*T*D); no factors are written (inv unused).
 template <int D, typename Idx, bool WRITE_K>
 __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* __restrict__ a0,
                                                            const __nv_bfloat16* __restrict__ a1,
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* 
   constexpr int NG = NORM_NG;
   const int lane = threadIdx.x & 31, sub = lane & 7;
   const long long rows_p = static_cast<long long>(BH) * Tp;
-  const long long total = 4 * rows_p;
+  const long long total = (WRITE_K ? 2 : 4) * rows_p;
   const long long warp0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   for (long long base = warp0 * 4 * NG; base < total; base += nwarps * 4 * NG) {
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* 
         int which, t;
         long long bh;
         norm_row<Idx>(row[g], rows_p, Tp, which, bh, t);
+        if constexpr (WRITE_K) which = 2 * which + 1;  // k1 or k2
         live[g] = t < T;
         which_g[g] = which;
         src_off[g] = (bh * T + t) * D;
@@ -183,9 +185,10 @@ __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* 
       acc += __shfl_xor_sync(0xffffffffu, acc, 2);
       acc += __shfl_xor_sync(0xffffffffu, acc, 4);
       const float r = 1.0f / fmaxf(sqrtf(acc), 1e-12f);
-      if (sub == 0 && row[g] < total) inv[row[g]] = live[g] ? r : 0.0f;
-      if constexpr (WRITE_K) {
-        if (live[g] && (which_g[g] & 1)) {  // k1 or k2
+      if constexpr (!WRITE_K) {
+        if (sub == 0 && row[g] < total) inv[row[g]] = live[g] ? r : 0.0f;
+      } else {
+        if (live[g]) {
           uint4* y = reinterpret_cast<uint4*>(kn + (which_g[g] == 3 ? static_cast<long long>(BH) * T * D : 0LL) +
                                               src_off[g]);
 #pragma unroll
@@ -401,11 +404,27 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
     const uint32_t tS = lane_base + t * BT;
     const PowParams wp = pow_params(tau, p);
     const float lc = fminf(fmaxf(lam, 0.0f), 1.0f);
-    // inv_norm: [q1 | k1 | q2 | k2] x [B*H] x [Tp], zero past T
-    const float rq = NM ? inv_norm[(static_cast<long long>(t == 0 ? 0 : 2) * BH + bh) * Tp + row] : 1.0f;
-    const uint64_t rq2 = f2_pack(rq, rq), ntau2 = f2_pack(-tau, -tau);
+    // Query factor: NM = 1 reads it from inv_norm ([q1 | k1 | q2 | k2] x
+    // [B*H] x [Tp], zero past T); NM = 2 sums the squares of this thread's row
+    // of the resident Q_t tile (once, before the MMA stream), as the pre-pass
+    // does for the keys.
+    float rq = 1.0f;
     bool ok = true;
-    for (int n = 0; n <= nmax; ++n) {
+    if constexpr (NM == 1) rq = inv_norm[(static_cast<long long>(t == 0 ? 0 : 2) * BH + bh) * Tp + row];
+    if constexpr (NM == 2) {
+      ok = mbar_wait(q_full, 0);
+      const int r = wq * 32 + lane;
+      float acc = 0.0f;
+#pragma unroll
+      for (int pnl = 0; pnl < D / 64; ++pnl)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          acc += sumsq_bf16x8(*reinterpret_cast<const uint4*>(smem + L::Q_OFF + t * L::TILE + pnl * PANEL_BYTES +
+                                                               r * 128 + ((k ^ (r & 7)) << 4)));
+      rq = 1.0f / fmaxf(sqrtf(acc), 1e-12f);
+    }
+    const uint64_t rq2 = f2_pack(rq, rq), ntau2 = f2_pack(-tau, -tau);
+    for (int n = 0; n <= nmax && ok; ++n) {
       if (!(ok = mbar_wait(&s_full[t], n & 1))) break;
       tc_fence_after();
       const bool diag = (n == nmax);
@@ -548,7 +567,7 @@ int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const v
   CUtensorMap maps[5];
   const uint64_t rs = static_cast<uint64_t>(D) * 2, hs = rs * T;
   // with knorm, the kernel reads the normalised k copies the pre-pass writes there
-  const bool kn = inv_norm != nullptr && knorm != nullptr;
+  const bool kn = knorm != nullptr;
   auto* kn1 = static_cast<__nv_bfloat16*>(knorm);
   const void* src[5] = {q1, q2, kn ? static_cast<const void*>(kn1) : k1,
                         kn ? static_cast<const void*>(kn1 + static_cast<size_t>(BH) * T * D) : k2, v};
@@ -556,10 +575,10 @@ int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const v
     const int st = encode_tmap_3d(&maps[i], src[i], D, T, BH, rs, hs, 64, BT, 1);
     if (st != OK) return st;
   }
-  const bool norm = inv_norm != nullptr;
+  const bool norm = inv_norm != nullptr || kn;
   if (norm) {
     const int Tp = ((T + BT - 1) / BT) * BT;
-    const long long rows = 4LL * BH * Tp;  // 32 * NORM_NG rows per 256-thread block per pass
+    const long long rows = (kn ? 2LL : 4LL) * BH * Tp;  // 32 * NORM_NG rows per 256-thread block per pass
     const int sms = sm_count();
     if (sms <= 0) return ERR_DEVICE;
     const long long want = (rows + 32 * NORM_NG - 1) / (32 * NORM_NG), cap = 8LL * sms;

@@ -248,13 +248,12 @@ BSA_API int tra_backward_ex(const void* q, const void* k, const void* v,
  * runs both score streams on the same query tile and shares each V tile;
  * each stream accumulates its P.V product in fp32 and the two are combined
  * (first minus clamp(lambda, 0, 1) times second) before the bf16 store.
- * With normalize (bf16), a pre-pass kernel first computes 1/max(||row||, 1e-12)
- * of every row of q1, k1, q2, k2 and writes bf16 copies of k1 and k2 with
- * their rows normalised (as the page normalises q and k before its kernel);
- * the kernel then reads those copies and scales each score by its query
- * row's factor.  Both go to a temporary of 16 * B * H * Tp + 4 * B * H * T * D
- * bytes (Tp = T rounded up to a multiple of 128; the factors rounded up to 256
- * bytes) taken with cudaMallocFromPoolAsync on `stream` and returned with
+ * With normalize (bf16), a pre-pass kernel first writes bf16 copies of k1
+ * and k2 with their rows normalised (as the page normalises q and k before
+ * its kernel), into a temporary of 4 * B * H * T * D bytes; the kernel reads
+ * those copies and scales each score by 1/max(||q_i||, 1e-12), which it
+ * computes from its own query tile.  The temporary is
+ * taken with cudaMallocFromPoolAsync on `stream` and returned with
  * cudaFreeAsync on `stream`, from a memory pool the library creates on the
  * device at first use (it keeps up to 1 GiB of freed temporaries mapped; the
  * caller's default pool is not touched); without
