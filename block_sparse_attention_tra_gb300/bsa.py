@@ -108,6 +108,8 @@ def open_library(path):
     lib.bsa_selftest_wait_timeout.restype = i32
     lib.bsa_selftest_log2.argtypes = [vp, vp, vp, i32, vp]
     lib.bsa_selftest_log2.restype = i32
+    lib.bsa_selftest_exp2.argtypes = [vp, vp, vp, i32, vp]
+    lib.bsa_selftest_exp2.restype = i32
     lib.bsa_read_probe.argtypes = [vp, ctypes.c_size_t, i32, vp, vp]
     lib.bsa_read_probe.restype = i32
     return lib
@@ -424,6 +426,19 @@ def selftest_log2(x, stream=None):
     _check(load_library().bsa_selftest_log2(x.data_ptr(), y_fma.data_ptr(), y_ref.data_ptr(), x.numel(),
                                             _stream_handle(stream)), "bsa_selftest_log2")
     return y_fma, y_ref
+
+
+def selftest_exp2(y, stream=None):
+    """The epilogue's FMA-pipe exp2 (fp32, before the bf16 rounding) and
+    CUDA's exp2f on the same float32 device tensor; returns ``(w_fma, w_ref)``."""
+    import torch
+
+    if not (y.is_cuda and y.dtype == torch.float32 and y.is_contiguous()):
+        raise BsaError("selftest_exp2 needs a contiguous float32 CUDA tensor")
+    w_fma, w_ref = torch.empty_like(y), torch.empty_like(y)
+    _check(load_library().bsa_selftest_exp2(y.data_ptr(), w_fma.data_ptr(), w_ref.data_ptr(), y.numel(),
+                                            _stream_handle(stream)), "bsa_selftest_exp2")
+    return w_fma, w_ref
 
 
 def read_probe(buf, reps: int, sink, stream=None):

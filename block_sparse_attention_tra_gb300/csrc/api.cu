@@ -385,6 +385,17 @@ int bsa_selftest_log2(const float* x, float* y_fma, float* y_ref, int n, cudaStr
   return launch_selftest_log2(x, y_fma, y_ref, n, stream);
 }
 
+int bsa_selftest_exp2(const float* y, float* w_fma, float* w_ref, int n, cudaStream_t stream) {
+  if (y == nullptr || w_fma == nullptr || w_ref == nullptr) return BSA_ERR_NULLPTR;
+  if (n < 1) return BSA_ERR_SHAPE;
+  const uintptr_t mis = (reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(w_fma) |
+                         reinterpret_cast<uintptr_t>(w_ref)) & 3u;
+  if (mis != 0) return BSA_ERR_ALIGN;
+  const int dv = check_device();
+  if (dv != OK) return dv;
+  return launch_selftest_exp2(y, w_fma, w_ref, n, stream);
+}
+
 int bsa_read_probe(const void* buf, size_t bytes, int reps, unsigned int* sink, cudaStream_t stream) {
   if (buf == nullptr || sink == nullptr) return BSA_ERR_NULLPTR;
   if (bytes < 16 || bytes % 16 != 0 || bytes > (1ull << 40) || reps < 1 || reps > 100000) return BSA_ERR_SHAPE;

@@ -121,6 +121,7 @@ int launch_nsa_fsa(const void* q, const void* k, const void* v, const int32_t* b
 // beside CUDA's log2f.
 int launch_selftest_wait_timeout(long long limit_cycles, int* result, cudaStream_t stream);
 int launch_selftest_log2(const float* x, float* y_fma, float* y_ref, int n, cudaStream_t stream);
+int launch_selftest_exp2(const float* y, float* w_fma, float* w_ref, int n, cudaStream_t stream);
 // Streaming read of a device buffer `reps` times (L2 / HBM read-rate probe).
 int launch_read_probe(const void* buf, long long bytes, int reps, unsigned int* sink, cudaStream_t stream);
 

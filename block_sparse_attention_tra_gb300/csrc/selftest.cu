@@ -6,8 +6,9 @@
 //    (ptx.cuh, mbar_wait_bounded): one thread waits, with a short limit, on an
 //    mbarrier that nothing arrives on; no TMA copy or tcgen05 operation is in
 //    flight, so the kernel simply records the timeout code and returns;
-//  * the FMA-pipe log2 of the general-power epilogue (tra_math.cuh,
-//    p_log2_fma), evaluated beside CUDA's own log2f on the same inputs.
+//  * the FMA-pipe log2 and exp2 of the general-power epilogue (tra_math.cuh,
+//    p_log2_fma and exp2_fma2), evaluated beside CUDA's own log2f and exp2f
+//    on the same inputs.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tra_math.cuh"
@@ -43,6 +44,23 @@ __global__ void log2_compare_kernel(const float* __restrict__ x, float* __restri
     if (i2 + 1 < n) {
       y_fma[i2 + 1] = y1;
       y_ref[i2 + 1] = log2f(x1);
+    }
+  }
+}
+
+// w_fma[i] = exp2(y[i]) from the epilogue's FMA-pipe evaluation (before its
+// bf16 rounding); w_ref[i] = CUDA's exp2f(y[i]).
+__global__ void exp2_compare_kernel(const float* __restrict__ y, float* __restrict__ w_fma,
+                                    float* __restrict__ w_ref, int n) {
+  for (int i2 = 2 * (blockIdx.x * blockDim.x + threadIdx.x); i2 < n; i2 += 2 * gridDim.x * blockDim.x) {
+    const float y0 = y[i2], y1 = (i2 + 1 < n) ? y[i2 + 1] : 0.0f;
+    float w0, w1;
+    f2_unpack(exp2_fma2(f2_pack(y0, y1)), w0, w1);
+    w_fma[i2] = w0;
+    w_ref[i2] = exp2f(y0);
+    if (i2 + 1 < n) {
+      w_fma[i2 + 1] = w1;
+      w_ref[i2 + 1] = exp2f(y1);
     }
   }
 }
@@ -94,6 +112,13 @@ int launch_selftest_log2(const float* x, float* y_fma, float* y_ref, int n, cuda
   const int threads = 256;
   const int blocks = static_cast<int>(((n + 1) / 2 + threads - 1) / threads);
   log2_compare_kernel<<<blocks < 1024 ? (blocks > 0 ? blocks : 1) : 1024, threads, 0, stream>>>(x, y_fma, y_ref, n);
+  return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
+}
+
+int launch_selftest_exp2(const float* y, float* w_fma, float* w_ref, int n, cudaStream_t stream) {
+  const int threads = 256;
+  const int blocks = static_cast<int>(((n + 1) / 2 + threads - 1) / threads);
+  exp2_compare_kernel<<<blocks < 1024 ? (blocks > 0 ? blocks : 1) : 1024, threads, 0, stream>>>(y, w_fma, w_ref, n);
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;
 }
 

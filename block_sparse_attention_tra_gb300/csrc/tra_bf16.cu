@@ -43,6 +43,18 @@ constexpr int BM = tile::ROWS;          // query rows per tile
 constexpr int BN = tile::ROWS;          // keys per tile
 constexpr uint32_t TMEM_COLS = 512;
 
+// The weights of pair e (0 .. 15) of a quarter, two raw fp32 scores: the
+// units each pair's log2 and exp2 run on are fixed at compile time by the
+// plan (the loops that call this are unrolled).
+template <int PC, int PLAN>
+__device__ __forceinline__ uint32_t mix_weights2(int e, uint32_t s0, uint32_t s1, const PowParams& wp) {
+  if (PC == POW_GENERAL_MIX && mix_pair_on_fma<PLAN>(e))
+    return weights2<PC, true>(__uint_as_float(s0), __uint_as_float(s1), wp);
+  if (PC == POW_GENERAL_MIX && mix_exp_on_fma<PLAN>(e))
+    return weights2<PC, false, true>(__uint_as_float(s0), __uint_as_float(s1), wp);
+  return weights2<PC, false>(__uint_as_float(s0), __uint_as_float(s1), wp);
+}
+
 // 32 scores (tile columns c0 .. c0+31) -> 16 packed weights, stored to TMEM
 // columns c0/2 .. c0/2+15 of the same buffer (already-consumed scores).
 // DIAG: the tile holds the diagonal, mask keys after the row (a compile-time
@@ -54,9 +66,7 @@ __device__ __forceinline__ void epilogue_quarter(const uint32_t (&s)[32], uint32
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     // (unrolled: the choice of log2 unit per pair is made at compile time)
-    uint32_t w = (PC == POW_GENERAL_MIX && mix_pair_on_fma<MUFU_PAIRS>(e))
-                     ? weights2<PC, true>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp)
-                     : weights2<PC, false>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp);
+    uint32_t w = mix_weights2<PC, MUFU_PAIRS>(e, s[2 * e], s[2 * e + 1], wp);
     if constexpr (DIAG) {
       const int key = key0 + c0 + 2 * e;  // keys key, key + 1
       if (key > row) w = 0u;
@@ -77,9 +87,7 @@ __device__ __forceinline__ void epilogue_eighth(const uint32_t (&s)[16], uint32_
   uint32_t pk[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    uint32_t w = (PC == POW_GENERAL_MIX && mix_pair_on_fma<MUFU_PAIRS>(e0 + e))
-                     ? weights2<PC, true>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp)
-                     : weights2<PC, false>(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]), wp);
+    uint32_t w = mix_weights2<PC, MUFU_PAIRS>(e0 + e, s[2 * e], s[2 * e + 1], wp);
     if constexpr (DIAG) {
       const int key = key0 + c0 + 2 * e;
       if (key > row) w = 0u;

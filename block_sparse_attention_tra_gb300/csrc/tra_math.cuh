@@ -11,7 +11,10 @@
 // one LOP3), log2 m from a degree-5 minimax polynomial (Remez exchange fit,
 // block_sparse_attention_tra_gb300/log2_poly.py; max error 1.6e-5 evaluated
 // in float32) by Horner's rule on packed f32x2 FMAs, with p folded into the
-// coefficients.  exp2 stays on MUFU for every score.
+// coefficients.  A smaller share takes exp2 off MUFU as well (exp2_fma):
+// n = round(y), f = y - n, 2^f from a degree-4 minimax polynomial (Remez
+// exchange on the relative error, exp2_poly.py), the exponent raised by n
+// with one integer add.
 #pragma once
 
 #include "kernels.h"
@@ -39,6 +42,13 @@ __device__ __forceinline__ float lg2_approx(float x) {
 __device__ __forceinline__ uint32_t relu_pack(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.relu.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// max(w, 0) per bf16 half; a NaN half gives 0 (max returns the operand that
+// is not NaN).
+__device__ __forceinline__ uint32_t relu_nan_bf16x2(uint32_t w) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0u));
   return r;
 }
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
@@ -121,25 +131,87 @@ __device__ __forceinline__ uint64_t p_log2_fma(float x0, float x1, const PowPara
   return f2_fma(ef, w.p2, r);
 }
 
-// Which pairs of a 16-pair quarter take the FMA-pipe log2 under
-// POW_GENERAL_MIX: M of every 16 stay on MUFU lg2, spread evenly.  M is
-// chosen per head dim (measured on the T=8192 D=64 and the T=4096 D=128
+// exp2(y0), exp2(y1) on the FMA pipe (then rounded to bf16x2).  y is clamped to
+// [-127, 128]; t = y + 1.5 * 2^23 holds n = round(y) in its low mantissa bits
+// (round to nearest), f = y - (t - 1.5 * 2^23) lies in [-1/2, 1/2], and
+// 2^f ~= 1 + f (c1 + c2 f + c3 f^2 + c4 f^3): the Remez fit with p(0) = 1 of
+// block_sparse_attention_tra_gb300/exp2_poly.py (relative error 2.9e-6
+// evaluated in float32, against 2^-9 for the bf16 rounding that follows).
+// Adding t's bits shifted left by 23 adds n to the exponent field (the
+// constant part of t shifts out).  y = -127 (the ReLU's zeros, p >= 1) gives
+// the bits of +0.0 exactly and y = 128 those of +inf; between -127 and -126
+// the pattern is a small subnormal (the MUFU form flushes those to 0).
+#ifndef BSA_EXP2_DEG
+#define BSA_EXP2_DEG 4
+#endif
+#if BSA_EXP2_DEG == 4
+__device__ constexpr float EXP2_C[4] = {6.931241934e-01f, 2.402409861e-01f, 5.590642460e-02f, 9.582853096e-03f};
+#elif BSA_EXP2_DEG == 3
+__device__ constexpr float EXP2_C[3] = {6.932829271e-01f, 2.422109593e-01f, 5.500893113e-02f};  // 1.0e-4
+#else
+#error "BSA_EXP2_DEG must be 3 or 4"
+#endif
+constexpr float ROUND_MAGIC = 12582912.0f;  // 1.5 * 2^23
+__device__ __forceinline__ uint64_t exp2_fma2(uint64_t y2) {
+  float y0, y1;
+  f2_unpack(y2, y0, y1);
+  const uint64_t y = f2_pack(fminf(fmaxf(y0, -127.0f), 128.0f), fminf(fmaxf(y1, -127.0f), 128.0f));
+  const uint64_t magic = f2_pack(ROUND_MAGIC, ROUND_MAGIC);
+  const uint64_t t = f2_add(y, magic);
+  const uint64_t f = f2_sub(y, f2_sub(t, magic));
+  uint64_t r = f2_pack(EXP2_C[BSA_EXP2_DEG - 1], EXP2_C[BSA_EXP2_DEG - 1]);
+#pragma unroll
+  for (int k = BSA_EXP2_DEG - 2; k >= 0; --k) r = f2_fma(r, f, f2_pack(EXP2_C[k], EXP2_C[k]));
+  r = f2_fma(r, f, f2_pack(1.0f, 1.0f));
+  float r0, r1, t0, t1;
+  f2_unpack(r, r0, r1);
+  f2_unpack(t, t0, t1);
+  return f2_pack(__uint_as_float(__float_as_uint(r0) + (__float_as_uint(t0) << 23)),
+                 __uint_as_float(__float_as_uint(r1) + (__float_as_uint(t1) << 23)));
+}
+__device__ __forceinline__ uint32_t exp2_fma_bf16x2(uint64_t y2) {
+  float w0, w1;
+  f2_unpack(exp2_fma2(y2), w0, w1);
+  return pack_bf16x2(w0, w1);
+}
+
+// Which units each pair of a 16-pair quarter uses under POW_GENERAL_MIX, as a
+// plan MUFU_LOG + 32 EXP_FMA: MUFU_LOG of every 16 pairs take MUFU lg2 (the
+// rest the FMA-pipe log2), and EXP_FMA of those MUFU_LOG pairs take the
+// FMA-pipe exp2 (the rest MUFU ex2), each share spread evenly.  The shares
+// are chosen per head dim (measured on the T=8192 D=64 and the T=4096 D=128
 // p = 1.5 workloads with two epilogue warpgroups per query tile); more
 // FMA-pipe pairs than that are slower, since the packed f32x2 FMAs, LOP3 and
-// funnel shifts of the polynomial path all run at half rate.
+// funnel shifts of the polynomial paths all run at half rate.
 #ifndef BSA_MIX_MUFU_PAIRS_D64
 #define BSA_MIX_MUFU_PAIRS_D64 10
 #endif
 #ifndef BSA_MIX_MUFU_PAIRS_D128
 #define BSA_MIX_MUFU_PAIRS_D128 10
 #endif
+#ifndef BSA_MIX_EXP_FMA_PAIRS_D64
+#define BSA_MIX_EXP_FMA_PAIRS_D64 0
+#endif
+#ifndef BSA_MIX_EXP_FMA_PAIRS_D128
+#define BSA_MIX_EXP_FMA_PAIRS_D128 0
+#endif
 template <int D>
 __host__ __device__ constexpr int mix_mufu_pairs() {
-  return D == 64 ? BSA_MIX_MUFU_PAIRS_D64 : BSA_MIX_MUFU_PAIRS_D128;
+  return D == 64 ? BSA_MIX_MUFU_PAIRS_D64 + 32 * BSA_MIX_EXP_FMA_PAIRS_D64
+                 : BSA_MIX_MUFU_PAIRS_D128 + 32 * BSA_MIX_EXP_FMA_PAIRS_D128;
 }
-template <int M>
+template <int PLAN>
 __host__ __device__ constexpr bool mix_pair_on_fma(int e) {
+  constexpr int M = PLAN % 32;
   return ((e % 16) * M) % 16 >= M;
+}
+template <int PLAN>
+__host__ __device__ constexpr bool mix_exp_on_fma(int e) {
+  constexpr int M = PLAN % 32, E = PLAN / 32;
+  if (E == 0 || mix_pair_on_fma<PLAN>(e)) return false;
+  int k = 0;  // rank of pair e among the MUFU-log2 pairs
+  for (int j = 0; j < e % 16; ++j) k += mix_pair_on_fma<PLAN>(j) ? 0 : 1;
+  return (k * E) % M < E;
 }
 
 // p = 2: round x to bf16 and square in bf16 (0: two roundings, at most ~1.5
@@ -152,8 +224,9 @@ __host__ __device__ constexpr bool mix_pair_on_fma(int e) {
 #endif
 
 // Weights of two adjacent keys from x = s - tau (packed): ReLU(x)^p, bf16x2.
-// FMA_LOG2 (POW_GENERAL_MIX only): this pair's log2 runs on the FMA pipe.
-template <int PC, bool FMA_LOG2 = false>
+// FMA_LOG2, FMA_EXP2 (POW_GENERAL_MIX only): this pair's log2, exp2 runs on
+// the FMA pipe.
+template <int PC, bool FMA_LOG2 = false, bool FMA_EXP2 = false>
 __device__ __forceinline__ uint32_t weights2_x(uint64_t x2, const PowParams& w) {
   float x0, x1;
   f2_unpack(x2, x0, x1);
@@ -169,16 +242,24 @@ __device__ __forceinline__ uint32_t weights2_x(uint64_t x2, const PowParams& w) 
     return mul_bf16x2(h, h);
 #endif
   } else if constexpr (PC == POW_GENERAL_MIX) {
-    x0 = fmaxf(x0, 0.0f);
-    x1 = fmaxf(x1, 0.0f);
-    uint64_t y;
-    if constexpr (FMA_LOG2)
-      y = p_log2_fma(x0, x1, w);
-    else
-      y = f2_mul(f2_pack(lg2_approx(x0), lg2_approx(x1)), w.p2);
-    float y0, y1;
-    f2_unpack(y, y0, y1);
-    return pack_bf16x2(ex2_approx(y0), ex2_approx(y1));
+    if constexpr (FMA_LOG2) {
+      // the exponent and mantissa fields need x >= 0
+      const uint64_t y = p_log2_fma(fmaxf(x0, 0.0f), fmaxf(x1, 0.0f), w);
+      if constexpr (FMA_EXP2) return exp2_fma_bf16x2(y);
+      float y0, y1;
+      f2_unpack(y, y0, y1);
+      return pack_bf16x2(ex2_approx(y0), ex2_approx(y1));
+    } else {
+      // MUFU lg2 of x <= 0 is -inf (x = 0) or NaN (x < 0): exp2 gives 0 or
+      // NaN, and the ReLU is applied after the rounding to bf16 (max with 0,
+      // which maps NaN to 0) -- one instruction per pair instead of two.
+      // The FMA-pipe exp2 clamps its input, which also maps NaN to 0.
+      const uint64_t y = f2_mul(f2_pack(lg2_approx(x0), lg2_approx(x1)), w.p2);
+      if constexpr (FMA_EXP2) return exp2_fma_bf16x2(y);
+      float y0, y1;
+      f2_unpack(y, y0, y1);
+      return relu_nan_bf16x2(pack_bf16x2(ex2_approx(y0), ex2_approx(y1)));
+    }
   } else if constexpr (PC >= POW_HALF0 && PC <= POW_HALF3) {
     // p = k + 1/2: x^p = x^k sqrt(x), one MUFU operation per score; the
     // ReLU's zeros give sqrt(0) = 0 exactly.
@@ -192,20 +273,19 @@ __device__ __forceinline__ uint32_t weights2_x(uint64_t x2, const PowParams& w) 
     f2_unpack(r, r0, r1);
     return pack_bf16x2(r0, r1);
   } else {
-    // x^p = exp2(p log2 x); the ReLU's zeros give log2 = -inf and exp2 of it 0.
-    x0 = fmaxf(x0, 0.0f);
-    x1 = fmaxf(x1, 0.0f);
+    // x^p = exp2(p log2 x); lg2 of x = 0 is -inf (exp2 of it 0) and of x < 0
+    // NaN, which the ReLU after the bf16 rounding maps to 0.
     const uint64_t y = f2_mul(f2_pack(lg2_approx(x0), lg2_approx(x1)), w.p2);
     float y0, y1;
     f2_unpack(y, y0, y1);
-    return pack_bf16x2(ex2_approx(y0), ex2_approx(y1));
+    return relu_nan_bf16x2(pack_bf16x2(ex2_approx(y0), ex2_approx(y1)));
   }
 }
 
 // Weights of two adjacent keys from their scores: ReLU(s - tau)^p, bf16x2.
-template <int PC, bool FMA_LOG2 = false>
+template <int PC, bool FMA_LOG2 = false, bool FMA_EXP2 = false>
 __device__ __forceinline__ uint32_t weights2(float s0, float s1, const PowParams& w) {
-  return weights2_x<PC, FMA_LOG2>(f2_sub(f2_pack(s0, s1), w.tau2), w);
+  return weights2_x<PC, FMA_LOG2, FMA_EXP2>(f2_sub(f2_pack(s0, s1), w.tau2), w);
 }
 
 }  // namespace

@@ -453,10 +453,20 @@ BSA_API int bsa_device_error(void);
  * non-negative finite floats.  Errors: BSA_ERR_NULLPTR, BSA_ERR_SHAPE (n < 1),
  * BSA_ERR_ALIGN (a pointer not 4-byte aligned), BSA_ERR_DEVICE,
  * BSA_ERR_LAUNCH.
+ *
+ * bsa_selftest_exp2 -- for n floats y (device memory), writes the
+ * general-power epilogue's FMA-pipe exp2 (y clamped to [-127, 128], rounding
+ * to an integer n and a degree-4 minimax polynomial for 2^(y - n), the path
+ * POW_GENERAL_MIX uses for part of the scores) to w_fma, in fp32 before the
+ * epilogue's bf16 rounding, and CUDA's exp2f to w_ref.  y = -127 (and below)
+ * gives +0.0 exactly, y = 128 (and above) +inf.  Errors as for
+ * bsa_selftest_log2.
  */
 BSA_API int bsa_selftest_wait_timeout(long long limit_cycles, int* result,
                                       cudaStream_t stream);
 BSA_API int bsa_selftest_log2(const float* x, float* y_fma, float* y_ref,
+                              int n, cudaStream_t stream);
+BSA_API int bsa_selftest_exp2(const float* y, float* w_fma, float* w_ref,
                               int n, cudaStream_t stream);
 
 /*

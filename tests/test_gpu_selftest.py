@@ -5,8 +5,8 @@
   wait must give up, the library must report code 1 through
   bsa_device_error (and clear it on read), and the context must stay usable:
   a threshold-attention call right after it matches the oracle.
-* The FMA-pipe log2 of the general-power epilogue against CUDA's log2f on a
-  dense sweep of float32 inputs.
+* The FMA-pipe log2 and exp2 of the general-power epilogue against CUDA's
+  log2f and exp2f on dense sweeps of float32 inputs.
 """
 
 import numpy as np
@@ -66,3 +66,26 @@ def test_fma_log2_against_cuda_log2f():
     # x = 0 (the ReLU's zeros): -127, so exp2(p * it) flushes to 0 for p >= 1
     z, _ = bsa.selftest_log2(torch.zeros(2, dtype=torch.float32, device="cuda"))
     assert float(z.max()) <= -126.99
+
+
+def test_fma_exp2_against_cuda_exp2f():
+    # y over the whole normal range, the neighbourhood of 0 and the integers,
+    # then the clamped ends
+    r = np.random.default_rng(1)
+    y = np.concatenate([r.uniform(-126.0, 127.9, 1 << 20), np.linspace(-4.0, 4.0, 40001),
+                        np.arange(-126, 128, dtype=np.float64)]).astype(np.float32)
+    yt = torch.from_numpy(y).cuda()
+    w_fma, w_ref = bsa.selftest_exp2(yt)
+    torch.cuda.synchronize()
+    a, b = w_fma.double().cpu().numpy(), w_ref.double().cpu().numpy()
+    exact = np.exp2(y.astype(np.float64))
+    rel_ref = float(np.max(np.abs(a - b) / b))
+    rel_exact = float(np.max(np.abs(a - exact) / exact))
+    print(f"FMA-pipe exp2: max rel |fma - exp2f| = {rel_ref:.3e}, max rel |fma - exp2| = {rel_exact:.3e}")
+    # the polynomial's own bound (2.9e-6 in float32) plus exp2f's rounding
+    assert rel_exact <= 3.5e-6 and rel_ref <= 4e-6
+    ends = torch.tensor([-float("inf"), -1e4, -200.0, -127.0, 128.0, 1e4, float("inf")], device="cuda")
+    e, _ = bsa.selftest_exp2(ends)
+    e = e.cpu()
+    assert torch.all(e[:4] == 0.0) and not torch.any(torch.signbit(e[:4]))
+    assert torch.all(torch.isinf(e[4:])) and torch.all(e[4:] > 0)
