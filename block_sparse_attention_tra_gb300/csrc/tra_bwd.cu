@@ -296,6 +296,7 @@ __device__ __forceinline__ void bwd_dkdv_block(const CUtensorMap& tmQ, const CUt
     const int wq = warp & 3, grp = warp >> 2;  // TMEM lane quarter; chunk of each half (two warpgroups)
     const int r = wq * 32 + lane;              // key row within the tile
     const int key = n * BT + r;
+    const float lp = log2f(p);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     bool ok = true;
     for (int j = 0; j < nq && ok; ++j) {
@@ -326,8 +327,8 @@ __device__ __forceinline__ void bwd_dkdv_block(const CUtensorMap& tmQ, const CUt
           for (int e = 0; e < 16; ++e) {
             float w0, g0, w1, g1;
             const int i0 = 32 * c + 2 * e;  // query column within the tile
-            weight_and_grad<PC>(__uint_as_float(sv[2 * e]) - tau_m[i0], p, w0, g0);
-            weight_and_grad<PC>(__uint_as_float(sv[2 * e + 1]) - tau_m[i0 + 1], p, w1, g1);
+            weight_and_grad<PC>(__uint_as_float(sv[2 * e]) - tau_m[i0], p, lp, w0, g0);
+            weight_and_grad<PC>(__uint_as_float(sv[2 * e + 1]) - tau_m[i0 + 1], p, lp, w1, g1);
             float a0 = __uint_as_float(dp[2 * e]) * g0, a1 = __uint_as_float(dp[2 * e + 1]) * g1;
             if (diag) {  // causal: key r <= query column
               if (i0 < r) w0 = a0 = 0.0f;
@@ -443,6 +444,7 @@ __device__ __forceinline__ void bwd_dq_block(const CUtensorMap& tmQ, const CUten
     const int r = wq * 32 + lane;
     const int row = m * BT + r;
     const float tau = tile::tau_of_row(row, beta, dr);
+    const float lp = log2f(p);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     bool ok = true;
     for (int n = 0; n <= m && ok; ++n) {
@@ -462,8 +464,8 @@ __device__ __forceinline__ void bwd_dq_block(const CUtensorMap& tmQ, const CUten
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             float w0, g0, w1, g1;
-            weight_and_grad<PC>(__uint_as_float(sv[2 * e]) - tau, p, w0, g0);
-            weight_and_grad<PC>(__uint_as_float(sv[2 * e + 1]) - tau, p, w1, g1);
+            weight_and_grad<PC>(__uint_as_float(sv[2 * e]) - tau, p, lp, w0, g0);
+            weight_and_grad<PC>(__uint_as_float(sv[2 * e + 1]) - tau, p, lp, w1, g1);
             float a0 = __uint_as_float(dp[2 * e]) * g0, a1 = __uint_as_float(dp[2 * e + 1]) * g1;
             if (diag) {  // causal: key column <= query row r
               const int kc = 32 * c + 2 * e;
@@ -581,15 +583,17 @@ int launch_tra_bwd_bf16(const void* q, const void* k, const void* v, const void*
     const int st = encode_tmap_3d(&maps[i], src[i], D, T, BH, rs, hs, 64, BT, 1);
     if (st != OK) return st;
   }
-  const int pc = power_class(p);
+  const int pc = bwd::bwd_power_class(p);
   if (D == 128) {
     if (pc == POW_TWO) return launch_bwd<128, POW_TWO>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
     if (pc == POW_ONE) return launch_bwd<128, POW_ONE>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
+    if (pc == POW_GENERAL_MIX) return launch_bwd<128, POW_GENERAL_MIX>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
     return launch_bwd<128, POW_GENERAL>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
   }
   if (D == 64 || D == 32 || D == 16) {  // 16 and 32 at width 64 on zero-filled columns
     if (pc == POW_TWO) return launch_bwd<64, POW_TWO>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
     if (pc == POW_ONE) return launch_bwd<64, POW_ONE>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
+    if (pc == POW_GENERAL_MIX) return launch_bwd<64, POW_GENERAL_MIX>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
     return launch_bwd<64, POW_GENERAL>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
   }
   return ERR_UNSUPPORTED;

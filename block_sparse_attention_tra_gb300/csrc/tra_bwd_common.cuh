@@ -26,9 +26,13 @@ __device__ __forceinline__ float lg2a(float x) {
   return y;
 }
 
-// ReLU(x)^p and its derivative p ReLU(x)^(p-1) (0 for x <= 0).
+// ReLU(x)^p and its derivative p ReLU(x)^(p-1) (0 for x <= 0).  For p > 1
+// (POW_GENERAL_MIX) the factor p goes into the exponent, g = exp2((p - 1)
+// log2 r + log2 p) with lp = log2 p, and r = 0 needs no test: (p - 1) (-inf)
+// is -inf and exp2 of it 0.  Other general powers (p < 1, where (p - 1)
+// (-inf) is +inf) test x.
 template <int PC>
-__device__ __forceinline__ void weight_and_grad(float x, float p, float& w, float& g) {
+__device__ __forceinline__ void weight_and_grad(float x, float p, float lp, float& w, float& g) {
   const float r = fmaxf(x, 0.0f);
   if constexpr (PC == POW_ONE) {
     w = r;
@@ -36,11 +40,22 @@ __device__ __forceinline__ void weight_and_grad(float x, float p, float& w, floa
   } else if constexpr (PC == POW_TWO) {
     w = r * r;
     g = 2.0f * r;
-  } else {
+  } else if constexpr (PC == POW_GENERAL_MIX) {
     const float l = lg2a(r);  // -inf for r = 0
+    w = ex2a(p * l);
+    g = ex2a(fmaf(p - 1.0f, l, lp));
+  } else {
+    const float l = lg2a(r);
     w = ex2a(p * l);
     g = x > 0.0f ? p * ex2a((p - 1.0f) * l) : 0.0f;
   }
+}
+
+// Backward power class: p = 1, p = 2, p > 1 (POW_GENERAL_MIX) or any other.
+__host__ __device__ inline int bwd_power_class(float p) {
+  if (p == 1.0f) return POW_ONE;
+  if (p == 2.0f) return POW_TWO;
+  return p > 1.0f ? POW_GENERAL_MIX : POW_GENERAL;
 }
 
 // TMA producer of a backward block: two resident 128-row tiles (row res_row

@@ -182,9 +182,22 @@ __device__ __forceinline__ float tau_fast(int row, float beta, float k2, int d) 
 // g = r + r in one packed multiply and add for p = 2), bit-identical to
 // bwd::weight_and_grad; other powers take the scalar form.
 template <int PC>
-__device__ __forceinline__ void weight_and_grad2(float s0, float s1, float t0, float t1, float p, float& w0,
-                                                 float& w1, uint64_t& g) {
-  if constexpr (PC == POW_TWO || PC == POW_ONE) {
+__device__ __forceinline__ void weight_and_grad2(float s0, float s1, float t0, float t1, float p, float lp,
+                                                 float& w0, float& w1, uint64_t& g) {
+  if constexpr (PC == POW_GENERAL_MIX) {
+    // p > 1: the exponents p l and (p - 1) l + log2 p of one score in one
+    // packed multiply-add, the same roundings as the scalar form
+    float x0, x1;
+    f2_unpack(f2_sub(f2_pack(s0, s1), f2_pack(t0, t1)), x0, x1);
+    const float l0 = bwd::lg2a(fmaxf(x0, 0.0f)), l1 = bwd::lg2a(fmaxf(x1, 0.0f));
+    const uint64_t pq = f2_pack(p, p - 1.0f), z = f2_pack(0.0f, lp);
+    float a0, b0, a1, b1;
+    f2_unpack(f2_fma(f2_pack(l0, l0), pq, z), a0, b0);
+    f2_unpack(f2_fma(f2_pack(l1, l1), pq, z), a1, b1);
+    w0 = bwd::ex2a(a0);
+    w1 = bwd::ex2a(a1);
+    g = f2_pack(bwd::ex2a(b0), bwd::ex2a(b1));
+  } else if constexpr (PC == POW_TWO || PC == POW_ONE) {
     float x0, x1;
     f2_unpack(f2_sub(f2_pack(s0, s1), f2_pack(t0, t1)), x0, x1);
     const float r0 = fmaxf(x0, 0.0f), r1 = fmaxf(x1, 0.0f);
@@ -199,8 +212,8 @@ __device__ __forceinline__ void weight_and_grad2(float s0, float s1, float t0, f
     }
   } else {
     float g0, g1;
-    bwd::weight_and_grad<PC>(s0 - t0, p, w0, g0);
-    bwd::weight_and_grad<PC>(s1 - t1, p, w1, g1);
+    bwd::weight_and_grad<PC>(s0 - t0, p, lp, w0, g0);
+    bwd::weight_and_grad<PC>(s1 - t1, p, lp, w1, g1);
     g = f2_pack(g0, g1);
   }
 }
@@ -238,6 +251,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // tensor maps cover the real d_real columns); width 128 serves 128 alone.
   const int dr = D == 128 ? D : d_real;
   const float k2 = 2.0f * 0.6931471805599453f / static_cast<float>(dr);  // 2 ln 2 / d
+  const float lp = log2f(p);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const FusedBars B = fused_bars<D>(smem);
@@ -453,7 +467,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float ta = (e & 1) ? t4.z : t4.x, tb = (e & 1) ? t4.w : t4.y;
           float w0, w1;
           uint64_t g2;
-          weight_and_grad2<PC>(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1]), ta, tb, p, w0, w1, g2);
+          weight_and_grad2<PC>(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1]), ta, tb, p, lp, w0, w1,
+                               g2);
           if (diag) {  // causal: key r <= query column
             float g0, g1;
             f2_unpack(g2, g0, g1);
@@ -568,9 +583,11 @@ int launch_fused(const CUtensorMap* maps, const CUtensorMap& mdq, void* dk, void
 template <int D>
 int launch_fused_pc(const CUtensorMap* maps, const CUtensorMap& mdq, void* dk, void* dv, int BH, int T, float beta,
                     float p, int d_real, cudaStream_t stream) {
-  const int pc = power_class(p);
+  const int pc = bwd::bwd_power_class(p);
   if (pc == POW_TWO) return launch_fused<D, POW_TWO>(maps, mdq, dk, dv, BH, T, beta, p, d_real, stream);
   if (pc == POW_ONE) return launch_fused<D, POW_ONE>(maps, mdq, dk, dv, BH, T, beta, p, d_real, stream);
+  if (pc == POW_GENERAL_MIX)
+    return launch_fused<D, POW_GENERAL_MIX>(maps, mdq, dk, dv, BH, T, beta, p, d_real, stream);
   return launch_fused<D, POW_GENERAL>(maps, mdq, dk, dv, BH, T, beta, p, d_real, stream);
 }
 
