@@ -174,7 +174,7 @@ int tra_forward_ex(const void* q, const void* k, const void* v, void* out, int B
   if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
-  if (D != 16 && D != 32 && D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (!tra_head_dim_supported(D)) return BSA_ERR_UNSUPPORTED;
   if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f)) return BSA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return BSA_ERR_ALIGN;
   const int dv = check_device();
@@ -187,7 +187,7 @@ int tra_forward_ex(const void* q, const void* k, const void* v, void* out, int B
 
 size_t tra_forward_host_workspace_size(int B, int H, int T, int D, int dtype) {
   if (dtype != BSA_F32 && dtype != BSA_BF16) return 0;
-  if (B < 1 || H < 1 || T < 1 || (D != 16 && D != 32 && D != 64 && D != 128)) return 0;
+  if (B < 1 || H < 1 || T < 1 || !tra_head_dim_supported(D)) return 0;
   if (static_cast<long long>(B) * H > 0x7fffffffLL || static_cast<long long>(B) * H * T * D >= (1LL << 40)) return 0;
   return tra_host_workspace_bytes(static_cast<long long>(B) * H, T, D, dtype == BSA_F32 ? 4 : 2);
 }
@@ -199,7 +199,7 @@ int tra_forward_host(const void* q, const void* k, const void* v, void* out, int
   if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
-  if (D != 16 && D != 32 && D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (!tra_head_dim_supported(D)) return BSA_ERR_UNSUPPORTED;
   if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f)) return BSA_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return BSA_ERR_ALIGN;
   if (workspace_bytes < tra_forward_host_workspace_size(B, H, T, D, dtype)) return BSA_ERR_SCRATCH_LIMIT;
@@ -217,7 +217,7 @@ int tra_backward_ex(const void* q, const void* k, const void* v, const void* dou
   if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
-  if (D != 16 && D != 32 && D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (!tra_head_dim_supported(D)) return BSA_ERR_UNSUPPORTED;
   if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f)) return BSA_ERR_UNSUPPORTED;
   if ((flags & ~BSA_TRA_BWD_DETERMINISTIC) != 0) return BSA_ERR_UNSUPPORTED;
   const void* ptrs[7] = {q, k, v, dout, dq, dk, dv};
@@ -259,7 +259,7 @@ static int check_diff_args(const void* q1, const void* q2, const void* k1, const
   if (B < 1 || H < 1 || T < 1 || D < 1) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H > 0x7fffffffLL) return BSA_ERR_SHAPE;
   if (static_cast<long long>(B) * H * T * D >= (1LL << 40)) return BSA_ERR_SHAPE;
-  if (D != 16 && D != 32 && D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+  if (!tra_head_dim_supported(D)) return BSA_ERR_UNSUPPORTED;
   if (!isfinite(beta) || !isfinite(p) || !(p > 0.0f) || isnan(lambda)) return BSA_ERR_UNSUPPORTED;
   const void* ptrs[6] = {q1, q2, k1, k2, v, out};
   for (const void* ptr : ptrs)

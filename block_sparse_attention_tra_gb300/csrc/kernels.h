@@ -149,6 +149,11 @@ inline int power_class(float p) {
   return (p >= 1.0f && p <= POW_MIX_MAX_P) ? POW_GENERAL_MIX : POW_GENERAL;
 }
 
+// Head dims of the threshold-attention entry points: multiples of 16 up to
+// 128.  The bf16 kernels run tile width 64 (D <= 64) or 128 on the tensor
+// maps' zero-filled columns past D; the fp32 kernels are built per D.
+inline bool tra_head_dim_supported(int D) { return D >= 16 && D <= 128 && D % 16 == 0; }
+
 // POW_HALF0 + k for p = k + 1/2 with k in 0..3, else -1.
 inline int half_power_class(float p) {
   for (int k = 0; k <= POW_HALF3 - POW_HALF0; ++k)

@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(PairCfg<PC>::THREADS, 1)
   using L = PairLayout<D>;
   using Cfg = PairCfg<PC>;
   constexpr int PAIR_TMA_WARP = Cfg::TMA_WARP;
-  const int dr = D == 128 ? D : d_real;  // tile width 128 serves head dim 128 alone
+  const int dr = d_real;  // head dim (the tile width D or less: zero-filled columns)
   constexpr int PAIR_MMA_WARP = Cfg::MMA_WARP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -679,7 +679,7 @@ int launch_width(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap
 int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int B, int H, int T, int D,
                     float beta, float p, bool sqrt_half_powers, cudaStream_t stream) {
   const int BH = B * H;
-  if (D != 16 && D != 32 && D != 64 && D != 128) return ERR_UNSUPPORTED;
+  if (!tra_head_dim_supported(D)) return ERR_UNSUPPORTED;
   CUtensorMap mq, mk, mv;
   const uint64_t rs = static_cast<uint64_t>(D) * 2;  // row stride in bytes
   const uint64_t hs = rs * T;                        // (b, h) stride in bytes
@@ -689,9 +689,9 @@ int launch_tra_bf16(const void* q, const void* k, const void* v, void* out, int 
   if (st != OK) return st;
   const int pc = power_class(p);
   const int hc = sqrt_half_powers ? half_power_class(p) : -1;
-  // Head dims 16 and 32 run at tile width 64: the TMA box of 64 columns reads
-  // zeros past the tensor's D columns, which change neither q.k nor P V, and
-  // only the D real columns of O are stored.
+  // Head dims below the tile width (64 for D <= 64, else 128): the TMA boxes
+  // of 64 columns read zeros past the tensor's D columns, which change neither
+  // q.k nor P V, and only the D real columns of O are stored.
   const int width = D <= 64 ? 64 : 128;
   if (hc >= 0)
     return width == 128 ? launch_half<128>(mq, mk, mv, out, BH, T, beta, p, hc, stream, D)

@@ -223,7 +223,7 @@ __device__ __forceinline__ void bwd_dkdv_block(const CUtensorMap& tmQ, const CUt
                                                __nv_bfloat16* __restrict__ dv, int BH, int T, int nT, int G,
                                                float beta, float p, int blk, int d_real) {
   using L = BwdLayout<D>;
-  const int dr = D == 128 ? D : d_real;  // head dims 16, 32 run at width 64 on zero-filled columns
+  const int dr = d_real;  // head dim (the tile width D or less: zero-filled columns)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const BwdBars B = bwd_bars<D>(smem);
@@ -375,7 +375,7 @@ __device__ __forceinline__ void bwd_dq_block(const CUtensorMap& tmQ, const CUten
                                              const CUtensorMap& tmDO, __nv_bfloat16* __restrict__ dq, int BH, int T,
                                              int nT, int G, float beta, float p, int blk, int d_real) {
   using L = BwdLayout<D>;
-  const int dr = D == 128 ? D : d_real;
+  const int dr = d_real;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const BwdBars B = bwd_bars<D>(smem);
@@ -584,13 +584,13 @@ int launch_tra_bwd_bf16(const void* q, const void* k, const void* v, const void*
     if (st != OK) return st;
   }
   const int pc = bwd::bwd_power_class(p);
-  if (D == 128) {
+  if (D > 64) {  // width 128 (head dims 80 .. 128 on zero-filled columns)
     if (pc == POW_TWO) return launch_bwd<128, POW_TWO>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
     if (pc == POW_ONE) return launch_bwd<128, POW_ONE>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
     if (pc == POW_GENERAL_MIX) return launch_bwd<128, POW_GENERAL_MIX>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
     return launch_bwd<128, POW_GENERAL>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
   }
-  if (D == 64 || D == 32 || D == 16) {  // 16 and 32 at width 64 on zero-filled columns
+  if (tra_head_dim_supported(D)) {  // width 64 (16 .. 48 on zero-filled columns)
     if (pc == POW_TWO) return launch_bwd<64, POW_TWO>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
     if (pc == POW_ONE) return launch_bwd<64, POW_ONE>(maps, dq, dk, dv, BH, T, beta, p, D, stream);
     if (pc == POW_GENERAL_MIX) return launch_bwd<64, POW_GENERAL_MIX>(maps, dq, dk, dv, BH, T, beta, p, D, stream);

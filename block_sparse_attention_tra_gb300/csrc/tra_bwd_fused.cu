@@ -247,9 +247,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                          __nv_bfloat16* __restrict__ dv, int BH, int T, int nT, int G, float beta, float p,
                          int d_real) {
   using L = FusedLayout<D>;
-  // Head dims 16 and 32 run at tile width 64 on zero-filled columns (the
-  // tensor maps cover the real d_real columns); width 128 serves 128 alone.
-  const int dr = D == 128 ? D : d_real;
+  // Head dims below the tile width run on zero-filled columns (the tensor
+  // maps cover the real d_real columns).
+  const int dr = d_real;
   const float k2 = 2.0f * 0.6931471805599453f / static_cast<float>(dr);  // 2 ln 2 / d
   const float lp = log2f(p);
   extern __shared__ uint8_t smem_raw[];
@@ -418,8 +418,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_proxy_async_smem();
         bar_sync(DRAIN_BAR, 128);
         if (issuer) {
-          tma_reduce_add_3d(&tmDQ, sStg, 64, m * BT, bh);
-          tma_reduce_add_3d(&tmDQ, sStg + L::BOX_BYTES, 96, m * BT, bh);
+          tma_reduce_add_3d(&tmDQ, sStg, 64, m * BT, bh);  // dr > 64 at width 128
+          if (dr > 96) tma_reduce_add_3d(&tmDQ, sStg + L::BOX_BYTES, 96, m * BT, bh);
           bulk_commit();
           bulk_wait_read<0>();
         }
@@ -596,7 +596,7 @@ int launch_fused_pc(const CUtensorMap* maps, const CUtensorMap& mdq, void* dk, v
 int launch_tra_bwd_fused_bf16(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
                               void* dv, int B, int H, int T, int D, float beta, float p, float* dq_acc,
                               cudaStream_t stream) {
-  if (D != 16 && D != 32 && D != 64 && D != 128) return ERR_UNSUPPORTED;
+  if (!tra_head_dim_supported(D)) return ERR_UNSUPPORTED;
   const int BH = B * H;
   CUtensorMap maps[4], mdq;
   const uint64_t rs = static_cast<uint64_t>(D) * 2, hs = rs * T;
@@ -617,7 +617,7 @@ int launch_tra_bwd_fused_bf16(const void* q, const void* k, const void* v, const
   tra_bwd_dq_zero_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(reinterpret_cast<uint4*>(dq_acc),
                                                                              elems / 4);
   if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
-  const int rc = D == 128 ? launch_fused_pc<128>(maps, mdq, dk, dv, BH, T, beta, p, D, stream)
+  const int rc = D > 64 ? launch_fused_pc<128>(maps, mdq, dk, dv, BH, T, beta, p, D, stream)
                           : launch_fused_pc<64>(maps, mdq, dk, dv, BH, T, beta, p, D, stream);
   if (rc != OK) return rc;
   tra_bwd_dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(

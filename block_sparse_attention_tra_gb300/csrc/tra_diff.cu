@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
                     __nv_bfloat16* __restrict__ out, int BH, int T, int nQ, int G, float beta, float p, float lam,
                     int d_real) {
   const int Tp = nQ * BT;  // row stride of the normalisation buffer
-  const int dr = D == 128 ? D : d_real;  // head dims 16, 32 run at width 64 on zero-filled columns
+  const int dr = d_real;  // head dim (the tile width D or less: zero-filled columns)
   using L = DiffLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -562,7 +562,7 @@ size_t tra_diff_scratch_bytes(int B, int H, int T) {
 int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const void* k2, const void* v, void* out,
                          int B, int H, int T, int D, float beta, float lam, float p, float* inv_norm, void* knorm,
                          cudaStream_t stream) {
-  if (D != 16 && D != 32 && D != 64 && D != 128) return ERR_UNSUPPORTED;
+  if (!tra_head_dim_supported(D)) return ERR_UNSUPPORTED;
   const int BH = B * H;
   CUtensorMap maps[5];
   const uint64_t rs = static_cast<uint64_t>(D) * 2, hs = rs * T;
@@ -590,20 +590,22 @@ int launch_tra_diff_bf16(const void* q1, const void* q2, const void* k1, const v
     const bool idx32 = rows < (1LL << 32);  // every row index (and the division by Tp) fits 32 bits
     auto* kw = kn ? kn1 : nullptr;
     switch (D) {
-      case 128: launch_row_norms<128>(blocks, a0, a1, a2, a3, inv_norm, kw, BH, T, Tp, idx32, stream); break;
-      case 64: launch_row_norms<64>(blocks, a0, a1, a2, a3, inv_norm, kw, BH, T, Tp, idx32, stream); break;
-      case 32: launch_row_norms<32>(blocks, a0, a1, a2, a3, inv_norm, kw, BH, T, Tp, idx32, stream); break;
-      default: launch_row_norms<16>(blocks, a0, a1, a2, a3, inv_norm, kw, BH, T, Tp, idx32, stream); break;
+#define BSA_ROW_NORMS(d) \
+  case d: launch_row_norms<d>(blocks, a0, a1, a2, a3, inv_norm, kw, BH, T, Tp, idx32, stream); break;
+      BSA_ROW_NORMS(16) BSA_ROW_NORMS(32) BSA_ROW_NORMS(48) BSA_ROW_NORMS(64)
+      BSA_ROW_NORMS(80) BSA_ROW_NORMS(96) BSA_ROW_NORMS(112) BSA_ROW_NORMS(128)
+#undef BSA_ROW_NORMS
+      default: return ERR_UNSUPPORTED;
     }
     if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
   }
   const int nm = !norm ? 0 : kn ? 2 : 1;
-  if (D == 128) {
+  if (D > 64) {  // width 128 (80 .. 128 on zero-filled columns)
     if (nm == 2) return dispatch_pc<128, 2>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
     if (nm == 1) return dispatch_pc<128, 1>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
     return dispatch_pc<128, 0>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
   }
-  // 64, and 16 or 32 at width 64 on zero-filled columns
+  // width 64 (16 .. 48 on zero-filled columns)
   if (nm == 2) return dispatch_pc<64, 2>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
   if (nm == 1) return dispatch_pc<64, 1>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);
   return dispatch_pc<64, 0>(maps, inv_norm, out, BH, T, beta, p, lam, D, stream);

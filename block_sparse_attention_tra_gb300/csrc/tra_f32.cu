@@ -165,7 +165,11 @@ int launch_tra_f32(const float* q, const float* k, const float* v, float* out, i
   switch (D) {
     case 16: return launch_d<16>(q, k, v, out, BH, T, beta, p, stream);
     case 32: return launch_d<32>(q, k, v, out, BH, T, beta, p, stream);
+    case 48: return launch_d<48>(q, k, v, out, BH, T, beta, p, stream);
     case 64: return launch_d<64>(q, k, v, out, BH, T, beta, p, stream);
+    case 80: return launch_d<80>(q, k, v, out, BH, T, beta, p, stream);
+    case 96: return launch_d<96>(q, k, v, out, BH, T, beta, p, stream);
+    case 112: return launch_d<112>(q, k, v, out, BH, T, beta, p, stream);
     case 128: return launch_d<128>(q, k, v, out, BH, T, beta, p, stream);
     default: return ERR_UNSUPPORTED;
   }

@@ -408,7 +408,11 @@ int launch_tra_bwd_f32(const float* q, const float* k, const float* v, const flo
   switch (D) {
     case 16: return bwd_pc<16>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
     case 32: return bwd_pc<32>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
+    case 48: return bwd_pc<48>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
     case 64: return bwd_pc<64>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
+    case 80: return bwd_pc<80>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
+    case 96: return bwd_pc<96>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
+    case 112: return bwd_pc<112>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
     case 128: return bwd_pc<128>(q, k, v, dout, dq, dk, dv, BH, T, beta, p, stream);
     default: return ERR_UNSUPPORTED;
   }
@@ -421,7 +425,11 @@ int launch_tra_diff_f32(const float* q1, const float* q2, const float* k1, const
   switch (D) {
     case 16: return diff_norm<16>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, normalize, stream);
     case 32: return diff_norm<32>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, normalize, stream);
+    case 48: return diff_norm<48>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, normalize, stream);
     case 64: return diff_norm<64>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, normalize, stream);
+    case 80: return diff_norm<80>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, normalize, stream);
+    case 96: return diff_norm<96>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, normalize, stream);
+    case 112: return diff_norm<112>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, normalize, stream);
     case 128: return diff_norm<128>(q1, q2, k1, k2, v, out, BH, T, beta, p, lam, normalize, stream);
     default: return ERR_UNSUPPORTED;
   }

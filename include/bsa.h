@@ -92,9 +92,10 @@ typedef enum {
  *   q, k, v, out : [B, H, T, D], element type `dtype`; out has the input type
  *                  (the page casts its fp32 result back to the input dtype).
  *   B, H, T      : >= 1; B * H <= 2^31 - 1 and B*H*T*D < 2^40.
- *   D            : 16, 32, 64 or 128 (head dim; the page's kernel takes any
- *                  power of two up to 128 as its BLOCK_D).  16 and 32 run the
- *                  width-64 kernel on zero-filled columns.
+ *   D            : a multiple of 16 from 16 to 128 (head dim; the page's
+ *                  kernel takes the head dim as its BLOCK_D).  Head dims
+ *                  below 64 run the width-64 bf16 kernel and 80 .. 112 the
+ *                  width-128 one, on zero-filled columns.
  *   beta         : finite.      p : finite and > 0.
  *   dtype        : BSA_BF16 -- tensor-core (tcgen05) path, bf16 operands,
  *                  fp32 accumulation, weights rounded to bf16 before W.V;
@@ -102,7 +103,8 @@ typedef enum {
  *   stream       : CUDA stream the kernel is enqueued on.
  *
  * Errors: BSA_ERR_NULLPTR, BSA_ERR_SHAPE (sizes), BSA_ERR_DTYPE,
- * BSA_ERR_UNSUPPORTED (D not 16/32/64/128, p <= 0, non-finite beta/p),
+ * BSA_ERR_UNSUPPORTED (D not a multiple of 16 in 16..128, p <= 0,
+ * non-finite beta/p),
  * BSA_ERR_ALIGN, BSA_ERR_DEVICE, BSA_ERR_LAUNCH.
  */
 BSA_API int tra_forward(const void* q, const void* k, const void* v, void* out,
@@ -194,8 +196,8 @@ BSA_API int tra_forward_host(const void* q, const void* k, const void* v,
  *   q, k, v, dout       : [B, H, T, D] inputs of `dtype` (dout = dL/d out).
  *   dq, dk, dv          : [B, H, T, D] outputs of `dtype` (fp32 accumulation);
  *                         they must not alias the inputs or each other.
- *   D                   : 16, 32, 64 or 128 (16 and 32 run the width-64
- *                         kernels on zero-filled columns).
+ *   D                   : as for tra_forward (a multiple of 16 up to 128;
+ *                         below the tile width on zero-filled columns).
  *   B, H, T, beta, p    : as for tra_forward.  For 0 < p < 1 the derivative
  *                         p x^(p-1) grows without bound as x -> 0+, so a
  *                         score within rounding of tau(i) makes dq and dk
@@ -203,8 +205,7 @@ BSA_API int tra_forward_host(const void* q, const void* k, const void* v,
  *                         differ there).
  *   dtype               : BSA_BF16 or BSA_F32.
  *
- * Errors: as for tra_forward (BSA_ERR_UNSUPPORTED for D other than 16, 32,
- * 64, 128),
+ * Errors: as for tra_forward (BSA_ERR_UNSUPPORTED for other D),
  * plus BSA_ERR_MEMORY if the bf16 temporary cannot be allocated or released.
  */
 BSA_API int tra_backward(const void* q, const void* k, const void* v,
@@ -263,7 +264,7 @@ BSA_API int tra_backward_ex(const void* q, const void* k, const void* v,
  *
  *   q1, q2, k1, k2, v, out : [B, H, T, D] of `dtype` (out may not alias
  *                            inputs).
- *   D                      : 16, 32, 64 or 128 (as for tra_forward).
+ *   D                      : as for tra_forward.
  *   B, H, T, beta, p       : as for tra_forward.
  *   lambda                 : any non-NaN value; clamped to [0, 1].
  *   dtype                  : BSA_BF16 or BSA_F32.

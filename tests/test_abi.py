@@ -68,8 +68,10 @@ def test_tra_argument_errors(lib):
     assert tra(lib, B=0) == 2
     assert tra(lib, T=0) == 2
     assert tra(lib, T=-5) == 2
-    assert tra(lib, D=96) == 4
-    assert tra(lib, D=48) == 4
+    assert tra(lib, D=100) == 4  # head dims: multiples of 16 up to 128
+    assert tra(lib, D=40) == 4
+    assert tra(lib, D=8) == 4
+    assert tra(lib, D=144) == 4
     assert tra(lib, D=256) == 4
     assert tra(lib, p=0.0) == 4
     assert tra(lib, p=-1.0) == 4
@@ -123,9 +125,9 @@ def test_backward_and_diff_argument_errors(lib):
 
     assert bsa.tra_backward_raw(P, P, P, None, P, P, P, 1, 1, 16, 64, 1.0, 2.0, 1, 0) == 1
     assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 64, 1.0, 2.0, 7, 0) == 3  # not a bsa_dtype
-    assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 96, 1.0, 2.0, 0, 0) == 4  # f32, D = 96
-    assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 96, 1.0, 2.0, 1, 0) == 4
-    assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 48, 1.0, 2.0, 1, 0) == 4
+    assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 100, 1.0, 2.0, 0, 0) == 4  # f32, D = 100
+    assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 100, 1.0, 2.0, 1, 0) == 4
+    assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 40, 1.0, 2.0, 1, 0) == 4
     assert bsa.tra_backward_raw(P, P, P, P, P, P, P, 1, 1, 16, 8, 1.0, 2.0, 1, 0) == 4
     assert bsa.tra_backward_raw(P, P, P, P, P + 2, P, P, 1, 1, 16, 64, 1.0, 2.0, 1, 0) == 7
     assert bsa.tra_backward_ex_raw(P, P, P, P, P, P, P, 1, 1, 16, 64, 1.0, 2.0, 1, 2, 0) == 4  # unknown flag bit
@@ -177,11 +179,12 @@ def test_tra_forward_ex_flags(lib):
         return bsa.tra_forward_ex_raw(P, P, P, P, 1, 1, 16, D, 1.0, p, 1, flags, 0)
 
     assert ex(2) == 4 and ex(-1) == 4  # unknown flag bits
-    assert ex(1, D=96) == 4
+    assert ex(1, D=100) == 4
     assert ex(1, p=0.0) == 4
     assert bsa.tra_forward_ex_raw(None, P, P, P, 1, 1, 16, 64, 1.0, 1.5, 1, 1, 0) == 1
     if not __import__("torch").cuda.is_available():
         assert ex(0) == 6 and ex(1) == 6 and ex(1, p=2.0) == 6
+        assert ex(0, D=96) == 6 and ex(0, D=48) == 6 and ex(1, D=112) == 6  # other multiples of 16: valid
 
 
 def test_tra_forward_host_workspace_and_argument_errors(lib):
@@ -190,7 +193,7 @@ def test_tra_forward_host_workspace_and_argument_errors(lib):
     # three stages of q, k, v, out for one chunk of ceil(B*H / 8) heads
     assert bsa.tra_forward_host_workspace_size(4, 16, 4096, 128, 1) == 3 * 4 * 8 * 4096 * 128 * 2
     assert bsa.tra_forward_host_workspace_size(1, 3, 100, 64, 0) == 3 * 4 * ((1 * 100 * 64 * 4 + 255) // 256 * 256)
-    assert bsa.tra_forward_host_workspace_size(1, 1, 16, 48, 1) == 0     # D
+    assert bsa.tra_forward_host_workspace_size(1, 1, 16, 40, 1) == 0     # D
     assert bsa.tra_forward_host_workspace_size(1, 1, 16, 64, 7) == 0     # dtype
     assert bsa.tra_forward_host_workspace_size(0, 1, 16, 64, 1) == 0     # B
     ws, need = 1 << 20, bsa.tra_forward_host_workspace_size(1, 1, 16, 64, 1)
@@ -201,7 +204,7 @@ def test_tra_forward_host_workspace_and_argument_errors(lib):
     assert call(q=None) == 1 and call(w=None) == 1
     assert call(dtype=5) == 3
     assert call(B=0) == 2 and call(T=0) == 2
-    assert call(D=96) == 4 and call(p=0.0) == 4 and call(beta=float("nan")) == 4
+    assert call(D=100) == 4 and call(p=0.0) == 4 and call(beta=float("nan")) == 4
     assert call(w=ws + 16) == 7                      # workspace not 256-byte aligned
     assert call(nbytes=need - 1) == 9                # workspace too small
     if not __import__("torch").cuda.is_available():  # (with a device it would copy from the fake host pointers)

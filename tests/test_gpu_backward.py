@@ -43,6 +43,10 @@ CASES = [
     (2, 2, 1024, 128, 1.0, 2.0), # medium size
     (1, 2, 300, 32, 1.0, 2.0),   # head dim 32 (width-64 tiles, zero-filled columns), ragged
     (1, 1, 257, 16, 0.5, 1.5),   # head dim 16, general power
+    (1, 2, 300, 96, 1.0, 2.0),   # head dim 96 (tile width 128, zero-filled columns)
+    (1, 1, 257, 48, 0.5, 1.5),   # head dim 48 (tile width 64)
+    (1, 1, 200, 112, 1.0, 3.0),
+    (1, 1, 150, 80, 0.5, 0.75),  # p < 1 at width 128
 ]
 
 
@@ -114,6 +118,8 @@ F32_CASES = [
     (1, 1, 320, 64, -0.5, 3.7),   # beta < 0 reading, large power
     (1, 2, 150, 32, 1.0, 2.0),    # head dim 32
     (1, 1, 100, 16, 0.5, 1.5),    # head dim 16
+    (1, 1, 150, 80, 1.0, 2.0),    # head dims 80, 48
+    (1, 2, 100, 48, 0.5, 1.5),
 ]
 
 

@@ -50,6 +50,9 @@ CASES = [
     (1, 2, 300, 32, 0.2, 0.5, 2.0, True),   # head dim 32 (width-64 tiles, zero-filled columns)
     (1, 1, 257, 16, 0.0, 0.7, 1.5, True),   # head dim 16, general power
     (1, 2, 130, 32, 0.3, 0.4, 1.0, False),
+    (1, 2, 300, 96, 0.2, 0.5, 2.0, True),   # head dims 96, 48, 112 (zero-filled columns)
+    (1, 1, 257, 48, 0.0, 0.7, 1.5, True),
+    (1, 2, 200, 112, 0.3, 0.4, 1.0, False),
 ]
 
 
@@ -120,6 +123,7 @@ F32_CASES = [
     (1, 1, 320, 64, 0.1, 1.5, 2.0, False),   # lambda clamps to 1
     (1, 2, 150, 32, 0.2, 0.5, 2.0, True),    # head dim 32
     (1, 1, 100, 16, 0.0, 0.6, 1.5, True),    # head dim 16
+    (1, 1, 120, 96, 0.2, 0.5, 2.0, True),    # head dim 96
 ]
 
 

@@ -85,6 +85,15 @@ TRA_SMALL = [
     (1, 3, 200, 32, 0.0, 1.0, "bf16"),
     (1, 2, 130, 16, 1.0, 2.0, "f32"),
     (1, 1, 200, 32, 0.5, 1.5, "f32"),
+    # other multiples of 16: 48 at tile width 64, 80 .. 112 at width 128 (zero-filled columns)
+    (1, 2, 300, 48, 1.0, 2.0, "bf16"),
+    (1, 2, 257, 80, 2.0, 1.5, "bf16"),
+    (1, 1, 200, 96, 0.5, 2.0, "bf16"),
+    (2, 1, 130, 112, 1.0, 1.0, "bf16"),
+    (1, 1, 384, 96, 2.0, 3.7, "bf16"),
+    (1, 2, 130, 48, 1.0, 1.5, "f32"),
+    (1, 1, 100, 96, 0.5, 2.0, "f32"),
+    (1, 1, 90, 112, 1.0, 1.0, "f32"),
 ]
 
 
@@ -129,7 +138,8 @@ def test_tra_many_short_items_per_cta(B, H, T, D, beta, p):
 # Half-integer powers evaluated as x^k sqrt(x) (tra_forward_ex flag): the same
 # map, so the same oracle and bar; other powers must match tra_forward bit
 # for bit.
-@pytest.mark.parametrize("p,D,T", [(1.5, 64, 333), (0.5, 128, 300), (2.5, 64, 640), (3.5, 128, 257), (1.5, 32, 200)])
+@pytest.mark.parametrize("p,D,T", [(1.5, 64, 333), (0.5, 128, 300), (2.5, 64, 640), (3.5, 128, 257), (1.5, 32, 200),
+                                   (2.5, 80, 200), (1.5, 48, 150)])
 def test_tra_sqrt_half_powers(p, D, T):
     q, k, v = workloads.tra_inputs(2, 3, T, D, "bf16", seed=T + D)
     gpu = f64(bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), 1.0, p, sqrt_half_powers=True))
@@ -386,6 +396,7 @@ def test_nsa_full_workload_sampled_rows(name):
     (3, 8, 1000, 128, 1.0, "bf16", False),  # pageable host memory, 8 chunks of 3
     (1, 3, 130, 64, 2.0, "f32", True),      # fp32 path
     (2, 3, 200, 32, 1.5, "bf16", True),     # head dim 32
+    (1, 3, 200, 96, 2.0, "bf16", True),     # head dim 96 (tile width 128)
 ])
 def test_tra_forward_host_matches_device_path(B, H, T, D, p, dtype, pinned):
     import torch
