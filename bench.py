@@ -13,9 +13,12 @@ general power p=1.5 on the exp/log path.  The secondary workloads (the
 B=4 H=16 T=4096 D=128 p=2 TRA and the NSA selection workloads) are measured
 in the same run and reported under ``secondary``.
 
-Multi-GPU (torchrun): every rank runs the same workload on its own GPU with no
-collective on the data path (the work is independent per (batch, head));
-``value`` is the total FLOPs of all ranks over the max elapsed time.
+Multi-GPU (torchrun): the problem is sharded by batch with no collective on
+the data path (the work is independent per (batch, head)): with N ranks the
+global problem has N times the workload's batches, and rank r draws and
+processes its own slice of them (seed r; rank 0's slice is the single-GPU
+input), so the work per GPU is fixed ("scaling": "weak"); ``value`` is the
+total FLOPs of all ranks over the max elapsed time.
 """
 
 from __future__ import annotations
@@ -182,11 +185,13 @@ def barrier(world: int):
 
 # --------------------------------------------------------------- our kernels
 
-def make_inputs(name, device):
+def make_inputs(name, device, rank=0):
+    """The workload and this rank's slice of the batch-sharded problem (host
+    tensors and device copies)."""
     from block_sparse_attention_tra_gb300 import workloads
 
     w = workloads.TRA_WORKLOADS.get(name) or workloads.NSA_WORKLOADS[name]
-    tensors = workloads.workload_inputs(w)
+    tensors = workloads.workload_inputs(w, seed=workloads.shard_seed(rank))
     return w, tensors, [t.to(device) for t in tensors]
 
 
@@ -204,7 +209,9 @@ def workload_config(w, world):
     """The `config` object of the JSON line for a TRA or NSA workload."""
     from block_sparse_attention_tra_gb300 import workloads
 
-    par = f"replica x{world} (independent work per GPU, no collective)"
+    par = ("single GPU" if world == 1 else
+           f"batch-sharded over {world} GPUs: global batch {w.B * world}, rank r takes batches "
+           f"[r*{w.B}, (r+1)*{w.B}) drawn with seed r; no collective")
     if isinstance(w, workloads.TraWorkload):
         return {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "D": w.D, "beta": w.beta, "p": w.p,
                 "causal": True, "l2": "no flush: q,k,v,out = %d MB > 129 MB L2" % (w.io_bytes // 2**20),
@@ -373,7 +380,7 @@ def run_ours(args):
     bsa.load_library()
     pk = peaks()
 
-    w, host, dev = make_inputs(args.workload, device)
+    w, host, dev = make_inputs(args.workload, device, rank)
     out = torch.empty_like(dev[0])
     fn = launcher(w, dev, out)
 
@@ -474,7 +481,7 @@ def run_ours(args):
         for name in SECONDARY:
             del dev, out
             torch.cuda.empty_cache()
-            w2, _, dev = make_inputs(name, device)
+            w2, _, dev = make_inputs(name, device, rank)
             out = torch.empty_like(dev[0])
             lse = None
             if isinstance(w2, workloads.NsaWorkload):

@@ -186,6 +186,24 @@ def nsa_inputs(B: int, Hq: int, Hkv: int, T: int, D: int, block_size: int, S: in
     return q, k, v, idx
 
 
+def shard_range(units: int, world: int, rank: int) -> tuple[int, int]:
+    """The contiguous slice [start, end) of ``units`` independent units (the
+    (b, h) heads of TRA, the (b, hkv) groups of NSA) that rank ``rank`` of
+    ``world`` takes: sizes differ by at most one, and the slices of all ranks
+    cover 0..units-1 exactly once."""
+    if world < 1 or not 0 <= rank < world or units < 0:
+        raise ValueError("shard_range: need 0 <= rank < world and units >= 0")
+    base, extra = divmod(units, world)
+    start = rank * base + min(rank, extra)
+    return start, start + base + (1 if rank < extra else 0)
+
+
+def shard_seed(rank: int, seed: int = 0) -> int:
+    """Seed of rank ``rank``'s slice of a batch-sharded problem: rank 0 draws
+    exactly the single-GPU inputs, the others their own batches."""
+    return seed + rank
+
+
 def workload_inputs(w, seed: int = 0):
     """Inputs of a named workload (a ``TraWorkload`` or ``NsaWorkload``)."""
     if isinstance(w, TraWorkload):

@@ -112,3 +112,65 @@ def test_clock_records_that_reject_a_measurement():
     assert bench.clocks_rejected({"sm_mhz": 1200.0, "sm_max_mhz": 2070.0, "reasons": []})
     # no samples (no nvidia-smi): nothing to judge
     assert not bench.clocks_rejected({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]})
+
+
+def test_shard_range_covers_every_unit_once():
+    from block_sparse_attention_tra_gb300 import workloads
+
+    for units in (0, 1, 5, 64, 1000, 1023):
+        for world in (1, 2, 3, 4, 7, 8):
+            slices = [workloads.shard_range(units, world, r) for r in range(world)]
+            assert slices[0][0] == 0 and slices[-1][1] == units
+            assert all(a[1] == b[0] for a, b in zip(slices, slices[1:]))
+            sizes = [e - s for s, e in slices]
+            assert max(sizes) - min(sizes) <= 1
+    with pytest.raises(ValueError):
+        workloads.shard_range(8, 2, 2)
+
+
+SHARD_WORKER = r"""
+import os, sys, json
+sys.path.insert(0, {root!r})
+import numpy as np, torch, torch.distributed as dist
+from block_sparse_attention_tra_gb300 import workloads
+from oracle import tra as otra
+dist.init_process_group("gloo")
+r, n = dist.get_rank(), dist.get_world_size()
+# this rank's slice of a batch-sharded problem, as bench.py draws it, and the
+# oracle's output on it; rank 0 gathers every slice
+B, H, T, D = 1, 2, 40, 16
+q, k, v = workloads.tra_inputs(B, H, T, D, "f32", seed=workloads.shard_seed(r))
+o = torch.from_numpy(otra.tra_forward(q.double().numpy(), k.double().numpy(), v.double().numpy(), 0.5, 1.5))
+parts = [torch.zeros_like(o) for _ in range(n)] if r == 0 else None
+dist.gather(o, parts, dst=0)
+qs = [torch.zeros_like(q) for _ in range(n)] if r == 0 else None
+dist.gather(q, qs, dst=0)
+ks = [torch.zeros_like(k) for _ in range(n)] if r == 0 else None
+dist.gather(k, ks, dst=0)
+vs = [torch.zeros_like(v) for _ in range(n)] if r == 0 else None
+dist.gather(v, vs, dst=0)
+if r == 0:
+    # the global problem: the slices stacked along the batch; its oracle output
+    # equals the gathered per-rank outputs, and the slices differ
+    Q, K, V = (torch.cat(x, 0).double().numpy() for x in (qs, ks, vs))
+    full = otra.tra_forward(Q, K, V, 0.5, 1.5)
+    ok = bool(np.array_equal(full, torch.cat(parts, 0).numpy())) and not torch.equal(qs[0], qs[1])
+    print(json.dumps({{"ok": ok}}))
+dist.destroy_process_group()
+"""
+
+
+def test_batch_sharded_ranks_partition_the_global_problem(tmp_path):
+    script = tmp_path / "s.py"
+    script.write_text(SHARD_WORKER.format(root=ROOT))
+    port = _free_port()
+    procs = []
+    for rank in range(2):
+        env = dict(os.environ, RANK=str(rank), WORLD_SIZE="2", LOCAL_RANK=str(rank),
+                   MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, str(script)], env=env, stdout=subprocess.PIPE,
+                                      stderr=subprocess.PIPE, text=True))
+    outs = [p.communicate(timeout=180) for p in procs]
+    for p, (o, e) in zip(procs, outs):
+        assert p.returncode == 0, e
+    assert json.loads(outs[0][0].strip().splitlines()[-1])["ok"]
