@@ -163,3 +163,43 @@ def test_tra_diff_random_shapes(B, H, T, D, beta, lam, p, norm):
         return
     err = rel_err(f64(out), ref)
     assert err <= 2e-2, f"max err {err:.3e} of max|ref|"
+
+
+# Head dims below the bf16 tile widths (16 .. 48 at width 64, 80 .. 112 at
+# width 128, zero-filled columns), and the fp32 kernels built per head dim:
+# a third seeded stream, so the cases above stay as they are.
+_rng3 = np.random.default_rng(20261204)
+_DIMS = [16, 32, 48, 80, 96, 112]
+DIM_FWD_CASES = [(int(_rng3.integers(1, 3)), int(_rng3.integers(1, 4)), int(_rng3.integers(1, 500)),
+                  int(_rng3.choice(_DIMS)), round(float(_rng3.uniform(-0.5, 2.0)), 3),
+                  float(_rng3.choice([1.0, 2.0, 1.5, 0.7, 3.0])), str(_rng3.choice(["bf16", "bf16", "f32"])))
+                 for _ in range(10)]
+DIM_BWD_CASES = [(1, int(_rng3.integers(1, 3)), int(_rng3.integers(1, 400)), int(_rng3.choice(_DIMS)),
+                  round(float(_rng3.uniform(-0.5, 2.0)), 3), float(_rng3.choice([1.0, 2.0, 1.5, 2.5])))
+                 for _ in range(6)]
+DIM_DIFF_CASES = [(1, int(_rng3.integers(1, 3)), int(_rng3.integers(1, 400)), int(_rng3.choice(_DIMS)),
+                   round(float(_rng3.uniform(-0.3, 1.0)), 3), round(float(_rng3.uniform(-0.5, 1.5)), 3),
+                   float(_rng3.choice([1.0, 2.0, 1.5])), bool(_rng3.integers(0, 2))) for _ in range(6)]
+
+
+@pytest.mark.parametrize("B,H,T,D,beta,p,dtype", DIM_FWD_CASES)
+def test_tra_forward_random_head_dims(B, H, T, D, beta, p, dtype):
+    q, k, v = workloads.tra_inputs(B, H, T, D, dtype, seed=T * 3 + D)
+    out = bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), beta, p)
+    torch.cuda.synchronize()
+    ref = otra.tra_forward(f64(q), f64(k), f64(v), beta, p)
+    if float(np.abs(ref).max()) == 0.0:
+        assert float(out.abs().max()) == 0.0
+        return
+    err = rel_err(f64(out), ref)
+    assert err <= (2e-2 if dtype == "bf16" else 1e-4), f"max err {err:.3e} of max|ref|"
+
+
+@pytest.mark.parametrize("B,H,T,D,beta,p", DIM_BWD_CASES)
+def test_tra_backward_random_head_dims(B, H, T, D, beta, p):
+    test_tra_backward_random_shapes(B, H, T, D, beta, p)
+
+
+@pytest.mark.parametrize("B,H,T,D,beta,lam,p,norm", DIM_DIFF_CASES)
+def test_tra_diff_random_head_dims(B, H, T, D, beta, lam, p, norm):
+    test_tra_diff_random_shapes(B, H, T, D, beta, lam, p, norm)
