@@ -11,10 +11,10 @@
 // one LOP3), log2 m from a degree-5 minimax polynomial (Remez exchange fit,
 // block_sparse_attention_tra_gb300/log2_poly.py; max error 1.6e-5 evaluated
 // in float32) by Horner's rule on packed f32x2 FMAs, with p folded into the
-// coefficients.  A smaller share takes exp2 off MUFU as well (exp2_fma):
-// n = round(y), f = y - n, 2^f from a degree-4 minimax polynomial (Remez
-// exchange on the relative error, exp2_poly.py), the exponent raised by n
-// with one integer add.
+// coefficients.  exp2 can leave MUFU for a share of the pairs too
+// (exp2_fma: n = round(y), f = y - n, 2^f from a degree-4 minimax
+// polynomial, the exponent raised by n with one integer add), but every
+// share of it measured slower, so none is taken by default.
 #pragma once
 
 #include "kernels.h"
