@@ -61,13 +61,15 @@ def same(a, b):
     (2, 3, 333, 64, 2.0, 1.5, "bf16"),
     (1, 2, 129, 128, 0.5, 1.0, "bf16"),
     (1, 2, 130, 64, 1.0, 1.5, "f32"),
+    (1, 2, 200, 96, 1.0, 2.0, "bf16"),   # head dim below the tile width 128
+    (1, 1, 150, 48, 2.0, 1.5, "bf16"),
 ])
 def test_tra_forward_debug_build(debug_lib, B, H, T, D, beta, p, dtype):
     q, k, v = (t.cuda() for t in workloads.tra_inputs(B, H, T, D, dtype, seed=T))
     same(*both(debug_lib, lambda: bsa.tra_forward(q, k, v, beta, p)))
 
 
-@pytest.mark.parametrize("T,D,p", [(1, 64, 2.0), (300, 128, 2.0), (257, 64, 1.5), (200, 32, 2.0)])
+@pytest.mark.parametrize("T,D,p", [(1, 64, 2.0), (300, 128, 2.0), (257, 64, 1.5), (200, 32, 2.0), (200, 80, 1.5)])
 def test_tra_backward_and_diff_debug_build(debug_lib, T, D, p):
     q, k, v = (t.cuda() for t in workloads.tra_inputs(1, 2, T, D, "bf16", seed=T + 1))
     q2, k2, _ = (t.cuda() for t in workloads.tra_inputs(1, 2, T, D, "bf16", seed=T + 2))
