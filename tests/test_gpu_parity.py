@@ -423,3 +423,42 @@ def test_tra_forward_host_reuses_workspace():
     torch.cuda.synchronize()
     for (q, k, v), got in zip(ins, outs):
         assert torch.equal(got, bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), 1.0, 2.0).cpu())
+
+
+def test_tra_forward_host_concurrent_callers():
+    # Two host threads, each with its own stream and workspace, call the
+    # host-buffer entry point on different inputs at the same time: the
+    # library's per-device pipeline serialises the enqueueing, and every
+    # result must equal the device path bit for bit.
+    import threading
+
+    import torch
+
+    B, H, T, D = 1, 6, 300, 64
+    ins = [workloads.tra_inputs(B, H, T, D, "bf16", seed=40 + s) for s in range(2)]
+    wants = [bsa.tra_forward(q.cuda(), k.cuda(), v.cuda(), 1.0, 1.5).cpu() for q, k, v in ins]
+    results, errors = [[None] * 4 for _ in range(2)], []
+
+    def worker(idx):
+        try:
+            stream = torch.cuda.Stream()
+            ws = torch.empty(bsa.tra_forward_host_workspace_size(B, H, T, D, 1), dtype=torch.uint8, device="cuda")
+            hq, hk, hv = (t.pin_memory() for t in ins[idx])
+            for rep in range(4):
+                out = torch.empty(hq.shape, dtype=hq.dtype, pin_memory=True)
+                results[idx][rep] = bsa.tra_forward_host(hq, hk, hv, 1.0, 1.5, out=out, workspace=ws,
+                                                         stream=stream)
+            stream.synchronize()
+        except Exception as e:  # reported on the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for idx in range(2):
+        for rep in range(4):
+            assert torch.equal(results[idx][rep], wants[idx]), (idx, rep)
