@@ -185,3 +185,49 @@ def test_tra_backward_repeatability(D):
         a, b = f64(a), f64(b)
         assert float(np.abs(a - b).max()) <= TOL * max(float(np.abs(b).max()), 1e-30)
 
+
+
+def test_tra_backward_concurrent_streams():
+    # Two host threads run the fused backward (whose fp32 dq accumulator is a
+    # stream-ordered temporary from the library's pool) and the normalised
+    # differential forward (pool temporary for the normalised keys) on their
+    # own streams at once; the results must equal the same calls made one
+    # after the other (dk, dv and the differential output bit for bit, dq
+    # within the bar: its partials are added in a run-dependent order).
+    import threading
+
+    B, H, T, D = 1, 3, 700, 128
+    ins = []
+    for s in range(2):
+        q, k, v = (t.cuda() for t in workloads.tra_inputs(B, H, T, D, "bf16", seed=60 + s))
+        do = torch.randn(q.shape, generator=torch.Generator().manual_seed(s)).to(torch.bfloat16).cuda()
+        ins.append((q, k, v, do))
+    want = [bsa.tra_backward(q, k, v, do, 1.0, 2.0) for q, k, v, do in ins]
+    want_d = [bsa.tra_diff_forward(q, k, v, do, v, 0.5, 0.3, 1.5, normalize=True) for q, k, v, do in ins]
+    torch.cuda.synchronize()
+    got, got_d, errors = [None, None], [None, None], []
+
+    def worker(i):
+        try:
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                q, k, v, do = ins[i]
+                for _ in range(3):
+                    got[i] = bsa.tra_backward(q, k, v, do, 1.0, 2.0, stream=st)
+                    got_d[i] = bsa.tra_diff_forward(q, k, v, do, v, 0.5, 0.3, 1.5, normalize=True, stream=st)
+            st.synchronize()
+        except Exception as e:
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for i in range(2):
+        assert torch.equal(got[i][1], want[i][1]) and torch.equal(got[i][2], want[i][2])
+        a, b = f64(got[i][0]), f64(want[i][0])
+        assert float(np.abs(a - b).max()) <= TOL * max(float(np.abs(b).max()), 1e-30)
+        assert torch.equal(got_d[i], want_d[i])
