@@ -13,6 +13,10 @@ kernel for sm_103a behind a C ABI (``include/bsa.h``, ``libbsa.so``):
   partials, a log-sum-exp combine.
 * ``tra_forward_host`` -- ``tra_forward`` on host tensors, streamed through
   the GPU in chunks of heads with overlapped copies.
+* ``tra_backward`` and ``tra_attention`` -- the gradients of ``tra_forward``,
+  and the forward as a ``torch.autograd.Function`` whose backward runs them
+  (the page's ThresholdRelaFunction); ``tra_diff_forward`` -- the page's
+  differential form.
 
 The binding in ``bsa`` only marshals arguments; every step runs in the CUDA
 library, which is loaded on first use and must be built (``build.build()``).
@@ -29,6 +33,7 @@ from .bsa import (  # noqa: F401
     nsa_select_forward_raw,
     nsa_select_fsa_workspace_size,
     status_string,
+    tra_attention,
     tra_backward,
     tra_backward_raw,
     tra_diff_forward,
@@ -52,6 +57,7 @@ __all__ = [
     "tra_forward_host",
     "tra_forward_host_raw",
     "tra_forward_host_workspace_size",
+    "tra_attention",
     "tra_backward",
     "tra_backward_raw",
     "tra_diff_forward",

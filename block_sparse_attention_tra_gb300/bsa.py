@@ -284,6 +284,42 @@ def tra_forward_host(q, k, v, beta: float, p: float = 2.0, out=None, workspace=N
     return out
 
 
+_TRA_FUNCTION = None
+
+
+def _tra_function():
+    """The autograd function of the threshold attention (page
+    "triton_threshold_attention.py", ThresholdRelaFunction): forward through
+    ``tra_forward``, backward through ``tra_backward``; both on torch's
+    current stream."""
+    global _TRA_FUNCTION
+    if _TRA_FUNCTION is None:
+        import torch
+
+        class TraFunction(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, beta, p):
+                ctx.save_for_backward(q, k, v)
+                ctx.beta, ctx.p = float(beta), float(p)
+                return tra_forward(q, k, v, beta, p)
+
+            @staticmethod
+            def backward(ctx, dout):
+                q, k, v = ctx.saved_tensors
+                dq, dk, dv = tra_backward(q, k, v, dout.to(q.dtype).contiguous(), ctx.beta, ctx.p)
+                return dq, dk, dv, None, None
+
+        _TRA_FUNCTION = TraFunction
+    return _TRA_FUNCTION
+
+
+def tra_attention(q, k, v, beta: float, p: float = 2.0):
+    """Threshold rectified attention with autograd: ``tra_forward`` whose
+    gradients with respect to q, k and v come from ``tra_backward`` (CUDA
+    tensors ``[B, H, T, D]``, bfloat16 or float32)."""
+    return _tra_function().apply(q, k, v, beta, p)
+
+
 def tra_backward(q, k, v, dout, beta: float, p: float = 2.0, stream=None, deterministic: bool = False):
     """Gradients ``(dq, dk, dv)`` of the threshold rectified attention
     forward for the upstream gradient ``dout``; bf16 or fp32 CUDA tensors

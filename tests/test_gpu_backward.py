@@ -231,3 +231,24 @@ def test_tra_backward_concurrent_streams():
         a, b = f64(got[i][0]), f64(want[i][0])
         assert float(np.abs(a - b).max()) <= TOL * max(float(np.abs(b).max()), 1e-30)
         assert torch.equal(got_d[i], want_d[i])
+
+
+@pytest.mark.parametrize("dtype,D,p", [("bf16", 128, 2.0), ("bf16", 64, 1.5), ("f32", 64, 2.0)])
+def test_tra_attention_autograd(dtype, D, p):
+    # the autograd form: forward through tra_forward, q/k/v gradients through
+    # tra_backward, against the float64 oracle's analytic gradients
+    B, H, T = 1, 2, 300
+    q, k, v = (t.cuda().requires_grad_(True) for t in workloads.tra_inputs(B, H, T, D, dtype, seed=T + D))
+    w = torch.randn((B, H, T, D), generator=torch.Generator().manual_seed(3))
+    out = bsa.tra_attention(q, k, v, 1.0, p)
+    assert out.dtype == q.dtype
+    (out.float() * w.cuda()).sum().backward()
+    torch.cuda.synchronize()
+    dout = w.to(q.dtype).double().numpy()  # the gradient reaching `out`, in its dtype
+    refs = otra.tra_backward(f64(q), f64(k), f64(v), dout, 1.0, p)
+    tol = TOL if dtype == "bf16" else F32_TOL
+    for name, t, ref in (("dq", q, refs[0]), ("dk", k, refs[1]), ("dv", v, refs[2])):
+        err = float(np.abs(f64(t.grad) - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
+        assert err <= tol, f"{name}: max err {err:.3e} of max|ref|"
+    fwd = otra.tra_forward(f64(q), f64(k), f64(v), 1.0, p)
+    assert float(np.abs(f64(out) - fwd).max()) <= tol * float(np.abs(fwd).max())
