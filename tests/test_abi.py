@@ -209,3 +209,16 @@ def test_tra_forward_host_workspace_and_argument_errors(lib):
     assert call(nbytes=need - 1) == 9                # workspace too small
     if not __import__("torch").cuda.is_available():  # (with a device it would copy from the fake host pointers)
         assert call() == 6                           # valid arguments, no device here
+
+
+def test_selftest_argument_errors(lib):
+    # the self-test entry points validate their arguments on the host too
+    assert lib.bsa_selftest_log2(None, P, P, 4, None) == 1
+    assert lib.bsa_selftest_exp2(P, None, P, 4, None) == 1
+    assert lib.bsa_selftest_exp2(P, P, P, 0, None) == 2
+    assert lib.bsa_selftest_log2(P, P, P, -3, None) == 2
+    assert lib.bsa_selftest_exp2(P + 2, P, P, 4, None) == 7
+    assert lib.bsa_selftest_wait_timeout(0, P, None) == 2       # limit out of range
+    assert lib.bsa_selftest_wait_timeout(1000, None, None) == 1
+    if not __import__("torch").cuda.is_available():
+        assert lib.bsa_selftest_exp2(P, P, P, 4, None) == 6
