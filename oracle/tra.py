@@ -183,6 +183,46 @@ def tra_diff_forward(q1, q2, k1, k2, v, beta: float, lam: float, p: float, norma
     return tra_forward(q1, k1, v, beta, p, block) - lam_c * tra_forward(q2, k2, v, beta, p, block)
 
 
+def l2_normalize_backward(x, dxn, eps: float = 1e-12) -> np.ndarray:
+    """Gradient of ``x -> x / max(||x||, eps)`` (row-wise, last axis) for the
+    upstream gradient ``dxn``: with n = ||x|| > eps and xn = x / n,
+    ``dx = (dxn - xn (xn . dxn)) / n``; rows with n <= eps (where the map is
+    x / eps) give ``dxn / eps``."""
+    x = np.asarray(x, dtype=np.float64)
+    dxn = np.asarray(dxn, dtype=np.float64)
+    n = np.sqrt((x * x).sum(axis=-1, keepdims=True))
+    big = n > eps
+    xn = x / np.where(big, n, 1.0)
+    proj = (xn * dxn).sum(axis=-1, keepdims=True)
+    return np.where(big, (dxn - xn * proj) / np.where(big, n, 1.0), dxn / eps)
+
+
+def tra_diff_backward(q1, q2, k1, k2, v, dout, beta: float, lam: float, p: float, normalize: bool = True):
+    """Gradients of ``tra_diff_forward`` (the page's
+    ``differential_threshold_rela_triton``, differentiated through its
+    normalisation, its two ``ThresholdRelaFunction`` calls and the clamp):
+
+        out = TRA(a1, b1, v) - c TRA(a2, b2, v),  c = clamp(lam, 0, 1),
+        a = n(q), b = n(k) (the identity without ``normalize``).
+
+    Returns ``(dq1, dq2, dk1, dk2, dv, dlam)``: each path's (da, db, dv) is
+    ``tra_backward`` with the upstream gradient dout and -c dout; dv sums
+    both paths; da, db go back through the normalisation; and
+    ``dlam = -sum(dout * TRA(a2, b2, v))`` where 0 < lam < 1 (the clamp's
+    derivative is 0 outside)."""
+    dout = np.asarray(dout, dtype=np.float64)
+    ins = [np.asarray(t, dtype=np.float64) for t in (q1, q2, k1, k2)]
+    a1, a2, b1, b2 = (l2_normalize(t) for t in ins) if normalize else ins
+    c = min(max(float(lam), 0.0), 1.0)
+    da1, db1, dv1 = tra_backward(a1, b1, v, dout, beta, p)
+    da2, db2, dv2 = tra_backward(a2, b2, v, -c * dout, beta, p)
+    dv = dv1 + dv2
+    if normalize:
+        da1, da2, db1, db2 = (l2_normalize_backward(x, g) for x, g in zip(ins, (da1, da2, db1, db2)))
+    dlam = -float((dout * tra_forward(a2, b2, v, beta, p)).sum()) if 0.0 < float(lam) < 1.0 else 0.0
+    return da1, da2, db1, db2, dv, dlam
+
+
 def tra_flops(B: int, H: int, T: int, D: int) -> int:
     """Algorithmic FLOPs of one causal TRA forward: two multiply-adds of length
     D (one for q_i.k_j, one for w_ij v_j) per causally valid pair (i, j<=i)."""

@@ -742,3 +742,63 @@ def test_planted_fsa_mistakes_are_caught(golden, monkeypatch):
         assert not pins(), bad.__name__
     monkeypatch.setattr(fsa, "fsa_partials", good)
     assert pins()
+
+
+def _torch_diff(q1, q2, k1, k2, v, beta, lam, p, normalize):
+    """The page's differential_threshold_rela_triton, written with torch
+    autograd ops on the textbook TRA (for the gradient pin)."""
+    if normalize:
+        q1, q2, k1, k2 = (torch.nn.functional.normalize(t, p=2, dim=-1) for t in (q1, q2, k1, k2))
+    return _torch_tra(q1, k1, v, beta, p) - torch.clamp(lam, 0.0, 1.0) * _torch_tra(q2, k2, v, beta, p)
+
+
+@pytest.mark.parametrize("normalize", [True, False])
+@pytest.mark.parametrize("p,lam", [(2.0, 0.4), (1.5, 0.7), (3.0, 1.3), (1.0, -0.2)])
+def test_tra_diff_backward_matches_torch_autograd(normalize, p, lam):
+    q1, k1, v = rand_tra(2, 2, 23, 6, seed=40)
+    q2, k2, _ = rand_tra(2, 2, 23, 6, seed=41)
+    do = rng(42).standard_normal(q1.shape)
+    beta = 0.3 if normalize else 0.8
+    got = tra.tra_diff_backward(q1, q2, k1, k2, v, do, beta, lam, p, normalize=normalize)
+    ts = [torch.tensor(a, requires_grad=True) for a in (q1, q2, k1, k2, v)]
+    lt = torch.tensor(float(lam), dtype=torch.float64, requires_grad=True)
+    out = _torch_diff(*ts, beta, lt, p, normalize)
+    want = torch.autograd.grad((out * torch.tensor(do)).sum(), ts + [lt])
+    for g, w in zip(got[:5], want[:5]):
+        np.testing.assert_allclose(g, w.numpy(), rtol=1e-9, atol=1e-11)
+    assert got[5] == pytest.approx(float(want[5]), rel=1e-9, abs=1e-11)
+
+
+def test_tra_diff_backward_finite_differences():
+    """Central differences of L = sum(out * dout) of the oracle's own forward."""
+    q1, k1, v = rand_tra(1, 1, 8, 4, seed=43)
+    q2, k2, _ = rand_tra(1, 1, 8, 4, seed=44)
+    do = rng(45).standard_normal(q1.shape)
+    beta, lam, p = 0.1, 0.35, 2.0
+    grads = tra.tra_diff_backward(q1, q2, k1, k2, v, do, beta, lam, p)
+
+    def L(args, lm=lam):
+        return float((tra.tra_diff_forward(*args, beta, lm, p) * do).sum())
+
+    base = [q1, q2, k1, k2, v]
+    h = 1e-6
+    r = rng(46)
+    for which in range(5):
+        for _ in range(6):
+            idx = tuple(int(r.integers(n)) for n in q1.shape)
+            a = [t.copy() for t in base]
+            a[which][idx] += h
+            lp = L(a)
+            a[which][idx] -= 2 * h
+            lm_ = L(a)
+            assert grads[which][idx] == pytest.approx((lp - lm_) / (2 * h), rel=1e-5, abs=1e-7)
+    assert grads[5] == pytest.approx((L(base, lam + h) - L(base, lam - h)) / (2 * h), rel=1e-5, abs=1e-7)
+
+
+def test_l2_normalize_backward_matches_torch():
+    x = rng(47).standard_normal((2, 3, 7, 5))
+    x[0, 0, 0] = 0.0  # below eps: the map is x / eps there
+    g = rng(48).standard_normal(x.shape)
+    xt = torch.tensor(x, requires_grad=True)
+    (want,) = torch.autograd.grad((torch.nn.functional.normalize(xt, p=2, dim=-1) * torch.tensor(g)).sum(), xt)
+    np.testing.assert_allclose(tra.l2_normalize_backward(x, g), want.numpy(), rtol=1e-10, atol=1e-12)
