@@ -15,8 +15,9 @@ kernel for sm_103a behind a C ABI (``include/bsa.h``, ``libbsa.so``):
   the GPU in chunks of heads with overlapped copies.
 * ``tra_backward`` and ``tra_attention`` -- the gradients of ``tra_forward``,
   and the forward as a ``torch.autograd.Function`` whose backward runs them
-  (the page's ThresholdRelaFunction); ``tra_diff_forward`` -- the page's
-  differential form.
+  (the page's ThresholdRelaFunction); ``tra_diff_forward``,
+  ``tra_diff_backward`` and ``tra_diff_attention`` -- the page's differential
+  form, its gradients and the two as an autograd function.
 
 The binding in ``bsa`` only marshals arguments; every step runs in the CUDA
 library, which is loaded on first use and must be built (``build.build()``).
@@ -36,6 +37,9 @@ from .bsa import (  # noqa: F401
     tra_attention,
     tra_backward,
     tra_backward_raw,
+    tra_diff_attention,
+    tra_diff_backward,
+    tra_diff_backward_raw,
     tra_diff_forward,
     tra_diff_forward_raw,
     tra_forward,
@@ -60,6 +64,9 @@ __all__ = [
     "tra_attention",
     "tra_backward",
     "tra_backward_raw",
+    "tra_diff_attention",
+    "tra_diff_backward",
+    "tra_diff_backward_raw",
     "tra_diff_forward",
     "tra_diff_forward_raw",
     "nsa_select_forward",

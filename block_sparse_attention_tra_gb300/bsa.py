@@ -90,6 +90,8 @@ def open_library(path):
     lib.tra_backward_ex.restype = i32
     lib.tra_diff_forward.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, f32, i32, i32, vp]
     lib.tra_diff_forward.restype = i32
+    lib.tra_diff_backward.argtypes = [vp] * 12 + [i32, i32, i32, i32, f32, f32, f32, i32, i32, vp]
+    lib.tra_diff_backward.restype = i32
     lib.tra_diff_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, f32, i32, i32,
                                              vp]
     lib.tra_diff_forward_noalloc.restype = i32
@@ -168,6 +170,15 @@ def tra_diff_forward_raw(q1, q2, k1, k2, v, out, B, H, T, D, beta, lam, p, norma
     """Direct C call with integer device pointers; returns the bsa_status."""
     return load_library().tra_diff_forward(q1, q2, k1, k2, v, out, B, H, T, D, float(beta), float(lam), float(p),
                                            int(bool(normalize)), int(dtype), stream)
+
+
+def tra_diff_backward_raw(q1, q2, k1, k2, v, dout, dq1, dq2, dk1, dk2, dv, dlam, B, H, T, D, beta, lam, p,
+                          normalize, dtype, stream=0) -> int:
+    """Direct C call of tra_diff_backward with integer device pointers (dlam
+    may be None); returns the bsa_status."""
+    return load_library().tra_diff_backward(q1, q2, k1, k2, v, dout, dq1, dq2, dk1, dk2, dv, dlam, B, H, T, D,
+                                            float(beta), float(lam), float(p), int(bool(normalize)), int(dtype),
+                                            stream)
 
 
 def tra_diff_forward_noalloc_raw(q1, q2, k1, k2, v, out, B, H, T, D, beta, lam, p, normalize, dtype,
@@ -369,6 +380,75 @@ def tra_diff_forward(q1, q2, k1, k2, v, beta: float, lam: float, p: float = 2.0,
     _check(st, "tra_diff_forward")
     return out
 
+
+
+def tra_diff_backward(q1, q2, k1, k2, v, dout, beta: float, lam: float, p: float = 2.0, normalize: bool = True,
+                      want_dlam: bool = False, stream=None):
+    """Gradients ``(dq1, dq2, dk1, dk2, dv, dlam)`` of ``tra_diff_forward`` for
+    the upstream gradient ``dout`` (bf16 or fp32 CUDA tensors ``[B, H, T,
+    D]``); ``dlam`` is a 1-element float32 CUDA tensor when ``want_dlam``,
+    else None."""
+    import torch
+
+    ts = (q1, q2, k1, k2, v, dout)
+    if q1.device.type != "cuda":
+        raise BsaError("tra_diff_backward takes CUDA tensors (no CPU path)")
+    if any(t.shape != q1.shape for t in ts) or q1.dim() != 4:
+        raise BsaError("q1, q2, k1, k2, v, dout must share one shape [B, H, T, D]", 2)
+    if any(t.dtype != q1.dtype for t in ts):
+        raise BsaError("q1, q2, k1, k2, v, dout must share one dtype", 3)
+    ts = tuple(t.contiguous() for t in ts)
+    grads = tuple(torch.empty_like(q1) for _ in range(5))
+    dlam = torch.empty(1, dtype=torch.float32, device=q1.device) if want_dlam else None
+    B, H, T, D = q1.shape
+    st = tra_diff_backward_raw(*(t.data_ptr() for t in ts), *(g.data_ptr() for g in grads),
+                               dlam.data_ptr() if dlam is not None else None, B, H, T, D, beta, lam, p, normalize,
+                               _dtype_code(q1), _stream_handle(stream))
+    _check(st, "tra_diff_backward")
+    return grads + (dlam,)
+
+
+_TRA_DIFF_FUNCTION = None
+
+
+def _tra_diff_function():
+    """The autograd function of the differential form (page
+    "triton_threshold_attention.py", differential_threshold_rela_triton):
+    forward through ``tra_diff_forward``, backward through
+    ``tra_diff_backward``; lambda may be a float or a 0-d / 1-element tensor
+    (its gradient is returned when it requires one)."""
+    global _TRA_DIFF_FUNCTION
+    if _TRA_DIFF_FUNCTION is None:
+        import torch
+
+        class TraDiffFunction(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q1, q2, k1, k2, v, beta, lam, p, normalize):
+                lam_f = float(lam)
+                ctx.save_for_backward(q1, q2, k1, k2, v)
+                ctx.args = (float(beta), lam_f, float(p), bool(normalize))
+                ctx.lam_tensor = isinstance(lam, torch.Tensor)
+                return tra_diff_forward(q1, q2, k1, k2, v, beta, lam_f, p, normalize=normalize)
+
+            @staticmethod
+            def backward(ctx, dout):
+                q1, q2, k1, k2, v = ctx.saved_tensors
+                beta, lam, p, normalize = ctx.args
+                want = ctx.lam_tensor and ctx.needs_input_grad[6]
+                dq1, dq2, dk1, dk2, dv, dlam = tra_diff_backward(q1, q2, k1, k2, v, dout.to(q1.dtype), beta, lam, p,
+                                                                 normalize, want_dlam=want)
+                dl = dlam.reshape(()) if want else None
+                return dq1, dq2, dk1, dk2, dv, None, dl, None, None
+
+        _TRA_DIFF_FUNCTION = TraDiffFunction
+    return _TRA_DIFF_FUNCTION
+
+
+def tra_diff_attention(q1, q2, k1, k2, v, beta: float, lam, p: float = 2.0, normalize: bool = True):
+    """Threshold differential attention with autograd: ``tra_diff_forward``
+    whose gradients with respect to q1, q2, k1, k2, v (and lambda, when it is
+    a tensor that requires one) come from ``tra_diff_backward``."""
+    return _tra_diff_function().apply(q1, q2, k1, k2, v, beta, lam, p, normalize)
 
 def nsa_select_forward(q, k, v, block_idx, block_size: int = 64, out=None, lse=None,
                        return_lse: bool = False, stream=None):

@@ -295,6 +295,33 @@ int tra_diff_forward(const void* q1, const void* q2, const void* k1, const void*
   return st;
 }
 
+int tra_diff_backward(const void* q1, const void* q2, const void* k1, const void* k2, const void* v,
+                      const void* dout, void* dq1, void* dq2, void* dk1, void* dk2, void* dv, float* dlambda, int B,
+                      int H, int T, int D, float beta, float lambda, float p, int normalize, int dtype,
+                      cudaStream_t stream) {
+  const int chk = check_diff_args(q1, q2, k1, k2, v, dq1, B, H, T, D, beta, lambda, p, dtype);
+  if (chk != BSA_OK) return chk;
+  const void* more[5] = {dout, dq2, dk1, dk2, dv};
+  for (const void* ptr : more) {
+    if (ptr == nullptr) return BSA_ERR_NULLPTR;
+    if (!aligned16(ptr)) return BSA_ERR_ALIGN;
+  }
+  if ((reinterpret_cast<uintptr_t>(dlambda) & 3u) != 0) return BSA_ERR_ALIGN;
+  const int dvs = check_device();
+  if (dvs != OK) return dvs;
+  const bool f32 = dtype == BSA_F32;
+  const size_t bytes = tra_diff_bwd_scratch_bytes(B, H, T, D, f32, normalize != 0, dlambda != nullptr);
+  void* scratch = nullptr;
+  int dev = 0;
+  cudaMemPool_t pool = cudaGetDevice(&dev) == cudaSuccess ? scratch_pool(dev) : nullptr;
+  if (pool == nullptr) return BSA_ERR_MEMORY;
+  if (cudaMallocFromPoolAsync(&scratch, bytes, pool, stream) != cudaSuccess) return BSA_ERR_MEMORY;
+  const int st = launch_tra_diff_bwd(q1, q2, k1, k2, v, dout, dq1, dq2, dk1, dk2, dv, dlambda, B, H, T, D, beta,
+                                     lambda, p, normalize != 0, f32, scratch, stream);
+  if (cudaFreeAsync(scratch, stream) != cudaSuccess && st == OK) return BSA_ERR_MEMORY;
+  return st;
+}
+
 int tra_diff_forward_noalloc(const void* q1, const void* q2, const void* k1, const void* k2, const void* v,
                              void* out, int B, int H, int T, int D, float beta, float lambda, float p, int normalize,
                              int dtype, cudaStream_t stream) {

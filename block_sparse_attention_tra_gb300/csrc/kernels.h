@@ -62,6 +62,16 @@ int launch_tra_bwd_fused_bf16(const void* q, const void* k, const void* v, const
                               void* dv, int B, int H, int T, int D, float beta, float p, float* dq_acc,
                               cudaStream_t stream);
 
+// Gradients of the threshold differential attention (tra_diff_bwd.cu): the
+// normalisation, both paths' backward passes, their combination and dlam
+// (nullable; written, 0 outside 0 < lam < 1).  scratch: 256-byte aligned, at
+// least tra_diff_bwd_scratch_bytes(B, H, T, D, f32, normalize, dlam != null).
+size_t tra_diff_bwd_scratch_bytes(int B, int H, int T, int D, bool f32, bool normalize, bool dlam);
+int launch_tra_diff_bwd(const void* q1, const void* q2, const void* k1, const void* k2, const void* v,
+                        const void* dout, void* dq1, void* dq2, void* dk1, void* dk2, void* dv, float* dlam, int B,
+                        int H, int T, int D, float beta, float lam, float p, bool normalize, bool f32, void* scratch,
+                        cudaStream_t stream);
+
 // fp32 forms of the backward and of the differential forward (CUDA-core FFMA
 // kernels, tra_f32_ext.cu); the differential one needs no scratch memory.
 int launch_tra_bwd_f32(const float* q, const float* k, const float* v, const float* dout, float* dq, float* dk,

@@ -279,6 +279,49 @@ BSA_API int tra_diff_forward(const void* q1, const void* q2, const void* k1,
                              cudaStream_t stream);
 
 /*
+ * tra_diff_backward -- gradients of tra_diff_forward (page
+ * "triton_threshold_attention.py", differential_threshold_rela_triton,
+ * differentiated through its normalisation, its two ThresholdRelaFunction
+ * calls and the clamp of lambda).  With a = n(q), b = n(k) (row-wise L2
+ * normalisation x / max(||x||, 1e-12) when normalize, else the identity) and
+ * c = clamp(lambda, 0, 1):
+ *   out = TRA(a1, b1, v) - c TRA(a2, b2, v),
+ *   dv  = dv1 - c dv2, (da1, db1, dv1) = tra_backward(a1, b1, v, dout),
+ *   (da2, db2, dv2) = -c ... of tra_backward(a2, b2, v, dout) (TRA's gradients
+ *   are linear in dout), dq1 = n'(q1)^T da1 etc. through the normalisation,
+ *   dlambda = -sum(dout * TRA(a2, b2, v)) for 0 < lambda < 1, else 0.
+ * bf16 runs the fused tcgen05 backward twice on normalised bf16 copies of
+ * q1, q2, k1, k2 (taken from the inputs in fp32 and rounded once) and takes
+ * the gradients through the normalisation in fp32; BSA_F32 the CUDA-core
+ * kernels.  Temporaries (the copies, both passes' gradients, the fused
+ * backward's fp32 dq accumulator and, for dlambda, TRA(a2, b2, v)) come
+ * from the library's stream-ordered pool as for tra_diff_forward.  The dq
+ * outputs, like tra_backward's, may differ in their last bf16 bit between
+ * runs (fp32 partials added in a run-dependent order); so may dlambda (one
+ * atomic addition per block).
+ *
+ *   q1, q2, k1, k2, v, dout        : [B, H, T, D] of `dtype` (inputs).
+ *   dq1, dq2, dk1, dk2, dv         : [B, H, T, D] of `dtype` (outputs; they
+ *                                    must not alias the inputs or each other).
+ *   dlambda                        : device float (4-byte aligned) written
+ *                                    with dlambda, or NULL to skip it (then
+ *                                    TRA(a2, b2, v) is not formed).
+ *   B, H, T, D, beta, lambda, p,
+ *   normalize, dtype               : as for tra_diff_forward.
+ *
+ * Errors: as for tra_diff_forward (BSA_ERR_NULLPTR for any null tensor,
+ * BSA_ERR_ALIGN for a tensor not 16-byte aligned or a misaligned dlambda),
+ * plus BSA_ERR_MEMORY.
+ */
+BSA_API int tra_diff_backward(const void* q1, const void* q2, const void* k1,
+                              const void* k2, const void* v,
+                              const void* dout, void* dq1, void* dq2,
+                              void* dk1, void* dk2, void* dv, float* dlambda,
+                              int B, int H, int T, int D, float beta,
+                              float lambda, float p, int normalize, int dtype,
+                              cudaStream_t stream);
+
+/*
  * tra_diff_forward_noalloc -- tra_diff_forward without any allocation.
  *
  * The source pages have no counterpart to this entry point; it exists for

@@ -222,3 +222,19 @@ def test_selftest_argument_errors(lib):
     assert lib.bsa_selftest_wait_timeout(1000, None, None) == 1
     if not __import__("torch").cuda.is_available():
         assert lib.bsa_selftest_exp2(P, P, P, 4, None) == 6
+
+
+def test_diff_backward_argument_errors(lib):
+    from block_sparse_attention_tra_gb300 import bsa
+
+    def call(dout=P, dq1=P, dv=P, dlam=None, D=64, lam=0.5, dtype=1):
+        return bsa.tra_diff_backward_raw(P, P, P, P, P, dout, dq1, P, P, P, dv, dlam, 1, 1, 16, D, 1.0, lam, 2.0, 1,
+                                         dtype, 0)
+
+    assert call(dout=None) == 1 and call(dq1=None) == 1 and call(dv=None) == 1
+    assert call(dv=P + 8) == 7
+    assert call(dlam=P + 2) == 7
+    assert call(D=100) == 4 and call(lam=float("nan")) == 4
+    assert call(dtype=5) == 3
+    if not __import__("torch").cuda.is_available():
+        assert call() == 6 and call(dlam=P, dtype=0) == 6

@@ -144,3 +144,67 @@ def test_tra_diff_f32(B, H, T, D, beta, lam, p, norm):
                                           norm, bsa.BSA_F32, torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert st == 0 and torch.equal(out, out2)
+
+
+# Gradients of the differential form (tra_diff_backward) against the float64
+# oracle: each of dq1, dq2, dk1, dk2, dv within the bar of its own max|ref|,
+# and dlambda within the bar of sum|dout * TRA(a2, b2, v)| (the size of the
+# terms it sums).  Powers p > 1 only (plus p = 1 without normalisation): the
+# gradient's factor p x^(p-1) jumps at x = 0 for p = 1, and normalised scores
+# crowd around tau, so bf16 rounding of the inputs flips it for some pairs.
+BWD_CASES = [
+    # (B, H, T, D, beta, lam, p, normalize, dtype)
+    (1, 2, 300, 64, 0.2, 0.5, 2.0, True, "bf16"),
+    (1, 2, 257, 128, 0.1, 0.7, 1.5, True, "bf16"),
+    (2, 1, 200, 64, 0.5, 0.3, 2.0, False, "bf16"),
+    (1, 1, 150, 96, 0.0, 1.3, 2.0, True, "bf16"),   # lambda clamps to 1: dlambda 0
+    (1, 2, 130, 48, 0.3, -0.2, 2.0, True, "bf16"),  # lambda clamps to 0: path 2 gives nothing
+    (1, 1, 1, 64, 0.1, 0.4, 2.0, True, "bf16"),     # T = 1
+    (1, 2, 130, 64, 0.2, 0.5, 2.0, True, "f32"),
+    (1, 1, 100, 32, 0.1, 0.6, 1.5, False, "f32"),
+]
+
+
+@pytest.mark.parametrize("B,H,T,D,beta,lam,p,norm,dtype", BWD_CASES)
+def test_tra_diff_backward(B, H, T, D, beta, lam, p, norm, dtype):
+    g = torch.Generator().manual_seed(T + D)
+    scale = D ** -0.25 if not norm else 1.0
+    q1, q2, k1, k2, v, do = (torch.randn((B, H, T, D), generator=g) * (scale if i < 4 else 1.0) for i in range(6))
+    q1, q2, k1, k2, v, do = (t.to(torch.bfloat16 if dtype == "bf16" else torch.float32) for t in
+                             (q1, q2, k1, k2, v, do))
+    grads = bsa.tra_diff_backward(*(t.cuda() for t in (q1, q2, k1, k2, v, do)), beta, lam, p, normalize=norm,
+                                  want_dlam=True)
+    torch.cuda.synchronize()
+    h = [f64(t) for t in (q1, q2, k1, k2, v, do)]
+    refs = otra.tra_diff_backward(*h, beta, lam, p, normalize=norm)
+    tol = 2e-2 if dtype == "bf16" else 1e-4
+    for name, got, ref in zip(("dq1", "dq2", "dk1", "dk2", "dv"), grads[:5], refs[:5]):
+        scale_ref = float(np.abs(ref).max())
+        err = float(np.abs(f64(got) - ref).max())
+        assert err <= tol * max(scale_ref, 1e-30) or (scale_ref == 0.0 and err == 0.0), f"{name}: {err:.3e}"
+    a2, b2 = (otra.l2_normalize(x) for x in (h[1], h[3])) if norm else (h[1], h[3])
+    size = float(np.abs(h[5] * otra.tra_forward(a2, b2, h[4], beta, p)).sum())
+    assert abs(float(grads[5].item()) - refs[5]) <= tol * max(size, 1e-30)
+    if not 0.0 < lam < 1.0:
+        assert float(grads[5].item()) == 0.0
+
+
+def test_tra_diff_attention_autograd():
+    # the autograd form, with lambda a tensor that requires a gradient
+    B, H, T, D = 1, 2, 200, 64
+    g = torch.Generator().manual_seed(9)
+    ts = [torch.randn((B, H, T, D), generator=g).to(torch.bfloat16).cuda().requires_grad_(True) for _ in range(5)]
+    lam = torch.tensor(0.4, device="cuda", requires_grad=True)
+    w = torch.randn((B, H, T, D), generator=g).cuda()
+    out = bsa.tra_diff_attention(*ts, 0.2, lam, 2.0, normalize=True)
+    (out.float() * w).sum().backward()
+    torch.cuda.synchronize()
+    h = [f64(t) for t in ts]
+    refs = otra.tra_diff_backward(*h, f64(w.to(torch.bfloat16)), 0.2, 0.4, 2.0, normalize=True)
+    for name, t, ref in zip(("dq1", "dq2", "dk1", "dk2", "dv"), ts, refs[:5]):
+        err = float(np.abs(f64(t.grad) - ref).max()) / max(float(np.abs(ref).max()), 1e-30)
+        assert err <= 2e-2, f"{name}: max err {err:.3e} of max|ref|"
+    assert lam.grad is not None
+    a2, b2 = otra.l2_normalize(h[1]), otra.l2_normalize(h[3])
+    size = float(np.abs(f64(w.to(torch.bfloat16)) * otra.tra_forward(a2, b2, h[4], 0.2, 2.0)).sum())
+    assert abs(float(lam.grad) - refs[5]) <= 2e-2 * size
