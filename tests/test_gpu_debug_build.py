@@ -81,6 +81,12 @@ def test_tra_backward_and_diff_debug_build(debug_lib, T, D, p):
     ref = a[0].double()
     assert float((b[0].double() - ref).abs().max()) <= 2e-2 * max(float(ref.abs().max()), 1e-30)
     same(*both(debug_lib, lambda: bsa.tra_diff_forward(q, q2, k, k2, v, 0.1, 0.5, p, normalize=True)))
+    # the differential backward: dk1, dk2, dv bit for bit; dq1, dq2 (fused-backward partials) and dlambda
+    # (block sums added atomically) within the bar
+    a, b = both(debug_lib, lambda: bsa.tra_diff_backward(q, q2, k, k2, v, do, 0.1, 0.5, p, want_dlam=True))
+    same(a[2:5], b[2:5])
+    for x, y in ((a[0], b[0]), (a[1], b[1]), (a[5], b[5])):
+        assert float((y.double() - x.double()).abs().max()) <= 2e-2 * max(float(x.double().abs().max()), 1e-30)
 
 
 def odd_rows(idx, n_blk):
