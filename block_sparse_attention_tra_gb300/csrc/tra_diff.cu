@@ -43,6 +43,11 @@ using tile::PANEL_BYTES;
 constexpr int BT = tile::ROWS;
 constexpr int DIFF_TMA_WARP = 8;
 constexpr int DIFF_MMA_WARP = 9;  // first MMA warp (allocates TMEM)
+// General powers 1 <= p <= 64 with part of log2 on the FMA pipe (as the
+// single-stream kernel does).
+#ifndef BSA_DIFF_MIX
+#define BSA_DIFF_MIX 1
+#endif
 template <int D, int PC>
 struct DiffCfg {
   static constexpr int ISSUERS = (D == 64 && (PC == POW_ONE || PC == POW_TWO)) ? 2 : 1;
@@ -205,7 +210,9 @@ __global__ void __launch_bounds__(256) row_inv_norm_kernel(const __nv_bfloat16* 
 // of row and key): x = s (rq rk) - tau in one packed multiply and one packed
 // fused multiply-add per key pair.
 // DIAG (compile time): the tile holds the diagonal, mask keys after the row.
-template <int PC, int NM, bool DIAG>
+// POW_GENERAL_MIX: log2 of a share of the pairs on the FMA pipe, as in the
+// single-stream kernel (tra_math.cuh, mix_mufu_pairs; PLAN its plan).
+template <int PC, int NM, bool DIAG, int PLAN = 0>
 __device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t tS, int c0, const PowParams& wp,
                                              uint64_t rq2, uint64_t ntau2, const float (&rk)[32], int key0,
                                              int row) {
@@ -220,7 +227,8 @@ __device__ __forceinline__ void diff_quarter(const uint32_t (&s)[32], uint32_t t
       x2 = f2_fma(s2, rq2, ntau2);
     else
       x2 = f2_sub(s2, wp.tau2);
-    uint32_t w = weights2_x<PC>(x2, wp);
+    uint32_t w = (PC == POW_GENERAL_MIX && mix_pair_on_fma<PLAN>(e)) ? weights2_x<PC, true>(x2, wp)
+                                                                    : weights2_x<PC>(x2, wp);
     if constexpr (DIAG) {
       const int key = key0 + c0 + 2 * e;
       if (key > row) w = 0u;
@@ -447,9 +455,9 @@ __global__ void __launch_bounds__(DiffCfg<D, PC>::THREADS, 1)
           }
         }
         if (diag)
-          diff_quarter<PC, NM, true>(sv, tS, 32 * c, wp, rq2, ntau2, rk, n * BT, row);
+          diff_quarter<PC, NM, true, mix_mufu_pairs<D>()>(sv, tS, 32 * c, wp, rq2, ntau2, rk, n * BT, row);
         else
-          diff_quarter<PC, NM, false>(sv, tS, 32 * c, wp, rq2, ntau2, rk, n * BT, row);
+          diff_quarter<PC, NM, false, mix_mufu_pairs<D>()>(sv, tS, 32 * c, wp, rq2, ntau2, rk, n * BT, row);
       };
       uint32_t sa[32], sb[32];
       tmem_ld32(tS, sa);
@@ -531,6 +539,8 @@ int dispatch_pc(const CUtensorMap* maps, const float* inv, void* out, int BH, in
   const int pc = power_class(p);
   if (pc == POW_TWO) return launch_diff_kernel<D, POW_TWO, NM>(maps, inv, out, BH, T, beta, p, lam, d_real, stream);
   if (pc == POW_ONE) return launch_diff_kernel<D, POW_ONE, NM>(maps, inv, out, BH, T, beta, p, lam, d_real, stream);
+  if (pc == POW_GENERAL_MIX && BSA_DIFF_MIX)
+    return launch_diff_kernel<D, POW_GENERAL_MIX, NM>(maps, inv, out, BH, T, beta, p, lam, d_real, stream);
   return launch_diff_kernel<D, POW_GENERAL, NM>(maps, inv, out, BH, T, beta, p, lam, d_real, stream);
 }
 
