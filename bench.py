@@ -536,10 +536,11 @@ def run_ours(args):
              lambda: bsa.tra_backward(qb, kb, vb, dob, wb.beta, wb.p, deterministic=True), 10 * wb.flops // 4),
             ("tra_diff_forward(normalize=1, lambda=0.5)", wb.name,
              lambda: bsa.tra_diff_forward(qb, q2b, kb, k2b, vb, wb.beta, 0.5, wb.p, normalize=True), 2 * wb.flops),
-            # gradients of the differential form: two backward passes (10 D FLOPs per pair each) and the
-            # normalisation / combination glue; dlambda (one more forward) not requested
-            ("tra_diff_backward(normalize=1, lambda=0.5)", wb.name,
-             lambda: bsa.tra_diff_backward(qb, q2b, kb, k2b, vb, dob, wb.beta, 0.5, wb.p, normalize=True),
+            # gradients of the differential form, dlambda included: two backward passes (10 D FLOPs per pair
+            # each) and the normalisation / combination glue (dlambda is summed in the combination)
+            ("tra_diff_backward(normalize=1, lambda=0.5, dlambda)", wb.name,
+             lambda: bsa.tra_diff_backward(qb, q2b, kb, k2b, vb, dob, wb.beta, 0.5, wb.p, normalize=True,
+                                           want_dlam=True),
              2 * 10 * wb.flops // 4),
         ]
         # The half-power variant on the T=8192 general-power workload (p = 1.5

@@ -13,12 +13,15 @@
 //     dx = (g - n(x) (n(x) . g)) / ||x||  through the normalisation
 //     (g / 1e-12 for rows whose norm is at most 1e-12),
 //     dlambda = -sum(dout * TRA(a2, b2, v)) for 0 < lambda < 1, else 0.
+// With TRA(a2, b2, v) = W2 v and path 2's unscaled dv2 = W2^T dout, that sum
+// is sum_ij dout_i W2_ij v_j = sum(v * dv2): dlambda comes from a dot product
+// over gradients the backward passes already made, with no forward pass.
 // The normalised rows go to the backward kernels as copies in the input
 // dtype; the gradients through the normalisation are taken in fp32 from the
-// inputs and their inverse norms.  Glue kernels here: the normalisation
-// and the combination (16-byte accesses, the lanes of a row summing by
-// shuffles) and the dlambda reduction; the two backward passes and the forward for dlambda are the
-// library's own kernels.
+// inputs and their inverse norms.  Glue kernels here: the normalisation and
+// the combination (16-byte accesses, the lanes of a row summing by shuffles;
+// the combination also sums v * dv2 for dlambda); the two backward passes are
+// the library's own kernels.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -28,19 +31,6 @@ namespace bsa {
 namespace {
 
 constexpr float NORM_EPS = 1e-12f;
-
-__device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
-template <typename T>
-__device__ __forceinline__ T from_f(float x);
-template <>
-__device__ __forceinline__ float from_f<float>(float x) {
-  return x;
-}
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
-  return __float2bfloat16_rn(x);
-}
 
 __device__ __forceinline__ float warp_sum(float s) {
 #pragma unroll
@@ -141,12 +131,16 @@ struct DiffGrads {
 // dv = dv1 - c dv2, and for q1, q2, k1, k2 the gradient g (path 2 scaled by
 // -c) taken back through the normalisation when inv is given (inv: 4 * rows
 // factors in the order q1, q2, k1, k2); rows laid out as in the
-// normalisation kernel.
+// normalisation kernel.  With dlam (zeroed before): *dlam -= sum(v * dv2),
+// block sums added with one fp32 atomic per block.
 template <typename T>
 __global__ void __launch_bounds__(256) diff_bwd_combine_kernel(const T* __restrict__ q1, const T* __restrict__ q2,
                                                                const T* __restrict__ k1, const T* __restrict__ k2,
-                                                               const float* __restrict__ inv, DiffGrads g, float c,
-                                                               long long rows, int D, int L) {
+                                                               const T* __restrict__ v, const float* __restrict__ inv,
+                                                               DiffGrads g, float c, long long rows, int D, int L,
+                                                               float* dlam) {
+  __shared__ float part[8];
+  float sl = 0.0f;  // this thread's share of sum(v * dv2)
   constexpr int V = Vec<T>::V;
   const int lane = threadIdx.x & 31, j = lane % L;
   const long long rpw = 32 / L;
@@ -161,6 +155,12 @@ __global__ void __launch_bounds__(256) diff_bwd_combine_kernel(const T* __restri
       Vec<T> a, b;
       a.load(static_cast<const T*>(g.dv1) + off);
       b.load(static_cast<const T*>(g.dv2) + off);
+      if (dlam != nullptr) {
+        Vec<T> vv;
+        vv.load(v + off);
+#pragma unroll
+        for (int i = 0; i < V; ++i) sl += vv.f[i] * b.f[i];
+      }
 #pragma unroll
       for (int i = 0; i < V; ++i) a.f[i] -= c * b.f[i];
       a.store(static_cast<T*>(g.dv) + off);
@@ -195,25 +195,15 @@ __global__ void __launch_bounds__(256) diff_bwd_combine_kernel(const T* __restri
       }
     }
   }
-}
-
-// *dlam -= sum(dout * out2) (dlam zeroed before): block sums, one fp32 atomic
-// add per block.
-template <typename T>
-__global__ void __launch_bounds__(256) diff_bwd_dlam_kernel(const T* __restrict__ dout, const T* __restrict__ out2,
-                                                            long long n, float* dlam) {
-  __shared__ float part[8];
-  float s = 0.0f;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x)
-    s += to_f(dout[i]) * to_f(out2[i]);
-  s = warp_sum(s);
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    s = threadIdx.x < (blockDim.x >> 5) ? part[threadIdx.x] : 0.0f;
-    s = warp_sum(s);
-    if (threadIdx.x == 0) atomicAdd(dlam, -s);
+  if (dlam != nullptr) {  // uniform across the launch: every thread reaches the barrier
+    sl = warp_sum(sl);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = sl;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      sl = threadIdx.x < (blockDim.x >> 5) ? part[threadIdx.x] : 0.0f;
+      sl = warp_sum(sl);
+      if (threadIdx.x == 0) atomicAdd(dlam, -sl);
+    }
   }
 }
 
@@ -241,7 +231,7 @@ size_t tra_diff_bwd_scratch_bytes(int B, int H, int T, int D, bool f32, bool nor
   size_t b = 6 * align256(n * el);                      // da1, da2, db1, db2, dv1, dv2
   if (normalize) b += align256(4 * n * el) + align256(4 * rows * sizeof(float));
   if (!f32) b += align256(n * sizeof(float));           // fp32 dq accumulator of the fused backward
-  if (dlam) b += align256(n * el);                      // TRA(a2, b2, v)
+  (void)dlam;  // dlambda needs no temporary: it is summed from v and dv2
   return b;
 }
 
@@ -301,38 +291,21 @@ int launch_tra_diff_bwd(const void* q1, const void* q2, const void* k1, const vo
       st = launch_tra_bwd_fused_bf16(a2, b2, v, dout, gr[1], gr[3], gr[5], B, H, T, D, beta, p, acc, stream);
   }
   if (st != OK) return st;
+  if (dlam != nullptr && cudaMemsetAsync(dlam, 0, sizeof(float), stream) != cudaSuccess) return ERR_LAUNCH;
+  float* dl = want_dlam ? dlam : nullptr;
   const DiffGrads g{gr[0], gr[1], gr[2], gr[3], gr[4], gr[5], dq1, dq2, dk1, dk2, dv};
   const int L = lanes_per_row(D, f32 ? 4 : 8);
   const unsigned grid = grid_for((rows * L + 31) / 32);
   if (f32)
     diff_bwd_combine_kernel<float><<<grid, 256, 0, stream>>>(
         static_cast<const float*>(q1), static_cast<const float*>(q2), static_cast<const float*>(k1),
-        static_cast<const float*>(k2), inv, g, c, rows, D, L);
+        static_cast<const float*>(k2), static_cast<const float*>(v), inv, g, c, rows, D, L, dl);
   else
     diff_bwd_combine_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(q1), static_cast<const __nv_bfloat16*>(q2),
-        static_cast<const __nv_bfloat16*>(k1), static_cast<const __nv_bfloat16*>(k2), inv, g, c, rows, D, L);
+        static_cast<const __nv_bfloat16*>(k1), static_cast<const __nv_bfloat16*>(k2),
+        static_cast<const __nv_bfloat16*>(v), inv, g, c, rows, D, L, dl);
   if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
-  if (dlam != nullptr) {
-    if (cudaMemsetAsync(dlam, 0, sizeof(float), stream) != cudaSuccess) return ERR_LAUNCH;
-    if (want_dlam) {
-      void* out2 = take(n * el);
-      st = f32 ? launch_tra_f32(static_cast<const float*>(a2), static_cast<const float*>(b2),
-                                static_cast<const float*>(v), static_cast<float*>(out2), B, H, T, D, beta, p, stream)
-               : launch_tra_bf16(a2, b2, v, out2, B, H, T, D, beta, p, false, stream);
-      if (st != OK) return st;
-      const unsigned gb = grid_for(static_cast<long long>(n) / 256 * 8 + 8);
-      if (f32)
-        diff_bwd_dlam_kernel<float><<<gb, 256, 0, stream>>>(static_cast<const float*>(dout),
-                                                           static_cast<const float*>(out2), static_cast<long long>(n),
-                                                           dlam);
-      else
-        diff_bwd_dlam_kernel<__nv_bfloat16><<<gb, 256, 0, stream>>>(
-            static_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(out2),
-            static_cast<long long>(n), dlam);
-      if (cudaGetLastError() != cudaSuccess) return ERR_LAUNCH;
-    }
-  }
   return OK;
 }
 

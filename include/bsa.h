@@ -289,13 +289,16 @@ BSA_API int tra_diff_forward(const void* q1, const void* q2, const void* k1,
  *   dv  = dv1 - c dv2, (da1, db1, dv1) = tra_backward(a1, b1, v, dout),
  *   (da2, db2, dv2) = -c ... of tra_backward(a2, b2, v, dout) (TRA's gradients
  *   are linear in dout), dq1 = n'(q1)^T da1 etc. through the normalisation,
- *   dlambda = -sum(dout * TRA(a2, b2, v)) for 0 < lambda < 1, else 0.
+ *   dlambda = -sum(dout * TRA(a2, b2, v)) for 0 < lambda < 1, else 0,
+ *   summed as -sum(v * W2^T dout), W2^T dout being the dv of
+ *   tra_backward(a2, b2, v, dout) before the -c (the same sum regrouped,
+ *   TRA(a2, b2, v) = W2 v), so it needs no forward pass.
  * bf16 runs the fused tcgen05 backward twice on normalised bf16 copies of
  * q1, q2, k1, k2 (taken from the inputs in fp32 and rounded once) and takes
  * the gradients through the normalisation in fp32; BSA_F32 the CUDA-core
- * kernels.  Temporaries (the copies, both passes' gradients, the fused
- * backward's fp32 dq accumulator and, for dlambda, TRA(a2, b2, v)) come
- * from the library's stream-ordered pool as for tra_diff_forward.  The dq
+ * kernels.  Temporaries (the copies, both passes' gradients and the fused
+ * backward's fp32 dq accumulator) come from the library's stream-ordered
+ * pool as for tra_diff_forward.  The dq
  * outputs, like tra_backward's, may differ in their last bf16 bit between
  * runs (fp32 partials added in a run-dependent order); so may dlambda (one
  * atomic addition per block).
@@ -304,8 +307,7 @@ BSA_API int tra_diff_forward(const void* q1, const void* q2, const void* k1,
  *   dq1, dq2, dk1, dk2, dv         : [B, H, T, D] of `dtype` (outputs; they
  *                                    must not alias the inputs or each other).
  *   dlambda                        : device float (4-byte aligned) written
- *                                    with dlambda, or NULL to skip it (then
- *                                    TRA(a2, b2, v) is not formed).
+ *                                    with dlambda, or NULL to skip it.
  *   B, H, T, D, beta, lambda, p,
  *   normalize, dtype               : as for tra_diff_forward.
  *
