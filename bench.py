@@ -1,7 +1,10 @@
 """Benchmark of the fused causal attention forwards on GB300.
 
 ``python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-[--workload NAME] [--no-secondary]`` prints ONE JSON line.
+[--workload NAME] [--no-secondary]`` prints ONE JSON line.  ``--op`` times one
+widened op on its own instead (backward, backward-deterministic, diff,
+diff-backward on a TRA workload; fsa on an NSA workload), for per-kernel
+measurements and ncu captures.
 
 A step is one pass of the whole threshold-rectified-attention (TRA) path --
 tau table, Q K^T, causal mask, threshold and power, W V, store -- fused in one
@@ -731,6 +734,16 @@ def run_op(args):
         fn = lambda: bsa.tra_backward(q, k, v, extra[0], w.beta, w.p)  # noqa: E731
         flops = 10 * w.flops // 4
         launches = 3  # dq accumulator zeroing, the fused kernel, dq conversion
+    elif args.op == "backward-deterministic":
+        fn = lambda: bsa.tra_backward(q, k, v, extra[0], w.beta, w.p, deterministic=True)  # noqa: E731
+        flops = 10 * w.flops // 4
+        launches = 1  # dK/dV and dQ blocks in one grid
+    elif args.op == "diff-backward":
+        q2, k2 = (torch.randn(q.shape, generator=gen).to(torch.bfloat16).cuda() for _ in range(2))
+        fn = lambda: bsa.tra_diff_backward(q, q2, k, k2, v, extra[0], w.beta, 0.5, w.p,  # noqa: E731
+                                           normalize=True, want_dlam=True)
+        flops = 2 * 10 * w.flops // 4
+        launches = 8  # normalisation, two fused backward passes (3 each), combination
     else:
         fn = lambda: bsa.tra_diff_forward(q, extra[0], k, extra[1], v, w.beta, 0.5, w.p, normalize=True)  # noqa: E731
         flops = 2 * w.flops
@@ -755,7 +768,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--op", choices=["forward", "backward", "diff", "fsa"], default="forward",
+    ap.add_argument("--op", choices=["forward", "backward", "backward-deterministic", "diff", "diff-backward", "fsa"],
+                    default="forward",
                     help="forward (the headline path), or one widened op timed on its own")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")

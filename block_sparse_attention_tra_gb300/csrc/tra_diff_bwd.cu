@@ -99,26 +99,36 @@ __global__ void __launch_bounds__(256) diff_bwd_normalize_kernel(const T* __rest
   const long long rpw = 32 / L;  // rows per warp
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
   const bool has = j * V < D;
+  // two rows per lane group and pass, both loads issued before either is used
   for (long long w0 = ((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * rpw; w0 < 4 * rows;
-       w0 += nw * rpw) {
-    const long long w = w0 + lane / L;
-    const bool live = w < 4 * rows && has;
-    Vec<T> x;
-    x.zero();
-    if (live) {
-      const int which = static_cast<int>(w / rows);
-      const long long r = w - which * rows;
-      x.load((which == 0 ? x0 : which == 1 ? x1 : which == 2 ? x2 : x3) + r * D + j * V);
+       w0 += 2 * nw * rpw) {
+    long long w[2];
+    bool live[2];
+    Vec<T> x[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      w[u] = w0 + u * nw * rpw + lane / L;
+      live[u] = w[u] < 4 * rows && has;
+      x[u].zero();
+      if (live[u]) {
+        // which input (no 64-bit division: this kernel is otherwise a copy)
+        const int which = (w[u] >= rows) + (w[u] >= 2 * rows) + (w[u] >= 3 * rows);
+        const long long r = w[u] - which * rows;
+        x[u].load((which == 0 ? x0 : which == 1 ? x1 : which == 2 ? x2 : x3) + r * D + j * V);
+      }
     }
-    float s = 0.0f;
 #pragma unroll
-    for (int i = 0; i < V; ++i) s += x.f[i] * x.f[i];
-    const float iv = 1.0f / fmaxf(sqrtf(group_sum(s, L)), NORM_EPS);
-    if (live) {
+    for (int u = 0; u < 2; ++u) {
+      float s = 0.0f;
 #pragma unroll
-      for (int i = 0; i < V; ++i) x.f[i] *= iv;
-      x.store(xn + w * D + j * V);
-      if (j == 0) inv[w] = iv;
+      for (int i = 0; i < V; ++i) s += x[u].f[i] * x[u].f[i];
+      const float iv = 1.0f / fmaxf(sqrtf(group_sum(s, L)), NORM_EPS);
+      if (live[u]) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) x[u].f[i] *= iv;
+        x[u].store(xn + w[u] * D + j * V);
+        if (j == 0) inv[w[u]] = iv;
+      }
     }
   }
 }
@@ -151,13 +161,27 @@ __global__ void __launch_bounds__(256) diff_bwd_combine_kernel(const T* __restri
     const long long r = r0 + lane / L;
     const bool live = r < rows && has;
     const long long off = r * D + j * V;
+    // every load of the row first (dv1, dv2, v, the four gradients and their
+    // inputs), then the arithmetic and the stores
+    Vec<T> a, b, vv, gv[4], xv[4];
+    float iv[4];
+#pragma unroll
+    for (int which = 0; which < 4; ++which) {
+      gv[which].zero();
+      xv[which].zero();
+      iv[which] = inv != nullptr && r < rows ? inv[which * rows + r] : 1.0f;
+    }
     if (live) {
-      Vec<T> a, b;
       a.load(static_cast<const T*>(g.dv1) + off);
       b.load(static_cast<const T*>(g.dv2) + off);
+      if (dlam != nullptr) vv.load(v + off);
+#pragma unroll
+      for (int which = 0; which < 4; ++which) {
+        gv[which].load(static_cast<const T*>(which == 0 ? g.da1 : which == 1 ? g.da2 : which == 2 ? g.db1 : g.db2) +
+                       off);
+        if (inv != nullptr) xv[which].load((which == 0 ? q1 : which == 1 ? q2 : which == 2 ? k1 : k2) + off);
+      }
       if (dlam != nullptr) {
-        Vec<T> vv;
-        vv.load(v + off);
 #pragma unroll
         for (int i = 0; i < V; ++i) sl += vv.f[i] * b.f[i];
       }
@@ -165,33 +189,26 @@ __global__ void __launch_bounds__(256) diff_bwd_combine_kernel(const T* __restri
       for (int i = 0; i < V; ++i) a.f[i] -= c * b.f[i];
       a.store(static_cast<T*>(g.dv) + off);
     }
-#pragma unroll 1
+#pragma unroll
     for (int which = 0; which < 4; ++which) {
       const float scale = (which & 1) ? -c : 1.0f;  // path 2 (q2, k2) carries -c
-      Vec<T> gv, xv;
-      gv.zero();
-      xv.zero();
-      const float iv = inv != nullptr && r < rows ? inv[which * rows + r] : 1.0f;
-      if (live) {
-        gv.load(static_cast<const T*>(which == 0 ? g.da1 : which == 1 ? g.da2 : which == 2 ? g.db1 : g.db2) + off);
-        if (inv != nullptr) xv.load((which == 0 ? q1 : which == 1 ? q2 : which == 2 ? k1 : k2) + off);
-      }
       float dot = 0.0f;
 #pragma unroll
       for (int i = 0; i < V; ++i) {
-        gv.f[i] *= scale;
-        xv.f[i] *= iv;
-        dot += xv.f[i] * gv.f[i];
+        gv[which].f[i] *= scale;
+        xv[which].f[i] *= iv[which];
+        dot += xv[which].f[i] * gv[which].f[i];
       }
       dot = group_sum(dot, L);
       // rows with a norm above eps: (g - xn (xn . g)) / ||x||; else g / eps
-      const bool proj = iv < 1.0f / NORM_EPS;
+      const bool proj = iv[which] < 1.0f / NORM_EPS;
       if (live) {
         if (inv != nullptr) {
 #pragma unroll
-          for (int i = 0; i < V; ++i) gv.f[i] = (proj ? gv.f[i] - xv.f[i] * dot : gv.f[i]) * iv;
+          for (int i = 0; i < V; ++i)
+            gv[which].f[i] = (proj ? gv[which].f[i] - xv[which].f[i] * dot : gv[which].f[i]) * iv[which];
         }
-        gv.store(static_cast<T*>(which == 0 ? g.dq1 : which == 1 ? g.dq2 : which == 2 ? g.dk1 : g.dk2) + off);
+        gv[which].store(static_cast<T*>(which == 0 ? g.dq1 : which == 1 ? g.dq2 : which == 2 ? g.dk1 : g.dk2) + off);
       }
     }
   }
