@@ -77,10 +77,6 @@ struct FsaLayout {
   static_assert(O_COL + 2 * D <= TMEM_COLS, "TMEM budget");
 };
 
-__device__ __forceinline__ bool slot_live(int blk, int i, int n_blk) {
-  return blk >= 0 && blk < n_blk && blk * FSA_BS <= i;
-}
-
 // ------------------------------------------------------------------ CSR build
 
 __global__ void fsa_zero_kernel(int* __restrict__ counts, int n, int* __restrict__ meta) {
@@ -89,25 +85,27 @@ __global__ void fsa_zero_kernel(int* __restrict__ counts, int n, int* __restrict
 }
 
 // FILL = false: counts[bh, j] += 1 per live slot.  FILL = true: append the
-// pair (packed i * 32 + slot) at the block's cursor.
+// pair (packed i * 32 + slot) at the block's cursor.  One warp per index row
+// (lane s takes slot s): the live slots, de-duplicated under the set reading
+// of the row, come from nsa_live_slots as in the query-outer kernels.
 template <bool FILL>
 __global__ void fsa_pairs_kernel(const int32_t* __restrict__ block_idx, int* __restrict__ counter,
-                                 int* __restrict__ list, long long n_slots, int T, int S, int n_blk) {
-  for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < n_slots;
-       e += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int blk = block_idx[e];
-    const long long row = e / S;  // (bh, i)
+                                 int* __restrict__ list, long long n_rows, int T, int S, int n_blk) {
+  const int lane = static_cast<int>(threadIdx.x & 31u);
+  const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long row = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; row < n_rows;
+       row += n_warps) {  // warp-uniform: the whole warp takes a row
     const int i = static_cast<int>(row % T);
-    if (!slot_live(blk, i, n_blk)) continue;
-    // Set semantics: a block listed again later in the row forms no second pair.
-    if (!nsa_first_occurrence(block_idx + row * S, static_cast<int>(e - row * S), blk)) continue;
     const long long bh = row / T;
-    int* c = counter + bh * n_blk + blk;
-    if constexpr (FILL) {
-      const int pos = debug_index(atomicAdd(c, 1), 0, static_cast<int>(n_slots));
-      list[pos] = i * 32 + static_cast<int>(e % S);
-    } else {
-      atomicAdd(c, 1);
+    const SlotRow r = nsa_live_slots(block_idx + row * S, S, i, n_blk, FSA_BS);
+    if ((r.live >> lane) & 1u) {
+      int* c = counter + bh * n_blk + r.blk_lane;
+      if constexpr (FILL) {
+        const int pos = debug_index(atomicAdd(c, 1), 0, static_cast<int>(n_rows * S));
+        list[pos] = i * 32 + lane;
+      } else {
+        atomicAdd(c, 1);
+      }
     }
   }
 }
@@ -603,9 +601,12 @@ int launch_fsa(const void* q, const void* k, const void* v, const int32_t* block
     return static_cast<unsigned>(std::min<long long>((n + threads - 1) / threads, 148LL * 64));
   };
   fsa_zero_kernel<<<grid_for(pl.NB, 256), 256, 0, stream>>>(cnt, static_cast<int>(pl.NB), meta);
-  fsa_pairs_kernel<false><<<grid_for(pl.slots, 256), 256, 0, stream>>>(block_idx, cnt, list, pl.slots, T, S, n_blk);
+  const long long idx_rows = pl.slots / S;  // one warp per index row
+  fsa_pairs_kernel<false><<<grid_for(idx_rows * 32, 256), 256, 0, stream>>>(block_idx, cnt, list, idx_rows, T, S,
+                                                                             n_blk);
   fsa_scan_kernel<<<1, SCAN_THREADS, 0, stream>>>(cnt, off, items, meta, static_cast<int>(pl.NB), pl.qch);
-  fsa_pairs_kernel<true><<<grid_for(pl.slots, 256), 256, 0, stream>>>(block_idx, cnt, list, pl.slots, T, S, n_blk);
+  fsa_pairs_kernel<true><<<grid_for(idx_rows * 32, 256), 256, 0, stream>>>(block_idx, cnt, list, idx_rows, T, S,
+                                                                            n_blk);
 
   // G = 8 or 16: each query's G partial rows are contiguous, so they leave by
   // TMA tensor stores (fp32 [rows, D] map, 32 x G boxes).

@@ -36,12 +36,4 @@ __device__ __forceinline__ int nsa_slot_block(const SlotRow& r, int s) {
   return __shfl_sync(0xffffffffu, r.blk_lane, s);
 }
 
-// Single-thread form for a slot `s` of row `sel` whose block `blk` already
-// passed the causal test: true when no earlier slot of the row holds `blk`.
-__device__ __forceinline__ bool nsa_first_occurrence(const int32_t* __restrict__ sel, int s, int blk) {
-  for (int s2 = 0; s2 < s; ++s2)
-    if (__ldg(sel + s2) == blk) return false;
-  return true;
-}
-
 }  // namespace bsa
