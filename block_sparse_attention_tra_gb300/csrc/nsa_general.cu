@@ -93,15 +93,21 @@ struct GenLayout {
   static constexpr int BYTES = GEN_WARPS * WARP_BYTES;
 };
 
-// The minimum CTAs per SM are what each head dim's shared memory and
-// registers allow at once; without them the compiler takes more registers
-// than that occupancy leaves (139 instead of 64 at D = 16).
+// The minimum CTAs per SM are what each form's shared memory and registers
+// allow at once; without them the compiler takes more registers than that
+// occupancy leaves (139 instead of 64 at D = 16).
+template <int D, int C>
+constexpr int gen_min_ctas() {
+  if constexpr (C == 32) return D == 16 ? 6 : 4;
+  return D == 16 ? 8 : D == 32 ? 7 : D == 64 ? 4 : 2;
+}
+
 template <int D, int NB, int C>
-__global__ void __launch_bounds__(GEN_THREADS, C == 32 ? (D == 16 ? 6 : 4) : D == 16 ? 8 : D == 32 ? 7 : D == 64 ? 4 : 2)
+__global__ void __launch_bounds__(GEN_THREADS, gen_min_ctas<D, C>())
     nsa_general_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                            const __nv_bfloat16* __restrict__ v, const int32_t* __restrict__ block_idx,
-                            __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int Hq, int Hkv, int G, int T,
-                            int S, int bs, long long n_queries, float scale_log2) {
+                       const __nv_bfloat16* __restrict__ v, const int32_t* __restrict__ block_idx,
+                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int Hq, int Hkv, int G, int T,
+                       int S, int bs, long long n_queries, float scale_log2) {
   using L = GenLayout<D, NB, C>;
   static_assert(NB >= 2, "at least double buffering");
   static_assert(C == 16 || C == 32, "16 or 32 tokens per chunk");
