@@ -743,7 +743,7 @@ def run_op(args):
         fn = lambda: bsa.tra_diff_backward(q, q2, k, k2, v, extra[0], w.beta, 0.5, w.p,  # noqa: E731
                                            normalize=True, want_dlam=True)
         flops = 2 * 10 * w.flops // 4
-        launches = 8  # normalisation, two fused backward passes (3 each), combination
+        launches = 6  # normalisation, two fused backward passes (zeroing + kernel each), combination
     else:
         fn = lambda: bsa.tra_diff_forward(q, extra[0], k, extra[1], v, w.beta, 0.5, w.p, normalize=True)  # noqa: E731
         flops = 2 * w.flops

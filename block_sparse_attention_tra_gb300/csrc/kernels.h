@@ -57,7 +57,8 @@ int launch_tra_bwd_bf16(const void* q, const void* k, const void* v, const void*
 // query tile) pair are computed once, dk and dv accumulate in tensor memory
 // and each pair's dq partial is added into dq_acc (fp32, B*H*T*D elements,
 // 16-byte aligned), which this call zeroes first and converts into dq last.
-// The order of those fp32 additions varies from run to run.
+// The order of those fp32 additions varies from run to run.  dq may be null:
+// dQ is then left in dq_acc (fp32) and not converted.
 int launch_tra_bwd_fused_bf16(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
                               void* dv, int B, int H, int T, int D, float beta, float p, float* dq_acc,
                               cudaStream_t stream);

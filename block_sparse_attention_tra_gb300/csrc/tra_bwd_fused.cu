@@ -620,6 +620,7 @@ int launch_tra_bwd_fused_bf16(const void* q, const void* k, const void* v, const
   const int rc = D > 64 ? launch_fused_pc<128>(maps, mdq, dk, dv, BH, T, beta, p, D, stream)
                           : launch_fused_pc<64>(maps, mdq, dk, dv, BH, T, beta, p, D, stream);
   if (rc != OK) return rc;
+  if (dq == nullptr) return OK;  // the caller reads dQ from dq_acc (fp32)
   tra_bwd_dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
       dq_acc, static_cast<__nv_bfloat16*>(dq), n8);
   return cudaGetLastError() == cudaSuccess ? OK : ERR_LAUNCH;

@@ -134,9 +134,20 @@ __global__ void __launch_bounds__(256) diff_bwd_normalize_kernel(const T* __rest
 }
 
 struct DiffGrads {
-  const void *da1, *da2, *db1, *db2, *dv1, *dv2;  // the two backward passes (path 2 unscaled)
-  void *dq1, *dq2, *dk1, *dk2, *dv;               // outputs
+  const float *da1, *da2;                // the two passes' query gradients, fp32 (path 2 unscaled)
+  const void *db1, *db2, *dv1, *dv2;     // their key and value gradients, in T (path 2 unscaled)
+  void *dq1, *dq2, *dk1, *dk2, *dv;      // outputs
 };
+
+// V consecutive fp32 values (V = 4 or 8, 16-byte aligned).
+template <int V>
+__device__ __forceinline__ void load_f32(const float* p, float (&f)[V]) {
+#pragma unroll
+  for (int h = 0; h < V / 4; ++h) {
+    const float4 u = reinterpret_cast<const float4*>(p)[h];
+    f[4 * h] = u.x, f[4 * h + 1] = u.y, f[4 * h + 2] = u.z, f[4 * h + 3] = u.w;
+  }
+}
 
 // dv = dv1 - c dv2, and for q1, q2, k1, k2 the gradient g (path 2 scaled by
 // -c) taken back through the normalisation when inv is given (inv: 4 * rows
@@ -177,8 +188,10 @@ __global__ void __launch_bounds__(256) diff_bwd_combine_kernel(const T* __restri
       if (dlam != nullptr) vv.load(v + off);
 #pragma unroll
       for (int which = 0; which < 4; ++which) {
-        gv[which].load(static_cast<const T*>(which == 0 ? g.da1 : which == 1 ? g.da2 : which == 2 ? g.db1 : g.db2) +
-                       off);
+        if (which < 2)
+          load_f32<V>((which == 0 ? g.da1 : g.da2) + off, gv[which].f);
+        else
+          gv[which].load(static_cast<const T*>(which == 2 ? g.db1 : g.db2) + off);
         if (inv != nullptr) xv[which].load((which == 0 ? q1 : which == 1 ? q2 : which == 2 ? k1 : k2) + off);
       }
       if (dlam != nullptr) {
@@ -245,9 +258,10 @@ unsigned grid_for(long long warps_needed) {
 size_t tra_diff_bwd_scratch_bytes(int B, int H, int T, int D, bool f32, bool normalize, bool dlam) {
   const size_t n = static_cast<size_t>(B) * H * T * D, rows = static_cast<size_t>(B) * H * T;
   const size_t el = f32 ? 4 : 2;
-  size_t b = 6 * align256(n * el);                      // da1, da2, db1, db2, dv1, dv2
+  // da1, da2 in fp32 (for bf16 the fused backward's dq accumulators, read
+  // without a conversion), db1, db2, dv1, dv2 in the input dtype
+  size_t b = 2 * align256(n * sizeof(float)) + 4 * align256(n * el);
   if (normalize) b += align256(4 * n * el) + align256(4 * rows * sizeof(float));
-  if (!f32) b += align256(n * sizeof(float));           // fp32 dq accumulator of the fused backward
   (void)dlam;  // dlambda needs no temporary: it is summed from v and dv2
   return b;
 }
@@ -266,8 +280,8 @@ int launch_tra_diff_bwd(const void* q1, const void* q2, const void* k1, const vo
     s += align256(bytes);
     return static_cast<void*>(r);
   };
-  void* gr[6];
-  for (int i = 0; i < 6; ++i) gr[i] = take(n * el);
+  void* gr[6];  // da1, da2 (fp32), db1, db2, dv1, dv2 (input dtype)
+  for (int i = 0; i < 6; ++i) gr[i] = take(n * (i < 2 ? sizeof(float) : el));
   const void *a1 = q1, *a2 = q2, *b1 = k1, *b2 = k2;
   float* inv = nullptr;
   if (normalize) {
@@ -302,15 +316,18 @@ int launch_tra_diff_bwd(const void* q1, const void* q2, const void* k1, const vo
                               static_cast<const float*>(v), static_cast<const float*>(dout), static_cast<float*>(gr[1]),
                               static_cast<float*>(gr[3]), static_cast<float*>(gr[5]), B, H, T, D, beta, p, stream);
   } else {
-    float* acc = static_cast<float*>(take(n * sizeof(float)));
-    st = launch_tra_bwd_fused_bf16(a1, b1, v, dout, gr[0], gr[2], gr[4], B, H, T, D, beta, p, acc, stream);
+    // each pass leaves its dq in its own fp32 accumulator (no conversion)
+    st = launch_tra_bwd_fused_bf16(a1, b1, v, dout, nullptr, gr[2], gr[4], B, H, T, D, beta, p,
+                                   static_cast<float*>(gr[0]), stream);
     if (st == OK)
-      st = launch_tra_bwd_fused_bf16(a2, b2, v, dout, gr[1], gr[3], gr[5], B, H, T, D, beta, p, acc, stream);
+      st = launch_tra_bwd_fused_bf16(a2, b2, v, dout, nullptr, gr[3], gr[5], B, H, T, D, beta, p,
+                                     static_cast<float*>(gr[1]), stream);
   }
   if (st != OK) return st;
   if (dlam != nullptr && cudaMemsetAsync(dlam, 0, sizeof(float), stream) != cudaSuccess) return ERR_LAUNCH;
   float* dl = want_dlam ? dlam : nullptr;
-  const DiffGrads g{gr[0], gr[1], gr[2], gr[3], gr[4], gr[5], dq1, dq2, dk1, dk2, dv};
+  const DiffGrads g{static_cast<const float*>(gr[0]), static_cast<const float*>(gr[1]), gr[2], gr[3], gr[4], gr[5],
+                    dq1, dq2, dk1, dk2, dv};
   const int L = lanes_per_row(D, f32 ? 4 : 8);
   const unsigned grid = grid_for((rows * L + 31) / 32);
   if (f32)

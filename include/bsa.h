@@ -296,12 +296,12 @@ BSA_API int tra_diff_forward(const void* q1, const void* q2, const void* k1,
  * bf16 runs the fused tcgen05 backward twice on normalised bf16 copies of
  * q1, q2, k1, k2 (taken from the inputs in fp32 and rounded once) and takes
  * the gradients through the normalisation in fp32; BSA_F32 the CUDA-core
- * kernels.  Temporaries (the copies, both passes' gradients and the fused
- * backward's fp32 dq accumulator) come from the library's stream-ordered
- * pool as for tra_diff_forward.  The dq
- * outputs, like tra_backward's, may differ in their last bf16 bit between
- * runs (fp32 partials added in a run-dependent order); so may dlambda (one
- * atomic addition per block).
+ * kernels.  Temporaries (the copies and both passes' gradients, their dq in
+ * fp32: for bf16 the fused backward's accumulators, read without a
+ * conversion) come from the library's stream-ordered pool as for
+ * tra_diff_forward.  The dq outputs, like tra_backward's, may differ in
+ * their last bf16 bit between runs (fp32 partials added in a run-dependent
+ * order); so may dlambda (one atomic addition per block).
  *
  *   q1, q2, k1, k2, v, dout        : [B, H, T, D] of `dtype` (inputs).
  *   dq1, dq2, dk1, dk2, dv         : [B, H, T, D] of `dtype` (outputs; they
